@@ -1,0 +1,218 @@
+"""CPU oracle of the online NVFP4 lm_head path -- TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  The product library never loads it,
+and it shares no code with the CUDA sources: the arithmetic lives in
+``nvfp4_oracle.c`` (plain C, built with ``-ffp-contract=off``), and this file
+only marshals numpy arrays into it.
+
+What each function follows is stated in ``nvfp4_oracle.c``.  In short:
+
+* ``quantize``     -- ``_quantize_nvfp4`` on the page
+  *vllm.model_executor.layers.quantization.online.lm_head*: fp32 global
+  scale amax/(6*448) clamped at 1e-12, per-16 E4M3 block scales, E2M1 codes
+  with the sign in bit 3, two codes per byte, low nibble first.
+* ``dequant_rows`` / ``logits`` -- the W4A16 product of
+  ``CompressedTensorsW4A16Fp4`` (page *...compressed_tensors.schemes*):
+  logits = x . (e2m1 * f32(scale) * global)^T, here in float64.
+
+Parity: every function is pinned in ``tests/test_oracle_*.py`` against what
+the pages fix (the code table, the packing order, K % 16), closed forms,
+brute-force nearest rounding, torch's own float8_e4m3fn cast and numpy's
+matmul.  The one reading the pages cannot pin -- the multiply order inside
+the unprinted per-16 block quantizer -- is stated as a reading, not pinned.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "nvfp4_oracle.c")
+_LIB = os.path.join(_HERE, "_liboracle.so")
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle (gcc, no FMA contraction, OpenMP if available)."""
+    if not force and os.path.exists(_LIB) and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC):
+        return _LIB
+    tmp = _LIB + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared",
+           "-std=gnu11", _SRC, "-o", tmp, "-lm"]
+    try:
+        subprocess.run(cmd[:6] + ["-fopenmp"] + cmd[6:], check=True, capture_output=True)
+    except subprocess.CalledProcessError:
+        subprocess.run(cmd, check=True, capture_output=True)
+    os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        build()
+        lib = ctypes.CDLL(_LIB)
+        p = ctypes.c_void_p
+        i64 = ctypes.c_int64
+        f = ctypes.c_float
+        lib.oracle_e4m3_decode.argtypes = [ctypes.c_uint8]
+        lib.oracle_e4m3_decode.restype = f
+        lib.oracle_e4m3_encode.argtypes = [f]
+        lib.oracle_e4m3_encode.restype = ctypes.c_uint8
+        lib.oracle_e2m1_round.argtypes = [f]
+        lib.oracle_e2m1_round.restype = f
+        lib.oracle_e2m1_code.argtypes = [f]
+        lib.oracle_e2m1_code.restype = ctypes.c_uint8
+        lib.oracle_e2m1_decode.argtypes = [ctypes.c_uint8]
+        lib.oracle_e2m1_decode.restype = f
+        lib.oracle_weight_amax.argtypes = [p, i64, p]
+        lib.oracle_weight_amax.restype = ctypes.c_int
+        lib.oracle_global_scale.argtypes = [f, p, p]
+        lib.oracle_quantize_block.argtypes = [p, f, f, p, p]
+        lib.oracle_quantize_rows.argtypes = [p, i64, i64, p, i64, f, f, p, p]
+        lib.oracle_quantize.argtypes = [p, i64, i64, p, p, p]
+        lib.oracle_quantize.restype = ctypes.c_int
+        lib.oracle_dequant_rows.argtypes = [p, p, f, i64, p, i64, p]
+        lib.oracle_logits_cols.argtypes = [p, i64, i64, p, p, f, p, i64, p]
+        lib.oracle_e4m3_encode_array.argtypes = [p, i64, p]
+        lib.oracle_e2m1_round_array.argtypes = [p, i64, p]
+        lib.oracle_num_threads.restype = ctypes.c_int
+        _lib = lib
+    return _lib
+
+
+def _ptr(a: np.ndarray) -> ctypes.c_void_p:
+    assert a.flags["C_CONTIGUOUS"], "oracle needs contiguous arrays"
+    return ctypes.c_void_p(a.ctypes.data)
+
+
+class OracleError(ValueError):
+    pass
+
+
+# ------------------------------------------------------------------ scalars
+def e4m3_decode(byte: int) -> float:
+    return float(_load().oracle_e4m3_decode(byte))
+
+
+def e4m3_encode(t: float) -> int:
+    return int(_load().oracle_e4m3_encode(t))
+
+
+def e2m1_round(q: float) -> float:
+    return float(_load().oracle_e2m1_round(q))
+
+
+def e2m1_code(v: float) -> int:
+    return int(_load().oracle_e2m1_code(v))
+
+
+def e2m1_decode(code: int) -> float:
+    return float(_load().oracle_e2m1_decode(code))
+
+
+def e4m3_encode_array(t: np.ndarray) -> np.ndarray:
+    """Element-wise e4m3 encode (a loop over the scalar C routine)."""
+    t = np.ascontiguousarray(t, dtype=np.float32).ravel()
+    out = np.zeros(t.size, dtype=np.uint8)
+    _load().oracle_e4m3_encode_array(_ptr(t), t.size, _ptr(out))
+    return out
+
+
+def e2m1_round_array(q: np.ndarray) -> np.ndarray:
+    """Element-wise E2M1 grid rounding (a loop over the scalar C routine)."""
+    q = np.ascontiguousarray(q, dtype=np.float32).ravel()
+    out = np.zeros(q.size, dtype=np.float32)
+    _load().oracle_e2m1_round_array(_ptr(q), q.size, _ptr(out))
+    return out
+
+
+# ------------------------------------------------------------- global scale
+def weight_amax(W: np.ndarray) -> float:
+    W = np.ascontiguousarray(W, dtype=np.uint16)
+    out = np.zeros(1, dtype=np.float32)
+    rc = _load().oracle_weight_amax(_ptr(W), W.size, _ptr(out))
+    if rc != 0:
+        raise OracleError("non-finite weight")
+    return float(out[0])
+
+
+def global_scale(amax: float) -> tuple[np.float32, np.float32]:
+    g = np.zeros(1, dtype=np.float32)
+    ig = np.zeros(1, dtype=np.float32)
+    _load().oracle_global_scale(amax, _ptr(g), _ptr(ig))
+    return g[0], ig[0]
+
+
+# ------------------------------------------------------------ quantization
+def quantize_block(x16: np.ndarray, g: float, ig: float) -> tuple[np.ndarray, int]:
+    """One 16-value block: (grid values as float32[16], e4m3 scale byte)."""
+    x = np.ascontiguousarray(x16, dtype=np.float32)
+    assert x.shape == (16,)
+    v = np.zeros(16, dtype=np.float32)
+    s = np.zeros(1, dtype=np.uint8)
+    _load().oracle_quantize_block(_ptr(x), g, ig, _ptr(v), _ptr(s))
+    return v, int(s[0])
+
+
+def quantize(W: np.ndarray) -> tuple[np.ndarray, np.ndarray, np.float32]:
+    """`_quantize_nvfp4`: (packed u8[N,K/2], scales u8(e4m3)[N,K/16], global f32)."""
+    W = np.ascontiguousarray(W, dtype=np.uint16)
+    N, K = W.shape
+    packed = np.zeros((N, K // 2), dtype=np.uint8)
+    scales = np.zeros((N, max(K // 16, 0)), dtype=np.uint8)
+    g = np.zeros(1, dtype=np.float32)
+    rc = _load().oracle_quantize(_ptr(W), N, K, _ptr(packed), _ptr(scales), _ptr(g))
+    if rc == -1:
+        raise OracleError("non-finite weight")
+    if rc == -2:
+        raise OracleError("shape rejected (K % 16 != 0 or empty)")
+    return packed, scales, g[0]
+
+
+def quantize_rows(W: np.ndarray, rows, g: float, ig: float) -> tuple[np.ndarray, np.ndarray]:
+    """Quantize only the listed rows of W with a given global scale."""
+    W = np.ascontiguousarray(W, dtype=np.uint16)
+    N, K = W.shape
+    rows = np.ascontiguousarray(rows, dtype=np.int64)
+    packed = np.zeros((rows.size, K // 2), dtype=np.uint8)
+    scales = np.zeros((rows.size, K // 16), dtype=np.uint8)
+    _load().oracle_quantize_rows(_ptr(W), N, K, _ptr(rows), rows.size, g, ig, _ptr(packed),
+                                 _ptr(scales))
+    return packed, scales
+
+
+def dequant_rows(packed: np.ndarray, scales: np.ndarray, g: float, rows=None) -> np.ndarray:
+    """w = e2m1(code) * f32(scale) * global, float64 [len(rows), K]."""
+    packed = np.ascontiguousarray(packed, dtype=np.uint8)
+    scales = np.ascontiguousarray(scales, dtype=np.uint8)
+    N, K = packed.shape[0], packed.shape[1] * 2
+    rows = np.arange(N, dtype=np.int64) if rows is None else np.ascontiguousarray(rows, np.int64)
+    out = np.zeros((rows.size, K), dtype=np.float64)
+    _load().oracle_dequant_rows(_ptr(packed), _ptr(scales), g, K, _ptr(rows), rows.size,
+                                _ptr(out))
+    return out
+
+
+def logits(x: np.ndarray, packed: np.ndarray, scales: np.ndarray, g: float,
+           cols=None) -> np.ndarray:
+    """float64 logits[M, len(cols)] = x . dequant(W[cols])^T (all rows if cols is None)."""
+    x = np.ascontiguousarray(x, dtype=np.uint16)
+    packed = np.ascontiguousarray(packed, dtype=np.uint8)
+    scales = np.ascontiguousarray(scales, dtype=np.uint8)
+    M, K = x.shape
+    N = packed.shape[0]
+    assert packed.shape[1] * 2 == K
+    cols = np.arange(N, dtype=np.int64) if cols is None else np.ascontiguousarray(cols, np.int64)
+    out = np.zeros((M, cols.size), dtype=np.float64)
+    _load().oracle_logits_cols(_ptr(x), M, K, _ptr(packed), _ptr(scales), g, _ptr(cols),
+                               cols.size, _ptr(out))
+    return out
+
+
+def num_threads() -> int:
+    return int(_load().oracle_num_threads())
