@@ -1,0 +1,169 @@
+/*
+ * nvfp4_lm_head.h -- C ABI of the GB300 (sm_103a) online NVFP4 lm_head library.
+ *
+ * Two operations, as the pages define them:
+ *
+ *  1. Row quantization of an already-loaded bf16 lm_head to NVFP4 in the
+ *     checkpoint layout -- page "vllm.model_executor.layers.quantization.
+ *     online.lm_head", section `_quantize_nvfp4`: an fp32 global scale equal
+ *     to amax(W) / (6 * 448) (clamped at 1e-12; the raw dequant multiplier,
+ *     no reciprocal, as `KNvfp4Static.process` on the page of
+ *     vllm/model_executor/layers/quantization/modelopt.py keeps it), one
+ *     E4M3 scale per 16 consecutive values of a row, and E2M1 codes with the
+ *     sign in bit 3, two per byte with the low nibble first.  Section
+ *     `refresh_quantized_lm_heads` of the same page adds the in-place
+ *     re-derivation that keeps tensor addresses stable for CUDA graphs.
+ *
+ *  2. The weight-only W4A16 product against bf16 activations -- section
+ *     `_LMHeadNvfp4Method.apply` of the first page and
+ *     `CompressedTensorsW4A16Fp4.apply_weights` on the page
+ *     "vllm.model_executor.layers.quantization.compressed_tensors.schemes":
+ *     logits[m, n] = global * sum_k x[m, k] * e2m1(code[n, k]) * f32(scale[n, k/16]).
+ *
+ * Conventions for every call:
+ *  - All tensor pointers are DEVICE pointers on the current CUDA device,
+ *    row-major and contiguous.  The caller owns every buffer; the library
+ *    never allocates, frees or synchronizes (except
+ *    nvfp4_read_device_status, which is documented as synchronizing).
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *    stream).  Work is enqueued on it and the call returns at once.
+ *  - bf16 tensors are passed as void* holding IEEE bfloat16 bit patterns;
+ *    E4M3 scales are uint8_t holding float8_e4m3fn bit patterns.
+ *  - Argument errors are detected on the host and returned as a status
+ *    before anything is enqueued.  Conditions that only the device can see
+ *    (non-finite weights, a pipeline wait that ran out of time) are written
+ *    to a status word inside the workspace; kernels never trap.
+ *  - Workspaces must be 256-byte aligned and at least the size the matching
+ *    *_workspace_bytes() call returns.  Their contents need no
+ *    initialisation and may be reused between calls on the same stream.
+ */
+#ifndef NVFP4_LM_HEAD_H_
+#define NVFP4_LM_HEAD_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  NVFP4_OK = 0,
+  NVFP4_ERR_SHAPE = 1,      /* a size is out of range (e.g. K % 16 != 0) */
+  NVFP4_ERR_ALIGN = 2,      /* a pointer or row stride is not aligned as required */
+  NVFP4_ERR_NULL = 3,       /* a required pointer is NULL */
+  NVFP4_ERR_WORKSPACE = 4,  /* workspace missing or smaller than required */
+  NVFP4_ERR_DTYPE = 5,      /* unknown output dtype code */
+  NVFP4_ERR_CUDA = 6,       /* a CUDA runtime/driver call failed */
+  NVFP4_ERR_NONFINITE = 7,  /* device status: W held an Inf or NaN */
+  NVFP4_ERR_TIMEOUT = 8,    /* device status: a pipeline wait ran out of time */
+  NVFP4_ERR_UNSUPPORTED = 9 /* no sm_103a device / kernel image for it */
+} nvfp4_status;
+
+/* Output dtype codes of w4a16_lm_head. */
+#define NVFP4_OUT_F32 0
+#define NVFP4_OUT_BF16 1
+
+/* Human-readable name of a status; never NULL. */
+const char *nvfp4_status_string(nvfp4_status status);
+
+/* ABI version of this header (major * 100 + minor). */
+int nvfp4_abi_version(void);
+
+/* ------------------------------------------------------------ quantizer */
+
+/*
+ * Workspace bytes nvfp4_quantize_rows / nvfp4_refresh need for W[N, K]:
+ * per-block partial maxima of the first pass plus the device status word.
+ * Returns 0 for shapes the quantizer rejects.
+ */
+size_t nvfp4_quantize_workspace_bytes(int64_t N, int64_t K);
+
+/*
+ * NVFP4-quantize the rows of W (`_quantize_nvfp4`).
+ *
+ *   W            bf16 [N, K], device, 16-byte aligned.  Read only.
+ *   N, K         N >= 1; K >= 16 and K % 16 == 0 (the K % 16 rule of
+ *                `KNvfp4Static.create_weights`).
+ *   packed       u8 [N, K/2], device, 16-byte aligned.  Written: byte j of
+ *                row n holds the code of W[n, 2j] in bits 3..0 and of
+ *                W[n, 2j+1] in bits 7..4; code = grid index | (value < 0) << 3.
+ *   scales       u8 (float8_e4m3fn) [N, K/16], device.  Written, row-major
+ *                (not swizzled).
+ *   global_scale f32 [1], device.  Written: max(amax / 2688, 1e-12).
+ *   workspace    device, >= nvfp4_quantize_workspace_bytes(N, K), 256-byte
+ *                aligned.  Scratch; also holds the device status word.
+ *
+ * Two kernels run on `stream`: a grid-wide amax and the per-row encoder.
+ * Nothing is read back to the host, so the call can be captured in a CUDA
+ * graph.  If W holds an Inf or NaN the status word becomes
+ * NVFP4_ERR_NONFINITE, global_scale is set to NaN and packed/scales are left
+ * unspecified (the pages assume finite weights).
+ */
+nvfp4_status nvfp4_quantize_rows(const void *W, int64_t N, int64_t K, uint8_t *packed,
+                                 uint8_t *scales, float *global_scale, void *workspace,
+                                 size_t workspace_bytes, void *stream);
+
+/*
+ * Re-derive the quantized copy of W in place (`refresh_quantized_lm_heads`):
+ * the same computation and arguments as nvfp4_quantize_rows, writing into
+ * the caller's existing packed / scales / global_scale buffers, so that
+ * device addresses captured by CUDA graphs stay valid.  No allocation, no
+ * host synchronization.
+ */
+nvfp4_status nvfp4_refresh(const void *W, int64_t N, int64_t K, uint8_t *packed,
+                           uint8_t *scales, float *global_scale, void *workspace,
+                           size_t workspace_bytes, void *stream);
+
+/*
+ * Read the device status word that the last call using `workspace` left
+ * (NVFP4_OK, NVFP4_ERR_NONFINITE or NVFP4_ERR_TIMEOUT) into *status_out.
+ * SYNCHRONIZES `stream`; meant for tests and diagnostics, not the hot path.
+ * Works for both quantizer and lm_head workspaces.
+ */
+nvfp4_status nvfp4_read_device_status(const void *workspace, int32_t *status_out, void *stream);
+
+/* --------------------------------------------------------- W4A16 GEMM */
+
+/*
+ * Workspace bytes w4a16_lm_head needs for x[M, K] against N vocabulary rows:
+ * the activations rescaled to fp16 (M * K * 2 bytes), one fp32 scale per
+ * token, the device status word and room for split-K partial tiles.
+ * Returns 0 for shapes the call rejects.
+ */
+size_t w4a16_lm_head_workspace_bytes(int64_t M, int64_t N, int64_t K);
+
+/*
+ * logits = x . dequant(W)^T with dequant(W)[n, k] =
+ * e2m1(code[n, k]) * f32(scale[n, k/16]) * global_scale.
+ *
+ *   x            bf16 [M, K], device, 16-byte aligned.  M >= 0 (M == 0 is a
+ *                no-op), K >= 256 and K % 256 == 0 (the row strides of the
+ *                packed and scale tensors must be 16-byte multiples for the
+ *                tensor-memory-access copies; all lm_head widths are).
+ *   packed, scales, global_scale
+ *                exactly as nvfp4_quantize_rows writes them for W[N, K];
+ *                packed and scales 16-byte aligned.
+ *   N            vocabulary rows, N >= 0 (N == 0 is a no-op).
+ *   logits       [M, N] device, 16-byte aligned; fp32 (out_dtype
+ *                NVFP4_OUT_F32) or bf16 (NVFP4_OUT_BF16, round to nearest even).
+ *   workspace    device, >= w4a16_lm_head_workspace_bytes(M, N, K),
+ *                256-byte aligned.
+ *
+ * Accumulation is fp32 on the tensor cores; each product x * w is exact.
+ * The activations are carried into the tensor cores as fp16 after an exact
+ * power-of-two rescale per token (exact for every bf16 value within 2^28
+ * of the token's largest magnitude; smaller ones keep at least an absolute
+ * accuracy of 2^-39 of that maximum).  The result is deterministic: no
+ * floating-point atomics, fixed reduction order.
+ */
+nvfp4_status w4a16_lm_head(const void *x, int64_t M, int64_t K, const uint8_t *packed,
+                           const uint8_t *scales, const float *global_scale, int64_t N,
+                           void *logits, int out_dtype, void *workspace, size_t workspace_bytes,
+                           void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* NVFP4_LM_HEAD_H_ */

@@ -1,0 +1,217 @@
+"""Online NVFP4 lm_head for GB300 (sm_103a): a thin ctypes binding.
+
+Every step of the path runs in the CUDA kernels of ``libnvfp4_lm_head.so``
+(see ``include/nvfp4_lm_head.h``); this module only checks tensor metadata,
+allocates outputs and workspaces with PyTorch when the caller gives none,
+and passes device pointers plus the current CUDA stream through the C ABI.
+There is no CPU or PyTorch fallback: if the library is missing, every call
+raises.
+
+Entry points (same names as the C ABI):
+
+* ``nvfp4_quantize_rows(W)`` -> ``(packed u8[N,K/2], scales e4m3[N,K/16], global f32[1])``
+  -- ``_quantize_nvfp4`` of the page
+  "vllm.model_executor.layers.quantization.online.lm_head".
+* ``nvfp4_refresh(W, packed, scales, global_scale)`` -- in-place re-derivation
+  (``refresh_quantized_lm_heads``); the buffers keep their addresses.
+* ``w4a16_lm_head(x, packed, scales, global_scale)`` -> ``logits[M, N]`` -- the
+  weight-only W4A16 product (``_LMHeadNvfp4Method.apply``).
+"""
+from __future__ import annotations
+
+import ctypes
+import enum
+import os
+
+import torch
+
+__all__ = [
+    "NVFP4Error", "Status", "library_path", "load_library", "nvfp4_quantize_rows",
+    "nvfp4_refresh", "w4a16_lm_head", "nvfp4_quantize_workspace_bytes",
+    "w4a16_lm_head_workspace_bytes", "nvfp4_read_device_status", "OUT_F32", "OUT_BF16",
+]
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "libnvfp4_lm_head.so")
+_lib = None
+
+OUT_F32 = 0
+OUT_BF16 = 1
+
+
+class Status(enum.IntEnum):
+    OK = 0
+    ERR_SHAPE = 1
+    ERR_ALIGN = 2
+    ERR_NULL = 3
+    ERR_WORKSPACE = 4
+    ERR_DTYPE = 5
+    ERR_CUDA = 6
+    ERR_NONFINITE = 7
+    ERR_TIMEOUT = 8
+    ERR_UNSUPPORTED = 9
+
+
+class NVFP4Error(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = Status(status)
+        msg = load_library().nvfp4_status_string(int(status)).decode()
+        super().__init__(f"{where}: {self.status.name} ({msg})")
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def load_library() -> ctypes.CDLL:
+    """Load the CUDA library; raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(_LIB_PATH):
+        raise RuntimeError(
+            f"{_LIB_PATH} is missing: build it first "
+            "(python -c 'import __graft_entry__ as g; g.build()')")
+    lib = ctypes.CDLL(_LIB_PATH)
+    vp, i64, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_size_t
+    st = ctypes.c_int
+    lib.nvfp4_status_string.argtypes = [st]
+    lib.nvfp4_status_string.restype = ctypes.c_char_p
+    lib.nvfp4_abi_version.restype = ctypes.c_int
+    lib.nvfp4_quantize_workspace_bytes.argtypes = [i64, i64]
+    lib.nvfp4_quantize_workspace_bytes.restype = sz
+    for name in ("nvfp4_quantize_rows", "nvfp4_refresh"):
+        f = getattr(lib, name)
+        f.argtypes = [vp, i64, i64, vp, vp, vp, vp, sz, vp]
+        f.restype = st
+    lib.nvfp4_read_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_int32), vp]
+    lib.nvfp4_read_device_status.restype = st
+    lib.w4a16_lm_head_workspace_bytes.argtypes = [i64, i64, i64]
+    lib.w4a16_lm_head_workspace_bytes.restype = sz
+    lib.w4a16_lm_head.argtypes = [vp, i64, i64, vp, vp, vp, i64, vp, ctypes.c_int, vp, sz, vp]
+    lib.w4a16_lm_head.restype = st
+    _lib = lib
+    return lib
+
+
+def _ptr(t: torch.Tensor | None) -> ctypes.c_void_p:
+    return ctypes.c_void_p(t.data_ptr() if t is not None else 0)
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _check(rc: int, where: str) -> None:
+    if rc != 0:
+        raise NVFP4Error(rc, where)
+
+
+def _need(t: torch.Tensor, dtype, name: str, shape=None) -> None:
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+
+
+def _workspace(nbytes: int, device) -> torch.Tensor:
+    # 256-byte alignment: torch's caching allocator returns 512-byte aligned blocks
+    return torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
+
+
+def nvfp4_quantize_workspace_bytes(N: int, K: int) -> int:
+    return int(load_library().nvfp4_quantize_workspace_bytes(N, K))
+
+
+def w4a16_lm_head_workspace_bytes(M: int, N: int, K: int) -> int:
+    return int(load_library().w4a16_lm_head_workspace_bytes(M, N, K))
+
+
+def nvfp4_quantize_rows(W: torch.Tensor, packed: torch.Tensor | None = None,
+                        scales: torch.Tensor | None = None,
+                        global_scale: torch.Tensor | None = None,
+                        workspace: torch.Tensor | None = None, stream=None):
+    """Quantize W bf16[N, K] to (packed u8[N, K/2], scales e4m3[N, K/16], global f32[1])."""
+    lib = load_library()
+    _need(W, torch.bfloat16, "W")
+    if W.dim() != 2:
+        raise ValueError("W must be 2-D [N, K]")
+    N, K = W.shape
+    dev = W.device
+    if packed is None:
+        packed = torch.empty(N, K // 2, dtype=torch.uint8, device=dev)
+    if scales is None:
+        scales = torch.empty(N, K // 16, dtype=torch.float8_e4m3fn, device=dev)
+    if global_scale is None:
+        global_scale = torch.empty(1, dtype=torch.float32, device=dev)
+    _quantize_into(lib.nvfp4_quantize_rows, "nvfp4_quantize_rows", W, packed, scales,
+                   global_scale, workspace, stream)
+    return packed, scales, global_scale
+
+
+def nvfp4_refresh(W: torch.Tensor, packed: torch.Tensor, scales: torch.Tensor,
+                  global_scale: torch.Tensor, workspace: torch.Tensor | None = None,
+                  stream=None) -> None:
+    """Re-derive the quantized copy of W into the existing buffers (addresses kept)."""
+    lib = load_library()
+    _need(W, torch.bfloat16, "W")
+    _quantize_into(lib.nvfp4_refresh, "nvfp4_refresh", W, packed, scales, global_scale,
+                   workspace, stream)
+
+
+def _quantize_into(fn, where, W, packed, scales, global_scale, workspace, stream):
+    N, K = W.shape
+    _need(packed, torch.uint8, "packed", (N, K // 2))
+    if scales.dtype not in (torch.float8_e4m3fn, torch.uint8):
+        raise ValueError("scales must be float8_e4m3fn (or uint8 bit patterns)")
+    _need(scales, scales.dtype, "scales", (N, K // 16))
+    _need(global_scale, torch.float32, "global_scale")
+    need = nvfp4_quantize_workspace_bytes(N, K)
+    if workspace is None:
+        workspace = _workspace(need, W.device)
+    rc = fn(_ptr(W), N, K, _ptr(packed), _ptr(scales), _ptr(global_scale), _ptr(workspace),
+            workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(rc, where)
+
+
+def w4a16_lm_head(x: torch.Tensor, packed: torch.Tensor, scales: torch.Tensor,
+                  global_scale: torch.Tensor, out: torch.Tensor | None = None,
+                  out_dtype: torch.dtype = torch.float32,
+                  workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """logits[M, N] = x . dequant(W)^T for x bf16[M, K] and the packed NVFP4 weight."""
+    lib = load_library()
+    _need(x, torch.bfloat16, "x")
+    M, K = x.shape
+    N = packed.shape[0]
+    _need(packed, torch.uint8, "packed", (N, K // 2))
+    _need(scales, scales.dtype, "scales", (N, K // 16))
+    _need(global_scale, torch.float32, "global_scale")
+    if out is None:
+        out = torch.empty(M, N, dtype=out_dtype, device=x.device)
+    _need(out, out.dtype, "out", (M, N))
+    code = {torch.float32: OUT_F32, torch.bfloat16: OUT_BF16}.get(out.dtype)
+    if code is None:
+        raise ValueError("out must be float32 or bfloat16")
+    need = w4a16_lm_head_workspace_bytes(M, N, K)
+    if workspace is None:
+        workspace = _workspace(need, x.device)
+    rc = lib.w4a16_lm_head(_ptr(x), M, K, _ptr(packed), _ptr(scales), _ptr(global_scale), N,
+                           _ptr(out), code, _ptr(workspace),
+                           workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(rc, "w4a16_lm_head")
+    return out
+
+
+def nvfp4_read_device_status(workspace: torch.Tensor, stream=None) -> Status:
+    """Status word a kernel left in `workspace` (synchronizes the stream)."""
+    v = ctypes.c_int32(0)
+    rc = load_library().nvfp4_read_device_status(_ptr(workspace), ctypes.byref(v),
+                                                 _stream(stream))
+    _check(rc, "nvfp4_read_device_status")
+    return Status(v.value)

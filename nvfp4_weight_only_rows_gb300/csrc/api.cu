@@ -1,0 +1,133 @@
+// api.cu -- the extern "C" entry points declared in include/nvfp4_lm_head.h:
+// host-side argument checks, workspace sizing and dispatch to the kernels in
+// quantize.cu and lm_head.cu.  No entry point allocates device memory.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "common.cuh"
+
+namespace nvfp4 {
+size_t quantize_workspace_bytes();
+nvfp4_status quantize_launch(const void* W, int64_t N, int64_t K, uint8_t* packed,
+                             uint8_t* scales, float* global_scale, void* workspace,
+                             cudaStream_t stream);
+size_t lm_head_workspace_bytes(int64_t M, int64_t N, int64_t K);
+nvfp4_status lm_head_launch(const void* x, int64_t M, int64_t K, const uint8_t* packed,
+                            const uint8_t* scales, const float* global_scale, int64_t N,
+                            void* logits, int out_dtype, void* workspace, cudaStream_t stream);
+
+static bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// The kernels are built for sm_103a only; refuse other devices up front.
+static nvfp4_status check_device() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return NVFP4_ERR_CUDA;
+  int major = 0, minor = 0;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+    return NVFP4_ERR_CUDA;
+  if (major != 10 || minor != 3) return NVFP4_ERR_UNSUPPORTED;
+  return NVFP4_OK;
+}
+
+static constexpr int64_t kMaxDim = (int64_t)1 << 31;
+
+static nvfp4_status check_quantize_args(const void* W, int64_t N, int64_t K, const uint8_t* packed,
+                                        const uint8_t* scales, const float* global_scale,
+                                        const void* workspace, size_t workspace_bytes) {
+  if (N <= 0 || K <= 0 || K % 16 != 0 || N >= kMaxDim || K >= kMaxDim) return NVFP4_ERR_SHAPE;
+  if (!W || !packed || !scales || !global_scale) return NVFP4_ERR_NULL;
+  if (!workspace || workspace_bytes < quantize_workspace_bytes()) return NVFP4_ERR_WORKSPACE;
+  if (!aligned(W, 16) || !aligned(packed, 16) || !aligned(global_scale, 4) ||
+      !aligned(workspace, 256))
+    return NVFP4_ERR_ALIGN;
+  return check_device();
+}
+
+}  // namespace nvfp4
+
+using namespace nvfp4;
+
+extern "C" {
+
+const char* nvfp4_status_string(nvfp4_status s) {
+  switch (s) {
+    case NVFP4_OK: return "ok";
+    case NVFP4_ERR_SHAPE: return "shape out of range";
+    case NVFP4_ERR_ALIGN: return "pointer not aligned as required";
+    case NVFP4_ERR_NULL: return "required pointer is NULL";
+    case NVFP4_ERR_WORKSPACE: return "workspace missing or too small";
+    case NVFP4_ERR_DTYPE: return "unknown output dtype";
+    case NVFP4_ERR_CUDA: return "CUDA call failed";
+    case NVFP4_ERR_NONFINITE: return "weight holds Inf or NaN";
+    case NVFP4_ERR_TIMEOUT: return "device pipeline wait timed out";
+    case NVFP4_ERR_UNSUPPORTED: return "device is not sm_103 (GB300)";
+  }
+  return "unknown status";
+}
+
+int nvfp4_abi_version(void) { return 100; }
+
+size_t nvfp4_quantize_workspace_bytes(int64_t N, int64_t K) {
+  if (N <= 0 || K <= 0 || K % 16 != 0) return 0;
+  return quantize_workspace_bytes();
+}
+
+nvfp4_status nvfp4_quantize_rows(const void* W, int64_t N, int64_t K, uint8_t* packed,
+                                 uint8_t* scales, float* global_scale, void* workspace,
+                                 size_t workspace_bytes, void* stream) {
+  nvfp4_status st =
+      check_quantize_args(W, N, K, packed, scales, global_scale, workspace, workspace_bytes);
+  if (st != NVFP4_OK) return st;
+  return quantize_launch(W, N, K, packed, scales, global_scale, workspace,
+                         static_cast<cudaStream_t>(stream));
+}
+
+nvfp4_status nvfp4_refresh(const void* W, int64_t N, int64_t K, uint8_t* packed, uint8_t* scales,
+                           float* global_scale, void* workspace, size_t workspace_bytes,
+                           void* stream) {
+  // Same kernels, same buffers: re-deriving in place is what keeps the
+  // addresses captured by CUDA graphs valid.
+  return nvfp4_quantize_rows(W, N, K, packed, scales, global_scale, workspace, workspace_bytes,
+                             stream);
+}
+
+nvfp4_status nvfp4_read_device_status(const void* workspace, int32_t* status_out, void* stream) {
+  if (!workspace || !status_out) return NVFP4_ERR_NULL;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int32_t v = 0;
+  if (cudaMemcpyAsync(&v, workspace, sizeof(v), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+      cudaStreamSynchronize(s) != cudaSuccess)
+    return NVFP4_ERR_CUDA;
+  *status_out = v;
+  return NVFP4_OK;
+}
+
+size_t w4a16_lm_head_workspace_bytes(int64_t M, int64_t N, int64_t K) {
+  if (M < 0 || N < 0 || K < 256 || K % 256 != 0) return 0;
+  return lm_head_workspace_bytes(M, N, K);
+}
+
+nvfp4_status w4a16_lm_head(const void* x, int64_t M, int64_t K, const uint8_t* packed,
+                           const uint8_t* scales, const float* global_scale, int64_t N,
+                           void* logits, int out_dtype, void* workspace, size_t workspace_bytes,
+                           void* stream) {
+  if (M < 0 || N < 0 || K < 256 || K % 256 != 0 || M >= kMaxDim || N >= kMaxDim ||
+      K >= kMaxDim)
+    return NVFP4_ERR_SHAPE;
+  if (out_dtype != NVFP4_OUT_F32 && out_dtype != NVFP4_OUT_BF16) return NVFP4_ERR_DTYPE;
+  if (M == 0 || N == 0) return NVFP4_OK;  // empty product: nothing to write
+  if (!x || !packed || !scales || !global_scale || !logits) return NVFP4_ERR_NULL;
+  if (!workspace || workspace_bytes < lm_head_workspace_bytes(M, N, K))
+    return NVFP4_ERR_WORKSPACE;
+  if (!aligned(x, 16) || !aligned(packed, 16) || !aligned(scales, 16) ||
+      !aligned(global_scale, 4) || !aligned(logits, 16) || !aligned(workspace, 256))
+    return NVFP4_ERR_ALIGN;
+  nvfp4_status st = check_device();
+  if (st != NVFP4_OK) return st;
+  return lm_head_launch(x, M, K, packed, scales, global_scale, N, logits, out_dtype, workspace,
+                        static_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"

@@ -1,0 +1,533 @@
+// lm_head.cu -- the weight-only W4A16 lm_head product on sm_103a tensor cores.
+//
+// logits[m, n] = global * sum_k x[m, k] * e2m1(code[n, k]) * f32(scale[n, k/16])
+// (`CompressedTensorsW4A16Fp4.apply_weights` on the page
+// "vllm.model_executor.layers.quantization.compressed_tensors.schemes", with
+// the checkpoint layout `_quantize_nvfp4` writes on the page
+// "vllm.model_executor.layers.quantization.online.lm_head").
+//
+// Two kernels per call:
+//  1. w4a16_prep_x_kernel: each token row of x (bf16) is rescaled by an
+//     exact power of two 2^e so that its largest magnitude lands in
+//     [2^14, 2^15), and stored as fp16 in the workspace; the token's output
+//     multiplier global * 2^-e is stored beside it.  fp16 holds every bf16
+//     value of that row exactly down to 2^-28 of the row maximum.
+//  2. w4a16_tc_kernel: a persistent, warp-specialized tcgen05 GEMM in the
+//     swapped orientation D[vocab row, token] = A . B^T:
+//       A = dequantized weights, 128 vocabulary rows x 64 k per stage, held
+//           in TENSOR MEMORY (the "ts" MMA form), written by four dequant
+//           warps with one thread per row: e2m1 pairs -> fp16 pairs with the
+//           hardware cvt, times the E4M3 block scale (fp16, exact);
+//       B = the fp16 activations, a TMA tile [BN tokens x 64 k] in shared
+//           memory with the 128-byte swizzle;
+//       D = fp32 accumulators in tensor memory, double buffered, drained by
+//           four epilogue warps (tcgen05.ld, x token multiplier, store).
+//     Packed codes and scales arrive by TMA in 256-k stages; every product
+//     x * w is exact in fp32, so the only rounding is the fp32 summation.
+//
+// Warp roles (352 threads): 0 packed/scale TMA producer, 1 activation TMA
+// producer, 2 MMA issuer (and TMEM owner), 3-6 dequant, 7-10 epilogue.
+// Every pipeline wait is bounded in time; on expiry the CTA raises
+// NVFP4_ERR_TIMEOUT in the workspace status word, drains what it issued and
+// returns.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <mutex>
+
+#include "common.cuh"
+
+namespace nvfp4 {
+
+constexpr int kRows = 128;          // vocabulary rows per tile (MMA M)
+constexpr int kKB = 64;             // k per A / activation stage
+constexpr int kKS = 256;            // k per packed/scale stage
+constexpr int kPStages = 4;         // packed/scale ring depth (18 KB each)
+constexpr int kXStages = 6;         // activation ring depth
+constexpr int kAStages = 4;         // TMEM A ring depth (32 columns each)
+constexpr int kThreads = 352;
+constexpr uint32_t kPackedStageBytes = kRows * (kKS / 2);   // 16384
+constexpr uint32_t kScaleStageBytes = kRows * (kKS / 16);   // 2048
+constexpr int kMaxBN = 128;
+constexpr uint64_t kWaitLimitNs = 2000000000ull;            // 2 s per pipeline wait
+
+struct GemmArgs {
+  int64_t M, N, K;
+  int BN;              // token tile, multiple of 16, <= 128
+  int n_ttiles;        // token tiles
+  int64_t n_units;     // weight tiles x token tiles
+  uint32_t tmem_cols;  // allocated TMEM columns
+  const float* tok_scale;
+  void* out;
+  int32_t* status;
+};
+
+// ------------------------------------------------------------ activations
+__global__ void __launch_bounds__(256) w4a16_prep_x_kernel(const uint16_t* __restrict__ x,
+                                                           int64_t M, int64_t K,
+                                                           const float* __restrict__ global,
+                                                           __half* __restrict__ x16,
+                                                           float* __restrict__ tok_scale) {
+  const int64_t m = blockIdx.x;
+  __half* dst = x16 + m * K;
+  const int64_t nv = K / 8;
+  if (m >= M) {  // padding rows of the last token tile
+    for (int64_t i = threadIdx.x; i < nv; i += blockDim.x)
+      reinterpret_cast<uint4*>(dst)[i] = make_uint4(0, 0, 0, 0);
+    return;
+  }
+  const uint4* src = reinterpret_cast<const uint4*>(x + m * K);
+  uint32_t mx = 0;
+  for (int64_t i = threadIdx.x; i < nv; i += blockDim.x) {
+    uint4 v = src[i];
+    const uint32_t k = 0x7FFF7FFFu;
+    mx = __vmaxu2(mx, v.x & k);
+    mx = __vmaxu2(mx, v.y & k);
+    mx = __vmaxu2(mx, v.z & k);
+    mx = __vmaxu2(mx, v.w & k);
+  }
+  mx = max(mx & 0xFFFFu, mx >> 16);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
+  __shared__ uint32_t red[8];
+  __shared__ int s_e;
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = mx;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    uint32_t a = 0;
+    for (int w = 0; w < (int)(blockDim.x >> 5); ++w) a = max(a, red[w]);
+    int e = 0;
+    if (a != 0 && a < 0x7F80u) {
+      const int E = ilogbf(__uint_as_float(a << 16));  // floor(log2(max|x|))
+      e = min(max(14 - E, -126), 126);
+    }
+    s_e = e;
+    tok_scale[m] = __fmul_rn(*global, __int_as_float((127 - e) << 23));
+  }
+  __syncthreads();
+  const float p2 = __int_as_float((127 + s_e) << 23);
+  uint4* d4 = reinterpret_cast<uint4*>(dst);
+  for (int64_t i = threadIdx.x; i < nv; i += blockDim.x) {
+    uint4 v = src[i];
+    uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float lo = __fmul_rn(__uint_as_float(w[j] << 16), p2);
+      const float hi = __fmul_rn(__uint_as_float(w[j] & 0xFFFF0000u), p2);
+      __half2 h = __floats2half2_rn(lo, hi);
+      o[j] = *reinterpret_cast<uint32_t*>(&h);
+    }
+    d4[i] = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+}
+
+// ------------------------------------------------------------ dequant helpers
+// 8 e2m1 codes (one word; byte j = codes 2j | 2j+1 << 4) -> 4 fp16 pairs,
+// element 2j in the low half, each multiplied by the block scale pair sf2.
+__device__ __forceinline__ void dequant8(uint32_t w, uint32_t sf2, uint32_t* out) {
+  uint32_t h0, h1, h2, h3;
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+      "mov.b32 {b0, b1, b2, b3}, %4;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %0, b0;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %2, b2;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+      : "=r"(h0), "=r"(h1), "=r"(h2), "=r"(h3)
+      : "r"(w));
+  asm("mul.rn.f16x2 %0, %0, %4;\n\t"
+      "mul.rn.f16x2 %1, %1, %4;\n\t"
+      "mul.rn.f16x2 %2, %2, %4;\n\t"
+      "mul.rn.f16x2 %3, %3, %4;"
+      : "+r"(h0), "+r"(h1), "+r"(h2), "+r"(h3)
+      : "r"(sf2));
+  out[0] = h0;
+  out[1] = h1;
+  out[2] = h2;
+  out[3] = h3;
+}
+
+// 4 E4M3 scale bytes -> two fp16 pairs (s0, s1) and (s2, s3)
+__device__ __forceinline__ void scales4_to_f16(uint32_t s, uint32_t& s01, uint32_t& s23) {
+  asm("{\n\t.reg .b16 lo, hi;\n\t"
+      "mov.b32 {lo, hi}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, lo;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %1, hi;\n\t}"
+      : "=r"(s01), "=r"(s23)
+      : "r"(s));
+}
+
+__device__ __forceinline__ uint32_t dup_lo(uint32_t v) { return __byte_perm(v, 0, 0x1010); }
+__device__ __forceinline__ uint32_t dup_hi(uint32_t v) { return __byte_perm(v, 0, 0x3232); }
+
+// warp-uniform bounded wait: every lane polls, the warp agrees on the outcome
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const WaitCtl& wc) {
+  const bool ok = mbar_wait(bar, parity, wc);
+  return __all_sync(0xFFFFFFFFu, ok);
+}
+
+// ------------------------------------------------------------ the GEMM
+template <bool kOutBf16>
+__global__ void __launch_bounds__(kThreads, 1)
+    w4a16_tc_kernel(const __grid_constant__ CUtensorMap tm_packed,
+                    const __grid_constant__ CUtensorMap tm_scales,
+                    const __grid_constant__ CUtensorMap tm_x, const GemmArgs p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  const int BN = p.BN;
+  const uint32_t x_stage_bytes = (uint32_t)BN * (kKB * 2);
+  uint8_t* s_packed = smem;                                        // kPStages x 16 KB
+  uint8_t* s_scales = s_packed + kPStages * kPackedStageBytes;     // kPStages x 2 KB
+  uint8_t* s_x = s_scales + kPStages * kScaleStageBytes;           // kXStages x BN*128
+  uint64_t* bars = reinterpret_cast<uint64_t*>(s_x + kXStages * x_stage_bytes);
+  uint64_t* p_full = bars;
+  uint64_t* p_empty = p_full + kPStages;
+  uint64_t* x_full = p_empty + kPStages;
+  uint64_t* x_empty = x_full + kXStages;
+  uint64_t* a_full = x_empty + kXStages;
+  uint64_t* a_empty = a_full + kAStages;
+  uint64_t* d_full = a_empty + kAStages;
+  uint64_t* d_empty = d_full + 2;
+  uint64_t* done_bar = d_empty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done_bar + 1);
+  volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kPStages; ++i) {
+      mbar_init(&p_full[i], 1);
+      mbar_init(&p_empty[i], 4);
+    }
+    for (int i = 0; i < kXStages; ++i) {
+      mbar_init(&x_full[i], 1);
+      mbar_init(&x_empty[i], 1);
+    }
+    for (int i = 0; i < kAStages; ++i) {
+      mbar_init(&a_full[i], 4);
+      mbar_init(&a_empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&d_full[i], 1);
+      mbar_init(&d_empty[i], 4);
+    }
+    mbar_init(done_bar, 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tm_packed);
+    tma_prefetch_desc(&tm_scales);
+    tma_prefetch_desc(&tm_x);
+  }
+  if (warp == 2) {
+    tmem_alloc(tmem_slot, p.tmem_cols);
+    tc_fence_before();
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const uint32_t tmem_a = tmem_base + 2 * BN;  // A ring after the two D buffers
+
+  WaitCtl wc{p.status, abort_flag, kWaitLimitNs};
+  const int64_t K = p.K;
+  const int n_super = (int)(K / kKS);
+  const int n_kb = (int)(K / kKB);
+
+  if (warp == 0) {
+    // ---------------- packed codes + scales producer
+    if (lane == 0) {
+      const uint64_t pol = policy_evict_first();
+      uint32_t st = 0, ph = 0, issued = 0;
+      bool ok = true;
+      for (int64_t u = blockIdx.x; ok && u < p.n_units; u += gridDim.x) {
+        const int32_t n0 = (int32_t)((u / p.n_ttiles) * kRows);
+        for (int sb = 0; sb < n_super; ++sb) {
+          if (!mbar_wait(&p_empty[st], ph ^ 1, wc)) { ok = false; break; }
+          mbar_arrive_expect_tx(&p_full[st], kPackedStageBytes + kScaleStageBytes);
+          tma_load_2d_hint(s_packed + st * kPackedStageBytes, &tm_packed, sb * (kKS / 2), n0,
+                           &p_full[st], pol);
+          tma_load_2d_hint(s_scales + st * kScaleStageBytes, &tm_scales, sb * (kKS / 16), n0,
+                           &p_full[st], pol);
+          ++issued;
+          if (++st == kPStages) { st = 0; ph ^= 1; }
+        }
+      }
+      // drain: wait (bounded) until the last load of every slot has landed
+      WaitCtl drain{p.status, abort_flag, 100000000ull};
+      volatile int32_t zero = 0;
+      drain.abort = &zero;
+      for (uint32_t s = 0; s < kPStages && s < issued; ++s) {
+        const uint32_t fills = issued / kPStages + (s < issued % kPStages ? 1u : 0u);
+        mbar_wait(&p_full[s], (fills - 1) & 1, drain);
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------- activation producer
+    if (lane == 0) {
+      const uint64_t pol = policy_evict_last();
+      uint32_t st = 0, ph = 0, issued = 0;
+      bool ok = true;
+      for (int64_t u = blockIdx.x; ok && u < p.n_units; u += gridDim.x) {
+        const int32_t t0 = (int32_t)((u % p.n_ttiles) * BN);
+        for (int kb = 0; kb < n_kb; ++kb) {
+          if (!mbar_wait(&x_empty[st], ph ^ 1, wc)) { ok = false; break; }
+          mbar_arrive_expect_tx(&x_full[st], x_stage_bytes);
+          tma_load_2d_hint(s_x + st * x_stage_bytes, &tm_x, kb * kKB, t0, &x_full[st], pol);
+          ++issued;
+          if (++st == kXStages) { st = 0; ph ^= 1; }
+        }
+      }
+      WaitCtl drain{p.status, abort_flag, 100000000ull};
+      volatile int32_t zero = 0;
+      drain.abort = &zero;
+      for (uint32_t s = 0; s < kXStages && s < issued; ++s) {
+        const uint32_t fills = issued / kXStages + (s < issued % kXStages ? 1u : 0u);
+        mbar_wait(&x_full[s], (fills - 1) & 1, drain);
+      }
+    }
+  } else if (warp == 2) {
+    // ---------------- MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc = idesc_f16_f32((uint32_t)BN);
+      uint32_t as = 0, aph = 0, xs = 0, xph = 0;
+      bool ok = true;
+      int64_t i = 0;
+      for (int64_t u = blockIdx.x; ok && u < p.n_units; u += gridDim.x, ++i) {
+        const uint32_t buf = (uint32_t)(i & 1), dph = (uint32_t)((i >> 1) & 1);
+        if (!mbar_wait(&d_empty[buf], dph ^ 1, wc)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + buf * BN;
+        for (int kb = 0; kb < n_kb; ++kb) {
+          if (!mbar_wait(&a_full[as], aph, wc) || !mbar_wait(&x_full[xs], xph, wc)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t xa = smem_u32(s_x + xs * x_stage_bytes);
+#pragma unroll
+          for (int kk = 0; kk < kKB / 16; ++kk) {
+            tc_mma_ts(d_tmem, tmem_a + as * 32 + kk * 8, smem_desc_sw128(xa + kk * 32), idesc,
+                      (kb | kk) != 0);
+          }
+          tc_commit(&a_empty[as]);
+          tc_commit(&x_empty[xs]);
+          if (++as == kAStages) { as = 0; aph ^= 1; }
+          if (++xs == kXStages) { xs = 0; xph ^= 1; }
+        }
+        if (ok) tc_commit(&d_full[buf]);
+      }
+      // every MMA issued above has completed once done_bar flips
+      tc_commit(done_bar);
+      WaitCtl drain{p.status, abort_flag, 100000000ull};
+      volatile int32_t zero = 0;
+      drain.abort = &zero;
+      mbar_wait(done_bar, 0, drain);
+    }
+  } else if (warp <= 6) {
+    // ---------------- dequant: one thread per vocabulary row of the tile
+    const int q = warp & 3;
+    const int row = q * 32 + lane;
+    const uint32_t lane_off = (uint32_t)(q * 32) << 16;
+    const int sw = row & 7;
+    uint32_t ps = 0, pph = 0, as = 0, aph = 0;
+    bool ok = true;
+    for (int64_t u = blockIdx.x; ok && u < p.n_units; u += gridDim.x) {
+      for (int sb = 0; ok && sb < n_super; ++sb) {
+        if (!warp_wait(&p_full[ps], pph, wc)) { ok = false; break; }
+        const uint8_t* prow = s_packed + ps * kPackedStageBytes + row * (kKS / 2);
+        const uint4 sc = *reinterpret_cast<const uint4*>(s_scales + ps * kScaleStageBytes +
+                                                         row * (kKS / 16));
+        const uint32_t scw[4] = {sc.x, sc.y, sc.z, sc.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const uint4 c0 = *reinterpret_cast<const uint4*>(prow + (((2 * j) ^ sw) << 4));
+          const uint4 c1 = *reinterpret_cast<const uint4*>(prow + (((2 * j + 1) ^ sw) << 4));
+          uint32_t s01, s23;
+          scales4_to_f16(scw[j], s01, s23);
+          const uint32_t f0 = dup_lo(s01), f1 = dup_hi(s01), f2 = dup_lo(s23), f3 = dup_hi(s23);
+          uint32_t v[32];
+          dequant8(c0.x, f0, v + 0);
+          dequant8(c0.y, f0, v + 4);
+          dequant8(c0.z, f1, v + 8);
+          dequant8(c0.w, f1, v + 12);
+          dequant8(c1.x, f2, v + 16);
+          dequant8(c1.y, f2, v + 20);
+          dequant8(c1.z, f3, v + 24);
+          dequant8(c1.w, f3, v + 28);
+          if (!warp_wait(&a_empty[as], aph ^ 1, wc)) { ok = false; break; }
+          tmem_st32(tmem_a + lane_off + as * 32, reinterpret_cast<uint32_t(&)[32]>(v));
+          tc_wait_st();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&a_full[as]);
+          if (++as == kAStages) { as = 0; aph ^= 1; }
+        }
+        __syncwarp();
+        if (ok && lane == 0) mbar_arrive(&p_empty[ps]);
+        if (++ps == kPStages) { ps = 0; pph ^= 1; }
+      }
+    }
+  } else {
+    // ---------------- epilogue: one thread per vocabulary row, BN tokens
+    const int q = warp & 3;
+    const int row = q * 32 + lane;
+    const uint32_t lane_off = (uint32_t)(q * 32) << 16;
+    int64_t i = 0;
+    for (int64_t u = blockIdx.x; u < p.n_units; u += gridDim.x, ++i) {
+      const uint32_t buf = (uint32_t)(i & 1), dph = (uint32_t)((i >> 1) & 1);
+      if (!warp_wait(&d_full[buf], dph, wc)) break;
+      tc_fence_after();
+      const int64_t n = (u / p.n_ttiles) * kRows + row;
+      const int64_t t0 = (u % p.n_ttiles) * BN;
+      for (int c = 0; c < BN; c += 16) {
+        uint32_t v[16];
+        tmem_ld16(tmem_base + lane_off + buf * BN + c, v);
+        tc_wait_ld();
+        if (n < p.N) {
+#pragma unroll
+          for (int t = 0; t < 16; ++t) {
+            const int64_t tok = t0 + c + t;
+            if (tok < p.M) {
+              const float val = __fmul_rn(__uint_as_float(v[t]), __ldg(p.tok_scale + tok));
+              if (kOutBf16)
+                reinterpret_cast<__nv_bfloat16*>(p.out)[tok * p.N + n] = __float2bfloat16_rn(val);
+              else
+                reinterpret_cast<float*>(p.out)[tok * p.N + n] = val;
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&d_empty[buf]);
+    }
+  }
+
+  __syncthreads();
+  if (warp == 2) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, p.tmem_cols);
+  }
+}
+
+// ------------------------------------------------------------ host side
+static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
+}
+
+static bool encode_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64_t inner,
+                      uint64_t outer, uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer,
+                      CUtensorMapSwizzle swz) {
+  auto fn = tensor_map_encoder();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {row_bytes};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+static int lm_head_token_tile(int64_t M) {
+  if (M >= kMaxBN) return kMaxBN;
+  return (int)((M + 15) / 16 * 16);
+}
+
+static size_t gemm_smem_bytes(int BN) {
+  return 1024 + kPStages * (size_t)(kPackedStageBytes + kScaleStageBytes) +
+         kXStages * (size_t)BN * kKB * 2 + 256;
+}
+
+size_t lm_head_workspace_bytes(int64_t M, int64_t N, int64_t K) {
+  (void)N;
+  const int BN = lm_head_token_tile(M);
+  const int64_t m_pad = (M + BN - 1) / BN * BN;
+  return kWsHeader + align_up((size_t)m_pad * K * 2, 1024) + align_up((size_t)m_pad * 4, 256);
+}
+
+static int sm_count() {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  return sms;
+}
+
+template <bool kOutBf16>
+static cudaError_t set_smem_attr() {
+  static cudaError_t err = cudaFuncSetAttribute(w4a16_tc_kernel<kOutBf16>,
+                                                cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                (int)gemm_smem_bytes(kMaxBN));
+  return err;
+}
+
+nvfp4_status lm_head_launch(const void* x, int64_t M, int64_t K, const uint8_t* packed,
+                            const uint8_t* scales, const float* global_scale, int64_t N,
+                            void* logits, int out_dtype, void* workspace, cudaStream_t stream) {
+  const int sms = sm_count();
+  if (sms <= 0) return NVFP4_ERR_CUDA;
+  const int BN = lm_head_token_tile(M);
+  const int n_ttiles = (int)((M + BN - 1) / BN);
+  const int64_t m_pad = (int64_t)n_ttiles * BN;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  int32_t* status = reinterpret_cast<int32_t*>(ws);
+  __half* x16 = reinterpret_cast<__half*>(ws + kWsHeader);
+  float* tok_scale =
+      reinterpret_cast<float*>(ws + kWsHeader + align_up((size_t)m_pad * K * 2, 1024));
+
+  CUtensorMap tm_packed, tm_scales, tm_x;
+  if (!encode_2d(&tm_packed, CU_TENSOR_MAP_DATA_TYPE_UINT8, packed, (uint64_t)K / 2, (uint64_t)N,
+                 (uint64_t)K / 2, kKS / 2, kRows, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !encode_2d(&tm_scales, CU_TENSOR_MAP_DATA_TYPE_UINT8, scales, (uint64_t)K / 16, (uint64_t)N,
+                 (uint64_t)K / 16, kKS / 16, kRows, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+      !encode_2d(&tm_x, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, x16, (uint64_t)K, (uint64_t)m_pad,
+                 (uint64_t)K * 2, kKB, (uint32_t)BN, CU_TENSOR_MAP_SWIZZLE_128B))
+    return NVFP4_ERR_CUDA;
+
+  if (cudaMemsetAsync(status, 0, sizeof(int32_t), stream) != cudaSuccess) return NVFP4_ERR_CUDA;
+  w4a16_prep_x_kernel<<<(unsigned)m_pad, 256, 0, stream>>>(static_cast<const uint16_t*>(x), M, K,
+                                                            global_scale, x16, tok_scale);
+  if (cudaGetLastError() != cudaSuccess) return NVFP4_ERR_CUDA;
+
+  GemmArgs a;
+  a.M = M;
+  a.N = N;
+  a.K = K;
+  a.BN = BN;
+  a.n_ttiles = n_ttiles;
+  a.n_units = ((N + kRows - 1) / kRows) * n_ttiles;
+  a.tmem_cols = (2 * BN + kAStages * 32 <= 256) ? 256u : 512u;
+  a.tok_scale = tok_scale;
+  a.out = logits;
+  a.status = status;
+  const int grid = (int)std::min<int64_t>(sms, a.n_units);
+  const size_t smem = gemm_smem_bytes(BN);
+  if (out_dtype == NVFP4_OUT_BF16) {
+    if (set_smem_attr<true>() != cudaSuccess) return NVFP4_ERR_CUDA;
+    w4a16_tc_kernel<true><<<grid, kThreads, smem, stream>>>(tm_packed, tm_scales, tm_x, a);
+  } else {
+    if (set_smem_attr<false>() != cudaSuccess) return NVFP4_ERR_CUDA;
+    w4a16_tc_kernel<false><<<grid, kThreads, smem, stream>>>(tm_packed, tm_scales, tm_x, a);
+  }
+  if (cudaGetLastError() != cudaSuccess) return NVFP4_ERR_CUDA;
+  return NVFP4_OK;
+}
+
+}  // namespace nvfp4

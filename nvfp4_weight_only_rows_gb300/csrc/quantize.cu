@@ -1,0 +1,229 @@
+// quantize.cu -- the NVFP4 row quantizer (`_quantize_nvfp4` on the page
+// "vllm.model_executor.layers.quantization.online.lm_head") for sm_103a.
+//
+// Two HBM passes over W, because every block scale depends on the
+// tensor-wide amax:
+//   pass 1 (nvfp4_amax_kernel): grid-stride 16-byte loads, |bf16| maxima
+//          taken on the integer bit patterns (exact), one partial per CTA.
+//   pass 2 (nvfp4_encode_kernel): every CTA folds the partials into amax,
+//          derives global = max(amax / 2688, 1e-12) and its reciprocal,
+//          then one warp per 256-value row segment encodes: each lane loads
+//          8 bf16 (16 bytes), a lane pair forms one 16-value block, one
+//          shuffle gives the block max, and each lane stores one 32-bit
+//          word of 8 packed codes; even lanes store the E4M3 scale byte.
+//          Segments are walked from the end of W backwards so the tail that
+//          pass 1 left in L2 is consumed first.
+//
+// Arithmetic (each an IEEE binary32 operation, round to nearest even):
+//   t  = min((vmax * fl(1/6)) * inv_global, 448)     block scale before E4M3
+//   s  = e4m3_rn_satfinite(t)
+//   r  = s == 0 ? 0 : 1 / (f32(s) * global)
+//   q  = x * r, rounded to E2M1 with satfinite (+-6) and ties to even code
+//   code 0x8 (negative zero) is rewritten to 0x0: the sign bit is set only
+//   for values < 0.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+
+#include <algorithm>
+
+#include "common.cuh"
+
+namespace nvfp4 {
+
+constexpr int kAmaxThreads = 256;
+constexpr int kEncodeThreads = 256;
+constexpr int kMaxAmaxBlocks = 4096;
+
+__device__ __forceinline__ uint4 ld_stream(const uint4* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+// max of |bf16| over the 8 values of a 16-byte vector, as packed u16 pairs
+__device__ __forceinline__ uint32_t absmax8(uint4 v, uint32_t m) {
+  const uint32_t k = 0x7FFF7FFFu;
+  m = __vmaxu2(m, v.x & k);
+  m = __vmaxu2(m, v.y & k);
+  m = __vmaxu2(m, v.z & k);
+  m = __vmaxu2(m, v.w & k);
+  return m;
+}
+
+__device__ __forceinline__ uint32_t fold_u16x2(uint32_t m) { return max(m & 0xFFFFu, m >> 16); }
+
+__global__ void __launch_bounds__(kAmaxThreads) nvfp4_amax_kernel(const uint4* __restrict__ W,
+                                                                  int64_t n_vec,
+                                                                  uint32_t* __restrict__ partial) {
+  uint32_t m = 0;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  for (; i + 3 * stride < n_vec; i += 4 * stride) {
+    uint4 a = ld_stream(W + i);
+    uint4 b = ld_stream(W + i + stride);
+    uint4 c = ld_stream(W + i + 2 * stride);
+    uint4 d = ld_stream(W + i + 3 * stride);
+    m = absmax8(a, m);
+    m = absmax8(b, m);
+    m = absmax8(c, m);
+    m = absmax8(d, m);
+  }
+  for (; i < n_vec; i += stride) m = absmax8(ld_stream(W + i), m);
+  m = fold_u16x2(m);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+  __shared__ uint32_t red[kAmaxThreads / 32];
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    uint32_t r = 0;
+    for (int w = 0; w < kAmaxThreads / 32; ++w) r = max(r, red[w]);
+    partial[blockIdx.x] = r;
+  }
+}
+
+// 8 fp32 values -> 8 E2M1 codes in one word (byte j: value 2j low nibble,
+// value 2j+1 high nibble), round to nearest even, saturating at +-6.
+__device__ __forceinline__ uint32_t cvt_e2m1x8(const float (&q)[8]) {
+  uint32_t w;
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n\t"
+      "mov.b32 %0, {b0, b1, b2, b3};\n\t}"
+      : "=r"(w)
+      : "f"(q[0]), "f"(q[1]), "f"(q[2]), "f"(q[3]), "f"(q[4]), "f"(q[5]), "f"(q[6]), "f"(q[7]));
+  // a code whose magnitude is zero carries no sign: 0x8 -> 0x0 per nibble
+  const uint32_t mag = w & 0x77777777u;
+  const uint32_t nonzero = (mag + 0x77777777u) & 0x88888888u;
+  return mag | (w & nonzero);
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
+
+__global__ void __launch_bounds__(kEncodeThreads) nvfp4_encode_kernel(
+    const uint16_t* __restrict__ W, int64_t N, int64_t K, const uint32_t* __restrict__ partial,
+    int n_partial, uint32_t* __restrict__ packed, uint8_t* __restrict__ scales,
+    float* __restrict__ global_out, int32_t* __restrict__ status) {
+  // ---- amax from the pass-1 partials (every CTA, from L2)
+  __shared__ uint32_t red[kEncodeThreads / 32];
+  __shared__ float sg[2];
+  uint32_t m = 0;
+  for (int i = threadIdx.x; i < n_partial; i += blockDim.x) m = max(m, partial[i]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    uint32_t a = 0;
+    for (int w = 0; w < kEncodeThreads / 32; ++w) a = max(a, red[w]);
+    if (a >= 0x7F80u) {  // Inf or NaN somewhere in W
+      sg[0] = __int_as_float(0x7FC00000);
+      if (blockIdx.x == 0) {
+        raise_status(status, NVFP4_ERR_NONFINITE);
+        *global_out = __int_as_float(0x7FC00000);
+      }
+    } else {
+      const float amax = __uint_as_float(a << 16);
+      float g = __fdiv_rn(amax, 2688.0f);  // amax / (6 * 448)
+      g = fmaxf(g, 1e-12f);
+      sg[0] = g;
+      sg[1] = __frcp_rn(g);
+      if (blockIdx.x == 0) *global_out = g;
+    }
+  }
+  __syncthreads();
+  const float g = sg[0];
+  if (!(g == g)) return;  // non-finite W: nothing to encode
+  const float ig = sg[1];
+  const float inv6 = 1.0f / 6.0f;
+
+  // ---- encode: one warp per 256-value row segment, walked backwards
+  const int lane = threadIdx.x & 31;
+  const int64_t segs_per_row = (K + 255) / 256;
+  const int64_t n_units = N * segs_per_row;
+  const int64_t warp_id = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int64_t n_warps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  const int64_t kp = K / 2, ks = K / 16;
+
+  for (int64_t u = n_units - 1 - warp_id; u >= 0; u -= n_warps) {
+    const int64_t row = u / segs_per_row;
+    const int64_t col = (u - row * segs_per_row) * 256 + lane * 8;
+    const bool valid = col < K;  // K % 16 == 0: both lanes of a block agree
+    uint4 v = make_uint4(0, 0, 0, 0);
+    if (valid) v = ld_stream(reinterpret_cast<const uint4*>(W + row * K + col));
+    // block max over the lane pair (16 values)
+    uint32_t bm = fold_u16x2(absmax8(v, 0));
+    bm = max(bm, __shfl_xor_sync(0xFFFFFFFFu, bm, 1));
+    const float vmax = __uint_as_float(bm << 16);
+    float t = __fmul_rn(__fmul_rn(vmax, inv6), ig);
+    t = fminf(t, 448.0f);
+    const __nv_fp8_storage_t s8 = __nv_cvt_float_to_fp8(t, __NV_SATFINITE, __NV_E4M3);
+    const float sf = __half2float(__half(__nv_cvt_fp8_to_halfraw(s8, __NV_E4M3)));
+    const float r = (sf == 0.0f) ? 0.0f : __frcp_rn(__fmul_rn(sf, g));
+    float q[8];
+    q[0] = __fmul_rn(bf16_lo(v.x), r);
+    q[1] = __fmul_rn(bf16_hi(v.x), r);
+    q[2] = __fmul_rn(bf16_lo(v.y), r);
+    q[3] = __fmul_rn(bf16_hi(v.y), r);
+    q[4] = __fmul_rn(bf16_lo(v.z), r);
+    q[5] = __fmul_rn(bf16_hi(v.z), r);
+    q[6] = __fmul_rn(bf16_lo(v.w), r);
+    q[7] = __fmul_rn(bf16_hi(v.w), r);
+    const uint32_t word = cvt_e2m1x8(q);
+    if (valid) {
+      packed[(row * kp + col / 2) >> 2] = word;
+      if ((lane & 1) == 0) scales[row * ks + col / 16] = (uint8_t)s8;
+    }
+  }
+}
+
+// ------------------------------------------------------------ host side
+static int device_sms() {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  return sms;
+}
+
+size_t quantize_workspace_bytes() {
+  return kWsHeader + align_up(sizeof(uint32_t) * kMaxAmaxBlocks, 256);
+}
+
+nvfp4_status quantize_launch(const void* W, int64_t N, int64_t K, uint8_t* packed,
+                             uint8_t* scales, float* global_scale, void* workspace,
+                             cudaStream_t stream) {
+  const int sms = device_sms();
+  if (sms <= 0) return NVFP4_ERR_CUDA;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  int32_t* status = reinterpret_cast<int32_t*>(ws);
+  uint32_t* partial = reinterpret_cast<uint32_t*>(ws + kWsHeader);
+
+  const int64_t n_vec = N * K / 8;
+  int64_t want = (n_vec + kAmaxThreads * 4 - 1) / (kAmaxThreads * 4);
+  int blocks1 = (int)std::min<int64_t>(std::min<int64_t>(want, (int64_t)sms * 8), kMaxAmaxBlocks);
+  if (blocks1 < 1) blocks1 = 1;
+
+  if (cudaMemsetAsync(status, 0, sizeof(int32_t), stream) != cudaSuccess) return NVFP4_ERR_CUDA;
+  nvfp4_amax_kernel<<<blocks1, kAmaxThreads, 0, stream>>>(static_cast<const uint4*>(W), n_vec,
+                                                          partial);
+  if (cudaGetLastError() != cudaSuccess) return NVFP4_ERR_CUDA;
+
+  const int64_t units = N * ((K + 255) / 256);
+  const int64_t warps_per_block = kEncodeThreads / 32;
+  int64_t want2 = (units + warps_per_block - 1) / warps_per_block;
+  int blocks2 = (int)std::min<int64_t>(want2, (int64_t)sms * 8);
+  if (blocks2 < 1) blocks2 = 1;
+  nvfp4_encode_kernel<<<blocks2, kEncodeThreads, 0, stream>>>(
+      static_cast<const uint16_t*>(W), N, K, partial, blocks1,
+      reinterpret_cast<uint32_t*>(packed), scales, global_scale, status);
+  if (cudaGetLastError() != cudaSuccess) return NVFP4_ERR_CUDA;
+  return NVFP4_OK;
+}
+
+}  // namespace nvfp4

@@ -1,0 +1,84 @@
+"""The C-ABI library builds, loads and exports every symbol its header declares,
+and rejects bad arguments on the host before touching the GPU (CPU only)."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+from tests.conftest import ROOT
+
+HEADER = os.path.join(ROOT, "include", "nvfp4_lm_head.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import __graft_entry__
+
+    __graft_entry__.build()
+    import nvfp4_weight_only_rows_gb300 as nv
+
+    return nv.load_library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b([a-z0-9_]+)\s*\(", text)) - {"defined"})
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ("nvfp4_quantize_rows", "nvfp4_refresh", "w4a16_lm_head",
+              "nvfp4_quantize_workspace_bytes", "w4a16_lm_head_workspace_bytes",
+              "nvfp4_status_string", "nvfp4_read_device_status", "nvfp4_abi_version"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    path = lib._name
+    out = subprocess.run(["nm", "-D", "--defined-only", path], capture_output=True, text=True,
+                         check=True).stdout
+    exported = set(re.findall(r" T (\S+)", out))
+    missing = [n for n in declared_functions() if n not in exported]
+    assert not missing, missing
+    for n in declared_functions():
+        getattr(lib, n)
+
+
+def test_status_strings_and_version(lib):
+    assert lib.nvfp4_abi_version() == 100
+    for code in range(10):
+        assert lib.nvfp4_status_string(code)
+    assert lib.nvfp4_status_string(7) == b"weight holds Inf or NaN"
+
+
+def test_workspace_sizes(lib):
+    assert lib.nvfp4_quantize_workspace_bytes(10, 24) == 0      # K % 16 != 0
+    assert lib.nvfp4_quantize_workspace_bytes(0, 32) == 0
+    assert lib.nvfp4_quantize_workspace_bytes(10, 32) >= 256
+    assert lib.w4a16_lm_head_workspace_bytes(4, 512, 300) == 0   # K % 256 != 0
+    w = lib.w4a16_lm_head_workspace_bytes(64, 128256, 4096)
+    assert w >= 64 * 4096 * 2 + 64 * 4 + 256
+
+
+def test_host_argument_errors_before_any_cuda_call(lib):
+    vp = ctypes.c_void_p
+    fake = vp(1 << 20)  # never dereferenced: every case fails a host check first
+    q = lib.nvfp4_quantize_rows
+    assert q(fake, 4, 24, fake, fake, fake, fake, 1 << 20, None) == 1        # SHAPE
+    assert q(fake, 0, 32, fake, fake, fake, fake, 1 << 20, None) == 1        # SHAPE
+    assert q(None, 4, 32, fake, fake, fake, fake, 1 << 20, None) == 3        # NULL
+    assert q(fake, 4, 32, fake, fake, fake, fake, 16, None) == 4             # WORKSPACE
+    assert q(vp((1 << 20) + 8), 4, 32, fake, fake, fake, fake, 1 << 20, None) == 2  # ALIGN
+    g = lib.w4a16_lm_head
+    assert g(fake, 4, 300, fake, fake, fake, 8, fake, 0, fake, 1 << 30, None) == 1   # K % 256
+    assert g(fake, -1, 256, fake, fake, fake, 8, fake, 0, fake, 1 << 30, None) == 1  # M < 0
+    assert g(fake, 4, 256, fake, fake, fake, 8, fake, 7, fake, 1 << 30, None) == 5   # DTYPE
+    assert g(fake, 0, 256, fake, fake, fake, 8, fake, 0, None, 0, None) == 0         # empty
+    assert g(fake, 4, 256, fake, fake, fake, 0, fake, 0, None, 0, None) == 0         # empty
+    assert g(None, 4, 256, fake, fake, fake, 8, fake, 0, fake, 1 << 30, None) == 3   # NULL
+    assert g(fake, 4, 256, fake, fake, fake, 8, fake, 0, fake, 64, None) == 4        # WORKSPACE
+    assert g(vp((1 << 20) + 2), 4, 256, fake, fake, fake, 8, fake, 0, fake, 1 << 30,
+             None) == 2                                                              # ALIGN

@@ -1,0 +1,169 @@
+"""GPU parity of the W4A16 lm_head product against the CPU oracle.
+
+The weights are quantized by the CPU oracle and uploaded, so these tests
+check the product alone; the bar is |err| <= 2e-3 * max|row of oracle
+logits| + 1e-3 per element, and argmax agreement except where the oracle's
+top two logits are closer than 1e-3.
+"""
+import numpy as np
+import pytest
+import torch
+
+import nvfp4_weight_only_rows_gb300 as nv
+import oracle
+import synth
+from tests._gpu import assert_argmax_agrees, assert_logits_close, to_bf16_dev
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import __graft_entry__
+
+    __graft_entry__.build()
+    assert torch.cuda.is_available()
+
+
+def upload_quantized(W_bits):
+    p, s, g = oracle.quantize(W_bits)
+    pd = torch.from_numpy(p).cuda()
+    sd = torch.from_numpy(s).cuda().view(torch.float8_e4m3fn)
+    gd = torch.tensor([g], dtype=torch.float32, device="cuda")
+    return (p, s, g), (pd, sd, gd)
+
+
+def run(x_bits, dev_q, out_dtype=torch.float32):
+    xd = to_bf16_dev(x_bits)
+    out = nv.w4a16_lm_head(xd, *dev_q, out_dtype=out_dtype)
+    torch.cuda.synchronize()
+    return out.double().cpu().numpy()
+
+
+def test_tiny_workload():
+    W, x = synth.tiny_weight(), synth.tiny_x()
+    host_q, dev_q = upload_quantized(W)
+    ref = oracle.logits(x, *host_q)
+    for dt in (torch.float32, torch.bfloat16):
+        got = run(x, dev_q, dt)
+        assert_logits_close(got, ref, f"tiny {dt}", dt == torch.bfloat16)
+        assert_argmax_agrees(got, ref, dt == torch.bfloat16)
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 300, 512), (5, 129, 256), (16, 128, 768),
+                                   (17, 1000, 512), (64, 777, 1024), (100, 513, 256),
+                                   (130, 260, 512), (200, 384, 1280), (1, 1, 256)])
+def test_ragged_shapes(M, N, K):
+    W = synth.quant_weight(N=N, K=K, seed=M + N)
+    x = synth.decode_x(M, K=K)
+    host_q, dev_q = upload_quantized(W)
+    ref = oracle.logits(x, *host_q)
+    got = run(x, dev_q)
+    assert_logits_close(got, ref, f"M={M} N={N} K={K}")
+    assert_argmax_agrees(got, ref)
+    got16 = run(x, dev_q, torch.bfloat16)
+    assert_logits_close(got16, ref, f"bf16 M={M} N={N} K={K}", True)
+
+
+def test_activation_range_extremes():
+    """Token rows of very different magnitude: the per-token rescale keeps them exact."""
+    N, K, M = 256, 512, 6
+    W = synth.quant_weight(N=N, K=K, seed=31)
+    xf = synth.bf16_bits_to_f32(synth.decode_x(M, K=K)).copy()
+    xf[0] *= 1e-30
+    xf[1] *= 1e30
+    xf[2] = 0.0
+    xf[3, ::7] *= 1e-8
+    xf[4] *= 3e4
+    x = synth.f32_to_bf16_bits(xf)
+    host_q, dev_q = upload_quantized(W)
+    ref = oracle.logits(x, *host_q)
+    assert_logits_close(run(x, dev_q), ref, "extremes")
+
+
+def test_deterministic_and_empty():
+    W = synth.quant_weight(N=500, K=512, seed=8)
+    x = synth.decode_x(9, K=512)
+    _, dev_q = upload_quantized(W)
+    a = run(x, dev_q)
+    b = run(x, dev_q)
+    assert np.array_equal(a, b)
+    xd = to_bf16_dev(x[:0])
+    out = nv.w4a16_lm_head(xd, *dev_q)
+    assert out.shape == (0, 500)
+
+
+def test_errors_are_status_codes():
+    W = synth.quant_weight(N=64, K=256, seed=1)
+    _, (pd, sd, gd) = upload_quantized(W)
+    x = to_bf16_dev(synth.decode_x(4, K=256))
+    with pytest.raises(nv.NVFP4Error) as e:
+        nv.w4a16_lm_head(x, pd, sd, gd, workspace=torch.empty(64, dtype=torch.uint8,
+                                                               device="cuda"))
+    assert e.value.status == nv.Status.ERR_WORKSPACE
+    W2 = synth.quant_weight(N=64, K=272, seed=1)
+    _, (p2, s2, g2) = upload_quantized(W2)
+    x2 = to_bf16_dev(synth.decode_x(4, K=272))
+    with pytest.raises(nv.NVFP4Error) as e:
+        nv.w4a16_lm_head(x2, p2, s2, g2)
+    assert e.value.status == nv.Status.ERR_SHAPE
+
+
+@pytest.fixture(scope="module")
+def decode_case():
+    W = synth.decode_weight()
+    host_q = oracle.quantize(W)
+    return W, host_q
+
+
+@pytest.mark.parametrize("M", [1, 8, 32, 64])
+def test_decode_workload(decode_case, M):
+    """W[128256, 4096] decode, fp32 logits; the oracle computes every logit."""
+    _, host_q = decode_case
+    p, s, g = host_q
+    dev_q = (torch.from_numpy(p).cuda(), torch.from_numpy(s).cuda().view(torch.float8_e4m3fn),
+             torch.tensor([g], device="cuda"))
+    x = synth.decode_x(M)
+    got = run(x, dev_q)
+    ref = oracle.logits(x, p, s, g)
+    assert_logits_close(got, ref, f"decode M={M}")
+    assert_argmax_agrees(got, ref)
+
+
+def test_prefill_workload_sampled(decode_case):
+    """x[2048, 4096] against the same W, bf16 logits; 48 sampled token rows
+    (first, last, random) are checked against the oracle over all 128256 columns."""
+    _, (p, s, g) = decode_case
+    dev_q = (torch.from_numpy(p).cuda(), torch.from_numpy(s).cuda().view(torch.float8_e4m3fn),
+             torch.tensor([g], device="cuda"))
+    x = synth.prefill_x()
+    got = run(x, dev_q, torch.bfloat16)
+    rng = np.random.default_rng(2)
+    rows = np.unique(np.concatenate([[0, 127, 128, 2047], rng.integers(0, 2048, 44)]))
+    ref = oracle.logits(x[rows], p, s, g)
+    assert_logits_close(got[rows], ref, "prefill", True)
+    assert_argmax_agrees(got[rows], ref, True)
+
+
+def test_sweep_workload_sampled():
+    """W[262144, 8192]; M in {1, 4, 16, 64, 256, 1024}, fp32 logits.  Each M:
+    512 sampled vocabulary columns for every token, plus full rows for up
+    to 4 tokens (argmax)."""
+    W = synth.sweep_weight()
+    p, s, g = oracle.quantize(W)
+    del W
+    dev_q = (torch.from_numpy(p).cuda(), torch.from_numpy(s).cuda().view(torch.float8_e4m3fn),
+             torch.tensor([g], device="cuda"))
+    rng = np.random.default_rng(6)
+    cols = np.unique(np.concatenate([[0, 262143], rng.integers(0, 262144, 510)]))
+    x_all = synth.sweep_x(1024)
+    for M in (1, 4, 16, 64, 256, 1024):
+        x = x_all[:M]
+        got = run(x, dev_q)
+        ref_c = oracle.logits(x, p, s, g, cols=cols)
+        tol = 2e-3 * np.abs(ref_c).max(axis=1, keepdims=True) + 1e-3
+        assert np.all(np.abs(got[:, cols] - ref_c) <= tol), f"sweep M={M}"
+        rows = np.unique([0, M - 1, M // 2])[:4]
+        ref_r = oracle.logits(x[rows], p, s, g)
+        assert_logits_close(got[rows], ref_r, f"sweep rows M={M}")
+        assert_argmax_agrees(got[rows], ref_r)
