@@ -1,0 +1,464 @@
+#!/usr/bin/env python3
+"""Benchmark of the online NVFP4 lm_head hot path on GB300.
+
+One step is one pass of the whole path over the Llama-3-8B-shaped lm_head
+W[128256, 4096] (synthetic, seeded):
+  1. refresh: re-quantize W in place (amax pass + encode pass),
+  2. decode: the W4A16 product for M = 1, 8, 32 and 64 tokens (fp32 logits),
+  3. prefill: the W4A16 product for M = 2048 tokens (bf16 logits).
+Two source weights and two quantized copies are alternated so that no call
+reads what the previous call left in L2 (every input is larger than L2).
+
+`value` is the decode-regime HBM throughput (algorithmic bytes of the four
+decode calls / their device time, CUDA events on the launching stream), the
+first clause of the headline metric; the prefill TFLOP/s and quantizer GB/s
+are reported beside it with their own roofline fractions.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun every rank runs the same workload on its own GPU (replicas:
+the path has no exchange step); times are the max over ranks and `value`
+sums the ranks' bytes.  `--impl reference` times the CPU oracle instead, on
+a bounded sample of the same workload, on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+METRIC = "NVFP4 W4A16 lm_head: HBM GB/s at M≤64, TFLOP/s at M=2048; quant GB/s"
+N_VOCAB, K_HID = 128256, 4096
+DECODE_MS = (1, 8, 32, 64)
+PREFILL_M = 2048
+WORKLOAD = ("Llama-3-8B-shaped lm_head W[128256,4096] bf16 (synthetic N(0,0.02), 0.1% x20): "
+            "refresh (in-place NVFP4 quantize) + decode M in {1,8,32,64} fp32 logits + "
+            "prefill M=2048 bf16 logits")
+
+
+# --------------------------------------------------------------------- units
+def decode_bytes(M: int, N: int = N_VOCAB, K: int = K_HID) -> int:
+    """Algorithmic bytes of one decode call: packed + scales + x + fp32 logits."""
+    return N * K // 2 + N * K // 16 + 2 * M * K + 4 * M * N
+
+
+def quant_bytes(N: int = N_VOCAB, K: int = K_HID) -> int:
+    """Two reads of W (the tensor-wide amax precedes every block) + codes + scales + global."""
+    return 2 * 2 * N * K + N * K // 2 + N * K // 16 + 4
+
+
+def prefill_flops(M: int = PREFILL_M, N: int = N_VOCAB, K: int = K_HID) -> int:
+    return 2 * M * N * K
+
+
+def load_peaks() -> dict:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": p["hbm_gbs"], "bf16_tflops": p["bf16_tflops"],
+                "bf16_tflops_sustained": p.get("bf16_tflops_sustained"), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+def load_traffic() -> dict:
+    """Per-launch DRAM bytes from the committed ncu summary, when it is current."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return json.load(f)
+    return {}
+
+
+# --------------------------------------------------------------- distributed
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def aggregate(elapsed_s: float, units: float, world: int) -> tuple[float, float]:
+    """(max elapsed over ranks, sum of units over ranks)."""
+    if world <= 1:
+        return elapsed_s, units
+    import torch.distributed as dist
+
+    dev = torch.device("cuda") if dist.get_backend() == "nccl" else torch.device("cpu")
+    t = torch.tensor([elapsed_s], dtype=torch.float64, device=dev)
+    u = torch.tensor([units], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM)
+    return float(t.item()), float(u.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+# ------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi samples every 200 ms while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.path = tempfile.mktemp(prefix="clocks_", suffix=".csv")
+        self.gpu = gpu_index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-i", str(self.gpu), "-lms", "200"], stdout=self.f, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        self.proc.wait()
+        self.f.close()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                cols = [c.strip() for c in line.split(",")]
+                if len(cols) < 9:
+                    continue
+                try:
+                    sm.append(float(cols[1]))
+                    smax.append(float(cols[2]))
+                except ValueError:
+                    continue
+                for name, val in zip(names, cols[5:9]):
+                    if val.lower() == "active":
+                        reasons.add(name)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ our arm
+def run_ours(args, world, rank, local):
+    import nvfp4_weight_only_rows_gb300 as nv
+    import synth
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    nv.load_library()
+    N, K = N_VOCAB, K_HID
+
+    def up(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(
+            torch.bfloat16).to(dev)
+
+    W = [up(synth.decode_weight(seed=1)), up(synth.decode_weight(seed=2))]
+    xs = synth.decode_x(max(DECODE_MS))
+    x_dec = {M: up(xs[:M]) for M in DECODE_MS}
+    x_pre = up(synth.prefill_x())
+    qws = torch.empty(nv.nvfp4_quantize_workspace_bytes(N, K), dtype=torch.uint8, device=dev)
+    copies = [nv.nvfp4_quantize_rows(W[i], workspace=qws) for i in range(2)]
+    gws = torch.empty(nv.w4a16_lm_head_workspace_bytes(PREFILL_M, N, K), dtype=torch.uint8,
+                      device=dev)
+    out_dec = {M: torch.empty(M, N, dtype=torch.float32, device=dev) for M in DECODE_MS}
+    out_pre = torch.empty(PREFILL_M, N, dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream()
+    launches_per_step = 2 + 2 * len(DECODE_MS) + 2
+
+    def step(s, marks=None):
+        c = s % 2
+
+        def mark():
+            if marks is not None:
+                e = torch.cuda.Event(enable_timing=True)
+                e.record(stream)
+                marks.append(e)
+
+        mark()
+        p, sc, g = copies[c]
+        nv.nvfp4_refresh(W[c], p, sc, g, workspace=qws)
+        mark()
+        for i, M in enumerate(DECODE_MS):
+            p, sc, g = copies[(c + 1 + i) % 2]
+            nv.w4a16_lm_head(x_dec[M], p, sc, g, out=out_dec[M], workspace=gws)
+            mark()
+        p, sc, g = copies[(c + 1) % 2]
+        nv.w4a16_lm_head(x_pre, p, sc, g, out=out_pre, workspace=gws)
+        mark()
+
+    for s in range(args.warmup):
+        step(s)
+    torch.cuda.synchronize()
+
+    clocks = ClockSampler(local)
+    marks_all = []
+    barrier(world)
+    torch.cuda.synchronize()
+    clocks.start()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for s in range(args.steps):
+        marks = []
+        step(args.warmup + s, marks)
+        marks_all.append(marks)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    clock_info = clocks.stop()
+    barrier(world)
+    total_ms = t_start.elapsed_time(t_end)
+
+    t_quant = t_pre = 0.0
+    t_dec = {M: 0.0 for M in DECODE_MS}
+    for marks in marks_all:
+        t_quant += marks[0].elapsed_time(marks[1])
+        for i, M in enumerate(DECODE_MS):
+            t_dec[M] += marks[1 + i].elapsed_time(marks[2 + i])
+        t_pre += marks[-2].elapsed_time(marks[-1])
+    K_steps = args.steps
+    dec_bytes = K_steps * sum(decode_bytes(M) for M in DECODE_MS)
+    dec_s = sum(t_dec.values()) / 1e3
+    dec_s_max, dec_bytes_all = aggregate(dec_s, dec_bytes, world)
+    total_s_max, _ = aggregate(total_ms / 1e3, 0.0, world)
+    value = dec_bytes_all / dec_s_max / 1e9
+
+    # ---- end to end through the public call: x from pinned host, logits back
+    x_host = {M: x_dec[M].cpu().pin_memory() for M in DECODE_MS}
+    o_host = {M: torch.empty(M, N, dtype=torch.float32).pin_memory() for M in DECODE_MS}
+    x_tmp = {M: torch.empty_like(x_dec[M]) for M in DECODE_MS}
+
+    def e2e_step(s):
+        for i, M in enumerate(DECODE_MS):
+            p, sc, g = copies[(s + i) % 2]
+            x_tmp[M].copy_(x_host[M], non_blocking=True)
+            nv.w4a16_lm_head(x_tmp[M], p, sc, g, out=out_dec[M], workspace=gws)
+            o_host[M].copy_(out_dec[M], non_blocking=True)
+
+    for s in range(args.warmup):
+        e2e_step(s)
+    torch.cuda.synchronize()
+    barrier(world)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for s in range(args.steps):
+        e2e_step(s)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_s, _ = aggregate(e0.elapsed_time(e1) / 1e3, 0.0, world)
+    e2e_value = dec_bytes_all / e2e_s / 1e9
+
+    peaks = load_peaks()
+    traffic = load_traffic()
+    quant_gbs = K_steps * quant_bytes() / (t_quant / 1e3) / 1e9
+    pre_tflops = K_steps * prefill_flops() / (t_pre / 1e3) / 1e12
+    per_call_dec = {M: t_dec[M] / K_steps * 1e3 for M in DECODE_MS}  # us
+
+    def hbm_roof(name, gbs, tkey):
+        return {"kernel": name, "bound": "hbm", "achieved": round(gbs, 1),
+                "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": round(gbs / peaks["hbm_gbs"], 4),
+                "traffic": traffic.get(tkey), "peak_source": peaks["source"] + " copy"}
+
+    roofs = {
+        "quantize": hbm_roof("nvfp4 amax + encode (refresh call)", quant_gbs, "quantize"),
+        "prefill": {"kernel": "w4a16_lm_head M=2048 (prep + tcgen05 GEMM)", "bound": "tensor",
+                    "achieved": round(pre_tflops, 1), "peak": peaks["bf16_tflops"],
+                    "unit": "TFLOP/s", "frac": round(pre_tflops / peaks["bf16_tflops"], 4),
+                    "traffic": traffic.get("prefill"),
+                    "peak_source": peaks["source"] + " dense bf16 burst (fp16 MMA, same rate)"},
+    }
+    for M in DECODE_MS:
+        gbs = decode_bytes(M) / (per_call_dec[M] / 1e6) / 1e9
+        roofs[f"decode_M{M}"] = hbm_roof(f"w4a16_lm_head M={M} (prep + tcgen05 GEMM)", gbs,
+                                         f"decode_M{M}")
+    times = {"quantize": t_quant, "prefill": t_pre, **{f"decode_M{M}": t_dec[M] for M in DECODE_MS}}
+    dominant = max(times, key=times.get)
+
+    result = {
+        "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
+        "steps": K_steps, "warmup": args.warmup, "ms_per_step": round(total_s_max * 1e3 / K_steps, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "e2m1*e4m3 x f16 -> f32",
+        "data": "synthetic (seeded generator; random weights of the stated shape)",
+        "config": {"workload": WORKLOAD, "N": N, "K": K, "decode_M": list(DECODE_MS),
+                   "prefill_M": PREFILL_M,
+                   "value_basis": "decode calls only: sum of algorithmic bytes / their event time",
+                   "l2": "inputs larger than L2 (bf16 W 1.05 GB, packed W 296 MB); two weights and "
+                         "two quantized copies alternated between calls",
+                   "parallelism": f"replicas x{world}"},
+        "parts": {"decode_gbs": round(value, 1),
+                  "decode_us_per_call": {str(M): round(per_call_dec[M], 2) for M in DECODE_MS},
+                  "prefill_tflops": round(pre_tflops, 1),
+                  "prefill_ms_per_call": round(t_pre / K_steps, 4),
+                  "quant_gbs": round(quant_gbs, 1),
+                  "quant_ms_per_call": round(t_quant / K_steps, 4)},
+        "roofline": roofs[dominant], "rooflines": roofs,
+        "e2e": {"value": round(e2e_value, 1), "unit": "GB/s",
+                "h2d_bytes_per_step": sum(2 * M * K for M in DECODE_MS),
+                "d2h_bytes_per_step": sum(4 * M * N for M in DECODE_MS),
+                "what": "decode calls through w4a16_lm_head with x copied from pinned host memory "
+                        "and logits copied back every call"},
+        "gpu_launches": launches_per_step * K_steps,
+        "clocks": clock_info,
+    }
+    if rank == 0:
+        result["cpu_baseline"] = cpu_baseline(budget_s=args.cpu_budget)
+        print(json.dumps(result), flush=True)
+
+
+# ----------------------------------------------------------- the CPU oracle
+def cpu_baseline(budget_s: float = 15.0, steps: int = 1) -> dict:
+    """The oracle's decode product (float64, OpenMP over vocabulary rows) on a
+    sample of vocabulary rows, sized to about `budget_s` seconds of work.  The
+    sample's weights are quantized by the oracle with the full tensor's
+    global scale."""
+    import oracle
+    import synth
+
+    W = synth.decode_weight(seed=1)
+    g, ig = oracle.global_scale(oracle.weight_amax(W))
+    xs = synth.decode_x(max(DECODE_MS))
+
+    def sample(n):
+        p, s = oracle.quantize_rows(W, np.arange(n, dtype=np.int64), g, ig)
+        return p, s
+
+    n_probe = 512
+    p, s = sample(n_probe)
+    t0 = time.perf_counter()
+    for M in DECODE_MS:
+        oracle.logits(xs[:M], p, s, g)
+    probe = time.perf_counter() - t0
+    n_cols = int(min(N_VOCAB, max(n_probe, n_probe * budget_s / max(probe, 1e-3) / steps)))
+    p, s = sample(n_cols)
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        for M in DECODE_MS:
+            oracle.logits(xs[:M], p, s, g)
+    dt = time.perf_counter() - t0
+    nbytes = steps * sum(n_cols * K_HID // 2 + n_cols * K_HID // 16 + 2 * M * K_HID +
+                         4 * M * n_cols for M in DECODE_MS)
+    return {"value": round(nbytes / dt / 1e9, 4), "unit": "GB/s", "cores": oracle.num_threads(),
+            "kind": "oracle",
+            "sample": f"decode product M in {{1,8,32,64}} over the first {n_cols} of "
+                      f"{N_VOCAB} vocabulary rows (K={K_HID}), {steps} pass(es), "
+                      f"{dt:.1f} s wall"}
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return
+    cb = cpu_baseline(budget_s=args.cpu_budget / max(args.steps, 1) * args.steps,
+                      steps=max(1, args.steps))
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": cb["value"], "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded generator)",
+        "config": {"workload": WORKLOAD, "N": N_VOCAB, "K": K_HID, "decode_M": list(DECODE_MS),
+                   "value_basis": "decode product only, on a sample of vocabulary rows"},
+        "cpu_baseline": cb,
+        "e2e": {"value": cb["value"], "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def run_profile_case(case: str):
+    """A small, fixed case for ncu: three warm-up calls, then exactly one call
+    of the profiled entry point (decode M=1 / M=64, prefill, or refresh) on
+    the decode-shaped weight; the device holds under 1.5 GB."""
+    import nvfp4_weight_only_rows_gb300 as nv
+    import synth
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    N, K = N_VOCAB, K_HID
+
+    def up(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(
+            torch.bfloat16).to(dev)
+
+    W = up(synth.decode_weight(seed=1))
+    qws = torch.empty(nv.nvfp4_quantize_workspace_bytes(N, K), dtype=torch.uint8, device=dev)
+    packed, scales, g = nv.nvfp4_quantize_rows(W, workspace=qws)
+    if case == "quant":
+        for _ in range(4):
+            nv.nvfp4_refresh(W, packed, scales, g, workspace=qws)
+        torch.cuda.synchronize()
+        return
+    del W
+    torch.cuda.empty_cache()
+    if case == "prefill":
+        M, x, dt = PREFILL_M, up(synth.prefill_x()), torch.bfloat16
+    else:
+        M = int(case.replace("decode", ""))
+        x, dt = up(synth.decode_x(M)), torch.float32
+    gws = torch.empty(nv.w4a16_lm_head_workspace_bytes(M, N, K), dtype=torch.uint8, device=dev)
+    out = torch.empty(M, N, dtype=dt, device=dev)
+    for _ in range(4):
+        nv.w4a16_lm_head(x, packed, scales, g, out=out, workspace=gws)
+    torch.cuda.synchronize()
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-budget", type=float, default=15.0,
+                    help="seconds of CPU work for the oracle baseline")
+    ap.add_argument("--profile", choices=["decode1", "decode64", "prefill", "quant"],
+                    help="run one small fixed case for ncu instead of the benchmark")
+    args = ap.parse_args()
+    if args.profile:
+        run_profile_case(args.profile)
+        return
+    if args.warmup < 3 and args.impl == "ours":
+        ap.error("--warmup must be >= 3")
+    world, rank, local = dist_env()
+    if args.impl == "reference":
+        # the oracle runs on rank 0's host cores only; other ranks have no work
+        run_reference(args, world, rank)
+        return
+    if world > 1:
+        import torch.distributed as dist
+
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    try:
+        run_ours(args, world, rank, local)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -15,9 +15,10 @@
 //  2. w4a16_tc_kernel: a persistent, warp-specialized tcgen05 GEMM in the
 //     swapped orientation D[vocab row, token] = A . B^T:
 //       A = dequantized weights, 128 vocabulary rows x 64 k per stage, held
-//           in TENSOR MEMORY (the "ts" MMA form), written by four dequant
-//           warps with one thread per row: e2m1 pairs -> fp16 pairs with the
-//           hardware cvt, times the E4M3 block scale (fp16, exact);
+//           in TENSOR MEMORY (the "ts" MMA form), written by eight dequant
+//           warps with one thread per row and half a stage per warp: e2m1
+//           pairs -> fp16 pairs with the hardware cvt, times the E4M3 block
+//           scale (fp16, exact);
 //       B = the fp16 activations, a TMA tile [BN tokens x 64 k] in shared
 //           memory with the 128-byte swizzle;
 //       D = fp32 accumulators in tensor memory, double buffered, drained by
@@ -25,8 +26,10 @@
 //     Packed codes and scales arrive by TMA in 256-k stages; every product
 //     x * w is exact in fp32, so the only rounding is the fp32 summation.
 //
-// Warp roles (352 threads): 0 packed/scale TMA producer, 1 activation TMA
-// producer, 2 MMA issuer (and TMEM owner), 3-6 dequant, 7-10 epilogue.
+// Warp roles (480 threads): 0 packed/scale TMA producer, 1 activation TMA
+// producer, 2 MMA issuer (and TMEM owner), 3-10 dequant (two warps per TMEM
+// lane quadrant taking 64-k stages in turn), 11-14 epilogue.  The producer
+// and MMA warps run warp-uniform loops and issue from one elected lane.
 // Every pipeline wait is bounded in time; on expiry the CTA raises
 // NVFP4_ERR_TIMEOUT in the workspace status word, drains what it issued and
 // returns.
@@ -45,9 +48,12 @@ constexpr int kRows = 128;          // vocabulary rows per tile (MMA M)
 constexpr int kKB = 64;             // k per A / activation stage
 constexpr int kKS = 256;            // k per packed/scale stage
 constexpr int kPStages = 4;         // packed/scale ring depth (18 KB each)
-constexpr int kXStages = 6;         // activation ring depth
-constexpr int kAStages = 4;         // TMEM A ring depth (32 columns each)
-constexpr int kThreads = 352;
+constexpr int kStages = 8;          // A (TMEM, 32 columns) and activation ring depth
+constexpr int kDqPerQuad = 2;       // dequant warps per TMEM lane quadrant
+constexpr int kDqWarps = 4 * kDqPerQuad;
+constexpr int kFirstDqWarp = 3;
+constexpr int kFirstEpiWarp = kFirstDqWarp + kDqWarps;
+constexpr int kThreads = 32 * (kFirstEpiWarp + 4);
 constexpr uint32_t kPackedStageBytes = kRows * (kKS / 2);   // 16384
 constexpr uint32_t kScaleStageBytes = kRows * (kKS / 16);   // 2048
 constexpr int kMaxBN = 128;
@@ -162,6 +168,29 @@ __device__ __forceinline__ void scales4_to_f16(uint32_t s, uint32_t& s01, uint32
 __device__ __forceinline__ uint32_t dup_lo(uint32_t v) { return __byte_perm(v, 0, 0x1010); }
 __device__ __forceinline__ uint32_t dup_hi(uint32_t v) { return __byte_perm(v, 0, 0x3232); }
 
+// one lane of a converged warp (the lowest active lane)
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b32 r;\n\t"
+      "elect.sync r|p, 0xffffffff;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(pred));
+  return pred != 0;
+}
+
+// Before a producer warp exits, wait (bounded) until the last TMA load it
+// issued into each ring slot has landed, so no copy targets freed memory.
+__device__ __forceinline__ void drain_loads(uint64_t* full, uint32_t n_slots, uint32_t issued,
+                                            int32_t* status) {
+  volatile int32_t zero = 0;
+  WaitCtl drain{status, &zero, 100000000ull};
+  for (uint32_t s = 0; s < n_slots && s < issued; ++s) {
+    const uint32_t fills = issued / n_slots + (s < issued % n_slots ? 1u : 0u);
+    mbar_wait(&full[s], (fills - 1) & 1, drain);
+  }
+}
+
 // warp-uniform bounded wait: every lane polls, the warp agrees on the outcome
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const WaitCtl& wc) {
   const bool ok = mbar_wait(bar, parity, wc);
@@ -181,15 +210,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t x_stage_bytes = (uint32_t)BN * (kKB * 2);
   uint8_t* s_packed = smem;                                        // kPStages x 16 KB
   uint8_t* s_scales = s_packed + kPStages * kPackedStageBytes;     // kPStages x 2 KB
-  uint8_t* s_x = s_scales + kPStages * kScaleStageBytes;           // kXStages x BN*128
-  uint64_t* bars = reinterpret_cast<uint64_t*>(s_x + kXStages * x_stage_bytes);
-  uint64_t* p_full = bars;
-  uint64_t* p_empty = p_full + kPStages;
-  uint64_t* x_full = p_empty + kPStages;
-  uint64_t* x_empty = x_full + kXStages;
-  uint64_t* a_full = x_empty + kXStages;
-  uint64_t* a_empty = a_full + kAStages;
-  uint64_t* d_full = a_empty + kAStages;
+  uint8_t* s_x = s_scales + kPStages * kScaleStageBytes;           // kStages x BN*128
+  uint64_t* bars = reinterpret_cast<uint64_t*>(s_x + kStages * x_stage_bytes);
+  uint64_t* p_full = bars;                 // packed/scale stage landed (TMA)
+  uint64_t* p_empty = p_full + kPStages;   // packed/scale stage read by every dequant warp
+  uint64_t* x_full = p_empty + kPStages;   // activation stage landed (TMA)
+  uint64_t* a_full = x_full + kStages;     // A stage written to TMEM (one warp per quadrant)
+  uint64_t* s_empty = a_full + kStages;    // the MMAs reading A/activation stage s completed
+  uint64_t* d_full = s_empty + kStages;
   uint64_t* d_empty = d_full + 2;
   uint64_t* done_bar = d_empty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done_bar + 1);
@@ -201,15 +229,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < kPStages; ++i) {
       mbar_init(&p_full[i], 1);
-      mbar_init(&p_empty[i], 4);
+      mbar_init(&p_empty[i], kDqWarps);
     }
-    for (int i = 0; i < kXStages; ++i) {
+    for (int i = 0; i < kStages; ++i) {
       mbar_init(&x_full[i], 1);
-      mbar_init(&x_empty[i], 1);
-    }
-    for (int i = 0; i < kAStages; ++i) {
       mbar_init(&a_full[i], 4);
-      mbar_init(&a_empty[i], 1);
+      mbar_init(&s_empty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&d_full[i], 1);
@@ -238,114 +263,113 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int64_t K = p.K;
   const int n_super = (int)(K / kKS);
   const int n_kb = (int)(K / kKB);
+  // the producer and MMA loops below are warp-uniform; one elected lane
+  // issues each TMA / tcgen05 instruction
 
   if (warp == 0) {
     // ---------------- packed codes + scales producer
-    if (lane == 0) {
-      const uint64_t pol = policy_evict_first();
-      uint32_t st = 0, ph = 0, issued = 0;
-      bool ok = true;
-      for (int64_t u = blockIdx.x; ok && u < p.n_units; u += gridDim.x) {
-        const int32_t n0 = (int32_t)((u / p.n_ttiles) * kRows);
-        for (int sb = 0; sb < n_super; ++sb) {
-          if (!mbar_wait(&p_empty[st], ph ^ 1, wc)) { ok = false; break; }
+    const uint64_t pol = policy_evict_first();
+    uint32_t issued = 0;
+    bool ok = true;
+    for (int64_t u = blockIdx.x; ok && u < p.n_units; u += gridDim.x) {
+      const int32_t n0 = (int32_t)((u / p.n_ttiles) * kRows);
+      for (int sb = 0; sb < n_super; ++sb, ++issued) {
+        const uint32_t st = issued % kPStages, ph = (issued / kPStages) & 1;
+        if (!warp_wait(&p_empty[st], ph ^ 1, wc)) { ok = false; break; }
+        if (elect_one()) {
           mbar_arrive_expect_tx(&p_full[st], kPackedStageBytes + kScaleStageBytes);
           tma_load_2d_hint(s_packed + st * kPackedStageBytes, &tm_packed, sb * (kKS / 2), n0,
                            &p_full[st], pol);
           tma_load_2d_hint(s_scales + st * kScaleStageBytes, &tm_scales, sb * (kKS / 16), n0,
                            &p_full[st], pol);
-          ++issued;
-          if (++st == kPStages) { st = 0; ph ^= 1; }
         }
-      }
-      // drain: wait (bounded) until the last load of every slot has landed
-      WaitCtl drain{p.status, abort_flag, 100000000ull};
-      volatile int32_t zero = 0;
-      drain.abort = &zero;
-      for (uint32_t s = 0; s < kPStages && s < issued; ++s) {
-        const uint32_t fills = issued / kPStages + (s < issued % kPStages ? 1u : 0u);
-        mbar_wait(&p_full[s], (fills - 1) & 1, drain);
+        __syncwarp();
       }
     }
+    drain_loads(p_full, kPStages, issued, p.status);
   } else if (warp == 1) {
     // ---------------- activation producer
-    if (lane == 0) {
-      const uint64_t pol = policy_evict_last();
-      uint32_t st = 0, ph = 0, issued = 0;
-      bool ok = true;
-      for (int64_t u = blockIdx.x; ok && u < p.n_units; u += gridDim.x) {
-        const int32_t t0 = (int32_t)((u % p.n_ttiles) * BN);
-        for (int kb = 0; kb < n_kb; ++kb) {
-          if (!mbar_wait(&x_empty[st], ph ^ 1, wc)) { ok = false; break; }
+    const uint64_t pol = policy_evict_last();
+    uint32_t issued = 0;
+    bool ok = true;
+    for (int64_t u = blockIdx.x; ok && u < p.n_units; u += gridDim.x) {
+      const int32_t t0 = (int32_t)((u % p.n_ttiles) * BN);
+      for (int kb = 0; kb < n_kb; ++kb, ++issued) {
+        const uint32_t st = issued % kStages, ph = (issued / kStages) & 1;
+        if (!warp_wait(&s_empty[st], ph ^ 1, wc)) { ok = false; break; }
+        if (elect_one()) {
           mbar_arrive_expect_tx(&x_full[st], x_stage_bytes);
           tma_load_2d_hint(s_x + st * x_stage_bytes, &tm_x, kb * kKB, t0, &x_full[st], pol);
-          ++issued;
-          if (++st == kXStages) { st = 0; ph ^= 1; }
         }
-      }
-      WaitCtl drain{p.status, abort_flag, 100000000ull};
-      volatile int32_t zero = 0;
-      drain.abort = &zero;
-      for (uint32_t s = 0; s < kXStages && s < issued; ++s) {
-        const uint32_t fills = issued / kXStages + (s < issued % kXStages ? 1u : 0u);
-        mbar_wait(&x_full[s], (fills - 1) & 1, drain);
+        __syncwarp();
       }
     }
+    drain_loads(x_full, kStages, issued, p.status);
   } else if (warp == 2) {
-    // ---------------- MMA issuer
-    if (lane == 0) {
-      const uint32_t idesc = idesc_f16_f32((uint32_t)BN);
-      uint32_t as = 0, aph = 0, xs = 0, xph = 0;
-      bool ok = true;
-      int64_t i = 0;
-      for (int64_t u = blockIdx.x; ok && u < p.n_units; u += gridDim.x, ++i) {
-        const uint32_t buf = (uint32_t)(i & 1), dph = (uint32_t)((i >> 1) & 1);
-        if (!mbar_wait(&d_empty[buf], dph ^ 1, wc)) break;
-        tc_fence_after();
-        const uint32_t d_tmem = tmem_base + buf * BN;
-        for (int kb = 0; kb < n_kb; ++kb) {
-          if (!mbar_wait(&a_full[as], aph, wc) || !mbar_wait(&x_full[xs], xph, wc)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t xa = smem_u32(s_x + xs * x_stage_bytes);
-#pragma unroll
-          for (int kk = 0; kk < kKB / 16; ++kk) {
-            tc_mma_ts(d_tmem, tmem_a + as * 32 + kk * 8, smem_desc_sw128(xa + kk * 32), idesc,
-                      (kb | kk) != 0);
-          }
-          tc_commit(&a_empty[as]);
-          tc_commit(&x_empty[xs]);
-          if (++as == kAStages) { as = 0; aph ^= 1; }
-          if (++xs == kXStages) { xs = 0; xph ^= 1; }
+    // ---------------- MMA issuer (whole warp; one elected lane issues)
+    const uint32_t idesc = idesc_f16_f32((uint32_t)BN);
+    const uint64_t xdesc0 = smem_desc_sw128(smem_u32(s_x));
+    uint32_t g = 0;
+    bool ok = true;
+    int64_t i = 0;
+    for (int64_t u = blockIdx.x; ok && u < p.n_units; u += gridDim.x, ++i) {
+      const uint32_t buf = (uint32_t)(i & 1), dph = (uint32_t)((i >> 1) & 1);
+      if (!warp_wait(&d_empty[buf], dph ^ 1, wc)) break;
+      tc_fence_after();
+      const uint32_t d_tmem = tmem_base + buf * BN;
+      for (int kb = 0; kb < n_kb; ++kb, ++g) {
+        const uint32_t st = g % kStages, ph = (g / kStages) & 1;
+        if (!warp_wait(&a_full[st], ph, wc) || !warp_wait(&x_full[st], ph, wc)) {
+          ok = false;
+          break;
         }
-        if (ok) tc_commit(&d_full[buf]);
+        tc_fence_after();
+        const uint64_t bdesc = xdesc0 + ((st * x_stage_bytes) >> 4);
+        const uint32_t a_t = tmem_a + st * 32;
+        if (elect_one()) {
+#pragma unroll
+          for (int kk = 0; kk < kKB / 16; ++kk)
+            tc_mma_ts(d_tmem, a_t + kk * 8, bdesc + 2 * kk, idesc, (kb | kk) != 0);
+          tc_commit(&s_empty[st]);
+        }
+        __syncwarp();
       }
-      // every MMA issued above has completed once done_bar flips
-      tc_commit(done_bar);
-      WaitCtl drain{p.status, abort_flag, 100000000ull};
-      volatile int32_t zero = 0;
-      drain.abort = &zero;
-      mbar_wait(done_bar, 0, drain);
+      if (ok) {
+        if (elect_one()) tc_commit(&d_full[buf]);
+        __syncwarp();
+      }
     }
-  } else if (warp <= 6) {
-    // ---------------- dequant: one thread per vocabulary row of the tile
+    // every MMA issued above has completed once done_bar flips
+    if (elect_one()) tc_commit(done_bar);
+    __syncwarp();
+    WaitCtl drain{p.status, abort_flag, 100000000ull};
+    volatile int32_t zero = 0;
+    drain.abort = &zero;
+    mbar_wait(done_bar, 0, drain);
+  } else if (warp < kFirstEpiWarp) {
+    // ---------------- dequant: one thread per vocabulary row.  The kDqPerQuad
+    // warps of a TMEM lane quadrant take the 64-k stages round-robin; a
+    // stage's TMEM store is completed (wait::st) only after the warp's next
+    // stage has been converted, so the store latency overlaps that work.
     const int q = warp & 3;
+    const int r = (warp - kFirstDqWarp) >> 2;
     const int row = q * 32 + lane;
     const uint32_t lane_off = (uint32_t)(q * 32) << 16;
     const int sw = row & 7;
-    uint32_t ps = 0, pph = 0, as = 0, aph = 0;
+    uint32_t g = 0, ps_i = 0;
+    int pending = -1;  // A stage whose store is in flight
     bool ok = true;
     for (int64_t u = blockIdx.x; ok && u < p.n_units; u += gridDim.x) {
-      for (int sb = 0; ok && sb < n_super; ++sb) {
+      for (int sb = 0; ok && sb < n_super; ++sb, ++ps_i) {
+        const uint32_t ps = ps_i % kPStages, pph = (ps_i / kPStages) & 1;
         if (!warp_wait(&p_full[ps], pph, wc)) { ok = false; break; }
         const uint8_t* prow = s_packed + ps * kPackedStageBytes + row * (kKS / 2);
         const uint4 sc = *reinterpret_cast<const uint4*>(s_scales + ps * kScaleStageBytes +
                                                          row * (kKS / 16));
         const uint32_t scw[4] = {sc.x, sc.y, sc.z, sc.w};
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
+        for (int j = 0; j < kKS / kKB; ++j, ++g) {
+          if ((int)(g % kDqPerQuad) != r) continue;
           const uint4 c0 = *reinterpret_cast<const uint4*>(prow + (((2 * j) ^ sw) << 4));
           const uint4 c1 = *reinterpret_cast<const uint4*>(prow + (((2 * j + 1) ^ sw) << 4));
           uint32_t s01, s23;
@@ -360,18 +384,27 @@ __global__ void __launch_bounds__(kThreads, 1)
           dequant8(c1.y, f2, v + 20);
           dequant8(c1.z, f3, v + 24);
           dequant8(c1.w, f3, v + 28);
-          if (!warp_wait(&a_empty[as], aph ^ 1, wc)) { ok = false; break; }
-          tmem_st32(tmem_a + lane_off + as * 32, reinterpret_cast<uint32_t(&)[32]>(v));
-          tc_wait_st();
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&a_full[as]);
-          if (++as == kAStages) { as = 0; aph ^= 1; }
+          const uint32_t st = g % kStages, ph = (g / kStages) & 1;
+          if (!warp_wait(&s_empty[st], ph ^ 1, wc)) { ok = false; break; }
+          if (pending >= 0) {
+            tc_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&a_full[pending]);
+          }
+          tmem_st32(tmem_a + lane_off + st * 32, v);
+          pending = (int)st;
         }
+        // this warp is done reading the packed stage
         __syncwarp();
         if (ok && lane == 0) mbar_arrive(&p_empty[ps]);
-        if (++ps == kPStages) { ps = 0; pph ^= 1; }
       }
+    }
+    if (pending >= 0) {
+      tc_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (ok && lane == 0) mbar_arrive(&a_full[pending]);
     }
   } else {
     // ---------------- epilogue: one thread per vocabulary row, BN tokens
@@ -453,7 +486,7 @@ static int lm_head_token_tile(int64_t M) {
 
 static size_t gemm_smem_bytes(int BN) {
   return 1024 + kPStages * (size_t)(kPackedStageBytes + kScaleStageBytes) +
-         kXStages * (size_t)BN * kKB * 2 + 256;
+         kStages * (size_t)BN * kKB * 2 + 256;
 }
 
 size_t lm_head_workspace_bytes(int64_t M, int64_t N, int64_t K) {
@@ -513,7 +546,7 @@ nvfp4_status lm_head_launch(const void* x, int64_t M, int64_t K, const uint8_t* 
   a.BN = BN;
   a.n_ttiles = n_ttiles;
   a.n_units = ((N + kRows - 1) / kRows) * n_ttiles;
-  a.tmem_cols = (2 * BN + kAStages * 32 <= 256) ? 256u : 512u;
+  a.tmem_cols = (2 * BN + kStages * 32 <= 256) ? 256u : 512u;
   a.tok_scale = tok_scale;
   a.out = logits;
   a.status = status;

@@ -151,34 +151,46 @@ __global__ void __launch_bounds__(kEncodeThreads) nvfp4_encode_kernel(
   const int64_t n_warps = ((int64_t)gridDim.x * blockDim.x) >> 5;
   const int64_t kp = K / 2, ks = K / 16;
 
-  for (int64_t u = n_units - 1 - warp_id; u >= 0; u -= n_warps) {
-    const int64_t row = u / segs_per_row;
-    const int64_t col = (u - row * segs_per_row) * 256 + lane * 8;
-    const bool valid = col < K;  // K % 16 == 0: both lanes of a block agree
-    uint4 v = make_uint4(0, 0, 0, 0);
-    if (valid) v = ld_stream(reinterpret_cast<const uint4*>(W + row * K + col));
-    // block max over the lane pair (16 values)
-    uint32_t bm = fold_u16x2(absmax8(v, 0));
-    bm = max(bm, __shfl_xor_sync(0xFFFFFFFFu, bm, 1));
-    const float vmax = __uint_as_float(bm << 16);
-    float t = __fmul_rn(__fmul_rn(vmax, inv6), ig);
-    t = fminf(t, 448.0f);
-    const __nv_fp8_storage_t s8 = __nv_cvt_float_to_fp8(t, __NV_SATFINITE, __NV_E4M3);
-    const float sf = __half2float(__half(__nv_cvt_fp8_to_halfraw(s8, __NV_E4M3)));
-    const float r = (sf == 0.0f) ? 0.0f : __frcp_rn(__fmul_rn(sf, g));
-    float q[8];
-    q[0] = __fmul_rn(bf16_lo(v.x), r);
-    q[1] = __fmul_rn(bf16_hi(v.x), r);
-    q[2] = __fmul_rn(bf16_lo(v.y), r);
-    q[3] = __fmul_rn(bf16_hi(v.y), r);
-    q[4] = __fmul_rn(bf16_lo(v.z), r);
-    q[5] = __fmul_rn(bf16_hi(v.z), r);
-    q[6] = __fmul_rn(bf16_lo(v.w), r);
-    q[7] = __fmul_rn(bf16_hi(v.w), r);
-    const uint32_t word = cvt_e2m1x8(q);
-    if (valid) {
-      packed[(row * kp + col / 2) >> 2] = word;
-      if ((lane & 1) == 0) scales[row * ks + col / 16] = (uint8_t)s8;
+  // four segments per warp iteration: their loads are issued together so
+  // that each lane keeps 64 bytes in flight
+  constexpr int kU = 4;
+  for (int64_t u0 = n_units - 1 - warp_id; u0 >= 0; u0 -= kU * n_warps) {
+    uint4 v[kU];
+    int64_t row[kU], col[kU];
+#pragma unroll
+    for (int i = 0; i < kU; ++i) {
+      const int64_t u = u0 - i * n_warps;
+      row[i] = u >= 0 ? u / segs_per_row : 0;
+      col[i] = u >= 0 ? (u - row[i] * segs_per_row) * 256 + lane * 8 : K;
+      v[i] = make_uint4(0, 0, 0, 0);
+      if (col[i] < K) v[i] = ld_stream(reinterpret_cast<const uint4*>(W + row[i] * K + col[i]));
+    }
+#pragma unroll
+    for (int i = 0; i < kU; ++i) {
+      const bool valid = col[i] < K;  // K % 16 == 0: both lanes of a block agree
+      // block max over the lane pair (16 values)
+      uint32_t bm = fold_u16x2(absmax8(v[i], 0));
+      bm = max(bm, __shfl_xor_sync(0xFFFFFFFFu, bm, 1));
+      const float vmax = __uint_as_float(bm << 16);
+      float t = __fmul_rn(__fmul_rn(vmax, inv6), ig);
+      t = fminf(t, 448.0f);
+      const __nv_fp8_storage_t s8 = __nv_cvt_float_to_fp8(t, __NV_SATFINITE, __NV_E4M3);
+      const float sf = __half2float(__half(__nv_cvt_fp8_to_halfraw(s8, __NV_E4M3)));
+      const float r = (sf == 0.0f) ? 0.0f : __frcp_rn(__fmul_rn(sf, g));
+      float q[8];
+      q[0] = __fmul_rn(bf16_lo(v[i].x), r);
+      q[1] = __fmul_rn(bf16_hi(v[i].x), r);
+      q[2] = __fmul_rn(bf16_lo(v[i].y), r);
+      q[3] = __fmul_rn(bf16_hi(v[i].y), r);
+      q[4] = __fmul_rn(bf16_lo(v[i].z), r);
+      q[5] = __fmul_rn(bf16_hi(v[i].z), r);
+      q[6] = __fmul_rn(bf16_lo(v[i].w), r);
+      q[7] = __fmul_rn(bf16_hi(v[i].w), r);
+      const uint32_t word = cvt_e2m1x8(q);
+      if (valid) {
+        packed[(row[i] * kp + col[i] / 2) >> 2] = word;
+        if ((lane & 1) == 0) scales[row[i] * ks + col[i] / 16] = (uint8_t)s8;
+      }
     }
   }
 }

@@ -150,8 +150,8 @@ def tiny_x(M: int = 4, K: int = 256) -> np.ndarray:
     return activations(M, K, seed=100, rms_normalize=False)
 
 
-def decode_weight(N: int = 128256, K: int = 4096) -> np.ndarray:
-    return weight(N, K, seed=1, sigma=0.02, p=0.001, mult=20.0)
+def decode_weight(N: int = 128256, K: int = 4096, seed: int = 1) -> np.ndarray:
+    return weight(N, K, seed=seed, sigma=0.02, p=0.001, mult=20.0)
 
 
 def decode_x(M: int, K: int = 4096) -> np.ndarray:
