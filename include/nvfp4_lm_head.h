@@ -57,7 +57,8 @@ typedef enum {
   NVFP4_ERR_CUDA = 6,       /* a CUDA runtime/driver call failed */
   NVFP4_ERR_NONFINITE = 7,  /* device status: W held an Inf or NaN */
   NVFP4_ERR_TIMEOUT = 8,    /* device status: a pipeline wait ran out of time */
-  NVFP4_ERR_UNSUPPORTED = 9 /* no sm_103a device / kernel image for it */
+  NVFP4_ERR_UNSUPPORTED = 9, /* no sm_103a device / kernel image for it */
+  NVFP4_ERR_SCRATCH_LIMIT = 10 /* w4a16_lm_head_noalloc: M*K needs more than its fixed scratch */
 } nvfp4_status;
 
 /* Output dtype codes of w4a16_lm_head. */
@@ -161,6 +162,38 @@ nvfp4_status w4a16_lm_head(const void *x, int64_t M, int64_t K, const uint8_t *p
                            const uint8_t *scales, const float *global_scale, int64_t N,
                            void *logits, int out_dtype, void *workspace, size_t workspace_bytes,
                            void *stream);
+
+/* ------------------------------------------- allocation-free variant */
+
+/* Size of the fixed device scratch array behind w4a16_lm_head_noalloc. */
+#define NVFP4_NOALLOC_SCRATCH_BYTES (2u << 20)
+
+/*
+ * The same product as w4a16_lm_head, for callers that cannot allocate device
+ * memory: runtimes that fix their device-memory budget at start-up and allow
+ * no later cudaMalloc (which may also synchronize the device), or plain C
+ * callers with no device allocator to take a workspace from.  The pages have
+ * no counterpart of this call; it exists for such callers only.
+ *
+ * Arguments, layouts, ownership and accuracy are those of w4a16_lm_head
+ * minus the workspace.  The scratch is one static device array of
+ * NVFP4_NOALLOC_SCRATCH_BYTES (2 MiB) that every GPU loading the library
+ * holds until the process exits.  Its first call on a device looks up the
+ * array's device address (cudaGetSymbolAddress) with that device current;
+ * make that first call before any stream capture.  Shapes whose rescaled
+ * activations do not fit (roughly M_pad * K * 2 bytes, M_pad = M rounded up
+ * to 16, or to 128 above 128 tokens) return NVFP4_ERR_SCRATCH_LIMIT before
+ * anything is enqueued; for example M <= 64 at K <= 8192 fits.  Nothing is
+ * allocated: no cudaMalloc, no cudaFree, no allocating library routine.
+ *
+ * Every call shares the array.  Each call rewrites what it reads and clears
+ * the status word first, but calls that overlap on the GPU (unordered
+ * streams) race on the array.  The device status word of this call lives in
+ * the array and is not exposed.
+ */
+nvfp4_status w4a16_lm_head_noalloc(const void *x, int64_t M, int64_t K, const uint8_t *packed,
+                                   const uint8_t *scales, const float *global_scale, int64_t N,
+                                   void *logits, int out_dtype, void *stream);
 
 #ifdef __cplusplus
 }

@@ -28,7 +28,8 @@ import torch
 __all__ = [
     "NVFP4Error", "Status", "library_path", "load_library", "nvfp4_quantize_rows",
     "nvfp4_refresh", "w4a16_lm_head", "nvfp4_quantize_workspace_bytes",
-    "w4a16_lm_head_workspace_bytes", "nvfp4_read_device_status", "OUT_F32", "OUT_BF16",
+    "w4a16_lm_head_workspace_bytes", "nvfp4_read_device_status", "w4a16_lm_head_noalloc",
+    "OUT_F32", "OUT_BF16",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -50,6 +51,7 @@ class Status(enum.IntEnum):
     ERR_NONFINITE = 7
     ERR_TIMEOUT = 8
     ERR_UNSUPPORTED = 9
+    ERR_SCRATCH_LIMIT = 10
 
 
 class NVFP4Error(RuntimeError):
@@ -90,6 +92,8 @@ def load_library() -> ctypes.CDLL:
     lib.w4a16_lm_head_workspace_bytes.restype = sz
     lib.w4a16_lm_head.argtypes = [vp, i64, i64, vp, vp, vp, i64, vp, ctypes.c_int, vp, sz, vp]
     lib.w4a16_lm_head.restype = st
+    lib.w4a16_lm_head_noalloc.argtypes = [vp, i64, i64, vp, vp, vp, i64, vp, ctypes.c_int, vp]
+    lib.w4a16_lm_head_noalloc.restype = st
     _lib = lib
     return lib
 
@@ -205,6 +209,28 @@ def w4a16_lm_head(x: torch.Tensor, packed: torch.Tensor, scales: torch.Tensor,
                            _ptr(out), code, _ptr(workspace),
                            workspace.numel() * workspace.element_size(), _stream(stream))
     _check(rc, "w4a16_lm_head")
+    return out
+
+
+def w4a16_lm_head_noalloc(x: torch.Tensor, packed: torch.Tensor, scales: torch.Tensor,
+                          global_scale: torch.Tensor, out: torch.Tensor, stream=None) -> torch.Tensor:
+    """w4a16_lm_head without a workspace: the library's fixed 2 MiB device scratch is
+    used instead (for callers that cannot allocate; see the C header).  `out` must be
+    given, so this call allocates nothing."""
+    lib = load_library()
+    _need(x, torch.bfloat16, "x")
+    M, K = x.shape
+    N = packed.shape[0]
+    _need(packed, torch.uint8, "packed", (N, K // 2))
+    _need(scales, scales.dtype, "scales", (N, K // 16))
+    _need(global_scale, torch.float32, "global_scale")
+    _need(out, out.dtype, "out", (M, N))
+    code = {torch.float32: OUT_F32, torch.bfloat16: OUT_BF16}.get(out.dtype)
+    if code is None:
+        raise ValueError("out must be float32 or bfloat16")
+    rc = lib.w4a16_lm_head_noalloc(_ptr(x), M, K, _ptr(packed), _ptr(scales), _ptr(global_scale),
+                                   N, _ptr(out), code, _stream(stream))
+    _check(rc, "w4a16_lm_head_noalloc")
     return out
 
 

@@ -63,6 +63,7 @@ const char* nvfp4_status_string(nvfp4_status s) {
     case NVFP4_ERR_NONFINITE: return "weight holds Inf or NaN";
     case NVFP4_ERR_TIMEOUT: return "device pipeline wait timed out";
     case NVFP4_ERR_UNSUPPORTED: return "device is not sm_103 (GB300)";
+    case NVFP4_ERR_SCRATCH_LIMIT: return "shape needs more than the fixed scratch of the allocation-free call";
   }
   return "unknown status";
 }

@@ -49,7 +49,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 def test_status_strings_and_version(lib):
     assert lib.nvfp4_abi_version() == 100
-    for code in range(10):
+    for code in range(11):
         assert lib.nvfp4_status_string(code)
     assert lib.nvfp4_status_string(7) == b"weight holds Inf or NaN"
 
