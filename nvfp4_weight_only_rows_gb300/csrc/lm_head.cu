@@ -14,13 +14,13 @@
 //     value of that row exactly down to 2^-28 of the row maximum.
 //  2. w4a16_tc_kernel: a persistent, warp-specialized tcgen05 GEMM in the
 //     swapped orientation D[vocab row, token] = A . B^T:
-//       A = dequantized weights, 128 vocabulary rows x 64 k per stage, held
+//       A = dequantized weights, 128 vocabulary rows x 128 k per stage, held
 //           in TENSOR MEMORY (the "ts" MMA form), written by eight dequant
 //           warps with one thread per row and half a stage per warp: e2m1
 //           pairs -> fp16 pairs with the hardware cvt, times the E4M3 block
 //           scale (fp16, exact);
-//       B = the fp16 activations, a TMA tile [BN tokens x 64 k] in shared
-//           memory with the 128-byte swizzle;
+//       B = the fp16 activations, two TMA boxes [BN tokens x 64 k] per
+//           stage in shared memory with the 128-byte swizzle;
 //       D = fp32 accumulators in tensor memory, double buffered, drained by
 //           four epilogue warps (tcgen05.ld, x token multiplier, store).
 //     Packed codes and scales arrive by TMA in 256-k stages; every product
@@ -28,7 +28,7 @@
 //
 // Warp roles (480 threads): 0 packed/scale TMA producer, 1 activation TMA
 // producer, 2 MMA issuer (and TMEM owner), 3-10 dequant (two warps per TMEM
-// lane quadrant taking 64-k stages in turn), 11-14 epilogue.  The producer
+// lane quadrant taking 128-k stages in turn), 11-14 epilogue.  The producer
 // and MMA warps run warp-uniform loops and issue from one elected lane.
 // Every pipeline wait is bounded in time; on expiry the CTA raises
 // NVFP4_ERR_TIMEOUT in the workspace status word, drains what it issued and
@@ -45,10 +45,10 @@
 namespace nvfp4 {
 
 constexpr int kRows = 128;          // vocabulary rows per tile (MMA M)
-constexpr int kKB = 64;             // k per A / activation stage
+constexpr int kKB = 128;            // k per A / activation stage (8 MMAs of K = 16)
 constexpr int kKS = 256;            // k per packed/scale stage
 constexpr int kPStages = 4;         // packed/scale ring depth (18 KB each)
-constexpr int kStages = 8;          // A (TMEM, 32 columns) and activation ring depth
+constexpr int kStages = 4;          // A (TMEM, 64 columns) and activation ring depth
 constexpr int kDqPerQuad = 2;       // dequant warps per TMEM lane quadrant
 constexpr int kDqWarps = 4 * kDqPerQuad;
 constexpr int kFirstDqWarp = 3;
@@ -182,7 +182,7 @@ __device__ __forceinline__ bool elect_one() {
 // Before a producer warp exits, wait (bounded) until the last TMA load it
 // issued into each ring slot has landed, so no copy targets freed memory.
 __device__ __forceinline__ void drain_loads(uint64_t* full, uint32_t n_slots, uint32_t issued,
-                                            int32_t* status) {
+                                            int /*arrivals*/, int32_t* status) {
   volatile int32_t zero = 0;
   WaitCtl drain{status, &zero, 100000000ull};
   for (uint32_t s = 0; s < n_slots && s < issued; ++s) {
@@ -207,16 +207,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   const int BN = p.BN;
-  const uint32_t x_stage_bytes = (uint32_t)BN * (kKB * 2);
+  const uint32_t x_half_bytes = (uint32_t)BN * 128;  // one 64-k box of the activations
+  const uint32_t x_stage_bytes = 2 * x_half_bytes;
   uint8_t* s_packed = smem;                                        // kPStages x 16 KB
   uint8_t* s_scales = s_packed + kPStages * kPackedStageBytes;     // kPStages x 2 KB
-  uint8_t* s_x = s_scales + kPStages * kScaleStageBytes;           // kStages x BN*128
+  uint8_t* s_x = s_scales + kPStages * kScaleStageBytes;           // kStages x BN*256
   uint64_t* bars = reinterpret_cast<uint64_t*>(s_x + kStages * x_stage_bytes);
   uint64_t* p_full = bars;                 // packed/scale stage landed (TMA)
   uint64_t* p_empty = p_full + kPStages;   // packed/scale stage read by every dequant warp
-  uint64_t* x_full = p_empty + kPStages;   // activation stage landed (TMA)
-  uint64_t* a_full = x_full + kStages;     // A stage written to TMEM (one warp per quadrant)
-  uint64_t* s_empty = a_full + kStages;    // the MMAs reading A/activation stage s completed
+  uint64_t* s_full = p_empty + kPStages;   // A stage in TMEM (4 warps) + activation TMA landed
+  uint64_t* s_empty = s_full + kStages;    // the MMAs reading stage s completed
   uint64_t* d_full = s_empty + kStages;
   uint64_t* d_empty = d_full + 2;
   uint64_t* done_bar = d_empty + 2;
@@ -232,8 +232,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&p_empty[i], kDqWarps);
     }
     for (int i = 0; i < kStages; ++i) {
-      mbar_init(&x_full[i], 1);
-      mbar_init(&a_full[i], 4);
+      mbar_init(&s_full[i], 4 + 1);
       mbar_init(&s_empty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
@@ -256,7 +255,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem_base = *tmem_slot;
+  // warp-uniform copy of the TMEM base (lets the compiler keep it uniform)
+  const uint32_t tmem_base = __shfl_sync(0xFFFFFFFFu, *tmem_slot, 0);
   const uint32_t tmem_a = tmem_base + 2 * BN;  // A ring after the two D buffers
 
   WaitCtl wc{p.status, abort_flag, kWaitLimitNs};
@@ -286,9 +286,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
       }
     }
-    drain_loads(p_full, kPStages, issued, p.status);
+    drain_loads(p_full, kPStages, issued, 1, p.status);
   } else if (warp == 1) {
-    // ---------------- activation producer
+    // ---------------- activation producer (two 64-k boxes per stage)
     const uint64_t pol = policy_evict_last();
     uint32_t issued = 0;
     bool ok = true;
@@ -298,17 +298,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t st = issued % kStages, ph = (issued / kStages) & 1;
         if (!warp_wait(&s_empty[st], ph ^ 1, wc)) { ok = false; break; }
         if (elect_one()) {
-          mbar_arrive_expect_tx(&x_full[st], x_stage_bytes);
-          tma_load_2d_hint(s_x + st * x_stage_bytes, &tm_x, kb * kKB, t0, &x_full[st], pol);
+          mbar_arrive_expect_tx(&s_full[st], x_stage_bytes);
+          uint8_t* dst = s_x + st * x_stage_bytes;
+          tma_load_2d_hint(dst, &tm_x, kb * kKB, t0, &s_full[st], pol);
+          tma_load_2d_hint(dst + x_half_bytes, &tm_x, kb * kKB + 64, t0, &s_full[st], pol);
         }
         __syncwarp();
       }
     }
-    drain_loads(x_full, kStages, issued, p.status);
+    drain_loads(s_full, kStages, issued, 5, p.status);
   } else if (warp == 2) {
     // ---------------- MMA issuer (whole warp; one elected lane issues)
     const uint32_t idesc = idesc_f16_f32((uint32_t)BN);
     const uint64_t xdesc0 = smem_desc_sw128(smem_u32(s_x));
+    const uint32_t half_desc = x_half_bytes >> 4;
     uint32_t g = 0;
     bool ok = true;
     int64_t i = 0;
@@ -319,17 +322,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t d_tmem = tmem_base + buf * BN;
       for (int kb = 0; kb < n_kb; ++kb, ++g) {
         const uint32_t st = g % kStages, ph = (g / kStages) & 1;
-        if (!warp_wait(&a_full[st], ph, wc) || !warp_wait(&x_full[st], ph, wc)) {
-          ok = false;
-          break;
-        }
+        if (!warp_wait(&s_full[st], ph, wc)) { ok = false; break; }
         tc_fence_after();
         const uint64_t bdesc = xdesc0 + ((st * x_stage_bytes) >> 4);
-        const uint32_t a_t = tmem_a + st * 32;
+        const uint32_t a_t = tmem_a + st * (kKB / 2);
         if (elect_one()) {
 #pragma unroll
           for (int kk = 0; kk < kKB / 16; ++kk)
-            tc_mma_ts(d_tmem, a_t + kk * 8, bdesc + 2 * kk, idesc, (kb | kk) != 0);
+            tc_mma_ts(d_tmem, a_t + kk * 8, bdesc + (kk >> 2) * half_desc + 2 * (kk & 3), idesc,
+                      (kb | kk) != 0);
           tc_commit(&s_empty[st]);
         }
         __syncwarp();
@@ -348,9 +349,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_wait(done_bar, 0, drain);
   } else if (warp < kFirstEpiWarp) {
     // ---------------- dequant: one thread per vocabulary row.  The kDqPerQuad
-    // warps of a TMEM lane quadrant take the 64-k stages round-robin; a
-    // stage's TMEM store is completed (wait::st) only after the warp's next
-    // stage has been converted, so the store latency overlaps that work.
+    // warps of a TMEM lane quadrant take the 128-k stages in turn; a stage's
+    // TMEM store is completed (wait::st) only after the warp's next stage has
+    // been converted, so the store latency overlaps that work.
     const int q = warp & 3;
     const int r = (warp - kFirstDqWarp) >> 2;
     const int row = q * 32 + lane;
@@ -370,29 +371,31 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int j = 0; j < kKS / kKB; ++j, ++g) {
           if ((int)(g % kDqPerQuad) != r) continue;
-          const uint4 c0 = *reinterpret_cast<const uint4*>(prow + (((2 * j) ^ sw) << 4));
-          const uint4 c1 = *reinterpret_cast<const uint4*>(prow + (((2 * j + 1) ^ sw) << 4));
-          uint32_t s01, s23;
-          scales4_to_f16(scw[j], s01, s23);
-          const uint32_t f0 = dup_lo(s01), f1 = dup_hi(s01), f2 = dup_lo(s23), f3 = dup_hi(s23);
-          uint32_t v[32];
-          dequant8(c0.x, f0, v + 0);
-          dequant8(c0.y, f0, v + 4);
-          dequant8(c0.z, f1, v + 8);
-          dequant8(c0.w, f1, v + 12);
-          dequant8(c1.x, f2, v + 16);
-          dequant8(c1.y, f2, v + 20);
-          dequant8(c1.z, f3, v + 24);
-          dequant8(c1.w, f3, v + 28);
+          uint32_t v[kKB / 2];
+#pragma unroll
+          for (int c = 0; c < kKB / 32; ++c) {  // 16-byte chunks: 32 codes, two 16-blocks
+            const uint4 ch =
+                *reinterpret_cast<const uint4*>(prow + ((((kKB / 32) * j + c) ^ sw) << 4));
+            uint32_t s01, s23;
+            scales4_to_f16(scw[(kKB / 64) * j + (c >> 1)], s01, s23);
+            const uint32_t sp = (c & 1) ? s23 : s01;
+            const uint32_t f0 = dup_lo(sp), f1 = dup_hi(sp);
+            dequant8(ch.x, f0, v + 16 * c + 0);
+            dequant8(ch.y, f0, v + 16 * c + 4);
+            dequant8(ch.z, f1, v + 16 * c + 8);
+            dequant8(ch.w, f1, v + 16 * c + 12);
+          }
           const uint32_t st = g % kStages, ph = (g / kStages) & 1;
           if (!warp_wait(&s_empty[st], ph ^ 1, wc)) { ok = false; break; }
           if (pending >= 0) {
             tc_wait_st();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&a_full[pending]);
+            if (lane == 0) mbar_arrive(&s_full[pending]);
           }
-          tmem_st32(tmem_a + lane_off + st * 32, v);
+          const uint32_t ta = tmem_a + lane_off + st * (kKB / 2);
+          tmem_st32(ta, *reinterpret_cast<const uint32_t(*)[32]>(v));
+          tmem_st32(ta + 32, *reinterpret_cast<const uint32_t(*)[32]>(v + 32));
           pending = (int)st;
         }
         // this warp is done reading the packed stage
@@ -404,7 +407,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (ok && lane == 0) mbar_arrive(&a_full[pending]);
+      if (ok && lane == 0) mbar_arrive(&s_full[pending]);
     }
   } else {
     // ---------------- epilogue: one thread per vocabulary row, BN tokens
@@ -531,7 +534,7 @@ nvfp4_status lm_head_launch(const void* x, int64_t M, int64_t K, const uint8_t* 
       !encode_2d(&tm_scales, CU_TENSOR_MAP_DATA_TYPE_UINT8, scales, (uint64_t)K / 16, (uint64_t)N,
                  (uint64_t)K / 16, kKS / 16, kRows, CU_TENSOR_MAP_SWIZZLE_NONE) ||
       !encode_2d(&tm_x, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, x16, (uint64_t)K, (uint64_t)m_pad,
-                 (uint64_t)K * 2, kKB, (uint32_t)BN, CU_TENSOR_MAP_SWIZZLE_128B))
+                 (uint64_t)K * 2, 64, (uint32_t)BN, CU_TENSOR_MAP_SWIZZLE_128B))
     return NVFP4_ERR_CUDA;
 
   if (cudaMemsetAsync(status, 0, sizeof(int32_t), stream) != cudaSuccess) return NVFP4_ERR_CUDA;
@@ -546,7 +549,7 @@ nvfp4_status lm_head_launch(const void* x, int64_t M, int64_t K, const uint8_t* 
   a.BN = BN;
   a.n_ttiles = n_ttiles;
   a.n_units = ((N + kRows - 1) / kRows) * n_ttiles;
-  a.tmem_cols = (2 * BN + kStages * 32 <= 256) ? 256u : 512u;
+  a.tmem_cols = (2 * BN + kStages * (kKB / 2) <= 256) ? 256u : 512u;
   a.tok_scale = tok_scale;
   a.out = logits;
   a.status = status;
