@@ -14,12 +14,12 @@
 //     value of that row exactly down to 2^-28 of the row maximum.
 //  2. w4a16_tc_kernel: a persistent, warp-specialized tcgen05 GEMM in the
 //     swapped orientation D[vocab row, token] = A . B^T:
-//       A = dequantized weights, 128 vocabulary rows x 128 k per stage, held
+//       A = dequantized weights, 128 vocabulary rows x 256 k per stage, held
 //           in TENSOR MEMORY (the "ts" MMA form), written by eight dequant
 //           warps with one thread per row and half a stage per warp: e2m1
 //           pairs -> fp16 pairs with the hardware cvt, times the E4M3 block
 //           scale (fp16, exact);
-//       B = the fp16 activations, two TMA boxes [BN tokens x 64 k] per
+//       B = the fp16 activations, four TMA boxes [BN tokens x 64 k] per
 //           stage in shared memory with the 128-byte swizzle;
 //       D = fp32 accumulators in tensor memory, double buffered, drained by
 //           four epilogue warps (tcgen05.ld, x token multiplier, store).
@@ -28,7 +28,7 @@
 //
 // Warp roles (480 threads): 0 packed/scale TMA producer, 1 activation TMA
 // producer, 2 MMA issuer (and TMEM owner), 3-10 dequant (two warps per TMEM
-// lane quadrant taking 128-k stages in turn), 11-14 epilogue.  The producer
+// lane quadrant taking 256-k stages in turn), 11-14 epilogue.  The producer
 // and MMA warps run warp-uniform loops and issue from one elected lane.
 // Every pipeline wait is bounded in time; on expiry the CTA raises
 // NVFP4_ERR_TIMEOUT in the workspace status word, drains what it issued and
@@ -45,10 +45,10 @@
 namespace nvfp4 {
 
 constexpr int kRows = 128;          // vocabulary rows per tile (MMA M)
-constexpr int kKB = 128;            // k per A / activation stage (8 MMAs of K = 16)
+constexpr int kKB = 256;            // k per A / activation stage (16 MMAs of K = 16)
 constexpr int kKS = 256;            // k per packed/scale stage
 constexpr int kPStages = 4;         // packed/scale ring depth (18 KB each)
-constexpr int kStages = 4;          // A (TMEM, 64 columns) and activation ring depth
+constexpr int kStages = 2;          // A (TMEM, 128 columns) and activation ring depth
 constexpr int kDqPerQuad = 2;       // dequant warps per TMEM lane quadrant
 constexpr int kDqWarps = 4 * kDqPerQuad;
 constexpr int kFirstDqWarp = 3;
@@ -207,14 +207,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   const int BN = p.BN;
-  const uint32_t x_half_bytes = (uint32_t)BN * 128;  // one 64-k box of the activations
-  const uint32_t x_stage_bytes = 2 * x_half_bytes;
+  const uint32_t x_box_bytes = (uint32_t)BN * 128;  // one 64-k TMA box of the activations
+  const uint32_t x_stage_bytes = (kKB / 64) * x_box_bytes;
   uint8_t* s_packed = smem;                                        // kPStages x 16 KB
   uint8_t* s_scales = s_packed + kPStages * kPackedStageBytes;     // kPStages x 2 KB
-  uint8_t* s_x = s_scales + kPStages * kScaleStageBytes;           // kStages x BN*256
+  uint8_t* s_x = s_scales + kPStages * kScaleStageBytes;           // kStages x BN*512
   uint64_t* bars = reinterpret_cast<uint64_t*>(s_x + kStages * x_stage_bytes);
   uint64_t* p_full = bars;                 // packed/scale stage landed (TMA)
-  uint64_t* p_empty = p_full + kPStages;   // packed/scale stage read by every dequant warp
+  uint64_t* p_empty = p_full + kPStages;   // packed/scale stage read by its 4 dequant warps
   uint64_t* s_full = p_empty + kPStages;   // A stage in TMEM (4 warps) + activation TMA landed
   uint64_t* s_empty = s_full + kStages;    // the MMAs reading stage s completed
   uint64_t* d_full = s_empty + kStages;
@@ -229,7 +229,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < kPStages; ++i) {
       mbar_init(&p_full[i], 1);
-      mbar_init(&p_empty[i], kDqWarps);
+      mbar_init(&p_empty[i], 4);
     }
     for (int i = 0; i < kStages; ++i) {
       mbar_init(&s_full[i], 4 + 1);
@@ -261,8 +261,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   WaitCtl wc{p.status, abort_flag, kWaitLimitNs};
   const int64_t K = p.K;
-  const int n_super = (int)(K / kKS);
-  const int n_kb = (int)(K / kKB);
+  const int n_kb = (int)(K / kKB);  // stages per unit: one packed stage = one A stage
   // the producer and MMA loops below are warp-uniform; one elected lane
   // issues each TMA / tcgen05 instruction
 
@@ -273,7 +272,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     for (int64_t u = blockIdx.x; ok && u < p.n_units; u += gridDim.x) {
       const int32_t n0 = (int32_t)((u / p.n_ttiles) * kRows);
-      for (int sb = 0; sb < n_super; ++sb, ++issued) {
+      for (int sb = 0; sb < n_kb; ++sb, ++issued) {
         const uint32_t st = issued % kPStages, ph = (issued / kPStages) & 1;
         if (!warp_wait(&p_empty[st], ph ^ 1, wc)) { ok = false; break; }
         if (elect_one()) {
@@ -288,7 +287,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     drain_loads(p_full, kPStages, issued, 1, p.status);
   } else if (warp == 1) {
-    // ---------------- activation producer (two 64-k boxes per stage)
+    // ---------------- activation producer (four 64-k boxes per stage)
     const uint64_t pol = policy_evict_last();
     uint32_t issued = 0;
     bool ok = true;
@@ -300,8 +299,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (elect_one()) {
           mbar_arrive_expect_tx(&s_full[st], x_stage_bytes);
           uint8_t* dst = s_x + st * x_stage_bytes;
-          tma_load_2d_hint(dst, &tm_x, kb * kKB, t0, &s_full[st], pol);
-          tma_load_2d_hint(dst + x_half_bytes, &tm_x, kb * kKB + 64, t0, &s_full[st], pol);
+#pragma unroll
+          for (int b = 0; b < kKB / 64; ++b)
+            tma_load_2d_hint(dst + b * x_box_bytes, &tm_x, kb * kKB + 64 * b, t0, &s_full[st],
+                             pol);
         }
         __syncwarp();
       }
@@ -311,7 +312,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------- MMA issuer (whole warp; one elected lane issues)
     const uint32_t idesc = idesc_f16_f32((uint32_t)BN);
     const uint64_t xdesc0 = smem_desc_sw128(smem_u32(s_x));
-    const uint32_t half_desc = x_half_bytes >> 4;
+    const uint32_t box_desc = x_box_bytes >> 4;
     uint32_t g = 0;
     bool ok = true;
     int64_t i = 0;
@@ -329,7 +330,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (elect_one()) {
 #pragma unroll
           for (int kk = 0; kk < kKB / 16; ++kk)
-            tc_mma_ts(d_tmem, a_t + kk * 8, bdesc + (kk >> 2) * half_desc + 2 * (kk & 3), idesc,
+            tc_mma_ts(d_tmem, a_t + kk * 8, bdesc + (kk >> 2) * box_desc + 2 * (kk & 3), idesc,
                       (kb | kk) != 0);
           tc_commit(&s_empty[st]);
         }
@@ -349,65 +350,56 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_wait(done_bar, 0, drain);
   } else if (warp < kFirstEpiWarp) {
     // ---------------- dequant: one thread per vocabulary row.  The kDqPerQuad
-    // warps of a TMEM lane quadrant take the 128-k stages in turn; a stage's
-    // TMEM store is completed (wait::st) only after the warp's next stage has
-    // been converted, so the store latency overlaps that work.
+    // warps of a TMEM lane quadrant take the 256-k stages in turn: wait for
+    // the packed stage, convert 64 k at a time into 32 registers and store
+    // them to the stage's TMEM columns, then signal the MMA warp.
     const int q = warp & 3;
     const int r = (warp - kFirstDqWarp) >> 2;
     const int row = q * 32 + lane;
     const uint32_t lane_off = (uint32_t)(q * 32) << 16;
     const int sw = row & 7;
-    uint32_t g = 0, ps_i = 0;
-    int pending = -1;  // A stage whose store is in flight
+    uint32_t g = 0;
     bool ok = true;
     for (int64_t u = blockIdx.x; ok && u < p.n_units; u += gridDim.x) {
-      for (int sb = 0; ok && sb < n_super; ++sb, ++ps_i) {
-        const uint32_t ps = ps_i % kPStages, pph = (ps_i / kPStages) & 1;
+      for (int sb = 0; sb < n_kb; ++sb, ++g) {
+        if ((int)(g % kDqPerQuad) != r) continue;
+        const uint32_t ps = g % kPStages, pph = (g / kPStages) & 1;
+        const uint32_t st = g % kStages, ph = (g / kStages) & 1;
         if (!warp_wait(&p_full[ps], pph, wc)) { ok = false; break; }
         const uint8_t* prow = s_packed + ps * kPackedStageBytes + row * (kKS / 2);
         const uint4 sc = *reinterpret_cast<const uint4*>(s_scales + ps * kScaleStageBytes +
                                                          row * (kKS / 16));
         const uint32_t scw[4] = {sc.x, sc.y, sc.z, sc.w};
+        const uint32_t ta = tmem_a + lane_off + st * (kKB / 2);
 #pragma unroll
-        for (int j = 0; j < kKS / kKB; ++j, ++g) {
-          if ((int)(g % kDqPerQuad) != r) continue;
-          uint32_t v[kKB / 2];
-#pragma unroll
-          for (int c = 0; c < kKB / 32; ++c) {  // 16-byte chunks: 32 codes, two 16-blocks
-            const uint4 ch =
-                *reinterpret_cast<const uint4*>(prow + ((((kKB / 32) * j + c) ^ sw) << 4));
-            uint32_t s01, s23;
-            scales4_to_f16(scw[(kKB / 64) * j + (c >> 1)], s01, s23);
-            const uint32_t sp = (c & 1) ? s23 : s01;
-            const uint32_t f0 = dup_lo(sp), f1 = dup_hi(sp);
-            dequant8(ch.x, f0, v + 16 * c + 0);
-            dequant8(ch.y, f0, v + 16 * c + 4);
-            dequant8(ch.z, f1, v + 16 * c + 8);
-            dequant8(ch.w, f1, v + 16 * c + 12);
-          }
-          const uint32_t st = g % kStages, ph = (g / kStages) & 1;
-          if (!warp_wait(&s_empty[st], ph ^ 1, wc)) { ok = false; break; }
-          if (pending >= 0) {
-            tc_wait_st();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&s_full[pending]);
-          }
-          const uint32_t ta = tmem_a + lane_off + st * (kKB / 2);
-          tmem_st32(ta, *reinterpret_cast<const uint32_t(*)[32]>(v));
-          tmem_st32(ta + 32, *reinterpret_cast<const uint32_t(*)[32]>(v + 32));
-          pending = (int)st;
+        for (int c4 = 0; c4 < kKB / 64; ++c4) {
+          const uint4 c0 = *reinterpret_cast<const uint4*>(prow + (((2 * c4) ^ sw) << 4));
+          const uint4 c1 = *reinterpret_cast<const uint4*>(prow + (((2 * c4 + 1) ^ sw) << 4));
+          uint32_t s01, s23;
+          scales4_to_f16(scw[c4], s01, s23);
+          const uint32_t f0 = dup_lo(s01), f1 = dup_hi(s01), f2 = dup_lo(s23), f3 = dup_hi(s23);
+          uint32_t v[32];
+          dequant8(c0.x, f0, v + 0);
+          dequant8(c0.y, f0, v + 4);
+          dequant8(c0.z, f1, v + 8);
+          dequant8(c0.w, f1, v + 12);
+          dequant8(c1.x, f2, v + 16);
+          dequant8(c1.y, f2, v + 20);
+          dequant8(c1.z, f3, v + 24);
+          dequant8(c1.w, f3, v + 28);
+          if (c4 == 0 && !warp_wait(&s_empty[st], ph ^ 1, wc)) { ok = false; break; }
+          tmem_st32(ta + c4 * 32, v);
         }
-        // this warp is done reading the packed stage
+        if (!ok) break;
+        // the packed stage has been read; the A stage is complete once the
+        // TMEM stores land
         __syncwarp();
-        if (ok && lane == 0) mbar_arrive(&p_empty[ps]);
+        if (lane == 0) mbar_arrive(&p_empty[ps]);
+        tc_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&s_full[st]);
       }
-    }
-    if (pending >= 0) {
-      tc_wait_st();
-      tc_fence_before();
-      __syncwarp();
-      if (ok && lane == 0) mbar_arrive(&s_full[pending]);
     }
   } else {
     // ---------------- epilogue: one thread per vocabulary row, BN tokens
