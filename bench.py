@@ -75,11 +75,11 @@ def load_peaks() -> dict:
 
 
 def load_traffic() -> dict:
-    """Per-launch DRAM bytes from the committed ncu summary, when it is current."""
+    """Per-launch DRAM bytes (read + write) from the committed ncu summaries."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if os.path.exists(path):
         with open(path) as f:
-            return json.load(f)
+            return {k: v for k, v in json.load(f).items() if not k.startswith("_")}
     return {}
 
 

@@ -6,7 +6,8 @@
 // the checkpoint layout `_quantize_nvfp4` writes on the page
 // "vllm.model_executor.layers.quantization.online.lm_head").
 //
-// Two kernels per call:
+// Two kernels per call (the second launched as a programmatic dependent of
+// the first, so it streams weights while the first finishes):
 //  1. w4a16_prep_x_kernel: each token row of x (bf16) is rescaled by an
 //     exact power of two 2^e so that its largest magnitude lands in
 //     [2^14, 2^15), and stored as fp16 in the workspace; the token's output
@@ -75,7 +76,12 @@ __global__ void __launch_bounds__(256) w4a16_prep_x_kernel(const uint16_t* __res
                                                            int64_t M, int64_t K,
                                                            const float* __restrict__ global,
                                                            __half* __restrict__ x16,
-                                                           float* __restrict__ tok_scale) {
+                                                           float* __restrict__ tok_scale,
+                                                           int32_t* __restrict__ status) {
+  // the GEMM may launch now: it waits for this grid's results (griddepcontrol.wait)
+  // only where it reads them, and streams the weights meanwhile
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  if (blockIdx.x == 0 && threadIdx.x == 0) *status = NVFP4_OK;  // a fresh call: clear the word
   const int64_t m = blockIdx.x;
   __half* dst = x16 + m * K;
   const int64_t nv = K / 8;
@@ -191,6 +197,12 @@ __device__ __forceinline__ void drain_loads(uint64_t* full, uint32_t n_slots, ui
   }
 }
 
+// Wait until the preceding kernel in the stream (launched with programmatic
+// stream serialization) has completed and its writes are visible.
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // warp-uniform bounded wait: every lane polls, the warp agrees on the outcome
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const WaitCtl& wc) {
   const bool ok = mbar_wait(bar, parity, wc);
@@ -288,6 +300,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     drain_loads(p_full, kPStages, issued, 1, p.status);
   } else if (warp == 1) {
     // ---------------- activation producer (four 64-k boxes per stage)
+    grid_dependency_wait();  // the rescaled activations come from the prep kernel
     const uint64_t pol = policy_evict_last();
     uint32_t issued = 0;
     bool ok = true;
@@ -403,6 +416,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ---------------- epilogue: one thread per vocabulary row, BN tokens
+    grid_dependency_wait();  // token multipliers come from the prep kernel
     const int q = warp & 3;
     const int row = q * 32 + lane;
     const uint32_t lane_off = (uint32_t)(q * 32) << 16;
@@ -529,9 +543,8 @@ nvfp4_status lm_head_launch(const void* x, int64_t M, int64_t K, const uint8_t* 
                  (uint64_t)K * 2, 64, (uint32_t)BN, CU_TENSOR_MAP_SWIZZLE_128B))
     return NVFP4_ERR_CUDA;
 
-  if (cudaMemsetAsync(status, 0, sizeof(int32_t), stream) != cudaSuccess) return NVFP4_ERR_CUDA;
   w4a16_prep_x_kernel<<<(unsigned)m_pad, 256, 0, stream>>>(static_cast<const uint16_t*>(x), M, K,
-                                                            global_scale, x16, tok_scale);
+                                                            global_scale, x16, tok_scale, status);
   if (cudaGetLastError() != cudaSuccess) return NVFP4_ERR_CUDA;
 
   GemmArgs a;
@@ -547,14 +560,27 @@ nvfp4_status lm_head_launch(const void* x, int64_t M, int64_t K, const uint8_t* 
   a.status = status;
   const int grid = (int)std::min<int64_t>(sms, a.n_units);
   const size_t smem = gemm_smem_bytes(BN);
+  // programmatic dependent launch: the GEMM starts streaming weights while
+  // the prep kernel is still running
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t err;
   if (out_dtype == NVFP4_OUT_BF16) {
     if (set_smem_attr<true>() != cudaSuccess) return NVFP4_ERR_CUDA;
-    w4a16_tc_kernel<true><<<grid, kThreads, smem, stream>>>(tm_packed, tm_scales, tm_x, a);
+    err = cudaLaunchKernelEx(&cfg, w4a16_tc_kernel<true>, tm_packed, tm_scales, tm_x, a);
   } else {
     if (set_smem_attr<false>() != cudaSuccess) return NVFP4_ERR_CUDA;
-    w4a16_tc_kernel<false><<<grid, kThreads, smem, stream>>>(tm_packed, tm_scales, tm_x, a);
+    err = cudaLaunchKernelEx(&cfg, w4a16_tc_kernel<false>, tm_packed, tm_scales, tm_x, a);
   }
-  if (cudaGetLastError() != cudaSuccess) return NVFP4_ERR_CUDA;
+  if (err != cudaSuccess || cudaGetLastError() != cudaSuccess) return NVFP4_ERR_CUDA;
   return NVFP4_OK;
 }
 

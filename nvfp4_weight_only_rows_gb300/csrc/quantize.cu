@@ -7,12 +7,12 @@
 //          taken on the integer bit patterns (exact), one partial per CTA.
 //   pass 2 (nvfp4_encode_kernel): every CTA folds the partials into amax,
 //          derives global = max(amax / 2688, 1e-12) and its reciprocal,
-//          then one warp per 256-value row segment encodes: each lane loads
-//          8 bf16 (16 bytes), a lane pair forms one 16-value block, one
-//          shuffle gives the block max, and each lane stores one 32-bit
-//          word of 8 packed codes; even lanes store the E4M3 scale byte.
-//          Segments are walked from the end of W backwards so the tail that
-//          pass 1 left in L2 is consumed first.
+//          then each warp encodes whole rows in 256-value segments: each
+//          lane loads 8 bf16 (16 bytes), a lane pair forms one 16-value
+//          block, one shuffle gives the block max, and each lane stores one
+//          32-bit word of 8 packed codes; even lanes store the E4M3 scale
+//          byte.  Rows are walked from the end of W backwards so the tail
+//          that pass 1 left in L2 is consumed first.
 //
 // Arithmetic (each an IEEE binary32 operation, round to nearest even):
 //   t  = min((vmax * fl(1/6)) * inv_global, 448)     block scale before E4M3
@@ -57,7 +57,9 @@ __device__ __forceinline__ uint32_t fold_u16x2(uint32_t m) { return max(m & 0xFF
 
 __global__ void __launch_bounds__(kAmaxThreads) nvfp4_amax_kernel(const uint4* __restrict__ W,
                                                                   int64_t n_vec,
-                                                                  uint32_t* __restrict__ partial) {
+                                                                  uint32_t* __restrict__ partial,
+                                                                  int32_t* __restrict__ status) {
+  if (blockIdx.x == 0 && threadIdx.x == 0) *status = NVFP4_OK;  // a fresh call: clear the word
   uint32_t m = 0;
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
@@ -143,53 +145,53 @@ __global__ void __launch_bounds__(kEncodeThreads) nvfp4_encode_kernel(
   const float ig = sg[1];
   const float inv6 = 1.0f / 6.0f;
 
-  // ---- encode: one warp per 256-value row segment, walked backwards
+  // ---- encode: each warp takes whole rows, from the last row backwards
+  // (pass 1 left the tail of W in L2); a row is walked in 256-value
+  // segments, four segment loads in flight per lane
   const int lane = threadIdx.x & 31;
-  const int64_t segs_per_row = (K + 255) / 256;
-  const int64_t n_units = N * segs_per_row;
+  const int segs = (int)((K + 255) / 256);
   const int64_t warp_id = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int64_t n_warps = ((int64_t)gridDim.x * blockDim.x) >> 5;
-  const int64_t kp = K / 2, ks = K / 16;
-
-  // four segments per warp iteration: their loads are issued together so
-  // that each lane keeps 64 bytes in flight
   constexpr int kU = 4;
-  for (int64_t u0 = n_units - 1 - warp_id; u0 >= 0; u0 -= kU * n_warps) {
-    uint4 v[kU];
-    int64_t row[kU], col[kU];
+  for (int64_t row = N - 1 - warp_id; row >= 0; row -= n_warps) {
+    const uint16_t* wrow = W + row * K;
+    uint32_t* prow = packed + row * (K / 8);
+    uint8_t* srow = scales + row * (K / 16);
+    for (int s0 = 0; s0 < segs; s0 += kU) {
+      uint4 v[kU];
 #pragma unroll
-    for (int i = 0; i < kU; ++i) {
-      const int64_t u = u0 - i * n_warps;
-      row[i] = u >= 0 ? u / segs_per_row : 0;
-      col[i] = u >= 0 ? (u - row[i] * segs_per_row) * 256 + lane * 8 : K;
-      v[i] = make_uint4(0, 0, 0, 0);
-      if (col[i] < K) v[i] = ld_stream(reinterpret_cast<const uint4*>(W + row[i] * K + col[i]));
-    }
+      for (int i = 0; i < kU; ++i) {
+        const int col = (s0 + i) * 256 + lane * 8;
+        v[i] = make_uint4(0, 0, 0, 0);
+        if (col < K) v[i] = ld_stream(reinterpret_cast<const uint4*>(wrow + col));
+      }
 #pragma unroll
-    for (int i = 0; i < kU; ++i) {
-      const bool valid = col[i] < K;  // K % 16 == 0: both lanes of a block agree
-      // block max over the lane pair (16 values)
-      uint32_t bm = fold_u16x2(absmax8(v[i], 0));
-      bm = max(bm, __shfl_xor_sync(0xFFFFFFFFu, bm, 1));
-      const float vmax = __uint_as_float(bm << 16);
-      float t = __fmul_rn(__fmul_rn(vmax, inv6), ig);
-      t = fminf(t, 448.0f);
-      const __nv_fp8_storage_t s8 = __nv_cvt_float_to_fp8(t, __NV_SATFINITE, __NV_E4M3);
-      const float sf = __half2float(__half(__nv_cvt_fp8_to_halfraw(s8, __NV_E4M3)));
-      const float r = (sf == 0.0f) ? 0.0f : __frcp_rn(__fmul_rn(sf, g));
-      float q[8];
-      q[0] = __fmul_rn(bf16_lo(v[i].x), r);
-      q[1] = __fmul_rn(bf16_hi(v[i].x), r);
-      q[2] = __fmul_rn(bf16_lo(v[i].y), r);
-      q[3] = __fmul_rn(bf16_hi(v[i].y), r);
-      q[4] = __fmul_rn(bf16_lo(v[i].z), r);
-      q[5] = __fmul_rn(bf16_hi(v[i].z), r);
-      q[6] = __fmul_rn(bf16_lo(v[i].w), r);
-      q[7] = __fmul_rn(bf16_hi(v[i].w), r);
-      const uint32_t word = cvt_e2m1x8(q);
-      if (valid) {
-        packed[(row[i] * kp + col[i] / 2) >> 2] = word;
-        if ((lane & 1) == 0) scales[row[i] * ks + col[i] / 16] = (uint8_t)s8;
+      for (int i = 0; i < kU; ++i) {
+        const int col = (s0 + i) * 256 + lane * 8;
+        // block max over the lane pair (16 values); K % 16 == 0, so both
+        // lanes of a pair are in or out of the row together
+        uint32_t bm = fold_u16x2(absmax8(v[i], 0));
+        bm = max(bm, __shfl_xor_sync(0xFFFFFFFFu, bm, 1));
+        const float vmax = __uint_as_float(bm << 16);
+        float t = __fmul_rn(__fmul_rn(vmax, inv6), ig);
+        t = fminf(t, 448.0f);
+        const __nv_fp8_storage_t s8 = __nv_cvt_float_to_fp8(t, __NV_SATFINITE, __NV_E4M3);
+        const float sf = __half2float(__half(__nv_cvt_fp8_to_halfraw(s8, __NV_E4M3)));
+        const float r = (sf == 0.0f) ? 0.0f : __frcp_rn(__fmul_rn(sf, g));
+        float q[8];
+        q[0] = __fmul_rn(bf16_lo(v[i].x), r);
+        q[1] = __fmul_rn(bf16_hi(v[i].x), r);
+        q[2] = __fmul_rn(bf16_lo(v[i].y), r);
+        q[3] = __fmul_rn(bf16_hi(v[i].y), r);
+        q[4] = __fmul_rn(bf16_lo(v[i].z), r);
+        q[5] = __fmul_rn(bf16_hi(v[i].z), r);
+        q[6] = __fmul_rn(bf16_lo(v[i].w), r);
+        q[7] = __fmul_rn(bf16_hi(v[i].w), r);
+        const uint32_t word = cvt_e2m1x8(q);
+        if (col < K) {
+          prow[col >> 3] = word;
+          if ((lane & 1) == 0) srow[col >> 4] = (uint8_t)s8;
+        }
       }
     }
   }
@@ -221,14 +223,12 @@ nvfp4_status quantize_launch(const void* W, int64_t N, int64_t K, uint8_t* packe
   int blocks1 = (int)std::min<int64_t>(std::min<int64_t>(want, (int64_t)sms * 8), kMaxAmaxBlocks);
   if (blocks1 < 1) blocks1 = 1;
 
-  if (cudaMemsetAsync(status, 0, sizeof(int32_t), stream) != cudaSuccess) return NVFP4_ERR_CUDA;
   nvfp4_amax_kernel<<<blocks1, kAmaxThreads, 0, stream>>>(static_cast<const uint4*>(W), n_vec,
-                                                          partial);
+                                                          partial, status);
   if (cudaGetLastError() != cudaSuccess) return NVFP4_ERR_CUDA;
 
-  const int64_t units = N * ((K + 255) / 256);
   const int64_t warps_per_block = kEncodeThreads / 32;
-  int64_t want2 = (units + warps_per_block - 1) / warps_per_block;
+  int64_t want2 = (N + warps_per_block - 1) / warps_per_block;
   int blocks2 = (int)std::min<int64_t>(want2, (int64_t)sms * 8);
   if (blocks2 < 1) blocks2 = 1;
   nvfp4_encode_kernel<<<blocks2, kEncodeThreads, 0, stream>>>(
