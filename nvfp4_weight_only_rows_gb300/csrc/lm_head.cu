@@ -48,13 +48,27 @@ namespace nvfp4 {
 constexpr int kRows = 128;          // vocabulary rows per tile (MMA M)
 constexpr int kKB = 256;            // k per A / activation stage (16 MMAs of K = 16)
 constexpr int kKS = 256;            // k per packed/scale stage
-constexpr int kPStages = 4;         // packed/scale ring depth (18 KB each)
-constexpr int kStages = 2;          // A (TMEM, 128 columns) and activation ring depth
-constexpr int kDqPerQuad = 2;       // dequant warps per TMEM lane quadrant
-constexpr int kDqWarps = 4 * kDqPerQuad;
 constexpr int kFirstDqWarp = 3;
-constexpr int kFirstEpiWarp = kFirstDqWarp + kDqWarps;
-constexpr int kThreads = 32 * (kFirstEpiWarp + 4);
+
+// Ring depths and the number of dequant warps per TMEM lane quadrant are
+// template parameters of the GEMM:
+//   token tiles of up to 64 (decode): 3 A/activation stages, 6 packed
+//     stages, 3 warps per quadrant (TMEM: 2 x 64 accumulator columns +
+//     3 x 128 A columns = 512);
+//   token tiles of 128 (prefill): 2 A/activation stages, 4 packed stages,
+//     2 warps per quadrant.
+// A dequant warp takes every kDq-th stage.  An mbarrier parity wait for
+// phase j is only sound once phase j-1 has completed; the warp itself has
+// checked that for the slot's previous use only if that use was one of its
+// own stages, i.e. if kDq divides the ring depth.
+template <int kStages, int kPStages, int kDq>
+struct GemmShape {
+  static_assert(kStages % kDq == 0 && kPStages % kDq == 0,
+                "dequant warps per quadrant must divide every ring depth they wait on");
+  static constexpr int kDqWarps = 4 * kDq;
+  static constexpr int kFirstEpiWarp = kFirstDqWarp + kDqWarps;
+  static constexpr int kThreads = 32 * (kFirstEpiWarp + 4);
+};
 constexpr uint32_t kPackedStageBytes = kRows * (kKS / 2);   // 16384
 constexpr uint32_t kScaleStageBytes = kRows * (kKS / 16);   // 2048
 constexpr int kMaxBN = 128;
@@ -210,11 +224,13 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const 
 }
 
 // ------------------------------------------------------------ the GEMM
-template <bool kOutBf16>
-__global__ void __launch_bounds__(kThreads, 1)
+template <bool kOutBf16, int kStages, int kPStages, int kDqPerQuad>
+__global__ void __launch_bounds__((GemmShape<kStages, kPStages, kDqPerQuad>::kThreads), 1)
     w4a16_tc_kernel(const __grid_constant__ CUtensorMap tm_packed,
                     const __grid_constant__ CUtensorMap tm_scales,
                     const __grid_constant__ CUtensorMap tm_x, const GemmArgs p) {
+  using Shape = GemmShape<kStages, kPStages, kDqPerQuad>;
+  constexpr int kFirstEpiWarp = Shape::kFirstEpiWarp;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -234,6 +250,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* done_bar = d_empty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done_bar + 1);
   volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(tmem_slot + 1);
+  float* s_tok = reinterpret_cast<float*>(bars + 32);  // 4 epilogue warps x kMaxBN multipliers
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -371,11 +388,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int row = q * 32 + lane;
     const uint32_t lane_off = (uint32_t)(q * 32) << 16;
     const int sw = row & 7;
-    uint32_t g = 0;
+    // this warp's stages are g = r, r + kDqPerQuad, ... of the CTA's sequence
+    // (n_kb stages per unit, units blockIdx.x, blockIdx.x + gridDim.x, ...)
+    const int64_t my_units = (p.n_units - blockIdx.x + gridDim.x - 1) / gridDim.x;
+    const uint32_t total = (uint32_t)(my_units * n_kb);
     bool ok = true;
-    for (int64_t u = blockIdx.x; ok && u < p.n_units; u += gridDim.x) {
-      for (int sb = 0; sb < n_kb; ++sb, ++g) {
-        if ((int)(g % kDqPerQuad) != r) continue;
+    for (uint32_t g = (uint32_t)r; ok && g < total; g += kDqPerQuad) {
+      {
         const uint32_t ps = g % kPStages, pph = (g / kPStages) & 1;
         const uint32_t st = g % kStages, ph = (g / kStages) & 1;
         if (!warp_wait(&p_full[ps], pph, wc)) { ok = false; break; }
@@ -427,6 +446,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const int64_t n = (u / p.n_ttiles) * kRows + row;
       const int64_t t0 = (u % p.n_ttiles) * BN;
+      // this unit's token multipliers, once per warp: they are written by the
+      // prep kernel, which may still have been running when this kernel
+      // started, so they are read coherently from L2 (not the read-only path)
+      float* tok = s_tok + (warp - kFirstEpiWarp) * kMaxBN;
+      for (int t = lane; t < BN; t += 32)
+        tok[t] = (t0 + t < p.M) ? __ldcg(p.tok_scale + t0 + t) : 0.0f;
+      __syncwarp();
       for (int c = 0; c < BN; c += 16) {
         uint32_t v[16];
         tmem_ld16(tmem_base + lane_off + buf * BN + c, v);
@@ -434,13 +460,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (n < p.N) {
 #pragma unroll
           for (int t = 0; t < 16; ++t) {
-            const int64_t tok = t0 + c + t;
-            if (tok < p.M) {
-              const float val = __fmul_rn(__uint_as_float(v[t]), __ldg(p.tok_scale + tok));
+            const int64_t tok_i = t0 + c + t;
+            if (tok_i < p.M) {
+              const float val = __fmul_rn(__uint_as_float(v[t]), tok[c + t]);
               if (kOutBf16)
-                reinterpret_cast<__nv_bfloat16*>(p.out)[tok * p.N + n] = __float2bfloat16_rn(val);
+                reinterpret_cast<__nv_bfloat16*>(p.out)[tok_i * p.N + n] = __float2bfloat16_rn(val);
               else
-                reinterpret_cast<float*>(p.out)[tok * p.N + n] = val;
+                reinterpret_cast<float*>(p.out)[tok_i * p.N + n] = val;
             }
           }
         }
@@ -493,9 +519,11 @@ static int lm_head_token_tile(int64_t M) {
   return (int)((M + 15) / 16 * 16);
 }
 
-static size_t gemm_smem_bytes(int BN) {
-  return 1024 + kPStages * (size_t)(kPackedStageBytes + kScaleStageBytes) +
-         kStages * (size_t)BN * kKB * 2 + 256;
+static size_t gemm_smem_bytes(int BN, int stages, int pstages) {
+  // ring buffers, then 256 B of barriers and flags, then the epilogue's
+  // per-warp token multipliers
+  return 1024 + pstages * (size_t)(kPackedStageBytes + kScaleStageBytes) +
+         stages * (size_t)BN * kKB * 2 + 256 + 4 * kMaxBN * sizeof(float);
 }
 
 size_t lm_head_workspace_bytes(int64_t M, int64_t N, int64_t K) {
@@ -512,12 +540,30 @@ static int sm_count() {
   return sms;
 }
 
-template <bool kOutBf16>
-static cudaError_t set_smem_attr() {
-  static cudaError_t err = cudaFuncSetAttribute(w4a16_tc_kernel<kOutBf16>,
-                                                cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                (int)gemm_smem_bytes(kMaxBN));
-  return err;
+// Launch one instantiation (programmatic dependent of the prep kernel).
+template <bool kOutBf16, int kStages, int kPStages, int kDq>
+static cudaError_t launch_gemm(const CUtensorMap& tm_packed, const CUtensorMap& tm_scales,
+                               const CUtensorMap& tm_x, const GemmArgs& a, int grid,
+                               cudaStream_t stream) {
+  auto kern = w4a16_tc_kernel<kOutBf16, kStages, kPStages, kDq>;
+  const size_t smem = gemm_smem_bytes(a.BN, kStages, kPStages);
+  // the 3-stage shape only serves token tiles of up to 64
+  constexpr int kMaxTileBN = kStages >= 3 ? 64 : kMaxBN;
+  static const cudaError_t attr_err = cudaFuncSetAttribute(
+      kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+      (int)gemm_smem_bytes(kMaxTileBN, kStages, kPStages));
+  if (attr_err != cudaSuccess) return attr_err;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(GemmShape<kStages, kPStages, kDq>::kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, tm_packed, tm_scales, tm_x, a);
 }
 
 nvfp4_status lm_head_launch(const void* x, int64_t M, int64_t K, const uint8_t* packed,
@@ -554,32 +600,25 @@ nvfp4_status lm_head_launch(const void* x, int64_t M, int64_t K, const uint8_t* 
   a.BN = BN;
   a.n_ttiles = n_ttiles;
   a.n_units = ((N + kRows - 1) / kRows) * n_ttiles;
-  a.tmem_cols = (2 * BN + kStages * (kKB / 2) <= 256) ? 256u : 512u;
+  // decode-sized token tiles get a third A stage, six packed stages and a
+  // third dequant warp per quadrant; 128-token tiles leave TMEM room for two
+  // A stages only
+  const bool deep = BN <= 64;
+  const int stages = deep ? 3 : 2;
+  a.tmem_cols = (2 * BN + stages * (kKB / 2) <= 256) ? 256u : 512u;
   a.tok_scale = tok_scale;
   a.out = logits;
   a.status = status;
   const int grid = (int)std::min<int64_t>(sms, a.n_units);
-  const size_t smem = gemm_smem_bytes(BN);
   // programmatic dependent launch: the GEMM starts streaming weights while
   // the prep kernel is still running
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)grid);
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
   cudaError_t err;
-  if (out_dtype == NVFP4_OUT_BF16) {
-    if (set_smem_attr<true>() != cudaSuccess) return NVFP4_ERR_CUDA;
-    err = cudaLaunchKernelEx(&cfg, w4a16_tc_kernel<true>, tm_packed, tm_scales, tm_x, a);
-  } else {
-    if (set_smem_attr<false>() != cudaSuccess) return NVFP4_ERR_CUDA;
-    err = cudaLaunchKernelEx(&cfg, w4a16_tc_kernel<false>, tm_packed, tm_scales, tm_x, a);
-  }
+  if (out_dtype == NVFP4_OUT_BF16)
+    err = deep ? launch_gemm<true, 3, 6, 3>(tm_packed, tm_scales, tm_x, a, grid, stream)
+               : launch_gemm<true, 2, 4, 2>(tm_packed, tm_scales, tm_x, a, grid, stream);
+  else
+    err = deep ? launch_gemm<false, 3, 6, 3>(tm_packed, tm_scales, tm_x, a, grid, stream)
+               : launch_gemm<false, 2, 4, 2>(tm_packed, tm_scales, tm_x, a, grid, stream);
   if (err != cudaSuccess || cudaGetLastError() != cudaSuccess) return NVFP4_ERR_CUDA;
   return NVFP4_OK;
 }
