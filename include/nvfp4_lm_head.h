@@ -166,7 +166,7 @@ nvfp4_status w4a16_lm_head(const void *x, int64_t M, int64_t K, const uint8_t *p
 /* ------------------------------------------- allocation-free variant */
 
 /* Size of the fixed device scratch array behind w4a16_lm_head_noalloc. */
-#define NVFP4_NOALLOC_SCRATCH_BYTES (2u << 20)
+#define NVFP4_NOALLOC_SCRATCH_BYTES (8u << 20)
 
 /*
  * The same product as w4a16_lm_head, for callers that cannot allocate device
@@ -177,13 +177,14 @@ nvfp4_status w4a16_lm_head(const void *x, int64_t M, int64_t K, const uint8_t *p
  *
  * Arguments, layouts, ownership and accuracy are those of w4a16_lm_head
  * minus the workspace.  The scratch is one static device array of
- * NVFP4_NOALLOC_SCRATCH_BYTES (2 MiB) that every GPU loading the library
+ * NVFP4_NOALLOC_SCRATCH_BYTES (8 MiB) that every GPU loading the library
  * holds until the process exits.  Its first call on a device looks up the
  * array's device address (cudaGetSymbolAddress) with that device current;
  * make that first call before any stream capture.  Shapes whose rescaled
- * activations do not fit (roughly M_pad * K * 2 bytes, M_pad = M rounded up
- * to 16, or to 128 above 128 tokens) return NVFP4_ERR_SCRATCH_LIMIT before
- * anything is enqueued; for example M <= 64 at K <= 8192 fits.  Nothing is
+ * activations and split-K partials do not fit (M_pad * K * 2 bytes plus up to
+ * SMs * 128 * M_pad * 4 bytes, M_pad = M rounded up to 16, or to 128 above
+ * 128 tokens) return NVFP4_ERR_SCRATCH_LIMIT before anything is enqueued;
+ * for example M <= 64 at K <= 8192 fits.  Nothing is
  * allocated: no cudaMalloc, no cudaFree, no allocating library routine.
  *
  * Every call shares the array.  Each call rewrites what it reads and clears

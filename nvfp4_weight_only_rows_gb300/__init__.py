@@ -214,7 +214,7 @@ def w4a16_lm_head(x: torch.Tensor, packed: torch.Tensor, scales: torch.Tensor,
 
 def w4a16_lm_head_noalloc(x: torch.Tensor, packed: torch.Tensor, scales: torch.Tensor,
                           global_scale: torch.Tensor, out: torch.Tensor, stream=None) -> torch.Tensor:
-    """w4a16_lm_head without a workspace: the library's fixed 2 MiB device scratch is
+    """w4a16_lm_head without a workspace: the library's fixed 8 MiB device scratch is
     used instead (for callers that cannot allocate; see the C header).  `out` must be
     given, so this call allocates nothing."""
     lib = load_library()

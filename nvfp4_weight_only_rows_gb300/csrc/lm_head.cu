@@ -79,10 +79,17 @@ struct GemmArgs {
   int BN;              // token tile, multiple of 16, <= 128
   int n_ttiles;        // token tiles
   int64_t n_units;     // weight tiles x token tiles
+  int n_kb;            // 256-k stages per unit
+  uint32_t n_dp;       // whole units per CTA in strided waves (unit c + j * grid)
+  uint64_t tail_s0;    // first stage of the stream-K tail (unit-major, k-minor)
+  uint64_t tail_len;   // stages in the tail, split evenly over the grid
   uint32_t tmem_cols;  // allocated TMEM columns
   const float* tok_scale;
   void* out;
   int32_t* status;
+  uint32_t* split_cnt;    // [grid][4] arrivals at a split unit, per TMEM lane quadrant
+  uint32_t* split_ready;  // [grid][4] the first arriver's partial is in split_part
+  float* split_part;      // [grid][4][BN][32] fp32 partial accumulators
 };
 
 // ------------------------------------------------------------ activations
@@ -91,11 +98,16 @@ __global__ void __launch_bounds__(256) w4a16_prep_x_kernel(const uint16_t* __res
                                                            const float* __restrict__ global,
                                                            __half* __restrict__ x16,
                                                            float* __restrict__ tok_scale,
-                                                           int32_t* __restrict__ status) {
+                                                           int32_t* __restrict__ status,
+                                                           uint32_t* __restrict__ split_flags,
+                                                           int n_split_flags) {
   // the GEMM may launch now: it waits for this grid's results (griddepcontrol.wait)
   // only where it reads them, and streams the weights meanwhile
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  if (blockIdx.x == 0 && threadIdx.x == 0) *status = NVFP4_OK;  // a fresh call: clear the word
+  if (blockIdx.x == 0) {  // a fresh call: clear the status word and the split-K flags
+    if (threadIdx.x == 0) *status = NVFP4_OK;
+    for (int i = threadIdx.x; i < n_split_flags; i += blockDim.x) split_flags[i] = 0;
+  }
   const int64_t m = blockIdx.x;
   __half* dst = x16 + m * K;
   const int64_t nv = K / 8;
@@ -217,10 +229,62 @@ __device__ __forceinline__ void grid_dependency_wait() {
   asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
+// Poll a global flag (acquire) until it is non-zero, at most the wait limit.
+// The writer is a CTA that has already announced itself, so this is short.
+__device__ __forceinline__ bool spin_until_set(const uint32_t* flag, const WaitCtl& w) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(flag) : "memory");
+  if (v) return __all_sync(0xFFFFFFFFu, true);
+  const uint64_t t0 = globaltimer_ns();
+  bool ok = true;
+  for (uint32_t it = 1;; ++it) {
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(flag) : "memory");
+    if (v) break;
+    if ((it & 63u) == 0 && globaltimer_ns() - t0 > w.limit_ns) {
+      raise_status(w.status, NVFP4_ERR_TIMEOUT);
+      *w.abort = 1;
+      ok = false;
+      break;
+    }
+  }
+  return __all_sync(0xFFFFFFFFu, ok);
+}
+
 // warp-uniform bounded wait: every lane polls, the warp agrees on the outcome
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const WaitCtl& wc) {
   const bool ok = mbar_wait(bar, parity, wc);
   return __all_sync(0xFFFFFFFFu, ok);
+}
+
+// ------------------------------------------------------------ schedule
+// A CTA's work is a list of pieces (a unit, or the part of a unit inside the
+// CTA's tail range): first n_dp whole units in strided waves (so that at any
+// time the CTAs stream neighbouring weight tiles and the same activation
+// stages), then an even share of the remaining units' stages (stream-K).
+// Every role walks the same list.
+struct Piece {
+  uint32_t u, kb0, kb1;
+};
+
+template <typename F>
+__device__ __forceinline__ void for_each_piece(const GemmArgs& p, F&& body) {
+  const uint32_t n_kb = (uint32_t)p.n_kb;
+  for (uint32_t j = 0; j < p.n_dp; ++j)
+    if (!body(Piece{blockIdx.x + j * gridDim.x, 0u, n_kb})) return;
+  const uint64_t t0 = p.tail_s0 + p.tail_len * blockIdx.x / gridDim.x;
+  const uint64_t t1 = p.tail_s0 + p.tail_len * (blockIdx.x + 1) / gridDim.x;
+  for (uint64_t s = t0; s < t1;) {
+    const uint32_t u = (uint32_t)(s / n_kb), kb0 = (uint32_t)(s - (uint64_t)u * n_kb);
+    const uint32_t kb1 = (uint32_t)(((uint64_t)kb0 + (t1 - s) < n_kb) ? kb0 + (t1 - s) : n_kb);
+    s += kb1 - kb0;
+    if (!body(Piece{u, kb0, kb1})) return;
+  }
+}
+
+__device__ __forceinline__ uint32_t cta_stages(const GemmArgs& p) {
+  const uint64_t t0 = p.tail_len * blockIdx.x / gridDim.x;
+  const uint64_t t1 = p.tail_len * (blockIdx.x + 1) / gridDim.x;
+  return (uint32_t)((uint64_t)p.n_dp * p.n_kb + (t1 - t0));
 }
 
 // ------------------------------------------------------------ the GEMM
@@ -289,43 +353,43 @@ __global__ void __launch_bounds__((GemmShape<kStages, kPStages, kDqPerQuad>::kTh
   const uint32_t tmem_a = tmem_base + 2 * BN;  // A ring after the two D buffers
 
   WaitCtl wc{p.status, abort_flag, kWaitLimitNs};
-  const int64_t K = p.K;
-  const int n_kb = (int)(K / kKB);  // stages per unit: one packed stage = one A stage
+  const int n_kb = p.n_kb;  // stages per unit: one packed stage = one A stage
   // the producer and MMA loops below are warp-uniform; one elected lane
   // issues each TMA / tcgen05 instruction
 
   if (warp == 0) {
     // ---------------- packed codes + scales producer
-    const uint64_t pol = policy_evict_first();
+    // a weight tile read once (one token tile) is not kept in L2; one read
+    // by several token tiles in a row is
+    const uint64_t pol = p.n_ttiles == 1 ? policy_evict_first() : policy_evict_last();
     uint32_t issued = 0;
-    bool ok = true;
-    for (int64_t u = blockIdx.x; ok && u < p.n_units; u += gridDim.x) {
-      const int32_t n0 = (int32_t)((u / p.n_ttiles) * kRows);
-      for (int sb = 0; sb < n_kb; ++sb, ++issued) {
+    for_each_piece(p, [&](const Piece& pc) {
+      const int32_t n0 = (int32_t)((pc.u / p.n_ttiles) * kRows);
+      for (uint32_t kb = pc.kb0; kb < pc.kb1; ++kb, ++issued) {
         const uint32_t st = issued % kPStages, ph = (issued / kPStages) & 1;
-        if (!warp_wait(&p_empty[st], ph ^ 1, wc)) { ok = false; break; }
+        if (!warp_wait(&p_empty[st], ph ^ 1, wc)) return false;
         if (elect_one()) {
           mbar_arrive_expect_tx(&p_full[st], kPackedStageBytes + kScaleStageBytes);
-          tma_load_2d_hint(s_packed + st * kPackedStageBytes, &tm_packed, sb * (kKS / 2), n0,
+          tma_load_2d_hint(s_packed + st * kPackedStageBytes, &tm_packed, kb * (kKS / 2), n0,
                            &p_full[st], pol);
-          tma_load_2d_hint(s_scales + st * kScaleStageBytes, &tm_scales, sb * (kKS / 16), n0,
+          tma_load_2d_hint(s_scales + st * kScaleStageBytes, &tm_scales, kb * (kKS / 16), n0,
                            &p_full[st], pol);
         }
         __syncwarp();
       }
-    }
+      return true;
+    });
     drain_loads(p_full, kPStages, issued, 1, p.status);
   } else if (warp == 1) {
     // ---------------- activation producer (four 64-k boxes per stage)
     grid_dependency_wait();  // the rescaled activations come from the prep kernel
     const uint64_t pol = policy_evict_last();
     uint32_t issued = 0;
-    bool ok = true;
-    for (int64_t u = blockIdx.x; ok && u < p.n_units; u += gridDim.x) {
-      const int32_t t0 = (int32_t)((u % p.n_ttiles) * BN);
-      for (int kb = 0; kb < n_kb; ++kb, ++issued) {
+    for_each_piece(p, [&](const Piece& pc) {
+      const int32_t t0 = (int32_t)((pc.u % p.n_ttiles) * BN);
+      for (uint32_t kb = pc.kb0; kb < pc.kb1; ++kb, ++issued) {
         const uint32_t st = issued % kStages, ph = (issued / kStages) & 1;
-        if (!warp_wait(&s_empty[st], ph ^ 1, wc)) { ok = false; break; }
+        if (!warp_wait(&s_empty[st], ph ^ 1, wc)) return false;
         if (elect_one()) {
           mbar_arrive_expect_tx(&s_full[st], x_stage_bytes);
           uint8_t* dst = s_x + st * x_stage_bytes;
@@ -336,24 +400,26 @@ __global__ void __launch_bounds__((GemmShape<kStages, kPStages, kDqPerQuad>::kTh
         }
         __syncwarp();
       }
-    }
+      return true;
+    });
     drain_loads(s_full, kStages, issued, 5, p.status);
   } else if (warp == 2) {
-    // ---------------- MMA issuer (whole warp; one elected lane issues)
+    // ---------------- MMA issuer (whole warp; one elected lane issues).
+    // One accumulator per piece, double buffered.
     const uint32_t idesc = idesc_f16_f32((uint32_t)BN);
     const uint64_t xdesc0 = smem_desc_sw128(smem_u32(s_x));
     const uint32_t box_desc = x_box_bytes >> 4;
     uint32_t g = 0;
-    bool ok = true;
     int64_t i = 0;
-    for (int64_t u = blockIdx.x; ok && u < p.n_units; u += gridDim.x, ++i) {
+    for_each_piece(p, [&](const Piece& pc) {
       const uint32_t buf = (uint32_t)(i & 1), dph = (uint32_t)((i >> 1) & 1);
-      if (!warp_wait(&d_empty[buf], dph ^ 1, wc)) break;
+      ++i;
+      if (!warp_wait(&d_empty[buf], dph ^ 1, wc)) return false;
       tc_fence_after();
       const uint32_t d_tmem = tmem_base + buf * BN;
-      for (int kb = 0; kb < n_kb; ++kb, ++g) {
+      for (uint32_t kb = pc.kb0; kb < pc.kb1; ++kb, ++g) {
         const uint32_t st = g % kStages, ph = (g / kStages) & 1;
-        if (!warp_wait(&s_full[st], ph, wc)) { ok = false; break; }
+        if (!warp_wait(&s_full[st], ph, wc)) return false;
         tc_fence_after();
         const uint64_t bdesc = xdesc0 + ((st * x_stage_bytes) >> 4);
         const uint32_t a_t = tmem_a + st * (kKB / 2);
@@ -361,16 +427,15 @@ __global__ void __launch_bounds__((GemmShape<kStages, kPStages, kDqPerQuad>::kTh
 #pragma unroll
           for (int kk = 0; kk < kKB / 16; ++kk)
             tc_mma_ts(d_tmem, a_t + kk * 8, bdesc + (kk >> 2) * box_desc + 2 * (kk & 3), idesc,
-                      (kb | kk) != 0);
+                      (kb != pc.kb0) || (kk != 0));
           tc_commit(&s_empty[st]);
         }
         __syncwarp();
       }
-      if (ok) {
-        if (elect_one()) tc_commit(&d_full[buf]);
-        __syncwarp();
-      }
-    }
+      if (elect_one()) tc_commit(&d_full[buf]);
+      __syncwarp();
+      return true;
+    });
     // every MMA issued above has completed once done_bar flips
     if (elect_one()) tc_commit(done_bar);
     __syncwarp();
@@ -389,9 +454,7 @@ __global__ void __launch_bounds__((GemmShape<kStages, kPStages, kDqPerQuad>::kTh
     const uint32_t lane_off = (uint32_t)(q * 32) << 16;
     const int sw = row & 7;
     // this warp's stages are g = r, r + kDqPerQuad, ... of the CTA's sequence
-    // (n_kb stages per unit, units blockIdx.x, blockIdx.x + gridDim.x, ...)
-    const int64_t my_units = (p.n_units - blockIdx.x + gridDim.x - 1) / gridDim.x;
-    const uint32_t total = (uint32_t)(my_units * n_kb);
+    const uint32_t total = cta_stages(p);
     bool ok = true;
     for (uint32_t g = (uint32_t)r; ok && g < total; g += kDqPerQuad) {
       {
@@ -435,28 +498,64 @@ __global__ void __launch_bounds__((GemmShape<kStages, kPStages, kDqPerQuad>::kTh
     }
   } else {
     // ---------------- epilogue: one thread per vocabulary row, BN tokens
-    grid_dependency_wait();  // token multipliers come from the prep kernel
+    grid_dependency_wait();  // token multipliers and split flags come from the prep kernel
     const int q = warp & 3;
     const int row = q * 32 + lane;
     const uint32_t lane_off = (uint32_t)(q * 32) << 16;
+    float* tok = s_tok + (warp - kFirstEpiWarp) * kMaxBN;
     int64_t i = 0;
-    for (int64_t u = blockIdx.x; u < p.n_units; u += gridDim.x, ++i) {
+    for_each_piece(p, [&](const Piece& pc) {
+      const uint32_t u = pc.u, kb0 = pc.kb0, kb1 = pc.kb1;
       const uint32_t buf = (uint32_t)(i & 1), dph = (uint32_t)((i >> 1) & 1);
-      if (!warp_wait(&d_full[buf], dph, wc)) break;
+      ++i;
+      if (!warp_wait(&d_full[buf], dph, wc)) return false;
       tc_fence_after();
-      const int64_t n = (u / p.n_ttiles) * kRows + row;
-      const int64_t t0 = (u % p.n_ttiles) * BN;
+      const int64_t n = (int64_t)(u / p.n_ttiles) * kRows + row;
+      const int64_t t0 = (int64_t)(u % p.n_ttiles) * BN;
       // this unit's token multipliers, once per warp: they are written by the
       // prep kernel, which may still have been running when this kernel
       // started, so they are read coherently from L2 (not the read-only path)
-      float* tok = s_tok + (warp - kFirstEpiWarp) * kMaxBN;
       for (int t = lane; t < BN; t += 32)
         tok[t] = (t0 + t < p.M) ? __ldcg(p.tok_scale + t0 + t) : 0.0f;
       __syncwarp();
+      // A tail unit cut by a range boundary: its two CTAs share slot `key`
+      // (the CTA whose tail range starts inside the unit).  The first to get here parks
+      // its fp32 partial; the second adds it to its own and stores logits.
+      // fp32 addition is commutative, so the result does not depend on which
+      // CTA comes second.
+      const bool whole = kb0 == 0 && kb1 == (uint32_t)n_kb;
+      bool finish = true;
+      float* part = nullptr;
+      uint32_t slot = 0;
+      if (!whole) {
+        const uint32_t key = kb0 == 0 ? blockIdx.x + 1 : blockIdx.x;
+        slot = key * 4 + q;
+        part = p.split_part + (size_t)slot * BN * 32;
+        uint32_t first = 0;
+        if (lane == 0) first = atomicAdd(p.split_cnt + slot, 1u) == 0u;
+        finish = __shfl_sync(0xFFFFFFFFu, first, 0) == 0u;
+        if (finish && !spin_until_set(p.split_ready + slot, wc)) finish = false;
+      }
       for (int c = 0; c < BN; c += 16) {
         uint32_t v[16];
         tmem_ld16(tmem_base + lane_off + buf * BN + c, v);
         tc_wait_ld();
+        if (!whole && !finish) {
+          // park this partial: token-major, so a warp's 32 rows are one line
+#pragma unroll
+          for (int t = 0; t < 16; ++t) part[(c + t) * 32 + lane] = __uint_as_float(v[t]);
+          continue;
+        }
+        if (!whole) {
+          // the other CTA's partial for these 16 tokens: all loads first, so
+          // they are in flight together (the logits stores below could alias)
+          float other[16];
+#pragma unroll
+          for (int t = 0; t < 16; ++t) other[t] = __ldcg(part + (c + t) * 32 + lane);
+#pragma unroll
+          for (int t = 0; t < 16; ++t)
+            v[t] = __float_as_uint(__fadd_rn(__uint_as_float(v[t]), other[t]));
+        }
         if (n < p.N) {
 #pragma unroll
           for (int t = 0; t < 16; ++t) {
@@ -471,10 +570,16 @@ __global__ void __launch_bounds__((GemmShape<kStages, kPStages, kDqPerQuad>::kTh
           }
         }
       }
+      if (!whole && !finish) {
+        __threadfence();  // the partial is visible before the flag
+        __syncwarp();
+        if (lane == 0) atomicExch(p.split_ready + slot, 1u);
+      }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&d_empty[buf]);
-    }
+      return true;
+    });
   }
 
   __syncthreads();
@@ -526,18 +631,38 @@ static size_t gemm_smem_bytes(int BN, int stages, int pstages) {
          stages * (size_t)BN * kKB * 2 + 256 + 4 * kMaxBN * sizeof(float);
 }
 
-size_t lm_head_workspace_bytes(int64_t M, int64_t N, int64_t K) {
-  (void)N;
-  const int BN = lm_head_token_tile(M);
-  const int64_t m_pad = (M + BN - 1) / BN * BN;
-  return kWsHeader + align_up((size_t)m_pad * K * 2, 1024) + align_up((size_t)m_pad * 4, 256);
-}
-
 static int sm_count() {
   int dev = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 0;
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
   return sms;
+}
+
+// Workspace layout of one call: [status header][x as fp16, m_pad x K]
+// [token multipliers, m_pad][split counters, grid x 4][split ready flags,
+// grid x 4][split partials, grid x 4 x BN x 32 fp32].
+struct WsLayout {
+  size_t x16, tok, cnt, ready, part, total;
+  int grid;
+};
+
+static WsLayout ws_layout(int64_t M, int64_t N, int64_t K, int sms) {
+  WsLayout l;
+  const int BN = lm_head_token_tile(M);
+  const int64_t m_pad = (M + BN - 1) / BN * BN;
+  const int64_t n_units = ((N + kRows - 1) / kRows) * ((M + BN - 1) / BN);
+  l.grid = (int)std::max<int64_t>(1, std::min<int64_t>(sms, n_units));
+  l.x16 = kWsHeader;
+  l.tok = l.x16 + align_up((size_t)m_pad * K * 2, 1024);
+  l.cnt = l.tok + align_up((size_t)m_pad * 4, 256);
+  l.ready = l.cnt + align_up((size_t)l.grid * 4 * 4, 256);
+  l.part = l.ready + align_up((size_t)l.grid * 4 * 4, 256);
+  l.total = l.part + align_up((size_t)l.grid * 4 * BN * 32 * 4, 256);
+  return l;
+}
+
+size_t lm_head_workspace_bytes(int64_t M, int64_t N, int64_t K) {
+  return ws_layout(M, N, K, std::max(sm_count(), 1)).total;
 }
 
 // Launch one instantiation (programmatic dependent of the prep kernel).
@@ -574,11 +699,14 @@ nvfp4_status lm_head_launch(const void* x, int64_t M, int64_t K, const uint8_t* 
   const int BN = lm_head_token_tile(M);
   const int n_ttiles = (int)((M + BN - 1) / BN);
   const int64_t m_pad = (int64_t)n_ttiles * BN;
+  const WsLayout L = ws_layout(M, N, K, sms);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   int32_t* status = reinterpret_cast<int32_t*>(ws);
-  __half* x16 = reinterpret_cast<__half*>(ws + kWsHeader);
-  float* tok_scale =
-      reinterpret_cast<float*>(ws + kWsHeader + align_up((size_t)m_pad * K * 2, 1024));
+  __half* x16 = reinterpret_cast<__half*>(ws + L.x16);
+  float* tok_scale = reinterpret_cast<float*>(ws + L.tok);
+  uint32_t* split_cnt = reinterpret_cast<uint32_t*>(ws + L.cnt);
+  uint32_t* split_ready = reinterpret_cast<uint32_t*>(ws + L.ready);
+  float* split_part = reinterpret_cast<float*>(ws + L.part);
 
   CUtensorMap tm_packed, tm_scales, tm_x;
   if (!encode_2d(&tm_packed, CU_TENSOR_MAP_DATA_TYPE_UINT8, packed, (uint64_t)K / 2, (uint64_t)N,
@@ -589,8 +717,10 @@ nvfp4_status lm_head_launch(const void* x, int64_t M, int64_t K, const uint8_t* 
                  (uint64_t)K * 2, 64, (uint32_t)BN, CU_TENSOR_MAP_SWIZZLE_128B))
     return NVFP4_ERR_CUDA;
 
-  w4a16_prep_x_kernel<<<(unsigned)m_pad, 256, 0, stream>>>(static_cast<const uint16_t*>(x), M, K,
-                                                            global_scale, x16, tok_scale, status);
+  // the counters and ready flags are adjacent: the prep kernel clears both
+  w4a16_prep_x_kernel<<<(unsigned)m_pad, 256, 0, stream>>>(
+      static_cast<const uint16_t*>(x), M, K, global_scale, x16, tok_scale, status, split_cnt,
+      (int)((L.part - L.cnt) / 4));
   if (cudaGetLastError() != cudaSuccess) return NVFP4_ERR_CUDA;
 
   GemmArgs a;
@@ -600,6 +730,18 @@ nvfp4_status lm_head_launch(const void* x, int64_t M, int64_t K, const uint8_t* 
   a.BN = BN;
   a.n_ttiles = n_ttiles;
   a.n_units = ((N + kRows - 1) / kRows) * n_ttiles;
+  a.n_kb = (int)(K / kKB);
+  // all but the last one to two waves in strided whole units; the rest
+  // stream-K, so every CTA's tail range holds at least one unit's stages
+  // and a unit is cut at most once
+  const int64_t grid_units = L.grid;
+  const int64_t dp_waves = a.n_units >= 2 * grid_units ? a.n_units / grid_units - 1 : 0;
+  a.n_dp = (uint32_t)dp_waves;
+  a.tail_s0 = (uint64_t)(dp_waves * grid_units) * a.n_kb;
+  a.tail_len = (uint64_t)(a.n_units - dp_waves * grid_units) * a.n_kb;
+  a.split_cnt = split_cnt;
+  a.split_ready = split_ready;
+  a.split_part = split_part;
   // decode-sized token tiles get a third A stage, six packed stages and a
   // third dequant warp per quadrant; 128-token tiles leave TMEM room for two
   // A stages only
@@ -609,7 +751,7 @@ nvfp4_status lm_head_launch(const void* x, int64_t M, int64_t K, const uint8_t* 
   a.tok_scale = tok_scale;
   a.out = logits;
   a.status = status;
-  const int grid = (int)std::min<int64_t>(sms, a.n_units);
+  const int grid = L.grid;  // min(SMs, units): every CTA's range spans >= one unit
   // programmatic dependent launch: the GEMM starts streaming weights while
   // the prep kernel is still running
   cudaError_t err;

@@ -8,12 +8,12 @@
 // entry point keeps its scratch in one static device array of this file
 // instead, so the caller passes only inputs and outputs.
 //
-// The array (NVFP4_NOALLOC_SCRATCH_BYTES, 2 MiB) lives in every GPU that
+// The array (NVFP4_NOALLOC_SCRATCH_BYTES, 8 MiB) lives in every GPU that
 // loads the library until the process exits.  All calls share it: the
-// kernels rewrite every byte they read (the rescaled activations, the token
-// multipliers) and the status word is cleared at the start of each call, but
-// two calls that overlap on the GPU (different streams, no ordering between
-// them) race on it.
+// kernels write every byte before they read it (the rescaled activations,
+// the token multipliers, the split-K partials), the status word and the
+// split-K counters are cleared at the start of each call, but two calls that
+// overlap on the GPU (different streams, no ordering between them) race on it.
 #include <cuda_runtime.h>
 
 #include <mutex>

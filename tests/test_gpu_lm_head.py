@@ -167,3 +167,19 @@ def test_sweep_workload_sampled():
         ref_r = oracle.logits(x[rows], p, s, g)
         assert_logits_close(got[rows], ref_r, f"sweep rows M={M}")
         assert_argmax_agrees(got[rows], ref_r)
+
+
+@pytest.mark.parametrize("M,N,K", [(8, 216 * 128, 1024), (1, 153 * 128 + 5, 512),
+                                   (40, 300 * 128, 768)])
+def test_split_units_deterministic(M, N, K):
+    """More weight tiles than SMs and not a multiple of them: the stream-K
+    ranges cut units between CTAs, whose two fp32 partials are added by the
+    CTA that finishes second.  Results match the oracle and repeat bit for bit."""
+    W = synth.quant_weight(N=N, K=K, seed=N % 97)
+    x = synth.decode_x(M, K=K)
+    host_q, dev_q = upload_quantized(W)
+    runs = [run(x, dev_q) for _ in range(3)]
+    assert all(np.array_equal(runs[0], r) for r in runs[1:])
+    cols = np.unique(np.linspace(0, N - 1, 4000).astype(np.int64))
+    ref = oracle.logits(x, *host_q, cols=cols)
+    assert_logits_close(runs[0][:, cols], ref, f"split M={M} N={N} K={K}")
