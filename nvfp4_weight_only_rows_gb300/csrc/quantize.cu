@@ -63,15 +63,13 @@ __global__ void __launch_bounds__(kAmaxThreads) nvfp4_amax_kernel(const uint4* _
   uint32_t m = 0;
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  for (; i + 3 * stride < n_vec; i += 4 * stride) {
-    uint4 a = ld_stream(W + i);
-    uint4 b = ld_stream(W + i + stride);
-    uint4 c = ld_stream(W + i + 2 * stride);
-    uint4 d = ld_stream(W + i + 3 * stride);
-    m = absmax8(a, m);
-    m = absmax8(b, m);
-    m = absmax8(c, m);
-    m = absmax8(d, m);
+  constexpr int kInFlight = 8;  // 128 bytes per thread in flight
+  for (; i + (kInFlight - 1) * stride < n_vec; i += kInFlight * stride) {
+    uint4 v[kInFlight];
+#pragma unroll
+    for (int j = 0; j < kInFlight; ++j) v[j] = ld_stream(W + i + j * stride);
+#pragma unroll
+    for (int j = 0; j < kInFlight; ++j) m = absmax8(v[j], m);
   }
   for (; i < n_vec; i += stride) m = absmax8(ld_stream(W + i), m);
   m = fold_u16x2(m);
@@ -144,6 +142,16 @@ __global__ void __launch_bounds__(kEncodeThreads) nvfp4_encode_kernel(
   if (!(g == g)) return;  // non-finite W: nothing to encode
   const float ig = sg[1];
   const float inv6 = 1.0f / 6.0f;
+  // r = 1 / (f32(scale) * global) for every E4M3 scale code the cast can
+  // produce (0x00..0x7E; satfinite never gives the NaN code 0x7F)
+  __shared__ float r_of_code[128];
+  if (threadIdx.x < 128) {
+    const float sf =
+        __half2float(__half(__nv_cvt_fp8_to_halfraw((__nv_fp8_storage_t)threadIdx.x, __NV_E4M3)));
+    r_of_code[threadIdx.x] =
+        (sf == 0.0f || threadIdx.x == 127) ? 0.0f : __frcp_rn(__fmul_rn(sf, g));
+  }
+  __syncthreads();
 
   // ---- encode: each warp takes whole rows, from the last row backwards
   // (pass 1 left the tail of W in L2); a row is walked in 256-value
@@ -176,8 +184,7 @@ __global__ void __launch_bounds__(kEncodeThreads) nvfp4_encode_kernel(
         float t = __fmul_rn(__fmul_rn(vmax, inv6), ig);
         t = fminf(t, 448.0f);
         const __nv_fp8_storage_t s8 = __nv_cvt_float_to_fp8(t, __NV_SATFINITE, __NV_E4M3);
-        const float sf = __half2float(__half(__nv_cvt_fp8_to_halfraw(s8, __NV_E4M3)));
-        const float r = (sf == 0.0f) ? 0.0f : __frcp_rn(__fmul_rn(sf, g));
+        const float r = r_of_code[s8 & 0x7F];
         float q[8];
         q[0] = __fmul_rn(bf16_lo(v[i].x), r);
         q[1] = __fmul_rn(bf16_hi(v[i].x), r);
