@@ -101,6 +101,10 @@ __global__ void __launch_bounds__(256) w4a16_prep_x_kernel(const uint16_t* __res
                                                            int32_t* __restrict__ status,
                                                            uint32_t* __restrict__ split_flags,
                                                            int n_split_flags) {
+  // launched as a programmatic dependent of whatever ran before it: wait for
+  // that kernel's results before touching memory (the previous call's GEMM
+  // may still be reading this workspace)
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   // the GEMM may launch now: it waits for this grid's results (griddepcontrol.wait)
   // only where it reads them, and streams the weights meanwhile
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -436,6 +440,9 @@ __global__ void __launch_bounds__((GemmShape<kStages, kPStages, kDqPerQuad>::kTh
       __syncwarp();
       return true;
     });
+    // this CTA has issued its last MMA: the next kernel in the stream may be
+    // launched (it waits for this grid's completion before touching memory)
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     // every MMA issued above has completed once done_bar flips
     if (elect_one()) tc_commit(done_bar);
     __syncwarp();
@@ -718,10 +725,21 @@ nvfp4_status lm_head_launch(const void* x, int64_t M, int64_t K, const uint8_t* 
     return NVFP4_ERR_CUDA;
 
   // the counters and ready flags are adjacent: the prep kernel clears both
-  w4a16_prep_x_kernel<<<(unsigned)m_pad, 256, 0, stream>>>(
-      static_cast<const uint16_t*>(x), M, K, global_scale, x16, tok_scale, status, split_cnt,
-      (int)((L.part - L.cnt) / 4));
-  if (cudaGetLastError() != cudaSuccess) return NVFP4_ERR_CUDA;
+  {
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)m_pad);
+    cfg.blockDim = dim3(256);
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, w4a16_prep_x_kernel, static_cast<const uint16_t*>(x), M, K,
+                           global_scale, x16, tok_scale, status, split_cnt,
+                           (int)((L.part - L.cnt) / 4)) != cudaSuccess)
+      return NVFP4_ERR_CUDA;
+  }
 
   GemmArgs a;
   a.M = M;

@@ -59,6 +59,9 @@ __global__ void __launch_bounds__(kAmaxThreads) nvfp4_amax_kernel(const uint4* _
                                                                   int64_t n_vec,
                                                                   uint32_t* __restrict__ partial,
                                                                   int32_t* __restrict__ status) {
+  // launched as a programmatic dependent of whatever ran before it: wait for
+  // that kernel's results before touching memory
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   if (blockIdx.x == 0 && threadIdx.x == 0) *status = NVFP4_OK;  // a fresh call: clear the word
   uint32_t m = 0;
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
@@ -72,6 +75,9 @@ __global__ void __launch_bounds__(kAmaxThreads) nvfp4_amax_kernel(const uint4* _
     for (int j = 0; j < kInFlight; ++j) m = absmax8(v[j], m);
   }
   for (; i < n_vec; i += stride) m = absmax8(ld_stream(W + i), m);
+  // this block's loads are done: the encode kernel may be launched (it waits
+  // for this grid's completion before reading the partials)
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   m = fold_u16x2(m);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
@@ -110,6 +116,7 @@ __global__ void __launch_bounds__(kEncodeThreads) nvfp4_encode_kernel(
     const uint16_t* __restrict__ W, int64_t N, int64_t K, const uint32_t* __restrict__ partial,
     int n_partial, uint32_t* __restrict__ packed, uint8_t* __restrict__ scales,
     float* __restrict__ global_out, int32_t* __restrict__ status) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");  // pass 1 complete and visible
   // ---- amax from the pass-1 partials (every CTA, from L2)
   __shared__ uint32_t red[kEncodeThreads / 32];
   __shared__ float sg[2];
@@ -202,6 +209,7 @@ __global__ void __launch_bounds__(kEncodeThreads) nvfp4_encode_kernel(
       }
     }
   }
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 // ------------------------------------------------------------ host side
@@ -230,18 +238,30 @@ nvfp4_status quantize_launch(const void* W, int64_t N, int64_t K, uint8_t* packe
   int blocks1 = (int)std::min<int64_t>(std::min<int64_t>(want, (int64_t)sms * 8), kMaxAmaxBlocks);
   if (blocks1 < 1) blocks1 = 1;
 
-  nvfp4_amax_kernel<<<blocks1, kAmaxThreads, 0, stream>>>(static_cast<const uint4*>(W), n_vec,
-                                                          partial, status);
-  if (cudaGetLastError() != cudaSuccess) return NVFP4_ERR_CUDA;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(kAmaxThreads);
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cfg.gridDim = dim3((unsigned)blocks1);
+  if (cudaLaunchKernelEx(&cfg, nvfp4_amax_kernel, static_cast<const uint4*>(W), n_vec, partial,
+                         status) != cudaSuccess)
+    return NVFP4_ERR_CUDA;
 
   const int64_t warps_per_block = kEncodeThreads / 32;
   int64_t want2 = (N + warps_per_block - 1) / warps_per_block;
   int blocks2 = (int)std::min<int64_t>(want2, (int64_t)sms * 8);
   if (blocks2 < 1) blocks2 = 1;
-  nvfp4_encode_kernel<<<blocks2, kEncodeThreads, 0, stream>>>(
-      static_cast<const uint16_t*>(W), N, K, partial, blocks1,
-      reinterpret_cast<uint32_t*>(packed), scales, global_scale, status);
-  if (cudaGetLastError() != cudaSuccess) return NVFP4_ERR_CUDA;
+  cfg.gridDim = dim3((unsigned)blocks2);
+  cfg.blockDim = dim3(kEncodeThreads);
+  if (cudaLaunchKernelEx(&cfg, nvfp4_encode_kernel, static_cast<const uint16_t*>(W), N, K,
+                         static_cast<const uint32_t*>(partial), blocks1,
+                         reinterpret_cast<uint32_t*>(packed), scales, global_scale,
+                         status) != cudaSuccess)
+    return NVFP4_ERR_CUDA;
   return NVFP4_OK;
 }
 
