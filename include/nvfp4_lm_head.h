@@ -124,6 +124,18 @@ nvfp4_status nvfp4_refresh(const void *W, int64_t N, int64_t K, uint8_t *packed,
  */
 nvfp4_status nvfp4_read_device_status(const void *workspace, int32_t *status_out, void *stream);
 
+/*
+ * Diagnostic: launch a one-CTA kernel whose pipeline wait can never complete
+ * (an mbarrier phase nobody arrives on, then a flag nobody sets) and that
+ * must give up after `limit_us` microseconds each, raising NVFP4_ERR_TIMEOUT
+ * in the status word of `workspace` (>= 256 bytes, 256-byte aligned; only
+ * its header is used).  It checks that the library's kernels report a stuck
+ * pipeline as a status instead of hanging the GPU; read the result with
+ * nvfp4_read_device_status.  0 < limit_us <= 10^7.
+ */
+nvfp4_status nvfp4_selftest_bounded_wait(void *workspace, size_t workspace_bytes,
+                                         int64_t limit_us, void *stream);
+
 /* --------------------------------------------------------- W4A16 GEMM */
 
 /*

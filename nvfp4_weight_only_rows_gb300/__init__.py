@@ -29,7 +29,7 @@ __all__ = [
     "NVFP4Error", "Status", "library_path", "load_library", "nvfp4_quantize_rows",
     "nvfp4_refresh", "w4a16_lm_head", "nvfp4_quantize_workspace_bytes",
     "w4a16_lm_head_workspace_bytes", "nvfp4_read_device_status", "w4a16_lm_head_noalloc",
-    "OUT_F32", "OUT_BF16",
+    "nvfp4_selftest_bounded_wait", "OUT_F32", "OUT_BF16",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -94,6 +94,8 @@ def load_library() -> ctypes.CDLL:
     lib.w4a16_lm_head.restype = st
     lib.w4a16_lm_head_noalloc.argtypes = [vp, i64, i64, vp, vp, vp, i64, vp, ctypes.c_int, vp]
     lib.w4a16_lm_head_noalloc.restype = st
+    lib.nvfp4_selftest_bounded_wait.argtypes = [vp, sz, i64, vp]
+    lib.nvfp4_selftest_bounded_wait.restype = st
     _lib = lib
     return lib
 
@@ -232,6 +234,13 @@ def w4a16_lm_head_noalloc(x: torch.Tensor, packed: torch.Tensor, scales: torch.T
                                    N, _ptr(out), code, _stream(stream))
     _check(rc, "w4a16_lm_head_noalloc")
     return out
+
+
+def nvfp4_selftest_bounded_wait(workspace: torch.Tensor, limit_us: int, stream=None) -> None:
+    """Run the device self-test of the bounded pipeline waits (see the C header)."""
+    rc = load_library().nvfp4_selftest_bounded_wait(
+        _ptr(workspace), workspace.numel() * workspace.element_size(), limit_us, _stream(stream))
+    _check(rc, "nvfp4_selftest_bounded_wait")
 
 
 def nvfp4_read_device_status(workspace: torch.Tensor, stream=None) -> Status:

@@ -464,44 +464,42 @@ __global__ void __launch_bounds__((GemmShape<kStages, kPStages, kDqPerQuad>::kTh
     const uint32_t total = cta_stages(p);
     bool ok = true;
     for (uint32_t g = (uint32_t)r; ok && g < total; g += kDqPerQuad) {
-      {
-        const uint32_t ps = g % kPStages, pph = (g / kPStages) & 1;
-        const uint32_t st = g % kStages, ph = (g / kStages) & 1;
-        if (!warp_wait(&p_full[ps], pph, wc)) { ok = false; break; }
-        const uint8_t* prow = s_packed + ps * kPackedStageBytes + row * (kKS / 2);
-        const uint4 sc = *reinterpret_cast<const uint4*>(s_scales + ps * kScaleStageBytes +
-                                                         row * (kKS / 16));
-        const uint32_t scw[4] = {sc.x, sc.y, sc.z, sc.w};
-        const uint32_t ta = tmem_a + lane_off + st * (kKB / 2);
+      const uint32_t ps = g % kPStages, pph = (g / kPStages) & 1;
+      const uint32_t st = g % kStages, ph = (g / kStages) & 1;
+      if (!warp_wait(&p_full[ps], pph, wc)) { ok = false; break; }
+      const uint8_t* prow = s_packed + ps * kPackedStageBytes + row * (kKS / 2);
+      const uint4 sc = *reinterpret_cast<const uint4*>(s_scales + ps * kScaleStageBytes +
+                                                       row * (kKS / 16));
+      const uint32_t scw[4] = {sc.x, sc.y, sc.z, sc.w};
+      const uint32_t ta = tmem_a + lane_off + st * (kKB / 2);
 #pragma unroll
-        for (int c4 = 0; c4 < kKB / 64; ++c4) {
-          const uint4 c0 = *reinterpret_cast<const uint4*>(prow + (((2 * c4) ^ sw) << 4));
-          const uint4 c1 = *reinterpret_cast<const uint4*>(prow + (((2 * c4 + 1) ^ sw) << 4));
-          uint32_t s01, s23;
-          scales4_to_f16(scw[c4], s01, s23);
-          const uint32_t f0 = dup_lo(s01), f1 = dup_hi(s01), f2 = dup_lo(s23), f3 = dup_hi(s23);
-          uint32_t v[32];
-          dequant8(c0.x, f0, v + 0);
-          dequant8(c0.y, f0, v + 4);
-          dequant8(c0.z, f1, v + 8);
-          dequant8(c0.w, f1, v + 12);
-          dequant8(c1.x, f2, v + 16);
-          dequant8(c1.y, f2, v + 20);
-          dequant8(c1.z, f3, v + 24);
-          dequant8(c1.w, f3, v + 28);
-          if (c4 == 0 && !warp_wait(&s_empty[st], ph ^ 1, wc)) { ok = false; break; }
-          tmem_st32(ta + c4 * 32, v);
-        }
-        if (!ok) break;
-        // the packed stage has been read; the A stage is complete once the
-        // TMEM stores land
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&p_empty[ps]);
-        tc_wait_st();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&s_full[st]);
+      for (int c4 = 0; c4 < kKB / 64; ++c4) {
+        const uint4 c0 = *reinterpret_cast<const uint4*>(prow + (((2 * c4) ^ sw) << 4));
+        const uint4 c1 = *reinterpret_cast<const uint4*>(prow + (((2 * c4 + 1) ^ sw) << 4));
+        uint32_t s01, s23;
+        scales4_to_f16(scw[c4], s01, s23);
+        const uint32_t f0 = dup_lo(s01), f1 = dup_hi(s01), f2 = dup_lo(s23), f3 = dup_hi(s23);
+        uint32_t v[32];
+        dequant8(c0.x, f0, v + 0);
+        dequant8(c0.y, f0, v + 4);
+        dequant8(c0.z, f1, v + 8);
+        dequant8(c0.w, f1, v + 12);
+        dequant8(c1.x, f2, v + 16);
+        dequant8(c1.y, f2, v + 20);
+        dequant8(c1.z, f3, v + 24);
+        dequant8(c1.w, f3, v + 28);
+        if (c4 == 0 && !warp_wait(&s_empty[st], ph ^ 1, wc)) { ok = false; break; }
+        tmem_st32(ta + c4 * 32, v);
       }
+      if (!ok) break;
+      // the packed stage has been read; the A stage is complete once the
+      // TMEM stores land
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&p_empty[ps]);
+      tc_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s_full[st]);
     }
   } else {
     // ---------------- epilogue: one thread per vocabulary row, BN tokens
