@@ -12,7 +12,9 @@ reads what the previous call left in L2 (every input is larger than L2).
 `value` is the decode-regime HBM throughput (algorithmic bytes of the four
 decode calls / their device time, CUDA events on the launching stream), the
 first clause of the headline metric; the prefill TFLOP/s and quantizer GB/s
-are reported beside it with their own roofline fractions.
+are reported beside it with their own roofline fractions.  The fused greedy
+argmax (each token's largest logit and its row, logits never stored) is
+timed call by call after the steps and reported under "argmax".
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -53,6 +55,11 @@ WORKLOAD = ("Llama-3-8B-shaped lm_head W[128256,4096] bf16 (synthetic N(0,0.02),
 def decode_bytes(M: int, N: int = N_VOCAB, K: int = K_HID) -> int:
     """Algorithmic bytes of one decode call: packed + scales + x + fp32 logits."""
     return N * K // 2 + N * K // 16 + 2 * M * K + 4 * M * N
+
+
+def argmax_bytes(M: int, N: int = N_VOCAB, K: int = K_HID) -> int:
+    """Algorithmic bytes of one fused-argmax call: packed + scales + x + (i64 id, f32 value)."""
+    return N * K // 2 + N * K // 16 + 2 * M * K + 12 * M
 
 
 def quant_bytes(N: int = N_VOCAB, K: int = K_HID) -> int:
@@ -300,16 +307,29 @@ def run_ours(args, world, rank, local):
                                                            workspace=gws))
                  for c in range(2)] for M in DECODE_MS}
 
-    def per_call_us(M, reps=20):
+    def per_call_us(graphs, reps=20):
         evs = []
         for r in range(reps + 3):
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(stream)
-            g_one[M][r % 2].replay()
+            graphs[r % 2].replay()
             e1.record(stream)
             evs.append((e0, e1))
         torch.cuda.synchronize()
         return statistics.median(a.elapsed_time(b) for a, b in evs[3:]) * 1e3
+
+    # the fused greedy argmax (logits never stored), each call alone
+    x_am = dict(x_dec)
+    x_am[PREFILL_M] = x_pre
+    am_ids = {M: torch.empty(M, dtype=torch.int64, device=dev) for M in x_am}
+    am_vals = {M: torch.empty(M, dtype=torch.float32, device=dev) for M in x_am}
+    aws = torch.empty(nv.w4a16_lm_head_argmax_workspace_bytes(PREFILL_M, N, K), dtype=torch.uint8,
+                      device=dev)
+    g_am = {M: [capture(lambda M=M, c=c: nv.w4a16_lm_head_argmax(
+        x_am[M], *copies[c], token_ids=am_ids[M], max_logits=am_vals[M], workspace=aws))
+        for c in range(2)] for M in x_am}
+    g_pre_one = [capture(lambda c=c: nv.w4a16_lm_head(x_pre, *copies[c], out=out_pre,
+                                                      workspace=gws)) for c in range(2)]
 
     for s in range(args.warmup):
         step(s)
@@ -375,7 +395,9 @@ def run_ours(args, world, rank, local):
     traffic = load_traffic()
     quant_gbs = K_steps * quant_bytes() / (t_quant / 1e3) / 1e9
     pre_tflops = K_steps * prefill_flops() / (t_pre / 1e3) / 1e12
-    per_call_dec = {M: per_call_us(M) for M in DECODE_MS}  # us, each call alone
+    per_call_dec = {M: per_call_us(g_one[M]) for M in DECODE_MS}  # us, each call alone
+    per_call_am = {M: per_call_us(g_am[M]) for M in x_am}
+    pre_alone_us = per_call_us(g_pre_one)
 
     def hbm_roof(name, gbs, tkey):
         return {"kernel": name, "bound": "hbm", "achieved": round(gbs, 1),
@@ -397,6 +419,25 @@ def run_ours(args, world, rank, local):
         gbs = decode_bytes(M) / (per_call_dec[M] / 1e6) / 1e9
         roofs[f"decode_M{M}"] = hbm_roof(f"w4a16_lm_head M={M} alone (prep + tcgen05 GEMM)", gbs,
                                          f"decode_M{M}")
+    am_roofs = {}
+    for M in DECODE_MS:
+        gbs = argmax_bytes(M) / (per_call_am[M] / 1e6) / 1e9
+        am_roofs[f"argmax_M{M}"] = hbm_roof(f"w4a16_lm_head_argmax M={M} alone", gbs,
+                                            f"argmax_M{M}")
+    am_tflops = prefill_flops() / (per_call_am[PREFILL_M] / 1e6) / 1e12
+    am_roofs[f"argmax_M{PREFILL_M}"] = {
+        "kernel": f"w4a16_lm_head_argmax M={PREFILL_M} alone", "bound": "tensor",
+        "achieved": round(am_tflops, 1), "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+        "frac": round(am_tflops / peaks["bf16_tflops"], 4), "traffic": traffic.get("argmax_prefill"),
+        "peak_source": peaks["source"] + " dense bf16 burst (fp16 MMA, same rate)"}
+    argmax_part = {
+        "what": "fused greedy argmax (token id + max logit per token, logits not stored); "
+                "each call alone from its own CUDA graph, not part of the timed step",
+        "us_per_call_alone": {str(M): round(per_call_am[M], 2) for M in x_am},
+        "logits_call_us_alone": {**{str(M): round(per_call_dec[M], 2) for M in DECODE_MS},
+                                 str(PREFILL_M) + "_bf16": round(pre_alone_us, 2)},
+        "rooflines": am_roofs,
+    }
     times = {"quantize": t_quant, "prefill": t_pre, "decode": t_dec_all}
     dominant = max(times, key=times.get)
 
@@ -425,6 +466,7 @@ def run_ours(args, world, rank, local):
                 "d2h_bytes_per_step": sum(4 * M * N for M in DECODE_MS),
                 "what": "decode calls through w4a16_lm_head with x copied from pinned host memory "
                         "and logits copied back every call"},
+        "argmax": argmax_part,
         "gpu_launches": launches_per_step * K_steps,
         "clocks": clock_info,
     }
@@ -492,7 +534,8 @@ def run_reference(args, world, rank):
 
 def run_profile_case(case: str):
     """A small, fixed case for ncu: three warm-up calls, then exactly one call
-    of the profiled entry point (decode M=1 / M=64, prefill, or refresh) on
+    of the profiled entry point (decode M=1 / M=64, prefill, refresh, or the
+    fused argmax at M=1 / M=64 / M=2048) on
     the decode-shaped weight; the device holds under 1.5 GB."""
     import nvfp4_weight_only_rows_gb300 as nv
     import synth
@@ -515,6 +558,15 @@ def run_profile_case(case: str):
         return
     del W
     torch.cuda.empty_cache()
+    if case.startswith("argmax"):
+        M = PREFILL_M if case == "argmax_prefill" else int(case.replace("argmax", ""))
+        x = up(synth.prefill_x()) if M == PREFILL_M else up(synth.decode_x(M))
+        aws = torch.empty(nv.w4a16_lm_head_argmax_workspace_bytes(M, N, K), dtype=torch.uint8,
+                          device=dev)
+        for _ in range(4):
+            nv.w4a16_lm_head_argmax(x, packed, scales, g, workspace=aws)
+        torch.cuda.synchronize()
+        return
     if case == "prefill":
         M, x, dt = PREFILL_M, up(synth.prefill_x()), torch.bfloat16
     else:
@@ -535,7 +587,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-budget", type=float, default=15.0,
                     help="seconds of CPU work for the oracle baseline")
-    ap.add_argument("--profile", choices=["decode1", "decode64", "prefill", "quant"],
+    ap.add_argument("--profile", choices=["decode1", "decode64", "prefill", "quant", "argmax1",
+                                          "argmax64", "argmax_prefill"],
                     help="run one small fixed case for ncu instead of the benchmark")
     args = ap.parse_args()
     if args.profile:

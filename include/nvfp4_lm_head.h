@@ -175,6 +175,46 @@ nvfp4_status w4a16_lm_head(const void *x, int64_t M, int64_t K, const uint8_t *p
                            void *logits, int out_dtype, void *workspace, size_t workspace_bytes,
                            void *stream);
 
+/* ------------------------------------------- fused greedy argmax */
+
+/*
+ * Workspace bytes w4a16_lm_head_argmax needs: those of w4a16_lm_head plus
+ * one 64-bit candidate per token (M rounded up to the token tile) and a
+ * counter.  Returns 0 for shapes the call rejects (including N == 0).
+ */
+size_t w4a16_lm_head_argmax_workspace_bytes(int64_t M, int64_t N, int64_t K);
+
+/*
+ * Greedy next-token choice fused into the W4A16 product: for each token m,
+ *   token_ids[m]  = the smallest n with logits[m, n] == max_n' logits[m, n'],
+ *   max_logits[m] = that largest logit,
+ * where logits[m, n] are bit for bit the fp32 values w4a16_lm_head writes
+ * with NVFP4_OUT_F32 for the same inputs.  -0 and +0 count as equal and a
+ * NaN logit as larger than every number (first NaN wins).  The [M, N]
+ * logits are never written to memory: each CTA reduces its tiles in
+ * registers and shared memory and merges one candidate per token with a
+ * 64-bit atomic maximum, so the result does not depend on the schedule.
+ *
+ * The pages define the logits (the lm_head output of
+ * `_LMHeadNvfp4Method.apply`), not what a sampler does with them; this call
+ * is the greedy (temperature 0) reading of "pick the next token".
+ *
+ *   x, packed, scales, global_scale, K
+ *                as for w4a16_lm_head.
+ *   N            vocabulary rows, 1 <= N < 2^31 (N == 0 is NVFP4_ERR_SHAPE).
+ *   M            tokens, M >= 0 (M == 0 is a no-op).
+ *   token_ids    int64 [M], device, 8-byte aligned.
+ *   max_logits   fp32 [M], device, 4-byte aligned, or NULL to skip.
+ *   workspace    device, >= w4a16_lm_head_argmax_workspace_bytes(M, N, K),
+ *                256-byte aligned.
+ * A device-side timeout (NVFP4_ERR_TIMEOUT in the workspace status word)
+ * leaves token_ids and max_logits undefined.
+ */
+nvfp4_status w4a16_lm_head_argmax(const void *x, int64_t M, int64_t K, const uint8_t *packed,
+                                  const uint8_t *scales, const float *global_scale, int64_t N,
+                                  int64_t *token_ids, float *max_logits, void *workspace,
+                                  size_t workspace_bytes, void *stream);
+
 /* ------------------------------------------- allocation-free variant */
 
 /* Size of the fixed device scratch array behind w4a16_lm_head_noalloc. */

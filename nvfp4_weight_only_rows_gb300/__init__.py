@@ -16,6 +16,9 @@ Entry points (same names as the C ABI):
   (``refresh_quantized_lm_heads``); the buffers keep their addresses.
 * ``w4a16_lm_head(x, packed, scales, global_scale)`` -> ``logits[M, N]`` -- the
   weight-only W4A16 product (``_LMHeadNvfp4Method.apply``).
+* ``w4a16_lm_head_argmax(x, packed, scales, global_scale)`` ->
+  ``(token_ids i64[M], max_logits f32[M])`` -- the same product reduced to each
+  token's largest logit inside the kernel (greedy choice; logits never stored).
 """
 from __future__ import annotations
 
@@ -29,7 +32,8 @@ __all__ = [
     "NVFP4Error", "Status", "library_path", "load_library", "nvfp4_quantize_rows",
     "nvfp4_refresh", "w4a16_lm_head", "nvfp4_quantize_workspace_bytes",
     "w4a16_lm_head_workspace_bytes", "nvfp4_read_device_status", "w4a16_lm_head_noalloc",
-    "nvfp4_selftest_bounded_wait", "OUT_F32", "OUT_BF16",
+    "nvfp4_selftest_bounded_wait", "OUT_F32", "OUT_BF16", "w4a16_lm_head_argmax",
+    "w4a16_lm_head_argmax_workspace_bytes",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -92,6 +96,10 @@ def load_library() -> ctypes.CDLL:
     lib.w4a16_lm_head_workspace_bytes.restype = sz
     lib.w4a16_lm_head.argtypes = [vp, i64, i64, vp, vp, vp, i64, vp, ctypes.c_int, vp, sz, vp]
     lib.w4a16_lm_head.restype = st
+    lib.w4a16_lm_head_argmax_workspace_bytes.argtypes = [i64, i64, i64]
+    lib.w4a16_lm_head_argmax_workspace_bytes.restype = sz
+    lib.w4a16_lm_head_argmax.argtypes = [vp, i64, i64, vp, vp, vp, i64, vp, vp, vp, sz, vp]
+    lib.w4a16_lm_head_argmax.restype = st
     lib.w4a16_lm_head_noalloc.argtypes = [vp, i64, i64, vp, vp, vp, i64, vp, ctypes.c_int, vp]
     lib.w4a16_lm_head_noalloc.restype = st
     lib.nvfp4_selftest_bounded_wait.argtypes = [vp, sz, i64, vp]
@@ -212,6 +220,40 @@ def w4a16_lm_head(x: torch.Tensor, packed: torch.Tensor, scales: torch.Tensor,
                            workspace.numel() * workspace.element_size(), _stream(stream))
     _check(rc, "w4a16_lm_head")
     return out
+
+
+def w4a16_lm_head_argmax_workspace_bytes(M: int, N: int, K: int) -> int:
+    return int(load_library().w4a16_lm_head_argmax_workspace_bytes(M, N, K))
+
+
+def w4a16_lm_head_argmax(x: torch.Tensor, packed: torch.Tensor, scales: torch.Tensor,
+                         global_scale: torch.Tensor, token_ids: torch.Tensor | None = None,
+                         max_logits: torch.Tensor | None = None, with_values: bool = True,
+                         workspace: torch.Tensor | None = None, stream=None):
+    """Each token's largest logit and its vocabulary row (smallest row on ties),
+    without writing the logits: returns (token_ids i64[M], max_logits f32[M] or None)."""
+    lib = load_library()
+    _need(x, torch.bfloat16, "x")
+    M, K = x.shape
+    N = packed.shape[0]
+    _need(packed, torch.uint8, "packed", (N, K // 2))
+    _need(scales, scales.dtype, "scales", (N, K // 16))
+    _need(global_scale, torch.float32, "global_scale")
+    if token_ids is None:
+        token_ids = torch.empty(M, dtype=torch.int64, device=x.device)
+    _need(token_ids, torch.int64, "token_ids", (M,))
+    if max_logits is None and with_values:
+        max_logits = torch.empty(M, dtype=torch.float32, device=x.device)
+    if max_logits is not None:
+        _need(max_logits, torch.float32, "max_logits", (M,))
+    need = w4a16_lm_head_argmax_workspace_bytes(M, N, K)
+    if workspace is None:
+        workspace = _workspace(need, x.device)
+    rc = lib.w4a16_lm_head_argmax(_ptr(x), M, K, _ptr(packed), _ptr(scales), _ptr(global_scale),
+                                  N, _ptr(token_ids), _ptr(max_logits), _ptr(workspace),
+                                  workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(rc, "w4a16_lm_head_argmax")
+    return token_ids, max_logits
 
 
 def w4a16_lm_head_noalloc(x: torch.Tensor, packed: torch.Tensor, scales: torch.Tensor,

@@ -12,10 +12,12 @@ size_t quantize_workspace_bytes();
 nvfp4_status quantize_launch(const void* W, int64_t N, int64_t K, uint8_t* packed,
                              uint8_t* scales, float* global_scale, void* workspace,
                              cudaStream_t stream);
-size_t lm_head_workspace_bytes(int64_t M, int64_t N, int64_t K);
+size_t lm_head_workspace_bytes(int64_t M, int64_t N, int64_t K, bool argmax);
 nvfp4_status lm_head_launch(const void* x, int64_t M, int64_t K, const uint8_t* packed,
                             const uint8_t* scales, const float* global_scale, int64_t N,
-                            void* logits, int out_dtype, void* workspace, cudaStream_t stream);
+                            void* logits, int out_mode, int64_t* token_ids, float* max_logits,
+                            void* workspace, cudaStream_t stream);
+constexpr int kOutArgmax = 2;  // lm_head_launch's third output mode
 
 static bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
@@ -107,7 +109,7 @@ nvfp4_status nvfp4_read_device_status(const void* workspace, int32_t* status_out
 
 size_t w4a16_lm_head_workspace_bytes(int64_t M, int64_t N, int64_t K) {
   if (M < 0 || N < 0 || K < 256 || K % 256 != 0) return 0;
-  return lm_head_workspace_bytes(M, N, K);
+  return lm_head_workspace_bytes(M, N, K, false);
 }
 
 nvfp4_status w4a16_lm_head(const void* x, int64_t M, int64_t K, const uint8_t* packed,
@@ -120,15 +122,42 @@ nvfp4_status w4a16_lm_head(const void* x, int64_t M, int64_t K, const uint8_t* p
   if (out_dtype != NVFP4_OUT_F32 && out_dtype != NVFP4_OUT_BF16) return NVFP4_ERR_DTYPE;
   if (M == 0 || N == 0) return NVFP4_OK;  // empty product: nothing to write
   if (!x || !packed || !scales || !global_scale || !logits) return NVFP4_ERR_NULL;
-  if (!workspace || workspace_bytes < lm_head_workspace_bytes(M, N, K))
+  if (!workspace || workspace_bytes < lm_head_workspace_bytes(M, N, K, false))
     return NVFP4_ERR_WORKSPACE;
   if (!aligned(x, 16) || !aligned(packed, 16) || !aligned(scales, 16) ||
       !aligned(global_scale, 4) || !aligned(logits, 16) || !aligned(workspace, 256))
     return NVFP4_ERR_ALIGN;
   nvfp4_status st = check_device();
   if (st != NVFP4_OK) return st;
-  return lm_head_launch(x, M, K, packed, scales, global_scale, N, logits, out_dtype, workspace,
-                        static_cast<cudaStream_t>(stream));
+  return lm_head_launch(x, M, K, packed, scales, global_scale, N, logits, out_dtype, nullptr,
+                        nullptr, workspace, static_cast<cudaStream_t>(stream));
+}
+
+size_t w4a16_lm_head_argmax_workspace_bytes(int64_t M, int64_t N, int64_t K) {
+  if (M < 0 || N <= 0 || K < 256 || K % 256 != 0) return 0;
+  return lm_head_workspace_bytes(M, N, K, true);
+}
+
+nvfp4_status w4a16_lm_head_argmax(const void* x, int64_t M, int64_t K, const uint8_t* packed,
+                                  const uint8_t* scales, const float* global_scale, int64_t N,
+                                  int64_t* token_ids, float* max_logits, void* workspace,
+                                  size_t workspace_bytes, void* stream) {
+  // N <= 0: the maximum over no logits does not exist
+  if (M < 0 || N <= 0 || K < 256 || K % 256 != 0 || M >= kMaxDim || N >= kMaxDim ||
+      K >= kMaxDim)
+    return NVFP4_ERR_SHAPE;
+  if (M == 0) return NVFP4_OK;
+  if (!x || !packed || !scales || !global_scale || !token_ids) return NVFP4_ERR_NULL;
+  if (!workspace || workspace_bytes < lm_head_workspace_bytes(M, N, K, true))
+    return NVFP4_ERR_WORKSPACE;
+  if (!aligned(x, 16) || !aligned(packed, 16) || !aligned(scales, 16) ||
+      !aligned(global_scale, 4) || !aligned(token_ids, 8) || !aligned(max_logits, 4) ||
+      !aligned(workspace, 256))
+    return NVFP4_ERR_ALIGN;
+  nvfp4_status st = check_device();
+  if (st != NVFP4_OK) return st;
+  return lm_head_launch(x, M, K, packed, scales, global_scale, N, nullptr, kOutArgmax, token_ids,
+                        max_logits, workspace, static_cast<cudaStream_t>(stream));
 }
 
 }  // extern "C"

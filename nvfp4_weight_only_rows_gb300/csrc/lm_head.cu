@@ -72,6 +72,7 @@ struct GemmShape {
 constexpr uint32_t kPackedStageBytes = kRows * (kKS / 2);   // 16384
 constexpr uint32_t kScaleStageBytes = kRows * (kKS / 16);   // 2048
 constexpr int kMaxBN = 128;
+constexpr int kOutArgmax = 2;                               // third output mode (after f32, bf16)
 constexpr uint64_t kWaitLimitNs = 2000000000ull;            // 2 s per pipeline wait
 
 struct GemmArgs {
@@ -90,6 +91,11 @@ struct GemmArgs {
   uint32_t* split_cnt;    // [grid][4] arrivals at a split unit, per TMEM lane quadrant
   uint32_t* split_ready;  // [grid][4] the first arriver's partial is in split_part
   float* split_part;      // [grid][4][BN][32] fp32 partial accumulators
+  // greedy argmax output mode only
+  unsigned long long* am_keys;  // [m_pad] running (order key << 32 | ~n) maxima, zeroed per call
+  uint32_t* am_done;            // CTAs that have merged their keys, zeroed per call
+  int64_t* am_idx;              // [M] result: vocabulary row of the largest logit
+  float* am_val;                // [M] result: that logit (may be null)
 };
 
 // ------------------------------------------------------------ activations
@@ -260,6 +266,36 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const 
   return __all_sync(0xFFFFFFFFu, ok);
 }
 
+// ------------------------------------------------------------ greedy argmax
+// A logit's 32-bit order key: unsigned order of the keys is the order of the
+// values, -0 and +0 share one key, every NaN is above +Inf, and no value
+// maps to 0 (which therefore means "no candidate").  A candidate is the
+// 64-bit word key << 32 | ~n: the larger word has the larger logit, and of
+// equal logits the smaller vocabulary row.
+__device__ __forceinline__ uint32_t order_key(float v) {
+  if (v != v) return 0xFFFFFFFFu;
+  uint32_t b = __float_as_uint(v);
+  if (b == 0x80000000u) b = 0u;
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+
+__device__ __forceinline__ float key_value(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
+
+// Merge a warp's running candidates for the tokens tok0 .. tok0+BN-1 into
+// the global maxima (one 64-bit atomic max per token) and clear them.
+__device__ __forceinline__ void argmax_flush(unsigned long long* best, unsigned long long* keys,
+                                             int64_t tok0, int64_t M, int BN, int lane) {
+  __syncwarp();
+  for (int t = lane; t < BN; t += 32) {
+    const unsigned long long k = best[t];
+    if (k != 0ull && tok0 + t < M) atomicMax(keys + tok0 + t, k);
+    best[t] = 0ull;
+  }
+  __syncwarp();
+}
+
 // ------------------------------------------------------------ schedule
 // A CTA's work is a list of pieces (a unit, or the part of a unit inside the
 // CTA's tail range): first n_dp whole units in strided waves (so that at any
@@ -292,7 +328,9 @@ __device__ __forceinline__ uint32_t cta_stages(const GemmArgs& p) {
 }
 
 // ------------------------------------------------------------ the GEMM
-template <bool kOutBf16, int kStages, int kPStages, int kDqPerQuad>
+// kOut: NVFP4_OUT_F32 / NVFP4_OUT_BF16 store the logits; kOutArgmax keeps
+// only each token's largest logit and its vocabulary row.
+template <int kOut, int kStages, int kPStages, int kDqPerQuad>
 __global__ void __launch_bounds__((GemmShape<kStages, kPStages, kDqPerQuad>::kThreads), 1)
     w4a16_tc_kernel(const __grid_constant__ CUtensorMap tm_packed,
                     const __grid_constant__ CUtensorMap tm_scales,
@@ -319,6 +357,11 @@ __global__ void __launch_bounds__((GemmShape<kStages, kPStages, kDqPerQuad>::kTh
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done_bar + 1);
   volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(tmem_slot + 1);
   float* s_tok = reinterpret_cast<float*>(bars + 32);  // 4 epilogue warps x kMaxBN multipliers
+  // argmax mode: 4 epilogue warps x kMaxBN running candidates, the token tile
+  // each warp's candidates belong to, and the "last CTA" flag
+  unsigned long long* s_best = reinterpret_cast<unsigned long long*>(s_tok + 4 * kMaxBN);
+  int32_t* s_tt = reinterpret_cast<int32_t*>(s_best + 4 * kMaxBN);
+  int32_t* s_last = s_tt + 4;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -508,6 +551,12 @@ __global__ void __launch_bounds__((GemmShape<kStages, kPStages, kDqPerQuad>::kTh
     const int row = q * 32 + lane;
     const uint32_t lane_off = (uint32_t)(q * 32) << 16;
     float* tok = s_tok + (warp - kFirstEpiWarp) * kMaxBN;
+    unsigned long long* best = s_best + (warp - kFirstEpiWarp) * kMaxBN;
+    int cur_tt = -1;  // argmax mode: the token tile `best` belongs to
+    if (kOut == kOutArgmax) {
+      for (int t = lane; t < kMaxBN; t += 32) best[t] = 0ull;
+      __syncwarp();
+    }
     int64_t i = 0;
     for_each_piece(p, [&](const Piece& pc) {
       const uint32_t u = pc.u, kb0 = pc.kb0, kb1 = pc.kb1;
@@ -517,6 +566,11 @@ __global__ void __launch_bounds__((GemmShape<kStages, kPStages, kDqPerQuad>::kTh
       tc_fence_after();
       const int64_t n = (int64_t)(u / p.n_ttiles) * kRows + row;
       const int64_t t0 = (int64_t)(u % p.n_ttiles) * BN;
+      if (kOut == kOutArgmax && (int)(u % p.n_ttiles) != cur_tt) {
+        // a new token tile: hand the finished tile's candidates to the global maxima
+        if (cur_tt >= 0) argmax_flush(best, p.am_keys, (int64_t)cur_tt * BN, p.M, BN, lane);
+        cur_tt = (int)(u % p.n_ttiles);
+      }
       // this unit's token multipliers, once per warp: they are written by the
       // prep kernel, which may still have been running when this kernel
       // started, so they are read coherently from L2 (not the read-only path)
@@ -561,13 +615,33 @@ __global__ void __launch_bounds__((GemmShape<kStages, kPStages, kDqPerQuad>::kTh
           for (int t = 0; t < 16; ++t)
             v[t] = __float_as_uint(__fadd_rn(__uint_as_float(v[t]), other[t]));
         }
-        if (n < p.N) {
+        if (kOut == kOutArgmax) {
+          // per token: the warp's largest key over its 32 rows, and the
+          // lowest lane holding it; lane t keeps token c + t's result
+          uint32_t my_m = 0, my_bal = 0;
+#pragma unroll
+          for (int t = 0; t < 16; ++t) {
+            const float val = __fmul_rn(__uint_as_float(v[t]), tok[c + t]);
+            const uint32_t k32 = n < p.N ? order_key(val) : 0u;
+            const uint32_t m = __reduce_max_sync(0xFFFFFFFFu, k32);
+            const uint32_t bal = __ballot_sync(0xFFFFFFFFu, k32 == m);
+            if (lane == t) {
+              my_m = m;
+              my_bal = bal;
+            }
+          }
+          if (lane < 16 && my_m != 0u && t0 + c + lane < p.M) {
+            const uint32_t nb = (uint32_t)(n - lane) + (uint32_t)(__ffs(my_bal) - 1);
+            const unsigned long long key = ((unsigned long long)my_m << 32) | (uint32_t)~nb;
+            if (key > best[c + lane]) best[c + lane] = key;
+          }
+        } else if (n < p.N) {
 #pragma unroll
           for (int t = 0; t < 16; ++t) {
             const int64_t tok_i = t0 + c + t;
             if (tok_i < p.M) {
               const float val = __fmul_rn(__uint_as_float(v[t]), tok[c + t]);
-              if (kOutBf16)
+              if (kOut == NVFP4_OUT_BF16)
                 reinterpret_cast<__nv_bfloat16*>(p.out)[tok_i * p.N + n] = __float2bfloat16_rn(val);
               else
                 reinterpret_cast<float*>(p.out)[tok_i * p.N + n] = val;
@@ -585,12 +659,51 @@ __global__ void __launch_bounds__((GemmShape<kStages, kPStages, kDqPerQuad>::kTh
       if (lane == 0) mbar_arrive(&d_empty[buf]);
       return true;
     });
+    if (kOut == kOutArgmax) {
+      __syncwarp();
+      if (lane == 0) s_tt[warp - kFirstEpiWarp] = cur_tt;
+    }
   }
 
   __syncthreads();
   if (warp == 2) {
     tc_fence_after();
     tmem_dealloc(tmem_base, p.tmem_cols);
+  }
+  if constexpr (kOut == kOutArgmax) {
+    // Merge the four epilogue warps' candidates (one atomic max per token),
+    // then the last CTA to finish turns the maxima into rows and values.
+    const int e = threadIdx.x - 32 * kFirstEpiWarp;
+    if (e >= 0 && e < BN) {
+      const int tt0 = s_tt[0];
+      unsigned long long k = 0ull;
+#pragma unroll
+      for (int w = 0; w < 4; ++w) {
+        const int ttw = s_tt[w];
+        const unsigned long long kw = s_best[w * kMaxBN + e];
+        if (ttw < 0 || kw == 0ull) continue;
+        if (ttw == tt0) {
+          k = kw > k ? kw : k;
+        } else if ((int64_t)ttw * BN + e < p.M) {
+          atomicMax(p.am_keys + (int64_t)ttw * BN + e, kw);
+        }
+      }
+      if (k != 0ull && tt0 >= 0 && (int64_t)tt0 * BN + e < p.M)
+        atomicMax(p.am_keys + (int64_t)tt0 * BN + e, k);
+    }
+    __threadfence();
+    __syncthreads();
+    if (e == 0) *s_last = atomicAdd(p.am_done, 1u) == gridDim.x - 1 ? 1 : 0;
+    __syncthreads();
+    if (*s_last) {
+      __threadfence();
+      for (int64_t t = threadIdx.x; t < p.M; t += blockDim.x) {
+        const unsigned long long k = __ldcg(p.am_keys + t);
+        const uint32_t k32 = (uint32_t)(k >> 32);
+        p.am_idx[t] = k32 ? (int64_t)(uint32_t)~(uint32_t)k : (int64_t)-1;
+        if (p.am_val) p.am_val[t] = key_value(k32);
+      }
+    }
   }
 }
 
@@ -629,11 +742,13 @@ static int lm_head_token_tile(int64_t M) {
   return (int)((M + 15) / 16 * 16);
 }
 
-static size_t gemm_smem_bytes(int BN, int stages, int pstages) {
+static size_t gemm_smem_bytes(int BN, int stages, int pstages, bool argmax) {
   // ring buffers, then 256 B of barriers and flags, then the epilogue's
-  // per-warp token multipliers
+  // per-warp token multipliers (and, for argmax, per-warp candidates, their
+  // token tiles and a flag)
   return 1024 + pstages * (size_t)(kPackedStageBytes + kScaleStageBytes) +
-         stages * (size_t)BN * kKB * 2 + 256 + 4 * kMaxBN * sizeof(float);
+         stages * (size_t)BN * kKB * 2 + 256 + 4 * kMaxBN * sizeof(float) +
+         (argmax ? 4 * kMaxBN * sizeof(unsigned long long) + 64 : 0);
 }
 
 static int sm_count() {
@@ -645,13 +760,15 @@ static int sm_count() {
 
 // Workspace layout of one call: [status header][x as fp16, m_pad x K]
 // [token multipliers, m_pad][split counters, grid x 4][split ready flags,
-// grid x 4][split partials, grid x 4 x BN x 32 fp32].
+// grid x 4] and, for argmax only, [CTAs done, 1][candidate maxima, m_pad
+// x 64 bit]; then [split partials, grid x 4 x BN x 32 fp32].  Everything
+// from the split counters up to the partials is zeroed by the prep kernel.
 struct WsLayout {
-  size_t x16, tok, cnt, ready, part, total;
+  size_t x16, tok, cnt, ready, done, keys, part, total;
   int grid;
 };
 
-static WsLayout ws_layout(int64_t M, int64_t N, int64_t K, int sms) {
+static WsLayout ws_layout(int64_t M, int64_t N, int64_t K, int sms, bool argmax) {
   WsLayout l;
   const int BN = lm_head_token_tile(M);
   const int64_t m_pad = (M + BN - 1) / BN * BN;
@@ -661,27 +778,30 @@ static WsLayout ws_layout(int64_t M, int64_t N, int64_t K, int sms) {
   l.tok = l.x16 + align_up((size_t)m_pad * K * 2, 1024);
   l.cnt = l.tok + align_up((size_t)m_pad * 4, 256);
   l.ready = l.cnt + align_up((size_t)l.grid * 4 * 4, 256);
-  l.part = l.ready + align_up((size_t)l.grid * 4 * 4, 256);
+  l.done = l.ready + align_up((size_t)l.grid * 4 * 4, 256);
+  l.keys = l.done + (argmax ? 256 : 0);
+  l.part = l.keys + (argmax ? align_up((size_t)m_pad * 8, 256) : 0);
   l.total = l.part + align_up((size_t)l.grid * 4 * BN * 32 * 4, 256);
   return l;
 }
 
-size_t lm_head_workspace_bytes(int64_t M, int64_t N, int64_t K) {
-  return ws_layout(M, N, K, std::max(sm_count(), 1)).total;
+size_t lm_head_workspace_bytes(int64_t M, int64_t N, int64_t K, bool argmax) {
+  return ws_layout(M, N, K, std::max(sm_count(), 1), argmax).total;
 }
 
 // Launch one instantiation (programmatic dependent of the prep kernel).
-template <bool kOutBf16, int kStages, int kPStages, int kDq>
+template <int kOut, int kStages, int kPStages, int kDq>
 static cudaError_t launch_gemm(const CUtensorMap& tm_packed, const CUtensorMap& tm_scales,
                                const CUtensorMap& tm_x, const GemmArgs& a, int grid,
                                cudaStream_t stream) {
-  auto kern = w4a16_tc_kernel<kOutBf16, kStages, kPStages, kDq>;
-  const size_t smem = gemm_smem_bytes(a.BN, kStages, kPStages);
+  auto kern = w4a16_tc_kernel<kOut, kStages, kPStages, kDq>;
+  constexpr bool kArgmax = kOut == kOutArgmax;
+  const size_t smem = gemm_smem_bytes(a.BN, kStages, kPStages, kArgmax);
   // the 3-stage shape only serves token tiles of up to 64
   constexpr int kMaxTileBN = kStages >= 3 ? 64 : kMaxBN;
   static const cudaError_t attr_err = cudaFuncSetAttribute(
       kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-      (int)gemm_smem_bytes(kMaxTileBN, kStages, kPStages));
+      (int)gemm_smem_bytes(kMaxTileBN, kStages, kPStages, kArgmax));
   if (attr_err != cudaSuccess) return attr_err;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)grid);
@@ -696,15 +816,19 @@ static cudaError_t launch_gemm(const CUtensorMap& tm_packed, const CUtensorMap& 
   return cudaLaunchKernelEx(&cfg, kern, tm_packed, tm_scales, tm_x, a);
 }
 
+// out_mode: NVFP4_OUT_F32 / NVFP4_OUT_BF16 write logits[M, N] to `logits`;
+// kOutArgmax writes token_ids[M] (and max_logits[M] unless null) instead.
 nvfp4_status lm_head_launch(const void* x, int64_t M, int64_t K, const uint8_t* packed,
                             const uint8_t* scales, const float* global_scale, int64_t N,
-                            void* logits, int out_dtype, void* workspace, cudaStream_t stream) {
+                            void* logits, int out_mode, int64_t* token_ids, float* max_logits,
+                            void* workspace, cudaStream_t stream) {
   const int sms = sm_count();
   if (sms <= 0) return NVFP4_ERR_CUDA;
+  const bool argmax = out_mode == kOutArgmax;
   const int BN = lm_head_token_tile(M);
   const int n_ttiles = (int)((M + BN - 1) / BN);
   const int64_t m_pad = (int64_t)n_ttiles * BN;
-  const WsLayout L = ws_layout(M, N, K, sms);
+  const WsLayout L = ws_layout(M, N, K, sms, argmax);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   int32_t* status = reinterpret_cast<int32_t*>(ws);
   __half* x16 = reinterpret_cast<__half*>(ws + L.x16);
@@ -722,7 +846,8 @@ nvfp4_status lm_head_launch(const void* x, int64_t M, int64_t K, const uint8_t* 
                  (uint64_t)K * 2, 64, (uint32_t)BN, CU_TENSOR_MAP_SWIZZLE_128B))
     return NVFP4_ERR_CUDA;
 
-  // the counters and ready flags are adjacent: the prep kernel clears both
+  // the counters, ready flags and argmax maxima are adjacent: the prep
+  // kernel clears them all
   {
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -758,6 +883,10 @@ nvfp4_status lm_head_launch(const void* x, int64_t M, int64_t K, const uint8_t* 
   a.split_cnt = split_cnt;
   a.split_ready = split_ready;
   a.split_part = split_part;
+  a.am_keys = argmax ? reinterpret_cast<unsigned long long*>(ws + L.keys) : nullptr;
+  a.am_done = argmax ? reinterpret_cast<uint32_t*>(ws + L.done) : nullptr;
+  a.am_idx = token_ids;
+  a.am_val = max_logits;
   // decode-sized token tiles get a third A stage, six packed stages and a
   // third dequant warp per quadrant; 128-token tiles leave TMEM room for two
   // A stages only
@@ -771,12 +900,15 @@ nvfp4_status lm_head_launch(const void* x, int64_t M, int64_t K, const uint8_t* 
   // programmatic dependent launch: the GEMM starts streaming weights while
   // the prep kernel is still running
   cudaError_t err;
-  if (out_dtype == NVFP4_OUT_BF16)
-    err = deep ? launch_gemm<true, 3, 6, 3>(tm_packed, tm_scales, tm_x, a, grid, stream)
-               : launch_gemm<true, 2, 4, 2>(tm_packed, tm_scales, tm_x, a, grid, stream);
+  if (argmax)
+    err = deep ? launch_gemm<kOutArgmax, 3, 6, 3>(tm_packed, tm_scales, tm_x, a, grid, stream)
+               : launch_gemm<kOutArgmax, 2, 4, 2>(tm_packed, tm_scales, tm_x, a, grid, stream);
+  else if (out_mode == NVFP4_OUT_BF16)
+    err = deep ? launch_gemm<NVFP4_OUT_BF16, 3, 6, 3>(tm_packed, tm_scales, tm_x, a, grid, stream)
+               : launch_gemm<NVFP4_OUT_BF16, 2, 4, 2>(tm_packed, tm_scales, tm_x, a, grid, stream);
   else
-    err = deep ? launch_gemm<false, 3, 6, 3>(tm_packed, tm_scales, tm_x, a, grid, stream)
-               : launch_gemm<false, 2, 4, 2>(tm_packed, tm_scales, tm_x, a, grid, stream);
+    err = deep ? launch_gemm<NVFP4_OUT_F32, 3, 6, 3>(tm_packed, tm_scales, tm_x, a, grid, stream)
+               : launch_gemm<NVFP4_OUT_F32, 2, 4, 2>(tm_packed, tm_scales, tm_x, a, grid, stream);
   if (err != cudaSuccess || cudaGetLastError() != cudaSuccess) return NVFP4_ERR_CUDA;
   return NVFP4_OK;
 }

@@ -21,10 +21,7 @@
 #include "common.cuh"
 
 namespace nvfp4 {
-size_t lm_head_workspace_bytes(int64_t M, int64_t N, int64_t K);
-nvfp4_status lm_head_launch(const void* x, int64_t M, int64_t K, const uint8_t* packed,
-                            const uint8_t* scales, const float* global_scale, int64_t N,
-                            void* logits, int out_dtype, void* workspace, cudaStream_t stream);
+size_t lm_head_workspace_bytes(int64_t M, int64_t N, int64_t K, bool argmax);
 
 // The fixed scratch.  In host code `g_noalloc_scratch` is only a host-side
 // stand-in for the symbol; its device address comes from
@@ -61,7 +58,7 @@ extern "C" nvfp4_status w4a16_lm_head_noalloc(const void* x, int64_t M, int64_t 
   if (out_dtype != NVFP4_OUT_F32 && out_dtype != NVFP4_OUT_BF16) return NVFP4_ERR_DTYPE;
   if (M == 0 || N == 0) return NVFP4_OK;
   // M * K decides the scratch: reject what the fixed array cannot hold
-  if (lm_head_workspace_bytes(M, N, K) > NVFP4_NOALLOC_SCRATCH_BYTES)
+  if (lm_head_workspace_bytes(M, N, K, false) > NVFP4_NOALLOC_SCRATCH_BYTES)
     return NVFP4_ERR_SCRATCH_LIMIT;
   void* scratch = nullptr;
   nvfp4_status st = scratch_for_current_device(&scratch);

@@ -32,7 +32,8 @@ def test_header_declares_the_boundary():
     names = declared_functions()
     for n in ("nvfp4_quantize_rows", "nvfp4_refresh", "w4a16_lm_head",
               "nvfp4_quantize_workspace_bytes", "w4a16_lm_head_workspace_bytes",
-              "nvfp4_status_string", "nvfp4_read_device_status", "nvfp4_abi_version"):
+              "nvfp4_status_string", "nvfp4_read_device_status", "nvfp4_abi_version",
+              "w4a16_lm_head_argmax", "w4a16_lm_head_argmax_workspace_bytes"):
         assert n in names
 
 
@@ -82,3 +83,22 @@ def test_host_argument_errors_before_any_cuda_call(lib):
     assert g(fake, 4, 256, fake, fake, fake, 8, fake, 0, fake, 64, None) == 4        # WORKSPACE
     assert g(vp((1 << 20) + 2), 4, 256, fake, fake, fake, 8, fake, 0, fake, 1 << 30,
              None) == 2                                                              # ALIGN
+    a = lib.w4a16_lm_head_argmax
+    ids, vals = vp(1 << 20), vp(1 << 21)
+    assert a(fake, 4, 256, fake, fake, fake, 0, ids, vals, fake, 1 << 30, None) == 1   # N == 0
+    assert a(fake, 4, 300, fake, fake, fake, 8, ids, vals, fake, 1 << 30, None) == 1   # K % 256
+    assert a(fake, 0, 256, fake, fake, fake, 8, ids, vals, None, 0, None) == 0         # empty
+    assert a(fake, 4, 256, fake, fake, fake, 8, None, vals, fake, 1 << 30, None) == 3  # NULL ids
+    assert a(fake, 4, 256, fake, fake, fake, 8, ids, vals, fake, 64, None) == 4        # WORKSPACE
+    assert a(fake, 4, 256, fake, fake, fake, 8, vp((1 << 20) + 4), vals, fake, 1 << 30,
+             None) == 2                                                              # ALIGN ids
+    assert a(fake, 4, 256, fake, fake, fake, 8, ids, vp((1 << 21) + 2), fake, 1 << 30,
+             None) == 2                                                              # ALIGN vals
+
+
+def test_argmax_workspace_sizes(lib):
+    assert lib.w4a16_lm_head_argmax_workspace_bytes(4, 0, 256) == 0
+    for M in (1, 64, 200, 2048):
+        plain = lib.w4a16_lm_head_workspace_bytes(M, 128256, 4096)
+        am = lib.w4a16_lm_head_argmax_workspace_bytes(M, 128256, 4096)
+        assert am >= plain + 8 * M
