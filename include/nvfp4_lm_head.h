@@ -179,8 +179,9 @@ nvfp4_status w4a16_lm_head(const void *x, int64_t M, int64_t K, const uint8_t *p
 
 /*
  * Workspace bytes w4a16_lm_head_argmax needs: those of w4a16_lm_head plus
- * one 64-bit candidate per token (M rounded up to the token tile) and a
- * counter.  Returns 0 for shapes the call rejects (including N == 0).
+ * 128 bytes per token (one 64-bit maximum per line, M rounded up to the
+ * token tile) and a counter.  Returns 0 for shapes the call rejects
+ * (including N == 0).
  */
 size_t w4a16_lm_head_argmax_workspace_bytes(int64_t M, int64_t N, int64_t K);
 
@@ -189,11 +190,12 @@ size_t w4a16_lm_head_argmax_workspace_bytes(int64_t M, int64_t N, int64_t K);
  *   token_ids[m]  = the smallest n with logits[m, n] == max_n' logits[m, n'],
  *   max_logits[m] = that largest logit,
  * where logits[m, n] are bit for bit the fp32 values w4a16_lm_head writes
- * with NVFP4_OUT_F32 for the same inputs.  -0 and +0 count as equal and a
- * NaN logit as larger than every number (first NaN wins).  The [M, N]
- * logits are never written to memory: each CTA reduces its tiles in
- * registers and shared memory and merges one candidate per token with a
- * 64-bit atomic maximum, so the result does not depend on the schedule.
+ * with NVFP4_OUT_F32 for the same inputs.  -0 and +0 count as equal (a zero
+ * maximum is returned as +0) and a NaN logit as larger than every number
+ * (first NaN wins).  The [M, N] logits are never written to memory: each
+ * warp compares its logits with the token's current maximum and, where one
+ * may reach it, merges its best (logit, row) with one 64-bit atomic
+ * maximum, so the result does not depend on the schedule.
  *
  * The pages define the logits (the lm_head output of
  * `_LMHeadNvfp4Method.apply`), not what a sampler does with them; this call

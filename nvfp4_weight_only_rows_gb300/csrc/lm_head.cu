@@ -73,6 +73,7 @@ constexpr uint32_t kPackedStageBytes = kRows * (kKS / 2);   // 16384
 constexpr uint32_t kScaleStageBytes = kRows * (kKS / 16);   // 2048
 constexpr int kMaxBN = 128;
 constexpr int kOutArgmax = 2;                               // third output mode (after f32, bf16)
+constexpr int kKeyStride = 16;  // argmax: one 64-bit candidate per 128-byte line (spreads the atomics)
 constexpr uint64_t kWaitLimitNs = 2000000000ull;            // 2 s per pipeline wait
 
 struct GemmArgs {
@@ -92,8 +93,9 @@ struct GemmArgs {
   uint32_t* split_ready;  // [grid][4] the first arriver's partial is in split_part
   float* split_part;      // [grid][4][BN][32] fp32 partial accumulators
   // greedy argmax output mode only
-  unsigned long long* am_keys;  // [m_pad] running (order key << 32 | ~n) maxima, zeroed per call
-  uint32_t* am_done;            // CTAs that have merged their keys, zeroed per call
+  unsigned long long* am_keys;  // [m_pad * kKeyStride] per-token maxima (order key << 32 | ~n),
+                                // zeroed per call by the prep kernel
+  uint32_t* am_done;            // CTAs that have finished, zeroed per call
   int64_t* am_idx;              // [M] result: vocabulary row of the largest logit
   float* am_val;                // [M] result: that logit (may be null)
 };
@@ -106,7 +108,8 @@ __global__ void __launch_bounds__(256) w4a16_prep_x_kernel(const uint16_t* __res
                                                            float* __restrict__ tok_scale,
                                                            int32_t* __restrict__ status,
                                                            uint32_t* __restrict__ split_flags,
-                                                           int n_split_flags) {
+                                                           int n_split_flags,
+                                                           unsigned long long* __restrict__ am_keys) {
   // launched as a programmatic dependent of whatever ran before it: wait for
   // that kernel's results before touching memory (the previous call's GEMM
   // may still be reading this workspace)
@@ -119,6 +122,7 @@ __global__ void __launch_bounds__(256) w4a16_prep_x_kernel(const uint16_t* __res
     for (int i = threadIdx.x; i < n_split_flags; i += blockDim.x) split_flags[i] = 0;
   }
   const int64_t m = blockIdx.x;
+  if (am_keys && threadIdx.x == 0) am_keys[m * kKeyStride] = 0ull;  // argmax: no candidate yet
   __half* dst = x16 + m * K;
   const int64_t nv = K / 8;
   if (m >= M) {  // padding rows of the last token tile
@@ -267,33 +271,30 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const 
 }
 
 // ------------------------------------------------------------ greedy argmax
-// A logit's 32-bit order key: unsigned order of the keys is the order of the
-// values, -0 and +0 share one key, every NaN is above +Inf, and no value
-// maps to 0 (which therefore means "no candidate").  A candidate is the
-// 64-bit word key << 32 | ~n: the larger word has the larger logit, and of
-// equal logits the smaller vocabulary row.
+// A logit's 32-bit order key: for the logits the epilogue forms (never -0;
+// a NaN only in the positive form the GPU's arithmetic produces) unsigned
+// order of keys is the order of values and every NaN is above +Inf.  A
+// candidate is key << 32 | ~n: the larger 64-bit word has the larger
+// logit, and of equal logits the smaller row.
 __device__ __forceinline__ uint32_t order_key(float v) {
-  if (v != v) return 0xFFFFFFFFu;
-  uint32_t b = __float_as_uint(v);
-  if (b == 0x80000000u) b = 0u;
-  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+  const uint32_t b = __float_as_uint(v);
+  return b ^ ((uint32_t)((int32_t)b >> 31) | 0x80000000u);
+}
+
+// 16 consecutive floats of shared memory (16-byte aligned)
+__device__ __forceinline__ void lds_f32x16(const float* src, float (&d)[16]) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float4 f = reinterpret_cast<const float4*>(src)[i];
+    d[4 * i] = f.x;
+    d[4 * i + 1] = f.y;
+    d[4 * i + 2] = f.z;
+    d[4 * i + 3] = f.w;
+  }
 }
 
 __device__ __forceinline__ float key_value(uint32_t k) {
   return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
-}
-
-// Merge a warp's running candidates for the tokens tok0 .. tok0+BN-1 into
-// the global maxima (one 64-bit atomic max per token) and clear them.
-__device__ __forceinline__ void argmax_flush(unsigned long long* best, unsigned long long* keys,
-                                             int64_t tok0, int64_t M, int BN, int lane) {
-  __syncwarp();
-  for (int t = lane; t < BN; t += 32) {
-    const unsigned long long k = best[t];
-    if (k != 0ull && tok0 + t < M) atomicMax(keys + tok0 + t, k);
-    best[t] = 0ull;
-  }
-  __syncwarp();
 }
 
 // ------------------------------------------------------------ schedule
@@ -357,11 +358,10 @@ __global__ void __launch_bounds__((GemmShape<kStages, kPStages, kDqPerQuad>::kTh
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done_bar + 1);
   volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(tmem_slot + 1);
   float* s_tok = reinterpret_cast<float*>(bars + 32);  // 4 epilogue warps x kMaxBN multipliers
-  // argmax mode: 4 epilogue warps x kMaxBN running candidates, the token tile
-  // each warp's candidates belong to, and the "last CTA" flag
-  unsigned long long* s_best = reinterpret_cast<unsigned long long*>(s_tok + 4 * kMaxBN);
-  int32_t* s_tt = reinterpret_cast<int32_t*>(s_best + 4 * kMaxBN);
-  int32_t* s_last = s_tt + 4;
+  // argmax: the "last CTA" flag, then per epilogue warp the thresholds of
+  // its current unit's tokens (lower bounds of each token's largest logit)
+  int32_t* s_last = reinterpret_cast<int32_t*>(s_tok + 4 * kMaxBN);
+  float* s_thr = reinterpret_cast<float*>(s_last + 4);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -551,32 +551,34 @@ __global__ void __launch_bounds__((GemmShape<kStages, kPStages, kDqPerQuad>::kTh
     const int row = q * 32 + lane;
     const uint32_t lane_off = (uint32_t)(q * 32) << 16;
     float* tok = s_tok + (warp - kFirstEpiWarp) * kMaxBN;
-    unsigned long long* best = s_best + (warp - kFirstEpiWarp) * kMaxBN;
-    int cur_tt = -1;  // argmax mode: the token tile `best` belongs to
-    if (kOut == kOutArgmax) {
-      for (int t = lane; t < kMaxBN; t += 32) best[t] = 0ull;
-      __syncwarp();
-    }
+    float* wthr = s_thr + (warp - kFirstEpiWarp) * kMaxBN;
     int64_t i = 0;
     for_each_piece(p, [&](const Piece& pc) {
       const uint32_t u = pc.u, kb0 = pc.kb0, kb1 = pc.kb1;
       const uint32_t buf = (uint32_t)(i & 1), dph = (uint32_t)((i >> 1) & 1);
       ++i;
-      if (!warp_wait(&d_full[buf], dph, wc)) return false;
-      tc_fence_after();
       const int64_t n = (int64_t)(u / p.n_ttiles) * kRows + row;
       const int64_t t0 = (int64_t)(u % p.n_ttiles) * BN;
-      if (kOut == kOutArgmax && (int)(u % p.n_ttiles) != cur_tt) {
-        // a new token tile: hand the finished tile's candidates to the global maxima
-        if (cur_tt >= 0) argmax_flush(best, p.am_keys, (int64_t)cur_tt * BN, p.M, BN, lane);
-        cur_tt = (int)(u % p.n_ttiles);
+      // Before the accumulators are ready: this unit's token multipliers,
+      // once per warp (written by the prep kernel, which may still have been
+      // running when this kernel started, so read coherently from L2, not
+      // the read-only path) and, for argmax, each token's current maximum
+      // as a threshold (a stale one is only lower; no candidate yet: -Inf;
+      // tokens past M: +Inf, nothing passes).
+      for (int t = lane; t < BN; t += 32) {
+        const bool live = t0 + t < p.M;
+        tok[t] = live ? __ldcg(p.tok_scale + t0 + t) : 0.0f;
+        if (kOut == kOutArgmax) {
+          const uint32_t kh =
+              live ? __ldcg(reinterpret_cast<const uint32_t*>(p.am_keys + (t0 + t) * kKeyStride) + 1)
+                   : 0u;
+          wthr[t] = !live ? __int_as_float(0x7F800000)
+                          : (kh ? key_value(kh) : __int_as_float(0xFF800000));
+        }
       }
-      // this unit's token multipliers, once per warp: they are written by the
-      // prep kernel, which may still have been running when this kernel
-      // started, so they are read coherently from L2 (not the read-only path)
-      for (int t = lane; t < BN; t += 32)
-        tok[t] = (t0 + t < p.M) ? __ldcg(p.tok_scale + t0 + t) : 0.0f;
       __syncwarp();
+      if (!warp_wait(&d_full[buf], dph, wc)) return false;
+      tc_fence_after();
       // A tail unit cut by a range boundary: its two CTAs share slot `key`
       // (the CTA whose tail range starts inside the unit).  The first to get here parks
       // its fp32 partial; the second adds it to its own and stores logits.
@@ -616,24 +618,42 @@ __global__ void __launch_bounds__((GemmShape<kStages, kPStages, kDqPerQuad>::kTh
             v[t] = __float_as_uint(__fadd_rn(__uint_as_float(v[t]), other[t]));
         }
         if (kOut == kOutArgmax) {
-          // per token: the warp's largest key over its 32 rows, and the
-          // lowest lane holding it; lane t keeps token c + t's result
-          uint32_t my_m = 0, my_bal = 0;
+          // Per token: the logit as the plain product rounds it (the fma
+          // with +0 rounds like the multiply and turns an exact -0 into +0).
+          // Only if some row of this warp reaches the CTA's threshold for
+          // the token (>=, so that ties reach the exact comparison) does the
+          // warp find its largest key and the lowest lane holding it, merge
+          // that candidate into the token's maximum with one atomic, and
+          // raise the threshold.  The threshold is shared by the epilogue
+          // warps without ordering: a stale value is only lower.
+          const bool valid = n < p.N;
+          const uint32_t n_base = (uint32_t)(n - lane);
+          float thr[16], mul[16], val[16];
+          lds_f32x16(wthr + c, thr);
+          lds_f32x16(tok + c, mul);
+          bool pass = false;
 #pragma unroll
-          for (int t = 0; t < 16; ++t) {
-            const float val = __fmul_rn(__uint_as_float(v[t]), tok[c + t]);
-            const uint32_t k32 = n < p.N ? order_key(val) : 0u;
-            const uint32_t m = __reduce_max_sync(0xFFFFFFFFu, k32);
-            const uint32_t bal = __ballot_sync(0xFFFFFFFFu, k32 == m);
-            if (lane == t) {
-              my_m = m;
-              my_bal = bal;
-            }
+          for (int t = 0; t < 16; t += 2) {
+            const float2 r = __ffma2_rn(make_float2(__uint_as_float(v[t]), __uint_as_float(v[t + 1])),
+                                        make_float2(mul[t], mul[t + 1]), make_float2(0.0f, 0.0f));
+            val[t] = r.x;
+            val[t + 1] = r.y;
+            pass |= !(r.x < thr[t]);
+            pass |= !(r.y < thr[t + 1]);
           }
-          if (lane < 16 && my_m != 0u && t0 + c + lane < p.M) {
-            const uint32_t nb = (uint32_t)(n - lane) + (uint32_t)(__ffs(my_bal) - 1);
-            const unsigned long long key = ((unsigned long long)my_m << 32) | (uint32_t)~nb;
-            if (key > best[c + lane]) best[c + lane] = key;
+          if (__any_sync(0xFFFFFFFFu, valid && pass)) {
+#pragma unroll
+            for (int t = 0; t < 16; ++t) {
+              if (__any_sync(0xFFFFFFFFu, valid && !(val[t] < thr[t]))) {
+                const uint32_t kk = valid ? order_key(val[t]) : 0u;
+                const uint32_t m = __reduce_max_sync(0xFFFFFFFFu, kk);
+                const uint32_t bal = __ballot_sync(0xFFFFFFFFu, valid && kk == m);
+                if (lane == 0)
+                  atomicMax(p.am_keys + (t0 + c + t) * kKeyStride,
+                            ((unsigned long long)m << 32) |
+                                (uint32_t)~(n_base + (uint32_t)(__ffs(bal) - 1)));
+              }
+            }
           }
         } else if (n < p.N) {
 #pragma unroll
@@ -659,10 +679,6 @@ __global__ void __launch_bounds__((GemmShape<kStages, kPStages, kDqPerQuad>::kTh
       if (lane == 0) mbar_arrive(&d_empty[buf]);
       return true;
     });
-    if (kOut == kOutArgmax) {
-      __syncwarp();
-      if (lane == 0) s_tt[warp - kFirstEpiWarp] = cur_tt;
-    }
   }
 
   __syncthreads();
@@ -671,37 +687,22 @@ __global__ void __launch_bounds__((GemmShape<kStages, kPStages, kDqPerQuad>::kTh
     tmem_dealloc(tmem_base, p.tmem_cols);
   }
   if constexpr (kOut == kOutArgmax) {
-    // Merge the four epilogue warps' candidates (one atomic max per token),
-    // then the last CTA to finish turns the maxima into rows and values.
-    const int e = threadIdx.x - 32 * kFirstEpiWarp;
-    if (e >= 0 && e < BN) {
-      const int tt0 = s_tt[0];
-      unsigned long long k = 0ull;
-#pragma unroll
-      for (int w = 0; w < 4; ++w) {
-        const int ttw = s_tt[w];
-        const unsigned long long kw = s_best[w * kMaxBN + e];
-        if (ttw < 0 || kw == 0ull) continue;
-        if (ttw == tt0) {
-          k = kw > k ? kw : k;
-        } else if ((int64_t)ttw * BN + e < p.M) {
-          atomicMax(p.am_keys + (int64_t)ttw * BN + e, kw);
-        }
-      }
-      if (k != 0ull && tt0 >= 0 && (int64_t)tt0 * BN + e < p.M)
-        atomicMax(p.am_keys + (int64_t)tt0 * BN + e, k);
+    // Every candidate of this CTA has been merged (the atomics precede the
+    // barrier above); the last CTA to get here turns the maxima into rows
+    // and values.  The release-acquire counter orders the other CTAs'
+    // atomics before its reads.
+    if (threadIdx.x == 32 * kFirstEpiWarp) {
+      uint32_t old;
+      asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], 1;"
+                   : "=r"(old) : "l"(p.am_done) : "memory");
+      *s_last = old == gridDim.x - 1 ? 1 : 0;
     }
-    __threadfence();
-    __syncthreads();
-    if (e == 0) *s_last = atomicAdd(p.am_done, 1u) == gridDim.x - 1 ? 1 : 0;
     __syncthreads();
     if (*s_last) {
-      __threadfence();
       for (int64_t t = threadIdx.x; t < p.M; t += blockDim.x) {
-        const unsigned long long k = __ldcg(p.am_keys + t);
-        const uint32_t k32 = (uint32_t)(k >> 32);
-        p.am_idx[t] = k32 ? (int64_t)(uint32_t)~(uint32_t)k : (int64_t)-1;
-        if (p.am_val) p.am_val[t] = key_value(k32);
+        const unsigned long long k = __ldcg(p.am_keys + t * kKeyStride);
+        p.am_idx[t] = k != 0ull ? (int64_t)(uint32_t)~(uint32_t)k : (int64_t)-1;
+        if (p.am_val) p.am_val[t] = key_value((uint32_t)(k >> 32));
       }
     }
   }
@@ -744,11 +745,11 @@ static int lm_head_token_tile(int64_t M) {
 
 static size_t gemm_smem_bytes(int BN, int stages, int pstages, bool argmax) {
   // ring buffers, then 256 B of barriers and flags, then the epilogue's
-  // per-warp token multipliers (and, for argmax, per-warp candidates, their
-  // token tiles and a flag)
+  // per-warp token multipliers (and, for argmax, a flag and per-warp
+  // token thresholds)
   return 1024 + pstages * (size_t)(kPackedStageBytes + kScaleStageBytes) +
          stages * (size_t)BN * kKB * 2 + 256 + 4 * kMaxBN * sizeof(float) +
-         (argmax ? 4 * kMaxBN * sizeof(unsigned long long) + 64 : 0);
+         (argmax ? 16 + 4 * kMaxBN * sizeof(float) : 0);
 }
 
 static int sm_count() {
@@ -760,9 +761,10 @@ static int sm_count() {
 
 // Workspace layout of one call: [status header][x as fp16, m_pad x K]
 // [token multipliers, m_pad][split counters, grid x 4][split ready flags,
-// grid x 4] and, for argmax only, [CTAs done, 1][candidate maxima, m_pad
-// x 64 bit]; then [split partials, grid x 4 x BN x 32 fp32].  Everything
-// from the split counters up to the partials is zeroed by the prep kernel.
+// grid x 4] and, for argmax only, [CTAs done, 1]; these are zeroed by the
+// prep kernel's first CTA.  Then [split partials, grid x 4 x BN x 32 fp32]
+// and, for argmax only, [per-token maxima, m_pad x 128 bytes, one 64-bit
+// word used per line], each word zeroed by the prep CTA of its token.
 struct WsLayout {
   size_t x16, tok, cnt, ready, done, keys, part, total;
   int grid;
@@ -779,9 +781,9 @@ static WsLayout ws_layout(int64_t M, int64_t N, int64_t K, int sms, bool argmax)
   l.cnt = l.tok + align_up((size_t)m_pad * 4, 256);
   l.ready = l.cnt + align_up((size_t)l.grid * 4 * 4, 256);
   l.done = l.ready + align_up((size_t)l.grid * 4 * 4, 256);
-  l.keys = l.done + (argmax ? 256 : 0);
-  l.part = l.keys + (argmax ? align_up((size_t)m_pad * 8, 256) : 0);
-  l.total = l.part + align_up((size_t)l.grid * 4 * BN * 32 * 4, 256);
+  l.part = l.done + (argmax ? 256 : 0);
+  l.keys = l.part + align_up((size_t)l.grid * 4 * BN * 32 * 4, 256);
+  l.total = l.keys + (argmax ? (size_t)m_pad * kKeyStride * 8 : 0);
   return l;
 }
 
@@ -846,8 +848,8 @@ nvfp4_status lm_head_launch(const void* x, int64_t M, int64_t K, const uint8_t* 
                  (uint64_t)K * 2, 64, (uint32_t)BN, CU_TENSOR_MAP_SWIZZLE_128B))
     return NVFP4_ERR_CUDA;
 
-  // the counters, ready flags and argmax maxima are adjacent: the prep
-  // kernel clears them all
+  // the counters, ready flags and the argmax counter are adjacent: the
+  // prep kernel clears them all
   {
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -860,7 +862,9 @@ nvfp4_status lm_head_launch(const void* x, int64_t M, int64_t K, const uint8_t* 
     cfg.numAttrs = 1;
     if (cudaLaunchKernelEx(&cfg, w4a16_prep_x_kernel, static_cast<const uint16_t*>(x), M, K,
                            global_scale, x16, tok_scale, status, split_cnt,
-                           (int)((L.part - L.cnt) / 4)) != cudaSuccess)
+                           (int)((L.part - L.cnt) / 4),
+                           argmax ? reinterpret_cast<unsigned long long*>(ws + L.keys)
+                                  : nullptr) != cudaSuccess)
       return NVFP4_ERR_CUDA;
   }
 
@@ -892,6 +896,7 @@ nvfp4_status lm_head_launch(const void* x, int64_t M, int64_t K, const uint8_t* 
   // A stages only
   const bool deep = BN <= 64;
   const int stages = deep ? 3 : 2;
+
   a.tmem_cols = (2 * BN + stages * (kKB / 2) <= 256) ? 256u : 512u;
   a.tok_scale = tok_scale;
   a.out = logits;

@@ -3,7 +3,8 @@
 Two bars:
 * bit for bit against the fp32 logits the plain product writes for the same
   inputs: the token id is the smallest row holding the row maximum (a NaN
-  counts as the maximum, first NaN wins), the value is that logit;
+  counts as the maximum, first NaN wins; -0 equals +0), the value is that
+  logit (+0 for a zero maximum);
 * against the CPU oracle's fp64 logits: the chosen row agrees with the
   oracle's argmax unless the oracle's top two are closer than 1e-3, and the
   returned value is within the logits tolerance of the oracle's logit there.
@@ -54,7 +55,8 @@ def assert_same_as_plain(xd, dev_q, what=""):
     assert bad.numel() == 0, (what, bad[:5].tolist(), ids[bad[:5, 0]].tolist(),
                               want_ids[bad[:5, 0]].tolist())
     both_nan = torch.isnan(vals) & torch.isnan(want_vals)
-    same = (vals.view(torch.int32) == want_vals.view(torch.int32)) | both_nan
+    both_zero = (vals == 0) & (want_vals == 0)  # a zero maximum is returned as +0
+    same = (vals.view(torch.int32) == want_vals.view(torch.int32)) | both_nan | both_zero
     assert bool(same.all()), (what, vals[~same][:5].tolist(), want_vals[~same][:5].tolist())
     return ids.cpu().numpy(), vals.cpu().numpy()
 
@@ -130,8 +132,9 @@ def test_exact_ties_take_the_smallest_row():
 
 
 def test_negative_maxima_and_nan_tokens():
-    """A token whose logits are all negative, and a token row holding a NaN
-    (every logit of that token is NaN: row 0, value NaN)."""
+    """A token whose logits are all negative, a token row holding a NaN
+    (every logit of that token is NaN: row 0, value NaN) and an all-zero
+    token row (all logits zero, of either sign: row 0, value +0)."""
     N, K, M = 1000, 512, 3
     x = synth.decode_x(M, K=K)
     xf = synth.bf16_bits_to_f32(x).copy()
@@ -139,13 +142,14 @@ def test_negative_maxima_and_nan_tokens():
     Wf = -np.abs(rng.uniform(0.5, 1.5, (N, 1))) * xf[0][None, :]
     W = synth.f32_to_bf16_bits(Wf.astype(np.float32))
     xf[1, 17] = np.nan
+    xf[2] = 0.0  # every logit of token 2 is a zero (+0 or -0): row 0, value +0
     xn = synth.f32_to_bf16_bits(xf)
     host_q = oracle.quantize(W)
     ids, vals = assert_same_as_plain(to_bf16_dev(xn), upload(*host_q), "neg/nan")
     assert vals[0] < 0
     assert ids[1] == 0 and np.isnan(vals[1])
-    keep = [0, 2]
-    assert_oracle_agrees(ids[keep], vals[keep], oracle.logits(x[keep], *host_q))
+    assert ids[2] == 0 and vals[2] == 0 and not np.signbit(vals[2])
+    assert_oracle_agrees(ids[:1], vals[:1], oracle.logits(x[:1], *host_q))
 
 
 def test_no_values_empty_and_status():
@@ -218,4 +222,4 @@ def test_graph_replay():
         want_ids, want_vals = expected_from_logits(nv.w4a16_lm_head(xd, *dev_q))
         torch.cuda.synchronize()
         assert torch.equal(ids, want_ids)
-        assert torch.equal(vals.view(torch.int32), want_vals.view(torch.int32))
+        assert torch.equal(vals, want_vals)
