@@ -15,6 +15,10 @@ What each function follows is stated in ``nvfp4_oracle.c``.  In short:
 * ``dequant_rows`` / ``logits`` -- the W4A16 product of
   ``CompressedTensorsW4A16Fp4`` (page *...compressed_tensors.schemes*):
   logits = x . (e2m1 * f32(scale) * global)^T, here in float64.
+* ``fp8_quantize`` / ``fp8_logits`` -- the "fp8" copy of
+  ``quantized_lm_head_copy`` (same lm_head page): per-row E4M3 weights with an
+  fp32 scale amax/448, per-token E4M3 activations likewise, and the W8A8
+  product xs * ws * (q_x . q_w) in float64.
 
 Parity: every function is pinned in ``tests/test_oracle_*.py`` against what
 the pages fix (the code table, the packing order, K % 16), closed forms,
@@ -79,6 +83,9 @@ def _load():
         lib.oracle_dequant_rows.argtypes = [p, p, f, i64, p, i64, p]
         lib.oracle_logits_cols.argtypes = [p, i64, i64, p, p, f, p, i64, p]
         lib.oracle_e4m3_encode_array.argtypes = [p, i64, p]
+        lib.oracle_fp8_quantize_rows.argtypes = [p, i64, i64, p, p]
+        lib.oracle_fp8_quantize_rows.restype = ctypes.c_int
+        lib.oracle_fp8_logits_cols.argtypes = [p, p, i64, i64, p, p, p, i64, p]
         lib.oracle_e2m1_round_array.argtypes = [p, i64, p]
         lib.oracle_num_threads.restype = ctypes.c_int
         _lib = lib
@@ -211,6 +218,35 @@ def logits(x: np.ndarray, packed: np.ndarray, scales: np.ndarray, g: float,
     out = np.zeros((M, cols.size), dtype=np.float64)
     _load().oracle_logits_cols(_ptr(x), M, K, _ptr(packed), _ptr(scales), g, _ptr(cols),
                                cols.size, _ptr(out))
+    return out
+
+
+def fp8_quantize(W: np.ndarray) -> tuple[np.ndarray, np.ndarray]:
+    """Per-row fp8 copy of bf16 rows (lm_head weights, or activation tokens):
+    (q u8(e4m3)[N,K], scale f32[N]); dequant = e4m3(q) * scale[row]."""
+    W = np.ascontiguousarray(W, dtype=np.uint16)
+    N, K = W.shape
+    q = np.zeros((N, K), dtype=np.uint8)
+    s = np.zeros(N, dtype=np.float32)
+    if _load().oracle_fp8_quantize_rows(_ptr(W), N, K, _ptr(q), _ptr(s)) != 0:
+        raise OracleError("non-finite value")
+    return q, s
+
+
+def fp8_logits(xq: np.ndarray, xs: np.ndarray, wq: np.ndarray, ws: np.ndarray,
+               cols=None) -> np.ndarray:
+    """float64 logits[M, len(cols)] = xs * ws * (e4m3(xq) . e4m3(wq[cols])^T)."""
+    xq = np.ascontiguousarray(xq, dtype=np.uint8)
+    wq = np.ascontiguousarray(wq, dtype=np.uint8)
+    xs = np.ascontiguousarray(xs, dtype=np.float32)
+    ws = np.ascontiguousarray(ws, dtype=np.float32)
+    M, K = xq.shape
+    N = wq.shape[0]
+    assert wq.shape[1] == K
+    cols = np.arange(N, dtype=np.int64) if cols is None else np.ascontiguousarray(cols, np.int64)
+    out = np.zeros((M, cols.size), dtype=np.float64)
+    _load().oracle_fp8_logits_cols(_ptr(xq), _ptr(xs), M, K, _ptr(wq), _ptr(ws), _ptr(cols),
+                                   cols.size, _ptr(out))
     return out
 
 

@@ -26,6 +26,9 @@
  * (nearest even); values are scaled by 1 / (f32(scale) * global), clamped
  * to [-6, 6] and rounded to the E2M1 grid, ties to the even code.
  *
+ * The fp8 copy (per-row E4M3 weights, per-token E4M3 activations) is at the
+ * end of the file, with its own reading stated there.
+ *
  * Parity pins: every function here is checked in tests/ against facts the
  * pages or mathematics fix (code table, packing order, closed forms,
  * brute-force nearest rounding, torch's own e4m3 cast, numpy matmul).
@@ -314,6 +317,79 @@ void oracle_logits_cols(const uint16_t *x, int64_t M, int64_t K, const uint8_t *
       }
     }
     free(w);
+  }
+}
+
+/* ============================================================ fp8 copy */
+/*
+ * The "fp8" lm_head copy of the page
+ * "vllm.model_executor.layers.quantization.online.lm_head"
+ * (`quantized_lm_head_copy`): per-row weight scales and per-token
+ * activation scales on an FP8 (E4M3) linear kernel -- the
+ * FP8_PER_CHANNEL_PER_TOKEN scheme of the page
+ * "vllm/model_executor/layers/quantization/modelopt.py" (static per-channel
+ * weight scale, dynamic per-token activation scale).  The quantizer body is
+ * not printed; the reading used here, for a row v[0..K) of W (or of x):
+ *   amax = max |v|;  s = max(fl32(amax / 448), fl32(1e-12));  r = fl32(1 / s);
+ *   q[k] = e4m3(clamp(fl32(v[k] * r), -448, 448)), round to nearest even,
+ *          the sign of the product kept (so -0 encodes as 0x80, as a cast does).
+ * The dequantized value is e4m3(q) * s.
+ */
+
+/* Signed E4M3 encode of a float already clamped to [-448, 448]. */
+static uint8_t e4m3_encode_signed(float v) {
+  uint8_t mag = oracle_e4m3_encode(fabsf(v));
+  return signbit(v) ? (uint8_t)(mag | 0x80u) : mag;
+}
+
+/* Per-row fp8 quantization of bf16 rows (weights, or activation tokens).
+ * Returns 0, or -1 if a row holds a non-finite value (outside the method). */
+int oracle_fp8_quantize_rows(const uint16_t *W, int64_t N, int64_t K, uint8_t *q,
+                             float *scale) {
+  int bad = 0;
+#pragma omp parallel for schedule(static) reduction(| : bad)
+  for (int64_t n = 0; n < N; ++n) {
+    const uint16_t *w = W + n * K;
+    float amax = 0.0f;
+    for (int64_t k = 0; k < K; ++k) {
+      if (!bf16_is_finite(w[k])) bad = 1;
+      float a = fabsf(bf16_to_f32(w[k]));
+      if (a > amax) amax = a;
+    }
+    float s = amax / E4M3_MAX;
+    const float floor_s = 1e-12f;
+    if (s < floor_s) s = floor_s;
+    const float r = 1.0f / s;
+    scale[n] = s;
+    for (int64_t k = 0; k < K; ++k) {
+      float v = bf16_to_f32(w[k]) * r;
+      if (v > E4M3_MAX) v = E4M3_MAX;
+      if (v < -E4M3_MAX) v = -E4M3_MAX;
+      q[n * K + k] = e4m3_encode_signed(v);
+    }
+  }
+  return bad ? -1 : 0;
+}
+
+/*
+ * W8A8 logits: out[m, j] = xs[m] * ws[c] * sum_k e4m3(xq[m, k]) * e4m3(wq[c, k])
+ * for c = cols[j], in double (every product and partial sum is exact in
+ * double for K <= 2^20), then scaled by the two fp32 scales.
+ */
+void oracle_fp8_logits_cols(const uint8_t *xq, const float *xs, int64_t M, int64_t K,
+                            const uint8_t *wq, const float *ws, const int64_t *cols,
+                            int64_t n_cols, double *out) {
+  double lut[256];
+  for (int i = 0; i < 256; ++i) lut[i] = (double)oracle_e4m3_decode((uint8_t)i);
+#pragma omp parallel for schedule(dynamic, 64)
+  for (int64_t j = 0; j < n_cols; ++j) {
+    const uint8_t *w = wq + cols[j] * K;
+    for (int64_t m = 0; m < M; ++m) {
+      const uint8_t *x = xq + m * K;
+      double acc = 0.0;
+      for (int64_t k = 0; k < K; ++k) acc += lut[x[k]] * lut[w[k]];
+      out[m * n_cols + j] = acc * (double)xs[m] * (double)ws[cols[j]];
+    }
   }
 }
 
