@@ -217,6 +217,81 @@ nvfp4_status w4a16_lm_head_argmax(const void *x, int64_t M, int64_t K, const uin
                                   int64_t *token_ids, float *max_logits, void *workspace,
                                   size_t workspace_bytes, void *stream);
 
+/* ------------------------------------------------------- fp8 copy */
+
+/*
+ * The "fp8" lm_head copy -- `quantized_lm_head_copy` on the page
+ * "vllm.model_executor.layers.quantization.online.lm_head": per-row weight
+ * scales and per-token activation scales on an FP8 linear kernel (the
+ * FP8_PER_CHANNEL_PER_TOKEN scheme of "vllm/model_executor/layers/
+ * quantization/modelopt.py").  The quantizer body is not on the pages; the
+ * reading implemented, for one row v of W (or one token of x):
+ *   s = max(fl32(max|v| / 448), fl32(1e-12)),  r = fl32(1 / s),
+ *   q[k] = e4m3(fl32(v[k] * r)), nearest even, saturated to +-448, sign kept.
+ */
+
+/* Workspace bytes of fp8_quantize_rows / fp8_refresh (the status word);
+ * 0 for shapes they reject. */
+size_t fp8_quantize_workspace_bytes(int64_t N, int64_t K);
+
+/*
+ * Quantize the rows of W to the fp8 copy.
+ *   W          bf16 [N, K], device, 16-byte aligned.  N >= 1, K % 16 == 0,
+ *              K <= 65536.
+ *   q          u8 (float8_e4m3fn) [N, K], device, 16-byte aligned.  Written.
+ *   row_scale  f32 [N], device.  Written: s of each row (dequant = e4m3(q) * s).
+ *   workspace  device, >= fp8_quantize_workspace_bytes(N, K), 256-byte
+ *              aligned: the status word (NVFP4_ERR_NONFINITE if W holds an
+ *              Inf or NaN; that row's outputs are then unspecified).
+ * One kernel, one read of W and one write of q; no host synchronization.
+ */
+nvfp4_status fp8_quantize_rows(const void *W, int64_t N, int64_t K, uint8_t *q, float *row_scale,
+                               void *workspace, size_t workspace_bytes, void *stream);
+
+/* Re-derive the fp8 copy in place after W changed (`refresh_quantized_lm_heads`):
+ * same arguments, same buffers, addresses unchanged. */
+nvfp4_status fp8_refresh(const void *W, int64_t N, int64_t K, uint8_t *q, float *row_scale,
+                         void *workspace, size_t workspace_bytes, void *stream);
+
+/* Workspace bytes of w8a8_lm_head: x as e4m3 (M_pad * K bytes), one scale
+ * per token, the status word and room for split-K partials.  0 for shapes
+ * the call rejects. */
+size_t w8a8_lm_head_workspace_bytes(int64_t M, int64_t N, int64_t K);
+
+/*
+ * logits[m, n] = fl32(fl32(acc[m, n] * s_x[m]) * row_scale[n]), acc the fp32
+ * sum over k of e4m3(q_x[m, k]) * e4m3(q[n, k]), where (q_x, s_x) is x
+ * quantized per token by the rule above (inside the call, into the
+ * workspace).
+ *   x          bf16 [M, K], device, 16-byte aligned.  M >= 0 (0: no-op),
+ *              K % 256 == 0, 256 <= K <= 16384.
+ *   q, row_scale  as fp8_quantize_rows writes them for W[N, K].
+ *   N          vocabulary rows, N >= 0 (0: no-op).
+ *   logits     [M, N] fp32 (NVFP4_OUT_F32) or bf16 (NVFP4_OUT_BF16), device,
+ *              16-byte aligned.
+ *   workspace  device, >= w8a8_lm_head_workspace_bytes(M, N, K), 256-byte aligned.
+ * Tensor-core fp32 accumulation, deterministic (no floating-point atomics).
+ */
+nvfp4_status w8a8_lm_head(const void *x, int64_t M, int64_t K, const uint8_t *q,
+                          const float *row_scale, int64_t N, void *logits, int out_dtype,
+                          void *workspace, size_t workspace_bytes, void *stream);
+
+/* Workspace bytes of w8a8_lm_head_argmax (0 for rejected shapes, N == 0 included). */
+size_t w8a8_lm_head_argmax_workspace_bytes(int64_t M, int64_t N, int64_t K);
+
+/*
+ * The greedy argmax of the W8A8 logits fused into the product, with the
+ * semantics of w4a16_lm_head_argmax: token_ids[m] is the smallest n whose
+ * logit (bit for bit the fp32 value w8a8_lm_head writes) is the row maximum,
+ * max_logits[m] that value (+0 for a zero maximum; NaN ranks highest).
+ * Arguments as for w8a8_lm_head, with token_ids int64 [M] (8-byte aligned)
+ * and max_logits fp32 [M] or NULL; N >= 1.
+ */
+nvfp4_status w8a8_lm_head_argmax(const void *x, int64_t M, int64_t K, const uint8_t *q,
+                                 const float *row_scale, int64_t N, int64_t *token_ids,
+                                 float *max_logits, void *workspace, size_t workspace_bytes,
+                                 void *stream);
+
 /* ------------------------------------------- allocation-free variant */
 
 /* Size of the fixed device scratch array behind w4a16_lm_head_noalloc. */

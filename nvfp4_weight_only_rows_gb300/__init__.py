@@ -19,6 +19,10 @@ Entry points (same names as the C ABI):
 * ``w4a16_lm_head_argmax(x, packed, scales, global_scale)`` ->
   ``(token_ids i64[M], max_logits f32[M])`` -- the same product reduced to each
   token's largest logit inside the kernel (greedy choice; logits never stored).
+* ``fp8_quantize_rows(W)`` -> ``(q e4m3[N,K], row_scale f32[N])`` and
+  ``fp8_refresh`` -- the "fp8" copy of ``quantized_lm_head_copy`` (per-row
+  scales); ``w8a8_lm_head(x, q, row_scale)`` / ``w8a8_lm_head_argmax`` -- its
+  product with per-token fp8 activations on the fp8 tensor cores.
 """
 from __future__ import annotations
 
@@ -33,7 +37,9 @@ __all__ = [
     "nvfp4_refresh", "w4a16_lm_head", "nvfp4_quantize_workspace_bytes",
     "w4a16_lm_head_workspace_bytes", "nvfp4_read_device_status", "w4a16_lm_head_noalloc",
     "nvfp4_selftest_bounded_wait", "OUT_F32", "OUT_BF16", "w4a16_lm_head_argmax",
-    "w4a16_lm_head_argmax_workspace_bytes",
+    "w4a16_lm_head_argmax_workspace_bytes", "fp8_quantize_rows", "fp8_refresh",
+    "fp8_quantize_workspace_bytes", "w8a8_lm_head", "w8a8_lm_head_argmax",
+    "w8a8_lm_head_workspace_bytes", "w8a8_lm_head_argmax_workspace_bytes",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -100,6 +106,20 @@ def load_library() -> ctypes.CDLL:
     lib.w4a16_lm_head_argmax_workspace_bytes.restype = sz
     lib.w4a16_lm_head_argmax.argtypes = [vp, i64, i64, vp, vp, vp, i64, vp, vp, vp, sz, vp]
     lib.w4a16_lm_head_argmax.restype = st
+    lib.fp8_quantize_workspace_bytes.argtypes = [i64, i64]
+    lib.fp8_quantize_workspace_bytes.restype = sz
+    for name in ("fp8_quantize_rows", "fp8_refresh"):
+        f = getattr(lib, name)
+        f.argtypes = [vp, i64, i64, vp, vp, vp, sz, vp]
+        f.restype = st
+    for name in ("w8a8_lm_head_workspace_bytes", "w8a8_lm_head_argmax_workspace_bytes"):
+        f = getattr(lib, name)
+        f.argtypes = [i64, i64, i64]
+        f.restype = sz
+    lib.w8a8_lm_head.argtypes = [vp, i64, i64, vp, vp, i64, vp, ctypes.c_int, vp, sz, vp]
+    lib.w8a8_lm_head.restype = st
+    lib.w8a8_lm_head_argmax.argtypes = [vp, i64, i64, vp, vp, i64, vp, vp, vp, sz, vp]
+    lib.w8a8_lm_head_argmax.restype = st
     lib.w4a16_lm_head_noalloc.argtypes = [vp, i64, i64, vp, vp, vp, i64, vp, ctypes.c_int, vp]
     lib.w4a16_lm_head_noalloc.restype = st
     lib.nvfp4_selftest_bounded_wait.argtypes = [vp, sz, i64, vp]
@@ -253,6 +273,106 @@ def w4a16_lm_head_argmax(x: torch.Tensor, packed: torch.Tensor, scales: torch.Te
                                   N, _ptr(token_ids), _ptr(max_logits), _ptr(workspace),
                                   workspace.numel() * workspace.element_size(), _stream(stream))
     _check(rc, "w4a16_lm_head_argmax")
+    return token_ids, max_logits
+
+
+def fp8_quantize_workspace_bytes(N: int, K: int) -> int:
+    return int(load_library().fp8_quantize_workspace_bytes(N, K))
+
+
+def w8a8_lm_head_workspace_bytes(M: int, N: int, K: int) -> int:
+    return int(load_library().w8a8_lm_head_workspace_bytes(M, N, K))
+
+
+def w8a8_lm_head_argmax_workspace_bytes(M: int, N: int, K: int) -> int:
+    return int(load_library().w8a8_lm_head_argmax_workspace_bytes(M, N, K))
+
+
+def fp8_quantize_rows(W: torch.Tensor, q: torch.Tensor | None = None,
+                      row_scale: torch.Tensor | None = None,
+                      workspace: torch.Tensor | None = None, stream=None):
+    """The fp8 copy of W bf16[N, K]: (q float8_e4m3fn[N, K], row_scale f32[N])."""
+    _need(W, torch.bfloat16, "W")
+    if W.dim() != 2:
+        raise ValueError("W must be 2-D [N, K]")
+    N, K = W.shape
+    if q is None:
+        q = torch.empty(N, K, dtype=torch.float8_e4m3fn, device=W.device)
+    if row_scale is None:
+        row_scale = torch.empty(N, dtype=torch.float32, device=W.device)
+    fp8_refresh(W, q, row_scale, workspace, stream, _where="fp8_quantize_rows")
+    return q, row_scale
+
+
+def fp8_refresh(W: torch.Tensor, q: torch.Tensor, row_scale: torch.Tensor,
+                workspace: torch.Tensor | None = None, stream=None, _where="fp8_refresh") -> None:
+    """Re-derive the fp8 copy of W into the existing buffers (addresses kept)."""
+    lib = load_library()
+    _need(W, torch.bfloat16, "W")
+    N, K = W.shape
+    if q.dtype not in (torch.float8_e4m3fn, torch.uint8):
+        raise ValueError("q must be float8_e4m3fn (or uint8 bit patterns)")
+    _need(q, q.dtype, "q", (N, K))
+    _need(row_scale, torch.float32, "row_scale", (N,))
+    if workspace is None:
+        workspace = _workspace(fp8_quantize_workspace_bytes(N, K), W.device)
+    fn = lib.fp8_quantize_rows if _where == "fp8_quantize_rows" else lib.fp8_refresh
+    rc = fn(_ptr(W), N, K, _ptr(q), _ptr(row_scale), _ptr(workspace),
+            workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(rc, _where)
+
+
+def _w8a8_args(x, q, row_scale):
+    _need(x, torch.bfloat16, "x")
+    M, K = x.shape
+    N = q.shape[0]
+    _need(q, q.dtype, "q", (N, K))
+    _need(row_scale, torch.float32, "row_scale", (N,))
+    return M, K, N
+
+
+def w8a8_lm_head(x: torch.Tensor, q: torch.Tensor, row_scale: torch.Tensor,
+                 out: torch.Tensor | None = None, out_dtype: torch.dtype = torch.float32,
+                 workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """logits[M, N] of the fp8 copy: x quantized per token to e4m3, fp8 tensor cores."""
+    lib = load_library()
+    M, K, N = _w8a8_args(x, q, row_scale)
+    if out is None:
+        out = torch.empty(M, N, dtype=out_dtype, device=x.device)
+    _need(out, out.dtype, "out", (M, N))
+    code = {torch.float32: OUT_F32, torch.bfloat16: OUT_BF16}.get(out.dtype)
+    if code is None:
+        raise ValueError("out must be float32 or bfloat16")
+    if workspace is None:
+        workspace = _workspace(w8a8_lm_head_workspace_bytes(M, N, K), x.device)
+    rc = lib.w8a8_lm_head(_ptr(x), M, K, _ptr(q), _ptr(row_scale), N, _ptr(out), code,
+                          _ptr(workspace), workspace.numel() * workspace.element_size(),
+                          _stream(stream))
+    _check(rc, "w8a8_lm_head")
+    return out
+
+
+def w8a8_lm_head_argmax(x: torch.Tensor, q: torch.Tensor, row_scale: torch.Tensor,
+                        token_ids: torch.Tensor | None = None,
+                        max_logits: torch.Tensor | None = None, with_values: bool = True,
+                        workspace: torch.Tensor | None = None, stream=None):
+    """Greedy argmax of the fp8 copy's logits without storing them:
+    (token_ids i64[M], max_logits f32[M] or None)."""
+    lib = load_library()
+    M, K, N = _w8a8_args(x, q, row_scale)
+    if token_ids is None:
+        token_ids = torch.empty(M, dtype=torch.int64, device=x.device)
+    _need(token_ids, torch.int64, "token_ids", (M,))
+    if max_logits is None and with_values:
+        max_logits = torch.empty(M, dtype=torch.float32, device=x.device)
+    if max_logits is not None:
+        _need(max_logits, torch.float32, "max_logits", (M,))
+    if workspace is None:
+        workspace = _workspace(w8a8_lm_head_argmax_workspace_bytes(M, N, K), x.device)
+    rc = lib.w8a8_lm_head_argmax(_ptr(x), M, K, _ptr(q), _ptr(row_scale), N, _ptr(token_ids),
+                                 _ptr(max_logits), _ptr(workspace),
+                                 workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(rc, "w8a8_lm_head_argmax")
     return token_ids, max_logits
 
 

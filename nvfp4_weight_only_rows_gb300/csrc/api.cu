@@ -18,6 +18,14 @@ nvfp4_status lm_head_launch(const void* x, int64_t M, int64_t K, const uint8_t* 
                             void* logits, int out_mode, int64_t* token_ids, float* max_logits,
                             void* workspace, cudaStream_t stream);
 constexpr int kOutArgmax = 2;  // lm_head_launch's third output mode
+int64_t fp8_max_k();
+nvfp4_status fp8_quantize_launch(const void* W, int64_t N, int64_t K, uint8_t* q,
+                                 float* row_scale, void* workspace, cudaStream_t stream);
+size_t w8a8_workspace_bytes(int64_t M, int64_t N, int64_t K, bool argmax);
+nvfp4_status w8a8_launch(const void* x, int64_t M, int64_t K, const uint8_t* wq,
+                         const float* w_scale, int64_t N, void* logits, int out_mode,
+                         int64_t* token_ids, float* max_logits, void* workspace,
+                         cudaStream_t stream);
 
 static bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
@@ -158,6 +166,89 @@ nvfp4_status w4a16_lm_head_argmax(const void* x, int64_t M, int64_t K, const uin
   if (st != NVFP4_OK) return st;
   return lm_head_launch(x, M, K, packed, scales, global_scale, N, nullptr, kOutArgmax, token_ids,
                         max_logits, workspace, static_cast<cudaStream_t>(stream));
+}
+
+/* ------------------------------------------------------------ fp8 copy */
+
+size_t fp8_quantize_workspace_bytes(int64_t N, int64_t K) {
+  if (N <= 0 || K <= 0 || K % 16 != 0 || K > fp8_max_k()) return 0;
+  return kWsHeader;
+}
+
+nvfp4_status fp8_quantize_rows(const void* W, int64_t N, int64_t K, uint8_t* q, float* row_scale,
+                               void* workspace, size_t workspace_bytes, void* stream) {
+  if (N <= 0 || K <= 0 || K % 16 != 0 || K > fp8_max_k() || N >= kMaxDim) return NVFP4_ERR_SHAPE;
+  if (!W || !q || !row_scale) return NVFP4_ERR_NULL;
+  if (!workspace || workspace_bytes < kWsHeader) return NVFP4_ERR_WORKSPACE;
+  if (!aligned(W, 16) || !aligned(q, 16) || !aligned(row_scale, 4) || !aligned(workspace, 256))
+    return NVFP4_ERR_ALIGN;
+  nvfp4_status st = check_device();
+  if (st != NVFP4_OK) return st;
+  return fp8_quantize_launch(W, N, K, q, row_scale, workspace, static_cast<cudaStream_t>(stream));
+}
+
+nvfp4_status fp8_refresh(const void* W, int64_t N, int64_t K, uint8_t* q, float* row_scale,
+                         void* workspace, size_t workspace_bytes, void* stream) {
+  // the same kernel into the same buffers: captured addresses stay valid
+  return fp8_quantize_rows(W, N, K, q, row_scale, workspace, workspace_bytes, stream);
+}
+
+// The activation quantizer of the W8A8 product holds a token row in one
+// 256-thread block: K <= 16384.
+static constexpr int64_t kW8MaxK = 16384;
+
+static nvfp4_status check_w8a8_shape(int64_t M, int64_t N, int64_t K) {
+  if (M < 0 || N < 0 || K < 256 || K % 256 != 0 || K > kW8MaxK || M >= kMaxDim || N >= kMaxDim)
+    return NVFP4_ERR_SHAPE;
+  return NVFP4_OK;
+}
+
+size_t w8a8_lm_head_workspace_bytes(int64_t M, int64_t N, int64_t K) {
+  if (check_w8a8_shape(M, N, K) != NVFP4_OK) return 0;
+  return w8a8_workspace_bytes(M, N, K, false);
+}
+
+nvfp4_status w8a8_lm_head(const void* x, int64_t M, int64_t K, const uint8_t* wq,
+                          const float* w_scale, int64_t N, void* logits, int out_dtype,
+                          void* workspace, size_t workspace_bytes, void* stream) {
+  nvfp4_status st = check_w8a8_shape(M, N, K);
+  if (st != NVFP4_OK) return st;
+  if (out_dtype != NVFP4_OUT_F32 && out_dtype != NVFP4_OUT_BF16) return NVFP4_ERR_DTYPE;
+  if (M == 0 || N == 0) return NVFP4_OK;
+  if (!x || !wq || !w_scale || !logits) return NVFP4_ERR_NULL;
+  if (!workspace || workspace_bytes < w8a8_workspace_bytes(M, N, K, false))
+    return NVFP4_ERR_WORKSPACE;
+  if (!aligned(x, 16) || !aligned(wq, 16) || !aligned(w_scale, 4) || !aligned(logits, 16) ||
+      !aligned(workspace, 256))
+    return NVFP4_ERR_ALIGN;
+  st = check_device();
+  if (st != NVFP4_OK) return st;
+  return w8a8_launch(x, M, K, wq, w_scale, N, logits, out_dtype, nullptr, nullptr, workspace,
+                     static_cast<cudaStream_t>(stream));
+}
+
+size_t w8a8_lm_head_argmax_workspace_bytes(int64_t M, int64_t N, int64_t K) {
+  if (check_w8a8_shape(M, N, K) != NVFP4_OK || N == 0) return 0;
+  return w8a8_workspace_bytes(M, N, K, true);
+}
+
+nvfp4_status w8a8_lm_head_argmax(const void* x, int64_t M, int64_t K, const uint8_t* wq,
+                                 const float* w_scale, int64_t N, int64_t* token_ids,
+                                 float* max_logits, void* workspace, size_t workspace_bytes,
+                                 void* stream) {
+  nvfp4_status st = check_w8a8_shape(M, N, K);
+  if (st != NVFP4_OK || N == 0) return NVFP4_ERR_SHAPE;
+  if (M == 0) return NVFP4_OK;
+  if (!x || !wq || !w_scale || !token_ids) return NVFP4_ERR_NULL;
+  if (!workspace || workspace_bytes < w8a8_workspace_bytes(M, N, K, true))
+    return NVFP4_ERR_WORKSPACE;
+  if (!aligned(x, 16) || !aligned(wq, 16) || !aligned(w_scale, 4) || !aligned(token_ids, 8) ||
+      !aligned(max_logits, 4) || !aligned(workspace, 256))
+    return NVFP4_ERR_ALIGN;
+  st = check_device();
+  if (st != NVFP4_OK) return st;
+  return w8a8_launch(x, M, K, wq, w_scale, N, nullptr, kOutArgmax, token_ids, max_logits,
+                     workspace, static_cast<cudaStream_t>(stream));
 }
 
 }  // extern "C"

@@ -156,6 +156,17 @@ __device__ __forceinline__ void tc_mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint
       : "memory");
 }
 
+// D (+)= A . B^T with A and B E4M3 in shared memory (kind::f8f6f4), K = 32.
+__device__ __forceinline__ void tc_mma_ss_f8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                             uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // Arrive on `bar` once every tcgen05.mma issued so far by this thread completes.
 __device__ __forceinline__ void tc_commit(uint64_t* bar) {
   asm volatile(
@@ -227,6 +238,16 @@ __host__ __device__ constexpr uint32_t idesc_f16_f32(uint32_t n) {
   return (1u << 4)             // D format: f32
          | (0u << 7)           // A format: f16
          | (0u << 10)          // B format: f16
+         | ((n >> 3) << 17)    // N / 8
+         | ((128u >> 4) << 24);  // M / 16
+}
+
+// Instruction descriptor of kind::f8f6f4: A and B E4M3 (format code 0), both
+// K-major, D fp32, M = 128, N = n.
+__host__ __device__ constexpr uint32_t idesc_e4m3_f32(uint32_t n) {
+  return (1u << 4)             // D format: f32
+         | (0u << 7)           // A format: E4M3
+         | (0u << 10)          // B format: E4M3
          | ((n >> 3) << 17)    // N / 8
          | ((128u >> 4) << 24);  // M / 16
 }

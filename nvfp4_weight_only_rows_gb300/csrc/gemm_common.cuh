@@ -1,0 +1,442 @@
+// gemm_common.cuh -- the parts of the persistent tcgen05 lm_head GEMMs that
+// the W4A16 (NVFP4 weights) and W8A8 (fp8 weights) products share: kernel
+// arguments, the unit schedule (strided whole units, then a stream-K tail),
+// bounded warp-level waits, the epilogue role (TMEM drain, per-token and
+// per-row scales, split-unit combine, logits stores or the fused greedy
+// argmax) and the host-side tensor-map and workspace helpers.
+//
+// A unit is 128 vocabulary rows x BN tokens; the MMA runs in the swapped
+// orientation D[row, token], so D lives in TMEM with one lane per row.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <mutex>
+
+#include "common.cuh"
+
+namespace nvfp4 {
+
+constexpr int kRows = 128;   // vocabulary rows per unit (MMA M)
+constexpr int kKB = 256;     // k per pipeline stage
+constexpr int kMaxBN = 128;  // largest token tile
+constexpr int kOutArgmax = 2;   // third output mode (after NVFP4_OUT_F32, NVFP4_OUT_BF16)
+constexpr int kKeyStride = 16;  // argmax: one 64-bit candidate per 128-byte line (spreads the atomics)
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per pipeline wait
+
+struct GemmArgs {
+  int64_t M, N, K;
+  int BN;              // token tile, multiple of 16, <= 128
+  int n_ttiles;        // token tiles
+  int64_t n_units;     // weight tiles x token tiles
+  int n_kb;            // 256-k stages per unit
+  uint32_t n_dp;       // whole units per CTA in strided waves (unit c + j * grid)
+  uint64_t tail_s0;    // first stage of the stream-K tail (unit-major, k-minor)
+  uint64_t tail_len;   // stages in the tail, split evenly over the grid
+  uint32_t tmem_cols;  // allocated TMEM columns
+  const float* tok_scale;
+  void* out;
+  int32_t* status;
+  uint32_t* split_cnt;    // [grid][4] arrivals at a split unit, per TMEM lane quadrant
+  uint32_t* split_ready;  // [grid][4] the first arriver's partial is in split_part
+  float* split_part;      // [grid][4][BN][32] fp32 partial accumulators
+  // greedy argmax output mode only
+  unsigned long long* am_keys;  // [m_pad * kKeyStride] per-token maxima (order key << 32 | ~n),
+                                // zeroed per call by the prep kernel
+  uint32_t* am_done;            // CTAs that have finished, zeroed per call
+  int64_t* am_idx;              // [M] result: vocabulary row of the largest logit
+  float* am_val;                // [M] result: that logit (may be null)
+  const float* row_scale;       // [N] per-row weight scale (fp8 weights), else null
+};
+
+// one lane of a converged warp (the lowest active lane)
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b32 r;\n\t"
+      "elect.sync r|p, 0xffffffff;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(pred));
+  return pred != 0;
+}
+
+// Before a producer warp exits, wait (bounded) until the last TMA load it
+// issued into each ring slot has landed, so no copy targets freed memory.
+__device__ __forceinline__ void drain_loads(uint64_t* full, uint32_t n_slots, uint32_t issued,
+                                            int /*arrivals*/, int32_t* status) {
+  volatile int32_t zero = 0;
+  WaitCtl drain{status, &zero, 100000000ull};
+  for (uint32_t s = 0; s < n_slots && s < issued; ++s) {
+    const uint32_t fills = issued / n_slots + (s < issued % n_slots ? 1u : 0u);
+    mbar_wait(&full[s], (fills - 1) & 1, drain);
+  }
+}
+
+// Wait until the preceding kernel in the stream (launched with programmatic
+// stream serialization) has completed and its writes are visible.
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Poll a global flag (acquire) until it is non-zero, at most the wait limit.
+// The writer is a CTA that has already announced itself, so this is short.
+__device__ __forceinline__ bool spin_until_set(const uint32_t* flag, const WaitCtl& w) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(flag) : "memory");
+  if (v) return __all_sync(0xFFFFFFFFu, true);
+  const uint64_t t0 = globaltimer_ns();
+  bool ok = true;
+  for (uint32_t it = 1;; ++it) {
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(flag) : "memory");
+    if (v) break;
+    if ((it & 63u) == 0 && globaltimer_ns() - t0 > w.limit_ns) {
+      raise_status(w.status, NVFP4_ERR_TIMEOUT);
+      *w.abort = 1;
+      ok = false;
+      break;
+    }
+  }
+  return __all_sync(0xFFFFFFFFu, ok);
+}
+
+// warp-uniform bounded wait: every lane polls, the warp agrees on the outcome
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const WaitCtl& wc) {
+  const bool ok = mbar_wait(bar, parity, wc);
+  return __all_sync(0xFFFFFFFFu, ok);
+}
+
+// ------------------------------------------------------------ greedy argmax
+// A logit's 32-bit order key: for the logits the epilogue forms (never -0;
+// a NaN only in the positive form the GPU's arithmetic produces) unsigned
+// order of keys is the order of values and every NaN is above +Inf.  A
+// candidate is key << 32 | ~n: the larger 64-bit word has the larger
+// logit, and of equal logits the smaller row.
+__device__ __forceinline__ uint32_t order_key(float v) {
+  const uint32_t b = __float_as_uint(v);
+  return b ^ ((uint32_t)((int32_t)b >> 31) | 0x80000000u);
+}
+
+// 16 consecutive floats of shared memory (16-byte aligned)
+__device__ __forceinline__ void lds_f32x16(const float* src, float (&d)[16]) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float4 f = reinterpret_cast<const float4*>(src)[i];
+    d[4 * i] = f.x;
+    d[4 * i + 1] = f.y;
+    d[4 * i + 2] = f.z;
+    d[4 * i + 3] = f.w;
+  }
+}
+
+__device__ __forceinline__ float key_value(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
+
+// ------------------------------------------------------------ schedule
+// A CTA's work is a list of pieces (a unit, or the part of a unit inside the
+// CTA's tail range): first n_dp whole units in strided waves (so that at any
+// time the CTAs stream neighbouring weight tiles and the same activation
+// stages), then an even share of the remaining units' stages (stream-K).
+// Every role walks the same list.
+struct Piece {
+  uint32_t u, kb0, kb1;
+};
+
+template <typename F>
+__device__ __forceinline__ void for_each_piece(const GemmArgs& p, F&& body) {
+  const uint32_t n_kb = (uint32_t)p.n_kb;
+  for (uint32_t j = 0; j < p.n_dp; ++j)
+    if (!body(Piece{blockIdx.x + j * gridDim.x, 0u, n_kb})) return;
+  const uint64_t t0 = p.tail_s0 + p.tail_len * blockIdx.x / gridDim.x;
+  const uint64_t t1 = p.tail_s0 + p.tail_len * (blockIdx.x + 1) / gridDim.x;
+  for (uint64_t s = t0; s < t1;) {
+    const uint32_t u = (uint32_t)(s / n_kb), kb0 = (uint32_t)(s - (uint64_t)u * n_kb);
+    const uint32_t kb1 = (uint32_t)(((uint64_t)kb0 + (t1 - s) < n_kb) ? kb0 + (t1 - s) : n_kb);
+    s += kb1 - kb0;
+    if (!body(Piece{u, kb0, kb1})) return;
+  }
+}
+
+__device__ __forceinline__ uint32_t cta_stages(const GemmArgs& p) {
+  const uint64_t t0 = p.tail_len * blockIdx.x / gridDim.x;
+  const uint64_t t1 = p.tail_len * (blockIdx.x + 1) / gridDim.x;
+  return (uint32_t)((uint64_t)p.n_dp * p.n_kb + (t1 - t0));
+}
+
+// ------------------------------------------------------------ epilogue
+// The epilogue role: four warps, warp % 4 = the TMEM lane quadrant it may
+// read, one thread per vocabulary row of the unit.  Per piece: the token
+// multipliers (and argmax thresholds) are fetched before the accumulator is
+// ready; then 16 tokens at a time are drained from TMEM, combined with the
+// other CTA's partial where a unit was split, scaled (token multiplier, then
+// the row's own scale for fp8 weights) and stored, or reduced to per-token
+// candidates (argmax).  `epi` is the warp's index among the four.
+template <int kOut, bool kRowScale>
+__device__ __forceinline__ void epilogue_role(const GemmArgs& p, int warp, int epi, int lane,
+                                              uint32_t tmem_base, uint64_t* d_full,
+                                              uint64_t* d_empty, const WaitCtl& wc,
+                                              float* s_tok, float* s_thr) {
+  grid_dependency_wait();  // token multipliers and split flags come from the prep kernel
+  const int BN = p.BN;
+  const int n_kb = p.n_kb;
+  const int q = warp & 3;
+  const int row = q * 32 + lane;
+  const uint32_t lane_off = (uint32_t)(q * 32) << 16;
+  float* tok = s_tok + epi * kMaxBN;
+  float* wthr = s_thr + epi * kMaxBN;
+  int64_t i = 0;
+  for_each_piece(p, [&](const Piece& pc) {
+    const uint32_t u = pc.u, kb0 = pc.kb0, kb1 = pc.kb1;
+    const uint32_t buf = (uint32_t)(i & 1), dph = (uint32_t)((i >> 1) & 1);
+    ++i;
+    const int64_t n = (int64_t)(u / p.n_ttiles) * kRows + row;
+    const int64_t t0 = (int64_t)(u % p.n_ttiles) * BN;
+    // Before the accumulators are ready: this unit's token multipliers,
+    // once per warp (written by the prep kernel, which may still have been
+    // running when this kernel started, so read coherently from L2, not
+    // the read-only path) and, for argmax, each token's current maximum
+    // as a threshold (a stale one is only lower; no candidate yet: -Inf;
+    // tokens past M: +Inf, nothing passes).
+    for (int t = lane; t < BN; t += 32) {
+      const bool live = t0 + t < p.M;
+      tok[t] = live ? __ldcg(p.tok_scale + t0 + t) : 0.0f;
+      if (kOut == kOutArgmax) {
+        const uint32_t kh =
+            live ? __ldcg(reinterpret_cast<const uint32_t*>(p.am_keys + (t0 + t) * kKeyStride) + 1)
+                 : 0u;
+        wthr[t] = !live ? __int_as_float(0x7F800000)
+                        : (kh ? key_value(kh) : __int_as_float(0xFF800000));
+      }
+    }
+    // the vocabulary row's own scale (fp8 weights), written before this grid began
+    const float rs = kRowScale ? (n < p.N ? __ldg(p.row_scale + n) : 0.0f) : 1.0f;
+    __syncwarp();
+    if (!warp_wait(&d_full[buf], dph, wc)) return false;
+    tc_fence_after();
+    // A tail unit cut by a range boundary: its two CTAs share slot `key`
+    // (the CTA whose tail range starts inside the unit).  The first to get here parks
+    // its fp32 partial; the second adds it to its own and stores logits.
+    // fp32 addition is commutative, so the result does not depend on which
+    // CTA comes second.
+    const bool whole = kb0 == 0 && kb1 == (uint32_t)n_kb;
+    bool finish = true;
+    float* part = nullptr;
+    uint32_t slot = 0;
+    if (!whole) {
+      const uint32_t key = kb0 == 0 ? blockIdx.x + 1 : blockIdx.x;
+      slot = key * 4 + q;
+      part = p.split_part + (size_t)slot * BN * 32;
+      uint32_t first = 0;
+      if (lane == 0) first = atomicAdd(p.split_cnt + slot, 1u) == 0u;
+      finish = __shfl_sync(0xFFFFFFFFu, first, 0) == 0u;
+      if (finish && !spin_until_set(p.split_ready + slot, wc)) finish = false;
+    }
+    for (int c = 0; c < BN; c += 16) {
+      uint32_t v[16];
+      tmem_ld16(tmem_base + lane_off + buf * BN + c, v);
+      tc_wait_ld();
+      if (!whole && !finish) {
+        // park this partial: token-major, so a warp's 32 rows are one line
+#pragma unroll
+        for (int t = 0; t < 16; ++t) part[(c + t) * 32 + lane] = __uint_as_float(v[t]);
+        continue;
+      }
+      if (!whole) {
+        // the other CTA's partial for these 16 tokens: all loads first, so
+        // they are in flight together (the logits stores below could alias)
+        float other[16];
+#pragma unroll
+        for (int t = 0; t < 16; ++t) other[t] = __ldcg(part + (c + t) * 32 + lane);
+#pragma unroll
+        for (int t = 0; t < 16; ++t)
+          v[t] = __float_as_uint(__fadd_rn(__uint_as_float(v[t]), other[t]));
+      }
+      if (kOut == kOutArgmax) {
+        // The logits as the plain product rounds them (the fma with +0
+        // rounds like the multiply and turns an exact -0 into +0), then one
+        // vote: does any row of this warp reach the threshold of its token
+        // (>=, so that ties and NaN reach the exact comparison)?  Only then,
+        // per such token, the warp finds its largest key and the lowest lane
+        // holding it and merges that candidate with one atomic maximum.
+        const bool valid = n < p.N;
+        const uint32_t n_base = (uint32_t)(n - lane);
+        float thr[16], mul[16], val[16];
+        lds_f32x16(wthr + c, thr);
+        lds_f32x16(tok + c, mul);
+        bool pass = false;
+#pragma unroll
+        for (int t = 0; t < 16; t += 2) {
+          float2 r = __ffma2_rn(make_float2(__uint_as_float(v[t]), __uint_as_float(v[t + 1])),
+                                make_float2(mul[t], mul[t + 1]), make_float2(0.0f, 0.0f));
+          if (kRowScale) r = __fmul2_rn(r, make_float2(rs, rs));
+          val[t] = r.x;
+          val[t + 1] = r.y;
+          pass |= !(r.x < thr[t]);
+          pass |= !(r.y < thr[t + 1]);
+        }
+        if (__any_sync(0xFFFFFFFFu, valid && pass)) {
+#pragma unroll
+          for (int t = 0; t < 16; ++t) {
+            if (__any_sync(0xFFFFFFFFu, valid && !(val[t] < thr[t]))) {
+              const uint32_t kk = valid ? order_key(val[t]) : 0u;
+              const uint32_t m = __reduce_max_sync(0xFFFFFFFFu, kk);
+              const uint32_t bal = __ballot_sync(0xFFFFFFFFu, valid && kk == m);
+              if (lane == 0)
+                atomicMax(p.am_keys + (t0 + c + t) * kKeyStride,
+                          ((unsigned long long)m << 32) |
+                              (uint32_t)~(n_base + (uint32_t)(__ffs(bal) - 1)));
+            }
+          }
+        }
+      } else if (n < p.N) {
+#pragma unroll
+        for (int t = 0; t < 16; ++t) {
+          const int64_t tok_i = t0 + c + t;
+          if (tok_i < p.M) {
+            float val = __fmul_rn(__uint_as_float(v[t]), tok[c + t]);
+            if (kRowScale) val = __fmul_rn(val, rs);
+            if (kOut == NVFP4_OUT_BF16)
+              reinterpret_cast<__nv_bfloat16*>(p.out)[tok_i * p.N + n] = __float2bfloat16_rn(val);
+            else
+              reinterpret_cast<float*>(p.out)[tok_i * p.N + n] = val;
+          }
+        }
+      }
+    }
+    if (!whole && !finish) {
+      __threadfence();  // the partial is visible before the flag
+      __syncwarp();
+      if (lane == 0) atomicExch(p.split_ready + slot, 1u);
+    }
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&d_empty[buf]);
+    return true;
+  });
+}
+
+// After every role of the CTA is done (call from all threads, after the
+// block barrier that follows the roles): the last CTA to finish turns the
+// per-token maxima into rows and values.
+__device__ __forceinline__ void argmax_finish(const GemmArgs& p, int first_epi_thread,
+                                              int32_t* s_last) {
+  // Every candidate of this CTA has been merged (the atomics precede the
+  // caller's barrier); the release-acquire counter orders the other CTAs'
+  // atomics before the last CTA's reads.
+  if ((int)threadIdx.x == first_epi_thread) {
+    uint32_t old;
+    asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], 1;"
+                 : "=r"(old) : "l"(p.am_done) : "memory");
+    *s_last = old == gridDim.x - 1 ? 1 : 0;
+  }
+  __syncthreads();
+  if (*s_last) {
+    for (int64_t t = threadIdx.x; t < p.M; t += blockDim.x) {
+      const unsigned long long k = __ldcg(p.am_keys + t * kKeyStride);
+      p.am_idx[t] = k != 0ull ? (int64_t)(uint32_t)~(uint32_t)k : (int64_t)-1;
+      if (p.am_val) p.am_val[t] = key_value((uint32_t)(k >> 32));
+    }
+  }
+}
+
+// ------------------------------------------------------------ host side
+static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
+}
+
+static bool encode_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64_t inner,
+                      uint64_t outer, uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer,
+                      CUtensorMapSwizzle swz) {
+  auto fn = tensor_map_encoder();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {row_bytes};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+static int lm_head_token_tile(int64_t M) {
+  if (M >= kMaxBN) return kMaxBN;
+  return (int)((M + 15) / 16 * 16);
+}
+
+static int sm_count() {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  return sms;
+}
+
+// Workspace layout of one call: [status header][activations as the MMA
+// reads them, m_pad x K x x_bytes (fp16: 2, e4m3: 1)]
+// [token multipliers, m_pad][split counters, grid x 4][split ready flags,
+// grid x 4] and, for argmax only, [CTAs done, 1]; these are zeroed by the
+// prep kernel's first CTA.  Then [split partials, grid x 4 x BN x 32 fp32]
+// and, for argmax only, [per-token maxima, m_pad x 128 bytes, one 64-bit
+// word used per line], each word zeroed by the prep CTA of its token.
+struct WsLayout {
+  size_t x16, tok, cnt, ready, done, keys, part, total;
+  int grid;
+};
+
+static WsLayout ws_layout(int64_t M, int64_t N, int64_t K, int sms, bool argmax, int x_bytes) {
+  WsLayout l;
+  const int BN = lm_head_token_tile(M);
+  const int64_t m_pad = (M + BN - 1) / BN * BN;
+  const int64_t n_units = ((N + kRows - 1) / kRows) * ((M + BN - 1) / BN);
+  l.grid = (int)std::max<int64_t>(1, std::min<int64_t>(sms, n_units));
+  l.x16 = kWsHeader;
+  l.tok = l.x16 + align_up((size_t)m_pad * K * x_bytes, 1024);
+  l.cnt = l.tok + align_up((size_t)m_pad * 4, 256);
+  l.ready = l.cnt + align_up((size_t)l.grid * 4 * 4, 256);
+  l.done = l.ready + align_up((size_t)l.grid * 4 * 4, 256);
+  l.part = l.done + (argmax ? 256 : 0);
+  l.keys = l.part + align_up((size_t)l.grid * 4 * BN * 32 * 4, 256);
+  l.total = l.keys + (argmax ? (size_t)m_pad * kKeyStride * 8 : 0);
+  return l;
+}
+
+// Split the units of a call into strided whole-unit waves and a stream-K
+// tail: all but the last one to two waves run whole; the rest is split
+// evenly, so every CTA's tail range holds at least one unit's stages and a
+// unit is cut at most once.
+static void schedule_units(GemmArgs& a, int64_t grid) {
+  const int64_t dp_waves = a.n_units >= 2 * grid ? a.n_units / grid - 1 : 0;
+  a.n_dp = (uint32_t)dp_waves;
+  a.tail_s0 = (uint64_t)(dp_waves * grid) * a.n_kb;
+  a.tail_len = (uint64_t)(a.n_units - dp_waves * grid) * a.n_kb;
+}
+
+// Launch configuration of a programmatic dependent launch.
+struct PdlLaunch {
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg;
+  PdlLaunch(dim3 grid, dim3 block, size_t smem, cudaStream_t stream) : cfg{} {
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
+};
+
+}  // namespace nvfp4

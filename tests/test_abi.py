@@ -33,7 +33,8 @@ def test_header_declares_the_boundary():
     for n in ("nvfp4_quantize_rows", "nvfp4_refresh", "w4a16_lm_head",
               "nvfp4_quantize_workspace_bytes", "w4a16_lm_head_workspace_bytes",
               "nvfp4_status_string", "nvfp4_read_device_status", "nvfp4_abi_version",
-              "w4a16_lm_head_argmax", "w4a16_lm_head_argmax_workspace_bytes"):
+              "w4a16_lm_head_argmax", "w4a16_lm_head_argmax_workspace_bytes",
+              "fp8_quantize_rows", "fp8_refresh", "w8a8_lm_head", "w8a8_lm_head_argmax"):
         assert n in names
 
 
@@ -94,6 +95,31 @@ def test_host_argument_errors_before_any_cuda_call(lib):
              None) == 2                                                              # ALIGN ids
     assert a(fake, 4, 256, fake, fake, fake, 8, ids, vp((1 << 21) + 2), fake, 1 << 30,
              None) == 2                                                              # ALIGN vals
+
+
+def test_fp8_host_argument_errors(lib):
+    vp = ctypes.c_void_p
+    fake = vp(1 << 20)
+    qz = lib.fp8_quantize_rows
+    assert qz(fake, 4, 24, fake, fake, fake, 1 << 20, None) == 1          # K % 16
+    assert qz(fake, 4, 65536 + 16, fake, fake, fake, 1 << 20, None) == 1  # K too large
+    assert qz(fake, 0, 32, fake, fake, fake, 1 << 20, None) == 1          # N == 0
+    assert qz(None, 4, 32, fake, fake, fake, 1 << 20, None) == 3          # NULL
+    assert qz(fake, 4, 32, fake, fake, fake, 16, None) == 4               # WORKSPACE
+    assert qz(fake, 4, 32, vp((1 << 20) + 4), fake, fake, 1 << 20, None) == 2  # ALIGN q
+    g = lib.w8a8_lm_head
+    assert g(fake, 4, 300, fake, fake, 8, fake, 0, fake, 1 << 30, None) == 1    # K % 256
+    assert g(fake, 4, 16640, fake, fake, 8, fake, 0, fake, 1 << 30, None) == 1  # K > 16384
+    assert g(fake, 4, 256, fake, fake, 8, fake, 9, fake, 1 << 30, None) == 5    # DTYPE
+    assert g(fake, 0, 256, fake, fake, 8, fake, 0, None, 0, None) == 0          # empty
+    assert g(fake, 4, 256, None, fake, 8, fake, 0, fake, 1 << 30, None) == 3    # NULL
+    assert g(fake, 4, 256, fake, fake, 8, fake, 0, fake, 64, None) == 4         # WORKSPACE
+    a = lib.w8a8_lm_head_argmax
+    assert a(fake, 4, 256, fake, fake, 0, fake, fake, fake, 1 << 30, None) == 1  # N == 0
+    assert a(fake, 4, 256, fake, fake, 8, None, fake, fake, 1 << 30, None) == 3  # NULL ids
+    assert lib.fp8_quantize_workspace_bytes(4, 32) == 256
+    assert lib.w8a8_lm_head_workspace_bytes(4, 8, 300) == 0
+    assert lib.w8a8_lm_head_argmax_workspace_bytes(4, 0, 256) == 0
 
 
 def test_argmax_workspace_sizes(lib):
