@@ -14,7 +14,9 @@ decode calls / their device time, CUDA events on the launching stream), the
 first clause of the headline metric; the prefill TFLOP/s and quantizer GB/s
 are reported beside it with their own roofline fractions.  The fused greedy
 argmax (each token's largest logit and its row, logits never stored) is
-timed call by call after the steps and reported under "argmax".
+timed call by call after the steps and reported under "argmax"; the fp8
+lm_head copy (refresh, W8A8 decode and prefill, its argmax) likewise under
+"fp8".
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -60,6 +62,16 @@ def decode_bytes(M: int, N: int = N_VOCAB, K: int = K_HID) -> int:
 def argmax_bytes(M: int, N: int = N_VOCAB, K: int = K_HID) -> int:
     """Algorithmic bytes of one fused-argmax call: packed + scales + x + (i64 id, f32 value)."""
     return N * K // 2 + N * K // 16 + 2 * M * K + 12 * M
+
+
+def fp8_quant_bytes(N: int = N_VOCAB, K: int = K_HID) -> int:
+    """fp8 copy: one read of W, the e4m3 codes and the row scales."""
+    return 2 * N * K + N * K + 4 * N
+
+
+def w8a8_bytes(M: int, N: int = N_VOCAB, K: int = K_HID) -> int:
+    """Algorithmic bytes of one W8A8 decode call: e4m3 W + row scales + x + fp32 logits."""
+    return N * K + 4 * N + 2 * M * K + 4 * M * N
 
 
 def quant_bytes(N: int = N_VOCAB, K: int = K_HID) -> int:
@@ -331,6 +343,22 @@ def run_ours(args, world, rank, local):
     g_pre_one = [capture(lambda c=c: nv.w4a16_lm_head(x_pre, *copies[c], out=out_pre,
                                                       workspace=gws)) for c in range(2)]
 
+    # the fp8 copy (per-row E4M3 weights, per-token E4M3 activations), each call alone
+    fws = torch.empty(nv.fp8_quantize_workspace_bytes(N, K), dtype=torch.uint8, device=dev)
+    f8 = [nv.fp8_quantize_rows(W[i], workspace=fws) for i in range(2)]
+    w8ws = torch.empty(max(nv.w8a8_lm_head_workspace_bytes(PREFILL_M, N, K),
+                           nv.w8a8_lm_head_argmax_workspace_bytes(PREFILL_M, N, K)),
+                       dtype=torch.uint8, device=dev)
+    g_f8q = [capture(lambda c=c: nv.fp8_refresh(W[c], *f8[c], workspace=fws)) for c in range(2)]
+    g_w8 = {M: [capture(lambda M=M, c=c: nv.w8a8_lm_head(x_dec[M], *f8[c], out=out_dec[M],
+                                                         workspace=w8ws)) for c in range(2)]
+            for M in DECODE_MS}
+    g_w8[PREFILL_M] = [capture(lambda c=c: nv.w8a8_lm_head(x_pre, *f8[c], out=out_pre,
+                                                           workspace=w8ws)) for c in range(2)]
+    g_w8am = {M: [capture(lambda M=M, c=c: nv.w8a8_lm_head_argmax(
+        x_am[M], *f8[c], token_ids=am_ids[M], max_logits=am_vals[M], workspace=w8ws))
+        for c in range(2)] for M in (64, PREFILL_M)}
+
     for s in range(args.warmup):
         step(s)
     torch.cuda.synchronize()
@@ -398,6 +426,9 @@ def run_ours(args, world, rank, local):
     per_call_dec = {M: per_call_us(g_one[M]) for M in DECODE_MS}  # us, each call alone
     per_call_am = {M: per_call_us(g_am[M]) for M in x_am}
     pre_alone_us = per_call_us(g_pre_one)
+    f8q_us = per_call_us(g_f8q)
+    w8_us = {M: per_call_us(g_w8[M]) for M in g_w8}
+    w8am_us = {M: per_call_us(g_w8am[M]) for M in g_w8am}
 
     def hbm_roof(name, gbs, tkey):
         return {"kernel": name, "bound": "hbm", "achieved": round(gbs, 1),
@@ -438,6 +469,27 @@ def run_ours(args, world, rank, local):
                                  str(PREFILL_M) + "_bf16": round(pre_alone_us, 2)},
         "rooflines": am_roofs,
     }
+    fp8_peak = 2.0 * peaks["bf16_tflops"]  # nominal fp8 : bf16 dense ratio (4.5 : 2.25 PF)
+    fp8_roofs = {"fp8_quantize": hbm_roof("fp8_quantize_kernel (refresh call)",
+                                          fp8_quant_bytes() / (f8q_us / 1e6) / 1e9, "fp8_quantize")}
+    for M in DECODE_MS:
+        fp8_roofs[f"w8a8_M{M}"] = hbm_roof(f"w8a8_lm_head M={M} alone (prep + tcgen05 f8f6f4 GEMM)",
+                                           w8a8_bytes(M) / (w8_us[M] / 1e6) / 1e9, f"w8a8_M{M}")
+    w8_tf = prefill_flops() / (w8_us[PREFILL_M] / 1e6) / 1e12
+    fp8_roofs[f"w8a8_M{PREFILL_M}"] = {
+        "kernel": f"w8a8_lm_head M={PREFILL_M} alone, bf16 logits", "bound": "tensor",
+        "achieved": round(w8_tf, 1), "peak": round(fp8_peak, 1), "unit": "TFLOP/s",
+        "frac": round(w8_tf / fp8_peak, 4), "traffic": traffic.get("w8a8_prefill"),
+        "peak_source": peaks["source"] + " dense bf16 burst x 2 (nominal fp8:bf16 ratio)"}
+    fp8_part = {
+        "what": "fp8 lm_head copy: per-row E4M3 weights, per-token E4M3 activations, W8A8 "
+                "product on kind::f8f6f4; each call alone from its own CUDA graph, not part "
+                "of the timed step",
+        "refresh_ms": round(f8q_us / 1e3, 4),
+        "us_per_call_alone": {str(M): round(v, 2) for M, v in w8_us.items()},
+        "argmax_us_per_call_alone": {str(M): round(v, 2) for M, v in w8am_us.items()},
+        "rooflines": fp8_roofs,
+    }
     times = {"quantize": t_quant, "prefill": t_pre, "decode": t_dec_all}
     dominant = max(times, key=times.get)
 
@@ -467,6 +519,7 @@ def run_ours(args, world, rank, local):
                 "what": "decode calls through w4a16_lm_head with x copied from pinned host memory "
                         "and logits copied back every call"},
         "argmax": argmax_part,
+        "fp8": fp8_part,
         "gpu_launches": launches_per_step * K_steps,
         "clocks": clock_info,
     }
@@ -558,6 +611,26 @@ def run_profile_case(case: str):
         return
     del W
     torch.cuda.empty_cache()
+    if case.startswith("fp8"):
+        W8 = up(synth.decode_weight(seed=1))
+        fws = torch.empty(nv.fp8_quantize_workspace_bytes(N, K), dtype=torch.uint8, device=dev)
+        q8, s8 = nv.fp8_quantize_rows(W8, workspace=fws)
+        if case == "fp8_quant":
+            for _ in range(4):
+                nv.fp8_refresh(W8, q8, s8, workspace=fws)
+            torch.cuda.synchronize()
+            return
+        del W8
+        M = PREFILL_M if case == "fp8_prefill" else int(case.replace("fp8_decode", ""))
+        x = up(synth.prefill_x()) if M == PREFILL_M else up(synth.decode_x(M))
+        out = torch.empty(M, N, dtype=torch.bfloat16 if M == PREFILL_M else torch.float32,
+                          device=dev)
+        w8ws = torch.empty(nv.w8a8_lm_head_workspace_bytes(M, N, K), dtype=torch.uint8,
+                           device=dev)
+        for _ in range(4):
+            nv.w8a8_lm_head(x, q8, s8, out=out, workspace=w8ws)
+        torch.cuda.synchronize()
+        return
     if case.startswith("argmax"):
         M = PREFILL_M if case == "argmax_prefill" else int(case.replace("argmax", ""))
         x = up(synth.prefill_x()) if M == PREFILL_M else up(synth.decode_x(M))
@@ -588,7 +661,8 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=15.0,
                     help="seconds of CPU work for the oracle baseline")
     ap.add_argument("--profile", choices=["decode1", "decode64", "prefill", "quant", "argmax1",
-                                          "argmax64", "argmax_prefill"],
+                                          "argmax64", "argmax_prefill", "fp8_quant",
+                                          "fp8_decode1", "fp8_decode64", "fp8_prefill"],
                     help="run one small fixed case for ncu instead of the benchmark")
     args = ap.parse_args()
     if args.profile:
