@@ -83,6 +83,8 @@ def _load():
         lib.oracle_dequant_rows.argtypes = [p, p, f, i64, p, i64, p]
         lib.oracle_logits_cols.argtypes = [p, i64, i64, p, p, f, p, i64, p]
         lib.oracle_e4m3_encode_array.argtypes = [p, i64, p]
+        lib.oracle_w4a4_logits_cols.argtypes = [p, i64, i64, f, p, p, f, p, i64, p]
+        lib.oracle_swizzle_scales.argtypes = [p, i64, i64, p]
         lib.oracle_fp8_quantize_rows.argtypes = [p, i64, i64, p, p]
         lib.oracle_fp8_quantize_rows.restype = ctypes.c_int
         lib.oracle_fp8_logits_cols.argtypes = [p, p, i64, i64, p, p, p, i64, p]
@@ -218,6 +220,33 @@ def logits(x: np.ndarray, packed: np.ndarray, scales: np.ndarray, g: float,
     out = np.zeros((M, cols.size), dtype=np.float64)
     _load().oracle_logits_cols(_ptr(x), M, K, _ptr(packed), _ptr(scales), g, _ptr(cols),
                                cols.size, _ptr(out))
+    return out
+
+
+def w4a4_logits(x: np.ndarray, gx: float, packed: np.ndarray, scales: np.ndarray, gw: float,
+                cols=None) -> np.ndarray:
+    """float64 logits[M, len(cols)] of the W4A4 product: x quantized to NVFP4 with
+    the input global gx (dequant multiplier), times the dequantized weight rows."""
+    x = np.ascontiguousarray(x, dtype=np.uint16)
+    packed = np.ascontiguousarray(packed, dtype=np.uint8)
+    scales = np.ascontiguousarray(scales, dtype=np.uint8)
+    M, K = x.shape
+    N = packed.shape[0]
+    cols = np.arange(N, dtype=np.int64) if cols is None else np.ascontiguousarray(cols, np.int64)
+    out = np.zeros((M, cols.size), dtype=np.float64)
+    _load().oracle_w4a4_logits_cols(_ptr(x), M, K, float(gx), _ptr(packed), _ptr(scales),
+                                    float(gw), _ptr(cols), cols.size, _ptr(out))
+    return out
+
+
+def swizzle_scales(scales: np.ndarray) -> np.ndarray:
+    """`swizzle_blockscale` of an [N, C] scale matrix: flat bytes, rows padded to 128,
+    columns to 4, in [N'/128][C'/4][32][4][4] order."""
+    scales = np.ascontiguousarray(scales, dtype=np.uint8)
+    N, C = scales.shape
+    Np, Cp = (N + 127) // 128 * 128, (C + 3) // 4 * 4
+    out = np.zeros(Np * Cp, dtype=np.uint8)
+    _load().oracle_swizzle_scales(_ptr(scales), N, C, _ptr(out))
     return out
 
 

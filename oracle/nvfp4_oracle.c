@@ -320,6 +320,66 @@ void oracle_logits_cols(const uint16_t *x, int64_t M, int64_t K, const uint8_t *
   }
 }
 
+/* ============================================================== W4A4 */
+/*
+ * W4A4 NVFP4 (`CompressedTensorsW4A4Fp4.apply_weights` on the page
+ * "vllm.model_executor.layers.quantization.compressed_tensors.schemes"):
+ * x is quantized per 16 values with the weight's rule against the
+ * per-tensor input global scale g_x (a dequant multiplier; its inverse is
+ * fl32(1/g_x)), and logits = (g_x * g_w) * sum e2m1*sf_x * e2m1*sf_w, here
+ * as the float64 sum of the dequantized operands' products.
+ */
+void oracle_w4a4_logits_cols(const uint16_t *x, int64_t M, int64_t K, float gx,
+                             const uint8_t *packed, const uint8_t *scales, float gw,
+                             const int64_t *cols, int64_t n_cols, double *out) {
+  const float igx = 1.0f / gx;
+  uint8_t *xp = (uint8_t *)malloc((size_t)M * (K / 2));
+  uint8_t *xs = (uint8_t *)malloc((size_t)M * (K / 16));
+  double *xd = (double *)malloc((size_t)M * K * sizeof(double));
+  for (int64_t m = 0; m < M; ++m) quantize_one_row(x + m * K, K, gx, igx, xp + m * (K / 2), xs + m * (K / 16));
+  int64_t *all = (int64_t *)malloc((size_t)M * sizeof(int64_t));
+  for (int64_t m = 0; m < M; ++m) all[m] = m;
+  oracle_dequant_rows(xp, xs, gx, K, all, M, xd);
+#pragma omp parallel
+  {
+    double *w = (double *)malloc((size_t)K * sizeof(double));
+#pragma omp for schedule(dynamic, 64)
+    for (int64_t j = 0; j < n_cols; ++j) {
+      oracle_dequant_rows(packed, scales, gw, K, &cols[j], 1, w);
+      for (int64_t m = 0; m < M; ++m) {
+        const double *xr = xd + m * K;
+        double acc = 0.0;
+        for (int64_t k = 0; k < K; ++k) acc += xr[k] * w[k];
+        out[m * n_cols + j] = acc;
+      }
+    }
+    free(w);
+  }
+  free(all);
+  free(xd);
+  free(xs);
+  free(xp);
+}
+
+/*
+ * `swizzle_blockscale` (same page): pad the [N, C] E4M3 block-scale matrix
+ * to rows a multiple of 128 and columns a multiple of 4, view it as
+ * [N'/128][4][32][C'/4][4] and store it in the order [N'/128][C'/4][32][4][4].
+ * Plain loops over the destination.
+ */
+void oracle_swizzle_scales(const uint8_t *scales, int64_t N, int64_t C, uint8_t *out) {
+  const int64_t Np = (N + 127) / 128 * 128, Cp = (C + 3) / 4 * 4;
+  int64_t o = 0;
+  for (int64_t i0 = 0; i0 < Np / 128; ++i0)
+    for (int64_t i4 = 0; i4 < Cp / 4; ++i4)
+      for (int64_t i3 = 0; i3 < 32; ++i3)
+        for (int64_t i2 = 0; i2 < 4; ++i2)
+          for (int64_t i5 = 0; i5 < 4; ++i5) {
+            const int64_t r = i0 * 128 + i2 * 32 + i3, c = i4 * 4 + i5;
+            out[o++] = (r < N && c < C) ? scales[r * C + c] : 0;
+          }
+}
+
 /* ============================================================ fp8 copy */
 /*
  * The "fp8" lm_head copy of the page
