@@ -292,6 +292,68 @@ nvfp4_status w8a8_lm_head_argmax(const void *x, int64_t M, int64_t K, const uint
                                  float *max_logits, void *workspace, size_t workspace_bytes,
                                  void *stream);
 
+/* ------------------------------------------------------- W4A4 NVFP4 */
+
+/*
+ * Bytes of the 128x4-interleaved copy of NVFP4 block scales of W[N, K]:
+ * round_up(N, 128) * K/16.  0 for rejected shapes (K % 64 != 0).
+ */
+size_t nvfp4_swizzled_scales_bytes(int64_t N, int64_t K);
+
+/*
+ * Re-lay row-major E4M3 block scales [N, K/16] (as nvfp4_quantize_rows writes
+ * them) into the order block-scaled FP4 tensor cores read, `swizzle_blockscale`
+ * on the page "vllm.model_executor.layers.quantization.compressed_tensors.
+ * schemes": rows padded to a multiple of 128 and columns (K/16, a multiple of
+ * 4 here) taken in 512-byte atoms of 128 rows x 4 columns, ordered
+ * [row / 128][column / 4]; inside an atom, row 32 a + b and column d sit at
+ * byte b * 16 + a * 4 + d.  Padding rows are zero.
+ *   scales  u8 [N, K/16], device, 4-byte aligned.  K % 64 == 0.
+ *   out     u8, device, 16-byte aligned, nvfp4_swizzled_scales_bytes(N, K).
+ * Run it after every nvfp4_quantize_rows / nvfp4_refresh that the W4A4
+ * product will read.
+ */
+nvfp4_status nvfp4_swizzle_scales(const uint8_t *scales, int64_t N, int64_t K, uint8_t *out,
+                                  void *stream);
+
+/* Workspace bytes of w4a4_lm_head (x as NVFP4 codes and interleaved scales,
+ * alpha per token, status, split-K partials); 0 for rejected shapes. */
+size_t w4a4_lm_head_workspace_bytes(int64_t M, int64_t N, int64_t K);
+
+/*
+ * The W4A4 NVFP4 product (`CompressedTensorsW4A4Fp4.apply_weights` on the
+ * page "...compressed_tensors.schemes"; alpha as `maybe_fuse_global_scales`
+ * on "vllm/model_executor/layers/quantization/modelopt.py"): x is quantized
+ * inside the call to NVFP4 with the weight's rule (per 16 values an E4M3
+ * scale e4m3(min(vmax / 6 / input_global_scale, 448)), E2M1 codes of
+ * x / (scale * input_global_scale), ties to even), then
+ *   logits[m, n] = fl32(acc[m, n] * alpha),  alpha = fl32(input_global_scale * global_scale),
+ * acc the fp32 tensor-core sum of the block-scaled E2M1 products (each exact).
+ *   x                   bf16 [M, K], device, 16-byte aligned; K % 256 == 0.
+ *   packed, global_scale  as nvfp4_quantize_rows writes them for W[N, K].
+ *   scales_swizzled     nvfp4_swizzle_scales of that call's scales.
+ *   input_global_scale  f32 [1], device: the activation dequant multiplier
+ *                       (amax_x / 2688 for a calibrated amax_x; positive and
+ *                       finite, else NVFP4_ERR_NONFINITE in the status word).
+ *   logits              [M, N] fp32 or bf16, device, 16-byte aligned.
+ *   workspace           >= w4a4_lm_head_workspace_bytes(M, N, K), 256-byte aligned.
+ */
+nvfp4_status w4a4_lm_head(const void *x, int64_t M, int64_t K, const uint8_t *packed,
+                          const uint8_t *scales_swizzled, const float *global_scale,
+                          const float *input_global_scale, int64_t N, void *logits,
+                          int out_dtype, void *workspace, size_t workspace_bytes, void *stream);
+
+/* Workspace bytes of w4a4_lm_head_argmax (0 for rejected shapes, N == 0 included). */
+size_t w4a4_lm_head_argmax_workspace_bytes(int64_t M, int64_t N, int64_t K);
+
+/* The greedy argmax of the W4A4 logits, fused (semantics of
+ * w4a16_lm_head_argmax; the logits are those w4a4_lm_head writes in fp32). */
+nvfp4_status w4a4_lm_head_argmax(const void *x, int64_t M, int64_t K, const uint8_t *packed,
+                                 const uint8_t *scales_swizzled, const float *global_scale,
+                                 const float *input_global_scale, int64_t N, int64_t *token_ids,
+                                 float *max_logits, void *workspace, size_t workspace_bytes,
+                                 void *stream);
+
 /* ------------------------------------------- allocation-free variant */
 
 /* Size of the fixed device scratch array behind w4a16_lm_head_noalloc. */

@@ -23,6 +23,10 @@ Entry points (same names as the C ABI):
   ``fp8_refresh`` -- the "fp8" copy of ``quantized_lm_head_copy`` (per-row
   scales); ``w8a8_lm_head(x, q, row_scale)`` / ``w8a8_lm_head_argmax`` -- its
   product with per-token fp8 activations on the fp8 tensor cores.
+* ``nvfp4_swizzle_scales(scales)`` and ``w4a4_lm_head(x, packed, scales_swizzled,
+  global_scale, input_global_scale)`` / ``w4a4_lm_head_argmax`` -- the W4A4 NVFP4
+  product (``CompressedTensorsW4A4Fp4``): x quantized to NVFP4 in the call,
+  block-scaled FP4 tensor cores, logits scaled by alpha = g_x * g_w.
 """
 from __future__ import annotations
 
@@ -40,6 +44,8 @@ __all__ = [
     "w4a16_lm_head_argmax_workspace_bytes", "fp8_quantize_rows", "fp8_refresh",
     "fp8_quantize_workspace_bytes", "w8a8_lm_head", "w8a8_lm_head_argmax",
     "w8a8_lm_head_workspace_bytes", "w8a8_lm_head_argmax_workspace_bytes",
+    "nvfp4_swizzle_scales", "nvfp4_swizzled_scales_bytes", "w4a4_lm_head",
+    "w4a4_lm_head_argmax", "w4a4_lm_head_workspace_bytes", "w4a4_lm_head_argmax_workspace_bytes",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -120,6 +126,18 @@ def load_library() -> ctypes.CDLL:
     lib.w8a8_lm_head.restype = st
     lib.w8a8_lm_head_argmax.argtypes = [vp, i64, i64, vp, vp, i64, vp, vp, vp, sz, vp]
     lib.w8a8_lm_head_argmax.restype = st
+    lib.nvfp4_swizzled_scales_bytes.argtypes = [i64, i64]
+    lib.nvfp4_swizzled_scales_bytes.restype = sz
+    lib.nvfp4_swizzle_scales.argtypes = [vp, i64, i64, vp, vp]
+    lib.nvfp4_swizzle_scales.restype = st
+    for name in ("w4a4_lm_head_workspace_bytes", "w4a4_lm_head_argmax_workspace_bytes"):
+        f = getattr(lib, name)
+        f.argtypes = [i64, i64, i64]
+        f.restype = sz
+    lib.w4a4_lm_head.argtypes = [vp, i64, i64, vp, vp, vp, vp, i64, vp, ctypes.c_int, vp, sz, vp]
+    lib.w4a4_lm_head.restype = st
+    lib.w4a4_lm_head_argmax.argtypes = [vp, i64, i64, vp, vp, vp, vp, i64, vp, vp, vp, sz, vp]
+    lib.w4a4_lm_head_argmax.restype = st
     lib.w4a16_lm_head_noalloc.argtypes = [vp, i64, i64, vp, vp, vp, i64, vp, ctypes.c_int, vp]
     lib.w4a16_lm_head_noalloc.restype = st
     lib.nvfp4_selftest_bounded_wait.argtypes = [vp, sz, i64, vp]
@@ -373,6 +391,95 @@ def w8a8_lm_head_argmax(x: torch.Tensor, q: torch.Tensor, row_scale: torch.Tenso
                                  _ptr(max_logits), _ptr(workspace),
                                  workspace.numel() * workspace.element_size(), _stream(stream))
     _check(rc, "w8a8_lm_head_argmax")
+    return token_ids, max_logits
+
+
+def nvfp4_swizzled_scales_bytes(N: int, K: int) -> int:
+    return int(load_library().nvfp4_swizzled_scales_bytes(N, K))
+
+
+def w4a4_lm_head_workspace_bytes(M: int, N: int, K: int) -> int:
+    return int(load_library().w4a4_lm_head_workspace_bytes(M, N, K))
+
+
+def w4a4_lm_head_argmax_workspace_bytes(M: int, N: int, K: int) -> int:
+    return int(load_library().w4a4_lm_head_argmax_workspace_bytes(M, N, K))
+
+
+def nvfp4_swizzle_scales(scales: torch.Tensor, out: torch.Tensor | None = None,
+                         stream=None) -> torch.Tensor:
+    """Row-major E4M3 block scales [N, K/16] -> the 128x4-interleaved copy (u8, flat)."""
+    lib = load_library()
+    N, C = scales.shape
+    K = C * 16
+    _need(scales, scales.dtype, "scales")
+    nbytes = nvfp4_swizzled_scales_bytes(N, K)
+    if out is None:
+        out = torch.empty(nbytes, dtype=torch.uint8, device=scales.device)
+    if out.numel() * out.element_size() < nbytes:
+        raise ValueError(f"out must hold {nbytes} bytes")
+    _check(lib.nvfp4_swizzle_scales(_ptr(scales), N, K, _ptr(out), _stream(stream)),
+           "nvfp4_swizzle_scales")
+    return out
+
+
+def _w4a4_args(x, packed, scales_swizzled, global_scale, input_global_scale):
+    _need(x, torch.bfloat16, "x")
+    M, K = x.shape
+    N = packed.shape[0]
+    _need(packed, torch.uint8, "packed", (N, K // 2))
+    _need(scales_swizzled, torch.uint8, "scales_swizzled")
+    if scales_swizzled.numel() < nvfp4_swizzled_scales_bytes(N, K):
+        raise ValueError("scales_swizzled is smaller than nvfp4_swizzled_scales_bytes(N, K)")
+    _need(global_scale, torch.float32, "global_scale")
+    _need(input_global_scale, torch.float32, "input_global_scale")
+    return M, K, N
+
+
+def w4a4_lm_head(x: torch.Tensor, packed: torch.Tensor, scales_swizzled: torch.Tensor,
+                 global_scale: torch.Tensor, input_global_scale: torch.Tensor,
+                 out: torch.Tensor | None = None, out_dtype: torch.dtype = torch.float32,
+                 workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """W4A4 NVFP4 logits[M, N]: x quantized to NVFP4 with input_global_scale."""
+    lib = load_library()
+    M, K, N = _w4a4_args(x, packed, scales_swizzled, global_scale, input_global_scale)
+    if out is None:
+        out = torch.empty(M, N, dtype=out_dtype, device=x.device)
+    _need(out, out.dtype, "out", (M, N))
+    code = {torch.float32: OUT_F32, torch.bfloat16: OUT_BF16}.get(out.dtype)
+    if code is None:
+        raise ValueError("out must be float32 or bfloat16")
+    if workspace is None:
+        workspace = _workspace(w4a4_lm_head_workspace_bytes(M, N, K), x.device)
+    rc = lib.w4a4_lm_head(_ptr(x), M, K, _ptr(packed), _ptr(scales_swizzled), _ptr(global_scale),
+                          _ptr(input_global_scale), N, _ptr(out), code, _ptr(workspace),
+                          workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(rc, "w4a4_lm_head")
+    return out
+
+
+def w4a4_lm_head_argmax(x: torch.Tensor, packed: torch.Tensor, scales_swizzled: torch.Tensor,
+                        global_scale: torch.Tensor, input_global_scale: torch.Tensor,
+                        token_ids: torch.Tensor | None = None,
+                        max_logits: torch.Tensor | None = None, with_values: bool = True,
+                        workspace: torch.Tensor | None = None, stream=None):
+    """Greedy argmax of the W4A4 logits without storing them."""
+    lib = load_library()
+    M, K, N = _w4a4_args(x, packed, scales_swizzled, global_scale, input_global_scale)
+    if token_ids is None:
+        token_ids = torch.empty(M, dtype=torch.int64, device=x.device)
+    _need(token_ids, torch.int64, "token_ids", (M,))
+    if max_logits is None and with_values:
+        max_logits = torch.empty(M, dtype=torch.float32, device=x.device)
+    if max_logits is not None:
+        _need(max_logits, torch.float32, "max_logits", (M,))
+    if workspace is None:
+        workspace = _workspace(w4a4_lm_head_argmax_workspace_bytes(M, N, K), x.device)
+    rc = lib.w4a4_lm_head_argmax(_ptr(x), M, K, _ptr(packed), _ptr(scales_swizzled),
+                                 _ptr(global_scale), _ptr(input_global_scale), N, _ptr(token_ids),
+                                 _ptr(max_logits), _ptr(workspace),
+                                 workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(rc, "w4a4_lm_head_argmax")
     return token_ids, max_logits
 
 

@@ -19,6 +19,14 @@ nvfp4_status lm_head_launch(const void* x, int64_t M, int64_t K, const uint8_t* 
                             void* workspace, cudaStream_t stream);
 constexpr int kOutArgmax = 2;  // lm_head_launch's third output mode
 int64_t fp8_max_k();
+size_t nvfp4_swizzled_scales_size(int64_t N, int64_t K);
+nvfp4_status swizzle_scales_launch(const uint8_t* scales, int64_t N, int64_t K, uint8_t* out,
+                                   cudaStream_t stream);
+size_t w4a4_workspace_bytes(int64_t M, int64_t N, int64_t K, bool argmax);
+nvfp4_status w4a4_launch(const void* x, int64_t M, int64_t K, const uint8_t* packed,
+                         const uint8_t* wsf, const float* g_w, const float* g_in, int64_t N,
+                         void* logits, int out_mode, int64_t* token_ids, float* max_logits,
+                         void* workspace, cudaStream_t stream);
 nvfp4_status fp8_quantize_launch(const void* W, int64_t N, int64_t K, uint8_t* q,
                                  float* row_scale, void* workspace, cudaStream_t stream);
 size_t w8a8_workspace_bytes(int64_t M, int64_t N, int64_t K, bool argmax);
@@ -249,6 +257,91 @@ nvfp4_status w8a8_lm_head_argmax(const void* x, int64_t M, int64_t K, const uint
   if (st != NVFP4_OK) return st;
   return w8a8_launch(x, M, K, wq, w_scale, N, nullptr, kOutArgmax, token_ids, max_logits,
                      workspace, static_cast<cudaStream_t>(stream));
+}
+
+/* ------------------------------------------------------------ W4A4 */
+
+size_t nvfp4_swizzled_scales_bytes(int64_t N, int64_t K) {
+  if (N <= 0 || K <= 0 || K % 64 != 0 || N >= kMaxDim || K >= kMaxDim) return 0;
+  return nvfp4_swizzled_scales_size(N, K);
+}
+
+nvfp4_status nvfp4_swizzle_scales(const uint8_t* scales, int64_t N, int64_t K, uint8_t* out,
+                                  void* stream) {
+  if (N <= 0 || K <= 0 || K % 64 != 0 || N >= kMaxDim || K >= kMaxDim) return NVFP4_ERR_SHAPE;
+  if (!scales || !out) return NVFP4_ERR_NULL;
+  if (!aligned(scales, 4) || !aligned(out, 16)) return NVFP4_ERR_ALIGN;
+  nvfp4_status st = check_device();
+  if (st != NVFP4_OK) return st;
+  return swizzle_scales_launch(scales, N, K, out, static_cast<cudaStream_t>(stream));
+}
+
+static nvfp4_status check_w4a4_shape(int64_t M, int64_t N, int64_t K) {
+  if (M < 0 || N < 0 || K < 256 || K % 256 != 0 || M >= kMaxDim || N >= kMaxDim || K >= kMaxDim)
+    return NVFP4_ERR_SHAPE;
+  return NVFP4_OK;
+}
+
+size_t w4a4_lm_head_workspace_bytes(int64_t M, int64_t N, int64_t K) {
+  if (check_w4a4_shape(M, N, K) != NVFP4_OK) return 0;
+  return w4a4_workspace_bytes(M, N, K, false);
+}
+
+size_t w4a4_lm_head_argmax_workspace_bytes(int64_t M, int64_t N, int64_t K) {
+  if (check_w4a4_shape(M, N, K) != NVFP4_OK || N == 0) return 0;
+  return w4a4_workspace_bytes(M, N, K, true);
+}
+
+static nvfp4_status check_w4a4_ptrs(const void* x, const uint8_t* packed,
+                                    const uint8_t* scales_swizzled, const float* global_scale,
+                                    const float* input_global_scale, const void* workspace) {
+  if (!x || !packed || !scales_swizzled || !global_scale || !input_global_scale)
+    return NVFP4_ERR_NULL;
+  if (!aligned(x, 16) || !aligned(packed, 16) || !aligned(scales_swizzled, 16) ||
+      !aligned(global_scale, 4) || !aligned(input_global_scale, 4) || !aligned(workspace, 256))
+    return NVFP4_ERR_ALIGN;
+  return NVFP4_OK;
+}
+
+nvfp4_status w4a4_lm_head(const void* x, int64_t M, int64_t K, const uint8_t* packed,
+                          const uint8_t* scales_swizzled, const float* global_scale,
+                          const float* input_global_scale, int64_t N, void* logits,
+                          int out_dtype, void* workspace, size_t workspace_bytes, void* stream) {
+  nvfp4_status st = check_w4a4_shape(M, N, K);
+  if (st != NVFP4_OK) return st;
+  if (out_dtype != NVFP4_OUT_F32 && out_dtype != NVFP4_OUT_BF16) return NVFP4_ERR_DTYPE;
+  if (M == 0 || N == 0) return NVFP4_OK;
+  if (!logits) return NVFP4_ERR_NULL;
+  if (!workspace || workspace_bytes < w4a4_workspace_bytes(M, N, K, false))
+    return NVFP4_ERR_WORKSPACE;
+  st = check_w4a4_ptrs(x, packed, scales_swizzled, global_scale, input_global_scale, workspace);
+  if (st != NVFP4_OK) return st;
+  if (!aligned(logits, 16)) return NVFP4_ERR_ALIGN;
+  st = check_device();
+  if (st != NVFP4_OK) return st;
+  return w4a4_launch(x, M, K, packed, scales_swizzled, global_scale, input_global_scale, N, logits,
+                     out_dtype, nullptr, nullptr, workspace, static_cast<cudaStream_t>(stream));
+}
+
+nvfp4_status w4a4_lm_head_argmax(const void* x, int64_t M, int64_t K, const uint8_t* packed,
+                                 const uint8_t* scales_swizzled, const float* global_scale,
+                                 const float* input_global_scale, int64_t N, int64_t* token_ids,
+                                 float* max_logits, void* workspace, size_t workspace_bytes,
+                                 void* stream) {
+  nvfp4_status st = check_w4a4_shape(M, N, K);
+  if (st != NVFP4_OK || N == 0) return NVFP4_ERR_SHAPE;
+  if (M == 0) return NVFP4_OK;
+  if (!token_ids) return NVFP4_ERR_NULL;
+  if (!workspace || workspace_bytes < w4a4_workspace_bytes(M, N, K, true))
+    return NVFP4_ERR_WORKSPACE;
+  st = check_w4a4_ptrs(x, packed, scales_swizzled, global_scale, input_global_scale, workspace);
+  if (st != NVFP4_OK) return st;
+  if (!aligned(token_ids, 8) || !aligned(max_logits, 4)) return NVFP4_ERR_ALIGN;
+  st = check_device();
+  if (st != NVFP4_OK) return st;
+  return w4a4_launch(x, M, K, packed, scales_swizzled, global_scale, input_global_scale, N,
+                     nullptr, kOutArgmax, token_ids, max_logits, workspace,
+                     static_cast<cudaStream_t>(stream));
 }
 
 }  // extern "C"

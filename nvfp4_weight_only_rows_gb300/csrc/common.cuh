@@ -124,6 +124,36 @@ __device__ __forceinline__ uint64_t policy_evict_last() {
   return p;
 }
 
+// ------------------------------------------------------------ NVFP4 codes
+// 8 fp32 values -> 8 E2M1 codes in one word (byte j: value 2j low nibble,
+// value 2j+1 high nibble), round to nearest even, saturating at +-6.
+__device__ __forceinline__ uint32_t cvt_e2m1x8(const float (&q)[8]) {
+  uint32_t w;
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n\t"
+      "mov.b32 %0, {b0, b1, b2, b3};\n\t}"
+      : "=r"(w)
+      : "f"(q[0]), "f"(q[1]), "f"(q[2]), "f"(q[3]), "f"(q[4]), "f"(q[5]), "f"(q[6]), "f"(q[7]));
+  // a code whose magnitude is zero carries no sign: 0x8 -> 0x0 per nibble
+  const uint32_t mag = w & 0x77777777u;
+  const uint32_t nonzero = (mag + 0x77777777u) & 0x88888888u;
+  return mag | (w & nonzero);
+}
+
+// One-dimensional bulk copy global -> shared, completing on `bar` (both
+// addresses 16-byte aligned, bytes a multiple of 16).
+__device__ __forceinline__ void bulk_load(void* smem_dst, const void* src, uint32_t bytes,
+                                          uint64_t* bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint "
+      "[%0], [%1], %2, [%3], %4;" ::"r"(smem_u32(smem_dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+
 // ------------------------------------------------------------ tcgen05
 __device__ __forceinline__ void tmem_alloc(uint32_t* smem_result, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -164,6 +194,33 @@ __device__ __forceinline__ void tc_mma_ss_f8(uint32_t d_tmem, uint64_t a_desc, u
       "setp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Copy 32 rows x 16 bytes of shared memory (four 8-row core matrices, 128
+// bytes apart, no swizzle) into 4 TMEM columns of lanes 0-31, repeated in
+// each of the four lane quadrants.
+__device__ __forceinline__ void tc_cp_32x128b_x4(uint32_t taddr, uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
+  d |= (uint64_t)(128 >> 4) << 16;  // leading byte offset (one 16-byte column: unused)
+  d |= (uint64_t)(128 >> 4) << 32;  // stride byte offset: 8 rows x 16 B
+  d |= (uint64_t)1 << 46;           // descriptor version
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(d) : "memory");
+}
+
+// D (+)= (A . sfA) (B . sfB)^T with A and B E2M1 in shared memory and one
+// UE4M3 scale per 16 values of K (kind::mxf4nvf4, scale_vec::4X), K = 64.
+// sfa / sfb: TMEM addresses of the 4 scale columns of this K step.
+__device__ __forceinline__ void tc_mma_fp4_bs(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                              uint32_t idesc, uint32_t sfa, uint32_t sfb,
+                                              uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X "
+      "[%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
       : "memory");
 }
 
@@ -239,6 +296,17 @@ __host__ __device__ constexpr uint32_t idesc_f16_f32(uint32_t n) {
          | (0u << 7)           // A format: f16
          | (0u << 10)          // B format: f16
          | ((n >> 3) << 17)    // N / 8
+         | ((128u >> 4) << 24);  // M / 16
+}
+
+// Instruction descriptor of the block-scaled kind::mxf4nvf4: A and B E2M1
+// (format code 1), K-major, UE4M3 scales (scale format 0), scale ids 0,
+// D fp32, M = 128, N = n.
+__host__ __device__ constexpr uint32_t idesc_e2m1_bs(uint32_t n) {
+  return (1u << 7)             // A format: E2M1
+         | (1u << 10)          // B format: E2M1
+         | ((n >> 3) << 17)    // N / 8
+         | (0u << 23)          // scale format: UE4M3
          | ((128u >> 4) << 24);  // M / 16
 }
 

@@ -91,24 +91,6 @@ __global__ void __launch_bounds__(kAmaxThreads) nvfp4_amax_kernel(const uint4* _
   }
 }
 
-// 8 fp32 values -> 8 E2M1 codes in one word (byte j: value 2j low nibble,
-// value 2j+1 high nibble), round to nearest even, saturating at +-6.
-__device__ __forceinline__ uint32_t cvt_e2m1x8(const float (&q)[8]) {
-  uint32_t w;
-  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
-      "cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n\t"
-      "cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n\t"
-      "cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n\t"
-      "cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n\t"
-      "mov.b32 %0, {b0, b1, b2, b3};\n\t}"
-      : "=r"(w)
-      : "f"(q[0]), "f"(q[1]), "f"(q[2]), "f"(q[3]), "f"(q[4]), "f"(q[5]), "f"(q[6]), "f"(q[7]));
-  // a code whose magnitude is zero carries no sign: 0x8 -> 0x0 per nibble
-  const uint32_t mag = w & 0x77777777u;
-  const uint32_t nonzero = (mag + 0x77777777u) & 0x88888888u;
-  return mag | (w & nonzero);
-}
-
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
 

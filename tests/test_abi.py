@@ -34,7 +34,8 @@ def test_header_declares_the_boundary():
               "nvfp4_quantize_workspace_bytes", "w4a16_lm_head_workspace_bytes",
               "nvfp4_status_string", "nvfp4_read_device_status", "nvfp4_abi_version",
               "w4a16_lm_head_argmax", "w4a16_lm_head_argmax_workspace_bytes",
-              "fp8_quantize_rows", "fp8_refresh", "w8a8_lm_head", "w8a8_lm_head_argmax"):
+              "fp8_quantize_rows", "fp8_refresh", "w8a8_lm_head", "w8a8_lm_head_argmax",
+              "nvfp4_swizzle_scales", "w4a4_lm_head", "w4a4_lm_head_argmax"):
         assert n in names
 
 
@@ -120,6 +121,25 @@ def test_fp8_host_argument_errors(lib):
     assert lib.fp8_quantize_workspace_bytes(4, 32) == 256
     assert lib.w8a8_lm_head_workspace_bytes(4, 8, 300) == 0
     assert lib.w8a8_lm_head_argmax_workspace_bytes(4, 0, 256) == 0
+
+
+def test_w4a4_host_argument_errors(lib):
+    vp = ctypes.c_void_p
+    fake = vp(1 << 20)
+    sw = lib.nvfp4_swizzle_scales
+    assert sw(fake, 4, 48, fake, None) == 1                      # K % 64
+    assert sw(None, 4, 64, fake, None) == 3                      # NULL
+    assert sw(fake, 4, 64, vp((1 << 20) + 4), None) == 2         # ALIGN out
+    assert lib.nvfp4_swizzled_scales_bytes(130, 128) == 256 * 8
+    g = lib.w4a4_lm_head
+    assert g(fake, 4, 300, fake, fake, fake, fake, 8, fake, 0, fake, 1 << 30, None) == 1  # K
+    assert g(fake, 4, 256, fake, fake, fake, fake, 8, fake, 3, fake, 1 << 30, None) == 5  # DTYPE
+    assert g(fake, 0, 256, fake, fake, fake, fake, 8, fake, 0, None, 0, None) == 0       # empty
+    assert g(fake, 4, 256, fake, fake, fake, None, 8, fake, 0, fake, 1 << 30, None) == 3  # NULL gx
+    assert g(fake, 4, 256, fake, fake, fake, fake, 8, fake, 0, fake, 64, None) == 4     # WORKSPACE
+    a = lib.w4a4_lm_head_argmax
+    assert a(fake, 4, 256, fake, fake, fake, fake, 0, fake, fake, fake, 1 << 30, None) == 1  # N 0
+    assert lib.w4a4_lm_head_argmax_workspace_bytes(4, 0, 256) == 0
 
 
 def test_argmax_workspace_sizes(lib):
