@@ -16,7 +16,7 @@ are reported beside it with their own roofline fractions.  The fused greedy
 argmax (each token's largest logit and its row, logits never stored) is
 timed call by call after the steps and reported under "argmax"; the fp8
 lm_head copy (refresh, W8A8 decode and prefill, its argmax) likewise under
-"fp8".
+"fp8", and the W4A4 NVFP4 product under "w4a4".
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -355,6 +355,25 @@ def run_ours(args, world, rank, local):
             for M in DECODE_MS}
     g_w8[PREFILL_M] = [capture(lambda c=c: nv.w8a8_lm_head(x_pre, *f8[c], out=out_pre,
                                                            workspace=w8ws)) for c in range(2)]
+    # W4A4 NVFP4 (x quantized to NVFP4 in the call, block-scaled FP4 tensor cores);
+    # the input global is x's amax / 2688, standing in for a calibrated value
+    sw4 = [nv.nvfp4_swizzle_scales(copies[i][1].view(torch.uint8)) for i in range(2)]
+    gx4 = {M: torch.tensor([max(float(xx.float().abs().max()) / 2688.0, 1e-12)],
+                           dtype=torch.float32, device=dev) for M, xx in x_am.items()}
+    w4ws = torch.empty(max(nv.w4a4_lm_head_workspace_bytes(PREFILL_M, N, K),
+                           nv.w4a4_lm_head_argmax_workspace_bytes(PREFILL_M, N, K)),
+                       dtype=torch.uint8, device=dev)
+    g_w4 = {M: [capture(lambda M=M, c=c: nv.w4a4_lm_head(
+        x_dec[M], copies[c][0], sw4[c], copies[c][2], gx4[M], out=out_dec[M], workspace=w4ws))
+        for c in range(2)] for M in DECODE_MS}
+    g_w4[PREFILL_M] = [capture(lambda c=c: nv.w4a4_lm_head(
+        x_pre, copies[c][0], sw4[c], copies[c][2], gx4[PREFILL_M], out=out_pre, workspace=w4ws))
+        for c in range(2)]
+    g_w4am = {M: [capture(lambda M=M, c=c: nv.w4a4_lm_head_argmax(
+        x_am[M], copies[c][0], sw4[c], copies[c][2], gx4[M], token_ids=am_ids[M],
+        max_logits=am_vals[M], workspace=w4ws)) for c in range(2)] for M in (64, PREFILL_M)}
+    g_sw4 = [capture(lambda c=c: nv.nvfp4_swizzle_scales(copies[c][1].view(torch.uint8),
+                                                         out=sw4[c])) for c in range(2)]
     g_w8am = {M: [capture(lambda M=M, c=c: nv.w8a8_lm_head_argmax(
         x_am[M], *f8[c], token_ids=am_ids[M], max_logits=am_vals[M], workspace=w8ws))
         for c in range(2)] for M in (64, PREFILL_M)}
@@ -429,6 +448,9 @@ def run_ours(args, world, rank, local):
     f8q_us = per_call_us(g_f8q)
     w8_us = {M: per_call_us(g_w8[M]) for M in g_w8}
     w8am_us = {M: per_call_us(g_w8am[M]) for M in g_w8am}
+    w4_us = {M: per_call_us(g_w4[M]) for M in g_w4}
+    w4am_us = {M: per_call_us(g_w4am[M]) for M in g_w4am}
+    sw4_us = per_call_us(g_sw4)
 
     def hbm_roof(name, gbs, tkey):
         return {"kernel": name, "bound": "hbm", "achieved": round(gbs, 1),
@@ -490,6 +512,26 @@ def run_ours(args, world, rank, local):
         "argmax_us_per_call_alone": {str(M): round(v, 2) for M, v in w8am_us.items()},
         "rooflines": fp8_roofs,
     }
+    fp4_peak = 6.0 * peaks["bf16_tflops"]  # nominal fp4 : bf16 dense ratio (13.5 : 2.25 PF)
+    w4_roofs = {}
+    for M in DECODE_MS:
+        w4_roofs[f"w4a4_M{M}"] = hbm_roof(f"w4a4_lm_head M={M} alone (prep + tcgen05 mxf4nvf4 GEMM)",
+                                          decode_bytes(M) / (w4_us[M] / 1e6) / 1e9, f"w4a4_M{M}")
+    w4_tf = prefill_flops() / (w4_us[PREFILL_M] / 1e6) / 1e12
+    w4_roofs[f"w4a4_M{PREFILL_M}"] = {
+        "kernel": f"w4a4_lm_head M={PREFILL_M} alone, bf16 logits", "bound": "tensor",
+        "achieved": round(w4_tf, 1), "peak": round(fp4_peak, 1), "unit": "TFLOP/s",
+        "frac": round(w4_tf / fp4_peak, 4), "traffic": traffic.get("w4a4_prefill"),
+        "peak_source": peaks["source"] + " dense bf16 burst x 6 (nominal fp4:bf16 ratio)"}
+    w4a4_part = {
+        "what": "W4A4 NVFP4: x quantized to NVFP4 in the call (input global = amax(x)/2688), "
+                "block-scaled FP4 tensor cores (kind::mxf4nvf4); each call alone from its own "
+                "CUDA graph, not part of the timed step",
+        "swizzle_scales_us": round(sw4_us, 2),
+        "us_per_call_alone": {str(M): round(v, 2) for M, v in w4_us.items()},
+        "argmax_us_per_call_alone": {str(M): round(v, 2) for M, v in w4am_us.items()},
+        "rooflines": w4_roofs,
+    }
     times = {"quantize": t_quant, "prefill": t_pre, "decode": t_dec_all}
     dominant = max(times, key=times.get)
 
@@ -520,6 +562,7 @@ def run_ours(args, world, rank, local):
                         "and logits copied back every call"},
         "argmax": argmax_part,
         "fp8": fp8_part,
+        "w4a4": w4a4_part,
         "gpu_launches": launches_per_step * K_steps,
         "clocks": clock_info,
     }
@@ -611,6 +654,19 @@ def run_profile_case(case: str):
         return
     del W
     torch.cuda.empty_cache()
+    if case.startswith("w4a4"):
+        M = PREFILL_M if case == "w4a4_prefill" else int(case.replace("w4a4_decode", ""))
+        x = up(synth.prefill_x()) if M == PREFILL_M else up(synth.decode_x(M))
+        sw = nv.nvfp4_swizzle_scales(scales.view(torch.uint8))
+        gx = torch.tensor([max(float(x.float().abs().max()) / 2688.0, 1e-12)], device=dev)
+        out = torch.empty(M, N, dtype=torch.bfloat16 if M == PREFILL_M else torch.float32,
+                          device=dev)
+        w4ws = torch.empty(nv.w4a4_lm_head_workspace_bytes(M, N, K), dtype=torch.uint8,
+                           device=dev)
+        for _ in range(4):
+            nv.w4a4_lm_head(x, packed, sw, g, gx, out=out, workspace=w4ws)
+        torch.cuda.synchronize()
+        return
     if case.startswith("fp8"):
         W8 = up(synth.decode_weight(seed=1))
         fws = torch.empty(nv.fp8_quantize_workspace_bytes(N, K), dtype=torch.uint8, device=dev)
@@ -662,7 +718,8 @@ def main():
                     help="seconds of CPU work for the oracle baseline")
     ap.add_argument("--profile", choices=["decode1", "decode64", "prefill", "quant", "argmax1",
                                           "argmax64", "argmax_prefill", "fp8_quant",
-                                          "fp8_decode1", "fp8_decode64", "fp8_prefill"],
+                                          "fp8_decode1", "fp8_decode64", "fp8_prefill",
+                                          "w4a4_decode1", "w4a4_decode64", "w4a4_prefill"],
                     help="run one small fixed case for ncu instead of the benchmark")
     args = ap.parse_args()
     if args.profile:
