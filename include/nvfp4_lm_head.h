@@ -292,6 +292,38 @@ nvfp4_status w8a8_lm_head_argmax(const void *x, int64_t M, int64_t K, const uint
                                  float *max_logits, void *workspace, size_t workspace_bytes,
                                  void *stream);
 
+/* ----------------------------------------------- grouped W4A16 (MoE) */
+
+/* Workspace bytes of w4a16_grouped_gemm; 0 for rejected shapes. */
+size_t w4a16_grouped_workspace_bytes(int64_t M, int64_t N, int64_t K, int64_t n_groups);
+
+/*
+ * The NVFP4 W4A16 product of a mixture-of-experts layer, all experts in one
+ * call (the `w13 [E, 2I, H/2]` / `w2 [E, H, I/2]` layouts of
+ * `ModelOptNvFp4FusedMoE.create_weights` on the page
+ * "vllm/model_executor/layers/quantization/modelopt.py", with one global
+ * scale per expert as its `w13_weight_scale_2` / `w2_weight_scale_2`):
+ *   out[m, n] = global[e] * sum_k x[m, k] * e2m1(code[e, n, k]) * f32(scale[e, n, k/16])
+ * for every token row m of group e, group_offsets[e] <= m < group_offsets[e + 1].
+ *   x              bf16 [M, K], device: token rows already grouped by expert
+ *                  (routing and the final combine are the caller's).  K % 256 == 0.
+ *   group_offsets  int32 [n_groups + 1], device, non-decreasing, [0] = 0,
+ *                  [n_groups] = M (rows outside [0, M) are never read or
+ *                  written).  Read by the kernels, never by the host: the call
+ *                  can be captured in a CUDA graph whatever the routing.
+ *   n_groups       experts, 1 <= n_groups <= 256.
+ *   packed, scales u8 [n_groups, N, K/2] and [n_groups, N, K/16], each expert as
+ *                  nvfp4_quantize_rows writes it; 16-byte aligned.
+ *   global_scales  f32 [n_groups], device: each expert's global scale.
+ *   out            [M, N] fp32 or bf16, device, 16-byte aligned.
+ *   workspace      >= w4a16_grouped_workspace_bytes(M, N, K, n_groups), 256-byte aligned.
+ * Accumulation and accuracy as w4a16_lm_head.
+ */
+nvfp4_status w4a16_grouped_gemm(const void *x, int64_t M, int64_t K, const int32_t *group_offsets,
+                                int64_t n_groups, const uint8_t *packed, const uint8_t *scales,
+                                const float *global_scales, int64_t N, void *out, int out_dtype,
+                                void *workspace, size_t workspace_bytes, void *stream);
+
 /* ------------------------------------------------------- W4A4 NVFP4 */
 
 /*

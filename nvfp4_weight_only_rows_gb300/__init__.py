@@ -27,6 +27,9 @@ Entry points (same names as the C ABI):
   global_scale, input_global_scale)`` / ``w4a4_lm_head_argmax`` -- the W4A4 NVFP4
   product (``CompressedTensorsW4A4Fp4``): x quantized to NVFP4 in the call,
   block-scaled FP4 tensor cores, logits scaled by alpha = g_x * g_w.
+* ``w4a16_grouped_gemm(x, group_offsets, packed, scales, global_scales)`` -- the
+  NVFP4 W4A16 product of all experts of a MoE layer in one call, tokens grouped
+  by expert (``ModelOptNvFp4FusedMoE`` weight layouts).
 """
 from __future__ import annotations
 
@@ -46,6 +49,7 @@ __all__ = [
     "w8a8_lm_head_workspace_bytes", "w8a8_lm_head_argmax_workspace_bytes",
     "nvfp4_swizzle_scales", "nvfp4_swizzled_scales_bytes", "w4a4_lm_head",
     "w4a4_lm_head_argmax", "w4a4_lm_head_workspace_bytes", "w4a4_lm_head_argmax_workspace_bytes",
+    "w4a16_grouped_gemm", "w4a16_grouped_workspace_bytes",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -138,6 +142,11 @@ def load_library() -> ctypes.CDLL:
     lib.w4a4_lm_head.restype = st
     lib.w4a4_lm_head_argmax.argtypes = [vp, i64, i64, vp, vp, vp, vp, i64, vp, vp, vp, sz, vp]
     lib.w4a4_lm_head_argmax.restype = st
+    lib.w4a16_grouped_workspace_bytes.argtypes = [i64, i64, i64, i64]
+    lib.w4a16_grouped_workspace_bytes.restype = sz
+    lib.w4a16_grouped_gemm.argtypes = [vp, i64, i64, vp, i64, vp, vp, vp, i64, vp, ctypes.c_int,
+                                       vp, sz, vp]
+    lib.w4a16_grouped_gemm.restype = st
     lib.w4a16_lm_head_noalloc.argtypes = [vp, i64, i64, vp, vp, vp, i64, vp, ctypes.c_int, vp]
     lib.w4a16_lm_head_noalloc.restype = st
     lib.nvfp4_selftest_bounded_wait.argtypes = [vp, sz, i64, vp]
@@ -481,6 +490,40 @@ def w4a4_lm_head_argmax(x: torch.Tensor, packed: torch.Tensor, scales_swizzled: 
                                  workspace.numel() * workspace.element_size(), _stream(stream))
     _check(rc, "w4a4_lm_head_argmax")
     return token_ids, max_logits
+
+
+def w4a16_grouped_workspace_bytes(M: int, N: int, K: int, n_groups: int) -> int:
+    return int(load_library().w4a16_grouped_workspace_bytes(M, N, K, n_groups))
+
+
+def w4a16_grouped_gemm(x: torch.Tensor, group_offsets: torch.Tensor, packed: torch.Tensor,
+                       scales: torch.Tensor, global_scales: torch.Tensor,
+                       out: torch.Tensor | None = None, out_dtype: torch.dtype = torch.float32,
+                       workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """out[M, N] = each token row times its expert's NVFP4 weight: x bf16[M, K]
+    grouped by expert (group_offsets int32[E + 1]), packed u8[E, N, K/2],
+    scales e4m3[E, N, K/16], global_scales f32[E]."""
+    lib = load_library()
+    _need(x, torch.bfloat16, "x")
+    M, K = x.shape
+    E, N = packed.shape[0], packed.shape[1]
+    _need(group_offsets, torch.int32, "group_offsets", (E + 1,))
+    _need(packed, torch.uint8, "packed", (E, N, K // 2))
+    _need(scales, scales.dtype, "scales", (E, N, K // 16))
+    _need(global_scales, torch.float32, "global_scales", (E,))
+    if out is None:
+        out = torch.empty(M, N, dtype=out_dtype, device=x.device)
+    _need(out, out.dtype, "out", (M, N))
+    code = {torch.float32: OUT_F32, torch.bfloat16: OUT_BF16}.get(out.dtype)
+    if code is None:
+        raise ValueError("out must be float32 or bfloat16")
+    if workspace is None:
+        workspace = _workspace(w4a16_grouped_workspace_bytes(M, N, K, E), x.device)
+    rc = lib.w4a16_grouped_gemm(_ptr(x), M, K, _ptr(group_offsets), E, _ptr(packed), _ptr(scales),
+                                _ptr(global_scales), N, _ptr(out), code, _ptr(workspace),
+                                workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(rc, "w4a16_grouped_gemm")
+    return out
 
 
 def w4a16_lm_head_noalloc(x: torch.Tensor, packed: torch.Tensor, scales: torch.Tensor,

@@ -19,6 +19,12 @@ nvfp4_status lm_head_launch(const void* x, int64_t M, int64_t K, const uint8_t* 
                             void* workspace, cudaStream_t stream);
 constexpr int kOutArgmax = 2;  // lm_head_launch's third output mode
 int64_t fp8_max_k();
+size_t grouped_workspace_bytes(int64_t M, int64_t N, int64_t K, int64_t n_groups);
+nvfp4_status grouped_launch(const void* x, int64_t M, int64_t K, const int32_t* grp_off,
+                            int64_t n_groups, const uint8_t* packed, const uint8_t* scales,
+                            const float* grp_global, int64_t N, void* out, int out_dtype,
+                            void* workspace, cudaStream_t stream);
+constexpr int64_t kMaxGroupsApi = 256;
 size_t nvfp4_swizzled_scales_size(int64_t N, int64_t K);
 nvfp4_status swizzle_scales_launch(const uint8_t* scales, int64_t N, int64_t K, uint8_t* out,
                                    cudaStream_t stream);
@@ -257,6 +263,41 @@ nvfp4_status w8a8_lm_head_argmax(const void* x, int64_t M, int64_t K, const uint
   if (st != NVFP4_OK) return st;
   return w8a8_launch(x, M, K, wq, w_scale, N, nullptr, kOutArgmax, token_ids, max_logits,
                      workspace, static_cast<cudaStream_t>(stream));
+}
+
+/* --------------------------------------------------------- grouped (MoE) */
+
+static nvfp4_status check_grouped_shape(int64_t M, int64_t N, int64_t K, int64_t n_groups) {
+  if (M < 0 || N < 0 || K < 256 || K % 256 != 0 || n_groups < 1 || n_groups > kMaxGroupsApi ||
+      M >= kMaxDim || N >= kMaxDim || K >= kMaxDim || n_groups * N >= kMaxDim)
+    return NVFP4_ERR_SHAPE;
+  return NVFP4_OK;
+}
+
+size_t w4a16_grouped_workspace_bytes(int64_t M, int64_t N, int64_t K, int64_t n_groups) {
+  if (check_grouped_shape(M, N, K, n_groups) != NVFP4_OK) return 0;
+  return grouped_workspace_bytes(M, N, K, n_groups);
+}
+
+nvfp4_status w4a16_grouped_gemm(const void* x, int64_t M, int64_t K, const int32_t* group_offsets,
+                                int64_t n_groups, const uint8_t* packed, const uint8_t* scales,
+                                const float* global_scales, int64_t N, void* out, int out_dtype,
+                                void* workspace, size_t workspace_bytes, void* stream) {
+  nvfp4_status st = check_grouped_shape(M, N, K, n_groups);
+  if (st != NVFP4_OK) return st;
+  if (out_dtype != NVFP4_OUT_F32 && out_dtype != NVFP4_OUT_BF16) return NVFP4_ERR_DTYPE;
+  if (M == 0 || N == 0) return NVFP4_OK;
+  if (!x || !group_offsets || !packed || !scales || !global_scales || !out) return NVFP4_ERR_NULL;
+  if (!workspace || workspace_bytes < grouped_workspace_bytes(M, N, K, n_groups))
+    return NVFP4_ERR_WORKSPACE;
+  if (!aligned(x, 16) || !aligned(packed, 16) || !aligned(scales, 16) ||
+      !aligned(group_offsets, 4) || !aligned(global_scales, 4) || !aligned(out, 16) ||
+      !aligned(workspace, 256))
+    return NVFP4_ERR_ALIGN;
+  st = check_device();
+  if (st != NVFP4_OK) return st;
+  return grouped_launch(x, M, K, group_offsets, n_groups, packed, scales, global_scales, N, out,
+                        out_dtype, workspace, static_cast<cudaStream_t>(stream));
 }
 
 /* ------------------------------------------------------------ W4A4 */

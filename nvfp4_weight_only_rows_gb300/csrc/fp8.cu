@@ -274,7 +274,7 @@ __global__ void __launch_bounds__(kW8Threads, 1)
     mbar_wait(done_bar, 0, drain);
   } else {
     // ---------------- epilogue: token scale, then the row's own scale
-    epilogue_role<kOut, true>(p, warp, warp - kW8FirstEpiWarp, lane, tmem_base, d_full, d_empty,
+    epilogue_role<kOut, true>(p, plain_sched(p), warp, warp - kW8FirstEpiWarp, lane, tmem_base, d_full, d_empty,
                               wc, s_tok, s_thr);
   }
 

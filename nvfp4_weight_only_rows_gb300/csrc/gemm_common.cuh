@@ -49,7 +49,92 @@ struct GemmArgs {
   int64_t* am_idx;              // [M] result: vocabulary row of the largest logit
   float* am_val;                // [M] result: that logit (may be null)
   const float* row_scale;       // [N] per-row weight scale (fp8 weights), else null
+  // grouped product (experts) only
+  const int32_t* grp_off;       // [n_groups + 1] token row offsets of the groups
+  const float* grp_global;      // [n_groups] per-group weight global scale
+  int n_groups;
 };
+
+constexpr int kMaxGroups = 256;  // experts of one grouped call
+
+// The schedule of a call.  For the plain product it comes from the host
+// (GemmArgs); for the grouped product every CTA derives it on the device
+// from the group offsets (shared memory), so the host never reads them.
+struct Sched {
+  uint32_t n_dp;      // whole units per CTA in strided waves
+  uint32_t grid;      // CTAs that take part (blockIdx.x >= grid: no work)
+  uint64_t tail_s0;   // first stage of the stream-K tail
+  uint64_t tail_len;  // stages in the tail
+  uint32_t nt;        // grouped: weight tiles per group
+  const uint32_t* unit_pre;  // grouped: [n_groups + 1] prefix of units per group (shared)
+  const int32_t* off;        // grouped: [n_groups + 1] token row offsets (shared)
+};
+
+__device__ __forceinline__ Sched plain_sched(const GemmArgs& p) {
+  return Sched{p.n_dp, gridDim.x, p.tail_s0, p.tail_len, 0u, nullptr, nullptr};
+}
+
+// Where a unit lives: its first weight row (the TMA coordinate), first
+// output column, token rows [t0, t_end) of its group, and whether its
+// weight tile is read by more than one token tile.
+struct UnitGeom {
+  int64_t w_row, n0, t0, t_end;
+  bool reused;
+};
+
+template <bool kGrouped>
+__device__ __forceinline__ UnitGeom unit_geom(const GemmArgs& p, const Sched& s, uint32_t u) {
+  UnitGeom g;
+  if constexpr (!kGrouped) {
+    g.n0 = g.w_row = (int64_t)(u / p.n_ttiles) * kRows;
+    g.t0 = (int64_t)(u % p.n_ttiles) * p.BN;
+    g.t_end = p.M;
+    g.reused = p.n_ttiles > 1;
+  } else {
+    int lo = 0, hi = p.n_groups;  // the group e with unit_pre[e] <= u < unit_pre[e + 1]
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (s.unit_pre[mid] <= u) lo = mid; else hi = mid;
+    }
+    const uint32_t local = u - s.unit_pre[lo];
+    const uint32_t ttc = (s.unit_pre[lo + 1] - s.unit_pre[lo]) / s.nt;  // token tiles of group lo
+    const uint32_t wt = local / ttc, tt = local % ttc;
+    g.n0 = (int64_t)wt * kRows;
+    g.w_row = (int64_t)lo * p.N + g.n0;
+    g.t0 = s.off[lo] + (int64_t)tt * p.BN;
+    g.t_end = s.off[lo + 1] < p.M ? s.off[lo + 1] : p.M;
+    g.reused = ttc > 1;
+  }
+  return g;
+}
+
+// Grouped product: derive the schedule from the group offsets (thread 0,
+// before the block barrier that publishes it; the other threads read it
+// after).  Units of group e: weight tiles x ceil(tokens_e / BN).
+__device__ __forceinline__ void grouped_sched_build(const GemmArgs& p, Sched* s, uint32_t* unit_pre,
+                                                    int32_t* off, uint32_t n_kb) {
+  const uint32_t nt = (uint32_t)((p.N + kRows - 1) / kRows);
+  uint32_t acc = 0;
+  int32_t prev = 0;
+  for (int e = 0; e <= p.n_groups; ++e) {
+    int32_t o = p.grp_off[e];
+    o = o < prev ? prev : (o > p.M ? (int32_t)p.M : o);  // clamp to a monotone range in [0, M]
+    off[e] = o;
+    if (e > 0) acc += nt * (uint32_t)((o - prev + p.BN - 1) / p.BN);
+    unit_pre[e] = acc;
+    prev = o;
+  }
+  const uint32_t n_units = acc;
+  const uint32_t grid = n_units < gridDim.x ? n_units : gridDim.x;
+  const uint32_t dp = (grid > 0 && n_units >= 2 * grid) ? n_units / grid - 1 : 0;
+  s->n_dp = dp;
+  s->grid = grid;
+  s->tail_s0 = (uint64_t)dp * grid * n_kb;
+  s->tail_len = (uint64_t)(n_units - dp * grid) * n_kb;
+  s->nt = nt;
+  s->unit_pre = unit_pre;
+  s->off = off;
+}
 
 // one lane of a converged warp (the lowest active lane)
 __device__ __forceinline__ bool elect_one() {
@@ -145,12 +230,12 @@ struct Piece {
 };
 
 template <typename F>
-__device__ __forceinline__ void for_each_piece(const GemmArgs& p, F&& body) {
-  const uint32_t n_kb = (uint32_t)p.n_kb;
-  for (uint32_t j = 0; j < p.n_dp; ++j)
-    if (!body(Piece{blockIdx.x + j * gridDim.x, 0u, n_kb})) return;
-  const uint64_t t0 = p.tail_s0 + p.tail_len * blockIdx.x / gridDim.x;
-  const uint64_t t1 = p.tail_s0 + p.tail_len * (blockIdx.x + 1) / gridDim.x;
+__device__ __forceinline__ void for_each_piece(const Sched& sc, uint32_t n_kb, F&& body) {
+  if (blockIdx.x >= sc.grid) return;
+  for (uint32_t j = 0; j < sc.n_dp; ++j)
+    if (!body(Piece{blockIdx.x + j * sc.grid, 0u, n_kb})) return;
+  const uint64_t t0 = sc.tail_s0 + sc.tail_len * blockIdx.x / sc.grid;
+  const uint64_t t1 = sc.tail_s0 + sc.tail_len * (blockIdx.x + 1) / sc.grid;
   for (uint64_t s = t0; s < t1;) {
     const uint32_t u = (uint32_t)(s / n_kb), kb0 = (uint32_t)(s - (uint64_t)u * n_kb);
     const uint32_t kb1 = (uint32_t)(((uint64_t)kb0 + (t1 - s) < n_kb) ? kb0 + (t1 - s) : n_kb);
@@ -159,10 +244,16 @@ __device__ __forceinline__ void for_each_piece(const GemmArgs& p, F&& body) {
   }
 }
 
-__device__ __forceinline__ uint32_t cta_stages(const GemmArgs& p) {
-  const uint64_t t0 = p.tail_len * blockIdx.x / gridDim.x;
-  const uint64_t t1 = p.tail_len * (blockIdx.x + 1) / gridDim.x;
-  return (uint32_t)((uint64_t)p.n_dp * p.n_kb + (t1 - t0));
+template <typename F>
+__device__ __forceinline__ void for_each_piece(const GemmArgs& p, F&& body) {
+  for_each_piece(plain_sched(p), (uint32_t)p.n_kb, body);
+}
+
+__device__ __forceinline__ uint32_t cta_stages(const Sched& sc, uint32_t n_kb) {
+  if (blockIdx.x >= sc.grid) return 0;
+  const uint64_t t0 = sc.tail_len * blockIdx.x / sc.grid;
+  const uint64_t t1 = sc.tail_len * (blockIdx.x + 1) / sc.grid;
+  return (uint32_t)((uint64_t)sc.n_dp * n_kb + (t1 - t0));
 }
 
 // ------------------------------------------------------------ epilogue
@@ -173,9 +264,9 @@ __device__ __forceinline__ uint32_t cta_stages(const GemmArgs& p) {
 // other CTA's partial where a unit was split, scaled (token multiplier, then
 // the row's own scale for fp8 weights) and stored, or reduced to per-token
 // candidates (argmax).  `epi` is the warp's index among the four.
-template <int kOut, bool kRowScale>
-__device__ __forceinline__ void epilogue_role(const GemmArgs& p, int warp, int epi, int lane,
-                                              uint32_t tmem_base, uint64_t* d_full,
+template <int kOut, bool kRowScale, bool kGrouped = false>
+__device__ __forceinline__ void epilogue_role(const GemmArgs& p, const Sched& sc, int warp, int epi,
+                                              int lane, uint32_t tmem_base, uint64_t* d_full,
                                               uint64_t* d_empty, const WaitCtl& wc,
                                               float* s_tok, float* s_thr) {
   grid_dependency_wait();  // token multipliers and split flags come from the prep kernel
@@ -187,12 +278,14 @@ __device__ __forceinline__ void epilogue_role(const GemmArgs& p, int warp, int e
   float* tok = s_tok + epi * kMaxBN;
   float* wthr = s_thr + epi * kMaxBN;
   int64_t i = 0;
-  for_each_piece(p, [&](const Piece& pc) {
+  for_each_piece(sc, (uint32_t)n_kb, [&](const Piece& pc) {
     const uint32_t u = pc.u, kb0 = pc.kb0, kb1 = pc.kb1;
     const uint32_t buf = (uint32_t)(i & 1), dph = (uint32_t)((i >> 1) & 1);
     ++i;
-    const int64_t n = (int64_t)(u / p.n_ttiles) * kRows + row;
-    const int64_t t0 = (int64_t)(u % p.n_ttiles) * BN;
+    const UnitGeom geo = unit_geom<kGrouped>(p, sc, u);
+    const int64_t n = geo.n0 + row;
+    const int64_t t0 = geo.t0;
+    const int64_t t_end = geo.t_end;
     // Before the accumulators are ready: this unit's token multipliers,
     // once per warp (written by the prep kernel, which may still have been
     // running when this kernel started, so read coherently from L2, not
@@ -200,7 +293,7 @@ __device__ __forceinline__ void epilogue_role(const GemmArgs& p, int warp, int e
     // as a threshold (a stale one is only lower; no candidate yet: -Inf;
     // tokens past M: +Inf, nothing passes).
     for (int t = lane; t < BN; t += 32) {
-      const bool live = t0 + t < p.M;
+      const bool live = t0 + t < t_end;
       tok[t] = live ? __ldcg(p.tok_scale + t0 + t) : 0.0f;
       if (kOut == kOutArgmax) {
         const uint32_t kh =
@@ -294,7 +387,7 @@ __device__ __forceinline__ void epilogue_role(const GemmArgs& p, int warp, int e
 #pragma unroll
         for (int t = 0; t < 16; ++t) {
           const int64_t tok_i = t0 + c + t;
-          if (tok_i < p.M) {
+          if (tok_i < t_end) {
             float val = __fmul_rn(__uint_as_float(v[t]), tok[c + t]);
             if (kRowScale) val = __fmul_rn(val, rs);
             if (kOut == NVFP4_OUT_BF16)

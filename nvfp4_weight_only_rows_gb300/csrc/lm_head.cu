@@ -75,7 +75,10 @@ __global__ void __launch_bounds__(256) w4a16_prep_x_kernel(const uint16_t* __res
                                                            int32_t* __restrict__ status,
                                                            uint32_t* __restrict__ split_flags,
                                                            int n_split_flags,
-                                                           unsigned long long* __restrict__ am_keys) {
+                                                           unsigned long long* __restrict__ am_keys,
+                                                           const int32_t* __restrict__ grp_off,
+                                                           const float* __restrict__ grp_global,
+                                                           int n_groups) {
   // launched as a programmatic dependent of whatever ran before it: wait for
   // that kernel's results before touching memory (the previous call's GEMM
   // may still be reading this workspace)
@@ -122,7 +125,18 @@ __global__ void __launch_bounds__(256) w4a16_prep_x_kernel(const uint16_t* __res
       e = min(max(14 - E, -126), 126);
     }
     s_e = e;
-    tok_scale[m] = __fmul_rn(*global, __int_as_float((127 - e) << 23));
+    float gw;
+    if (grp_off) {  // grouped: the global of the group holding token row m
+      int lo = 0, hi = n_groups;
+      while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (grp_off[mid] <= m) lo = mid; else hi = mid;
+      }
+      gw = (grp_off[lo] <= m && m < grp_off[lo + 1]) ? grp_global[lo] : 0.0f;
+    } else {
+      gw = *global;
+    }
+    tok_scale[m] = __fmul_rn(gw, __int_as_float((127 - e) << 23));
   }
   __syncthreads();
   const float p2 = __int_as_float((127 + s_e) << 23);
@@ -183,7 +197,9 @@ __device__ __forceinline__ uint32_t dup_hi(uint32_t v) { return __byte_perm(v, 0
 // ------------------------------------------------------------ the GEMM
 // kOut: NVFP4_OUT_F32 / NVFP4_OUT_BF16 store the logits; kOutArgmax keeps
 // only each token's largest logit and its vocabulary row.
-template <int kOut, int kStages, int kPStages, int kDqPerQuad>
+// kGrouped: the grouped (experts) product: weight rows e * N + n, token rows
+// grouped by the offsets in p.grp_off, one global scale per group.
+template <int kOut, int kStages, int kPStages, int kDqPerQuad, bool kGrouped = false>
 __global__ void __launch_bounds__((GemmShape<kStages, kPStages, kDqPerQuad>::kThreads), 1)
     w4a16_tc_kernel(const __grid_constant__ CUtensorMap tm_packed,
                     const __grid_constant__ CUtensorMap tm_scales,
@@ -214,11 +230,16 @@ __global__ void __launch_bounds__((GemmShape<kStages, kPStages, kDqPerQuad>::kTh
   // its current unit's tokens (lower bounds of each token's largest logit)
   int32_t* s_last = reinterpret_cast<int32_t*>(s_tok + 4 * kMaxBN);
   float* s_thr = reinterpret_cast<float*>(s_last + 4);
+  // grouped: the schedule derived from the group offsets
+  Sched* s_sched = reinterpret_cast<Sched*>(s_thr + 4 * kMaxBN);
+  uint32_t* s_unit_pre = reinterpret_cast<uint32_t*>(s_sched + 1);
+  int32_t* s_off = reinterpret_cast<int32_t*>(s_unit_pre + kMaxGroups + 1);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
+    if constexpr (kGrouped) grouped_sched_build(p, s_sched, s_unit_pre, s_off, (uint32_t)p.n_kb);
     for (int i = 0; i < kPStages; ++i) {
       mbar_init(&p_full[i], 1);
       mbar_init(&p_empty[i], 4);
@@ -252,6 +273,9 @@ __global__ void __launch_bounds__((GemmShape<kStages, kPStages, kDqPerQuad>::kTh
   const uint32_t tmem_a = tmem_base + 2 * BN;  // A ring after the two D buffers
 
   WaitCtl wc{p.status, abort_flag, kWaitLimitNs};
+  Sched sc;
+  if constexpr (kGrouped) sc = *s_sched; else sc = plain_sched(p);
+  const uint32_t n_kb_u = (uint32_t)p.n_kb;
   // the producer and MMA loops below are warp-uniform; one elected lane
   // issues each TMA / tcgen05 instruction
 
@@ -259,10 +283,12 @@ __global__ void __launch_bounds__((GemmShape<kStages, kPStages, kDqPerQuad>::kTh
     // ---------------- packed codes + scales producer
     // a weight tile read once (one token tile) is not kept in L2; one read
     // by several token tiles in a row is
-    const uint64_t pol = p.n_ttiles == 1 ? policy_evict_first() : policy_evict_last();
+    const uint64_t pol_once = policy_evict_first(), pol_reused = policy_evict_last();
     uint32_t issued = 0;
-    for_each_piece(p, [&](const Piece& pc) {
-      const int32_t n0 = (int32_t)((pc.u / p.n_ttiles) * kRows);
+    for_each_piece(sc, n_kb_u, [&](const Piece& pc) {
+      const UnitGeom geo = unit_geom<kGrouped>(p, sc, pc.u);
+      const int32_t n0 = (int32_t)geo.w_row;
+      const uint64_t pol = geo.reused ? pol_reused : pol_once;
       for (uint32_t kb = pc.kb0; kb < pc.kb1; ++kb, ++issued) {
         const uint32_t st = issued % kPStages, ph = (issued / kPStages) & 1;
         if (!warp_wait(&p_empty[st], ph ^ 1, wc)) return false;
@@ -283,8 +309,8 @@ __global__ void __launch_bounds__((GemmShape<kStages, kPStages, kDqPerQuad>::kTh
     grid_dependency_wait();  // the rescaled activations come from the prep kernel
     const uint64_t pol = policy_evict_last();
     uint32_t issued = 0;
-    for_each_piece(p, [&](const Piece& pc) {
-      const int32_t t0 = (int32_t)((pc.u % p.n_ttiles) * BN);
+    for_each_piece(sc, n_kb_u, [&](const Piece& pc) {
+      const int32_t t0 = (int32_t)unit_geom<kGrouped>(p, sc, pc.u).t0;
       for (uint32_t kb = pc.kb0; kb < pc.kb1; ++kb, ++issued) {
         const uint32_t st = issued % kStages, ph = (issued / kStages) & 1;
         if (!warp_wait(&s_empty[st], ph ^ 1, wc)) return false;
@@ -309,7 +335,7 @@ __global__ void __launch_bounds__((GemmShape<kStages, kPStages, kDqPerQuad>::kTh
     const uint32_t box_desc = x_box_bytes >> 4;
     uint32_t g = 0;
     int64_t i = 0;
-    for_each_piece(p, [&](const Piece& pc) {
+    for_each_piece(sc, n_kb_u, [&](const Piece& pc) {
       const uint32_t buf = (uint32_t)(i & 1), dph = (uint32_t)((i >> 1) & 1);
       ++i;
       if (!warp_wait(&d_empty[buf], dph ^ 1, wc)) return false;
@@ -355,7 +381,7 @@ __global__ void __launch_bounds__((GemmShape<kStages, kPStages, kDqPerQuad>::kTh
     const uint32_t lane_off = (uint32_t)(q * 32) << 16;
     const int sw = row & 7;
     // this warp's stages are g = r, r + kDqPerQuad, ... of the CTA's sequence
-    const uint32_t total = cta_stages(p);
+    const uint32_t total = cta_stages(sc, n_kb_u);
     bool ok = true;
     for (uint32_t g = (uint32_t)r; ok && g < total; g += kDqPerQuad) {
       const uint32_t ps = g % kPStages, pph = (g / kPStages) & 1;
@@ -397,8 +423,8 @@ __global__ void __launch_bounds__((GemmShape<kStages, kPStages, kDqPerQuad>::kTh
     }
   } else {
     // ---------------- epilogue: one thread per vocabulary row, BN tokens
-    epilogue_role<kOut, false>(p, warp, warp - kFirstEpiWarp, lane, tmem_base, d_full, d_empty,
-                               wc, s_tok, s_thr);
+    epilogue_role<kOut, false, kGrouped>(p, sc, warp, warp - kFirstEpiWarp, lane, tmem_base,
+                                         d_full, d_empty, wc, s_tok, s_thr);
   }
 
   __syncthreads();
@@ -410,13 +436,15 @@ __global__ void __launch_bounds__((GemmShape<kStages, kPStages, kDqPerQuad>::kTh
 }
 
 // ------------------------------------------------------------ host side
-static size_t gemm_smem_bytes(int BN, int stages, int pstages, bool argmax) {
+static size_t gemm_smem_bytes(int BN, int stages, int pstages, bool argmax, bool grouped = false) {
   // ring buffers, then 256 B of barriers and flags, then the epilogue's
   // per-warp token multipliers (and, for argmax, a flag and per-warp
-  // token thresholds)
+  // token thresholds; for the grouped product, after that region, its
+  // schedule and the per-group unit prefix and token offsets)
   return 1024 + pstages * (size_t)(kPackedStageBytes + kScaleStageBytes) +
          stages * (size_t)BN * kKB * 2 + 256 + 4 * kMaxBN * sizeof(float) +
-         (argmax ? 16 + 4 * kMaxBN * sizeof(float) : 0);
+         (argmax || grouped ? 16 + 4 * kMaxBN * sizeof(float) : 0) +
+         (grouped ? sizeof(Sched) + 2 * (kMaxGroups + 1) * sizeof(uint32_t) : 0);
 }
 
 size_t lm_head_workspace_bytes(int64_t M, int64_t N, int64_t K, bool argmax) {
@@ -424,18 +452,18 @@ size_t lm_head_workspace_bytes(int64_t M, int64_t N, int64_t K, bool argmax) {
 }
 
 // Launch one instantiation (programmatic dependent of the prep kernel).
-template <int kOut, int kStages, int kPStages, int kDq>
+template <int kOut, int kStages, int kPStages, int kDq, bool kGrouped = false>
 static cudaError_t launch_gemm(const CUtensorMap& tm_packed, const CUtensorMap& tm_scales,
                                const CUtensorMap& tm_x, const GemmArgs& a, int grid,
                                cudaStream_t stream) {
-  auto kern = w4a16_tc_kernel<kOut, kStages, kPStages, kDq>;
+  auto kern = w4a16_tc_kernel<kOut, kStages, kPStages, kDq, kGrouped>;
   constexpr bool kArgmax = kOut == kOutArgmax;
-  const size_t smem = gemm_smem_bytes(a.BN, kStages, kPStages, kArgmax);
+  const size_t smem = gemm_smem_bytes(a.BN, kStages, kPStages, kArgmax, kGrouped);
   // the 3-stage shape only serves token tiles of up to 64
   constexpr int kMaxTileBN = kStages >= 3 ? 64 : kMaxBN;
   static const cudaError_t attr_err = cudaFuncSetAttribute(
       kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-      (int)gemm_smem_bytes(kMaxTileBN, kStages, kPStages, kArgmax));
+      (int)gemm_smem_bytes(kMaxTileBN, kStages, kPStages, kArgmax, kGrouped));
   if (attr_err != cudaSuccess) return attr_err;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)grid);
@@ -496,7 +524,8 @@ nvfp4_status lm_head_launch(const void* x, int64_t M, int64_t K, const uint8_t* 
                            global_scale, x16, tok_scale, status, split_cnt,
                            (int)((L.part - L.cnt) / 4),
                            argmax ? reinterpret_cast<unsigned long long*>(ws + L.keys)
-                                  : nullptr) != cudaSuccess)
+                                  : nullptr,
+                           nullptr, nullptr, 0) != cudaSuccess)
       return NVFP4_ERR_CUDA;
   }
 
@@ -540,6 +569,93 @@ nvfp4_status lm_head_launch(const void* x, int64_t M, int64_t K, const uint8_t* 
   else
     err = deep ? launch_gemm<NVFP4_OUT_F32, 3, 6, 3>(tm_packed, tm_scales, tm_x, a, grid, stream)
                : launch_gemm<NVFP4_OUT_F32, 2, 4, 2>(tm_packed, tm_scales, tm_x, a, grid, stream);
+  if (err != cudaSuccess || cudaGetLastError() != cudaSuccess) return NVFP4_ERR_CUDA;
+  return NVFP4_OK;
+}
+
+// ------------------------------------------------------------ grouped product
+// Token tile of a grouped call: from the mean rows per group.
+static int grouped_token_tile(int64_t M, int64_t n_groups) {
+  return lm_head_token_tile(std::max<int64_t>(1, (M + n_groups - 1) / n_groups));
+}
+
+// Units of a grouped call are at most weight tiles x (token tiles of M + one
+// partial tile per group); the split-K arrays are sized for that grid.
+static int64_t grouped_units_bound(int64_t M, int64_t N, int64_t n_groups, int BN) {
+  return ((N + kRows - 1) / kRows) * ((M + BN - 1) / BN + n_groups);
+}
+
+size_t grouped_workspace_bytes(int64_t M, int64_t N, int64_t K, int64_t n_groups) {
+  const int BN = grouped_token_tile(M, n_groups);
+  const int sms = std::max(sm_count(), 1);
+  const int64_t units = grouped_units_bound(M, N, n_groups, BN);
+  // the plain product's layout for M token rows and a grid of at most
+  // min(SMs, unit bound); its token tile is never below the grouped one, so
+  // the split-K partials fit
+  return ws_layout(M, units * kRows, K, sms, false, 2).total;
+}
+
+nvfp4_status grouped_launch(const void* x, int64_t M, int64_t K, const int32_t* grp_off,
+                            int64_t n_groups, const uint8_t* packed, const uint8_t* scales,
+                            const float* grp_global, int64_t N, void* out, int out_dtype,
+                            void* workspace, cudaStream_t stream) {
+  const int sms = sm_count();
+  if (sms <= 0) return NVFP4_ERR_CUDA;
+  const int BN = grouped_token_tile(M, n_groups);
+  const int64_t units = grouped_units_bound(M, N, n_groups, BN);
+  // same byte layout as grouped_workspace_bytes: token rows M (TMA zero-fills
+  // past them), grid min(SMs, unit bound)
+  const WsLayout L = ws_layout(M, units * kRows, K, sms, false, 2);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  int32_t* status = reinterpret_cast<int32_t*>(ws);
+  __half* x16 = reinterpret_cast<__half*>(ws + L.x16);
+  float* tok_scale = reinterpret_cast<float*>(ws + L.tok);
+
+  CUtensorMap tm_packed, tm_scales, tm_x;
+  const uint64_t rows = (uint64_t)n_groups * (uint64_t)N;
+  if (!encode_2d(&tm_packed, CU_TENSOR_MAP_DATA_TYPE_UINT8, packed, (uint64_t)K / 2, rows,
+                 (uint64_t)K / 2, kKS / 2, kRows, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !encode_2d(&tm_scales, CU_TENSOR_MAP_DATA_TYPE_UINT8, scales, (uint64_t)K / 16, rows,
+                 (uint64_t)K / 16, kKS / 16, kRows, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+      !encode_2d(&tm_x, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, x16, (uint64_t)K, (uint64_t)M,
+                 (uint64_t)K * 2, 64, (uint32_t)BN, CU_TENSOR_MAP_SWIZZLE_128B))
+    return NVFP4_ERR_CUDA;
+  {
+    PdlLaunch l(dim3((unsigned)M), dim3(256), 0, stream);
+    if (cudaLaunchKernelEx(&l.cfg, w4a16_prep_x_kernel, static_cast<const uint16_t*>(x), M, K,
+                           (const float*)nullptr, x16, tok_scale, status,
+                           reinterpret_cast<uint32_t*>(ws + L.cnt), (int)((L.part - L.cnt) / 4),
+                           (unsigned long long*)nullptr, grp_off, grp_global,
+                           (int)n_groups) != cudaSuccess)
+      return NVFP4_ERR_CUDA;
+  }
+  GemmArgs a = {};
+  a.M = M;
+  a.N = N;
+  a.K = K;
+  a.BN = BN;
+  a.n_ttiles = 1;
+  a.n_kb = (int)(K / kKB);
+  a.split_cnt = reinterpret_cast<uint32_t*>(ws + L.cnt);
+  a.split_ready = reinterpret_cast<uint32_t*>(ws + L.ready);
+  a.split_part = reinterpret_cast<float*>(ws + L.part);
+  a.tok_scale = tok_scale;
+  a.out = out;
+  a.status = status;
+  a.grp_off = grp_off;
+  a.grp_global = grp_global;
+  a.n_groups = (int)n_groups;
+  const bool deep = BN <= 64;
+  const int stages = deep ? 3 : 2;
+  a.tmem_cols = (2 * BN + stages * (kKB / 2) <= 256) ? 256u : 512u;
+  const int grid = L.grid;
+  cudaError_t err;
+  if (out_dtype == NVFP4_OUT_BF16)
+    err = deep ? launch_gemm<NVFP4_OUT_BF16, 3, 6, 3, true>(tm_packed, tm_scales, tm_x, a, grid, stream)
+               : launch_gemm<NVFP4_OUT_BF16, 2, 4, 2, true>(tm_packed, tm_scales, tm_x, a, grid, stream);
+  else
+    err = deep ? launch_gemm<NVFP4_OUT_F32, 3, 6, 3, true>(tm_packed, tm_scales, tm_x, a, grid, stream)
+               : launch_gemm<NVFP4_OUT_F32, 2, 4, 2, true>(tm_packed, tm_scales, tm_x, a, grid, stream);
   if (err != cudaSuccess || cudaGetLastError() != cudaSuccess) return NVFP4_ERR_CUDA;
   return NVFP4_OK;
 }

@@ -270,7 +270,7 @@ __global__ void __launch_bounds__(kW4Threads, 1)
     mbar_wait(done_bar, 0, drain);
   } else {
     // ---------------- epilogue: x alpha (the token multiplier)
-    epilogue_role<kOut, false>(p, warp, warp - kW4FirstEpiWarp, lane, tmem_base, d_full, d_empty,
+    epilogue_role<kOut, false>(p, plain_sched(p), warp, warp - kW4FirstEpiWarp, lane, tmem_base, d_full, d_empty,
                                wc, s_tok, s_thr);
   }
 

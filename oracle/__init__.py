@@ -239,6 +239,19 @@ def w4a4_logits(x: np.ndarray, gx: float, packed: np.ndarray, scales: np.ndarray
     return out
 
 
+def grouped_logits(x: np.ndarray, offsets, packed: list, scales: list, globals_: list) -> np.ndarray:
+    """The grouped (MoE) W4A16 product: rows offsets[e]..offsets[e+1] of x times
+    expert e's dequantized weight, float64 [M, N] -- the plain product per group."""
+    M = x.shape[0]
+    N = packed[0].shape[0]
+    out = np.zeros((M, N), dtype=np.float64)
+    for e in range(len(packed)):
+        a, b = int(offsets[e]), int(offsets[e + 1])
+        if b > a:
+            out[a:b] = logits(x[a:b], packed[e], scales[e], globals_[e])
+    return out
+
+
 def swizzle_scales(scales: np.ndarray) -> np.ndarray:
     """`swizzle_blockscale` of an [N, C] scale matrix: flat bytes, rows padded to 128,
     columns to 4, in [N'/128][C'/4][32][4][4] order."""

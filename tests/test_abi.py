@@ -35,7 +35,8 @@ def test_header_declares_the_boundary():
               "nvfp4_status_string", "nvfp4_read_device_status", "nvfp4_abi_version",
               "w4a16_lm_head_argmax", "w4a16_lm_head_argmax_workspace_bytes",
               "fp8_quantize_rows", "fp8_refresh", "w8a8_lm_head", "w8a8_lm_head_argmax",
-              "nvfp4_swizzle_scales", "w4a4_lm_head", "w4a4_lm_head_argmax"):
+              "nvfp4_swizzle_scales", "w4a4_lm_head", "w4a4_lm_head_argmax",
+              "w4a16_grouped_gemm", "w4a16_grouped_workspace_bytes"):
         assert n in names
 
 
@@ -140,6 +141,20 @@ def test_w4a4_host_argument_errors(lib):
     a = lib.w4a4_lm_head_argmax
     assert a(fake, 4, 256, fake, fake, fake, fake, 0, fake, fake, fake, 1 << 30, None) == 1  # N 0
     assert lib.w4a4_lm_head_argmax_workspace_bytes(4, 0, 256) == 0
+
+
+def test_grouped_host_argument_errors(lib):
+    vp = ctypes.c_void_p
+    fake = vp(1 << 20)
+    g = lib.w4a16_grouped_gemm
+    assert g(fake, 8, 256, fake, 0, fake, fake, fake, 64, fake, 0, fake, 1 << 30, None) == 1    # E 0
+    assert g(fake, 8, 256, fake, 257, fake, fake, fake, 64, fake, 0, fake, 1 << 30, None) == 1  # E
+    assert g(fake, 8, 300, fake, 4, fake, fake, fake, 64, fake, 0, fake, 1 << 30, None) == 1    # K
+    assert g(fake, 0, 256, fake, 4, fake, fake, fake, 64, fake, 0, None, 0, None) == 0          # empty
+    assert g(fake, 8, 256, None, 4, fake, fake, fake, 64, fake, 0, fake, 1 << 30, None) == 3    # NULL
+    assert g(fake, 8, 256, fake, 4, fake, fake, fake, 64, fake, 0, fake, 64, None) == 4         # WS
+    assert g(fake, 8, 256, fake, 4, fake, fake, fake, 64, fake, 5, fake, 1 << 30, None) == 5    # DTYPE
+    assert lib.w4a16_grouped_workspace_bytes(8, 64, 256, 4) > 8 * 256 * 2
 
 
 def test_argmax_workspace_sizes(lib):
