@@ -16,7 +16,8 @@ are reported beside it with their own roofline fractions.  The fused greedy
 argmax (each token's largest logit and its row, logits never stored) is
 timed call by call after the steps and reported under "argmax"; the fp8
 lm_head copy (refresh, W8A8 decode and prefill, its argmax) likewise under
-"fp8", and the W4A4 NVFP4 product under "w4a4".
+"fp8", the W4A4 NVFP4 product under "w4a4", and the grouped MoE product under
+"moe".
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -72,6 +73,26 @@ def fp8_quant_bytes(N: int = N_VOCAB, K: int = K_HID) -> int:
 def w8a8_bytes(M: int, N: int = N_VOCAB, K: int = K_HID) -> int:
     """Algorithmic bytes of one W8A8 decode call: e4m3 W + row scales + x + fp32 logits."""
     return N * K + 4 * N + 2 * M * K + 4 * M * N
+
+
+MOE_E, MOE_H, MOE_I, MOE_TOPK = 128, 2048, 768, 8  # Qwen3-30B-A3B-shaped experts
+
+
+def moe_offsets(tokens: int, seed: int) -> np.ndarray:
+    """A seeded synthetic top-k router: expert-sorted row offsets."""
+    rng = np.random.default_rng(seed)
+    counts = np.zeros(MOE_E, dtype=np.int64)
+    for _ in range(tokens):
+        counts[rng.choice(MOE_E, MOE_TOPK, replace=False)] += 1
+    return np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+
+
+def grouped_bytes(offs: np.ndarray, N: int, K: int, out_bytes: int) -> int:
+    """Algorithmic bytes of one grouped call: the weights of the experts that
+    received rows, the rows of x (bf16) and the output."""
+    active = int(np.count_nonzero(np.diff(offs)))
+    M = int(offs[-1])
+    return active * (N * K // 2 + N * K // 16) + 2 * M * K + out_bytes * M * N
 
 
 def quant_bytes(N: int = N_VOCAB, K: int = K_HID) -> int:
@@ -532,6 +553,7 @@ def run_ours(args, world, rank, local):
         "argmax_us_per_call_alone": {str(M): round(v, 2) for M, v in w4am_us.items()},
         "rooflines": w4_roofs,
     }
+    moe_part = run_moe(nv, synth, dev, per_call_us, capture, peaks, traffic, hbm_roof)
     times = {"quantize": t_quant, "prefill": t_pre, "decode": t_dec_all}
     dominant = max(times, key=times.get)
 
@@ -563,12 +585,58 @@ def run_ours(args, world, rank, local):
         "argmax": argmax_part,
         "fp8": fp8_part,
         "w4a4": w4a4_part,
+        "moe": moe_part,
         "gpu_launches": launches_per_step * K_steps,
         "clocks": clock_info,
     }
     if rank == 0:
         result["cpu_baseline"] = cpu_baseline(budget_s=args.cpu_budget)
         print(json.dumps(result), flush=True)
+
+
+def run_moe(nv, synth, dev, per_call_us, capture, peaks, traffic, hbm_roof):
+    """The grouped NVFP4 W4A16 product of a MoE layer (w13: N = 2I, K = H; w2:
+    N = H, K = I) for a decode batch (64 tokens) and a prefill batch (2048
+    tokens), top-8 of 128 experts; each call alone from its own CUDA graph."""
+    res = {"what": f"grouped W4A16 MoE product, {MOE_E} experts, H={MOE_H}, I={MOE_I}, "
+                   f"top-{MOE_TOPK} (seeded synthetic router); each call alone, not part "
+                   "of the timed step", "us_per_call_alone": {}, "rooflines": {}}
+    for name, N, K in (("w13", 2 * MOE_I, MOE_H), ("w2", MOE_H, MOE_I)):
+        qws = torch.empty(nv.nvfp4_quantize_workspace_bytes(N, K), dtype=torch.uint8, device=dev)
+        packed = torch.empty(MOE_E, N, K // 2, dtype=torch.uint8, device=dev)
+        scales = torch.empty(MOE_E, N, K // 16, dtype=torch.float8_e4m3fn, device=dev)
+        gs = torch.empty(MOE_E, dtype=torch.float32, device=dev)
+        for e in range(MOE_E):
+            W = torch.from_numpy(synth.quant_weight(N=N, K=K, seed=1000 + e).view(np.int16)).view(
+                torch.bfloat16).to(dev)
+            nv.nvfp4_quantize_rows(W, packed[e], scales[e], gs[e:e + 1], workspace=qws)
+        for tokens in (64, 2048):
+            offs = moe_offsets(tokens, seed=tokens)
+            M = int(offs[-1])
+            x = torch.from_numpy(synth.decode_x(M, K=K).view(np.int16)).view(torch.bfloat16).to(dev)
+            od = torch.from_numpy(offs).to(dev)
+            odt = torch.float32 if tokens == 64 else torch.bfloat16
+            out = torch.empty(M, N, dtype=odt, device=dev)
+            ws = torch.empty(nv.w4a16_grouped_workspace_bytes(M, N, K, MOE_E), dtype=torch.uint8,
+                             device=dev)
+            g = capture(lambda: nv.w4a16_grouped_gemm(x, od, packed, scales, gs, out=out,
+                                                      workspace=ws))
+            us = per_call_us([g, g])
+            key = f"{name}_T{tokens}"
+            res["us_per_call_alone"][key] = round(us, 2)
+            if tokens == 64:
+                b = grouped_bytes(offs, N, K, 4)
+                res["rooflines"][key] = hbm_roof(f"w4a16_grouped_gemm {name} M={M} rows",
+                                                 b / (us / 1e6) / 1e9, f"moe_{key}")
+            else:
+                tf = 2.0 * M * N * K / (us / 1e6) / 1e12
+                res["rooflines"][key] = {
+                    "kernel": f"w4a16_grouped_gemm {name} M={M} rows", "bound": "tensor",
+                    "achieved": round(tf, 1), "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                    "frac": round(tf / peaks["bf16_tflops"], 4), "traffic": traffic.get(f"moe_{key}"),
+                    "peak_source": peaks["source"] + " dense bf16 burst (fp16 MMA, same rate)"}
+        del packed, scales, gs
+    return res
 
 
 # ----------------------------------------------------------- the CPU oracle
@@ -644,6 +712,25 @@ def run_profile_case(case: str):
         return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(
             torch.bfloat16).to(dev)
 
+    if case.startswith("moe_w13"):
+        Nm, Km = 2 * MOE_I, MOE_H
+        qws = torch.empty(nv.nvfp4_quantize_workspace_bytes(Nm, Km), dtype=torch.uint8, device=dev)
+        pk = torch.empty(MOE_E, Nm, Km // 2, dtype=torch.uint8, device=dev)
+        sc = torch.empty(MOE_E, Nm, Km // 16, dtype=torch.float8_e4m3fn, device=dev)
+        gs = torch.empty(MOE_E, dtype=torch.float32, device=dev)
+        for e in range(MOE_E):
+            We = up(synth.quant_weight(N=Nm, K=Km, seed=1000 + e))
+            nv.nvfp4_quantize_rows(We, pk[e], sc[e], gs[e:e + 1], workspace=qws)
+        offs = moe_offsets(64 if case == "moe_w13_decode" else 2048,
+                           seed=64 if case == "moe_w13_decode" else 2048)
+        x = up(synth.decode_x(int(offs[-1]), K=Km))
+        od = torch.from_numpy(offs).to(dev)
+        ws = torch.empty(nv.w4a16_grouped_workspace_bytes(int(offs[-1]), Nm, Km, MOE_E),
+                         dtype=torch.uint8, device=dev)
+        for _ in range(4):
+            nv.w4a16_grouped_gemm(x, od, pk, sc, gs, workspace=ws)
+        torch.cuda.synchronize()
+        return
     W = up(synth.decode_weight(seed=1))
     qws = torch.empty(nv.nvfp4_quantize_workspace_bytes(N, K), dtype=torch.uint8, device=dev)
     packed, scales, g = nv.nvfp4_quantize_rows(W, workspace=qws)
@@ -719,7 +806,8 @@ def main():
     ap.add_argument("--profile", choices=["decode1", "decode64", "prefill", "quant", "argmax1",
                                           "argmax64", "argmax_prefill", "fp8_quant",
                                           "fp8_decode1", "fp8_decode64", "fp8_prefill",
-                                          "w4a4_decode1", "w4a4_decode64", "w4a4_prefill"],
+                                          "w4a4_decode1", "w4a4_decode64", "w4a4_prefill",
+                                          "moe_w13_decode", "moe_w13_prefill"],
                     help="run one small fixed case for ncu instead of the benchmark")
     args = ap.parse_args()
     if args.profile:

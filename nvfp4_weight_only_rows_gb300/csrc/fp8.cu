@@ -378,6 +378,7 @@ nvfp4_status w8a8_launch(const void* x, int64_t M, int64_t K, const uint8_t* wq,
   uint32_t cols = 32;
   while (cols < 2u * BN) cols *= 2;
   a.tmem_cols = cols;
+  a.dbuf_log2 = 1;  // two accumulator buffers
   a.tok_scale = tok_scale;
   a.out = logits;
   a.status = status;

@@ -13,6 +13,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <type_traits>
 #include <mutex>
 
 #include "common.cuh"
@@ -36,6 +37,7 @@ struct GemmArgs {
   uint64_t tail_s0;    // first stage of the stream-K tail (unit-major, k-minor)
   uint64_t tail_len;   // stages in the tail, split evenly over the grid
   uint32_t tmem_cols;  // allocated TMEM columns
+  uint32_t dbuf_log2;  // accumulator buffers in TMEM: 1 << dbuf_log2 (2 or 4)
   const float* tok_scale;
   void* out;
   int32_t* status;
@@ -102,29 +104,54 @@ __device__ __forceinline__ UnitGeom unit_geom(const GemmArgs& p, const Sched& s,
     g.n0 = (int64_t)wt * kRows;
     g.w_row = (int64_t)lo * p.N + g.n0;
     g.t0 = s.off[lo] + (int64_t)tt * p.BN;
-    g.t_end = s.off[lo + 1] < p.M ? s.off[lo + 1] : p.M;
+    g.t_end = s.off[lo + 1] > s.off[lo] ? s.off[lo + 1] : s.off[lo];  // offsets are within [0, M]
     g.reused = ttc > 1;
   }
   return g;
 }
 
-// Grouped product: derive the schedule from the group offsets (thread 0,
-// before the block barrier that publishes it; the other threads read it
-// after).  Units of group e: weight tiles x ceil(tokens_e / BN).
-__device__ __forceinline__ void grouped_sched_build(const GemmArgs& p, Sched* s, uint32_t* unit_pre,
-                                                    int32_t* off, uint32_t n_kb) {
-  const uint32_t nt = (uint32_t)((p.N + kRows - 1) / kRows);
-  uint32_t acc = 0;
-  int32_t prev = 0;
-  for (int e = 0; e <= p.n_groups; ++e) {
-    int32_t o = p.grp_off[e];
-    o = o < prev ? prev : (o > p.M ? (int32_t)p.M : o);  // clamp to a monotone range in [0, M]
-    off[e] = o;
-    if (e > 0) acc += nt * (uint32_t)((o - prev + p.BN - 1) / p.BN);
-    unit_pre[e] = acc;
-    prev = o;
+// Grouped product: the whole block loads the group offsets into `off`,
+// each clamped to [0, M] (so no token row outside [0, M) is ever touched,
+// even for offsets that break the non-decreasing contract), then a block
+// barrier; warp 0 then derives the schedule (before the block barrier that
+// publishes it).  Units of group e: weight tiles x ceil(rows_e / BN), BN a
+// power of two.
+__device__ __forceinline__ void grouped_offsets_load(const GemmArgs& p, int32_t* off) {
+  for (int e = threadIdx.x; e <= p.n_groups; e += blockDim.x) {
+    const int32_t o = p.grp_off[e];
+    off[e] = o < 0 ? 0 : (o > p.M ? (int32_t)p.M : o);
   }
-  const uint32_t n_units = acc;
+}
+
+// Warp 0 (all lanes): lane l takes a contiguous run of groups, the warp
+// scans the run totals.
+__device__ __forceinline__ void grouped_sched_build(const GemmArgs& p, Sched* s, uint32_t* unit_pre,
+                                                    const int32_t* off, uint32_t n_kb, int lane) {
+  const uint32_t nt = (uint32_t)((p.N + kRows - 1) / kRows);
+  const int shift = __ffs(p.BN) - 1;  // BN = 1 << shift
+  const int E = p.n_groups;
+  const int per = (E + 31) / 32;
+  const int e0 = lane * per, e1 = min(E, e0 + per);
+  uint32_t run = 0;
+  for (int e = e0; e < e1; ++e) {
+    const int32_t rows = off[e + 1] > off[e] ? off[e + 1] - off[e] : 0;
+    run += nt * (uint32_t)((rows + p.BN - 1) >> shift);
+  }
+  uint32_t incl = run;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const uint32_t v = __shfl_up_sync(0xFFFFFFFFu, incl, d);
+    if (lane >= d) incl += v;
+  }
+  uint32_t acc = incl - run;  // units before this lane's run
+  for (int e = e0; e < e1; ++e) {
+    unit_pre[e] = acc;
+    const int32_t rows = off[e + 1] > off[e] ? off[e + 1] - off[e] : 0;
+    acc += nt * (uint32_t)((rows + p.BN - 1) >> shift);
+  }
+  const uint32_t n_units = __shfl_sync(0xFFFFFFFFu, incl, 31);
+  if (lane != 0) return;
+  unit_pre[E] = n_units;
   const uint32_t grid = n_units < gridDim.x ? n_units : gridDim.x;
   const uint32_t dp = (grid > 0 && n_units >= 2 * grid) ? n_units / grid - 1 : 0;
   s->n_dp = dp;
@@ -280,7 +307,8 @@ __device__ __forceinline__ void epilogue_role(const GemmArgs& p, const Sched& sc
   int64_t i = 0;
   for_each_piece(sc, (uint32_t)n_kb, [&](const Piece& pc) {
     const uint32_t u = pc.u, kb0 = pc.kb0, kb1 = pc.kb1;
-    const uint32_t buf = (uint32_t)(i & 1), dph = (uint32_t)((i >> 1) & 1);
+    const uint32_t buf = (uint32_t)(i & ((1 << p.dbuf_log2) - 1));
+    const uint32_t dph = (uint32_t)((i >> p.dbuf_log2) & 1);
     ++i;
     const UnitGeom geo = unit_geom<kGrouped>(p, sc, u);
     const int64_t n = geo.n0 + row;
@@ -384,16 +412,36 @@ __device__ __forceinline__ void epilogue_role(const GemmArgs& p, const Sched& sc
           }
         }
       } else if (n < p.N) {
+        // token multipliers by vector loads, scaled in pairs (each lane of
+        // the packed multiply rounds like the scalar one), one store per
+        // token walking down the column; a full chunk needs no predicate
+        float mul[16], val[16];
+        lds_f32x16(tok + c, mul);
 #pragma unroll
-        for (int t = 0; t < 16; ++t) {
-          const int64_t tok_i = t0 + c + t;
-          if (tok_i < t_end) {
-            float val = __fmul_rn(__uint_as_float(v[t]), tok[c + t]);
-            if (kRowScale) val = __fmul_rn(val, rs);
-            if (kOut == NVFP4_OUT_BF16)
-              reinterpret_cast<__nv_bfloat16*>(p.out)[tok_i * p.N + n] = __float2bfloat16_rn(val);
-            else
-              reinterpret_cast<float*>(p.out)[tok_i * p.N + n] = val;
+        for (int t = 0; t < 16; t += 2) {
+          float2 r = __fmul2_rn(make_float2(__uint_as_float(v[t]), __uint_as_float(v[t + 1])),
+                                make_float2(mul[t], mul[t + 1]));
+          if (kRowScale) r = __fmul2_rn(r, make_float2(rs, rs));
+          val[t] = r.x;
+          val[t + 1] = r.y;
+        }
+        const int64_t tc = t0 + c;
+        const int64_t live = t_end - tc;  // tokens of this chunk inside the group
+        using OutT = typename std::conditional<kOut == NVFP4_OUT_BF16, __nv_bfloat16, float>::type;
+        OutT* ptr = reinterpret_cast<OutT*>(p.out) + tc * p.N + n;
+        if (live >= 16) {
+#pragma unroll
+          for (int t = 0; t < 16; ++t, ptr += p.N) {
+            if constexpr (kOut == NVFP4_OUT_BF16) *ptr = __float2bfloat16_rn(val[t]);
+            else *ptr = val[t];
+          }
+        } else {
+#pragma unroll
+          for (int t = 0; t < 16; ++t, ptr += p.N) {
+            if (t < live) {
+              if constexpr (kOut == NVFP4_OUT_BF16) *ptr = __float2bfloat16_rn(val[t]);
+              else *ptr = val[t];
+            }
           }
         }
       }

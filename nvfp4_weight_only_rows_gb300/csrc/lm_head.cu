@@ -67,8 +67,13 @@ constexpr uint32_t kScaleStageBytes = kRows * (kKS / 16);   // 2048
 
 
 // ------------------------------------------------------------ activations
+// kWarpsPerRow warps per token row (8: the whole CTA, for few rows, where
+// the latency of one row is what counts; 1: a warp per row, 8 rows per CTA,
+// for many rows); rows m_rows and beyond do not exist, rows M .. m_rows-1
+// are the zero padding of the last token tile.
+template <int kWarpsPerRow>
 __global__ void __launch_bounds__(256) w4a16_prep_x_kernel(const uint16_t* __restrict__ x,
-                                                           int64_t M, int64_t K,
+                                                           int64_t M, int64_t K, int64_t m_rows,
                                                            const float* __restrict__ global,
                                                            __half* __restrict__ x16,
                                                            float* __restrict__ tok_scale,
@@ -90,19 +95,26 @@ __global__ void __launch_bounds__(256) w4a16_prep_x_kernel(const uint16_t* __res
     if (threadIdx.x == 0) *status = NVFP4_OK;
     for (int i = threadIdx.x; i < n_split_flags; i += blockDim.x) split_flags[i] = 0;
   }
-  const int64_t m = blockIdx.x;
-  if (am_keys && threadIdx.x == 0) am_keys[m * kKeyStride] = 0ull;  // argmax: no candidate yet
-  __half* dst = x16 + m * K;
+  __shared__ int32_t s_grp[kMaxGroups + 1];
+  if (grp_off) {  // grouped: the group offsets, loaded by the whole block
+    for (int e = threadIdx.x; e <= n_groups; e += blockDim.x) s_grp[e] = grp_off[e];
+    __syncthreads();
+  }
+  constexpr int kT = 32 * kWarpsPerRow;  // threads of one row
+  const int lane = threadIdx.x % kT;
+  const int64_t m = (int64_t)blockIdx.x * (8 / kWarpsPerRow) + threadIdx.x / kT;
+  if (m >= m_rows) return;  // uniform over the row's threads
+  if (am_keys && lane == 0) am_keys[m * kKeyStride] = 0ull;  // argmax: no candidate yet
+  uint4* d4 = reinterpret_cast<uint4*>(x16 + m * K);
   const int64_t nv = K / 8;
   if (m >= M) {  // padding rows of the last token tile
-    for (int64_t i = threadIdx.x; i < nv; i += blockDim.x)
-      reinterpret_cast<uint4*>(dst)[i] = make_uint4(0, 0, 0, 0);
+    for (int64_t i = lane; i < nv; i += kT) d4[i] = make_uint4(0, 0, 0, 0);
     return;
   }
   const uint4* src = reinterpret_cast<const uint4*>(x + m * K);
   uint32_t mx = 0;
-  for (int64_t i = threadIdx.x; i < nv; i += blockDim.x) {
-    uint4 v = src[i];
+  for (int64_t i = lane; i < nv; i += kT) {
+    const uint4 v = src[i];
     const uint32_t k = 0x7FFF7FFFu;
     mx = __vmaxu2(mx, v.x & k);
     mx = __vmaxu2(mx, v.y & k);
@@ -112,38 +124,36 @@ __global__ void __launch_bounds__(256) w4a16_prep_x_kernel(const uint16_t* __res
   mx = max(mx & 0xFFFFu, mx >> 16);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
-  __shared__ uint32_t red[8];
-  __shared__ int s_e;
-  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = mx;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    uint32_t a = 0;
-    for (int w = 0; w < (int)(blockDim.x >> 5); ++w) a = max(a, red[w]);
-    int e = 0;
-    if (a != 0 && a < 0x7F80u) {
-      const int E = ilogbf(__uint_as_float(a << 16));  // floor(log2(max|x|))
-      e = min(max(14 - E, -126), 126);
-    }
-    s_e = e;
+  if constexpr (kWarpsPerRow > 1) {  // the CTA is one row: combine its warps
+    __shared__ uint32_t red[8];
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = mx;
+    __syncthreads();
+    mx = 0;
+    for (int w = 0; w < kWarpsPerRow; ++w) mx = max(mx, red[w]);
+  }
+  int e = 0;
+  if (mx != 0 && mx < 0x7F80u) {
+    const int E = ilogbf(__uint_as_float(mx << 16));  // floor(log2(max|x|))
+    e = min(max(14 - E, -126), 126);
+  }
+  if (lane == 0) {
     float gw;
     if (grp_off) {  // grouped: the global of the group holding token row m
       int lo = 0, hi = n_groups;
       while (hi - lo > 1) {
         const int mid = (lo + hi) >> 1;
-        if (grp_off[mid] <= m) lo = mid; else hi = mid;
+        if (s_grp[mid] <= m) lo = mid; else hi = mid;
       }
-      gw = (grp_off[lo] <= m && m < grp_off[lo + 1]) ? grp_global[lo] : 0.0f;
+      gw = (s_grp[lo] <= m && m < s_grp[lo + 1]) ? grp_global[lo] : 0.0f;
     } else {
       gw = *global;
     }
     tok_scale[m] = __fmul_rn(gw, __int_as_float((127 - e) << 23));
   }
-  __syncthreads();
-  const float p2 = __int_as_float((127 + s_e) << 23);
-  uint4* d4 = reinterpret_cast<uint4*>(dst);
-  for (int64_t i = threadIdx.x; i < nv; i += blockDim.x) {
-    uint4 v = src[i];
-    uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  const float p2 = __int_as_float((127 + e) << 23);
+  for (int64_t i = lane; i < nv; i += kT) {
+    const uint4 v = src[i];
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
     uint32_t o[4];
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
@@ -155,6 +165,9 @@ __global__ void __launch_bounds__(256) w4a16_prep_x_kernel(const uint16_t* __res
     d4[i] = make_uint4(o[0], o[1], o[2], o[3]);
   }
 }
+
+// Up to this many token rows the prep kernel gives each row a whole CTA.
+constexpr int64_t kPrepWideRows = 256;
 
 // ------------------------------------------------------------ dequant helpers
 // 8 e2m1 codes (one word; byte j = codes 2j | 2j+1 << 4) -> 4 fp16 pairs,
@@ -220,9 +233,9 @@ __global__ void __launch_bounds__((GemmShape<kStages, kPStages, kDqPerQuad>::kTh
   uint64_t* p_empty = p_full + kPStages;   // packed/scale stage read by its 4 dequant warps
   uint64_t* s_full = p_empty + kPStages;   // A stage in TMEM (4 warps) + activation TMA landed
   uint64_t* s_empty = s_full + kStages;    // the MMAs reading stage s completed
-  uint64_t* d_full = s_empty + kStages;
-  uint64_t* d_empty = d_full + 2;
-  uint64_t* done_bar = d_empty + 2;
+  uint64_t* d_full = s_empty + kStages;   // accumulator buffer b holds a finished unit
+  uint64_t* d_empty = d_full + 4;         // the epilogue has drained buffer b
+  uint64_t* done_bar = d_empty + 4;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done_bar + 1);
   volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(tmem_slot + 1);
   float* s_tok = reinterpret_cast<float*>(bars + 32);  // 4 epilogue warps x kMaxBN multipliers
@@ -238,8 +251,11 @@ __global__ void __launch_bounds__((GemmShape<kStages, kPStages, kDqPerQuad>::kTh
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
+  if constexpr (kGrouped) {
+    grouped_offsets_load(p, s_off);
+    __syncthreads();
+  }
   if (threadIdx.x == 0) {
-    if constexpr (kGrouped) grouped_sched_build(p, s_sched, s_unit_pre, s_off, (uint32_t)p.n_kb);
     for (int i = 0; i < kPStages; ++i) {
       mbar_init(&p_full[i], 1);
       mbar_init(&p_empty[i], 4);
@@ -248,7 +264,7 @@ __global__ void __launch_bounds__((GemmShape<kStages, kPStages, kDqPerQuad>::kTh
       mbar_init(&s_full[i], 4 + 1);
       mbar_init(&s_empty[i], 1);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < 4; ++i) {
       mbar_init(&d_full[i], 1);
       mbar_init(&d_empty[i], 4);
     }
@@ -257,6 +273,8 @@ __global__ void __launch_bounds__((GemmShape<kStages, kPStages, kDqPerQuad>::kTh
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
+  if constexpr (kGrouped)
+    if (warp == 0) grouped_sched_build(p, s_sched, s_unit_pre, s_off, (uint32_t)p.n_kb, lane);
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tm_packed);
     tma_prefetch_desc(&tm_scales);
@@ -270,7 +288,7 @@ __global__ void __launch_bounds__((GemmShape<kStages, kPStages, kDqPerQuad>::kTh
   tc_fence_after();
   // warp-uniform copy of the TMEM base (lets the compiler keep it uniform)
   const uint32_t tmem_base = __shfl_sync(0xFFFFFFFFu, *tmem_slot, 0);
-  const uint32_t tmem_a = tmem_base + 2 * BN;  // A ring after the two D buffers
+  const uint32_t tmem_a = tmem_base + ((uint32_t)BN << p.dbuf_log2);  // A ring after the D buffers
 
   WaitCtl wc{p.status, abort_flag, kWaitLimitNs};
   Sched sc;
@@ -336,7 +354,8 @@ __global__ void __launch_bounds__((GemmShape<kStages, kPStages, kDqPerQuad>::kTh
     uint32_t g = 0;
     int64_t i = 0;
     for_each_piece(sc, n_kb_u, [&](const Piece& pc) {
-      const uint32_t buf = (uint32_t)(i & 1), dph = (uint32_t)((i >> 1) & 1);
+      const uint32_t buf = (uint32_t)(i & ((1 << p.dbuf_log2) - 1));
+      const uint32_t dph = (uint32_t)((i >> p.dbuf_log2) & 1);
       ++i;
       if (!warp_wait(&d_empty[buf], dph ^ 1, wc)) return false;
       tc_fence_after();
@@ -515,12 +534,15 @@ nvfp4_status lm_head_launch(const void* x, int64_t M, int64_t K, const uint8_t* 
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)m_pad);
+    // few rows: a CTA per row (latency); many rows: a warp per row
+    const bool wide = m_pad <= kPrepWideRows;
+    cfg.gridDim = dim3((unsigned)(wide ? m_pad : (m_pad + 7) / 8));
     cfg.blockDim = dim3(256);
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, w4a16_prep_x_kernel, static_cast<const uint16_t*>(x), M, K,
+    if (cudaLaunchKernelEx(&cfg, wide ? w4a16_prep_x_kernel<8> : w4a16_prep_x_kernel<1>,
+                           static_cast<const uint16_t*>(x), M, K, m_pad,
                            global_scale, x16, tok_scale, status, split_cnt,
                            (int)((L.part - L.cnt) / 4),
                            argmax ? reinterpret_cast<unsigned long long*>(ws + L.keys)
@@ -552,7 +574,10 @@ nvfp4_status lm_head_launch(const void* x, int64_t M, int64_t K, const uint8_t* 
   const bool deep = BN <= 64;
   const int stages = deep ? 3 : 2;
 
-  a.tmem_cols = (2 * BN + stages * (kKB / 2) <= 256) ? 256u : 512u;
+  // four accumulator buffers where TMEM has room for them (small token
+  // tiles: short units then overlap their epilogues), else two
+  a.dbuf_log2 = (4 * BN + stages * (kKB / 2) <= 512) ? 2u : 1u;
+  a.tmem_cols = ((BN << a.dbuf_log2) + stages * (kKB / 2) <= 256) ? 256u : 512u;
   a.tok_scale = tok_scale;
   a.out = logits;
   a.status = status;
@@ -576,7 +601,10 @@ nvfp4_status lm_head_launch(const void* x, int64_t M, int64_t K, const uint8_t* 
 // ------------------------------------------------------------ grouped product
 // Token tile of a grouped call: from the mean rows per group.
 static int grouped_token_tile(int64_t M, int64_t n_groups) {
-  return lm_head_token_tile(std::max<int64_t>(1, (M + n_groups - 1) / n_groups));
+  const int64_t mean = std::max<int64_t>(1, (M + n_groups - 1) / n_groups);
+  int bn = 16;  // a power of two (the device divides by shifting)
+  while (bn < kMaxBN && bn < mean) bn *= 2;
+  return bn;
 }
 
 // Units of a grouped call are at most weight tiles x (token tiles of M + one
@@ -621,8 +649,10 @@ nvfp4_status grouped_launch(const void* x, int64_t M, int64_t K, const int32_t* 
                  (uint64_t)K * 2, 64, (uint32_t)BN, CU_TENSOR_MAP_SWIZZLE_128B))
     return NVFP4_ERR_CUDA;
   {
-    PdlLaunch l(dim3((unsigned)M), dim3(256), 0, stream);
-    if (cudaLaunchKernelEx(&l.cfg, w4a16_prep_x_kernel, static_cast<const uint16_t*>(x), M, K,
+    const bool wide = M <= kPrepWideRows;
+    PdlLaunch l(dim3((unsigned)(wide ? M : (M + 7) / 8)), dim3(256), 0, stream);
+    if (cudaLaunchKernelEx(&l.cfg, wide ? w4a16_prep_x_kernel<8> : w4a16_prep_x_kernel<1>,
+                           static_cast<const uint16_t*>(x), M, K, M,
                            (const float*)nullptr, x16, tok_scale, status,
                            reinterpret_cast<uint32_t*>(ws + L.cnt), (int)((L.part - L.cnt) / 4),
                            (unsigned long long*)nullptr, grp_off, grp_global,
@@ -647,7 +677,10 @@ nvfp4_status grouped_launch(const void* x, int64_t M, int64_t K, const int32_t* 
   a.n_groups = (int)n_groups;
   const bool deep = BN <= 64;
   const int stages = deep ? 3 : 2;
-  a.tmem_cols = (2 * BN + stages * (kKB / 2) <= 256) ? 256u : 512u;
+  // four accumulator buffers where TMEM has room for them (small token
+  // tiles: short units then overlap their epilogues), else two
+  a.dbuf_log2 = (4 * BN + stages * (kKB / 2) <= 512) ? 2u : 1u;
+  a.tmem_cols = ((BN << a.dbuf_log2) + stages * (kKB / 2) <= 256) ? 256u : 512u;
   const int grid = L.grid;
   cudaError_t err;
   if (out_dtype == NVFP4_OUT_BF16)

@@ -375,6 +375,7 @@ nvfp4_status w4a4_launch(const void* x, int64_t M, int64_t K, const uint8_t* pac
   uint32_t cols = 32;
   while (cols < need) cols *= 2;
   a.tmem_cols = cols;
+  a.dbuf_log2 = 1;  // two accumulator buffers
   a.tok_scale = tok_scale;
   a.out = logits;
   a.status = status;
