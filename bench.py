@@ -410,6 +410,8 @@ def run_ours(args, world, rank, local):
     clocks.start()
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
+    # bracket the timed steps for a profiler run with --profile-from-start off
+    torch.cuda.profiler.start()
     t_start.record(stream)
     for s in range(args.steps):
         marks = []
@@ -417,6 +419,7 @@ def run_ours(args, world, rank, local):
         marks_all.append(marks)
     t_end.record(stream)
     torch.cuda.synchronize()
+    torch.cuda.profiler.stop()
     clock_info = clocks.stop()
     barrier(world)
     total_ms = t_start.elapsed_time(t_end)
