@@ -557,6 +557,7 @@ def run_ours(args, world, rank, local):
         "rooflines": w4_roofs,
     }
     moe_part = run_moe(nv, synth, dev, per_call_us, capture, peaks, traffic, hbm_roof)
+    cfg_part = run_other_configs(nv, synth, dev, per_call_us, capture, peaks, hbm_roof)
     times = {"quantize": t_quant, "prefill": t_pre, "decode": t_dec_all}
     dominant = max(times, key=times.get)
 
@@ -589,12 +590,62 @@ def run_ours(args, world, rank, local):
         "fp8": fp8_part,
         "w4a4": w4a4_part,
         "moe": moe_part,
+        "other_configs": cfg_part,
         "gpu_launches": launches_per_step * K_steps,
         "clocks": clock_info,
     }
     if rank == 0:
         result["cpu_baseline"] = cpu_baseline(budget_s=args.cpu_budget)
         print(json.dumps(result), flush=True)
+
+
+def run_other_configs(nv, synth, dev, per_call_us, capture, peaks, hbm_roof):
+    """The two other seeded workloads the throughput targets name, each call
+    alone from its own CUDA graph: the quantize/refresh of W[151936, 5120]
+    (Student-t row scales) and the large-vocabulary sweep W[262144, 8192]
+    with M in {1, 4, 16, 64} (HBM) and {256, 1024} (tensor), fp32 logits."""
+    res = {}
+    Nq, Kq = 151936, 5120
+    Wq = torch.from_numpy(synth.quant_weight(N=Nq, K=Kq, seed=4).view(np.int16)).view(
+        torch.bfloat16).to(dev)
+    qws = torch.empty(nv.nvfp4_quantize_workspace_bytes(Nq, Kq), dtype=torch.uint8, device=dev)
+    qq = nv.nvfp4_quantize_rows(Wq, workspace=qws)
+    g = capture(lambda: nv.nvfp4_refresh(Wq, *qq, workspace=qws))
+    us = per_call_us([g, g])
+    res["quantize_W151936x5120"] = {
+        "ms_per_call": round(us / 1e3, 4),
+        "roofline": hbm_roof("nvfp4 amax + encode, W[151936,5120]",
+                             quant_bytes(Nq, Kq) / (us / 1e6) / 1e9, "quantize_cfg4")}
+    del Wq, qq
+    Ns, Ks = 262144, 8192
+    Ws = torch.from_numpy(synth.sweep_weight().view(np.int16)).view(torch.bfloat16).to(dev)
+    qws = torch.empty(nv.nvfp4_quantize_workspace_bytes(Ns, Ks), dtype=torch.uint8, device=dev)
+    ps, ss, gs = nv.nvfp4_quantize_rows(Ws, workspace=qws)
+    del Ws
+    torch.cuda.empty_cache()
+    xs_all = torch.from_numpy(synth.sweep_x(1024).view(np.int16)).view(torch.bfloat16).to(dev)
+    ws = torch.empty(nv.w4a16_lm_head_workspace_bytes(1024, Ns, Ks), dtype=torch.uint8, device=dev)
+    sweep = {"us_per_call_alone": {}, "rooflines": {}}
+    for M in (1, 4, 16, 64, 256, 1024):
+        xs = xs_all[:M].contiguous()
+        out = torch.empty(M, Ns, dtype=torch.float32, device=dev)
+        gg = capture(lambda: nv.w4a16_lm_head(xs, ps, ss, gs, out=out, workspace=ws))
+        us = per_call_us([gg, gg])
+        sweep["us_per_call_alone"][str(M)] = round(us, 2)
+        if M <= 64:
+            sweep["rooflines"][f"M{M}"] = hbm_roof(
+                f"w4a16_lm_head W[262144,8192] M={M}",
+                decode_bytes(M, Ns, Ks) / (us / 1e6) / 1e9, f"sweep_M{M}")
+        else:
+            tf = prefill_flops(M, Ns, Ks) / (us / 1e6) / 1e12
+            sweep["rooflines"][f"M{M}"] = {
+                "kernel": f"w4a16_lm_head W[262144,8192] M={M}", "bound": "tensor",
+                "achieved": round(tf, 1), "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": round(tf / peaks["bf16_tflops"], 4), "traffic": None,
+                "peak_source": peaks["source"] + " dense bf16 burst (fp16 MMA, same rate)"}
+        del out
+    res["sweep_W262144x8192"] = sweep
+    return res
 
 
 def run_moe(nv, synth, dev, per_call_us, capture, peaks, traffic, hbm_roof):

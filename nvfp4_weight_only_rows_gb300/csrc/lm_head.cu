@@ -67,10 +67,11 @@ constexpr uint32_t kScaleStageBytes = kRows * (kKS / 16);   // 2048
 
 
 // ------------------------------------------------------------ activations
-// kWarpsPerRow warps per token row (8: the whole CTA, for few rows, where
-// the latency of one row is what counts; 1: a warp per row, 8 rows per CTA,
-// for many rows); rows m_rows and beyond do not exist, rows M .. m_rows-1
-// are the zero padding of the last token tile.
+// kWarpsPerRow warps per token row (4, with a 128-thread CTA per row, for
+// few rows, where the latency of one row is what counts and the CTA must
+// fit beside a GEMM CTA on its SM; 1: a warp per row, 8 rows per 256-thread
+// CTA, for many rows); rows m_rows and beyond do not exist, rows
+// M .. m_rows-1 are zero padding.
 template <int kWarpsPerRow>
 __global__ void __launch_bounds__(256) w4a16_prep_x_kernel(const uint16_t* __restrict__ x,
                                                            int64_t M, int64_t K, int64_t m_rows,
@@ -102,7 +103,7 @@ __global__ void __launch_bounds__(256) w4a16_prep_x_kernel(const uint16_t* __res
   }
   constexpr int kT = 32 * kWarpsPerRow;  // threads of one row
   const int lane = threadIdx.x % kT;
-  const int64_t m = (int64_t)blockIdx.x * (8 / kWarpsPerRow) + threadIdx.x / kT;
+  const int64_t m = (int64_t)blockIdx.x * (blockDim.x / kT) + threadIdx.x / kT;
   if (m >= m_rows) return;  // uniform over the row's threads
   if (am_keys && lane == 0) am_keys[m * kKeyStride] = 0ull;  // argmax: no candidate yet
   uint4* d4 = reinterpret_cast<uint4*>(x16 + m * K);
@@ -125,7 +126,7 @@ __global__ void __launch_bounds__(256) w4a16_prep_x_kernel(const uint16_t* __res
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
   if constexpr (kWarpsPerRow > 1) {  // the CTA is one row: combine its warps
-    __shared__ uint32_t red[8];
+    __shared__ uint32_t red[kWarpsPerRow];
     if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = mx;
     __syncthreads();
     mx = 0;
@@ -508,7 +509,6 @@ nvfp4_status lm_head_launch(const void* x, int64_t M, int64_t K, const uint8_t* 
   const bool argmax = out_mode == kOutArgmax;
   const int BN = lm_head_token_tile(M);
   const int n_ttiles = (int)((M + BN - 1) / BN);
-  const int64_t m_pad = (int64_t)n_ttiles * BN;
   const WsLayout L = ws_layout(M, N, K, sms, argmax, 2);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   int32_t* status = reinterpret_cast<int32_t*>(ws);
@@ -523,7 +523,7 @@ nvfp4_status lm_head_launch(const void* x, int64_t M, int64_t K, const uint8_t* 
                  (uint64_t)K / 2, kKS / 2, kRows, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !encode_2d(&tm_scales, CU_TENSOR_MAP_DATA_TYPE_UINT8, scales, (uint64_t)K / 16, (uint64_t)N,
                  (uint64_t)K / 16, kKS / 16, kRows, CU_TENSOR_MAP_SWIZZLE_NONE) ||
-      !encode_2d(&tm_x, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, x16, (uint64_t)K, (uint64_t)m_pad,
+      !encode_2d(&tm_x, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, x16, (uint64_t)K, (uint64_t)M,
                  (uint64_t)K * 2, 64, (uint32_t)BN, CU_TENSOR_MAP_SWIZZLE_128B))
     return NVFP4_ERR_CUDA;
 
@@ -535,14 +535,16 @@ nvfp4_status lm_head_launch(const void* x, int64_t M, int64_t K, const uint8_t* 
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cudaLaunchConfig_t cfg = {};
     // few rows: a CTA per row (latency); many rows: a warp per row
-    const bool wide = m_pad <= kPrepWideRows;
-    cfg.gridDim = dim3((unsigned)(wide ? m_pad : (m_pad + 7) / 8));
-    cfg.blockDim = dim3(256);
+    // the activation map has M rows: the TMA zero-fills the rows of the last
+    // token tile past M, so the prep kernel writes only the M real rows
+    const bool wide = M <= kPrepWideRows;
+    cfg.gridDim = dim3((unsigned)(wide ? M : (M + 7) / 8));
+    cfg.blockDim = dim3(wide ? 128 : 256);
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, wide ? w4a16_prep_x_kernel<8> : w4a16_prep_x_kernel<1>,
-                           static_cast<const uint16_t*>(x), M, K, m_pad,
+    if (cudaLaunchKernelEx(&cfg, wide ? w4a16_prep_x_kernel<4> : w4a16_prep_x_kernel<1>,
+                           static_cast<const uint16_t*>(x), M, K, M,
                            global_scale, x16, tok_scale, status, split_cnt,
                            (int)((L.part - L.cnt) / 4),
                            argmax ? reinterpret_cast<unsigned long long*>(ws + L.keys)
@@ -650,8 +652,8 @@ nvfp4_status grouped_launch(const void* x, int64_t M, int64_t K, const int32_t* 
     return NVFP4_ERR_CUDA;
   {
     const bool wide = M <= kPrepWideRows;
-    PdlLaunch l(dim3((unsigned)(wide ? M : (M + 7) / 8)), dim3(256), 0, stream);
-    if (cudaLaunchKernelEx(&l.cfg, wide ? w4a16_prep_x_kernel<8> : w4a16_prep_x_kernel<1>,
+    PdlLaunch l(dim3((unsigned)(wide ? M : (M + 7) / 8)), dim3(wide ? 128 : 256), 0, stream);
+    if (cudaLaunchKernelEx(&l.cfg, wide ? w4a16_prep_x_kernel<4> : w4a16_prep_x_kernel<1>,
                            static_cast<const uint16_t*>(x), M, K, M,
                            (const float*)nullptr, x16, tok_scale, status,
                            reinterpret_cast<uint32_t*>(ws + L.cnt), (int)((L.part - L.cnt) / 4),
