@@ -14,7 +14,8 @@ decode calls / their device time, CUDA events on the launching stream), the
 first clause of the headline metric; the prefill TFLOP/s and quantizer GB/s
 are reported beside it with their own roofline fractions.  The fused greedy
 argmax (each token's largest logit and its row, logits never stored) is
-timed call by call after the steps and reported under "argmax"; the fp8
+timed call by call after the steps and reported under "argmax", the fused
+top-k (k = 50) under "topk"; the fp8
 lm_head copy (refresh, W8A8 decode and prefill, its argmax) likewise under
 "fp8", the W4A4 NVFP4 product under "w4a4", and the grouped MoE product under
 "moe".
@@ -63,6 +64,14 @@ def decode_bytes(M: int, N: int = N_VOCAB, K: int = K_HID) -> int:
 def argmax_bytes(M: int, N: int = N_VOCAB, K: int = K_HID) -> int:
     """Algorithmic bytes of one fused-argmax call: packed + scales + x + (i64 id, f32 value)."""
     return N * K // 2 + N * K // 16 + 2 * M * K + 12 * M
+
+
+TOPK_K = 50  # k of the fused top-k lines (a common sampler default)
+
+
+def topk_bytes(M: int, k: int = TOPK_K, N: int = N_VOCAB, K: int = K_HID) -> int:
+    """Algorithmic bytes of one fused top-k call: packed + scales + x + k (i64 id, f32 value)."""
+    return N * K // 2 + N * K // 16 + 2 * M * K + 12 * M * k
 
 
 def fp8_quant_bytes(N: int = N_VOCAB, K: int = K_HID) -> int:
@@ -361,6 +370,14 @@ def run_ours(args, world, rank, local):
     g_am = {M: [capture(lambda M=M, c=c: nv.w4a16_lm_head_argmax(
         x_am[M], *copies[c], token_ids=am_ids[M], max_logits=am_vals[M], workspace=aws))
         for c in range(2)] for M in x_am}
+    # the fused top-k (k largest logits per token, logits never stored), each call alone
+    tk_ids = {M: torch.empty((M, TOPK_K), dtype=torch.int64, device=dev) for M in x_am}
+    tk_vals = {M: torch.empty((M, TOPK_K), dtype=torch.float32, device=dev) for M in x_am}
+    tkws = torch.empty(nv.w4a16_lm_head_topk_workspace_bytes(PREFILL_M, N, K, TOPK_K),
+                       dtype=torch.uint8, device=dev)
+    g_tk = {M: [capture(lambda M=M, c=c: nv.w4a16_lm_head_topk(
+        x_am[M], *copies[c], TOPK_K, token_ids=tk_ids[M], values=tk_vals[M], workspace=tkws))
+        for c in range(2)] for M in x_am}
     g_pre_one = [capture(lambda c=c: nv.w4a16_lm_head(x_pre, *copies[c], out=out_pre,
                                                       workspace=gws)) for c in range(2)]
 
@@ -468,6 +485,7 @@ def run_ours(args, world, rank, local):
     pre_tflops = K_steps * prefill_flops() / (t_pre / 1e3) / 1e12
     per_call_dec = {M: per_call_us(g_one[M]) for M in DECODE_MS}  # us, each call alone
     per_call_am = {M: per_call_us(g_am[M]) for M in x_am}
+    per_call_tk = {M: per_call_us(g_tk[M]) for M in x_am}
     pre_alone_us = per_call_us(g_pre_one)
     f8q_us = per_call_us(g_f8q)
     w8_us = {M: per_call_us(g_w8[M]) for M in g_w8}
@@ -514,6 +532,23 @@ def run_ours(args, world, rank, local):
         "logits_call_us_alone": {**{str(M): round(per_call_dec[M], 2) for M in DECODE_MS},
                                  str(PREFILL_M) + "_bf16": round(pre_alone_us, 2)},
         "rooflines": am_roofs,
+    }
+    tk_roofs = {}
+    for M in DECODE_MS:
+        gbs = topk_bytes(M) / (per_call_tk[M] / 1e6) / 1e9
+        tk_roofs[f"topk_M{M}"] = hbm_roof(f"w4a16_lm_head_topk k={TOPK_K} M={M} alone "
+                                          "(prep + GEMM + select)", gbs, f"topk_M{M}")
+    tk_tflops = prefill_flops() / (per_call_tk[PREFILL_M] / 1e6) / 1e12
+    tk_roofs[f"topk_M{PREFILL_M}"] = {
+        "kernel": f"w4a16_lm_head_topk k={TOPK_K} M={PREFILL_M} alone", "bound": "tensor",
+        "achieved": round(tk_tflops, 1), "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+        "frac": round(tk_tflops / peaks["bf16_tflops"], 4), "traffic": traffic.get("topk_prefill"),
+        "peak_source": peaks["source"] + " dense bf16 burst (fp16 MMA, same rate)"}
+    topk_part = {
+        "what": f"fused top-k, k={TOPK_K} (rows + logits of each token's k largest, logits not "
+                "stored); each call alone from its own CUDA graph, not part of the timed step",
+        "us_per_call_alone": {str(M): round(per_call_tk[M], 2) for M in x_am},
+        "rooflines": tk_roofs,
     }
     fp8_peak = 2.0 * peaks["bf16_tflops"]  # nominal fp8 : bf16 dense ratio (4.5 : 2.25 PF)
     fp8_roofs = {"fp8_quantize": hbm_roof("fp8_quantize_kernel (refresh call)",
@@ -587,6 +622,7 @@ def run_ours(args, world, rank, local):
                 "what": "decode calls through w4a16_lm_head with x copied from pinned host memory "
                         "and logits copied back every call"},
         "argmax": argmax_part,
+        "topk": topk_part,
         "fp8": fp8_part,
         "w4a4": w4a4_part,
         "moe": moe_part,
@@ -753,7 +789,7 @@ def run_reference(args, world, rank):
 def run_profile_case(case: str):
     """A small, fixed case for ncu: three warm-up calls, then exactly one call
     of the profiled entry point (decode M=1 / M=64, prefill, refresh, or the
-    fused argmax at M=1 / M=64 / M=2048) on
+    fused argmax or the fused top-k at M=1 / M=64 / M=2048) on
     the decode-shaped weight; the device holds under 1.5 GB."""
     import nvfp4_weight_only_rows_gb300 as nv
     import synth
@@ -828,6 +864,15 @@ def run_profile_case(case: str):
             nv.w8a8_lm_head(x, q8, s8, out=out, workspace=w8ws)
         torch.cuda.synchronize()
         return
+    if case.startswith("topk"):
+        M = PREFILL_M if case == "topk_prefill" else int(case.replace("topk", ""))
+        x = up(synth.prefill_x()) if M == PREFILL_M else up(synth.decode_x(M))
+        tws = torch.empty(nv.w4a16_lm_head_topk_workspace_bytes(M, N, K, TOPK_K),
+                          dtype=torch.uint8, device=dev)
+        for _ in range(4):
+            nv.w4a16_lm_head_topk(x, packed, scales, g, TOPK_K, workspace=tws)
+        torch.cuda.synchronize()
+        return
     if case.startswith("argmax"):
         M = PREFILL_M if case == "argmax_prefill" else int(case.replace("argmax", ""))
         x = up(synth.prefill_x()) if M == PREFILL_M else up(synth.decode_x(M))
@@ -861,7 +906,8 @@ def main():
                                           "argmax64", "argmax_prefill", "fp8_quant",
                                           "fp8_decode1", "fp8_decode64", "fp8_prefill",
                                           "w4a4_decode1", "w4a4_decode64", "w4a4_prefill",
-                                          "moe_w13_decode", "moe_w13_prefill"],
+                                          "moe_w13_decode", "moe_w13_prefill", "topk1",
+                                          "topk64", "topk_prefill"],
                     help="run one small fixed case for ncu instead of the benchmark")
     args = ap.parse_args()
     if args.profile:

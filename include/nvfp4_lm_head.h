@@ -217,6 +217,52 @@ nvfp4_status w4a16_lm_head_argmax(const void *x, int64_t M, int64_t K, const uin
                                   int64_t *token_ids, float *max_logits, void *workspace,
                                   size_t workspace_bytes, void *stream);
 
+/* ------------------------------------------------ fused top-k */
+
+#define NVFP4_TOPK_MAX 128 /* largest k of w4a16_lm_head_topk */
+
+/*
+ * Workspace bytes w4a16_lm_head_topk needs (0 for rejected shapes): those of
+ * w4a16_lm_head_argmax plus the candidate store, M x N x 8 bytes (every
+ * logit is a candidate at most once), and M x ceil(N / B) 4-byte block
+ * counts, B = max(64, 2k rounded up to a power of two).  Only the
+ * candidates that reach their token's threshold are ever written.
+ */
+size_t w4a16_lm_head_topk_workspace_bytes(int64_t M, int64_t N, int64_t K, int64_t k);
+
+/*
+ * The k largest logits of each token, fused into the W4A16 product:
+ *   token_ids[m, j], values[m, j] (j = 0 .. k-1) = the rows and logits of
+ *   token m's k largest, in descending order; of equal logits the smaller
+ *   row comes first,
+ * where the logits are bit for bit the fp32 values w4a16_lm_head writes with
+ * NVFP4_OUT_F32 for the same inputs, with -0 and +0 equal (a zero is
+ * returned as +0) and a NaN above every number, as in w4a16_lm_head_argmax
+ * (whose answer is column 0 here).  The [M, N] logits are never written:
+ * the epilogue appends only the logits that reach the token's running
+ * threshold, a lower bound of its k-th largest that rises as blocks of
+ * candidates complete, and a second kernel selects the exact k largest of
+ * those.  The result does not depend on the schedule.
+ *
+ * The pages define the logits, not a sampler; this is the top-k filter a
+ * sampler applies to them, for the same reason as the argmax.
+ *
+ *   x, packed, scales, global_scale, K, M, N
+ *                as for w4a16_lm_head_argmax; M x N <= 2^36.
+ *   k            1 <= k <= min(N, NVFP4_TOPK_MAX), else NVFP4_ERR_SHAPE.
+ *   token_ids    int64 [M, k] row-major, device, 8-byte aligned.
+ *   values       fp32 [M, k], device, 4-byte aligned, or NULL to skip.
+ *   workspace    device, >= w4a16_lm_head_topk_workspace_bytes(M, N, K, k),
+ *                256-byte aligned; no state is kept in it between calls.
+ * Two kernels on `stream`, no host synchronisation; graph-capturable.  A
+ * device-side timeout (NVFP4_ERR_TIMEOUT in the workspace status word)
+ * leaves token_ids and values undefined.
+ */
+nvfp4_status w4a16_lm_head_topk(const void *x, int64_t M, int64_t K, const uint8_t *packed,
+                                const uint8_t *scales, const float *global_scale, int64_t N,
+                                int64_t k, int64_t *token_ids, float *values, void *workspace,
+                                size_t workspace_bytes, void *stream);
+
 /* ------------------------------------------------------- fp8 copy */
 
 /*

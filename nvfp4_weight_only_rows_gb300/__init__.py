@@ -19,6 +19,9 @@ Entry points (same names as the C ABI):
 * ``w4a16_lm_head_argmax(x, packed, scales, global_scale)`` ->
   ``(token_ids i64[M], max_logits f32[M])`` -- the same product reduced to each
   token's largest logit inside the kernel (greedy choice; logits never stored).
+* ``w4a16_lm_head_topk(x, packed, scales, global_scale, k)`` ->
+  ``(token_ids i64[M, k], values f32[M, k])`` -- each token's k largest logits,
+  in descending order, selected without storing the logits.
 * ``fp8_quantize_rows(W)`` -> ``(q e4m3[N,K], row_scale f32[N])`` and
   ``fp8_refresh`` -- the "fp8" copy of ``quantized_lm_head_copy`` (per-row
   scales); ``w8a8_lm_head(x, q, row_scale)`` / ``w8a8_lm_head_argmax`` -- its
@@ -49,7 +52,8 @@ __all__ = [
     "w8a8_lm_head_workspace_bytes", "w8a8_lm_head_argmax_workspace_bytes",
     "nvfp4_swizzle_scales", "nvfp4_swizzled_scales_bytes", "w4a4_lm_head",
     "w4a4_lm_head_argmax", "w4a4_lm_head_workspace_bytes", "w4a4_lm_head_argmax_workspace_bytes",
-    "w4a16_grouped_gemm", "w4a16_grouped_workspace_bytes",
+    "w4a16_grouped_gemm", "w4a16_grouped_workspace_bytes", "w4a16_lm_head_topk",
+    "w4a16_lm_head_topk_workspace_bytes", "TOPK_MAX",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -58,6 +62,7 @@ _lib = None
 
 OUT_F32 = 0
 OUT_BF16 = 1
+TOPK_MAX = 128  # NVFP4_TOPK_MAX: largest k of the fused top-k
 
 
 class Status(enum.IntEnum):
@@ -116,6 +121,10 @@ def load_library() -> ctypes.CDLL:
     lib.w4a16_lm_head_argmax_workspace_bytes.restype = sz
     lib.w4a16_lm_head_argmax.argtypes = [vp, i64, i64, vp, vp, vp, i64, vp, vp, vp, sz, vp]
     lib.w4a16_lm_head_argmax.restype = st
+    lib.w4a16_lm_head_topk_workspace_bytes.argtypes = [i64, i64, i64, i64]
+    lib.w4a16_lm_head_topk_workspace_bytes.restype = sz
+    lib.w4a16_lm_head_topk.argtypes = [vp, i64, i64, vp, vp, vp, i64, i64, vp, vp, vp, sz, vp]
+    lib.w4a16_lm_head_topk.restype = st
     lib.fp8_quantize_workspace_bytes.argtypes = [i64, i64]
     lib.fp8_quantize_workspace_bytes.restype = sz
     for name in ("fp8_quantize_rows", "fp8_refresh"):
@@ -301,6 +310,40 @@ def w4a16_lm_head_argmax(x: torch.Tensor, packed: torch.Tensor, scales: torch.Te
                                   workspace.numel() * workspace.element_size(), _stream(stream))
     _check(rc, "w4a16_lm_head_argmax")
     return token_ids, max_logits
+
+
+def w4a16_lm_head_topk_workspace_bytes(M: int, N: int, K: int, k: int) -> int:
+    return int(load_library().w4a16_lm_head_topk_workspace_bytes(M, N, K, k))
+
+
+def w4a16_lm_head_topk(x: torch.Tensor, packed: torch.Tensor, scales: torch.Tensor,
+                       global_scale: torch.Tensor, k: int, token_ids: torch.Tensor | None = None,
+                       values: torch.Tensor | None = None, with_values: bool = True,
+                       workspace: torch.Tensor | None = None, stream=None):
+    """Each token's k largest logits and their vocabulary rows, largest first
+    (smaller row first on ties), without writing the logits: returns
+    (token_ids i64[M, k], values f32[M, k] or None)."""
+    lib = load_library()
+    _need(x, torch.bfloat16, "x")
+    M, K = x.shape
+    N = packed.shape[0]
+    _need(packed, torch.uint8, "packed", (N, K // 2))
+    _need(scales, scales.dtype, "scales", (N, K // 16))
+    _need(global_scale, torch.float32, "global_scale")
+    if token_ids is None:
+        token_ids = torch.empty((M, max(k, 0)), dtype=torch.int64, device=x.device)
+    _need(token_ids, torch.int64, "token_ids", (M, max(k, 0)))
+    if values is None and with_values:
+        values = torch.empty((M, max(k, 0)), dtype=torch.float32, device=x.device)
+    if values is not None:
+        _need(values, torch.float32, "values", (M, max(k, 0)))
+    if workspace is None:
+        workspace = _workspace(w4a16_lm_head_topk_workspace_bytes(M, N, K, k), x.device)
+    rc = lib.w4a16_lm_head_topk(_ptr(x), M, K, _ptr(packed), _ptr(scales), _ptr(global_scale),
+                                N, k, _ptr(token_ids), _ptr(values), _ptr(workspace),
+                                workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(rc, "w4a16_lm_head_topk")
+    return token_ids, values
 
 
 def fp8_quantize_workspace_bytes(N: int, K: int) -> int:

@@ -14,7 +14,7 @@ import subprocess
 HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 LIB = os.path.join(HERE, "libnvfp4_lm_head.so")
-SOURCES = ("quantize.cu", "lm_head.cu", "fp8.cu", "w4a4.cu", "api.cu", "noalloc.cu",
+SOURCES = ("quantize.cu", "lm_head.cu", "fp8.cu", "w4a4.cu", "topk.cu", "api.cu", "noalloc.cu",
            "selftest.cu")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",

@@ -18,6 +18,11 @@ nvfp4_status lm_head_launch(const void* x, int64_t M, int64_t K, const uint8_t* 
                             void* logits, int out_mode, int64_t* token_ids, float* max_logits,
                             void* workspace, cudaStream_t stream);
 constexpr int kOutArgmax = 2;  // lm_head_launch's third output mode
+size_t lm_head_topk_workspace_bytes(int64_t M, int64_t N, int64_t K, int k);
+nvfp4_status lm_head_topk_launch(const void* x, int64_t M, int64_t K, const uint8_t* packed,
+                                 const uint8_t* scales, const float* global_scale, int64_t N,
+                                 int k, int64_t* token_ids, float* values, void* workspace,
+                                 cudaStream_t stream);
 int64_t fp8_max_k();
 size_t grouped_workspace_bytes(int64_t M, int64_t N, int64_t K, int64_t n_groups);
 nvfp4_status grouped_launch(const void* x, int64_t M, int64_t K, const int32_t* grp_off,
@@ -180,6 +185,37 @@ nvfp4_status w4a16_lm_head_argmax(const void* x, int64_t M, int64_t K, const uin
   if (st != NVFP4_OK) return st;
   return lm_head_launch(x, M, K, packed, scales, global_scale, N, nullptr, kOutArgmax, token_ids,
                         max_logits, workspace, static_cast<cudaStream_t>(stream));
+}
+
+/* ------------------------------------------------------------ fused top-k */
+
+static bool topk_shape_ok(int64_t M, int64_t N, int64_t K, int64_t k) {
+  return M >= 0 && N > 0 && K >= 256 && K % 256 == 0 && M < kMaxDim && N < kMaxDim &&
+         K < kMaxDim && k >= 1 && k <= NVFP4_TOPK_MAX && k <= N && M * N <= ((int64_t)1 << 36);
+}
+
+size_t w4a16_lm_head_topk_workspace_bytes(int64_t M, int64_t N, int64_t K, int64_t k) {
+  if (!topk_shape_ok(M, N, K, k)) return 0;
+  return lm_head_topk_workspace_bytes(M, N, K, (int)k);
+}
+
+nvfp4_status w4a16_lm_head_topk(const void* x, int64_t M, int64_t K, const uint8_t* packed,
+                                const uint8_t* scales, const float* global_scale, int64_t N,
+                                int64_t k, int64_t* token_ids, float* values, void* workspace,
+                                size_t workspace_bytes, void* stream) {
+  if (!topk_shape_ok(M, N, K, k)) return NVFP4_ERR_SHAPE;
+  if (M == 0) return NVFP4_OK;
+  if (!x || !packed || !scales || !global_scale || !token_ids) return NVFP4_ERR_NULL;
+  if (!workspace || workspace_bytes < lm_head_topk_workspace_bytes(M, N, K, (int)k))
+    return NVFP4_ERR_WORKSPACE;
+  if (!aligned(x, 16) || !aligned(packed, 16) || !aligned(scales, 16) ||
+      !aligned(global_scale, 4) || !aligned(token_ids, 8) || !aligned(values, 4) ||
+      !aligned(workspace, 256))
+    return NVFP4_ERR_ALIGN;
+  nvfp4_status st = check_device();
+  if (st != NVFP4_OK) return st;
+  return lm_head_topk_launch(x, M, K, packed, scales, global_scale, N, (int)k, token_ids, values,
+                             workspace, static_cast<cudaStream_t>(stream));
 }
 
 /* ------------------------------------------------------------ fp8 copy */

@@ -24,7 +24,9 @@ constexpr int kRows = 128;   // vocabulary rows per unit (MMA M)
 constexpr int kKB = 256;     // k per pipeline stage
 constexpr int kMaxBN = 128;  // largest token tile
 constexpr int kOutArgmax = 2;   // third output mode (after NVFP4_OUT_F32, NVFP4_OUT_BF16)
-constexpr int kKeyStride = 16;  // argmax: one 64-bit candidate per 128-byte line (spreads the atomics)
+constexpr int kOutTopk = 3;     // fourth: the k largest logits of each token
+constexpr int kKeyStride = 16;  // argmax / top-k: one 128-byte line of per-token state (spreads the atomics)
+constexpr int kTopkMax = 128;   // largest k of the fused top-k
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per pipeline wait
 
 struct GemmArgs {
@@ -50,6 +52,14 @@ struct GemmArgs {
   uint32_t* am_done;            // CTAs that have finished, zeroed per call
   int64_t* am_idx;              // [M] result: vocabulary row of the largest logit
   float* am_val;                // [M] result: that logit (may be null)
+  // top-k output mode only (am_keys then holds per token line: word 0 the
+  // threshold key, a lower bound of the token's k-th largest candidate
+  // key; word 1 the number of candidates appended)
+  unsigned long long* tk_cand;  // [M][N] candidate keys in append order
+  uint32_t* tk_blk;             // [m_pad][tk_nblk] entries written per candidate block
+  int tk_k;                     // k, 1 .. kTopkMax
+  int tk_blog2;                 // log2 of the candidate block (>= 2k, >= 64)
+  int64_t tk_nblk;              // candidate blocks per token, ceil(N / block)
   const float* row_scale;       // [N] per-row weight scale (fp8 weights), else null
   // grouped product (experts) only
   const int32_t* grp_off;       // [n_groups + 1] token row offsets of the groups
@@ -246,6 +256,109 @@ __device__ __forceinline__ float key_value(uint32_t k) {
   return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
 }
 
+// ------------------------------------------------------------ fused top-k
+// Per token: a threshold key T (a lower bound of the token's k-th largest
+// candidate key, so every one of its k largest logits reaches it), a count
+// of appended candidates and the candidates themselves, N slots (every
+// logit is appended at most once).  The slots are cut into blocks of
+// B >= 2k; each block carries a count of entries written, and the warp whose
+// entries complete a block reads it back and raises T to the k-th largest
+// key among those B entries (k real logits of the token reach it).  T is
+// kept as (high word << 32): only the value part is selected, which is still
+// a valid lower bound.
+__device__ __forceinline__ unsigned long long* topk_thr(const GemmArgs& p, int64_t tok) {
+  return p.am_keys + tok * kKeyStride;
+}
+__device__ __forceinline__ uint32_t* topk_cnt(const GemmArgs& p, int64_t tok) {
+  return reinterpret_cast<uint32_t*>(p.am_keys + tok * kKeyStride + 1);
+}
+
+// The k-th largest value word among the B entries of block j of token
+// `tok`, merged into its threshold (whole warp; every entry has been
+// written and made visible before the block count reached B).
+__device__ __forceinline__ void topk_raise(const GemmArgs& p, int64_t tok, uint32_t j, int lane) {
+  const unsigned long long* blk = p.tk_cand + tok * p.N + ((int64_t)j << p.tk_blog2);
+  const int per_lane = (1 << p.tk_blog2) >> 5;  // 2 .. 8
+  uint32_t h[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+    h[i] = i < per_lane ? (uint32_t)(__ldcg(blk + i * 32 + lane) >> 32) : 0u;
+  // bit by bit from the top: the answer has bit b set iff at least `need`
+  // entries match the answer's higher bits with bit b set
+  uint32_t prefix = 0;
+  uint32_t need = (uint32_t)p.tk_k;
+#pragma unroll 1
+  for (int b = 31; b >= 0; --b) {
+    const uint32_t hmask = ~((1u << b) - 1u);
+    const uint32_t want = prefix | (1u << b);
+    uint32_t c = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) c += (i < per_lane && (h[i] & hmask) == want) ? 1u : 0u;
+    c = __reduce_add_sync(0xFFFFFFFFu, c);
+    if (c >= need) prefix = want;
+    else need -= c;
+  }
+  if (lane == 0) atomicMax(topk_thr(p, tok), (unsigned long long)prefix << 32);
+}
+
+// One chunk of 16 tokens (token rows tc .. tc + 15) in which some lane
+// reached its token's threshold: append the passing candidates of each
+// token, count them into their blocks, and raise the thresholds of the
+// blocks this warp completes.  Lane t < 16 does token t's atomics, so the
+// sixteen tokens' round trips overlap.
+__device__ __forceinline__ void topk_chunk(const GemmArgs& p, int64_t tc, int64_t t_end,
+                                           const float (&val)[16], const float (&thr)[16],
+                                           bool valid, uint32_t n, int lane) {
+  uint32_t my_bal = 0;
+#pragma unroll
+  for (int t = 0; t < 16; ++t) {
+    const uint32_t bal = __ballot_sync(0xFFFFFFFFu, valid && !(val[t] < thr[t]));
+    if (lane == t) my_bal = bal;
+  }
+  const int64_t my_tok = tc + lane;
+  const uint32_t my_n = (lane < 16 && my_tok < t_end) ? __popc(my_bal) : 0u;
+  uint32_t base = 0;
+  if (my_n) base = atomicAdd(topk_cnt(p, my_tok), my_n);
+  const uint32_t lt = (1u << lane) - 1u;
+#pragma unroll
+  for (int t = 0; t < 16; ++t) {
+    const uint32_t nt = __shfl_sync(0xFFFFFFFFu, my_n, t);
+    if (nt == 0) continue;
+    const uint32_t bal = __shfl_sync(0xFFFFFFFFu, my_bal, t);
+    const uint32_t b = __shfl_sync(0xFFFFFFFFu, base, t);
+    if ((bal >> lane) & 1u) {
+      const uint32_t idx = b + __popc(bal & lt);
+      if ((int64_t)idx < p.N)
+        p.tk_cand[(tc + t) * p.N + idx] =
+            ((unsigned long long)order_key(val[t]) << 32) | (uint32_t)~n;
+    }
+  }
+  __threadfence();  // the entries are visible before their block counts
+  __syncwarp();
+  uint32_t chk = 0;  // bit 0: this lane's token completed its first block, bit 1: its second
+  uint32_t j0 = 0, j1 = 0;
+  if (my_n && (int64_t)(base + my_n) <= p.N) {
+    const uint32_t B = 1u << p.tk_blog2;
+    j0 = base >> p.tk_blog2;
+    j1 = (base + my_n - 1) >> p.tk_blog2;
+    uint32_t* cnt = p.tk_blk + my_tok * p.tk_nblk;
+    const uint32_t n0 = j0 == j1 ? my_n : (j1 << p.tk_blog2) - base;
+    if (atomicAdd(cnt + j0, n0) + n0 == B) chk |= 1u;
+    if (j1 != j0 && atomicAdd(cnt + j1, my_n - n0) + (my_n - n0) == B) chk |= 2u;
+  }
+  uint32_t todo = __ballot_sync(0xFFFFFFFFu, chk != 0);
+  if (todo) __threadfence();  // the completed blocks' entries are read after the counts
+  while (todo) {
+    const int t = __ffs(todo) - 1;
+    todo &= todo - 1;
+    const uint32_t ck = __shfl_sync(0xFFFFFFFFu, chk, t);
+    const uint32_t a0 = __shfl_sync(0xFFFFFFFFu, j0, t);
+    const uint32_t a1 = __shfl_sync(0xFFFFFFFFu, j1, t);
+    if (ck & 1u) topk_raise(p, tc + t, a0, lane);
+    if (ck & 2u) topk_raise(p, tc + t, a1, lane);
+  }
+}
+
 // ------------------------------------------------------------ schedule
 // A CTA's work is a list of pieces (a unit, or the part of a unit inside the
 // CTA's tail range): first n_dp whole units in strided waves (so that at any
@@ -290,7 +403,7 @@ __device__ __forceinline__ uint32_t cta_stages(const Sched& sc, uint32_t n_kb) {
 // ready; then 16 tokens at a time are drained from TMEM, combined with the
 // other CTA's partial where a unit was split, scaled (token multiplier, then
 // the row's own scale for fp8 weights) and stored, or reduced to per-token
-// candidates (argmax).  `epi` is the warp's index among the four.
+// candidates (argmax, top-k).  `epi` is the warp's index among the four.
 template <int kOut, bool kRowScale, bool kGrouped = false>
 __device__ __forceinline__ void epilogue_role(const GemmArgs& p, const Sched& sc, int warp, int epi,
                                               int lane, uint32_t tmem_base, uint64_t* d_full,
@@ -318,12 +431,13 @@ __device__ __forceinline__ void epilogue_role(const GemmArgs& p, const Sched& sc
     // once per warp (written by the prep kernel, which may still have been
     // running when this kernel started, so read coherently from L2, not
     // the read-only path) and, for argmax, each token's current maximum
-    // as a threshold (a stale one is only lower; no candidate yet: -Inf;
-    // tokens past M: +Inf, nothing passes).
+    // as a threshold (top-k: the value part of its threshold key; a stale
+    // one is only lower; none yet: -Inf; tokens past M: +Inf, nothing
+    // passes).
     for (int t = lane; t < BN; t += 32) {
       const bool live = t0 + t < t_end;
       tok[t] = live ? __ldcg(p.tok_scale + t0 + t) : 0.0f;
-      if (kOut == kOutArgmax) {
+      if (kOut == kOutArgmax || kOut == kOutTopk) {
         const uint32_t kh =
             live ? __ldcg(reinterpret_cast<const uint32_t*>(p.am_keys + (t0 + t) * kKeyStride) + 1)
                  : 0u;
@@ -374,7 +488,27 @@ __device__ __forceinline__ void epilogue_role(const GemmArgs& p, const Sched& sc
         for (int t = 0; t < 16; ++t)
           v[t] = __float_as_uint(__fadd_rn(__uint_as_float(v[t]), other[t]));
       }
-      if (kOut == kOutArgmax) {
+      if (kOut == kOutTopk) {
+        // the logits as for argmax; one vote per chunk on the thresholds,
+        // then the appends of the tokens that some row reached
+        const bool valid = n < p.N;
+        float thr[16], mul[16], val[16];
+        lds_f32x16(wthr + c, thr);
+        lds_f32x16(tok + c, mul);
+        bool pass = false;
+#pragma unroll
+        for (int t = 0; t < 16; t += 2) {
+          float2 r = __ffma2_rn(make_float2(__uint_as_float(v[t]), __uint_as_float(v[t + 1])),
+                                make_float2(mul[t], mul[t + 1]), make_float2(0.0f, 0.0f));
+          if (kRowScale) r = __fmul2_rn(r, make_float2(rs, rs));
+          val[t] = r.x;
+          val[t + 1] = r.y;
+          pass |= !(r.x < thr[t]);
+          pass |= !(r.y < thr[t + 1]);
+        }
+        if (__any_sync(0xFFFFFFFFu, valid && pass))
+          topk_chunk(p, t0 + c, t_end, val, thr, valid, (uint32_t)n, lane);
+      } else if (kOut == kOutArgmax) {
         // The logits as the plain product rounds them (the fma with +0
         // rounds like the multiply and turns an exact -0 into +0), then one
         // vote: does any row of this warp reach the threshold of its token
@@ -527,17 +661,31 @@ static int sm_count() {
 // Workspace layout of one call: [status header][activations as the MMA
 // reads them, m_pad x K x x_bytes (fp16: 2, e4m3: 1)]
 // [token multipliers, m_pad][split counters, grid x 4][split ready flags,
-// grid x 4] and, for argmax only, [CTAs done, 1]; these are zeroed by the
-// prep kernel's first CTA.  Then [split partials, grid x 4 x BN x 32 fp32]
-// and, for argmax only, [per-token maxima, m_pad x 128 bytes, one 64-bit
-// word used per line], each word zeroed by the prep CTA of its token.
+// grid x 4] and, for argmax and top-k, [CTAs done, 1]; these are zeroed by
+// the prep kernel's first CTA.  Then [split partials, grid x 4 x BN x 32
+// fp32] and, for argmax and top-k, [per-token state, m_pad x 128 bytes: the
+// maximum or the threshold key in word 0, the top-k candidate count in word
+// 1], both words zeroed by the prep CTA of the token.  Top-k only: [block
+// counts, m_pad x ceil(N / block) u32, zeroed the same way][candidates,
+// M x N u64, written before they are read].
 struct WsLayout {
-  size_t x16, tok, cnt, ready, done, keys, part, total;
+  size_t x16, tok, cnt, ready, done, keys, part, blk, cand, total;
   int grid;
+  int tk_blog2;
+  int64_t tk_nblk;
 };
 
-static WsLayout ws_layout(int64_t M, int64_t N, int64_t K, int sms, bool argmax, int x_bytes) {
+// log2 of the top-k candidate block: at least 2k entries and 64 (two per lane)
+static int topk_block_log2(int k) {
+  int b = 6;
+  while ((1 << b) < 2 * k) ++b;
+  return b;
+}
+
+static WsLayout ws_layout(int64_t M, int64_t N, int64_t K, int sms, bool argmax, int x_bytes,
+                          int topk_k = 0) {
   WsLayout l;
+  const bool keys = argmax || topk_k > 0;
   const int BN = lm_head_token_tile(M);
   const int64_t m_pad = (M + BN - 1) / BN * BN;
   const int64_t n_units = ((N + kRows - 1) / kRows) * ((M + BN - 1) / BN);
@@ -547,11 +695,20 @@ static WsLayout ws_layout(int64_t M, int64_t N, int64_t K, int sms, bool argmax,
   l.cnt = l.tok + align_up((size_t)m_pad * 4, 256);
   l.ready = l.cnt + align_up((size_t)l.grid * 4 * 4, 256);
   l.done = l.ready + align_up((size_t)l.grid * 4 * 4, 256);
-  l.part = l.done + (argmax ? 256 : 0);
+  l.part = l.done + (keys ? 256 : 0);
   l.keys = l.part + align_up((size_t)l.grid * 4 * BN * 32 * 4, 256);
-  l.total = l.keys + (argmax ? (size_t)m_pad * kKeyStride * 8 : 0);
+  l.blk = l.keys + (keys ? (size_t)m_pad * kKeyStride * 8 : 0);
+  l.tk_blog2 = topk_k > 0 ? topk_block_log2(topk_k) : 0;
+  l.tk_nblk = topk_k > 0 ? (N + (1 << l.tk_blog2) - 1) >> l.tk_blog2 : 0;
+  l.cand = l.blk + align_up((size_t)m_pad * l.tk_nblk * 4, 256);
+  l.total = l.cand + (topk_k > 0 ? (size_t)M * N * 8 : 0);
   return l;
 }
+
+// The top-k selection kernel (topk.cu), launched after a top-k GEMM.
+cudaError_t topk_select_launch(const unsigned long long* lines, const unsigned long long* cand,
+                               int64_t M, int64_t N, int k, int64_t* ids, float* vals,
+                               cudaStream_t stream);
 
 // Split the units of a call into strided whole-unit waves and a stream-K
 // tail: all but the last one to two waves run whole; the rest is split

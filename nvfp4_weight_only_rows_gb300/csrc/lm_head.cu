@@ -82,6 +82,8 @@ __global__ void __launch_bounds__(256) w4a16_prep_x_kernel(const uint16_t* __res
                                                            uint32_t* __restrict__ split_flags,
                                                            int n_split_flags,
                                                            unsigned long long* __restrict__ am_keys,
+                                                           uint32_t* __restrict__ tk_blk,
+                                                           int64_t tk_nblk,
                                                            const int32_t* __restrict__ grp_off,
                                                            const float* __restrict__ grp_global,
                                                            int n_groups) {
@@ -105,7 +107,12 @@ __global__ void __launch_bounds__(256) w4a16_prep_x_kernel(const uint16_t* __res
   const int lane = threadIdx.x % kT;
   const int64_t m = (int64_t)blockIdx.x * (blockDim.x / kT) + threadIdx.x / kT;
   if (m >= m_rows) return;  // uniform over the row's threads
-  if (am_keys && lane == 0) am_keys[m * kKeyStride] = 0ull;  // argmax: no candidate yet
+  if (am_keys && lane == 0) {  // argmax / top-k: no candidate yet
+    am_keys[m * kKeyStride] = 0ull;
+    am_keys[m * kKeyStride + 1] = 0ull;
+  }
+  if (tk_blk)  // top-k: no candidate block written yet
+    for (int64_t i = lane; i < tk_nblk; i += kT) tk_blk[m * tk_nblk + i] = 0u;
   uint4* d4 = reinterpret_cast<uint4*>(x16 + m * K);
   const int64_t nv = K / 8;
   if (m >= M) {  // padding rows of the last token tile
@@ -210,7 +217,8 @@ __device__ __forceinline__ uint32_t dup_hi(uint32_t v) { return __byte_perm(v, 0
 
 // ------------------------------------------------------------ the GEMM
 // kOut: NVFP4_OUT_F32 / NVFP4_OUT_BF16 store the logits; kOutArgmax keeps
-// only each token's largest logit and its vocabulary row.
+// only each token's largest logit and its vocabulary row; kOutTopk appends
+// the candidates for each token's k largest (topk.cu selects them).
 // kGrouped: the grouped (experts) product: weight rows e * N + n, token rows
 // grouped by the offsets in p.grp_off, one global scale per group.
 template <int kOut, int kStages, int kPStages, int kDqPerQuad, bool kGrouped = false>
@@ -477,7 +485,7 @@ static cudaError_t launch_gemm(const CUtensorMap& tm_packed, const CUtensorMap& 
                                const CUtensorMap& tm_x, const GemmArgs& a, int grid,
                                cudaStream_t stream) {
   auto kern = w4a16_tc_kernel<kOut, kStages, kPStages, kDq, kGrouped>;
-  constexpr bool kArgmax = kOut == kOutArgmax;
+  constexpr bool kArgmax = kOut == kOutArgmax || kOut == kOutTopk;  // per-warp thresholds
   const size_t smem = gemm_smem_bytes(a.BN, kStages, kPStages, kArgmax, kGrouped);
   // the 3-stage shape only serves token tiles of up to 64
   constexpr int kMaxTileBN = kStages >= 3 ? 64 : kMaxBN;
@@ -498,18 +506,26 @@ static cudaError_t launch_gemm(const CUtensorMap& tm_packed, const CUtensorMap& 
   return cudaLaunchKernelEx(&cfg, kern, tm_packed, tm_scales, tm_x, a);
 }
 
+size_t lm_head_topk_workspace_bytes(int64_t M, int64_t N, int64_t K, int k) {
+  return ws_layout(M, N, K, std::max(sm_count(), 1), false, 2, k).total;
+}
+
 // out_mode: NVFP4_OUT_F32 / NVFP4_OUT_BF16 write logits[M, N] to `logits`;
-// kOutArgmax writes token_ids[M] (and max_logits[M] unless null) instead.
-nvfp4_status lm_head_launch(const void* x, int64_t M, int64_t K, const uint8_t* packed,
-                            const uint8_t* scales, const float* global_scale, int64_t N,
-                            void* logits, int out_mode, int64_t* token_ids, float* max_logits,
-                            void* workspace, cudaStream_t stream) {
+// kOutArgmax writes token_ids[M] (and max_logits[M] unless null) instead;
+// kOutTopk (topk_k > 0) writes token_ids[M, k] (and max_logits[M, k]).
+static nvfp4_status lm_head_run(const void* x, int64_t M, int64_t K, const uint8_t* packed,
+                                const uint8_t* scales, const float* global_scale, int64_t N,
+                                void* logits, int out_mode, int64_t* token_ids,
+                                float* max_logits, int topk_k, void* workspace,
+                                cudaStream_t stream) {
   const int sms = sm_count();
   if (sms <= 0) return NVFP4_ERR_CUDA;
   const bool argmax = out_mode == kOutArgmax;
+  const bool topk = out_mode == kOutTopk;
+  const bool keys = argmax || topk;
   const int BN = lm_head_token_tile(M);
   const int n_ttiles = (int)((M + BN - 1) / BN);
-  const WsLayout L = ws_layout(M, N, K, sms, argmax, 2);
+  const WsLayout L = ws_layout(M, N, K, sms, argmax, 2, topk ? topk_k : 0);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   int32_t* status = reinterpret_cast<int32_t*>(ws);
   __half* x16 = reinterpret_cast<__half*>(ws + L.x16);
@@ -547,8 +563,8 @@ nvfp4_status lm_head_launch(const void* x, int64_t M, int64_t K, const uint8_t* 
                            static_cast<const uint16_t*>(x), M, K, M,
                            global_scale, x16, tok_scale, status, split_cnt,
                            (int)((L.part - L.cnt) / 4),
-                           argmax ? reinterpret_cast<unsigned long long*>(ws + L.keys)
-                                  : nullptr,
+                           keys ? reinterpret_cast<unsigned long long*>(ws + L.keys) : nullptr,
+                           topk ? reinterpret_cast<uint32_t*>(ws + L.blk) : nullptr, L.tk_nblk,
                            nullptr, nullptr, 0) != cudaSuccess)
       return NVFP4_ERR_CUDA;
   }
@@ -565,10 +581,15 @@ nvfp4_status lm_head_launch(const void* x, int64_t M, int64_t K, const uint8_t* 
   a.split_cnt = split_cnt;
   a.split_ready = split_ready;
   a.split_part = split_part;
-  a.am_keys = argmax ? reinterpret_cast<unsigned long long*>(ws + L.keys) : nullptr;
+  a.am_keys = keys ? reinterpret_cast<unsigned long long*>(ws + L.keys) : nullptr;
   a.am_done = argmax ? reinterpret_cast<uint32_t*>(ws + L.done) : nullptr;
   a.am_idx = token_ids;
   a.am_val = max_logits;
+  a.tk_cand = topk ? reinterpret_cast<unsigned long long*>(ws + L.cand) : nullptr;
+  a.tk_blk = topk ? reinterpret_cast<uint32_t*>(ws + L.blk) : nullptr;
+  a.tk_k = topk_k;
+  a.tk_blog2 = L.tk_blog2;
+  a.tk_nblk = L.tk_nblk;
   a.row_scale = nullptr;
   // decode-sized token tiles get a third A stage, six packed stages and a
   // third dequant warp per quadrant; 128-token tiles leave TMEM room for two
@@ -590,7 +611,12 @@ nvfp4_status lm_head_launch(const void* x, int64_t M, int64_t K, const uint8_t* 
   if (argmax)
     err = deep ? launch_gemm<kOutArgmax, 3, 6, 3>(tm_packed, tm_scales, tm_x, a, grid, stream)
                : launch_gemm<kOutArgmax, 2, 4, 2>(tm_packed, tm_scales, tm_x, a, grid, stream);
-  else if (out_mode == NVFP4_OUT_BF16)
+  else if (topk) {
+    err = deep ? launch_gemm<kOutTopk, 3, 6, 3>(tm_packed, tm_scales, tm_x, a, grid, stream)
+               : launch_gemm<kOutTopk, 2, 4, 2>(tm_packed, tm_scales, tm_x, a, grid, stream);
+    if (err == cudaSuccess)
+      err = topk_select_launch(a.am_keys, a.tk_cand, M, N, topk_k, token_ids, max_logits, stream);
+  } else if (out_mode == NVFP4_OUT_BF16)
     err = deep ? launch_gemm<NVFP4_OUT_BF16, 3, 6, 3>(tm_packed, tm_scales, tm_x, a, grid, stream)
                : launch_gemm<NVFP4_OUT_BF16, 2, 4, 2>(tm_packed, tm_scales, tm_x, a, grid, stream);
   else
@@ -598,6 +624,22 @@ nvfp4_status lm_head_launch(const void* x, int64_t M, int64_t K, const uint8_t* 
                : launch_gemm<NVFP4_OUT_F32, 2, 4, 2>(tm_packed, tm_scales, tm_x, a, grid, stream);
   if (err != cudaSuccess || cudaGetLastError() != cudaSuccess) return NVFP4_ERR_CUDA;
   return NVFP4_OK;
+}
+
+nvfp4_status lm_head_launch(const void* x, int64_t M, int64_t K, const uint8_t* packed,
+                            const uint8_t* scales, const float* global_scale, int64_t N,
+                            void* logits, int out_mode, int64_t* token_ids, float* max_logits,
+                            void* workspace, cudaStream_t stream) {
+  return lm_head_run(x, M, K, packed, scales, global_scale, N, logits, out_mode, token_ids,
+                     max_logits, 0, workspace, stream);
+}
+
+nvfp4_status lm_head_topk_launch(const void* x, int64_t M, int64_t K, const uint8_t* packed,
+                                 const uint8_t* scales, const float* global_scale, int64_t N,
+                                 int k, int64_t* token_ids, float* values, void* workspace,
+                                 cudaStream_t stream) {
+  return lm_head_run(x, M, K, packed, scales, global_scale, N, nullptr, kOutTopk, token_ids,
+                     values, k, workspace, stream);
 }
 
 // ------------------------------------------------------------ grouped product
@@ -657,7 +699,8 @@ nvfp4_status grouped_launch(const void* x, int64_t M, int64_t K, const int32_t* 
                            static_cast<const uint16_t*>(x), M, K, M,
                            (const float*)nullptr, x16, tok_scale, status,
                            reinterpret_cast<uint32_t*>(ws + L.cnt), (int)((L.part - L.cnt) / 4),
-                           (unsigned long long*)nullptr, grp_off, grp_global,
+                           (unsigned long long*)nullptr, (uint32_t*)nullptr, (int64_t)0,
+                           grp_off, grp_global,
                            (int)n_groups) != cudaSuccess)
       return NVFP4_ERR_CUDA;
   }

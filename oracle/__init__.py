@@ -19,6 +19,9 @@ What each function follows is stated in ``nvfp4_oracle.c``.  In short:
   ``quantized_lm_head_copy`` (same lm_head page): per-row E4M3 weights with an
   fp32 scale amax/448, per-token E4M3 activations likewise, and the W8A8
   product xs * ws * (q_x . q_w) in float64.
+* ``topk`` -- the k largest logits of each token (the sampler's top-k filter
+  applied to the lm_head output; the pages define the logits, this selection
+  is the plain definition: descending value, of equal values the smaller row).
 
 Parity: every function is pinned in ``tests/test_oracle_*.py`` against what
 the pages fix (the code table, the packing order, K % 16), closed forms,
@@ -290,6 +293,14 @@ def fp8_logits(xq: np.ndarray, xs: np.ndarray, wq: np.ndarray, ws: np.ndarray,
     _load().oracle_fp8_logits_cols(_ptr(xq), _ptr(xs), M, K, _ptr(wq), _ptr(ws), _ptr(cols),
                                    cols.size, _ptr(out))
     return out
+
+
+def topk(L: np.ndarray, k: int) -> tuple[np.ndarray, np.ndarray]:
+    """Rows and values of the k largest entries of each row of L ([M, N]
+    float64, no NaN), largest first, of equal values the smaller index first:
+    a stable sort of the negated values."""
+    order = np.argsort(-L, axis=1, kind="stable")[:, :k]
+    return order, np.take_along_axis(L, order, axis=1)
 
 
 def num_threads() -> int:

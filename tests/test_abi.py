@@ -36,7 +36,8 @@ def test_header_declares_the_boundary():
               "w4a16_lm_head_argmax", "w4a16_lm_head_argmax_workspace_bytes",
               "fp8_quantize_rows", "fp8_refresh", "w8a8_lm_head", "w8a8_lm_head_argmax",
               "nvfp4_swizzle_scales", "w4a4_lm_head", "w4a4_lm_head_argmax",
-              "w4a16_grouped_gemm", "w4a16_grouped_workspace_bytes"):
+              "w4a16_grouped_gemm", "w4a16_grouped_workspace_bytes", "w4a16_lm_head_topk",
+              "w4a16_lm_head_topk_workspace_bytes"):
         assert n in names
 
 
@@ -163,3 +164,28 @@ def test_argmax_workspace_sizes(lib):
         plain = lib.w4a16_lm_head_workspace_bytes(M, 128256, 4096)
         am = lib.w4a16_lm_head_argmax_workspace_bytes(M, 128256, 4096)
         assert am >= plain + 128 * M
+
+
+def test_topk_host_argument_errors_and_sizes(lib):
+    vp = ctypes.c_void_p
+    fake = vp(1 << 20)
+    ids, vals = vp(1 << 20), vp(1 << 21)
+    big = 1 << 44
+    t = lib.w4a16_lm_head_topk
+    assert t(fake, 4, 256, fake, fake, fake, 100, 0, ids, vals, fake, big, None) == 1     # k == 0
+    assert t(fake, 4, 256, fake, fake, fake, 1000, 129, ids, vals, fake, big, None) == 1  # k > max
+    assert t(fake, 4, 256, fake, fake, fake, 7, 8, ids, vals, fake, big, None) == 1       # k > N
+    assert t(fake, 4, 300, fake, fake, fake, 100, 5, ids, vals, fake, big, None) == 1     # K % 256
+    assert t(fake, 1 << 20, 256, fake, fake, fake, 1 << 17, 5, ids, vals, fake, big,
+             None) == 1                                                                   # M*N > 2^36
+    assert t(fake, 0, 256, fake, fake, fake, 100, 5, ids, vals, None, 0, None) == 0      # empty
+    assert t(fake, 4, 256, fake, fake, fake, 100, 5, None, vals, fake, big, None) == 3   # NULL ids
+    assert t(fake, 4, 256, fake, fake, fake, 100, 5, ids, vals, fake, 4096, None) == 4   # WORKSPACE
+    assert t(fake, 4, 256, fake, fake, fake, 100, 5, vp((1 << 20) + 4), vals, fake, big,
+             None) == 2                                                                   # ALIGN ids
+    sz = lib.w4a16_lm_head_topk_workspace_bytes
+    assert sz(4, 0, 256, 1) == 0 and sz(4, 100, 256, 0) == 0 and sz(4, 100, 256, 129) == 0
+    for M in (1, 64, 2048):
+        am = lib.w4a16_lm_head_argmax_workspace_bytes(M, 128256, 4096)
+        tk = sz(M, 128256, 4096, 50)
+        assert tk >= am + M * 128256 * 8 + M * (128256 // 128) * 4
