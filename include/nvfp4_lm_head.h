@@ -224,9 +224,10 @@ nvfp4_status w4a16_lm_head_argmax(const void *x, int64_t M, int64_t K, const uin
 /*
  * Workspace bytes w4a16_lm_head_topk needs (0 for rejected shapes): those of
  * w4a16_lm_head_argmax plus the candidate store, M x N x 8 bytes (every
- * logit is a candidate at most once), and M x ceil(N / B) 4-byte block
- * counts, B = max(64, 2k rounded up to a power of two).  Only the
- * candidates that reach their token's threshold are ever written.
+ * logit is a candidate at most once), 8 bytes per token and 32 rows of
+ * candidate flags, and a 4,112-byte histogram per token (rounded up to the
+ * token tile).  Only the candidates that reach their token's threshold are
+ * ever written.
  */
 size_t w4a16_lm_head_topk_workspace_bytes(int64_t M, int64_t N, int64_t K, int64_t k);
 
@@ -240,9 +241,9 @@ size_t w4a16_lm_head_topk_workspace_bytes(int64_t M, int64_t N, int64_t K, int64
  * returned as +0) and a NaN above every number, as in w4a16_lm_head_argmax
  * (whose answer is column 0 here).  The [M, N] logits are never written:
  * the epilogue appends only the logits that reach the token's running
- * threshold, a lower bound of its k-th largest that rises as blocks of
- * candidates complete, and a second kernel selects the exact k largest of
- * those.  The result does not depend on the schedule.
+ * threshold, a lower bound of its k-th largest that rises with a histogram
+ * of the candidates appended so far, and a second kernel selects the exact
+ * k largest of those.  The result does not depend on the schedule.
  *
  * The pages define the logits, not a sampler; this is the top-k filter a
  * sampler applies to them, for the same reason as the argmax.

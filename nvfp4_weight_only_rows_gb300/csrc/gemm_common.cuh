@@ -55,11 +55,12 @@ struct GemmArgs {
   // top-k output mode only (am_keys then holds per token line: word 0 the
   // threshold key, a lower bound of the token's k-th largest candidate
   // key; word 1 the number of candidates appended)
-  unsigned long long* tk_cand;  // [M][N] candidate keys in append order
-  uint32_t* tk_blk;             // [m_pad][tk_nblk] entries written per candidate block
+  unsigned long long* tk_cand;  // [M][N] candidate keys, slot n for row n
+  uint2* tk_grp;                // [M][tk_groups] per 32 rows: {largest candidate order key,
+                                //   bit j: slot 32g + j holds a candidate}
+  int64_t tk_groups;            // ceil(N / 32)
+  uint32_t* tk_hist;            // [m_pad][kHistWords] histograms of the candidate keys
   int tk_k;                     // k, 1 .. kTopkMax
-  int tk_blog2;                 // log2 of the candidate block (>= 2k, >= 64)
-  int64_t tk_nblk;              // candidate blocks per token, ceil(N / block)
   const float* row_scale;       // [N] per-row weight scale (fp8 weights), else null
   // grouped product (experts) only
   const int32_t* grp_off;       // [n_groups + 1] token row offsets of the groups
@@ -258,105 +259,137 @@ __device__ __forceinline__ float key_value(uint32_t k) {
 
 // ------------------------------------------------------------ fused top-k
 // Per token: a threshold key T (a lower bound of the token's k-th largest
-// candidate key, so every one of its k largest logits reaches it), a count
-// of appended candidates and the candidates themselves, N slots (every
-// logit is appended at most once).  The slots are cut into blocks of
-// B >= 2k; each block carries a count of entries written, and the warp whose
-// entries complete a block reads it back and raises T to the k-th largest
-// key among those B entries (k real logits of the token reach it).  T is
-// kept as (high word << 32): only the value part is selected, which is still
-// a valid lower bound.
+// candidate key, so every one of its k largest logits reaches it), the
+// largest candidate order key, a histogram of candidate order keys and the
+// candidates themselves: the key of a logit that reached T sits in slot n
+// of the token's N slots.  Per token and group of 32 rows, the warp that
+// owns the group writes {largest candidate order key, bitmap of the slots
+// it filled} ({0, 0} without candidates), so the groups are complete
+// without clearing and the selection skips every group below its final T.
+// Histogram bins: all negative keys; positive keys below 2^-32; a
+// sixteenth of an octave each from 2^-32 to 2^32 (exponent and top 4
+// mantissa bits); 2^32 and above.  A candidate within an octave of its
+// group's largest adds one to its bin (an atomic add without a reply; the
+// others cannot hold the k-th largest unless the group holds an outlier,
+// and leaving them out only lowers the bin found).  A threshold warp in
+// every CTA keeps walking its tokens' bins down from the largest key's bin
+// to the one that holds the k-th counted candidate and raises T to that
+// bin's lower edge: at least k candidates of the token reach it (counts and
+// the maximum only ever lag, which lowers the edge, never invalidates it).
+constexpr int kHistBins = 1027;
+constexpr int kHistWords = 1028;  // u32 per token (whole 16-byte vectors)
+
+__device__ __forceinline__ uint32_t topk_bin(uint32_t ok) {
+  if (ok < 0x80000000u) return 0u;
+  const uint32_t e = (ok >> 23) & 0xFFu;
+  if (e < 96u) return 1u;
+  if (e >= 160u) return (uint32_t)kHistBins - 1u;
+  return 2u + ((e - 96u) << 4) + ((ok >> 19) & 15u);
+}
+__device__ __forceinline__ unsigned long long topk_edge(uint32_t bin) {
+  uint32_t ok;
+  if (bin == 0u) return 0ull;
+  if (bin == 1u) ok = 0x80000000u;
+  else if (bin == (uint32_t)kHistBins - 1u) ok = 0x80000000u | (160u << 23);
+  else ok = 0x80000000u | ((96u + ((bin - 2u) >> 4)) << 23) | (((bin - 2u) & 15u) << 19);
+  return (unsigned long long)ok << 32;
+}
+
 __device__ __forceinline__ unsigned long long* topk_thr(const GemmArgs& p, int64_t tok) {
   return p.am_keys + tok * kKeyStride;
 }
-__device__ __forceinline__ uint32_t* topk_cnt(const GemmArgs& p, int64_t tok) {
-  return reinterpret_cast<uint32_t*>(p.am_keys + tok * kKeyStride + 1);
+__device__ __forceinline__ uint32_t* topk_max(const GemmArgs& p, int64_t tok) {
+  return reinterpret_cast<uint32_t*>(p.am_keys + tok * kKeyStride + 2);
 }
 
-// The k-th largest value word among the B entries of block j of token
-// `tok`, merged into its threshold (whole warp; every entry has been
-// written and made visible before the block count reached B).
-__device__ __forceinline__ void topk_raise(const GemmArgs& p, int64_t tok, uint32_t j, int lane) {
-  const unsigned long long* blk = p.tk_cand + tok * p.N + ((int64_t)j << p.tk_blog2);
-  const int per_lane = (1 << p.tk_blog2) >> 5;  // 2 .. 8
-  uint32_t h[8];
-#pragma unroll
-  for (int i = 0; i < 8; ++i)
-    h[i] = i < per_lane ? (uint32_t)(__ldcg(blk + i * 32 + lane) >> 32) : 0u;
-  // bit by bit from the top: the answer has bit b set iff at least `need`
-  // entries match the answer's higher bits with bit b set
-  uint32_t prefix = 0;
+__device__ __forceinline__ void red_add_u32(uint32_t* a, uint32_t v) {
+  asm volatile("red.relaxed.gpu.global.add.u32 [%0], %1;" ::"l"(a), "r"(v) : "memory");
+}
+__device__ __forceinline__ void red_max_u32(uint32_t* a, uint32_t v) {
+  asm volatile("red.relaxed.gpu.global.max.u32 [%0], %1;" ::"l"(a), "r"(v) : "memory");
+}
+
+// Raise token `tok`'s threshold to the lower edge of the histogram bin that
+// holds its k-th largest counted candidate (whole warp): 32 bins per step,
+// downwards from the bin of the largest candidate key.
+__device__ __forceinline__ void topk_raise(const GemmArgs& p, int64_t tok, int lane) {
+  const uint32_t* h = p.tk_hist + tok * kHistWords;
+  int hi = (int)topk_bin(__ldcg(topk_max(p, tok)));
   uint32_t need = (uint32_t)p.tk_k;
 #pragma unroll 1
-  for (int b = 31; b >= 0; --b) {
-    const uint32_t hmask = ~((1u << b) - 1u);
-    const uint32_t want = prefix | (1u << b);
-    uint32_t c = 0;
+  for (; hi >= 0; hi -= 32) {
+    const int bin = hi - lane;
+    const uint32_t c = bin >= 0 ? __ldcg(h + bin) : 0u;
+    uint32_t incl = c;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) c += (i < per_lane && (h[i] & hmask) == want) ? 1u : 0u;
-    c = __reduce_add_sync(0xFFFFFFFFu, c);
-    if (c >= need) prefix = want;
-    else need -= c;
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    const uint32_t hit = __ballot_sync(0xFFFFFFFFu, incl >= need);
+    if (hit) {
+      if (lane == 0) atomicMax(topk_thr(p, tok), topk_edge((uint32_t)(hi - (__ffs(hit) - 1))));
+      return;
+    }
+    need -= __shfl_sync(0xFFFFFFFFu, incl, 31);
   }
-  if (lane == 0) atomicMax(topk_thr(p, tok), (unsigned long long)prefix << 32);
 }
 
-// One chunk of 16 tokens (token rows tc .. tc + 15) in which some lane
-// reached its token's threshold: append the passing candidates of each
-// token, count them into their blocks, and raise the thresholds of the
-// blocks this warp completes.  Lane t < 16 does token t's atomics, so the
-// sixteen tokens' round trips overlap.
+// The threshold warp of a CTA: tokens blockIdx.x, + gridDim.x, ... (below
+// M), one raise each per sweep, until the CTA's four epilogue warps have
+// counted themselves out in *epi_done (or a time limit passes).
+__device__ __forceinline__ void topk_threshold_role(const GemmArgs& p, volatile int32_t* epi_done,
+                                                    int lane) {
+  if ((int64_t)blockIdx.x >= p.M) return;
+  const uint64_t t0 = globaltimer_ns();
+  while (*epi_done < 4) {
+    for (int64_t tok = blockIdx.x; tok < p.M; tok += gridDim.x) topk_raise(p, tok, lane);
+    if (globaltimer_ns() - t0 > 4 * kWaitLimitNs) return;
+    __nanosleep(500);
+  }
+}
+
+// One chunk of 16 tokens (token rows tc .. tc + 15) x the warp's 32 rows
+// (n = n_base + lane): where some row reached its token's threshold, the
+// candidates, their histogram counts and each token's maximum; then the
+// group words (lane t < 16 owns token t's).  The epilogue shares its SM
+// sub-partitions with the dequant warps, so what counts is instructions:
+// one vote per token, and the rest only for the tokens that have
+// candidates (a warp-uniform branch).
 __device__ __forceinline__ void topk_chunk(const GemmArgs& p, int64_t tc, int64_t t_end,
                                            const float (&val)[16], const float (&thr)[16],
-                                           bool valid, uint32_t n, int lane) {
-  uint32_t my_bal = 0;
+                                           bool valid, bool any, uint32_t n_base, int lane) {
+  uint32_t my_bal = 0, my_mx = 0;
+  if (any) {
+    const uint32_t n = n_base + (uint32_t)lane;
+    const int64_t live = t_end - tc;  // tokens of the chunk below t_end
+    uint32_t b[16];
 #pragma unroll
-  for (int t = 0; t < 16; ++t) {
-    const uint32_t bal = __ballot_sync(0xFFFFFFFFu, valid && !(val[t] < thr[t]));
-    if (lane == t) my_bal = bal;
+    for (int t = 0; t < 16; ++t)
+      b[t] = __ballot_sync(0xFFFFFFFFu, valid && t < live && !(val[t] < thr[t]));
+#pragma unroll
+    for (int t = 0; t < 16; ++t) {
+      if (b[t] == 0u) continue;  // warp-uniform
+      const bool mine = (b[t] >> lane) & 1u;
+      const uint32_t ok = order_key(val[t]);
+      const uint32_t mx = __reduce_max_sync(0xFFFFFFFFu, mine ? ok : 0u);
+      if (lane == t) {
+        my_bal = b[t];
+        my_mx = mx;
+      }
+      if (mine) {
+        const int64_t tok = tc + t;
+        p.tk_cand[tok * p.N + n] = ((unsigned long long)ok << 32) | (uint32_t)~n;
+        // half the group's largest: lower candidates are not counted
+        const uint32_t floor = mx >= 0x80800000u ? mx - 0x00800000u : 0u;
+        if (ok >= floor) red_add_u32(p.tk_hist + tok * kHistWords + topk_bin(ok), 1u);
+      }
+    }
+    if (my_bal) red_max_u32(topk_max(p, tc + lane), my_mx);  // lane t < 16, live tokens only
   }
   const int64_t my_tok = tc + lane;
-  const uint32_t my_n = (lane < 16 && my_tok < t_end) ? __popc(my_bal) : 0u;
-  uint32_t base = 0;
-  if (my_n) base = atomicAdd(topk_cnt(p, my_tok), my_n);
-  const uint32_t lt = (1u << lane) - 1u;
-#pragma unroll
-  for (int t = 0; t < 16; ++t) {
-    const uint32_t nt = __shfl_sync(0xFFFFFFFFu, my_n, t);
-    if (nt == 0) continue;
-    const uint32_t bal = __shfl_sync(0xFFFFFFFFu, my_bal, t);
-    const uint32_t b = __shfl_sync(0xFFFFFFFFu, base, t);
-    if ((bal >> lane) & 1u) {
-      const uint32_t idx = b + __popc(bal & lt);
-      if ((int64_t)idx < p.N)
-        p.tk_cand[(tc + t) * p.N + idx] =
-            ((unsigned long long)order_key(val[t]) << 32) | (uint32_t)~n;
-    }
-  }
-  __threadfence();  // the entries are visible before their block counts
-  __syncwarp();
-  uint32_t chk = 0;  // bit 0: this lane's token completed its first block, bit 1: its second
-  uint32_t j0 = 0, j1 = 0;
-  if (my_n && (int64_t)(base + my_n) <= p.N) {
-    const uint32_t B = 1u << p.tk_blog2;
-    j0 = base >> p.tk_blog2;
-    j1 = (base + my_n - 1) >> p.tk_blog2;
-    uint32_t* cnt = p.tk_blk + my_tok * p.tk_nblk;
-    const uint32_t n0 = j0 == j1 ? my_n : (j1 << p.tk_blog2) - base;
-    if (atomicAdd(cnt + j0, n0) + n0 == B) chk |= 1u;
-    if (j1 != j0 && atomicAdd(cnt + j1, my_n - n0) + (my_n - n0) == B) chk |= 2u;
-  }
-  uint32_t todo = __ballot_sync(0xFFFFFFFFu, chk != 0);
-  if (todo) __threadfence();  // the completed blocks' entries are read after the counts
-  while (todo) {
-    const int t = __ffs(todo) - 1;
-    todo &= todo - 1;
-    const uint32_t ck = __shfl_sync(0xFFFFFFFFu, chk, t);
-    const uint32_t a0 = __shfl_sync(0xFFFFFFFFu, j0, t);
-    const uint32_t a1 = __shfl_sync(0xFFFFFFFFu, j1, t);
-    if (ck & 1u) topk_raise(p, tc + t, a0, lane);
-    if (ck & 2u) topk_raise(p, tc + t, a1, lane);
-  }
+  if (lane < 16 && my_tok < t_end && (int64_t)n_base < p.N)
+    p.tk_grp[my_tok * p.tk_groups + (n_base >> 5)] = make_uint2(my_mx, my_bal);
 }
 
 // ------------------------------------------------------------ schedule
@@ -450,6 +483,18 @@ __device__ __forceinline__ void epilogue_role(const GemmArgs& p, const Sched& sc
     __syncwarp();
     if (!warp_wait(&d_full[buf], dph, wc)) return false;
     tc_fence_after();
+    if (kOut == kOutTopk && i <= 2) {
+      // top-k thresholds rise fastest while the first units' accumulators
+      // fill: for those, read them again
+      for (int t = lane; t < BN; t += 32) {
+        if (t0 + t < t_end) {
+          const uint32_t kh = __ldcg(
+              reinterpret_cast<const uint32_t*>(p.am_keys + (t0 + t) * kKeyStride) + 1);
+          if (kh) wthr[t] = key_value(kh);
+        }
+      }
+      __syncwarp();
+    }
     // A tail unit cut by a range boundary: its two CTAs share slot `key`
     // (the CTA whose tail range starts inside the unit).  The first to get here parks
     // its fp32 partial; the second adds it to its own and stores logits.
@@ -490,7 +535,7 @@ __device__ __forceinline__ void epilogue_role(const GemmArgs& p, const Sched& sc
       }
       if (kOut == kOutTopk) {
         // the logits as for argmax; one vote per chunk on the thresholds,
-        // then the appends of the tokens that some row reached
+        // then the bitmap words and the candidates
         const bool valid = n < p.N;
         float thr[16], mul[16], val[16];
         lds_f32x16(wthr + c, thr);
@@ -506,8 +551,8 @@ __device__ __forceinline__ void epilogue_role(const GemmArgs& p, const Sched& sc
           pass |= !(r.x < thr[t]);
           pass |= !(r.y < thr[t + 1]);
         }
-        if (__any_sync(0xFFFFFFFFu, valid && pass))
-          topk_chunk(p, t0 + c, t_end, val, thr, valid, (uint32_t)n, lane);
+        topk_chunk(p, t0 + c, t_end, val, thr, valid, __any_sync(0xFFFFFFFFu, valid && pass),
+                   (uint32_t)(n - lane), lane);
       } else if (kOut == kOutArgmax) {
         // The logits as the plain product rounds them (the fma with +0
         // rounds like the multiply and turns an exact -0 into +0), then one
@@ -665,22 +710,15 @@ static int sm_count() {
 // the prep kernel's first CTA.  Then [split partials, grid x 4 x BN x 32
 // fp32] and, for argmax and top-k, [per-token state, m_pad x 128 bytes: the
 // maximum or the threshold key in word 0, the top-k candidate count in word
-// 1], both words zeroed by the prep CTA of the token.  Top-k only: [block
-// counts, m_pad x ceil(N / block) u32, zeroed the same way][candidates,
-// M x N u64, written before they are read].
+// 1], both words zeroed by the prep CTA of the token.  Top-k only:
+// [histograms, m_pad x kHistWords u32, zeroed the same way][candidate
+// groups, M x ceil(N / 32) x 8 bytes, all written by the GEMM][candidates,
+// M x N u64, read only where the group words say].
 struct WsLayout {
-  size_t x16, tok, cnt, ready, done, keys, part, blk, cand, total;
+  size_t x16, tok, cnt, ready, done, keys, part, hist, grp, cand, total;
   int grid;
-  int tk_blog2;
-  int64_t tk_nblk;
 };
 
-// log2 of the top-k candidate block: at least 2k entries and 64 (two per lane)
-static int topk_block_log2(int k) {
-  int b = 6;
-  while ((1 << b) < 2 * k) ++b;
-  return b;
-}
 
 static WsLayout ws_layout(int64_t M, int64_t N, int64_t K, int sms, bool argmax, int x_bytes,
                           int topk_k = 0) {
@@ -697,18 +735,17 @@ static WsLayout ws_layout(int64_t M, int64_t N, int64_t K, int sms, bool argmax,
   l.done = l.ready + align_up((size_t)l.grid * 4 * 4, 256);
   l.part = l.done + (keys ? 256 : 0);
   l.keys = l.part + align_up((size_t)l.grid * 4 * BN * 32 * 4, 256);
-  l.blk = l.keys + (keys ? (size_t)m_pad * kKeyStride * 8 : 0);
-  l.tk_blog2 = topk_k > 0 ? topk_block_log2(topk_k) : 0;
-  l.tk_nblk = topk_k > 0 ? (N + (1 << l.tk_blog2) - 1) >> l.tk_blog2 : 0;
-  l.cand = l.blk + align_up((size_t)m_pad * l.tk_nblk * 4, 256);
+  l.hist = l.keys + (keys ? (size_t)m_pad * kKeyStride * 8 : 0);
+  l.grp = l.hist + (topk_k > 0 ? (size_t)m_pad * kHistWords * 4 : 0);
+  l.cand = l.grp + (topk_k > 0 ? align_up((size_t)M * ((N + 31) / 32) * 8, 256) : 0);
   l.total = l.cand + (topk_k > 0 ? (size_t)M * N * 8 : 0);
   return l;
 }
 
 // The top-k selection kernel (topk.cu), launched after a top-k GEMM.
-cudaError_t topk_select_launch(const unsigned long long* lines, const unsigned long long* cand,
-                               int64_t M, int64_t N, int k, int64_t* ids, float* vals,
-                               cudaStream_t stream);
+cudaError_t topk_select_launch(const unsigned long long* lines, const uint2* grp,
+                               const unsigned long long* cand, int64_t M, int64_t N, int k,
+                               int64_t* ids, float* vals, cudaStream_t stream);
 
 // Split the units of a call into strided whole-unit waves and a stream-K
 // tail: all but the last one to two waves run whole; the rest is split

@@ -82,8 +82,7 @@ __global__ void __launch_bounds__(256) w4a16_prep_x_kernel(const uint16_t* __res
                                                            uint32_t* __restrict__ split_flags,
                                                            int n_split_flags,
                                                            unsigned long long* __restrict__ am_keys,
-                                                           uint32_t* __restrict__ tk_blk,
-                                                           int64_t tk_nblk,
+                                                           uint32_t* __restrict__ tk_hist,
                                                            const int32_t* __restrict__ grp_off,
                                                            const float* __restrict__ grp_global,
                                                            int n_groups) {
@@ -110,9 +109,12 @@ __global__ void __launch_bounds__(256) w4a16_prep_x_kernel(const uint16_t* __res
   if (am_keys && lane == 0) {  // argmax / top-k: no candidate yet
     am_keys[m * kKeyStride] = 0ull;
     am_keys[m * kKeyStride + 1] = 0ull;
+    am_keys[m * kKeyStride + 2] = 0ull;
   }
-  if (tk_blk)  // top-k: no candidate block written yet
-    for (int64_t i = lane; i < tk_nblk; i += kT) tk_blk[m * tk_nblk + i] = 0u;
+  if (tk_hist) {  // top-k: no candidate counted yet
+    uint4* h = reinterpret_cast<uint4*>(tk_hist + m * kHistWords);
+    for (int i = lane; i < kHistWords / 4; i += kT) h[i] = make_uint4(0, 0, 0, 0);
+  }
   uint4* d4 = reinterpret_cast<uint4*>(x16 + m * K);
   const int64_t nv = K / 8;
   if (m >= M) {  // padding rows of the last token tile
@@ -221,8 +223,14 @@ __device__ __forceinline__ uint32_t dup_hi(uint32_t v) { return __byte_perm(v, 0
 // the candidates for each token's k largest (topk.cu selects them).
 // kGrouped: the grouped (experts) product: weight rows e * N + n, token rows
 // grouped by the offsets in p.grp_off, one global scale per group.
+// Threads of one CTA: the shape's roles, plus the threshold warp in top-k mode.
+template <int kOut, int kStages, int kPStages, int kDq>
+constexpr int gemm_threads() {
+  return GemmShape<kStages, kPStages, kDq>::kThreads + (kOut == kOutTopk ? 32 : 0);
+}
+
 template <int kOut, int kStages, int kPStages, int kDqPerQuad, bool kGrouped = false>
-__global__ void __launch_bounds__((GemmShape<kStages, kPStages, kDqPerQuad>::kThreads), 1)
+__global__ void __launch_bounds__((gemm_threads<kOut, kStages, kPStages, kDqPerQuad>()), 1)
     w4a16_tc_kernel(const __grid_constant__ CUtensorMap tm_packed,
                     const __grid_constant__ CUtensorMap tm_scales,
                     const __grid_constant__ CUtensorMap tm_x, const GemmArgs p) {
@@ -279,6 +287,7 @@ __global__ void __launch_bounds__((GemmShape<kStages, kPStages, kDqPerQuad>::kTh
     }
     mbar_init(done_bar, 1);
     *abort_flag = 0;
+    if (kOut == kOutTopk) s_last[1] = 0;  // epilogue warps done (the region exists in this mode)
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
@@ -449,10 +458,14 @@ __global__ void __launch_bounds__((GemmShape<kStages, kPStages, kDqPerQuad>::kTh
       __syncwarp();
       if (lane == 0) mbar_arrive(&s_full[st]);
     }
-  } else {
+  } else if (warp < kFirstEpiWarp + 4) {
     // ---------------- epilogue: one thread per vocabulary row, BN tokens
     epilogue_role<kOut, false, kGrouped>(p, sc, warp, warp - kFirstEpiWarp, lane, tmem_base,
                                          d_full, d_empty, wc, s_tok, s_thr);
+    if (kOut == kOutTopk && lane == 0) atomicAdd(s_last + 1, 1);  // this warp is done
+  } else {
+    // ---------------- top-k thresholds (only launched in top-k mode)
+    topk_threshold_role(p, s_last + 1, lane);
   }
 
   __syncthreads();
@@ -495,7 +508,7 @@ static cudaError_t launch_gemm(const CUtensorMap& tm_packed, const CUtensorMap& 
   if (attr_err != cudaSuccess) return attr_err;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)grid);
-  cfg.blockDim = dim3(GemmShape<kStages, kPStages, kDq>::kThreads);
+  cfg.blockDim = dim3(gemm_threads<kOut, kStages, kPStages, kDq>());
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
@@ -564,7 +577,7 @@ static nvfp4_status lm_head_run(const void* x, int64_t M, int64_t K, const uint8
                            global_scale, x16, tok_scale, status, split_cnt,
                            (int)((L.part - L.cnt) / 4),
                            keys ? reinterpret_cast<unsigned long long*>(ws + L.keys) : nullptr,
-                           topk ? reinterpret_cast<uint32_t*>(ws + L.blk) : nullptr, L.tk_nblk,
+                           topk ? reinterpret_cast<uint32_t*>(ws + L.hist) : nullptr,
                            nullptr, nullptr, 0) != cudaSuccess)
       return NVFP4_ERR_CUDA;
   }
@@ -586,10 +599,10 @@ static nvfp4_status lm_head_run(const void* x, int64_t M, int64_t K, const uint8
   a.am_idx = token_ids;
   a.am_val = max_logits;
   a.tk_cand = topk ? reinterpret_cast<unsigned long long*>(ws + L.cand) : nullptr;
-  a.tk_blk = topk ? reinterpret_cast<uint32_t*>(ws + L.blk) : nullptr;
+  a.tk_hist = topk ? reinterpret_cast<uint32_t*>(ws + L.hist) : nullptr;
+  a.tk_grp = topk ? reinterpret_cast<uint2*>(ws + L.grp) : nullptr;
+  a.tk_groups = (N + 31) / 32;
   a.tk_k = topk_k;
-  a.tk_blog2 = L.tk_blog2;
-  a.tk_nblk = L.tk_nblk;
   a.row_scale = nullptr;
   // decode-sized token tiles get a third A stage, six packed stages and a
   // third dequant warp per quadrant; 128-token tiles leave TMEM room for two
@@ -615,7 +628,8 @@ static nvfp4_status lm_head_run(const void* x, int64_t M, int64_t K, const uint8
     err = deep ? launch_gemm<kOutTopk, 3, 6, 3>(tm_packed, tm_scales, tm_x, a, grid, stream)
                : launch_gemm<kOutTopk, 2, 4, 2>(tm_packed, tm_scales, tm_x, a, grid, stream);
     if (err == cudaSuccess)
-      err = topk_select_launch(a.am_keys, a.tk_cand, M, N, topk_k, token_ids, max_logits, stream);
+      err = topk_select_launch(a.am_keys, a.tk_grp, a.tk_cand, M, N, topk_k, token_ids,
+                               max_logits, stream);
   } else if (out_mode == NVFP4_OUT_BF16)
     err = deep ? launch_gemm<NVFP4_OUT_BF16, 3, 6, 3>(tm_packed, tm_scales, tm_x, a, grid, stream)
                : launch_gemm<NVFP4_OUT_BF16, 2, 4, 2>(tm_packed, tm_scales, tm_x, a, grid, stream);
@@ -699,7 +713,7 @@ nvfp4_status grouped_launch(const void* x, int64_t M, int64_t K, const int32_t* 
                            static_cast<const uint16_t*>(x), M, K, M,
                            (const float*)nullptr, x16, tok_scale, status,
                            reinterpret_cast<uint32_t*>(ws + L.cnt), (int)((L.part - L.cnt) / 4),
-                           (unsigned long long*)nullptr, (uint32_t*)nullptr, (int64_t)0,
+                           (unsigned long long*)nullptr, (uint32_t*)nullptr,
                            grp_off, grp_global,
                            (int)n_groups) != cudaSuccess)
       return NVFP4_ERR_CUDA;
