@@ -223,7 +223,7 @@ nvfp4_status w4a16_lm_head_argmax(const void *x, int64_t M, int64_t K, const uin
 
 /*
  * Workspace bytes w4a16_lm_head_topk needs (0 for rejected shapes): those of
- * w4a16_lm_head_argmax plus the candidate store, M x N x 8 bytes (every
+ * w4a16_lm_head_argmax plus the candidate store, M x N x 4 bytes (every
  * logit is a candidate at most once), 8 bytes per token and 32 rows of
  * candidate flags, and a 4,112-byte histogram per token (rounded up to the
  * token tile).  Only the candidates that reach their token's threshold are

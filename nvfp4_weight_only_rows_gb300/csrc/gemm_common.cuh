@@ -55,7 +55,7 @@ struct GemmArgs {
   // top-k output mode only (am_keys then holds per token line: word 0 the
   // threshold key, a lower bound of the token's k-th largest candidate
   // key; word 1 the number of candidates appended)
-  unsigned long long* tk_cand;  // [M][N] candidate keys, slot n for row n
+  uint32_t* tk_cand;            // [M][N] candidate order keys, slot n for row n
   uint2* tk_grp;                // [M][tk_groups] per 32 rows: {largest candidate order key,
                                 //   bit j: slot 32g + j holds a candidate}
   int64_t tk_groups;            // ceil(N / 32)
@@ -261,8 +261,8 @@ __device__ __forceinline__ float key_value(uint32_t k) {
 // Per token: a threshold key T (a lower bound of the token's k-th largest
 // candidate key, so every one of its k largest logits reaches it), the
 // largest candidate order key, a histogram of candidate order keys and the
-// candidates themselves: the key of a logit that reached T sits in slot n
-// of the token's N slots.  Per token and group of 32 rows, the warp that
+// candidates themselves: the order key of a logit that reached T sits in
+// slot n of the token's N slots (the row is the slot).  Per token and group of 32 rows, the warp that
 // owns the group writes {largest candidate order key, bitmap of the slots
 // it filled} ({0, 0} without candidates), so the groups are complete
 // without clearing and the selection skips every group below its final T.
@@ -340,6 +340,9 @@ __device__ __forceinline__ void topk_raise(const GemmArgs& p, int64_t tok, int l
 // counted themselves out in *epi_done (or a time limit passes).
 __device__ __forceinline__ void topk_threshold_role(const GemmArgs& p, volatile int32_t* epi_done,
                                                     int lane) {
+  // the histograms, maxima and thresholds are cleared by the prep kernel,
+  // which may still be running: nothing is read before it has finished
+  grid_dependency_wait();
   if ((int64_t)blockIdx.x >= p.M) return;
   const uint64_t t0 = globaltimer_ns();
   while (*epi_done < 4) {
@@ -379,7 +382,7 @@ __device__ __forceinline__ void topk_chunk(const GemmArgs& p, int64_t tc, int64_
       }
       if (mine) {
         const int64_t tok = tc + t;
-        p.tk_cand[tok * p.N + n] = ((unsigned long long)ok << 32) | (uint32_t)~n;
+        p.tk_cand[tok * p.N + n] = ok;
         // half the group's largest: lower candidates are not counted
         const uint32_t floor = mx >= 0x80800000u ? mx - 0x00800000u : 0u;
         if (ok >= floor) red_add_u32(p.tk_hist + tok * kHistWords + topk_bin(ok), 1u);
@@ -713,7 +716,7 @@ static int sm_count() {
 // 1], both words zeroed by the prep CTA of the token.  Top-k only:
 // [histograms, m_pad x kHistWords u32, zeroed the same way][candidate
 // groups, M x ceil(N / 32) x 8 bytes, all written by the GEMM][candidates,
-// M x N u64, read only where the group words say].
+// M x N u32 order keys, read only where the group words say].
 struct WsLayout {
   size_t x16, tok, cnt, ready, done, keys, part, hist, grp, cand, total;
   int grid;
@@ -738,14 +741,14 @@ static WsLayout ws_layout(int64_t M, int64_t N, int64_t K, int sms, bool argmax,
   l.hist = l.keys + (keys ? (size_t)m_pad * kKeyStride * 8 : 0);
   l.grp = l.hist + (topk_k > 0 ? (size_t)m_pad * kHistWords * 4 : 0);
   l.cand = l.grp + (topk_k > 0 ? align_up((size_t)M * ((N + 31) / 32) * 8, 256) : 0);
-  l.total = l.cand + (topk_k > 0 ? (size_t)M * N * 8 : 0);
+  l.total = l.cand + (topk_k > 0 ? (size_t)M * N * 4 : 0);
   return l;
 }
 
 // The top-k selection kernel (topk.cu), launched after a top-k GEMM.
 cudaError_t topk_select_launch(const unsigned long long* lines, const uint2* grp,
-                               const unsigned long long* cand, int64_t M, int64_t N, int k,
-                               int64_t* ids, float* vals, cudaStream_t stream);
+                               const uint32_t* cand, int64_t M, int64_t N, int k, int64_t* ids,
+                               float* vals, cudaStream_t stream);
 
 // Split the units of a call into strided whole-unit waves and a stream-K
 // tail: all but the last one to two waves run whole; the rest is split

@@ -598,7 +598,7 @@ static nvfp4_status lm_head_run(const void* x, int64_t M, int64_t K, const uint8
   a.am_done = argmax ? reinterpret_cast<uint32_t*>(ws + L.done) : nullptr;
   a.am_idx = token_ids;
   a.am_val = max_logits;
-  a.tk_cand = topk ? reinterpret_cast<unsigned long long*>(ws + L.cand) : nullptr;
+  a.tk_cand = topk ? reinterpret_cast<uint32_t*>(ws + L.cand) : nullptr;
   a.tk_hist = topk ? reinterpret_cast<uint32_t*>(ws + L.hist) : nullptr;
   a.tk_grp = topk ? reinterpret_cast<uint2*>(ws + L.grp) : nullptr;
   a.tk_groups = (N + 31) / 32;

@@ -1,7 +1,7 @@
 // topk.cu -- the selection step of the fused top-k: the GEMM epilogue has
 // kept, per token, every logit that reached the token's running threshold
-// (a superset of its k largest; slot n of the candidates, flagged in the
-// word of its 32-row group); here one CTA per token picks the exact k
+// (a superset of its k largest; the order key of row n in slot n, flagged
+// in the word of its 32-row group); here one CTA per token picks the exact k
 // largest candidate keys, sorts them (larger logit first, of equal logits
 // the smaller row; a NaN above every number) and writes their rows and
 // logits.
@@ -24,8 +24,8 @@ constexpr int kRankMax = 512;  // at most this many keys: selection by rank (one
 // Every candidate key of one token at or above T, through the group words,
 // one thread at a time (the overflow path only).
 template <typename F>
-__device__ __noinline__ void topk_scan_slow(const uint2* gw, const unsigned long long* src,
-                                            int64_t G, int64_t N, unsigned long long T, F f) {
+__device__ __noinline__ void topk_scan_slow(const uint2* gw, const uint32_t* src, int64_t G,
+                                            int64_t N, unsigned long long T, F f) {
   const uint32_t t_hi = (uint32_t)(T >> 32);
 #pragma unroll 1
   for (int64_t g = threadIdx.x; g < G; g += blockDim.x) {
@@ -38,7 +38,8 @@ __device__ __noinline__ void topk_scan_slow(const uint2* gw, const unsigned long
       bits &= bits - 1;
       const int64_t slot = g * 32 + b;
       if (slot >= N) break;
-      const unsigned long long key = __ldcg(src + slot);
+      const unsigned long long key =
+          ((unsigned long long)__ldcg(src + slot) << 32) | (uint32_t)~(uint32_t)slot;
       if (key >= T) f(key);
     }
   }
@@ -46,7 +47,7 @@ __device__ __noinline__ void topk_scan_slow(const uint2* gw, const unsigned long
 
 __global__ void __launch_bounds__(kSelThreads) topk_select_kernel(
     const unsigned long long* __restrict__ lines, const uint2* __restrict__ grp,
-    const unsigned long long* __restrict__ cand, int64_t N, int k, int64_t* __restrict__ ids,
+    const uint32_t* __restrict__ cand, int64_t N, int k, int64_t* __restrict__ ids,
     float* __restrict__ vals) {
   // the candidates come from the GEMM, which may still be running
   asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -63,7 +64,7 @@ __global__ void __launch_bounds__(kSelThreads) topk_select_kernel(
   const uint32_t t_hi = (uint32_t)(T >> 32);  // key >= T  <=>  order key >= t_hi
   const int64_t G = (N + 31) / 32;
   const uint2* gw = grp + tok * G;
-  const unsigned long long* src = cand + tok * N;
+  const uint32_t* src = cand + tok * N;
   if (tid == 0) {
     s_n = 0;
     s_prefix = 0;
@@ -108,7 +109,8 @@ __global__ void __launch_bounds__(kSelThreads) topk_select_kernel(
           if (lane == src_lane) pass &= pass - 1;
           const int64_t slot = (g0 + u * 32 + src_lane) * 32 + lane;
           keep[v] = ((bj >> lane) & 1u) && slot < N;
-          if (keep[v]) key[v] = __ldcg(src + slot);
+          if (keep[v])
+            key[v] = ((unsigned long long)__ldcg(src + slot) << 32) | (uint32_t)~(uint32_t)slot;
         }
       }
 #pragma unroll
@@ -251,8 +253,8 @@ __global__ void __launch_bounds__(kSelThreads) topk_select_kernel(
 }
 
 cudaError_t topk_select_launch(const unsigned long long* lines, const uint2* grp,
-                               const unsigned long long* cand, int64_t M, int64_t N, int k,
-                               int64_t* ids, float* vals, cudaStream_t stream) {
+                               const uint32_t* cand, int64_t M, int64_t N, int k, int64_t* ids,
+                               float* vals, cudaStream_t stream) {
   const size_t smem = (size_t)kSelCap * sizeof(unsigned long long);
   static const cudaError_t attr_err = cudaFuncSetAttribute(
       topk_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);

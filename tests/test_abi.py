@@ -188,4 +188,4 @@ def test_topk_host_argument_errors_and_sizes(lib):
     for M in (1, 64, 2048):
         am = lib.w4a16_lm_head_argmax_workspace_bytes(M, 128256, 4096)
         tk = sz(M, 128256, 4096, 50)
-        assert tk >= am + M * 128256 * 8 + M * (128256 // 128) * 4
+        assert tk >= am + M * 128256 * 4 + M * (128256 // 32) * 8 + M * 4112
