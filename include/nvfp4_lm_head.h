@@ -339,6 +339,19 @@ nvfp4_status w8a8_lm_head_argmax(const void *x, int64_t M, int64_t K, const uint
                                  float *max_logits, void *workspace, size_t workspace_bytes,
                                  void *stream);
 
+/* Workspace bytes of w8a8_lm_head_topk (0 for rejected shapes or k). */
+size_t w8a8_lm_head_topk_workspace_bytes(int64_t M, int64_t N, int64_t K, int64_t k);
+
+/*
+ * The k largest W8A8 logits of each token, fused (semantics and limits of
+ * w4a16_lm_head_topk; the logits are those w8a8_lm_head writes in fp32):
+ * token_ids int64 [M, k], values fp32 [M, k] or NULL.
+ */
+nvfp4_status w8a8_lm_head_topk(const void *x, int64_t M, int64_t K, const uint8_t *q,
+                               const float *row_scale, int64_t N, int64_t k, int64_t *token_ids,
+                               float *values, void *workspace, size_t workspace_bytes,
+                               void *stream);
+
 /* ----------------------------------------------- grouped W4A16 (MoE) */
 
 /* Workspace bytes of w4a16_grouped_gemm; 0 for rejected shapes. */
@@ -432,6 +445,17 @@ nvfp4_status w4a4_lm_head_argmax(const void *x, int64_t M, int64_t K, const uint
                                  const float *input_global_scale, int64_t N, int64_t *token_ids,
                                  float *max_logits, void *workspace, size_t workspace_bytes,
                                  void *stream);
+
+/* Workspace bytes of w4a4_lm_head_topk (0 for rejected shapes or k). */
+size_t w4a4_lm_head_topk_workspace_bytes(int64_t M, int64_t N, int64_t K, int64_t k);
+
+/* The k largest W4A4 logits of each token, fused (semantics and limits of
+ * w4a16_lm_head_topk; the logits are those w4a4_lm_head writes in fp32). */
+nvfp4_status w4a4_lm_head_topk(const void *x, int64_t M, int64_t K, const uint8_t *packed,
+                               const uint8_t *scales_swizzled, const float *global_scale,
+                               const float *input_global_scale, int64_t N, int64_t k,
+                               int64_t *token_ids, float *values, void *workspace,
+                               size_t workspace_bytes, void *stream);
 
 /* ------------------------------------------- allocation-free variant */
 

@@ -24,10 +24,12 @@ Entry points (same names as the C ABI):
   in descending order, selected without storing the logits.
 * ``fp8_quantize_rows(W)`` -> ``(q e4m3[N,K], row_scale f32[N])`` and
   ``fp8_refresh`` -- the "fp8" copy of ``quantized_lm_head_copy`` (per-row
-  scales); ``w8a8_lm_head(x, q, row_scale)`` / ``w8a8_lm_head_argmax`` -- its
+  scales); ``w8a8_lm_head(x, q, row_scale)`` / ``w8a8_lm_head_argmax`` /
+  ``w8a8_lm_head_topk`` -- its
   product with per-token fp8 activations on the fp8 tensor cores.
 * ``nvfp4_swizzle_scales(scales)`` and ``w4a4_lm_head(x, packed, scales_swizzled,
-  global_scale, input_global_scale)`` / ``w4a4_lm_head_argmax`` -- the W4A4 NVFP4
+  global_scale, input_global_scale)`` / ``w4a4_lm_head_argmax`` / ``w4a4_lm_head_topk`` -- the
+  W4A4 NVFP4
   product (``CompressedTensorsW4A4Fp4``): x quantized to NVFP4 in the call,
   block-scaled FP4 tensor cores, logits scaled by alpha = g_x * g_w.
 * ``w4a16_grouped_gemm(x, group_offsets, packed, scales, global_scales)`` -- the
@@ -53,7 +55,8 @@ __all__ = [
     "nvfp4_swizzle_scales", "nvfp4_swizzled_scales_bytes", "w4a4_lm_head",
     "w4a4_lm_head_argmax", "w4a4_lm_head_workspace_bytes", "w4a4_lm_head_argmax_workspace_bytes",
     "w4a16_grouped_gemm", "w4a16_grouped_workspace_bytes", "w4a16_lm_head_topk",
-    "w4a16_lm_head_topk_workspace_bytes", "TOPK_MAX",
+    "w4a16_lm_head_topk_workspace_bytes", "TOPK_MAX", "w8a8_lm_head_topk",
+    "w8a8_lm_head_topk_workspace_bytes", "w4a4_lm_head_topk", "w4a4_lm_head_topk_workspace_bytes",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -139,6 +142,10 @@ def load_library() -> ctypes.CDLL:
     lib.w8a8_lm_head.restype = st
     lib.w8a8_lm_head_argmax.argtypes = [vp, i64, i64, vp, vp, i64, vp, vp, vp, sz, vp]
     lib.w8a8_lm_head_argmax.restype = st
+    lib.w8a8_lm_head_topk_workspace_bytes.argtypes = [i64, i64, i64, i64]
+    lib.w8a8_lm_head_topk_workspace_bytes.restype = sz
+    lib.w8a8_lm_head_topk.argtypes = [vp, i64, i64, vp, vp, i64, i64, vp, vp, vp, sz, vp]
+    lib.w8a8_lm_head_topk.restype = st
     lib.nvfp4_swizzled_scales_bytes.argtypes = [i64, i64]
     lib.nvfp4_swizzled_scales_bytes.restype = sz
     lib.nvfp4_swizzle_scales.argtypes = [vp, i64, i64, vp, vp]
@@ -150,6 +157,10 @@ def load_library() -> ctypes.CDLL:
     lib.w4a4_lm_head.argtypes = [vp, i64, i64, vp, vp, vp, vp, i64, vp, ctypes.c_int, vp, sz, vp]
     lib.w4a4_lm_head.restype = st
     lib.w4a4_lm_head_argmax.argtypes = [vp, i64, i64, vp, vp, vp, vp, i64, vp, vp, vp, sz, vp]
+    lib.w4a4_lm_head_topk_workspace_bytes.argtypes = [i64, i64, i64, i64]
+    lib.w4a4_lm_head_topk_workspace_bytes.restype = sz
+    lib.w4a4_lm_head_topk.argtypes = [vp, i64, i64, vp, vp, vp, vp, i64, i64, vp, vp, vp, sz, vp]
+    lib.w4a4_lm_head_topk.restype = st
     lib.w4a4_lm_head_argmax.restype = st
     lib.w4a16_grouped_workspace_bytes.argtypes = [i64, i64, i64, i64]
     lib.w4a16_grouped_workspace_bytes.restype = sz
@@ -346,6 +357,18 @@ def w4a16_lm_head_topk(x: torch.Tensor, packed: torch.Tensor, scales: torch.Tens
     return token_ids, values
 
 
+def _topk_outputs(M: int, k: int, device, token_ids, values, with_values):
+    kk = max(int(k), 0)
+    if token_ids is None:
+        token_ids = torch.empty((M, kk), dtype=torch.int64, device=device)
+    _need(token_ids, torch.int64, "token_ids", (M, kk))
+    if values is None and with_values:
+        values = torch.empty((M, kk), dtype=torch.float32, device=device)
+    if values is not None:
+        _need(values, torch.float32, "values", (M, kk))
+    return token_ids, values
+
+
 def fp8_quantize_workspace_bytes(N: int, K: int) -> int:
     return int(load_library().fp8_quantize_workspace_bytes(N, K))
 
@@ -446,6 +469,28 @@ def w8a8_lm_head_argmax(x: torch.Tensor, q: torch.Tensor, row_scale: torch.Tenso
     return token_ids, max_logits
 
 
+def w8a8_lm_head_topk_workspace_bytes(M: int, N: int, K: int, k: int) -> int:
+    return int(load_library().w8a8_lm_head_topk_workspace_bytes(M, N, K, k))
+
+
+def w8a8_lm_head_topk(x: torch.Tensor, q: torch.Tensor, row_scale: torch.Tensor, k: int,
+                      token_ids: torch.Tensor | None = None, values: torch.Tensor | None = None,
+                      with_values: bool = True, workspace: torch.Tensor | None = None,
+                      stream=None):
+    """The k largest logits of the fp8 copy per token, largest first, without
+    storing the logits: (token_ids i64[M, k], values f32[M, k] or None)."""
+    lib = load_library()
+    M, K, N = _w8a8_args(x, q, row_scale)
+    token_ids, values = _topk_outputs(M, k, x.device, token_ids, values, with_values)
+    if workspace is None:
+        workspace = _workspace(w8a8_lm_head_topk_workspace_bytes(M, N, K, k), x.device)
+    rc = lib.w8a8_lm_head_topk(_ptr(x), M, K, _ptr(q), _ptr(row_scale), N, k, _ptr(token_ids),
+                               _ptr(values), _ptr(workspace),
+                               workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(rc, "w8a8_lm_head_topk")
+    return token_ids, values
+
+
 def nvfp4_swizzled_scales_bytes(N: int, K: int) -> int:
     return int(load_library().nvfp4_swizzled_scales_bytes(N, K))
 
@@ -533,6 +578,30 @@ def w4a4_lm_head_argmax(x: torch.Tensor, packed: torch.Tensor, scales_swizzled: 
                                  workspace.numel() * workspace.element_size(), _stream(stream))
     _check(rc, "w4a4_lm_head_argmax")
     return token_ids, max_logits
+
+
+def w4a4_lm_head_topk_workspace_bytes(M: int, N: int, K: int, k: int) -> int:
+    return int(load_library().w4a4_lm_head_topk_workspace_bytes(M, N, K, k))
+
+
+def w4a4_lm_head_topk(x: torch.Tensor, packed: torch.Tensor, scales_swizzled: torch.Tensor,
+                      global_scale: torch.Tensor, input_global_scale: torch.Tensor, k: int,
+                      token_ids: torch.Tensor | None = None, values: torch.Tensor | None = None,
+                      with_values: bool = True, workspace: torch.Tensor | None = None,
+                      stream=None):
+    """The k largest W4A4 logits per token, largest first, without storing
+    the logits: (token_ids i64[M, k], values f32[M, k] or None)."""
+    lib = load_library()
+    M, K, N = _w4a4_args(x, packed, scales_swizzled, global_scale, input_global_scale)
+    token_ids, values = _topk_outputs(M, k, x.device, token_ids, values, with_values)
+    if workspace is None:
+        workspace = _workspace(w4a4_lm_head_topk_workspace_bytes(M, N, K, k), x.device)
+    rc = lib.w4a4_lm_head_topk(_ptr(x), M, K, _ptr(packed), _ptr(scales_swizzled),
+                               _ptr(global_scale), _ptr(input_global_scale), N, k,
+                               _ptr(token_ids), _ptr(values), _ptr(workspace),
+                               workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(rc, "w4a4_lm_head_topk")
+    return token_ids, values
 
 
 def w4a16_grouped_workspace_bytes(M: int, N: int, K: int, n_groups: int) -> int:

@@ -45,6 +45,15 @@ nvfp4_status w8a8_launch(const void* x, int64_t M, int64_t K, const uint8_t* wq,
                          const float* w_scale, int64_t N, void* logits, int out_mode,
                          int64_t* token_ids, float* max_logits, void* workspace,
                          cudaStream_t stream);
+size_t w8a8_topk_workspace_bytes(int64_t M, int64_t N, int64_t K, int k);
+nvfp4_status w8a8_topk_launch(const void* x, int64_t M, int64_t K, const uint8_t* wq,
+                              const float* w_scale, int64_t N, int k, int64_t* token_ids,
+                              float* values, void* workspace, cudaStream_t stream);
+size_t w4a4_topk_workspace_bytes(int64_t M, int64_t N, int64_t K, int k);
+nvfp4_status w4a4_topk_launch(const void* x, int64_t M, int64_t K, const uint8_t* packed,
+                              const uint8_t* wsf, const float* g_w, const float* g_in, int64_t N,
+                              int k, int64_t* token_ids, float* values, void* workspace,
+                              cudaStream_t stream);
 
 static bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
@@ -301,6 +310,35 @@ nvfp4_status w8a8_lm_head_argmax(const void* x, int64_t M, int64_t K, const uint
                      workspace, static_cast<cudaStream_t>(stream));
 }
 
+// top-k over the W8A8 / W4A4 logits: k in 1 .. min(N, NVFP4_TOPK_MAX), M x N <= 2^36
+static bool topk_k_ok(int64_t M, int64_t N, int64_t k) {
+  return N > 0 && k >= 1 && k <= NVFP4_TOPK_MAX && k <= N && M * N <= ((int64_t)1 << 36);
+}
+
+size_t w8a8_lm_head_topk_workspace_bytes(int64_t M, int64_t N, int64_t K, int64_t k) {
+  if (check_w8a8_shape(M, N, K) != NVFP4_OK || !topk_k_ok(M, N, k)) return 0;
+  return w8a8_topk_workspace_bytes(M, N, K, (int)k);
+}
+
+nvfp4_status w8a8_lm_head_topk(const void* x, int64_t M, int64_t K, const uint8_t* wq,
+                               const float* w_scale, int64_t N, int64_t k, int64_t* token_ids,
+                               float* values, void* workspace, size_t workspace_bytes,
+                               void* stream) {
+  nvfp4_status st = check_w8a8_shape(M, N, K);
+  if (st != NVFP4_OK || !topk_k_ok(M, N, k)) return NVFP4_ERR_SHAPE;
+  if (M == 0) return NVFP4_OK;
+  if (!x || !wq || !w_scale || !token_ids) return NVFP4_ERR_NULL;
+  if (!workspace || workspace_bytes < w8a8_topk_workspace_bytes(M, N, K, (int)k))
+    return NVFP4_ERR_WORKSPACE;
+  if (!aligned(x, 16) || !aligned(wq, 16) || !aligned(w_scale, 4) || !aligned(token_ids, 8) ||
+      !aligned(values, 4) || !aligned(workspace, 256))
+    return NVFP4_ERR_ALIGN;
+  st = check_device();
+  if (st != NVFP4_OK) return st;
+  return w8a8_topk_launch(x, M, K, wq, w_scale, N, (int)k, token_ids, values, workspace,
+                          static_cast<cudaStream_t>(stream));
+}
+
 /* --------------------------------------------------------- grouped (MoE) */
 
 static nvfp4_status check_grouped_shape(int64_t M, int64_t N, int64_t K, int64_t n_groups) {
@@ -419,6 +457,32 @@ nvfp4_status w4a4_lm_head_argmax(const void* x, int64_t M, int64_t K, const uint
   return w4a4_launch(x, M, K, packed, scales_swizzled, global_scale, input_global_scale, N,
                      nullptr, kOutArgmax, token_ids, max_logits, workspace,
                      static_cast<cudaStream_t>(stream));
+}
+
+size_t w4a4_lm_head_topk_workspace_bytes(int64_t M, int64_t N, int64_t K, int64_t k) {
+  if (check_w4a4_shape(M, N, K) != NVFP4_OK || !topk_k_ok(M, N, k)) return 0;
+  return w4a4_topk_workspace_bytes(M, N, K, (int)k);
+}
+
+nvfp4_status w4a4_lm_head_topk(const void* x, int64_t M, int64_t K, const uint8_t* packed,
+                               const uint8_t* scales_swizzled, const float* global_scale,
+                               const float* input_global_scale, int64_t N, int64_t k,
+                               int64_t* token_ids, float* values, void* workspace,
+                               size_t workspace_bytes, void* stream) {
+  nvfp4_status st = check_w4a4_shape(M, N, K);
+  if (st != NVFP4_OK || !topk_k_ok(M, N, k)) return NVFP4_ERR_SHAPE;
+  if (M == 0) return NVFP4_OK;
+  if (!token_ids) return NVFP4_ERR_NULL;
+  if (!workspace || workspace_bytes < w4a4_topk_workspace_bytes(M, N, K, (int)k))
+    return NVFP4_ERR_WORKSPACE;
+  st = check_w4a4_ptrs(x, packed, scales_swizzled, global_scale, input_global_scale, workspace);
+  if (st != NVFP4_OK) return st;
+  if (!aligned(token_ids, 8) || !aligned(values, 4)) return NVFP4_ERR_ALIGN;
+  st = check_device();
+  if (st != NVFP4_OK) return st;
+  return w4a4_topk_launch(x, M, K, packed, scales_swizzled, global_scale, input_global_scale, N,
+                          (int)k, token_ids, values, workspace,
+                          static_cast<cudaStream_t>(stream));
 }
 
 }  // extern "C"

@@ -106,7 +106,8 @@ __global__ void __launch_bounds__(256) w8a8_prep_x_kernel(const uint16_t* __rest
                                                           int32_t* __restrict__ status,
                                                           uint32_t* __restrict__ split_flags,
                                                           int n_split_flags,
-                                                          unsigned long long* __restrict__ am_keys) {
+                                                          unsigned long long* __restrict__ am_keys,
+                                                          uint32_t* __restrict__ tk_hist) {
   // wait for the previous kernel in the stream (it may still read this
   // workspace), then let the GEMM launch: it streams the weights meanwhile
   asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -117,7 +118,7 @@ __global__ void __launch_bounds__(256) w8a8_prep_x_kernel(const uint16_t* __rest
     for (int i = threadIdx.x; i < n_split_flags; i += blockDim.x) split_flags[i] = 0;
   }
   const int64_t m = blockIdx.x;
-  if (am_keys && threadIdx.x == 0) am_keys[m * kKeyStride] = 0ull;
+  token_state_clear(am_keys, tk_hist, m, threadIdx.x, blockDim.x);  // argmax / top-k
   uint8_t* dst = xq + m * K;
   if (m >= M) {  // padding tokens of the last tile
     for (int64_t i = threadIdx.x; i < K / 16; i += blockDim.x)
@@ -132,10 +133,13 @@ __global__ void __launch_bounds__(256) w8a8_prep_x_kernel(const uint16_t* __rest
 // ------------------------------------------------------------ the GEMM
 constexpr int kW8FirstEpiWarp = 3;
 constexpr int kW8Threads = 32 * (kW8FirstEpiWarp + 4);
+// threads of one CTA: the roles above, plus the threshold warp in top-k mode
+template <int kOut>
+constexpr int w8a8_threads() { return kW8Threads + (kOut == kOutTopk ? 32 : 0); }
 constexpr uint32_t kW8AStageBytes = kRows * kKB;  // 128 rows x 256 e4m3 = 32 KB
 
 template <int kOut, int kStages>
-__global__ void __launch_bounds__(kW8Threads, 1)
+__global__ void __launch_bounds__(w8a8_threads<kOut>(), 1)
     w8a8_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_x,
                    const GemmArgs p) {
   extern __shared__ uint8_t smem_raw[];
@@ -156,7 +160,7 @@ __global__ void __launch_bounds__(kW8Threads, 1)
   volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(tmem_slot + 1);
   float* s_tok = reinterpret_cast<float*>(bars + 32);  // 4 epilogue warps x kMaxBN
   int32_t* s_last = reinterpret_cast<int32_t*>(s_tok + 4 * kMaxBN);
-  float* s_thr = reinterpret_cast<float*>(s_last + 4);  // argmax: 4 warps x kMaxBN
+  float* s_thr = reinterpret_cast<float*>(s_last + 4);  // argmax, top-k: 4 warps x kMaxBN
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -171,6 +175,7 @@ __global__ void __launch_bounds__(kW8Threads, 1)
     }
     mbar_init(done_bar, 1);
     *abort_flag = 0;
+    if (kOut == kOutTopk) s_last[1] = 0;  // epilogue warps done (the region exists in this mode)
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
@@ -272,10 +277,14 @@ __global__ void __launch_bounds__(kW8Threads, 1)
     volatile int32_t zero = 0;
     WaitCtl drain{p.status, &zero, 100000000ull};
     mbar_wait(done_bar, 0, drain);
-  } else {
+  } else if (warp < kW8FirstEpiWarp + 4) {
     // ---------------- epilogue: token scale, then the row's own scale
     epilogue_role<kOut, true>(p, plain_sched(p), warp, warp - kW8FirstEpiWarp, lane, tmem_base, d_full, d_empty,
                               wc, s_tok, s_thr);
+    if (kOut == kOutTopk && lane == 0) atomicAdd(s_last + 1, 1);  // this warp is done
+  } else {
+    // ---------------- top-k thresholds (only launched in top-k mode)
+    topk_threshold_role(p, s_last + 1, lane);
   }
 
   __syncthreads();
@@ -317,39 +326,46 @@ size_t w8a8_workspace_bytes(int64_t M, int64_t N, int64_t K, bool argmax) {
   return ws_layout(M, N, K, std::max(sm_count(), 1), argmax, 1).total;
 }
 
+size_t w8a8_topk_workspace_bytes(int64_t M, int64_t N, int64_t K, int k) {
+  return ws_layout(M, N, K, std::max(sm_count(), 1), false, 1, k).total;
+}
+
 template <int kOut, int kStages>
 static cudaError_t launch_w8a8(const CUtensorMap& tm_w, const CUtensorMap& tm_x, const GemmArgs& a,
                                int grid, cudaStream_t stream) {
   auto kern = w8a8_tc_kernel<kOut, kStages>;
-  constexpr bool kArgmax = kOut == kOutArgmax;
+  constexpr bool kArgmax = kOut == kOutArgmax || kOut == kOutTopk;  // per-warp thresholds
   constexpr int kMaxTileBN = kStages >= 4 ? 64 : kMaxBN;
   static const cudaError_t attr_err =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)w8a8_smem_bytes(kMaxTileBN, kStages, kArgmax));
   if (attr_err != cudaSuccess) return attr_err;
-  PdlLaunch l(dim3((unsigned)grid), dim3(kW8Threads), w8a8_smem_bytes(a.BN, kStages, kArgmax),
-              stream);
+  PdlLaunch l(dim3((unsigned)grid), dim3(w8a8_threads<kOut>()),
+              w8a8_smem_bytes(a.BN, kStages, kArgmax), stream);
   return cudaLaunchKernelEx(&l.cfg, kern, tm_w, tm_x, a);
 }
 
 // out_mode: NVFP4_OUT_F32 / NVFP4_OUT_BF16 write logits[M, N]; kOutArgmax
-// writes token_ids[M] (and max_logits[M] unless null).
-nvfp4_status w8a8_launch(const void* x, int64_t M, int64_t K, const uint8_t* wq,
-                         const float* w_scale, int64_t N, void* logits, int out_mode,
-                         int64_t* token_ids, float* max_logits, void* workspace,
-                         cudaStream_t stream) {
+// writes token_ids[M] (and max_logits[M] unless null); kOutTopk (topk_k > 0)
+// writes token_ids[M, k] (and max_logits[M, k]).
+static nvfp4_status w8a8_run(const void* x, int64_t M, int64_t K, const uint8_t* wq,
+                             const float* w_scale, int64_t N, void* logits, int out_mode,
+                             int64_t* token_ids, float* max_logits, int topk_k, void* workspace,
+                             cudaStream_t stream) {
   const int sms = sm_count();
   if (sms <= 0) return NVFP4_ERR_CUDA;
   const bool argmax = out_mode == kOutArgmax;
+  const bool topk = out_mode == kOutTopk;
   const int BN = lm_head_token_tile(M);
   const int n_ttiles = (int)((M + BN - 1) / BN);
   const int64_t m_pad = (int64_t)n_ttiles * BN;
-  const WsLayout L = ws_layout(M, N, K, sms, argmax, 1);
+  const WsLayout L = ws_layout(M, N, K, sms, argmax, 1, topk ? topk_k : 0);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   int32_t* status = reinterpret_cast<int32_t*>(ws);
   uint8_t* xq = ws + L.x16;
   float* tok_scale = reinterpret_cast<float*>(ws + L.tok);
-  unsigned long long* keys = argmax ? reinterpret_cast<unsigned long long*>(ws + L.keys) : nullptr;
+  unsigned long long* keys =
+      argmax || topk ? reinterpret_cast<unsigned long long*>(ws + L.keys) : nullptr;
 
   CUtensorMap tm_w, tm_x;
   if (!encode_2d(&tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, wq, (uint64_t)K, (uint64_t)N, (uint64_t)K,
@@ -362,7 +378,8 @@ nvfp4_status w8a8_launch(const void* x, int64_t M, int64_t K, const uint8_t* wq,
     PdlLaunch l(dim3((unsigned)m_pad), dim3(256), 0, stream);
     if (cudaLaunchKernelEx(&l.cfg, w8a8_prep_x_kernel, static_cast<const uint16_t*>(x), M, K, xq,
                            tok_scale, status, reinterpret_cast<uint32_t*>(ws + L.cnt),
-                           (int)((L.part - L.cnt) / 4), keys) != cudaSuccess)
+                           (int)((L.part - L.cnt) / 4), keys,
+                           topk ? reinterpret_cast<uint32_t*>(ws + L.hist) : nullptr) != cudaSuccess)
       return NVFP4_ERR_CUDA;
   }
 
@@ -390,13 +407,20 @@ nvfp4_status w8a8_launch(const void* x, int64_t M, int64_t K, const uint8_t* wq,
   a.am_idx = token_ids;
   a.am_val = max_logits;
   a.row_scale = w_scale;
+  if (topk) topk_args(a, ws, L, topk_k, N);
   const int grid = L.grid;
   const bool small = BN <= 64;
   cudaError_t err;
   if (argmax)
     err = small ? launch_w8a8<kOutArgmax, 4>(tm_w, tm_x, a, grid, stream)
                 : launch_w8a8<kOutArgmax, 3>(tm_w, tm_x, a, grid, stream);
-  else if (out_mode == NVFP4_OUT_BF16)
+  else if (topk) {
+    err = small ? launch_w8a8<kOutTopk, 4>(tm_w, tm_x, a, grid, stream)
+                : launch_w8a8<kOutTopk, 3>(tm_w, tm_x, a, grid, stream);
+    if (err == cudaSuccess)
+      err = topk_select_launch(a.am_keys, a.tk_grp, a.tk_cand, M, N, topk_k, token_ids,
+                               max_logits, stream);
+  } else if (out_mode == NVFP4_OUT_BF16)
     err = small ? launch_w8a8<NVFP4_OUT_BF16, 4>(tm_w, tm_x, a, grid, stream)
                 : launch_w8a8<NVFP4_OUT_BF16, 3>(tm_w, tm_x, a, grid, stream);
   else
@@ -404,6 +428,21 @@ nvfp4_status w8a8_launch(const void* x, int64_t M, int64_t K, const uint8_t* wq,
                 : launch_w8a8<NVFP4_OUT_F32, 3>(tm_w, tm_x, a, grid, stream);
   if (err != cudaSuccess || cudaGetLastError() != cudaSuccess) return NVFP4_ERR_CUDA;
   return NVFP4_OK;
+}
+
+nvfp4_status w8a8_launch(const void* x, int64_t M, int64_t K, const uint8_t* wq,
+                         const float* w_scale, int64_t N, void* logits, int out_mode,
+                         int64_t* token_ids, float* max_logits, void* workspace,
+                         cudaStream_t stream) {
+  return w8a8_run(x, M, K, wq, w_scale, N, logits, out_mode, token_ids, max_logits, 0, workspace,
+                  stream);
+}
+
+nvfp4_status w8a8_topk_launch(const void* x, int64_t M, int64_t K, const uint8_t* wq,
+                              const float* w_scale, int64_t N, int k, int64_t* token_ids,
+                              float* values, void* workspace, cudaStream_t stream) {
+  return w8a8_run(x, M, K, wq, w_scale, N, nullptr, kOutTopk, token_ids, values, k, workspace,
+                  stream);
 }
 
 }  // namespace nvfp4

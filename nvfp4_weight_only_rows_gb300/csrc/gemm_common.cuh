@@ -395,6 +395,21 @@ __device__ __forceinline__ void topk_chunk(const GemmArgs& p, int64_t tc, int64_
     p.tk_grp[my_tok * p.tk_groups + (n_base >> 5)] = make_uint2(my_mx, my_bal);
 }
 
+// The prep kernels' clearing of token m's argmax / top-k state (thread
+// `tid` of `nthreads` working on the token): the line's maximum or
+// threshold and the largest candidate key, and the top-k histogram.
+__device__ __forceinline__ void token_state_clear(unsigned long long* am_keys, uint32_t* tk_hist,
+                                                  int64_t m, int tid, int nthreads) {
+  if (am_keys && tid == 0) {
+    am_keys[m * kKeyStride] = 0ull;
+    am_keys[m * kKeyStride + 2] = 0ull;
+  }
+  if (tk_hist) {
+    uint4* h = reinterpret_cast<uint4*>(tk_hist + m * kHistWords);
+    for (int i = tid; i < kHistWords / 4; i += nthreads) h[i] = make_uint4(0, 0, 0, 0);
+  }
+}
+
 // ------------------------------------------------------------ schedule
 // A CTA's work is a list of pieces (a unit, or the part of a unit inside the
 // CTA's tail range): first n_dp whole units in strided waves (so that at any
@@ -749,6 +764,15 @@ static WsLayout ws_layout(int64_t M, int64_t N, int64_t K, int sms, bool argmax,
 cudaError_t topk_select_launch(const unsigned long long* lines, const uint2* grp,
                                const uint32_t* cand, int64_t M, int64_t N, int k, int64_t* ids,
                                float* vals, cudaStream_t stream);
+
+// The top-k arguments of a GEMM whose workspace follows layout L.
+static void topk_args(GemmArgs& a, uint8_t* ws, const WsLayout& L, int k, int64_t N) {
+  a.tk_cand = reinterpret_cast<uint32_t*>(ws + L.cand);
+  a.tk_hist = reinterpret_cast<uint32_t*>(ws + L.hist);
+  a.tk_grp = reinterpret_cast<uint2*>(ws + L.grp);
+  a.tk_groups = (N + 31) / 32;
+  a.tk_k = k;
+}
 
 // Split the units of a call into strided whole-unit waves and a stream-K
 // tail: all but the last one to two waves run whole; the rest is split

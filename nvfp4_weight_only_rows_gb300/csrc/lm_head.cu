@@ -106,15 +106,7 @@ __global__ void __launch_bounds__(256) w4a16_prep_x_kernel(const uint16_t* __res
   const int lane = threadIdx.x % kT;
   const int64_t m = (int64_t)blockIdx.x * (blockDim.x / kT) + threadIdx.x / kT;
   if (m >= m_rows) return;  // uniform over the row's threads
-  if (am_keys && lane == 0) {  // argmax / top-k: no candidate yet
-    am_keys[m * kKeyStride] = 0ull;
-    am_keys[m * kKeyStride + 1] = 0ull;
-    am_keys[m * kKeyStride + 2] = 0ull;
-  }
-  if (tk_hist) {  // top-k: no candidate counted yet
-    uint4* h = reinterpret_cast<uint4*>(tk_hist + m * kHistWords);
-    for (int i = lane; i < kHistWords / 4; i += kT) h[i] = make_uint4(0, 0, 0, 0);
-  }
+  token_state_clear(am_keys, tk_hist, m, lane, kT);  // argmax / top-k: nothing seen yet
   uint4* d4 = reinterpret_cast<uint4*>(x16 + m * K);
   const int64_t nv = K / 8;
   if (m >= M) {  // padding rows of the last token tile
@@ -582,7 +574,7 @@ static nvfp4_status lm_head_run(const void* x, int64_t M, int64_t K, const uint8
       return NVFP4_ERR_CUDA;
   }
 
-  GemmArgs a;
+  GemmArgs a = {};
   a.M = M;
   a.N = N;
   a.K = K;
@@ -598,11 +590,7 @@ static nvfp4_status lm_head_run(const void* x, int64_t M, int64_t K, const uint8
   a.am_done = argmax ? reinterpret_cast<uint32_t*>(ws + L.done) : nullptr;
   a.am_idx = token_ids;
   a.am_val = max_logits;
-  a.tk_cand = topk ? reinterpret_cast<uint32_t*>(ws + L.cand) : nullptr;
-  a.tk_hist = topk ? reinterpret_cast<uint32_t*>(ws + L.hist) : nullptr;
-  a.tk_grp = topk ? reinterpret_cast<uint2*>(ws + L.grp) : nullptr;
-  a.tk_groups = (N + 31) / 32;
-  a.tk_k = topk_k;
+  if (topk) topk_args(a, ws, L, topk_k, N);
   a.row_scale = nullptr;
   // decode-sized token tiles get a third A stage, six packed stages and a
   // third dequant warp per quadrant; 128-token tiles leave TMEM room for two

@@ -64,7 +64,8 @@ __global__ void __launch_bounds__(256) w4a4_prep_x_kernel(
     const uint16_t* __restrict__ x, int64_t M, int64_t K, int64_t m_pad,
     const float* __restrict__ g_in, const float* __restrict__ g_w, uint8_t* __restrict__ xq,
     uint8_t* __restrict__ xsf, float* __restrict__ tok_scale, int32_t* __restrict__ status,
-    uint32_t* __restrict__ split_flags, int n_split_flags, unsigned long long* __restrict__ am_keys) {
+    uint32_t* __restrict__ split_flags, int n_split_flags, unsigned long long* __restrict__ am_keys,
+    uint32_t* __restrict__ tk_hist) {
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (blockIdx.x == 0) {
@@ -76,10 +77,10 @@ __global__ void __launch_bounds__(256) w4a4_prep_x_kernel(
   const float g = *g_in;
   if (threadIdx.x == 0) {
     if (m < m_pad) tok_scale[m] = m < M ? __fmul_rn(g, *g_w) : 0.0f;
-    if (am_keys && m < m_pad) am_keys[m * kKeyStride] = 0ull;
     if (m == 0 && !(g > 0.0f && g < __int_as_float(0x7F800000)))
       raise_status(status, NVFP4_ERR_NONFINITE);  // the input global must be positive and finite
   }
+  if (m < m_pad) token_state_clear(am_keys, tk_hist, m, threadIdx.x, blockDim.x);  // argmax / top-k
   const float ig = __frcp_rn(g);
   const float inv6 = 1.0f / 6.0f;
   for (int64_t c = threadIdx.x; c < kb; c += blockDim.x) {
@@ -118,12 +119,15 @@ __global__ void __launch_bounds__(256) w4a4_prep_x_kernel(
 // ------------------------------------------------------------ the GEMM
 constexpr int kW4FirstEpiWarp = 3;
 constexpr int kW4Threads = 32 * (kW4FirstEpiWarp + 4);
+// threads of one CTA: the roles above, plus the threshold warp in top-k mode
+template <int kOut>
+constexpr int w4a4_threads() { return kW4Threads + (kOut == kOutTopk ? 32 : 0); }
 constexpr uint32_t kW4AStageBytes = kRows * (kKB / 2);  // 128 rows x 256 fp4 = 16 KB
 constexpr uint32_t kW4SfStageBytes = 4 * 512;            // 4 atoms (16 k-blocks) x 128 rows
 constexpr uint32_t kW4SfCols = 32;                       // TMEM columns per stage: A 16 + B 16
 
 template <int kOut, int kStages>
-__global__ void __launch_bounds__(kW4Threads, 1)
+__global__ void __launch_bounds__(w4a4_threads<kOut>(), 1)
     w4a4_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_x,
                    const uint8_t* __restrict__ wsf, const uint8_t* __restrict__ xsf,
                    const GemmArgs p) {
@@ -161,6 +165,7 @@ __global__ void __launch_bounds__(kW4Threads, 1)
     }
     mbar_init(done_bar, 1);
     *abort_flag = 0;
+    if (kOut == kOutTopk) s_last[1] = 0;  // epilogue warps done (the region exists in this mode)
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
@@ -268,10 +273,14 @@ __global__ void __launch_bounds__(kW4Threads, 1)
     volatile int32_t zero = 0;
     WaitCtl drain{p.status, &zero, 100000000ull};
     mbar_wait(done_bar, 0, drain);
-  } else {
+  } else if (warp < kW4FirstEpiWarp + 4) {
     // ---------------- epilogue: x alpha (the token multiplier)
     epilogue_role<kOut, false>(p, plain_sched(p), warp, warp - kW4FirstEpiWarp, lane, tmem_base, d_full, d_empty,
                                wc, s_tok, s_thr);
+    if (kOut == kOutTopk && lane == 0) atomicAdd(s_last + 1, 1);  // this warp is done
+  } else {
+    // ---------------- top-k thresholds (only launched in top-k mode)
+    topk_threshold_role(p, s_last + 1, lane);
   }
 
   __syncthreads();
@@ -310,40 +319,49 @@ size_t w4a4_workspace_bytes(int64_t M, int64_t N, int64_t K, bool argmax) {
   return ws_layout(M, N, K, std::max(sm_count(), 1), argmax, 1).total;
 }
 
+size_t w4a4_topk_workspace_bytes(int64_t M, int64_t N, int64_t K, int k) {
+  return ws_layout(M, N, K, std::max(sm_count(), 1), false, 1, k).total;
+}
+
 template <int kOut, int kStages>
 static cudaError_t launch_w4a4(const CUtensorMap& tm_w, const CUtensorMap& tm_x,
                                const uint8_t* wsf, const uint8_t* xsf, const GemmArgs& a, int grid,
                                cudaStream_t stream) {
   auto kern = w4a4_tc_kernel<kOut, kStages>;
-  constexpr bool kArgmax = kOut == kOutArgmax;
+  constexpr bool kArgmax = kOut == kOutArgmax || kOut == kOutTopk;  // per-warp thresholds
   constexpr int kMaxTileBN = kStages >= 6 ? 64 : kMaxBN;
   static const cudaError_t attr_err =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)w4a4_smem_bytes(kMaxTileBN, kStages, kArgmax));
   if (attr_err != cudaSuccess) return attr_err;
-  PdlLaunch l(dim3((unsigned)grid), dim3(kW4Threads), w4a4_smem_bytes(a.BN, kStages, kArgmax),
-              stream);
+  PdlLaunch l(dim3((unsigned)grid), dim3(w4a4_threads<kOut>()),
+              w4a4_smem_bytes(a.BN, kStages, kArgmax), stream);
   return cudaLaunchKernelEx(&l.cfg, kern, tm_w, tm_x, wsf, xsf, a);
 }
 
-nvfp4_status w4a4_launch(const void* x, int64_t M, int64_t K, const uint8_t* packed,
-                         const uint8_t* wsf, const float* g_w, const float* g_in, int64_t N,
-                         void* logits, int out_mode, int64_t* token_ids, float* max_logits,
-                         void* workspace, cudaStream_t stream) {
+// out_mode: NVFP4_OUT_F32 / NVFP4_OUT_BF16 write logits[M, N]; kOutArgmax
+// writes token_ids[M] (and max_logits[M] unless null); kOutTopk (topk_k > 0)
+// writes token_ids[M, k] (and max_logits[M, k]).
+static nvfp4_status w4a4_run(const void* x, int64_t M, int64_t K, const uint8_t* packed,
+                             const uint8_t* wsf, const float* g_w, const float* g_in, int64_t N,
+                             void* logits, int out_mode, int64_t* token_ids, float* max_logits,
+                             int topk_k, void* workspace, cudaStream_t stream) {
   const int sms = sm_count();
   if (sms <= 0) return NVFP4_ERR_CUDA;
   const bool argmax = out_mode == kOutArgmax;
+  const bool topk = out_mode == kOutTopk;
   const int BN = lm_head_token_tile(M);
   const int n_ttiles = (int)((M + BN - 1) / BN);
   const int64_t m_pad = (int64_t)n_ttiles * BN;
   const int64_t m_pad128 = round_up128(M);
-  const WsLayout L = ws_layout(M, N, K, sms, argmax, 1);
+  const WsLayout L = ws_layout(M, N, K, sms, argmax, 1, topk ? topk_k : 0);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   int32_t* status = reinterpret_cast<int32_t*>(ws);
   uint8_t* xq = ws + L.x16;
   uint8_t* xsf = xq + (size_t)m_pad * (K / 2);
   float* tok_scale = reinterpret_cast<float*>(ws + L.tok);
-  unsigned long long* keys = argmax ? reinterpret_cast<unsigned long long*>(ws + L.keys) : nullptr;
+  unsigned long long* keys =
+      argmax || topk ? reinterpret_cast<unsigned long long*>(ws + L.keys) : nullptr;
 
   CUtensorMap tm_w, tm_x;
   if (!encode_2d(&tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, packed, (uint64_t)K / 2, (uint64_t)N,
@@ -357,7 +375,8 @@ nvfp4_status w4a4_launch(const void* x, int64_t M, int64_t K, const uint8_t* pac
     if (cudaLaunchKernelEx(&l.cfg, w4a4_prep_x_kernel, static_cast<const uint16_t*>(x), M, K,
                            m_pad, g_in, g_w, xq, xsf, tok_scale, status,
                            reinterpret_cast<uint32_t*>(ws + L.cnt), (int)((L.part - L.cnt) / 4),
-                           keys) != cudaSuccess)
+                           keys, topk ? reinterpret_cast<uint32_t*>(ws + L.hist) : nullptr) !=
+        cudaSuccess)
       return NVFP4_ERR_CUDA;
   }
 
@@ -387,12 +406,19 @@ nvfp4_status w4a4_launch(const void* x, int64_t M, int64_t K, const uint8_t* pac
   a.am_idx = token_ids;
   a.am_val = max_logits;
   a.row_scale = nullptr;
+  if (topk) topk_args(a, ws, L, topk_k, N);
   const int grid = L.grid;
   cudaError_t err;
   if (argmax)
     err = small ? launch_w4a4<kOutArgmax, 6>(tm_w, tm_x, wsf, xsf, a, grid, stream)
                 : launch_w4a4<kOutArgmax, 5>(tm_w, tm_x, wsf, xsf, a, grid, stream);
-  else if (out_mode == NVFP4_OUT_BF16)
+  else if (topk) {
+    err = small ? launch_w4a4<kOutTopk, 6>(tm_w, tm_x, wsf, xsf, a, grid, stream)
+                : launch_w4a4<kOutTopk, 5>(tm_w, tm_x, wsf, xsf, a, grid, stream);
+    if (err == cudaSuccess)
+      err = topk_select_launch(a.am_keys, a.tk_grp, a.tk_cand, M, N, topk_k, token_ids,
+                               max_logits, stream);
+  } else if (out_mode == NVFP4_OUT_BF16)
     err = small ? launch_w4a4<NVFP4_OUT_BF16, 6>(tm_w, tm_x, wsf, xsf, a, grid, stream)
                 : launch_w4a4<NVFP4_OUT_BF16, 5>(tm_w, tm_x, wsf, xsf, a, grid, stream);
   else
@@ -400,6 +426,22 @@ nvfp4_status w4a4_launch(const void* x, int64_t M, int64_t K, const uint8_t* pac
                 : launch_w4a4<NVFP4_OUT_F32, 5>(tm_w, tm_x, wsf, xsf, a, grid, stream);
   if (err != cudaSuccess || cudaGetLastError() != cudaSuccess) return NVFP4_ERR_CUDA;
   return NVFP4_OK;
+}
+
+nvfp4_status w4a4_launch(const void* x, int64_t M, int64_t K, const uint8_t* packed,
+                         const uint8_t* wsf, const float* g_w, const float* g_in, int64_t N,
+                         void* logits, int out_mode, int64_t* token_ids, float* max_logits,
+                         void* workspace, cudaStream_t stream) {
+  return w4a4_run(x, M, K, packed, wsf, g_w, g_in, N, logits, out_mode, token_ids, max_logits, 0,
+                  workspace, stream);
+}
+
+nvfp4_status w4a4_topk_launch(const void* x, int64_t M, int64_t K, const uint8_t* packed,
+                              const uint8_t* wsf, const float* g_w, const float* g_in, int64_t N,
+                              int k, int64_t* token_ids, float* values, void* workspace,
+                              cudaStream_t stream) {
+  return w4a4_run(x, M, K, packed, wsf, g_w, g_in, N, nullptr, kOutTopk, token_ids, values, k,
+                  workspace, stream);
 }
 
 }  // namespace nvfp4

@@ -189,3 +189,26 @@ def test_topk_host_argument_errors_and_sizes(lib):
         am = lib.w4a16_lm_head_argmax_workspace_bytes(M, 128256, 4096)
         tk = sz(M, 128256, 4096, 50)
         assert tk >= am + M * 128256 * 4 + M * (128256 // 32) * 8 + M * 4112
+
+
+def test_w8a8_w4a4_topk_host_errors_and_sizes(lib):
+    vp = ctypes.c_void_p
+    fake = vp(1 << 20)
+    ids, vals = vp(1 << 20), vp(1 << 21)
+    big = 1 << 44
+    t8 = lib.w8a8_lm_head_topk
+    assert t8(fake, 4, 256, fake, fake, 100, 0, ids, vals, fake, big, None) == 1      # k == 0
+    assert t8(fake, 4, 256, fake, fake, 7, 8, ids, vals, fake, big, None) == 1        # k > N
+    assert t8(fake, 4, 32768, fake, fake, 100, 5, ids, vals, fake, big, None) == 1    # K > max
+    assert t8(fake, 0, 256, fake, fake, 100, 5, ids, vals, None, 0, None) == 0       # empty
+    assert t8(fake, 4, 256, fake, fake, 100, 5, None, vals, fake, big, None) == 3    # NULL ids
+    assert t8(fake, 4, 256, fake, fake, 100, 5, ids, vals, fake, 4096, None) == 4    # WORKSPACE
+    t4 = lib.w4a4_lm_head_topk
+    assert t4(fake, 4, 256, fake, fake, fake, fake, 100, 129, ids, vals, fake, big, None) == 1
+    assert t4(fake, 0, 256, fake, fake, fake, fake, 100, 5, ids, vals, None, 0, None) == 0
+    assert t4(fake, 4, 256, fake, fake, fake, fake, 100, 5, None, vals, fake, big, None) == 3
+    assert t4(fake, 4, 256, fake, fake, fake, fake, 100, 5, ids, vals, fake, 4096, None) == 4
+    for f, am in ((lib.w8a8_lm_head_topk_workspace_bytes, lib.w8a8_lm_head_argmax_workspace_bytes),
+                  (lib.w4a4_lm_head_topk_workspace_bytes, lib.w4a4_lm_head_argmax_workspace_bytes)):
+        assert f(4, 0, 256, 1) == 0 and f(4, 100, 256, 0) == 0
+        assert f(64, 128256, 4096, 50) >= am(64, 128256, 4096) + 64 * 128256 * 4

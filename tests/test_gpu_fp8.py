@@ -11,7 +11,8 @@ import torch
 import nvfp4_weight_only_rows_gb300 as nv
 import oracle
 import synth
-from tests._gpu import assert_argmax_agrees, assert_logits_close, logits_tolerance, to_bf16_dev
+from tests._gpu import (assert_argmax_agrees, assert_logits_close, assert_topk_equal,
+                        assert_topk_oracle_agrees, expected_topk, logits_tolerance, to_bf16_dev)
 
 pytestmark = pytest.mark.gpu
 
@@ -218,3 +219,30 @@ def test_argmax_decode_and_prefill(decode_case):
         torch.cuda.synchronize()
         assert torch.equal(ids, want_ids)
         assert torch.equal(vals, want_vals)
+
+
+@pytest.mark.parametrize("M,N,K,k", [(1, 300, 512, 10), (64, 777, 1024, 50), (200, 5000, 256, 128),
+                                     (8, 216 * 128, 1024, 50), (3, 7, 256, 7)])
+def test_topk_matches_plain_logits(M, N, K, k):
+    """The fused top-k of the W8A8 logits: bit for bit the k largest of the
+    fp32 logits w8a8_lm_head writes, and oracle-agreeing on two tokens."""
+    x, (wq, ws), (xq, xs) = product_case(N, K, M, seed=M * 5 + N)
+    xd, dev = to_bf16_dev(x), upload(wq, ws)
+    ids, vals = nv.w8a8_lm_head_topk(xd, *dev, k)
+    want_ids, want_vals = expected_topk(nv.w8a8_lm_head(xd, *dev), k)
+    torch.cuda.synchronize()
+    assert_topk_equal(ids, vals, want_ids, want_vals, f"M={M} N={N} k={k}")
+    sel = sorted({0, M - 1})
+    assert_topk_oracle_agrees(ids.cpu().numpy()[sel], vals.cpu().numpy()[sel],
+                              oracle.fp8_logits(xq[sel], xs[sel], wq, ws))
+
+
+def test_topk_decode_and_prefill(decode_case):
+    _, (wq, ws) = decode_case
+    dev = upload(wq, ws)
+    for x in (synth.decode_x(64), synth.prefill_x()):
+        xd = to_bf16_dev(x)
+        ids, vals = nv.w8a8_lm_head_topk(xd, *dev, 50)
+        want_ids, want_vals = expected_topk(nv.w8a8_lm_head(xd, *dev), 50)
+        torch.cuda.synchronize()
+        assert_topk_equal(ids, vals, want_ids, want_vals, f"M={x.shape[0]}")

@@ -16,7 +16,8 @@ import torch
 import nvfp4_weight_only_rows_gb300 as nv
 import oracle
 import synth
-from tests._gpu import logits_tolerance, to_bf16_dev
+from tests._gpu import (assert_topk_equal, assert_topk_oracle_agrees, expected_topk,
+                        to_bf16_dev)
 
 pytestmark = pytest.mark.gpu
 
@@ -34,47 +35,16 @@ def upload(p, s, g):
             torch.tensor([g], dtype=torch.float32, device="cuda"))
 
 
-def expected_topk(L: torch.Tensor, k: int):
-    """(rows, values) of the k largest of each row of fp32 logits, on the
-    device, by the 64-bit order key (value order with NaN on top, then the
-    smaller row), -0 counted as +0."""
-    L = torch.where(L == 0, torch.zeros_like(L), L)
-    b = L.view(torch.int32).to(torch.int64) & 0xFFFFFFFF
-    ok = torch.where(b >= 2 ** 31, b ^ 0xFFFFFFFF, b | 0x80000000)
-    n = torch.arange(L.shape[1], device=L.device, dtype=torch.int64)
-    key = ((ok - 2 ** 31) << 32) | (~n & 0xFFFFFFFF)
-    top = torch.topk(key, k, dim=1, sorted=True).values
-    ids = ~top & 0xFFFFFFFF
-    return ids, L.gather(1, ids)
-
-
 def assert_same_as_plain(xd, dev_q, k, what=""):
     L = nv.w4a16_lm_head(xd, *dev_q)
     ids, vals = nv.w4a16_lm_head_topk(xd, *dev_q, k)
     want_ids, want_vals = expected_topk(L, k)
     torch.cuda.synchronize()
-    bad = (ids != want_ids).any(dim=1).nonzero()[:, 0]
-    assert bad.numel() == 0, (what, bad[:3].tolist(), ids[bad[:1]].tolist(),
-                              want_ids[bad[:1]].tolist())
-    same = (vals.view(torch.int32) == want_vals.view(torch.int32)) | (
-        torch.isnan(vals) & torch.isnan(want_vals))
-    assert bool(same.all()), (what, vals[~same][:5].tolist(), want_vals[~same][:5].tolist())
+    assert_topk_equal(ids, vals, want_ids, want_vals, what)
     return ids.cpu().numpy(), vals.cpu().numpy()
 
 
-def assert_oracle_agrees(ids, vals, ref):
-    """ids, vals: [T, k] from the GPU; ref: the oracle's fp64 logits [T, N]."""
-    tol = logits_tolerance(ref)[:, 0]
-    k = ids.shape[1]
-    for m in range(ref.shape[0]):
-        sel = ids[m]
-        assert len(set(sel.tolist())) == k, m
-        err = np.abs(vals[m].astype(np.float64) - ref[m, sel])
-        assert np.all(err <= tol[m]), (m, err.max(), tol[m])
-        out = np.ones(ref.shape[1], dtype=bool)
-        out[sel] = False
-        if out.any():
-            assert ref[m, out].max() <= ref[m, sel].min() + 2 * tol[m], m
+assert_oracle_agrees = assert_topk_oracle_agrees
 
 
 def test_tiny_workload():

@@ -10,7 +10,8 @@ import torch
 import nvfp4_weight_only_rows_gb300 as nv
 import oracle
 import synth
-from tests._gpu import assert_argmax_agrees, assert_logits_close, logits_tolerance, to_bf16_dev
+from tests._gpu import (assert_argmax_agrees, assert_logits_close, assert_topk_equal,
+                        assert_topk_oracle_agrees, expected_topk, logits_tolerance, to_bf16_dev)
 
 pytestmark = pytest.mark.gpu
 
@@ -176,3 +177,36 @@ def test_argmax_prefill(decode_case):
     torch.cuda.synchronize()
     assert torch.equal(ids, want_ids)
     assert torch.equal(vals, want_vals)
+
+
+@pytest.mark.parametrize("M,N,K,k", [(1, 300, 512, 10), (64, 777, 1024, 50), (200, 5000, 256, 128),
+                                     (8, 216 * 128, 1024, 50), (3, 7, 256, 7)])
+def test_topk_matches_plain_logits(M, N, K, k):
+    """The fused top-k of the W4A4 logits: bit for bit the k largest of the
+    fp32 logits w4a4_lm_head writes, and oracle-agreeing on two tokens."""
+    W = synth.quant_weight(N=N, K=K, seed=M * 11 + N)
+    x = synth.decode_x(M, K=K)
+    host_q = oracle.quantize(W)
+    gx, _ = input_global(x)
+    pd, sw, gd = dev_weight(host_q)
+    gxd = torch.tensor([gx], dtype=torch.float32, device="cuda")
+    xd = to_bf16_dev(x)
+    ids, vals = nv.w4a4_lm_head_topk(xd, pd, sw, gd, gxd, k)
+    want_ids, want_vals = expected_topk(nv.w4a4_lm_head(xd, pd, sw, gd, gxd), k)
+    torch.cuda.synchronize()
+    assert_topk_equal(ids, vals, want_ids, want_vals, f"M={M} N={N} k={k}")
+    sel = sorted({0, M - 1})
+    assert_topk_oracle_agrees(ids.cpu().numpy()[sel], vals.cpu().numpy()[sel],
+                              oracle.w4a4_logits(x[sel], gx, *host_q))
+
+
+def test_topk_decode_and_prefill(decode_case):
+    pd, sw, gd = dev_weight(decode_case)
+    for x in (synth.decode_x(64), synth.prefill_x()):
+        gx, _ = input_global(x)
+        gxd = torch.tensor([gx], dtype=torch.float32, device="cuda")
+        xd = to_bf16_dev(x)
+        ids, vals = nv.w4a4_lm_head_topk(xd, pd, sw, gd, gxd, 50)
+        want_ids, want_vals = expected_topk(nv.w4a4_lm_head(xd, pd, sw, gd, gxd), 50)
+        torch.cuda.synchronize()
+        assert_topk_equal(ids, vals, want_ids, want_vals, f"M={x.shape[0]}")
