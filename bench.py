@@ -415,6 +415,17 @@ def run_ours(args, world, rank, local):
     g_w8am = {M: [capture(lambda M=M, c=c: nv.w8a8_lm_head_argmax(
         x_am[M], *f8[c], token_ids=am_ids[M], max_logits=am_vals[M], workspace=w8ws))
         for c in range(2)] for M in (64, PREFILL_M)}
+    # the fused top-k of the fp8 and W4A4 products (same k), at M = 64 and 2048
+    tkws8 = torch.empty(nv.w8a8_lm_head_topk_workspace_bytes(PREFILL_M, N, K, TOPK_K),
+                        dtype=torch.uint8, device=dev)
+    g_w8tk = {M: [capture(lambda M=M, c=c: nv.w8a8_lm_head_topk(
+        x_am[M], *f8[c], TOPK_K, token_ids=tk_ids[M], values=tk_vals[M], workspace=tkws8))
+        for c in range(2)] for M in (64, PREFILL_M)}
+    tkws4 = torch.empty(nv.w4a4_lm_head_topk_workspace_bytes(PREFILL_M, N, K, TOPK_K),
+                        dtype=torch.uint8, device=dev)
+    g_w4tk = {M: [capture(lambda M=M, c=c: nv.w4a4_lm_head_topk(
+        x_am[M], copies[c][0], sw4[c], copies[c][2], gx4[M], TOPK_K, token_ids=tk_ids[M],
+        values=tk_vals[M], workspace=tkws4)) for c in range(2)] for M in (64, PREFILL_M)}
 
     for s in range(args.warmup):
         step(s)
@@ -492,6 +503,8 @@ def run_ours(args, world, rank, local):
     w8am_us = {M: per_call_us(g_w8am[M]) for M in g_w8am}
     w4_us = {M: per_call_us(g_w4[M]) for M in g_w4}
     w4am_us = {M: per_call_us(g_w4am[M]) for M in g_w4am}
+    w8tk_us = {M: per_call_us(g_w8tk[M]) for M in g_w8tk}
+    w4tk_us = {M: per_call_us(g_w4tk[M]) for M in g_w4tk}
     sw4_us = per_call_us(g_sw4)
 
     def hbm_roof(name, gbs, tkey):
@@ -569,6 +582,7 @@ def run_ours(args, world, rank, local):
         "refresh_ms": round(f8q_us / 1e3, 4),
         "us_per_call_alone": {str(M): round(v, 2) for M, v in w8_us.items()},
         "argmax_us_per_call_alone": {str(M): round(v, 2) for M, v in w8am_us.items()},
+        f"topk{TOPK_K}_us_per_call_alone": {str(M): round(v, 2) for M, v in w8tk_us.items()},
         "rooflines": fp8_roofs,
     }
     fp4_peak = 6.0 * peaks["bf16_tflops"]  # nominal fp4 : bf16 dense ratio (13.5 : 2.25 PF)
@@ -589,6 +603,7 @@ def run_ours(args, world, rank, local):
         "swizzle_scales_us": round(sw4_us, 2),
         "us_per_call_alone": {str(M): round(v, 2) for M, v in w4_us.items()},
         "argmax_us_per_call_alone": {str(M): round(v, 2) for M, v in w4am_us.items()},
+        f"topk{TOPK_K}_us_per_call_alone": {str(M): round(v, 2) for M, v in w4tk_us.items()},
         "rooflines": w4_roofs,
     }
     moe_part = run_moe(nv, synth, dev, per_call_us, capture, peaks, traffic, hbm_roof)
