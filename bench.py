@@ -464,17 +464,31 @@ def run_ours(args, world, rank, local):
     total_s_max, _ = aggregate(total_ms / 1e3, 0.0, world)
     value = dec_bytes_all / dec_s_max / 1e9
 
-    # ---- end to end through the public call: x from pinned host, logits back
+    # ---- end to end through the public call: x from pinned host, logits back.
+    # A decode loop overlaps the read-back with the next products: the logits
+    # go to pinned host memory on a copy stream from two device buffers, and
+    # a product waits only for the copy that last read its buffer.
     x_host = {M: x_dec[M].cpu().pin_memory() for M in DECODE_MS}
     o_host = {M: torch.empty(M, N, dtype=torch.float32).pin_memory() for M in DECODE_MS}
     x_tmp = {M: torch.empty_like(x_dec[M]) for M in DECODE_MS}
+    out_e2e = [{M: torch.empty(M, N, dtype=torch.float32, device=dev) for M in DECODE_MS}
+               for _ in range(2)]
+    copy_stream = torch.cuda.Stream(device=dev)
+    made = [{M: torch.cuda.Event() for M in DECODE_MS} for _ in range(2)]
+    read = [{M: torch.cuda.Event() for M in DECODE_MS} for _ in range(2)]
 
     def e2e_step(s):
+        b = s % 2
         for i, M in enumerate(DECODE_MS):
             p, sc, g = copies[(s + i) % 2]
             x_tmp[M].copy_(x_host[M], non_blocking=True)
-            nv.w4a16_lm_head(x_tmp[M], p, sc, g, out=out_dec[M], workspace=gws)
-            o_host[M].copy_(out_dec[M], non_blocking=True)
+            stream.wait_event(read[b][M])  # the copy that last read this buffer is done
+            nv.w4a16_lm_head(x_tmp[M], p, sc, g, out=out_e2e[b][M], workspace=gws)
+            made[b][M].record(stream)
+            copy_stream.wait_event(made[b][M])
+            with torch.cuda.stream(copy_stream):
+                o_host[M].copy_(out_e2e[b][M], non_blocking=True)
+            read[b][M].record(copy_stream)
 
     for s in range(args.warmup):
         e2e_step(s)
@@ -485,6 +499,7 @@ def run_ours(args, world, rank, local):
     e0.record(stream)
     for s in range(args.steps):
         e2e_step(s)
+    stream.wait_stream(copy_stream)  # the last read-backs are inside the timed region
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_s, _ = aggregate(e0.elapsed_time(e1) / 1e3, 0.0, world)
@@ -635,7 +650,8 @@ def run_ours(args, world, rank, local):
                 "h2d_bytes_per_step": sum(2 * M * K for M in DECODE_MS),
                 "d2h_bytes_per_step": sum(4 * M * N for M in DECODE_MS),
                 "what": "decode calls through w4a16_lm_head with x copied from pinned host memory "
-                        "and logits copied back every call"},
+                        "and every call's fp32 logits copied back to pinned host memory on a copy "
+                        "stream (two device logits buffers), all copies inside the timed region"},
         "argmax": argmax_part,
         "topk": topk_part,
         "fp8": fp8_part,
