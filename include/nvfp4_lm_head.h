@@ -36,6 +36,12 @@
  *  - Workspaces must be 256-byte aligned and at least the size the matching
  *    *_workspace_bytes() call returns.  Their contents need no
  *    initialisation and may be reused between calls on the same stream.
+ *  - The kernels of a call are chained by programmatic dependent launch: a
+ *    call's first kernel waits for the grid launched just before it on the
+ *    stream to complete before it touches memory.  A workspace may be
+ *    reused by the next call when every kernel enqueued between the two
+ *    calls is either launched normally or, if launched as a programmatic
+ *    dependent, waits for its own predecessor before it completes.
  */
 #ifndef NVFP4_LM_HEAD_H_
 #define NVFP4_LM_HEAD_H_
