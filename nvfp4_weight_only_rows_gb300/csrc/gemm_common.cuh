@@ -268,10 +268,11 @@ __device__ __forceinline__ float key_value(uint32_t k) {
 // without clearing and the selection skips every group below its final T.
 // Histogram bins: all negative keys; positive keys below 2^-32; a
 // sixteenth of an octave each from 2^-32 to 2^32 (exponent and top 4
-// mantissa bits); 2^32 and above.  A candidate within an octave of its
-// group's largest adds one to its bin (an atomic add without a reply; the
-// others cannot hold the k-th largest unless the group holds an outlier,
-// and leaving them out only lowers the bin found).  A threshold warp in
+// mantissa bits); 2^32 and above.  A candidate within a quarter of an
+// exponent step of its group's largest (order keys differ by at most 2^21)
+// adds one to its bin (an atomic add without a reply; the token's largest
+// logits are almost always the largest of their groups, and leaving any
+// candidate out only lowers the bin found).  A threshold warp in
 // every CTA keeps walking its tokens' bins down from the largest key's bin
 // to the one that holds the k-th counted candidate and raises T to that
 // bin's lower edge: at least k candidates of the token reach it (counts and
@@ -383,8 +384,9 @@ __device__ __forceinline__ void topk_chunk(const GemmArgs& p, int64_t tc, int64_
       if (mine) {
         const int64_t tok = tc + t;
         p.tk_cand[tok * p.N + n] = ok;
-        // half the group's largest: lower candidates are not counted
-        const uint32_t floor = mx >= 0x80800000u ? mx - 0x00800000u : 0u;
+        // a quarter of an exponent step below the group's largest: lower
+        // candidates are not counted
+        const uint32_t floor = mx >= 0x80200000u ? mx - 0x00200000u : 0u;
         if (ok >= floor) red_add_u32(p.tk_hist + tok * kHistWords + topk_bin(ok), 1u);
       }
     }
