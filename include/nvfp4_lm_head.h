@@ -142,6 +142,17 @@ nvfp4_status nvfp4_read_device_status(const void *workspace, int32_t *status_out
 nvfp4_status nvfp4_selftest_bounded_wait(void *workspace, size_t workspace_bytes,
                                          int64_t limit_us, void *stream);
 
+/*
+ * Host-only check of the fused top-k's histogram (w4a16_lm_head_topk and
+ * its W8A8 / W4A4 counterparts): over every 32-bit logit order key in
+ * increasing order the bin never decreases and the bin's lower edge -- the
+ * threshold a raise to that bin sets -- never exceeds the key, which is
+ * what keeps every one of a token's k largest logits above its threshold.
+ * Returns -1 when every key passes, else the first failing key.  Runs on
+ * the CPU (a few seconds); needs no GPU.
+ */
+int64_t nvfp4_selftest_topk_bins(void);
+
 /* --------------------------------------------------------- W4A16 GEMM */
 
 /*

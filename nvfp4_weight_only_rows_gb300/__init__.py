@@ -48,7 +48,7 @@ __all__ = [
     "NVFP4Error", "Status", "library_path", "load_library", "nvfp4_quantize_rows",
     "nvfp4_refresh", "w4a16_lm_head", "nvfp4_quantize_workspace_bytes",
     "w4a16_lm_head_workspace_bytes", "nvfp4_read_device_status", "w4a16_lm_head_noalloc",
-    "nvfp4_selftest_bounded_wait", "OUT_F32", "OUT_BF16", "w4a16_lm_head_argmax",
+    "nvfp4_selftest_bounded_wait", "nvfp4_selftest_topk_bins", "OUT_F32", "OUT_BF16", "w4a16_lm_head_argmax",
     "w4a16_lm_head_argmax_workspace_bytes", "fp8_quantize_rows", "fp8_refresh",
     "fp8_quantize_workspace_bytes", "w8a8_lm_head", "w8a8_lm_head_argmax",
     "w8a8_lm_head_workspace_bytes", "w8a8_lm_head_argmax_workspace_bytes",
@@ -171,6 +171,8 @@ def load_library() -> ctypes.CDLL:
     lib.w4a16_lm_head_noalloc.restype = st
     lib.nvfp4_selftest_bounded_wait.argtypes = [vp, sz, i64, vp]
     lib.nvfp4_selftest_bounded_wait.restype = st
+    lib.nvfp4_selftest_topk_bins.argtypes = []
+    lib.nvfp4_selftest_topk_bins.restype = ctypes.c_int64
     _lib = lib
     return lib
 
@@ -658,6 +660,12 @@ def w4a16_lm_head_noalloc(x: torch.Tensor, packed: torch.Tensor, scales: torch.T
                                    N, _ptr(out), code, _stream(stream))
     _check(rc, "w4a16_lm_head_noalloc")
     return out
+
+
+def nvfp4_selftest_topk_bins() -> int:
+    """Host-only check of the fused top-k's histogram bins against every 32-bit
+    order key: -1 when all pass, else the first failing key."""
+    return int(load_library().nvfp4_selftest_topk_bins())
 
 
 def nvfp4_selftest_bounded_wait(workspace: torch.Tensor, limit_us: int, stream=None) -> None:

@@ -280,14 +280,14 @@ __device__ __forceinline__ float key_value(uint32_t k) {
 constexpr int kHistBins = 1027;
 constexpr int kHistWords = 1028;  // u32 per token (whole 16-byte vectors)
 
-__device__ __forceinline__ uint32_t topk_bin(uint32_t ok) {
+__host__ __device__ __forceinline__ uint32_t topk_bin(uint32_t ok) {
   if (ok < 0x80000000u) return 0u;
   const uint32_t e = (ok >> 23) & 0xFFu;
   if (e < 96u) return 1u;
   if (e >= 160u) return (uint32_t)kHistBins - 1u;
   return 2u + ((e - 96u) << 4) + ((ok >> 19) & 15u);
 }
-__device__ __forceinline__ unsigned long long topk_edge(uint32_t bin) {
+__host__ __device__ __forceinline__ unsigned long long topk_edge(uint32_t bin) {
   uint32_t ok;
   if (bin == 0u) return 0ull;
   if (bin == 1u) ok = 0x80000000u;

@@ -1,5 +1,6 @@
 // selftest.cu -- nvfp4_selftest_bounded_wait: check, on the device, that the
-// library's pipeline waits give up instead of hanging.
+// library's pipeline waits give up instead of hanging; nvfp4_selftest_topk_bins:
+// check, on the host, the fused top-k's histogram bins against the order keys.
 //
 // The kernel waits on an mbarrier phase that nothing completes, with the same
 // bounded wait (mbar_wait) every kernel of this library uses, and then on a
@@ -9,6 +10,7 @@
 #include <cuda_runtime.h>
 
 #include "common.cuh"
+#include "gemm_common.cuh"
 
 namespace nvfp4 {
 
@@ -58,4 +60,27 @@ extern "C" nvfp4_status nvfp4_selftest_bounded_wait(void* workspace, size_t work
   nvfp4_wait_selftest_kernel<<<1, 32, 0, s>>>(status, flag, (uint64_t)limit_us * 1000ull);
   if (cudaGetLastError() != cudaSuccess) return NVFP4_ERR_CUDA;
   return NVFP4_OK;
+}
+
+// Every 32-bit order key, in increasing order: its histogram bin never
+// decreases, and the lower edge of its bin (the threshold a raise to that
+// bin sets) never exceeds it; each bin's edge lies in the bin itself, and
+// the edges increase with the bin.  The first key that breaks a rule is
+// returned, -1 when none does.
+extern "C" int64_t nvfp4_selftest_topk_bins(void) {
+  using namespace nvfp4;
+  uint32_t prev = 0, edge_hi = 0;
+  for (uint64_t k = 0; k <= 0xFFFFFFFFull; ++k) {
+    const uint32_t ok = (uint32_t)k;
+    const uint32_t b = topk_bin(ok);
+    if (b < prev || b >= (uint32_t)kHistBins) return (int64_t)ok;
+    if (b != prev || k == 0) edge_hi = (uint32_t)(topk_edge(b) >> 32);
+    if (edge_hi > ok) return (int64_t)ok;
+    prev = b;
+  }
+  for (uint32_t b = 1; b < (uint32_t)kHistBins; ++b) {
+    const uint32_t e = (uint32_t)(topk_edge(b) >> 32);
+    if (topk_bin(e) != b || topk_edge(b) <= topk_edge(b - 1)) return (int64_t)e;
+  }
+  return -1;
 }

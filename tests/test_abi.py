@@ -212,3 +212,10 @@ def test_w8a8_w4a4_topk_host_errors_and_sizes(lib):
                   (lib.w4a4_lm_head_topk_workspace_bytes, lib.w4a4_lm_head_argmax_workspace_bytes)):
         assert f(4, 0, 256, 1) == 0 and f(4, 100, 256, 0) == 0
         assert f(64, 128256, 4096, 50) >= am(64, 128256, 4096) + 64 * 128256 * 4
+
+
+def test_topk_histogram_bins_never_exceed_their_keys(lib):
+    """Host check over every 32-bit order key: the threshold a raise can set
+    (a bin's lower edge) is never above a key of that bin, bins never
+    decrease with the key, and each edge lies in its own bin."""
+    assert lib.nvfp4_selftest_topk_bins() == -1
