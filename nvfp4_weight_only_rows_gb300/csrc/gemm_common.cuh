@@ -13,6 +13,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <atomic>
 #include <type_traits>
 #include <mutex>
 
@@ -682,7 +683,22 @@ __device__ __forceinline__ void argmax_finish(const GemmArgs& p, int first_epi_t
 }
 
 // ------------------------------------------------------------ host side
-static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+// Raise a kernel's dynamic shared memory limit on the current device, once
+// per device (the attribute belongs to the device's context).  `done` is the
+// launch site's own record of the devices already set.
+static inline cudaError_t smem_limit_once(std::atomic<uint64_t>& done, const void* kern,
+                                          size_t bytes) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = dev < 64 ? 1ull << dev : 0ull;
+  if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_acq_rel);
+  return e;
+}
+
+static inline PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   static std::once_flag once;
   std::call_once(once, [] {
@@ -696,9 +712,9 @@ static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   return fn;
 }
 
-static bool encode_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64_t inner,
-                      uint64_t outer, uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer,
-                      CUtensorMapSwizzle swz) {
+static inline bool encode_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base,
+                             uint64_t inner, uint64_t outer, uint64_t row_bytes,
+                             uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle swz) {
   auto fn = tensor_map_encoder();
   if (!fn) return false;
   cuuint64_t dims[2] = {inner, outer};
@@ -711,12 +727,12 @@ static bool encode_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base
   return r == CUDA_SUCCESS;
 }
 
-static int lm_head_token_tile(int64_t M) {
+static inline int lm_head_token_tile(int64_t M) {
   if (M >= kMaxBN) return kMaxBN;
   return (int)((M + 15) / 16 * 16);
 }
 
-static int sm_count() {
+static inline int sm_count() {
   int dev = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 0;
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
@@ -740,8 +756,8 @@ struct WsLayout {
 };
 
 
-static WsLayout ws_layout(int64_t M, int64_t N, int64_t K, int sms, bool argmax, int x_bytes,
-                          int topk_k = 0) {
+static inline WsLayout ws_layout(int64_t M, int64_t N, int64_t K, int sms, bool argmax,
+                                 int x_bytes, int topk_k = 0) {
   WsLayout l;
   const bool keys = argmax || topk_k > 0;
   const int BN = lm_head_token_tile(M);
@@ -768,7 +784,7 @@ cudaError_t topk_select_launch(const unsigned long long* lines, const uint2* grp
                                float* vals, cudaStream_t stream);
 
 // The top-k arguments of a GEMM whose workspace follows layout L.
-static void topk_args(GemmArgs& a, uint8_t* ws, const WsLayout& L, int k, int64_t N) {
+static inline void topk_args(GemmArgs& a, uint8_t* ws, const WsLayout& L, int k, int64_t N) {
   a.tk_cand = reinterpret_cast<uint32_t*>(ws + L.cand);
   a.tk_hist = reinterpret_cast<uint32_t*>(ws + L.hist);
   a.tk_grp = reinterpret_cast<uint2*>(ws + L.grp);
@@ -780,7 +796,7 @@ static void topk_args(GemmArgs& a, uint8_t* ws, const WsLayout& L, int k, int64_
 // tail: all but the last one to two waves run whole; the rest is split
 // evenly, so every CTA's tail range holds at least one unit's stages and a
 // unit is cut at most once.
-static void schedule_units(GemmArgs& a, int64_t grid) {
+static inline void schedule_units(GemmArgs& a, int64_t grid) {
   const int64_t dp_waves = a.n_units >= 2 * grid ? a.n_units / grid - 1 : 0;
   a.n_dp = (uint32_t)dp_waves;
   a.tail_s0 = (uint64_t)(dp_waves * grid) * a.n_kb;

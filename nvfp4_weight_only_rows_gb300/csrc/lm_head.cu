@@ -494,9 +494,10 @@ static cudaError_t launch_gemm(const CUtensorMap& tm_packed, const CUtensorMap& 
   const size_t smem = gemm_smem_bytes(a.BN, kStages, kPStages, kArgmax, kGrouped);
   // the 3-stage shape only serves token tiles of up to 64
   constexpr int kMaxTileBN = kStages >= 3 ? 64 : kMaxBN;
-  static const cudaError_t attr_err = cudaFuncSetAttribute(
-      kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-      (int)gemm_smem_bytes(kMaxTileBN, kStages, kPStages, kArgmax, kGrouped));
+  static std::atomic<uint64_t> limit_set{0};
+  const cudaError_t attr_err =
+      smem_limit_once(limit_set, reinterpret_cast<const void*>(kern),
+                      gemm_smem_bytes(kMaxTileBN, kStages, kPStages, kArgmax, kGrouped));
   if (attr_err != cudaSuccess) return attr_err;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)grid);

@@ -256,8 +256,9 @@ cudaError_t topk_select_launch(const unsigned long long* lines, const uint2* grp
                                const uint32_t* cand, int64_t M, int64_t N, int k, int64_t* ids,
                                float* vals, cudaStream_t stream) {
   const size_t smem = (size_t)kSelCap * sizeof(unsigned long long);
-  static const cudaError_t attr_err = cudaFuncSetAttribute(
-      topk_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  static std::atomic<uint64_t> limit_set{0};
+  const cudaError_t attr_err =
+      smem_limit_once(limit_set, reinterpret_cast<const void*>(topk_select_kernel), smem);
   if (attr_err != cudaSuccess) return attr_err;
   PdlLaunch l(dim3((unsigned)M), dim3(kSelThreads), smem, stream);
   return cudaLaunchKernelEx(&l.cfg, topk_select_kernel, lines, grp, cand, N, k, ids, vals);

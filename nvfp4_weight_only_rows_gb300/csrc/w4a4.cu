@@ -330,9 +330,9 @@ static cudaError_t launch_w4a4(const CUtensorMap& tm_w, const CUtensorMap& tm_x,
   auto kern = w4a4_tc_kernel<kOut, kStages>;
   constexpr bool kArgmax = kOut == kOutArgmax || kOut == kOutTopk;  // per-warp thresholds
   constexpr int kMaxTileBN = kStages >= 6 ? 64 : kMaxBN;
-  static const cudaError_t attr_err =
-      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)w4a4_smem_bytes(kMaxTileBN, kStages, kArgmax));
+  static std::atomic<uint64_t> limit_set{0};
+  const cudaError_t attr_err = smem_limit_once(limit_set, reinterpret_cast<const void*>(kern),
+                                               w4a4_smem_bytes(kMaxTileBN, kStages, kArgmax));
   if (attr_err != cudaSuccess) return attr_err;
   PdlLaunch l(dim3((unsigned)grid), dim3(w4a4_threads<kOut>()),
               w4a4_smem_bytes(a.BN, kStages, kArgmax), stream);
