@@ -1,7 +1,7 @@
 /*
  * nvfp4_lm_head.h -- C ABI of the GB300 (sm_103a) online NVFP4 lm_head library.
  *
- * Two operations, as the pages define them:
+ * Two operations, as the pages define them, are the core of the library:
  *
  *  1. Row quantization of an already-loaded bf16 lm_head to NVFP4 in the
  *     checkpoint layout -- page "vllm.model_executor.layers.quantization.
@@ -19,6 +19,14 @@
  *     `CompressedTensorsW4A16Fp4.apply_weights` on the page
  *     "vllm.model_executor.layers.quantization.compressed_tensors.schemes":
  *     logits[m, n] = global * sum_k x[m, k] * e2m1(code[n, k]) * f32(scale[n, k/16]).
+ *
+ * Around them, in the order of the sections below: the greedy argmax and
+ * the top-k of those logits fused into the product (the logits are never
+ * written); the "fp8" lm_head copy (per-row E4M3 weights, W8A8 product) of
+ * `quantized_lm_head_copy` on the first page; the grouped W4A16 product of
+ * all experts of an NVFP4 MoE layer; the W4A4 NVFP4 product of
+ * `CompressedTensorsW4A4Fp4`; an allocation-free variant of the W4A16
+ * product; and two self-tests.
  *
  * Conventions for every call:
  *  - All tensor pointers are DEVICE pointers on the current CUDA device,
