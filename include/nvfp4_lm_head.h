@@ -265,10 +265,10 @@ size_t w4a16_lm_head_topk_workspace_bytes(int64_t M, int64_t N, int64_t K, int64
  * NVFP4_OUT_F32 for the same inputs, with -0 and +0 equal (a zero is
  * returned as +0) and a NaN above every number, as in w4a16_lm_head_argmax
  * (whose answer is column 0 here).  The [M, N] logits are never written:
- * the epilogue appends only the logits that reach the token's running
+ * the epilogue keeps only the logits that reach the token's running
  * threshold, a lower bound of its k-th largest that rises with a histogram
- * of the candidates appended so far, and a second kernel selects the exact
- * k largest of those.  The result does not depend on the schedule.
+ * of the candidates kept so far, and a second kernel selects the exact k
+ * largest of those.  The result does not depend on the schedule.
  *
  * The pages define the logits, not a sampler; this is the top-k filter a
  * sampler applies to them, for the same reason as the argmax.

@@ -55,7 +55,7 @@ struct GemmArgs {
   float* am_val;                // [M] result: that logit (may be null)
   // top-k output mode only (am_keys then holds per token line: word 0 the
   // threshold key, a lower bound of the token's k-th largest candidate
-  // key; word 1 the number of candidates appended)
+  // key; the low half of word 2 the largest candidate order key)
   uint32_t* tk_cand;            // [M][N] candidate order keys, slot n for row n
   uint2* tk_grp;                // [M][tk_groups] per 32 rows: {largest candidate order key,
                                 //   bit j: slot 32g + j holds a candidate}
