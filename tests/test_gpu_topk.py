@@ -115,6 +115,19 @@ def test_all_rows_tied():
         assert np.all(vals == vals[:, :1])
 
 
+def test_tied_rows_within_shared_memory():
+    """3000 equal rows: every logit is a candidate at the final threshold,
+    more than the one-warp ranking takes and few enough for the radix
+    selection over shared memory; rows 0 .. k-1 must come out, in order."""
+    N, K, M = 3000, 256, 5
+    row = synth.quant_weight(N=1, K=K, seed=7)
+    host_q = oracle.quantize(np.repeat(row, N, axis=0))
+    x = synth.decode_x(M, K=K)
+    for k in (1, 37, 128):
+        ids, vals = assert_same_as_plain(to_bf16_dev(x), upload(*host_q), k, f"ties3000 k={k}")
+        assert np.all(ids == np.arange(k)[None, :])
+
+
 def test_rising_logits():
     """Logits that grow with the row: later tiles keep beating the
     thresholds that earlier ones set."""
