@@ -169,32 +169,22 @@ def test_no_values_empty_and_status():
     assert e_ids.shape == (0,) and e_vals.shape == (0,)
 
 
-@pytest.fixture(scope="module")
-def decode_case():
-    W = synth.decode_weight()
-    return oracle.quantize(W)
-
-
 @pytest.mark.parametrize("M", [1, 8, 32, 64])
-def test_decode_workload(decode_case, M):
-    """W[128256, 4096] decode: every token bit for bit against the plain
-    product; four tokens against the oracle over all 128256 rows."""
-    p, s, g = decode_case
+def test_decode_workload(decode_nvfp4, M):
+    """W[128256, 4096] quantized on the GPU: every token bit for bit against
+    the plain product and against the oracle over all 128256 rows."""
     x = synth.decode_x(M)
-    ids, vals = assert_same_as_plain(to_bf16_dev(x), upload(p, s, g), f"decode M={M}")
-    sel = sorted({0, M // 3, M // 2, M - 1})
-    assert_oracle_agrees(ids[sel], vals[sel], oracle.logits(x[sel], p, s, g))
+    ids, vals = assert_same_as_plain(to_bf16_dev(x), decode_nvfp4.dev, f"decode M={M}")
+    assert_oracle_agrees(ids, vals, oracle.logits(x, *decode_nvfp4.ref))
 
 
-def test_prefill_workload(decode_case):
+def test_prefill_workload(decode_nvfp4):
     """x[2048, 4096] (16 token tiles): all tokens against the plain product,
-    8 sampled tokens against the oracle."""
-    p, s, g = decode_case
+    64 tokens (each tile's first and last two) against the oracle."""
     x = synth.prefill_x()
-    ids, vals = assert_same_as_plain(to_bf16_dev(x), upload(p, s, g), "prefill")
-    rng = np.random.default_rng(4)
-    sel = np.unique(np.concatenate([[0, 2047], rng.integers(0, 2048, 6)]))
-    assert_oracle_agrees(ids[sel], vals[sel], oracle.logits(x[sel], p, s, g))
+    ids, vals = assert_same_as_plain(to_bf16_dev(x), decode_nvfp4.dev, "prefill")
+    sel = np.array(sorted({t for t0 in range(0, 2048, 128) for t in (t0, t0 + 1, t0 + 126, t0 + 127)}))
+    assert_oracle_agrees(ids[sel], vals[sel], oracle.logits(x[sel], *decode_nvfp4.ref))
 
 
 def test_graph_replay():

@@ -148,8 +148,8 @@ def test_deterministic_and_errors():
 
 
 @pytest.fixture(scope="module")
-def decode_case():
-    W = synth.decode_weight()
+def decode_case(decode_nvfp4):
+    W = decode_nvfp4.W
     return W, oracle.fp8_quantize(W)
 
 

@@ -2,7 +2,8 @@
 
 Every case calls the CUDA kernels through the C ABI (the ctypes binding in
 nvfp4_weight_only_rows_gb300) and compares packed codes, E4M3 scales and the
-global scale byte for byte with oracle.quantize / oracle.quantize_rows.
+global scale byte for byte with oracle.quantize.  Every row of the
+full-size workload weights is compared in test_gpu_workloads.py.
 """
 import numpy as np
 import pytest
@@ -110,28 +111,3 @@ def test_refresh_in_place_keeps_addresses():
     assert np.array_equal(packed.cpu().numpy(), p_ref)
     assert np.array_equal(scales_bytes(scales), s_ref)
     assert np.float32(g.item()) == g_ref
-
-
-def _sample_rows(N, W_bits, n=192, seed=0):
-    rng = np.random.default_rng(seed)
-    Wf = synth.bf16_bits_to_f32(W_bits)
-    amax_row = int(np.argmax(np.abs(Wf).max(axis=1)))
-    rows = np.unique(np.concatenate([[0, 1, N - 2, N - 1, amax_row],
-                                     rng.integers(0, N, size=n)]))
-    return rows.astype(np.int64)
-
-
-@pytest.mark.parametrize("seed", [4, 5])
-def test_full_size_quant_workload_sampled(seed):
-    """W bf16[151936, 5120] (Student-t row scales): full GPU run, global scale
-    exact, 197 sampled rows (first, last, the amax row, random) bit-exact;
-    seeds 4 and 5 are the two weights refresh alternates between."""
-    N, K = 151936, 5120
-    W = synth.quant_weight(N=N, K=K, seed=seed)
-    p, s, g = gpu_quantize(W)
-    g_ref, ig_ref = oracle.global_scale(oracle.weight_amax(W))
-    assert g == g_ref
-    rows = _sample_rows(N, W, seed=seed)
-    p_ref, s_ref = oracle.quantize_rows(W, rows, g_ref, ig_ref)
-    assert np.array_equal(s[rows], s_ref)
-    assert np.array_equal(p[rows], p_ref)

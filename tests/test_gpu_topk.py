@@ -181,31 +181,22 @@ def test_no_values_empty_and_status():
         assert e.value.status == nv.Status.ERR_SHAPE
 
 
-@pytest.fixture(scope="module")
-def decode_case():
-    return oracle.quantize(synth.decode_weight())
-
-
 @pytest.mark.parametrize("M,k", [(1, 50), (8, 50), (32, 50), (64, 50), (64, 128), (16, 1)])
-def test_decode_workload(decode_case, M, k):
-    """W[128256, 4096] decode: every token bit for bit against the plain
-    product; four tokens against the oracle over all 128256 rows."""
-    p, s, g = decode_case
+def test_decode_workload(decode_nvfp4, M, k):
+    """W[128256, 4096] quantized on the GPU: every token bit for bit against
+    the plain product and against the oracle over all 128256 rows."""
     x = synth.decode_x(M)
-    ids, vals = assert_same_as_plain(to_bf16_dev(x), upload(p, s, g), k, f"decode M={M}")
-    sel = sorted({0, M // 3, M // 2, M - 1})
-    assert_oracle_agrees(ids[sel], vals[sel], oracle.logits(x[sel], p, s, g))
+    ids, vals = assert_same_as_plain(to_bf16_dev(x), decode_nvfp4.dev, k, f"decode M={M}")
+    assert_oracle_agrees(ids, vals, oracle.logits(x, *decode_nvfp4.ref))
 
 
-def test_prefill_workload(decode_case):
+def test_prefill_workload(decode_nvfp4):
     """x[2048, 4096] (16 token tiles), k = 50: all tokens against the plain
-    product, 6 sampled tokens against the oracle."""
-    p, s, g = decode_case
+    product, 64 tokens (each tile's first and last two) against the oracle."""
     x = synth.prefill_x()
-    ids, vals = assert_same_as_plain(to_bf16_dev(x), upload(p, s, g), 50, "prefill")
-    rng = np.random.default_rng(7)
-    sel = np.unique(np.concatenate([[0, 2047], rng.integers(0, 2048, 4)]))
-    assert_oracle_agrees(ids[sel], vals[sel], oracle.logits(x[sel], p, s, g))
+    ids, vals = assert_same_as_plain(to_bf16_dev(x), decode_nvfp4.dev, 50, "prefill")
+    sel = np.array(sorted({t for t0 in range(0, 2048, 128) for t in (t0, t0 + 1, t0 + 126, t0 + 127)}))
+    assert_oracle_agrees(ids[sel], vals[sel], oracle.logits(x[sel], *decode_nvfp4.ref))
 
 
 def test_graph_replay():

@@ -112,8 +112,8 @@ def test_invalid_input_global_is_a_status():
 
 
 @pytest.fixture(scope="module")
-def decode_case():
-    return oracle.quantize(synth.decode_weight())
+def decode_case(decode_nvfp4):
+    return decode_nvfp4.ref
 
 
 @pytest.mark.parametrize("M", [1, 8, 32, 64])
