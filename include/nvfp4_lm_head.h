@@ -166,7 +166,10 @@ int64_t nvfp4_selftest_topk_bins(void);
 /*
  * Workspace bytes w4a16_lm_head needs for x[M, K] against N vocabulary rows:
  * the activations rescaled to fp16 (M * K * 2 bytes), one fp32 scale per
- * token, the device status word and room for split-K partial tiles.
+ * token, the device status word and room for split-K partial tiles; for a
+ * K that is not a multiple of 256 also a copy of the weight rows whose
+ * length is not a 16-byte multiple (block scales [N, K/16] when K % 256 != 0,
+ * packed codes [N, K/2] when K % 32 != 0), with the row stride rounded up.
  * Returns 0 for shapes the call rejects.
  */
 size_t w4a16_lm_head_workspace_bytes(int64_t M, int64_t N, int64_t K);
@@ -176,9 +179,15 @@ size_t w4a16_lm_head_workspace_bytes(int64_t M, int64_t N, int64_t K);
  * e2m1(code[n, k]) * f32(scale[n, k/16]) * global_scale.
  *
  *   x            bf16 [M, K], device, 16-byte aligned.  M >= 0 (M == 0 is a
- *                no-op), K >= 256 and K % 256 == 0 (the row strides of the
- *                packed and scale tensors must be 16-byte multiples for the
- *                tensor-memory-access copies; all lm_head widths are).
+ *                no-op), K >= 16 and K % 16 == 0 (the K % 16 rule of
+ *                `KNvfp4Static.create_weights` on the page
+ *                "vllm/model_executor/layers/quantization/modelopt.py").
+ *                The kernels read the weights by TMA, whose row strides must
+ *                be 16-byte multiples: for K % 256 == 0 (the usual lm_head
+ *                widths) packed and scales are read in place; otherwise the
+ *                call first copies the rows that break that rule into the
+ *                workspace (one extra pass over the block scales, and over
+ *                the packed codes when K % 32 != 0).
  *   packed, scales, global_scale
  *                exactly as nvfp4_quantize_rows writes them for W[N, K];
  *                packed and scales 16-byte aligned.
@@ -336,7 +345,7 @@ size_t w8a8_lm_head_workspace_bytes(int64_t M, int64_t N, int64_t K);
  * quantized per token by the rule above (inside the call, into the
  * workspace).
  *   x          bf16 [M, K], device, 16-byte aligned.  M >= 0 (0: no-op),
- *              K % 256 == 0, 256 <= K <= 16384.
+ *              K % 16 == 0, 16 <= K <= 16384.
  *   q, row_scale  as fp8_quantize_rows writes them for W[N, K].
  *   N          vocabulary rows, N >= 0 (0: no-op).
  *   logits     [M, N] fp32 (NVFP4_OUT_F32) or bf16 (NVFP4_OUT_BF16), device,
@@ -391,7 +400,8 @@ size_t w4a16_grouped_workspace_bytes(int64_t M, int64_t N, int64_t K, int64_t n_
  *   out[m, n] = global[e] * sum_k x[m, k] * e2m1(code[e, n, k]) * f32(scale[e, n, k/16])
  * for every token row m of group e, group_offsets[e] <= m < group_offsets[e + 1].
  *   x              bf16 [M, K], device: token rows already grouped by expert
- *                  (routing and the final combine are the caller's).  K % 256 == 0.
+ *                  (routing and the final combine are the caller's).
+ *                  K % 16 == 0 (K % 256 != 0 stages rows as w4a16_lm_head).
  *   group_offsets  int32 [n_groups + 1], device, non-decreasing, [0] = 0,
  *                  [n_groups] = M (rows outside [0, M) are never read or
  *                  written).  Read by the kernels, never by the host: the call
@@ -413,7 +423,7 @@ nvfp4_status w4a16_grouped_gemm(const void *x, int64_t M, int64_t K, const int32
 
 /*
  * Bytes of the 128x4-interleaved copy of NVFP4 block scales of W[N, K]:
- * round_up(N, 128) * K/16.  0 for rejected shapes (K % 64 != 0).
+ * round_up(N, 128) * round_up(K/16, 4).  0 for rejected shapes (K % 16 != 0).
  */
 size_t nvfp4_swizzled_scales_bytes(int64_t N, int64_t K);
 
@@ -421,11 +431,11 @@ size_t nvfp4_swizzled_scales_bytes(int64_t N, int64_t K);
  * Re-lay row-major E4M3 block scales [N, K/16] (as nvfp4_quantize_rows writes
  * them) into the order block-scaled FP4 tensor cores read, `swizzle_blockscale`
  * on the page "vllm.model_executor.layers.quantization.compressed_tensors.
- * schemes": rows padded to a multiple of 128 and columns (K/16, a multiple of
- * 4 here) taken in 512-byte atoms of 128 rows x 4 columns, ordered
+ * schemes": rows padded to a multiple of 128 and columns (K/16) to a
+ * multiple of 4, taken in 512-byte atoms of 128 rows x 4 columns, ordered
  * [row / 128][column / 4]; inside an atom, row 32 a + b and column d sit at
- * byte b * 16 + a * 4 + d.  Padding rows are zero.
- *   scales  u8 [N, K/16], device, 4-byte aligned.  K % 64 == 0.
+ * byte b * 16 + a * 4 + d.  Padding rows and columns are zero.
+ *   scales  u8 [N, K/16], device, 4-byte aligned.  K % 16 == 0.
  *   out     u8, device, 16-byte aligned, nvfp4_swizzled_scales_bytes(N, K).
  * Run it after every nvfp4_quantize_rows / nvfp4_refresh that the W4A4
  * product will read.
@@ -446,7 +456,9 @@ size_t w4a4_lm_head_workspace_bytes(int64_t M, int64_t N, int64_t K);
  * x / (scale * input_global_scale), ties to even), then
  *   logits[m, n] = fl32(acc[m, n] * alpha),  alpha = fl32(input_global_scale * global_scale),
  * acc the fp32 tensor-core sum of the block-scaled E2M1 products (each exact).
- *   x                   bf16 [M, K], device, 16-byte aligned; K % 256 == 0.
+ *   x                   bf16 [M, K], device, 16-byte aligned; K % 16 == 0 (when
+ *                       K % 32 != 0 the weight codes are first copied into the
+ *                       workspace with a 16-byte-multiple row stride).
  *   packed, global_scale  as nvfp4_quantize_rows writes them for W[N, K].
  *   scales_swizzled     nvfp4_swizzle_scales of that call's scales.
  *   input_global_scale  f32 [1], device: the activation dequant multiplier

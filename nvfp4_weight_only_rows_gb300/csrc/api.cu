@@ -144,7 +144,7 @@ nvfp4_status nvfp4_read_device_status(const void* workspace, int32_t* status_out
 }
 
 size_t w4a16_lm_head_workspace_bytes(int64_t M, int64_t N, int64_t K) {
-  if (M < 0 || N < 0 || K < 256 || K % 256 != 0) return 0;
+  if (M < 0 || N < 0 || K < 16 || K % 16 != 0) return 0;
   return lm_head_workspace_bytes(M, N, K, false);
 }
 
@@ -152,7 +152,7 @@ nvfp4_status w4a16_lm_head(const void* x, int64_t M, int64_t K, const uint8_t* p
                            const uint8_t* scales, const float* global_scale, int64_t N,
                            void* logits, int out_dtype, void* workspace, size_t workspace_bytes,
                            void* stream) {
-  if (M < 0 || N < 0 || K < 256 || K % 256 != 0 || M >= kMaxDim || N >= kMaxDim ||
+  if (M < 0 || N < 0 || K < 16 || K % 16 != 0 || M >= kMaxDim || N >= kMaxDim ||
       K >= kMaxDim)
     return NVFP4_ERR_SHAPE;
   if (out_dtype != NVFP4_OUT_F32 && out_dtype != NVFP4_OUT_BF16) return NVFP4_ERR_DTYPE;
@@ -170,7 +170,7 @@ nvfp4_status w4a16_lm_head(const void* x, int64_t M, int64_t K, const uint8_t* p
 }
 
 size_t w4a16_lm_head_argmax_workspace_bytes(int64_t M, int64_t N, int64_t K) {
-  if (M < 0 || N <= 0 || K < 256 || K % 256 != 0) return 0;
+  if (M < 0 || N <= 0 || K < 16 || K % 16 != 0) return 0;
   return lm_head_workspace_bytes(M, N, K, true);
 }
 
@@ -179,7 +179,7 @@ nvfp4_status w4a16_lm_head_argmax(const void* x, int64_t M, int64_t K, const uin
                                   int64_t* token_ids, float* max_logits, void* workspace,
                                   size_t workspace_bytes, void* stream) {
   // N <= 0: the maximum over no logits does not exist
-  if (M < 0 || N <= 0 || K < 256 || K % 256 != 0 || M >= kMaxDim || N >= kMaxDim ||
+  if (M < 0 || N <= 0 || K < 16 || K % 16 != 0 || M >= kMaxDim || N >= kMaxDim ||
       K >= kMaxDim)
     return NVFP4_ERR_SHAPE;
   if (M == 0) return NVFP4_OK;
@@ -199,7 +199,7 @@ nvfp4_status w4a16_lm_head_argmax(const void* x, int64_t M, int64_t K, const uin
 /* ------------------------------------------------------------ fused top-k */
 
 static bool topk_shape_ok(int64_t M, int64_t N, int64_t K, int64_t k) {
-  return M >= 0 && N > 0 && K >= 256 && K % 256 == 0 && M < kMaxDim && N < kMaxDim &&
+  return M >= 0 && N > 0 && K >= 16 && K % 16 == 0 && M < kMaxDim && N < kMaxDim &&
          K < kMaxDim && k >= 1 && k <= NVFP4_TOPK_MAX && k <= N && M * N <= ((int64_t)1 << 36);
 }
 
@@ -257,7 +257,7 @@ nvfp4_status fp8_refresh(const void* W, int64_t N, int64_t K, uint8_t* q, float*
 static constexpr int64_t kW8MaxK = 16384;
 
 static nvfp4_status check_w8a8_shape(int64_t M, int64_t N, int64_t K) {
-  if (M < 0 || N < 0 || K < 256 || K % 256 != 0 || K > kW8MaxK || M >= kMaxDim || N >= kMaxDim)
+  if (M < 0 || N < 0 || K < 16 || K % 16 != 0 || K > kW8MaxK || M >= kMaxDim || N >= kMaxDim)
     return NVFP4_ERR_SHAPE;
   return NVFP4_OK;
 }
@@ -342,7 +342,7 @@ nvfp4_status w8a8_lm_head_topk(const void* x, int64_t M, int64_t K, const uint8_
 /* --------------------------------------------------------- grouped (MoE) */
 
 static nvfp4_status check_grouped_shape(int64_t M, int64_t N, int64_t K, int64_t n_groups) {
-  if (M < 0 || N < 0 || K < 256 || K % 256 != 0 || n_groups < 1 || n_groups > kMaxGroupsApi ||
+  if (M < 0 || N < 0 || K < 16 || K % 16 != 0 || n_groups < 1 || n_groups > kMaxGroupsApi ||
       M >= kMaxDim || N >= kMaxDim || K >= kMaxDim || n_groups * N >= kMaxDim)
     return NVFP4_ERR_SHAPE;
   return NVFP4_OK;
@@ -377,13 +377,13 @@ nvfp4_status w4a16_grouped_gemm(const void* x, int64_t M, int64_t K, const int32
 /* ------------------------------------------------------------ W4A4 */
 
 size_t nvfp4_swizzled_scales_bytes(int64_t N, int64_t K) {
-  if (N <= 0 || K <= 0 || K % 64 != 0 || N >= kMaxDim || K >= kMaxDim) return 0;
+  if (N <= 0 || K <= 0 || K % 16 != 0 || N >= kMaxDim || K >= kMaxDim) return 0;
   return nvfp4_swizzled_scales_size(N, K);
 }
 
 nvfp4_status nvfp4_swizzle_scales(const uint8_t* scales, int64_t N, int64_t K, uint8_t* out,
                                   void* stream) {
-  if (N <= 0 || K <= 0 || K % 64 != 0 || N >= kMaxDim || K >= kMaxDim) return NVFP4_ERR_SHAPE;
+  if (N <= 0 || K <= 0 || K % 16 != 0 || N >= kMaxDim || K >= kMaxDim) return NVFP4_ERR_SHAPE;
   if (!scales || !out) return NVFP4_ERR_NULL;
   if (!aligned(scales, 4) || !aligned(out, 16)) return NVFP4_ERR_ALIGN;
   nvfp4_status st = check_device();
@@ -392,7 +392,7 @@ nvfp4_status nvfp4_swizzle_scales(const uint8_t* scales, int64_t N, int64_t K, u
 }
 
 static nvfp4_status check_w4a4_shape(int64_t M, int64_t N, int64_t K) {
-  if (M < 0 || N < 0 || K < 256 || K % 256 != 0 || M >= kMaxDim || N >= kMaxDim || K >= kMaxDim)
+  if (M < 0 || N < 0 || K < 16 || K % 16 != 0 || M >= kMaxDim || N >= kMaxDim || K >= kMaxDim)
     return NVFP4_ERR_SHAPE;
   return NVFP4_OK;
 }

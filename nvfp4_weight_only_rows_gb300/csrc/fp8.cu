@@ -323,11 +323,11 @@ nvfp4_status fp8_quantize_launch(const void* W, int64_t N, int64_t K, uint8_t* q
 }
 
 size_t w8a8_workspace_bytes(int64_t M, int64_t N, int64_t K, bool argmax) {
-  return ws_layout(M, N, K, std::max(sm_count(), 1), argmax, 1).total;
+  return ws_layout(M, N, K, std::max(sm_count(), 1), argmax, ActFormat::kE4M3).total;
 }
 
 size_t w8a8_topk_workspace_bytes(int64_t M, int64_t N, int64_t K, int k) {
-  return ws_layout(M, N, K, std::max(sm_count(), 1), false, 1, k).total;
+  return ws_layout(M, N, K, std::max(sm_count(), 1), false, ActFormat::kE4M3, k).total;
 }
 
 template <int kOut, int kStages>
@@ -359,7 +359,7 @@ static nvfp4_status w8a8_run(const void* x, int64_t M, int64_t K, const uint8_t*
   const int BN = lm_head_token_tile(M);
   const int n_ttiles = (int)((M + BN - 1) / BN);
   const int64_t m_pad = (int64_t)n_ttiles * BN;
-  const WsLayout L = ws_layout(M, N, K, sms, argmax, 1, topk ? topk_k : 0);
+  const WsLayout L = ws_layout(M, N, K, sms, argmax, ActFormat::kE4M3, topk ? topk_k : 0);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   int32_t* status = reinterpret_cast<int32_t*>(ws);
   uint8_t* xq = ws + L.x16;
@@ -390,7 +390,9 @@ static nvfp4_status w8a8_run(const void* x, int64_t M, int64_t K, const uint8_t*
   a.BN = BN;
   a.n_ttiles = n_ttiles;
   a.n_units = ((N + kRows - 1) / kRows) * n_ttiles;
-  a.n_kb = (int)(K / kKB);
+  // K % 16: the last stage's k past K reads zeros (the weight and activation
+  // maps end at K; a TMA box past the end is filled with zeros)
+  a.n_kb = (int)((K + kKB - 1) / kKB);
   schedule_units(a, L.grid);
   uint32_t cols = 32;
   while (cols < 2u * BN) cols *= 2;

@@ -739,8 +739,32 @@ static inline int sm_count() {
   return sms;
 }
 
+// How a product's activations sit in its workspace (the first region after
+// the status header): fp16 [m_pad, K] (W4A16), e4m3 [m_pad, K] (W8A8), or
+// e2m1 codes [m_pad, row stride] followed by their 128x4-interleaved block
+// scales (W4A4).  K % 16 == 0 in all three.
+enum class ActFormat { kF16, kE4M3, kE2M1 };
+
+// Row stride of the W4A4 x codes in the workspace: K/2 bytes rounded up to
+// the 16-byte multiple a TMA row stride needs.
+static inline int64_t e2m1_code_stride(int64_t K) { return (K / 2 + 15) / 16 * 16; }
+
+// Columns of a 128x4-interleaved block-scale matrix: K/16 rounded up to 4.
+static inline int64_t interleaved_sf_cols(int64_t K) { return (K / 16 + 3) / 4 * 4; }
+
+static inline size_t act_region_bytes(ActFormat f, int64_t m_pad, int64_t M, int64_t K) {
+  switch (f) {
+    case ActFormat::kF16: return (size_t)m_pad * K * 2;
+    case ActFormat::kE4M3: return (size_t)m_pad * K;
+    case ActFormat::kE2M1:
+      return align_up((size_t)m_pad * e2m1_code_stride(K), 256) +
+             (size_t)((M + 127) / 128 * 128) * interleaved_sf_cols(K);
+  }
+  return 0;
+}
+
 // Workspace layout of one call: [status header][activations as the MMA
-// reads them, m_pad x K x x_bytes (fp16: 2, e4m3: 1)]
+// reads them (ActFormat)]
 // [token multipliers, m_pad][split counters, grid x 4][split ready flags,
 // grid x 4] and, for argmax and top-k, [CTAs done, 1]; these are zeroed by
 // the prep kernel's first CTA.  Then [split partials, grid x 4 x BN x 32
@@ -757,7 +781,7 @@ struct WsLayout {
 
 
 static inline WsLayout ws_layout(int64_t M, int64_t N, int64_t K, int sms, bool argmax,
-                                 int x_bytes, int topk_k = 0) {
+                                 ActFormat act, int topk_k = 0) {
   WsLayout l;
   const bool keys = argmax || topk_k > 0;
   const int BN = lm_head_token_tile(M);
@@ -765,7 +789,7 @@ static inline WsLayout ws_layout(int64_t M, int64_t N, int64_t K, int sms, bool 
   const int64_t n_units = ((N + kRows - 1) / kRows) * ((M + BN - 1) / BN);
   l.grid = (int)std::max<int64_t>(1, std::min<int64_t>(sms, n_units));
   l.x16 = kWsHeader;
-  l.tok = l.x16 + align_up((size_t)m_pad * K * x_bytes, 1024);
+  l.tok = l.x16 + align_up(act_region_bytes(act, m_pad, M, K), 1024);
   l.cnt = l.tok + align_up((size_t)m_pad * 4, 256);
   l.ready = l.cnt + align_up((size_t)l.grid * 4 * 4, 256);
   l.done = l.ready + align_up((size_t)l.grid * 4 * 4, 256);
@@ -777,6 +801,39 @@ static inline WsLayout ws_layout(int64_t M, int64_t N, int64_t K, int sms, bool 
   l.total = l.cand + (topk_k > 0 ? (size_t)M * N * 4 : 0);
   return l;
 }
+
+// Weight rows whose byte length is not a 16-byte multiple cannot be read by
+// TMA in place (a tensor map's row stride must be one): such a matrix is
+// copied, row for row, into the workspace with the stride rounded up, and
+// the TMA zero-fills everything past the row's real length.  NVFP4 codes
+// [rows, K/2] need the copy when K % 32 != 0, block scales [rows, K/16] when
+// K % 256 != 0.  `off` is where the copies start (after the call's other
+// regions); a copy absent for this K has size 0.
+struct WeightStage {
+  size_t packed_off, packed_stride, scales_off, scales_stride, total;
+  bool packed, scales;
+};
+
+static inline int64_t round_up16(int64_t v) { return (v + 15) / 16 * 16; }
+
+static inline WeightStage weight_stage(int64_t rows, int64_t K, size_t off, bool with_scales) {
+  WeightStage w;
+  w.packed = (K / 2) % 16 != 0;
+  w.scales = with_scales && (K / 16) % 16 != 0;
+  w.packed_stride = (size_t)round_up16(K / 2);
+  w.scales_stride = (size_t)round_up16(K / 16);
+  w.packed_off = align_up(off, 256);
+  const size_t after_packed = w.packed_off + (w.packed ? align_up(rows * w.packed_stride, 256) : 0);
+  w.scales_off = after_packed;
+  w.total = w.scales_off + (w.scales ? align_up(rows * w.scales_stride, 256) : 0);
+  return w;
+}
+
+// Launch the row copy (lm_head.cu) as a programmatic dependent of the
+// previous kernel in the stream: `rows` rows of `row_bytes` bytes, read back
+// to back from `src`, written `dst_stride` bytes apart (a 16-byte multiple).
+cudaError_t stage_rows_launch(const uint8_t* src, int64_t rows, int64_t row_bytes, uint8_t* dst,
+                              int64_t dst_stride, cudaStream_t stream);
 
 // The top-k selection kernel (topk.cu), launched after a top-k GEMM.
 cudaError_t topk_select_launch(const unsigned long long* lines, const uint2* grp,

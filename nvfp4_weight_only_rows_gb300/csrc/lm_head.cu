@@ -168,6 +168,54 @@ __global__ void __launch_bounds__(256) w4a16_prep_x_kernel(const uint16_t* __res
   }
 }
 
+// ------------------------------------------------------------ weight rows
+// Row copy into a TMA-readable stride (see WeightStage): one warp per row,
+// in units of T (8 bytes for NVFP4 code rows, which K % 16 makes 8-byte
+// multiples; 1 byte for block-scale rows).  Launched as a programmatic
+// dependent: the weights may have been written by the kernel before it.
+template <typename T>
+__global__ void __launch_bounds__(256) stage_rows_kernel(const T* __restrict__ src, int64_t rows,
+                                                         int64_t row_elems, T* __restrict__ dst,
+                                                         int64_t dst_stride_elems) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const int lane = threadIdx.x & 31;
+  const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
+  for (int64_t r = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); r < rows;
+       r += warps) {
+    const T* s = src + r * row_elems;
+    T* d = dst + r * dst_stride_elems;
+    for (int64_t j = lane; j < row_elems; j += 32) d[j] = s[j];
+  }
+}
+
+cudaError_t stage_rows_launch(const uint8_t* src, int64_t rows, int64_t row_bytes, uint8_t* dst,
+                              int64_t dst_stride, cudaStream_t stream) {
+  const int sms = std::max(sm_count(), 1);
+  const int64_t blocks = std::min<int64_t>((rows + 7) / 8, (int64_t)sms * 8);
+  PdlLaunch l(dim3((unsigned)std::max<int64_t>(blocks, 1)), dim3(256), 0, stream);
+  if (row_bytes % 8 == 0)
+    return cudaLaunchKernelEx(&l.cfg, stage_rows_kernel<uint2>,
+                              reinterpret_cast<const uint2*>(src), rows, row_bytes / 8,
+                              reinterpret_cast<uint2*>(dst), dst_stride / 8);
+  return cudaLaunchKernelEx(&l.cfg, stage_rows_kernel<uint8_t>, src, rows, row_bytes, dst,
+                            dst_stride);
+}
+
+// Stage the weight rows that TMA cannot read in place (both copies are
+// no-ops for K % 256 == 0, the usual lm_head width).
+static cudaError_t stage_weights(const WeightStage& w, const uint8_t* packed,
+                                 const uint8_t* scales, int64_t rows, int64_t K, uint8_t* ws,
+                                 cudaStream_t stream) {
+  cudaError_t e = cudaSuccess;
+  if (w.packed)
+    e = stage_rows_launch(packed, rows, K / 2, ws + w.packed_off, (int64_t)w.packed_stride, stream);
+  if (e == cudaSuccess && w.scales)
+    e = stage_rows_launch(scales, rows, K / 16, ws + w.scales_off, (int64_t)w.scales_stride,
+                          stream);
+  return e;
+}
+
 // Up to this many token rows the prep kernel gives each row a whole CTA.
 constexpr int64_t kPrepWideRows = 256;
 
@@ -481,7 +529,8 @@ static size_t gemm_smem_bytes(int BN, int stages, int pstages, bool argmax, bool
 }
 
 size_t lm_head_workspace_bytes(int64_t M, int64_t N, int64_t K, bool argmax) {
-  return ws_layout(M, N, K, std::max(sm_count(), 1), argmax, 2).total;
+  const WsLayout L = ws_layout(M, N, K, std::max(sm_count(), 1), argmax, ActFormat::kF16);
+  return weight_stage(N, K, L.total, true).total;
 }
 
 // Launch one instantiation (programmatic dependent of the prep kernel).
@@ -512,8 +561,24 @@ static cudaError_t launch_gemm(const CUtensorMap& tm_packed, const CUtensorMap& 
   return cudaLaunchKernelEx(&cfg, kern, tm_packed, tm_scales, tm_x, a);
 }
 
+// Tensor maps of the packed codes and block scales of `rows` weight rows:
+// in place where the row length is a 16-byte multiple, else over the
+// staged copy.  The map's extent is the real row length, so the TMA fills
+// the k past K with zeros (code 0, scale 0: the weight is 0 there).
+static bool encode_weight_maps(CUtensorMap* tm_packed, CUtensorMap* tm_scales,
+                               const WeightStage& w, const uint8_t* packed, const uint8_t* scales,
+                               int64_t rows, int64_t K, uint8_t* ws) {
+  return encode_2d(tm_packed, CU_TENSOR_MAP_DATA_TYPE_UINT8, w.packed ? ws + w.packed_off : packed,
+                   (uint64_t)K / 2, (uint64_t)rows, w.packed ? w.packed_stride : (uint64_t)K / 2,
+                   kKS / 2, kRows, CU_TENSOR_MAP_SWIZZLE_128B) &&
+         encode_2d(tm_scales, CU_TENSOR_MAP_DATA_TYPE_UINT8, w.scales ? ws + w.scales_off : scales,
+                   (uint64_t)K / 16, (uint64_t)rows, w.scales ? w.scales_stride : (uint64_t)K / 16,
+                   kKS / 16, kRows, CU_TENSOR_MAP_SWIZZLE_NONE);
+}
+
 size_t lm_head_topk_workspace_bytes(int64_t M, int64_t N, int64_t K, int k) {
-  return ws_layout(M, N, K, std::max(sm_count(), 1), false, 2, k).total;
+  const WsLayout L = ws_layout(M, N, K, std::max(sm_count(), 1), false, ActFormat::kF16, k);
+  return weight_stage(N, K, L.total, true).total;
 }
 
 // out_mode: NVFP4_OUT_F32 / NVFP4_OUT_BF16 write logits[M, N] to `logits`;
@@ -531,7 +596,7 @@ static nvfp4_status lm_head_run(const void* x, int64_t M, int64_t K, const uint8
   const bool keys = argmax || topk;
   const int BN = lm_head_token_tile(M);
   const int n_ttiles = (int)((M + BN - 1) / BN);
-  const WsLayout L = ws_layout(M, N, K, sms, argmax, 2, topk ? topk_k : 0);
+  const WsLayout L = ws_layout(M, N, K, sms, argmax, ActFormat::kF16, topk ? topk_k : 0);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   int32_t* status = reinterpret_cast<int32_t*>(ws);
   __half* x16 = reinterpret_cast<__half*>(ws + L.x16);
@@ -539,15 +604,14 @@ static nvfp4_status lm_head_run(const void* x, int64_t M, int64_t K, const uint8
   uint32_t* split_cnt = reinterpret_cast<uint32_t*>(ws + L.cnt);
   uint32_t* split_ready = reinterpret_cast<uint32_t*>(ws + L.ready);
   float* split_part = reinterpret_cast<float*>(ws + L.part);
+  const WeightStage wst = weight_stage(N, K, L.total, true);
 
   CUtensorMap tm_packed, tm_scales, tm_x;
-  if (!encode_2d(&tm_packed, CU_TENSOR_MAP_DATA_TYPE_UINT8, packed, (uint64_t)K / 2, (uint64_t)N,
-                 (uint64_t)K / 2, kKS / 2, kRows, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !encode_2d(&tm_scales, CU_TENSOR_MAP_DATA_TYPE_UINT8, scales, (uint64_t)K / 16, (uint64_t)N,
-                 (uint64_t)K / 16, kKS / 16, kRows, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+  if (!encode_weight_maps(&tm_packed, &tm_scales, wst, packed, scales, N, K, ws) ||
       !encode_2d(&tm_x, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, x16, (uint64_t)K, (uint64_t)M,
                  (uint64_t)K * 2, 64, (uint32_t)BN, CU_TENSOR_MAP_SWIZZLE_128B))
     return NVFP4_ERR_CUDA;
+  if (stage_weights(wst, packed, scales, N, K, ws, stream) != cudaSuccess) return NVFP4_ERR_CUDA;
 
   // the counters, ready flags and the argmax counter are adjacent: the
   // prep kernel clears them all
@@ -582,7 +646,7 @@ static nvfp4_status lm_head_run(const void* x, int64_t M, int64_t K, const uint8
   a.BN = BN;
   a.n_ttiles = n_ttiles;
   a.n_units = ((N + kRows - 1) / kRows) * n_ttiles;
-  a.n_kb = (int)(K / kKB);
+  a.n_kb = (int)((K + kKB - 1) / kKB);  // the last stage's k past K reads zeros
   schedule_units(a, L.grid);
   a.split_cnt = split_cnt;
   a.split_ready = split_ready;
@@ -667,7 +731,8 @@ size_t grouped_workspace_bytes(int64_t M, int64_t N, int64_t K, int64_t n_groups
   // the plain product's layout for M token rows and a grid of at most
   // min(SMs, unit bound); its token tile is never below the grouped one, so
   // the split-K partials fit
-  return ws_layout(M, units * kRows, K, sms, false, 2).total;
+  const WsLayout L = ws_layout(M, units * kRows, K, sms, false, ActFormat::kF16);
+  return weight_stage(n_groups * N, K, L.total, true).total;
 }
 
 nvfp4_status grouped_launch(const void* x, int64_t M, int64_t K, const int32_t* grp_off,
@@ -680,21 +745,20 @@ nvfp4_status grouped_launch(const void* x, int64_t M, int64_t K, const int32_t* 
   const int64_t units = grouped_units_bound(M, N, n_groups, BN);
   // same byte layout as grouped_workspace_bytes: token rows M (TMA zero-fills
   // past them), grid min(SMs, unit bound)
-  const WsLayout L = ws_layout(M, units * kRows, K, sms, false, 2);
+  const WsLayout L = ws_layout(M, units * kRows, K, sms, false, ActFormat::kF16);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   int32_t* status = reinterpret_cast<int32_t*>(ws);
   __half* x16 = reinterpret_cast<__half*>(ws + L.x16);
   float* tok_scale = reinterpret_cast<float*>(ws + L.tok);
 
   CUtensorMap tm_packed, tm_scales, tm_x;
-  const uint64_t rows = (uint64_t)n_groups * (uint64_t)N;
-  if (!encode_2d(&tm_packed, CU_TENSOR_MAP_DATA_TYPE_UINT8, packed, (uint64_t)K / 2, rows,
-                 (uint64_t)K / 2, kKS / 2, kRows, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !encode_2d(&tm_scales, CU_TENSOR_MAP_DATA_TYPE_UINT8, scales, (uint64_t)K / 16, rows,
-                 (uint64_t)K / 16, kKS / 16, kRows, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+  const int64_t rows = n_groups * N;
+  const WeightStage wst = weight_stage(rows, K, L.total, true);
+  if (!encode_weight_maps(&tm_packed, &tm_scales, wst, packed, scales, rows, K, ws) ||
       !encode_2d(&tm_x, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, x16, (uint64_t)K, (uint64_t)M,
                  (uint64_t)K * 2, 64, (uint32_t)BN, CU_TENSOR_MAP_SWIZZLE_128B))
     return NVFP4_ERR_CUDA;
+  if (stage_weights(wst, packed, scales, rows, K, ws, stream) != cudaSuccess) return NVFP4_ERR_CUDA;
   {
     const bool wide = M <= kPrepWideRows;
     PdlLaunch l(dim3((unsigned)(wide ? M : (M + 7) / 8)), dim3(wide ? 128 : 256), 0, stream);
@@ -713,7 +777,7 @@ nvfp4_status grouped_launch(const void* x, int64_t M, int64_t K, const int32_t* 
   a.K = K;
   a.BN = BN;
   a.n_ttiles = 1;
-  a.n_kb = (int)(K / kKB);
+  a.n_kb = (int)((K + kKB - 1) / kKB);
   a.split_cnt = reinterpret_cast<uint32_t*>(ws + L.cnt);
   a.split_ready = reinterpret_cast<uint32_t*>(ws + L.ready);
   a.split_part = reinterpret_cast<float*>(ws + L.part);

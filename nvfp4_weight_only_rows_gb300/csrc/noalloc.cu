@@ -54,7 +54,7 @@ extern "C" nvfp4_status w4a16_lm_head_noalloc(const void* x, int64_t M, int64_t 
                                               const float* global_scale, int64_t N,
                                               void* logits, int out_dtype, void* stream) {
   using namespace nvfp4;
-  if (M < 0 || N < 0 || K < 256 || K % 256 != 0) return NVFP4_ERR_SHAPE;
+  if (M < 0 || N < 0 || K < 16 || K % 16 != 0) return NVFP4_ERR_SHAPE;
   if (out_dtype != NVFP4_OUT_F32 && out_dtype != NVFP4_OUT_BF16) return NVFP4_ERR_DTYPE;
   if (M == 0 || N == 0) return NVFP4_OK;
   // M * K decides the scratch: reject what the fixed array cannot hold

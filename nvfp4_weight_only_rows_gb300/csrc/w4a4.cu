@@ -18,7 +18,8 @@
 //
 // Kernels:
 //  nvfp4_swizzle_scales_kernel  row-major [N, K/16] -> interleaved
-//                               [N_pad128 / 128][K/64][32][4][4] bytes;
+//                               [N_pad128 / 128][ceil(K/64)][32][4][4] bytes
+//                               (rows padded to 128, columns to 4, with zeros);
 //  w4a4_prep_x_kernel           one CTA per token (padded to 128): codes,
 //                               interleaved scales, alpha; per-call clearing;
 //  w4a4_tc_kernel               persistent GEMM: warp 0 streams weight codes
@@ -35,8 +36,8 @@
 namespace nvfp4 {
 
 // Byte offset of scale (row r, k-block c) in the 128x4-interleaved layout of
-// a matrix with kb = K/16 scale columns (kb % 4 == 0): 512-byte atoms of 128
-// rows x 4 columns, ordered [row / 128][c / 4]; inside an atom row
+// a matrix with kb scale columns after padding (kb % 4 == 0): 512-byte atoms
+// of 128 rows x 4 columns, ordered [row / 128][c / 4]; inside an atom row
 // 32 a + b, column d sits at b * 16 + a * 4 + d.
 __host__ __device__ __forceinline__ int64_t sf_offset(int64_t r, int64_t c, int64_t kb) {
   const int64_t rr = r & 127, a = rr >> 5, b = rr & 31;
@@ -44,18 +45,28 @@ __host__ __device__ __forceinline__ int64_t sf_offset(int64_t r, int64_t c, int6
 }
 
 // ------------------------------------------------------------ scale layout
-// One thread per 4 output bytes (one row's 4 consecutive k-blocks).
+// One thread per 4 output bytes (one row's 4 consecutive k-blocks).  kb:
+// the source's scale columns (K/16); kbp: kb rounded up to 4.  Rows past N
+// and columns past kb are written as zero.
 __global__ void __launch_bounds__(256) nvfp4_swizzle_scales_kernel(
-    const uint8_t* __restrict__ scales, int64_t N, int64_t kb, uint8_t* __restrict__ out,
-    int64_t n_words) {
+    const uint8_t* __restrict__ scales, int64_t N, int64_t kb, int64_t kbp,
+    uint8_t* __restrict__ out, int64_t n_words) {
   const int64_t w = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (w >= n_words) return;
   // word w of the output: atom w / 128, inside it b = (w % 128) / 4, a = w % 4
   const int64_t atom = w >> 7, b = (w >> 2) & 31, a = w & 3;
-  const int64_t c4 = atom % (kb >> 2), rt = atom / (kb >> 2);
+  const int64_t c4 = atom % (kbp >> 2), rt = atom / (kbp >> 2);
   const int64_t r = rt * 128 + a * 32 + b;
   uint32_t v = 0;
-  if (r < N) v = *reinterpret_cast<const uint32_t*>(scales + r * kb + c4 * 4);
+  if (r < N) {
+    const uint8_t* src = scales + r * kb + c4 * 4;
+    if (kb % 4 == 0) {  // whole, 4-byte aligned words
+      v = *reinterpret_cast<const uint32_t*>(src);
+    } else {
+      for (int d = 0; d < 4; ++d)
+        if (c4 * 4 + d < kb) v |= (uint32_t)src[d] << (8 * d);
+    }
+  }
   reinterpret_cast<uint32_t*>(out)[w] = v;
 }
 
@@ -73,7 +84,9 @@ __global__ void __launch_bounds__(256) w4a4_prep_x_kernel(
     for (int i = threadIdx.x; i < n_split_flags; i += blockDim.x) split_flags[i] = 0;
   }
   const int64_t m = blockIdx.x;  // 0 .. round_up(M, 128) - 1
-  const int64_t kb = K / 16;
+  const int64_t kb = K / 16;                      // scale columns
+  const int64_t kbp = (kb + 3) / 4 * 4;           // ... padded to whole atoms (zero scales)
+  const int64_t xs = (K / 2 + 15) / 16 * 16;      // code row stride (a TMA row stride)
   const float g = *g_in;
   if (threadIdx.x == 0) {
     if (m < m_pad) tok_scale[m] = m < M ? __fmul_rn(g, *g_w) : 0.0f;
@@ -83,10 +96,10 @@ __global__ void __launch_bounds__(256) w4a4_prep_x_kernel(
   if (m < m_pad) token_state_clear(am_keys, tk_hist, m, threadIdx.x, blockDim.x);  // argmax / top-k
   const float ig = __frcp_rn(g);
   const float inv6 = 1.0f / 6.0f;
-  for (int64_t c = threadIdx.x; c < kb; c += blockDim.x) {
+  for (int64_t c = threadIdx.x; c < kbp; c += blockDim.x) {
     uint32_t word0 = 0, word1 = 0;
     uint8_t s8 = 0;
-    if (m < M) {
+    if (m < M && c < kb) {
       const uint4* src = reinterpret_cast<const uint4*>(x + m * K + c * 16);
       const uint4 v0 = src[0], v1 = src[1];
       const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
@@ -111,8 +124,8 @@ __global__ void __launch_bounds__(256) w4a4_prep_x_kernel(
         (h == 0 ? word0 : word1) = cvt_e2m1x8(q);
       }
     }
-    if (m < m_pad) reinterpret_cast<uint2*>(xq + m * (K / 2))[c] = make_uint2(word0, word1);
-    xsf[sf_offset(m, c, kb)] = s8;
+    if (m < m_pad && c < kb) reinterpret_cast<uint2*>(xq + m * xs)[c] = make_uint2(word0, word1);
+    xsf[sf_offset(m, c, kbp)] = s8;
   }
 }
 
@@ -125,6 +138,13 @@ constexpr int w4a4_threads() { return kW4Threads + (kOut == kOutTopk ? 32 : 0); 
 constexpr uint32_t kW4AStageBytes = kRows * (kKB / 2);  // 128 rows x 256 fp4 = 16 KB
 constexpr uint32_t kW4SfStageBytes = 4 * 512;            // 4 atoms (16 k-blocks) x 128 rows
 constexpr uint32_t kW4SfCols = 32;                       // TMEM columns per stage: A 16 + B 16
+
+// Scale atoms (one per 64 k, 512 bytes for 128 rows) of 256-k stage kb:
+// four, except in the last stage of a K that is not a multiple of 256.
+__device__ __forceinline__ uint32_t stage_atoms(int64_t kb4, uint32_t kb) {
+  const int64_t left = kb4 - 4 * (int64_t)kb;
+  return left < 4 ? (uint32_t)left : 4u;
+}
 
 template <int kOut, int kStages>
 __global__ void __launch_bounds__(w4a4_threads<kOut>(), 1)
@@ -181,7 +201,7 @@ __global__ void __launch_bounds__(w4a4_threads<kOut>(), 1)
   tc_fence_after();
   const uint32_t tmem_base = __shfl_sync(0xFFFFFFFFu, *tmem_slot, 0);
   WaitCtl wc{p.status, abort_flag, kWaitLimitNs};
-  const int64_t kb4 = p.K / 64;  // scale atoms per 128-row band
+  const int64_t kb4 = (p.K + 63) / 64;  // scale atoms per 128-row band (K/16 padded to 4)
 
   if (warp == 0) {
     // ---------------- weight codes (TMA) + their scale atoms (bulk copy)
@@ -193,11 +213,12 @@ __global__ void __launch_bounds__(w4a4_threads<kOut>(), 1)
         const uint32_t st = issued % kStages, ph = (issued / kStages) & 1;
         if (!warp_wait(&s_empty[st], ph ^ 1, wc)) return false;
         if (elect_one()) {
-          mbar_arrive_expect_tx(&s_full[st], kW4AStageBytes + kW4SfStageBytes);
+          const uint32_t sf_bytes = stage_atoms(kb4, kb) * 512;
+          mbar_arrive_expect_tx(&s_full[st], kW4AStageBytes + sf_bytes);
           tma_load_2d_hint(s_a + st * kW4AStageBytes, &tm_w, kb * (kKB / 2), (int32_t)(nt * kRows),
                            &s_full[st], pol);
           bulk_load(s_sfa + st * kW4SfStageBytes, wsf + ((int64_t)nt * kb4 + 4 * kb) * 512,
-                    kW4SfStageBytes, &s_full[st], pol);
+                    sf_bytes, &s_full[st], pol);
         }
         __syncwarp();
       }
@@ -215,11 +236,12 @@ __global__ void __launch_bounds__(w4a4_threads<kOut>(), 1)
         const uint32_t st = issued % kStages, ph = (issued / kStages) & 1;
         if (!warp_wait(&s_empty[st], ph ^ 1, wc)) return false;
         if (elect_one()) {
-          mbar_arrive_expect_tx(&s_full[st], x_stage_bytes + kW4SfStageBytes);
+          const uint32_t sf_bytes = stage_atoms(kb4, kb) * 512;
+          mbar_arrive_expect_tx(&s_full[st], x_stage_bytes + sf_bytes);
           tma_load_2d_hint(s_x + st * x_stage_bytes, &tm_x, kb * (kKB / 2), (int32_t)t0,
                            &s_full[st], pol);
           bulk_load(s_sfb + st * kW4SfStageBytes, xsf + ((t0 >> 7) * kb4 + 4 * kb) * 512,
-                    kW4SfStageBytes, &s_full[st], pol);
+                    sf_bytes, &s_full[st], pol);
         }
         __syncwarp();
       }
@@ -249,16 +271,22 @@ __global__ void __launch_bounds__(w4a4_threads<kOut>(), 1)
         const uint64_t ad = adesc0 + ((st * kW4AStageBytes) >> 4);
         const uint64_t xd = xdesc0 + ((st * x_stage_bytes) >> 4);
         const uint32_t sfa = sf_base + st * kW4SfCols, sfb = sfa + 16;
+        // one scale atom per MMA of K = 64; the last stage of a K that is not a
+        // multiple of 256 has fewer (the k past the last atom is not multiplied)
+        const uint32_t n_at = stage_atoms(kb4, kb);
         if (elect_one()) {
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
-            tc_cp_32x128b_x4(sfa + 4 * j, smem_u32(s_sfa + st * kW4SfStageBytes + 512 * j));
-            tc_cp_32x128b_x4(sfb + 4 * j, smem_u32(s_sfb + st * kW4SfStageBytes + 512 * j));
+            if ((uint32_t)j < n_at) {
+              tc_cp_32x128b_x4(sfa + 4 * j, smem_u32(s_sfa + st * kW4SfStageBytes + 512 * j));
+              tc_cp_32x128b_x4(sfb + 4 * j, smem_u32(s_sfb + st * kW4SfStageBytes + 512 * j));
+            }
           }
 #pragma unroll
           for (int j = 0; j < 4; ++j)
-            tc_mma_fp4_bs(d_tmem, ad + 2 * j, xd + 2 * j, idesc, sfa + 4 * j, sfb + 4 * j,
-                          (kb != pc.kb0) || (j != 0));
+            if ((uint32_t)j < n_at)
+              tc_mma_fp4_bs(d_tmem, ad + 2 * j, xd + 2 * j, idesc, sfa + 4 * j, sfb + 4 * j,
+                            (kb != pc.kb0) || (j != 0));
           tc_commit(&s_empty[st]);
         }
         __syncwarp();
@@ -295,14 +323,15 @@ __global__ void __launch_bounds__(w4a4_threads<kOut>(), 1)
 static int64_t round_up128(int64_t v) { return (v + 127) / 128 * 128; }
 
 size_t nvfp4_swizzled_scales_size(int64_t N, int64_t K) {
-  return (size_t)round_up128(N) * (size_t)(K / 16);
+  return (size_t)round_up128(N) * (size_t)interleaved_sf_cols(K);
 }
 
 nvfp4_status swizzle_scales_launch(const uint8_t* scales, int64_t N, int64_t K, uint8_t* out,
                                    cudaStream_t stream) {
   const int64_t n_words = (int64_t)nvfp4_swizzled_scales_size(N, K) / 4;
   const int64_t blocks = (n_words + 255) / 256;
-  nvfp4_swizzle_scales_kernel<<<(unsigned)blocks, 256, 0, stream>>>(scales, N, K / 16, out, n_words);
+  nvfp4_swizzle_scales_kernel<<<(unsigned)blocks, 256, 0, stream>>>(
+      scales, N, K / 16, interleaved_sf_cols(K), out, n_words);
   return cudaGetLastError() == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA;
 }
 
@@ -311,16 +340,18 @@ static size_t w4a4_smem_bytes(int BN, int stages, bool argmax) {
          4 * kMaxBN * sizeof(float) + (argmax ? 16 + 4 * kMaxBN * sizeof(float) : 0);
 }
 
-// Workspace: the generic layout with one byte per activation value, which
-// holds the x codes (M_pad x K/2) followed by the interleaved x scales
-// (round_up(M, 128) x K/16 bytes): the latter never exceed M_pad x K/2
-// because M_pad >= 16.
+// Workspace: the generic layout with the x codes (M_pad rows, a 16-byte
+// multiple apart) and the interleaved x scales (round_up(M, 128) x
+// round_up(K/16, 4) bytes) as the activation region; then, where K % 32 !=
+// 0, the weight codes staged to a TMA-readable row stride.
 size_t w4a4_workspace_bytes(int64_t M, int64_t N, int64_t K, bool argmax) {
-  return ws_layout(M, N, K, std::max(sm_count(), 1), argmax, 1).total;
+  const WsLayout L = ws_layout(M, N, K, std::max(sm_count(), 1), argmax, ActFormat::kE2M1);
+  return weight_stage(N, K, L.total, false).total;
 }
 
 size_t w4a4_topk_workspace_bytes(int64_t M, int64_t N, int64_t K, int k) {
-  return ws_layout(M, N, K, std::max(sm_count(), 1), false, 1, k).total;
+  const WsLayout L = ws_layout(M, N, K, std::max(sm_count(), 1), false, ActFormat::kE2M1, k);
+  return weight_stage(N, K, L.total, false).total;
 }
 
 template <int kOut, int kStages>
@@ -354,20 +385,27 @@ static nvfp4_status w4a4_run(const void* x, int64_t M, int64_t K, const uint8_t*
   const int n_ttiles = (int)((M + BN - 1) / BN);
   const int64_t m_pad = (int64_t)n_ttiles * BN;
   const int64_t m_pad128 = round_up128(M);
-  const WsLayout L = ws_layout(M, N, K, sms, argmax, 1, topk ? topk_k : 0);
+  const WsLayout L = ws_layout(M, N, K, sms, argmax, ActFormat::kE2M1, topk ? topk_k : 0);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   int32_t* status = reinterpret_cast<int32_t*>(ws);
   uint8_t* xq = ws + L.x16;
-  uint8_t* xsf = xq + (size_t)m_pad * (K / 2);
+  const int64_t xs = e2m1_code_stride(K);
+  uint8_t* xsf = xq + align_up((size_t)m_pad * xs, 256);
+  const WeightStage wst = weight_stage(N, K, L.total, false);
   float* tok_scale = reinterpret_cast<float*>(ws + L.tok);
   unsigned long long* keys =
       argmax || topk ? reinterpret_cast<unsigned long long*>(ws + L.keys) : nullptr;
 
   CUtensorMap tm_w, tm_x;
-  if (!encode_2d(&tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, packed, (uint64_t)K / 2, (uint64_t)N,
-                 (uint64_t)K / 2, 128, kRows, CU_TENSOR_MAP_SWIZZLE_128B) ||
+  // both maps end at K/2 bytes: the TMA fills the k past K with zero codes
+  if (!encode_2d(&tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, wst.packed ? ws + wst.packed_off : packed,
+                 (uint64_t)K / 2, (uint64_t)N, wst.packed ? wst.packed_stride : (uint64_t)K / 2,
+                 128, kRows, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !encode_2d(&tm_x, CU_TENSOR_MAP_DATA_TYPE_UINT8, xq, (uint64_t)K / 2, (uint64_t)m_pad,
-                 (uint64_t)K / 2, 128, (uint32_t)BN, CU_TENSOR_MAP_SWIZZLE_128B))
+                 (uint64_t)xs, 128, (uint32_t)BN, CU_TENSOR_MAP_SWIZZLE_128B))
+    return NVFP4_ERR_CUDA;
+  if (wst.packed && stage_rows_launch(packed, N, K / 2, ws + wst.packed_off,
+                                      (int64_t)wst.packed_stride, stream) != cudaSuccess)
     return NVFP4_ERR_CUDA;
 
   {
@@ -387,7 +425,7 @@ static nvfp4_status w4a4_run(const void* x, int64_t M, int64_t K, const uint8_t*
   a.BN = BN;
   a.n_ttiles = n_ttiles;
   a.n_units = ((N + kRows - 1) / kRows) * n_ttiles;
-  a.n_kb = (int)(K / kKB);
+  a.n_kb = (int)((K + kKB - 1) / kKB);
   schedule_units(a, L.grid);
   const bool small = BN <= 64;
   const uint32_t need = 2u * BN + (small ? 6u : 5u) * kW4SfCols;

@@ -63,7 +63,8 @@ def test_workspace_sizes(lib):
     assert lib.nvfp4_quantize_workspace_bytes(10, 24) == 0      # K % 16 != 0
     assert lib.nvfp4_quantize_workspace_bytes(0, 32) == 0
     assert lib.nvfp4_quantize_workspace_bytes(10, 32) >= 256
-    assert lib.w4a16_lm_head_workspace_bytes(4, 512, 300) == 0   # K % 256 != 0
+    assert lib.w4a16_lm_head_workspace_bytes(4, 512, 300) == 0   # K % 16 != 0
+    assert lib.w4a16_lm_head_workspace_bytes(4, 512, 272) > 0    # any K % 16 (staged rows)
     w = lib.w4a16_lm_head_workspace_bytes(64, 128256, 4096)
     assert w >= 64 * 4096 * 2 + 64 * 4 + 256
 
@@ -78,7 +79,7 @@ def test_host_argument_errors_before_any_cuda_call(lib):
     assert q(fake, 4, 32, fake, fake, fake, fake, 16, None) == 4             # WORKSPACE
     assert q(vp((1 << 20) + 8), 4, 32, fake, fake, fake, fake, 1 << 20, None) == 2  # ALIGN
     g = lib.w4a16_lm_head
-    assert g(fake, 4, 300, fake, fake, fake, 8, fake, 0, fake, 1 << 30, None) == 1   # K % 256
+    assert g(fake, 4, 300, fake, fake, fake, 8, fake, 0, fake, 1 << 30, None) == 1   # K % 16
     assert g(fake, -1, 256, fake, fake, fake, 8, fake, 0, fake, 1 << 30, None) == 1  # M < 0
     assert g(fake, 4, 256, fake, fake, fake, 8, fake, 7, fake, 1 << 30, None) == 5   # DTYPE
     assert g(fake, 0, 256, fake, fake, fake, 8, fake, 0, None, 0, None) == 0         # empty
@@ -90,7 +91,7 @@ def test_host_argument_errors_before_any_cuda_call(lib):
     a = lib.w4a16_lm_head_argmax
     ids, vals = vp(1 << 20), vp(1 << 21)
     assert a(fake, 4, 256, fake, fake, fake, 0, ids, vals, fake, 1 << 30, None) == 1   # N == 0
-    assert a(fake, 4, 300, fake, fake, fake, 8, ids, vals, fake, 1 << 30, None) == 1   # K % 256
+    assert a(fake, 4, 300, fake, fake, fake, 8, ids, vals, fake, 1 << 30, None) == 1   # K % 16
     assert a(fake, 0, 256, fake, fake, fake, 8, ids, vals, None, 0, None) == 0         # empty
     assert a(fake, 4, 256, fake, fake, fake, 8, None, vals, fake, 1 << 30, None) == 3  # NULL ids
     assert a(fake, 4, 256, fake, fake, fake, 8, ids, vals, fake, 64, None) == 4        # WORKSPACE
@@ -111,7 +112,7 @@ def test_fp8_host_argument_errors(lib):
     assert qz(fake, 4, 32, fake, fake, fake, 16, None) == 4               # WORKSPACE
     assert qz(fake, 4, 32, vp((1 << 20) + 4), fake, fake, 1 << 20, None) == 2  # ALIGN q
     g = lib.w8a8_lm_head
-    assert g(fake, 4, 300, fake, fake, 8, fake, 0, fake, 1 << 30, None) == 1    # K % 256
+    assert g(fake, 4, 300, fake, fake, 8, fake, 0, fake, 1 << 30, None) == 1    # K % 16
     assert g(fake, 4, 16640, fake, fake, 8, fake, 0, fake, 1 << 30, None) == 1  # K > 16384
     assert g(fake, 4, 256, fake, fake, 8, fake, 9, fake, 1 << 30, None) == 5    # DTYPE
     assert g(fake, 0, 256, fake, fake, 8, fake, 0, None, 0, None) == 0          # empty
@@ -129,10 +130,11 @@ def test_w4a4_host_argument_errors(lib):
     vp = ctypes.c_void_p
     fake = vp(1 << 20)
     sw = lib.nvfp4_swizzle_scales
-    assert sw(fake, 4, 48, fake, None) == 1                      # K % 64
+    assert sw(fake, 4, 40, fake, None) == 1                      # K % 16
     assert sw(None, 4, 64, fake, None) == 3                      # NULL
     assert sw(fake, 4, 64, vp((1 << 20) + 4), None) == 2         # ALIGN out
     assert lib.nvfp4_swizzled_scales_bytes(130, 128) == 256 * 8
+    assert lib.nvfp4_swizzled_scales_bytes(130, 48) == 256 * 4   # 3 scale columns padded to 4
     g = lib.w4a4_lm_head
     assert g(fake, 4, 300, fake, fake, fake, fake, 8, fake, 0, fake, 1 << 30, None) == 1  # K
     assert g(fake, 4, 256, fake, fake, fake, fake, 8, fake, 3, fake, 1 << 30, None) == 5  # DTYPE
@@ -175,7 +177,7 @@ def test_topk_host_argument_errors_and_sizes(lib):
     assert t(fake, 4, 256, fake, fake, fake, 100, 0, ids, vals, fake, big, None) == 1     # k == 0
     assert t(fake, 4, 256, fake, fake, fake, 1000, 129, ids, vals, fake, big, None) == 1  # k > max
     assert t(fake, 4, 256, fake, fake, fake, 7, 8, ids, vals, fake, big, None) == 1       # k > N
-    assert t(fake, 4, 300, fake, fake, fake, 100, 5, ids, vals, fake, big, None) == 1     # K % 256
+    assert t(fake, 4, 300, fake, fake, fake, 100, 5, ids, vals, fake, big, None) == 1     # K % 16
     assert t(fake, 1 << 20, 256, fake, fake, fake, 1 << 17, 5, ids, vals, fake, big,
              None) == 1                                                                   # M*N > 2^36
     assert t(fake, 0, 256, fake, fake, fake, 100, 5, ids, vals, None, 0, None) == 0      # empty

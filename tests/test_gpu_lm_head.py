@@ -102,11 +102,13 @@ def test_errors_are_status_codes():
         nv.w4a16_lm_head(x, pd, sd, gd, workspace=torch.empty(64, dtype=torch.uint8,
                                                                device="cuda"))
     assert e.value.status == nv.Status.ERR_WORKSPACE
-    W2 = synth.quant_weight(N=64, K=272, seed=1)
-    _, (p2, s2, g2) = upload_quantized(W2)
-    x2 = to_bf16_dev(synth.decode_x(4, K=272))
+    # K = 264 is not a multiple of 16: no NVFP4 weight has that width
+    x2 = torch.zeros(4, 264, dtype=torch.bfloat16, device="cuda")
+    p2 = torch.zeros(64, 132, dtype=torch.uint8, device="cuda")
+    s2 = torch.zeros(64, 16, dtype=torch.uint8, device="cuda")
     with pytest.raises(nv.NVFP4Error) as e:
-        nv.w4a16_lm_head(x2, p2, s2, g2)
+        nv.w4a16_lm_head(x2, p2, s2, gd, workspace=torch.empty(1 << 20, dtype=torch.uint8,
+                                                               device="cuda"))
     assert e.value.status == nv.Status.ERR_SHAPE
 
 
