@@ -761,42 +761,110 @@ def run_moe(nv, synth, dev, per_call_us, capture, peaks, traffic, hbm_roof):
 
 
 # ----------------------------------------------------------- the CPU oracle
+def _timed(fn, reps=1):
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        fn()
+    return (time.perf_counter() - t0) / reps
+
+
 def cpu_baseline(budget_s: float = 15.0, steps: int = 1) -> dict:
-    """The oracle's decode product (float64, OpenMP over vocabulary rows) on a
-    sample of vocabulary rows, sized to about `budget_s` seconds of work.  The
-    sample's weights are quantized by the oracle with the full tensor's
-    global scale."""
+    """The oracle as it stands (float64 products, OpenMP over rows), on the
+    host's cores, for the three parts of the path:
+
+    * quantizer: the tiny W[512, 256] and the W[151936, 5120] quantize/refresh
+      weight in full (amax pass, then every block) on all cores; on one core
+      a seeded sample of the big weight's rows (with the full tensor's global
+      scale), its rate taken as the rate of the whole;
+    * decode: the W4A16 product for M in {1, 8, 32, 64} over the decode W;
+    * prefill: 64 token rows of x[2048, 4096] (each tile's edges) over every
+      vocabulary row on all cores (a vocabulary sample on one core), and the
+      full M = 2048 time EXTRAPOLATED from it.
+
+    Each part runs on all cores and on one core; where a full run does not
+    fit the budget, a row sample is timed and its rate reported (the sample
+    is named).  `value` is the decode GB/s on all cores (the metric's unit);
+    `steps` repeats the decode timing."""
     import oracle
     import synth
+
+    all_cores = os.cpu_count() or 1
+    parts = {}
+    share = budget_s / 8.0  # seconds per timed piece, roughly
+
+    def rows_for(rate_rows_per_s, total):
+        return int(max(128, min(total, rate_rows_per_s * share)))
 
     W = synth.decode_weight(seed=1)
     g, ig = oracle.global_scale(oracle.weight_amax(W))
     xs = synth.decode_x(max(DECODE_MS))
-
-    def sample(n):
-        p, s = oracle.quantize_rows(W, np.arange(n, dtype=np.int64), g, ig)
-        return p, s
-
-    n_probe = 512
-    p, s = sample(n_probe)
-    t0 = time.perf_counter()
-    for M in DECODE_MS:
-        oracle.logits(xs[:M], p, s, g)
-    probe = time.perf_counter() - t0
-    n_cols = int(min(N_VOCAB, max(n_probe, n_probe * budget_s / max(probe, 1e-3) / steps)))
-    p, s = sample(n_cols)
-    t0 = time.perf_counter()
-    for _ in range(steps):
-        for M in DECODE_MS:
-            oracle.logits(xs[:M], p, s, g)
-    dt = time.perf_counter() - t0
-    nbytes = steps * sum(n_cols * K_HID // 2 + n_cols * K_HID // 16 + 2 * M * K_HID +
-                         4 * M * n_cols for M in DECODE_MS)
-    return {"value": round(nbytes / dt / 1e9, 4), "unit": "GB/s", "cores": oracle.num_threads(),
+    decode_value = None
+    for cores in (all_cores, 1):
+        oracle.set_num_threads(cores)
+        # probe the decode rate on 256 rows, then size the timed sample
+        p, s_ = oracle.quantize_rows(W, np.arange(256, dtype=np.int64), g, ig)
+        probe = _timed(lambda: [oracle.logits(xs[:M], p, s_, g) for M in DECODE_MS])
+        n = rows_for(256 / max(probe, 1e-6) / max(steps, 1), N_VOCAB)
+        p, s_ = oracle.quantize_rows(W, np.arange(n, dtype=np.int64), g, ig)
+        dt = _timed(lambda: [oracle.logits(xs[:M], p, s_, g) for M in DECODE_MS], reps=steps)
+        nbytes = sum(n * K_HID // 2 + n * K_HID // 16 + 2 * M * K_HID + 4 * M * n
+                     for M in DECODE_MS)
+        gbs = nbytes / dt / 1e9
+        parts[f"decode_cores{cores}"] = {
+            "gbs": round(gbs, 4), "s_per_pass": round(dt, 3),
+            "sample": f"M in {{1,8,32,64}} over the first {n} of {N_VOCAB} rows"}
+        if cores == all_cores:
+            decode_value = gbs
+    # prefill: 64 token rows (first and last 2 of each 128-token tile)
+    xp = synth.prefill_x()
+    rows = np.array(sorted({t for t0 in range(0, PREFILL_M, 128)
+                            for t in (t0, t0 + 1, t0 + 126, t0 + 127)}), dtype=np.int64)
+    p_all, s_all = oracle.quantize_rows(W, np.arange(N_VOCAB, dtype=np.int64), g, ig)
+    for cores in (all_cores, 1):
+        oracle.set_num_threads(cores)
+        # all 64 token rows in one call (the dequantized weight row is shared
+        # by the tokens); one core: over a sample of the vocabulary rows
+        probe = _timed(lambda: oracle.logits(xp[rows], p_all[:256], s_all[:256], g))
+        n = N_VOCAB if cores == all_cores else \
+            int(max(256, min(N_VOCAB, 256 * share / max(probe, 1e-6))))
+        dt = _timed(lambda: oracle.logits(xp[rows], p_all[:n], s_all[:n], g))
+        full_s = dt * (N_VOCAB / n) * (PREFILL_M / rows.size)
+        parts[f"prefill_cores{cores}"] = {
+            "tflops": round(2 * rows.size * n * K_HID / dt / 1e12, 6),
+            "s_sample": round(dt, 3),
+            "extrapolated_s_full_M2048": round(full_s, 1),
+            "sample": f"the 64 tile-edge token rows of x[2048,4096] x the first {n} of {N_VOCAB} "
+                      "vocabulary rows; the full-M time is EXTRAPOLATED from it"}
+    del p_all, s_all, W
+    # quantizer: the tiny weight and the W[151936, 5120] quantize/refresh weight
+    Wt = synth.tiny_weight()
+    Wq = synth.quant_weight(N=151936, K=5120, seed=4)
+    for cores in (all_cores, 1):
+        oracle.set_num_threads(cores)
+        dt = _timed(lambda: oracle.quantize(Wt), reps=20)
+        parts[f"quantize_tiny_cores{cores}"] = {
+            "gbs": round(quant_bytes(512, 256) / dt / 1e9, 4), "s": round(dt, 6),
+            "sample": "W[512,256] in full"}
+        if cores == all_cores:
+            dt = _timed(lambda: oracle.quantize(Wq))
+            parts[f"quantize_W151936x5120_cores{cores}"] = {
+                "gbs": round(quant_bytes(151936, 5120) / dt / 1e9, 4), "s": round(dt, 3),
+                "sample": "W[151936,5120] in full (amax pass, then every block)"}
+        else:
+            n = 4096
+            sub = np.ascontiguousarray(Wq[:n])
+            rows_q = np.arange(n, dtype=np.int64)
+            gq, igq = oracle.global_scale(oracle.weight_amax(Wq))
+            dt = _timed(lambda: (oracle.weight_amax(sub), oracle.quantize_rows(sub, rows_q, gq, igq)))
+            parts[f"quantize_W151936x5120_cores{cores}"] = {
+                "gbs": round(quant_bytes(n, 5120) / dt / 1e9, 4), "s_sample": round(dt, 3),
+                "sample": f"first {n} of 151936 rows (amax over them, then their blocks with "
+                          "the tensor's global scale); rate taken as the whole tensor's"}
+    oracle.set_num_threads(0)
+    return {"value": round(decode_value, 4), "unit": "GB/s", "cores": all_cores,
             "kind": "oracle",
-            "sample": f"decode product M in {{1,8,32,64}} over the first {n_cols} of "
-                      f"{N_VOCAB} vocabulary rows (K={K_HID}), {steps} pass(es), "
-                      f"{dt:.1f} s wall"}
+            "sample": parts[f"decode_cores{all_cores}"]["sample"] + " (decode product, all cores)",
+            "parts": parts}
 
 
 def run_reference(args, world, rank):

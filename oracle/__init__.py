@@ -93,6 +93,7 @@ def _load():
         lib.oracle_fp8_logits_cols.argtypes = [p, p, i64, i64, p, p, p, i64, p]
         lib.oracle_e2m1_round_array.argtypes = [p, i64, p]
         lib.oracle_num_threads.restype = ctypes.c_int
+        lib.oracle_set_num_threads.argtypes = [ctypes.c_int]
         _lib = lib
     return _lib
 
@@ -305,3 +306,8 @@ def topk(L: np.ndarray, k: int) -> tuple[np.ndarray, np.ndarray]:
 
 def num_threads() -> int:
     return int(_load().oracle_num_threads())
+
+
+def set_num_threads(n: int) -> None:
+    """Threads the oracle's loops use from now on (n <= 0: one per processor)."""
+    _load().oracle_set_num_threads(int(n))

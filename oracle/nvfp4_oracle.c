@@ -460,3 +460,13 @@ int oracle_num_threads(void) {
   return 1;
 #endif
 }
+
+/* Threads of the parallel loops above (n <= 0: one per processor).  Only
+ * the CPU baseline uses this, to time the oracle on one core and on all. */
+void oracle_set_num_threads(int n) {
+#ifdef _OPENMP
+  omp_set_num_threads(n > 0 ? n : omp_get_num_procs());
+#else
+  (void)n;
+#endif
+}
