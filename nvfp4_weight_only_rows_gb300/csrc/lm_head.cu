@@ -459,6 +459,12 @@ __global__ void __launch_bounds__((gemm_threads<kOut, kStages, kPStages, kDqPerQ
     const int sw = row & 7;
     // this warp's stages are g = r, r + kDqPerQuad, ... of the CTA's sequence
     const uint32_t total = cta_stages(sc, n_kb_u);
+    // NaN block scales (E4M3 S.1111.111: the "never loaded" sentinel of
+    // `KNvfp4Static.process` on the page
+    // "vllm/model_executor/layers/quantization/modelopt.py"): per byte,
+    // (b & 0x7F) + 1 carries into bit 7 only for 0x7F / 0xFF, and never into
+    // the next byte; the OR over the CTA's stages is tested once at the end
+    uint32_t nan_seen = 0;
     bool ok = true;
     for (uint32_t g = (uint32_t)r; ok && g < total; g += kDqPerQuad) {
       const uint32_t ps = g % kPStages, pph = (g / kPStages) & 1;
@@ -468,6 +474,8 @@ __global__ void __launch_bounds__((gemm_threads<kOut, kStages, kPStages, kDqPerQ
       const uint4 sc = *reinterpret_cast<const uint4*>(s_scales + ps * kScaleStageBytes +
                                                        row * (kKS / 16));
       const uint32_t scw[4] = {sc.x, sc.y, sc.z, sc.w};
+      nan_seen |= ((sc.x & 0x7F7F7F7Fu) + 0x01010101u) | ((sc.y & 0x7F7F7F7Fu) + 0x01010101u) |
+                  ((sc.z & 0x7F7F7F7Fu) + 0x01010101u) | ((sc.w & 0x7F7F7F7Fu) + 0x01010101u);
       const uint32_t ta = tmem_a + lane_off + st * (kKB / 2);
 #pragma unroll
       for (int c4 = 0; c4 < kKB / 64; ++c4) {
@@ -498,6 +506,8 @@ __global__ void __launch_bounds__((gemm_threads<kOut, kStages, kPStages, kDqPerQ
       __syncwarp();
       if (lane == 0) mbar_arrive(&s_full[st]);
     }
+    if (__any_sync(0xFFFFFFFFu, (nan_seen & 0x80808080u) != 0u) && lane == 0)
+      raise_status(p.status, NVFP4_ERR_NONFINITE);
   } else if (warp < kFirstEpiWarp + 4) {
     // ---------------- epilogue: one thread per vocabulary row, BN tokens
     epilogue_role<kOut, false, kGrouped>(p, sc, warp, warp - kFirstEpiWarp, lane, tmem_base,

@@ -112,6 +112,33 @@ def test_errors_are_status_codes():
     assert e.value.status == nv.Status.ERR_SHAPE
 
 
+def test_nan_block_scale_sets_device_status():
+    """A NaN block scale (E4M3 0x7F / 0xFF, the unloaded-scale sentinel of
+    `KNvfp4Static.process`) raises NVFP4_ERR_NONFINITE in the status word;
+    the next call on clean scales resets it to OK."""
+    N, K, M = 700, 1024, 4
+    W = synth.quant_weight(N=N, K=K, seed=3)
+    (p, s, g), (pd, sd, gd) = upload_quantized(W)
+    x = to_bf16_dev(synth.decode_x(M, K=K))
+    ws = torch.empty(nv.w4a16_lm_head_workspace_bytes(M, N, K), dtype=torch.uint8, device="cuda")
+    for row, col, byte in ((0, 0, 0x7F), (N - 1, K // 16 - 1, 0xFF), (345, 17, 0x7F)):
+        bad = s.copy()
+        bad[row, col] = byte
+        sb = torch.from_numpy(bad).cuda().view(torch.float8_e4m3fn)
+        out = nv.w4a16_lm_head(x, pd, sb, gd, workspace=ws)
+        assert nv.nvfp4_read_device_status(ws) == nv.Status.ERR_NONFINITE, (row, col)
+        assert torch.isnan(out[:, row]).all()
+        nv.w4a16_lm_head(x, pd, sd, gd, workspace=ws)
+        assert nv.nvfp4_read_device_status(ws) == nv.Status.OK
+    # the largest finite scales (0x7E = 448, 0xFE = -448) are not NaN
+    big = s.copy()
+    big[5, ::2] = 0x7E
+    big[5, 1::2] = 0xFE
+    nv.w4a16_lm_head(x, pd, torch.from_numpy(big).cuda().view(torch.float8_e4m3fn), gd,
+                     workspace=ws)
+    assert nv.nvfp4_read_device_status(ws) == nv.Status.OK
+
+
 @pytest.mark.parametrize("M,N,K", [(8, 216 * 128, 1024), (1, 153 * 128 + 5, 512),
                                    (40, 300 * 128, 768)])
 def test_split_units_deterministic(M, N, K):
