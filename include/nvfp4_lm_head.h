@@ -69,7 +69,8 @@ typedef enum {
   NVFP4_ERR_WORKSPACE = 4,  /* workspace missing or smaller than required */
   NVFP4_ERR_DTYPE = 5,      /* unknown output dtype code */
   NVFP4_ERR_CUDA = 6,       /* a CUDA runtime/driver call failed */
-  NVFP4_ERR_NONFINITE = 7,  /* device status: W held an Inf or NaN */
+  NVFP4_ERR_NONFINITE = 7,  /* device status: W held an Inf or NaN (quantizer), or a block
+                               scale read by a W4A16 product is NaN (an unloaded scale) */
   NVFP4_ERR_TIMEOUT = 8,    /* device status: a pipeline wait ran out of time */
   NVFP4_ERR_UNSUPPORTED = 9, /* no sm_103a device / kernel image for it */
   NVFP4_ERR_SCRATCH_LIMIT = 10 /* w4a16_lm_head_noalloc: M*K needs more than its fixed scratch */
@@ -196,6 +197,12 @@ size_t w4a16_lm_head_workspace_bytes(int64_t M, int64_t N, int64_t K);
  *                NVFP4_OUT_F32) or bf16 (NVFP4_OUT_BF16, round to nearest even).
  *   workspace    device, >= w4a16_lm_head_workspace_bytes(M, N, K),
  *                256-byte aligned.
+ *
+ * A NaN block-scale byte (0x7F / 0xFF: the "never loaded" sentinel that
+ * `KNvfp4Static.process` on the page
+ * "vllm/model_executor/layers/quantization/modelopt.py" rejects) raises
+ * NVFP4_ERR_NONFINITE in the workspace status word (read it with
+ * nvfp4_read_device_status); the logits of the rows concerned are NaN.
  *
  * Accumulation is fp32 on the tensor cores; each product x * w is exact.
  * The activations are carried into the tensor cores as fp16 after an exact
@@ -514,18 +521,34 @@ nvfp4_status w4a4_lm_head_topk(const void *x, int64_t M, int64_t K, const uint8_
  * make that first call before any stream capture.  Shapes whose rescaled
  * activations and split-K partials do not fit (M_pad * K * 2 bytes plus up to
  * SMs * 128 * M_pad * 4 bytes, M_pad = M rounded up to 16, or to 128 above
- * 128 tokens) return NVFP4_ERR_SCRATCH_LIMIT before anything is enqueued;
+ * 128 tokens; for K % 256 != 0 also the staged weight rows, N * K/16 bytes
+ * and more) return NVFP4_ERR_SCRATCH_LIMIT before anything is enqueued;
  * for example M <= 64 at K <= 8192 fits.  Nothing is
  * allocated: no cudaMalloc, no cudaFree, no allocating library routine.
  *
+ * The array's address is looked up once per CUDA context (the primary
+ * context of each device, or one the caller made current) and cached; the
+ * first call in a context does the lookup, later ones read the cache
+ * without a lock.
+ *
  * Every call shares the array.  Each call rewrites what it reads and clears
  * the status word first, but calls that overlap on the GPU (unordered
- * streams) race on the array.  The device status word of this call lives in
- * the array and is not exposed.
+ * streams) race on the array.  Device-side conditions (a NaN block scale, a
+ * pipeline wait that timed out) go to the status word at the start of the
+ * array, which w4a16_lm_head_noalloc_status reads.
  */
 nvfp4_status w4a16_lm_head_noalloc(const void *x, int64_t M, int64_t K, const uint8_t *packed,
                                    const uint8_t *scales, const float *global_scale, int64_t N,
                                    void *logits, int out_dtype, void *stream);
+
+/*
+ * The device status word the last w4a16_lm_head_noalloc call on `stream` in
+ * the current context left in the fixed scratch (what
+ * nvfp4_read_device_status reads from a workspace).  Like that call it
+ * synchronizes `stream`; the pages have no counterpart.
+ *   status_out  host, receives an nvfp4_status value.
+ */
+nvfp4_status w4a16_lm_head_noalloc_status(int32_t *status_out, void *stream);
 
 #ifdef __cplusplus
 }

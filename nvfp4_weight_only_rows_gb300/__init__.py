@@ -48,6 +48,7 @@ __all__ = [
     "NVFP4Error", "Status", "library_path", "load_library", "nvfp4_quantize_rows",
     "nvfp4_refresh", "w4a16_lm_head", "nvfp4_quantize_workspace_bytes",
     "w4a16_lm_head_workspace_bytes", "nvfp4_read_device_status", "w4a16_lm_head_noalloc",
+    "w4a16_lm_head_noalloc_status",
     "nvfp4_selftest_bounded_wait", "nvfp4_selftest_topk_bins", "OUT_F32", "OUT_BF16", "w4a16_lm_head_argmax",
     "w4a16_lm_head_argmax_workspace_bytes", "fp8_quantize_rows", "fp8_refresh",
     "fp8_quantize_workspace_bytes", "w8a8_lm_head", "w8a8_lm_head_argmax",
@@ -169,6 +170,8 @@ def load_library() -> ctypes.CDLL:
     lib.w4a16_grouped_gemm.restype = st
     lib.w4a16_lm_head_noalloc.argtypes = [vp, i64, i64, vp, vp, vp, i64, vp, ctypes.c_int, vp]
     lib.w4a16_lm_head_noalloc.restype = st
+    lib.w4a16_lm_head_noalloc_status.argtypes = [ctypes.POINTER(ctypes.c_int32), vp]
+    lib.w4a16_lm_head_noalloc_status.restype = st
     lib.nvfp4_selftest_bounded_wait.argtypes = [vp, sz, i64, vp]
     lib.nvfp4_selftest_bounded_wait.restype = st
     lib.nvfp4_selftest_topk_bins.argtypes = []
@@ -660,6 +663,15 @@ def w4a16_lm_head_noalloc(x: torch.Tensor, packed: torch.Tensor, scales: torch.T
                                    N, _ptr(out), code, _stream(stream))
     _check(rc, "w4a16_lm_head_noalloc")
     return out
+
+
+def w4a16_lm_head_noalloc_status(stream=None) -> Status:
+    """The device status word the last w4a16_lm_head_noalloc call left in the
+    fixed scratch of the current context (synchronizes `stream`)."""
+    v = ctypes.c_int32(0)
+    _check(load_library().w4a16_lm_head_noalloc_status(ctypes.byref(v), _stream(stream)),
+           "w4a16_lm_head_noalloc_status")
+    return Status(v.value)
 
 
 def nvfp4_selftest_topk_bins() -> int:
