@@ -364,7 +364,7 @@ __global__ void __launch_bounds__((gemm_threads<kOut, kStages, kPStages, kDqPerQ
     for_each_piece(sc, n_kb_u, [&](const Piece& pc) {
       const UnitGeom geo = unit_geom<kGrouped>(p, sc, pc.u);
       const int32_t n0 = (int32_t)geo.w_row;
-      const uint64_t pol = geo.reused ? pol_reused : pol_once;
+      const uint64_t pol = geo.reused ? pol_reused : pol_once;  // packed codes
       for (uint32_t kb = pc.kb0; kb < pc.kb1; ++kb, ++issued) {
         const uint32_t st = issued % kPStages, ph = (issued / kPStages) & 1;
         if (!warp_wait(&p_empty[st], ph ^ 1, wc)) return false;
@@ -372,8 +372,15 @@ __global__ void __launch_bounds__((gemm_threads<kOut, kStages, kPStages, kDqPerQ
           mbar_arrive_expect_tx(&p_full[st], kPackedStageBytes + kScaleStageBytes);
           tma_load_2d_hint(s_packed + st * kPackedStageBytes, &tm_packed, kb * (kKS / 2), n0,
                            &p_full[st], pol);
-          tma_load_2d_hint(s_scales + st * kScaleStageBytes, &tm_scales, kb * (kKS / 16), n0,
-                           &p_full[st], pol);
+          // a stage takes 16 bytes of each 32-byte scale sector, the next
+          // stage the other 16: scales read once keep the default policy
+          // (evict-first would drop the sector before its second half is read)
+          if (geo.reused)
+            tma_load_2d_hint(s_scales + st * kScaleStageBytes, &tm_scales, kb * (kKS / 16), n0,
+                             &p_full[st], pol_reused);
+          else
+            tma_load_2d(s_scales + st * kScaleStageBytes, &tm_scales, kb * (kKS / 16), n0,
+                        &p_full[st]);
         }
         __syncwarp();
       }
