@@ -835,6 +835,38 @@ static inline WeightStage weight_stage(int64_t rows, int64_t K, size_t off, bool
 cudaError_t stage_rows_launch(const uint8_t* src, int64_t rows, int64_t row_bytes, uint8_t* dst,
                               int64_t dst_stride, cudaStream_t stream);
 
+// Up to this many tokens a top-k call writes the fp32 logits (at most
+// 32 x N x 4 bytes, a twentieth of the weight bytes) and selects from them
+// (topk.cu, topk_logits_launch); beyond, the GEMM keeps thresholded
+// candidates in its epilogue and topk_select_launch picks from those.  (At
+// 64 tokens the selection's 2048 chunk CTAs cost as much as the epilogue
+// route, measured; at 1 to 32 tokens the logits route is 4 to 8 us faster.)
+constexpr int64_t kTopkLogitsMaxM = 32;
+constexpr int kLogitChunk = 4096;  // logits of one token per selecting CTA
+
+// Workspace of the logits route after a call's own layout ending at `base`:
+// [fp32 logits, M x N][per token and chunk of kLogitChunk rows, k candidate
+// keys].  The per-token chunk counters are word 0 of the argmax lines.
+struct TopkLogitsLayout {
+  size_t logits, cand, total;
+};
+static inline TopkLogitsLayout topk_logits_layout(size_t base, int64_t M, int64_t N, int k) {
+  TopkLogitsLayout t;
+  t.logits = align_up(base, 256);
+  t.cand = align_up(t.logits + (size_t)M * N * 4, 256);
+  t.total = t.cand + (size_t)M * ((N + kLogitChunk - 1) / kLogitChunk) * k * 8;
+  return t;
+}
+
+cudaError_t topk_logits_launch(const float* logits, int64_t M, int64_t N, int k,
+                               unsigned long long* cand, unsigned long long* lines, int64_t* ids,
+                               float* vals, cudaStream_t stream);
+// The selecting CTA holds a chunk's keys or the merge's (chunks x k) in
+// shared memory, at most this many bytes: the logits route takes the call
+// only where they fit (every vocabulary up to 1.4 M rows at k = 128).
+constexpr size_t kTopkLogitsMaxSmem = 176 * 1024;
+bool topk_logits_fits(int64_t N, int k);
+
 // The top-k selection kernel (topk.cu), launched after a top-k GEMM.
 cudaError_t topk_select_launch(const unsigned long long* lines, const uint2* grp,
                                const uint32_t* cand, int64_t M, int64_t N, int k, int64_t* ids,

@@ -594,7 +594,12 @@ static bool encode_weight_maps(CUtensorMap* tm_packed, CUtensorMap* tm_scales,
 }
 
 size_t lm_head_topk_workspace_bytes(int64_t M, int64_t N, int64_t K, int k) {
-  const WsLayout L = ws_layout(M, N, K, std::max(sm_count(), 1), false, ActFormat::kF16, k);
+  const int sms = std::max(sm_count(), 1);
+  if (M <= kTopkLogitsMaxM && topk_logits_fits(N, k)) {  // fp32 logits, then the selection
+    const WsLayout L = ws_layout(M, N, K, sms, true, ActFormat::kF16);
+    return weight_stage(N, K, topk_logits_layout(L.total, M, N, k).total, true).total;
+  }
+  const WsLayout L = ws_layout(M, N, K, sms, false, ActFormat::kF16, k);
   return weight_stage(N, K, L.total, true).total;
 }
 
@@ -609,11 +614,17 @@ static nvfp4_status lm_head_run(const void* x, int64_t M, int64_t K, const uint8
   const int sms = sm_count();
   if (sms <= 0) return NVFP4_ERR_CUDA;
   const bool argmax = out_mode == kOutArgmax;
-  const bool topk = out_mode == kOutTopk;
-  const bool keys = argmax || topk;
+  // top-k of a few tokens: the fp32 logits are written and selected from;
+  // of many tokens: thresholded candidates in the epilogue
+  const bool topk_logits =
+      out_mode == kOutTopk && M <= kTopkLogitsMaxM && topk_logits_fits(N, topk_k);
+  const bool topk = out_mode == kOutTopk && !topk_logits;
+  const bool keys = argmax || topk || topk_logits;  // per-token lines the prep kernel clears
   const int BN = lm_head_token_tile(M);
   const int n_ttiles = (int)((M + BN - 1) / BN);
-  const WsLayout L = ws_layout(M, N, K, sms, argmax, ActFormat::kF16, topk ? topk_k : 0);
+  const WsLayout L = ws_layout(M, N, K, sms, argmax || topk_logits, ActFormat::kF16,
+                               topk ? topk_k : 0);
+  const TopkLogitsLayout TL = topk_logits_layout(L.total, M, N, topk_k);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   int32_t* status = reinterpret_cast<int32_t*>(ws);
   __half* x16 = reinterpret_cast<__half*>(ws + L.x16);
@@ -621,7 +632,11 @@ static nvfp4_status lm_head_run(const void* x, int64_t M, int64_t K, const uint8
   uint32_t* split_cnt = reinterpret_cast<uint32_t*>(ws + L.cnt);
   uint32_t* split_ready = reinterpret_cast<uint32_t*>(ws + L.ready);
   float* split_part = reinterpret_cast<float*>(ws + L.part);
-  const WeightStage wst = weight_stage(N, K, L.total, true);
+  const WeightStage wst = weight_stage(N, K, topk_logits ? TL.total : L.total, true);
+  if (topk_logits) {
+    out_mode = NVFP4_OUT_F32;
+    logits = ws + TL.logits;
+  }
 
   CUtensorMap tm_packed, tm_scales, tm_x;
   if (!encode_weight_maps(&tm_packed, &tm_scales, wst, packed, scales, N, K, ws) ||
@@ -706,6 +721,11 @@ static nvfp4_status lm_head_run(const void* x, int64_t M, int64_t K, const uint8
   else
     err = deep ? launch_gemm<NVFP4_OUT_F32, 3, 6, 3>(tm_packed, tm_scales, tm_x, a, grid, stream)
                : launch_gemm<NVFP4_OUT_F32, 2, 4, 2>(tm_packed, tm_scales, tm_x, a, grid, stream);
+  if (err == cudaSuccess && topk_logits)
+    err = topk_logits_launch(reinterpret_cast<const float*>(ws + TL.logits), M, N, topk_k,
+                             reinterpret_cast<unsigned long long*>(ws + TL.cand),
+                             reinterpret_cast<unsigned long long*>(ws + L.keys), token_ids,
+                             max_logits, stream);
   if (err != cudaSuccess || cudaGetLastError() != cudaSuccess) return NVFP4_ERR_CUDA;
   return NVFP4_OK;
 }

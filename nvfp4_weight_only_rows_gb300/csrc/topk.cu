@@ -264,4 +264,219 @@ cudaError_t topk_select_launch(const unsigned long long* lines, const uint2* grp
   return cudaLaunchKernelEx(&l.cfg, topk_select_kernel, lines, grp, cand, N, k, ids, vals);
 }
 
+// ------------------------------------------------------------ from logits
+// Top-k of decode-sized products: the GEMM writes fp32 logits (M x N, a few
+// tens of MB next to hundreds of MB of weights), then one kernel selects.
+// CTA (c, m) takes token m's logits [c * kLogitChunk, (c + 1) * kLogitChunk):
+// it forms the 64-bit candidate keys (order key of the logit, -0 as +0,
+// << 32 | ~row), finds its min(k, rows) largest by a radix select and writes
+// them in order to the token's candidate list; the last of the token's CTAs
+// to finish (a counter in the token's line, cleared by the prep kernel)
+// loads every chunk's candidates into shared memory and selects the k
+// largest the same way.  The keys are distinct, so the answer is that of a
+// sort of the fp32 logits, bit for bit.
+constexpr int kLogitThreads = 256;
+constexpr int kLogitPer = kLogitChunk / kLogitThreads;  // 16 logits per thread
+constexpr int kRankCap = 256;     // keys ranked in shared memory at the end of a select
+constexpr int kDigitBits = 11;    // radix digit: 2048 bins (a quarter octave at the top)
+constexpr int kBins = 1 << kDigitBits;
+constexpr int kBinsPerThread = kBins / kLogitThreads;  // 8
+
+__device__ __forceinline__ unsigned long long logit_key(float v, uint32_t n) {
+  uint32_t b = __float_as_uint(v);
+  if ((b & 0x7FFFFFFFu) == 0u) b = 0u;  // -0 counts as +0
+  return ((unsigned long long)(b ^ ((uint32_t)((int32_t)b >> 31) | 0x80000000u)) << 32) |
+         (uint32_t)~n;
+}
+
+// The `want` largest of the `count` distinct keys in shared memory (whole
+// block of kLogitThreads, want <= count, want <= kTopkMax): an 11-bit digit
+// at a time from the top, the histogram of the next digit over the keys
+// inside the range chosen so far picks the digit of the want-th largest,
+// until the keys at or above that prefix (zeros below it) are few enough to
+// rank; each of those is then ranked against the others (the keys are
+// distinct) and out[r] receives the key of rank r < want.  (Measured
+// against warp-aggregated histogram adds, an atomic-free gather and a
+// count-based threshold search: none was faster.)
+__device__ void select_largest(const unsigned long long* keys, int count, int want,
+                               unsigned long long* out, unsigned long long* s_rank,
+                               uint32_t* hist) {
+  __shared__ unsigned long long s_prefix;
+  __shared__ uint32_t s_need, s_above, s_bin, s_n;
+  __shared__ uint32_t s_warp[kLogitThreads / 32];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  unsigned long long prefix = 0ull, mask = 0ull;
+  // need: keys still to find inside the range; above: keys above the range
+  uint32_t need = (uint32_t)want, above = 0;
+  if (count > kRankCap) {
+#pragma unroll 1
+    for (int top = 64; top > 0; top -= kDigitBits) {
+      const int width = top < kDigitBits ? top : kDigitBits;
+      const int shift = top - width;
+      for (int i = tid; i < kBins; i += blockDim.x) hist[i] = 0;
+      __syncthreads();
+      for (int i = tid; i < count; i += blockDim.x) {
+        const unsigned long long kk = keys[i];
+        if ((kk & mask) == prefix)
+          atomicAdd(&hist[(uint32_t)(kk >> shift) & ((1u << width) - 1u)], 1u);
+      }
+      __syncthreads();
+      // thread t holds the 8 bins below kBins - 8t (from the top); a block
+      // scan from the top counts the range's keys in higher bins
+      uint32_t c[kBinsPerThread], sum = 0;
+#pragma unroll
+      for (int j = 0; j < kBinsPerThread; ++j) {
+        c[j] = hist[kBins - 1 - kBinsPerThread * tid - j];
+        sum += c[j];
+      }
+      uint32_t incl = sum;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      if (lane == 31) s_warp[warp] = incl;
+      __syncthreads();
+      for (int w = 0; w < warp; ++w) incl += s_warp[w];
+      const uint32_t excl = incl - sum;
+      if (excl < need && need <= incl) {
+        uint32_t acc = excl;
+#pragma unroll 1
+        for (int j = 0; j < kBinsPerThread; ++j) {
+          if (acc + c[j] >= need) {
+            const uint32_t bin = kBins - 1 - kBinsPerThread * tid - j;
+            s_prefix = prefix | ((unsigned long long)bin << shift);
+            s_need = need - acc;
+            s_above = above + acc;
+            s_bin = c[j];
+            break;
+          }
+          acc += c[j];
+        }
+      }
+      __syncthreads();
+      prefix = s_prefix;
+      need = s_need;
+      above = s_above;
+      mask |= ((1ull << width) - 1ull) << shift;
+      // the keys at or above the new prefix: those above its range and its bin
+      if (above + s_bin <= (uint32_t)kRankCap) break;
+    }
+  }
+  // the keys at or above `prefix` (all of them when count <= kRankCap)
+  if (tid == 0) s_n = 0;
+  __syncthreads();
+  for (int i = tid; i < count; i += blockDim.x) {
+    const unsigned long long kk = keys[i];
+    if (kk >= prefix) {
+      const uint32_t pos = atomicAdd(&s_n, 1u);
+      if (pos < (uint32_t)kRankCap) s_rank[pos] = kk;
+    }
+  }
+  __syncthreads();
+  const int m = (int)min(s_n, (uint32_t)kRankCap);
+  for (int i = tid; i < m; i += blockDim.x) {
+    const unsigned long long kk = s_rank[i];
+    int rank = 0;
+#pragma unroll 8
+    for (int j = 0; j < m; ++j) rank += s_rank[j] > kk ? 1 : 0;
+    if (rank < want) out[rank] = kk;
+  }
+  __syncthreads();
+}
+
+// Keys held in shared memory: max(kLogitChunk, chunks x k) (the merge's).
+__global__ void __launch_bounds__(kLogitThreads) topk_logits_kernel(
+    const float* __restrict__ logits, int64_t N, int k, unsigned long long* __restrict__ cand,
+    unsigned long long* __restrict__ lines, int64_t* __restrict__ ids, float* __restrict__ vals) {
+  // the logits come from the GEMM, which may still be running
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  extern __shared__ unsigned long long s_keys[];
+  __shared__ unsigned long long s_rank[kRankCap];
+  __shared__ unsigned long long s_out[kTopkMax];
+  __shared__ uint32_t hist[kBins];
+  __shared__ int s_last;
+  const int64_t m = blockIdx.y;
+  const int n_chunks = gridDim.x;
+  const int64_t n0 = (int64_t)blockIdx.x * kLogitChunk;
+  const int rows = (int)min((int64_t)kLogitChunk, N - n0);
+  const float* src = logits + m * N + n0;
+  // all of this thread's loads in flight together
+  float v[kLogitPer];
+#pragma unroll
+  for (int j = 0; j < kLogitPer; ++j) {
+    const int i = threadIdx.x + j * kLogitThreads;
+    v[j] = i < rows ? __ldcg(src + i) : 0.0f;
+  }
+#pragma unroll
+  for (int j = 0; j < kLogitPer; ++j) {
+    const int i = threadIdx.x + j * kLogitThreads;
+    if (i < rows) s_keys[i] = logit_key(v[j], (uint32_t)(n0 + i));
+  }
+  __syncthreads();
+  const int kc = min(k, rows);
+  select_largest(s_keys, rows, kc, s_out, s_rank, hist);
+  unsigned long long* my = cand + (m * n_chunks + blockIdx.x) * (int64_t)k;
+  for (int j = threadIdx.x; j < k; j += blockDim.x) my[j] = j < kc ? s_out[j] : 0ull;
+  // the last CTA of the token merges (release: the list above is visible
+  // before the count; acquire: the others' lists are read after it)
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    uint32_t old;
+    asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], 1;"
+                 : "=r"(old) : "l"(reinterpret_cast<uint32_t*>(lines + m * kKeyStride)) : "memory");
+    s_last = old == (uint32_t)n_chunks - 1u;
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  // every chunk wrote k slots, the unused ones zero (below every key): the
+  // zeros are never among the k largest because the token has N >= k keys
+  const int total = n_chunks * k;
+  const unsigned long long* all = cand + m * (int64_t)total;
+  for (int i0 = 0; i0 < total; i0 += 8 * kLogitThreads) {  // eight loads in flight per thread
+    unsigned long long c8[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int i = i0 + threadIdx.x + j * kLogitThreads;
+      c8[j] = i < total ? __ldcg(all + i) : 0ull;
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int i = i0 + threadIdx.x + j * kLogitThreads;
+      if (i < total) s_keys[i] = c8[j];
+    }
+  }
+  __syncthreads();
+  select_largest(s_keys, total, k, s_out, s_rank, hist);
+  for (int j = threadIdx.x; j < k; j += blockDim.x) {
+    const unsigned long long kk = s_out[j];
+    ids[m * k + j] = (int64_t)(uint32_t)~(uint32_t)kk;
+    if (vals) vals[m * k + j] = key_value((uint32_t)(kk >> 32));
+  }
+}
+
+// Shared memory of the kernel for N rows and k: the chunk's keys and the
+// merge's (chunks x k), whichever is more.
+static size_t topk_logits_smem(int64_t N, int k) {
+  const int64_t chunks = (N + kLogitChunk - 1) / kLogitChunk;
+  return (size_t)std::max<int64_t>(kLogitChunk, chunks * k) * sizeof(unsigned long long);
+}
+
+bool topk_logits_fits(int64_t N, int k) { return topk_logits_smem(N, k) <= kTopkLogitsMaxSmem; }
+
+cudaError_t topk_logits_launch(const float* logits, int64_t M, int64_t N, int k,
+                               unsigned long long* cand, unsigned long long* lines, int64_t* ids,
+                               float* vals, cudaStream_t stream) {
+  static std::atomic<uint64_t> limit_set{0};
+  const cudaError_t attr_err = smem_limit_once(
+      limit_set, reinterpret_cast<const void*>(topk_logits_kernel), kTopkLogitsMaxSmem);
+  if (attr_err != cudaSuccess) return attr_err;
+  PdlLaunch l(dim3((unsigned)((N + kLogitChunk - 1) / kLogitChunk), (unsigned)M),
+              dim3(kLogitThreads), topk_logits_smem(N, k), stream);
+  return cudaLaunchKernelEx(&l.cfg, topk_logits_kernel, logits, N, k, cand, lines, ids, vals);
+}
+
 }  // namespace nvfp4

@@ -62,7 +62,8 @@ def test_tiny_workload():
 @pytest.mark.parametrize("M,N,K,k", [(1, 300, 512, 10), (5, 129, 256, 128), (17, 1000, 512, 50),
                                      (64, 777, 1024, 33), (100, 513, 256, 64),
                                      (130, 260, 512, 7), (200, 384, 1280, 100), (1, 1, 256, 1),
-                                     (3, 7, 256, 7), (300, 5000, 256, 50)])
+                                     (3, 7, 256, 7), (300, 5000, 256, 50),
+                                     (2, 262144, 256, 128)])
 def test_ragged_shapes(M, N, K, k):
     """Ragged token and vocabulary tails, k up to N and up to the limit."""
     W = synth.quant_weight(N=N, K=K, seed=M + N)
@@ -101,11 +102,18 @@ def test_first_column_is_the_argmax():
     assert torch.equal(vals[:, 0], a_vals)
 
 
-def test_all_rows_tied():
+# Up to 32 tokens the call writes the fp32 logits and selects from them; more
+# tokens keep thresholded candidates in the GEMM epilogue: the cases below
+# run both routes.
+ROUTES = [9, 70]
+
+
+@pytest.mark.parametrize("M", ROUTES)
+def test_all_rows_tied(M):
     """Every vocabulary row equal: every logit of a token is the same number,
     so every one reaches the threshold (more candidates than the selection
     keeps in shared memory) and rows 0 .. k-1 must come out, in order."""
-    N, K, M = 157 * 128 + 3, 256, 9
+    N, K = 157 * 128 + 3, 256
     row = synth.quant_weight(N=1, K=K, seed=5)
     host_q = oracle.quantize(np.repeat(row, N, axis=0))
     x = synth.decode_x(M, K=K)
@@ -115,11 +123,12 @@ def test_all_rows_tied():
         assert np.all(vals == vals[:, :1])
 
 
-def test_tied_rows_within_shared_memory():
+@pytest.mark.parametrize("M", ROUTES)
+def test_tied_rows_within_shared_memory(M):
     """3000 equal rows: every logit is a candidate at the final threshold,
     more than the one-warp ranking takes and few enough for the radix
     selection over shared memory; rows 0 .. k-1 must come out, in order."""
-    N, K, M = 3000, 256, 5
+    N, K = 3000, 256
     row = synth.quant_weight(N=1, K=K, seed=7)
     host_q = oracle.quantize(np.repeat(row, N, axis=0))
     x = synth.decode_x(M, K=K)
@@ -128,10 +137,11 @@ def test_tied_rows_within_shared_memory():
         assert np.all(ids == np.arange(k)[None, :])
 
 
-def test_rising_logits():
+@pytest.mark.parametrize("M", ROUTES)
+def test_rising_logits(M):
     """Logits that grow with the row: later tiles keep beating the
     thresholds that earlier ones set."""
-    N, K, M = 30000, 256, 4
+    N, K = 30000, 256
     x = synth.decode_x(M, K=K)
     xf = synth.bf16_bits_to_f32(x)
     ramp = np.linspace(0.01, 1.0, N, dtype=np.float32)[:, None]
@@ -141,10 +151,11 @@ def test_rising_logits():
     assert_oracle_agrees(ids[:1], vals[:1], oracle.logits(x[:1], *host_q))
 
 
-def test_negative_nan_and_zero_tokens():
+@pytest.mark.parametrize("M", [3, 70])
+def test_negative_nan_and_zero_tokens(M):
     """All-negative logits, a NaN token (every logit NaN: rows 0 .. k-1, all
     values NaN) and an all-zero token (rows 0 .. k-1, values +0)."""
-    N, K, M, k = 1000, 512, 3, 20
+    N, K, k = 1000, 512, 20
     x = synth.decode_x(M, K=K)
     xf = synth.bf16_bits_to_f32(x).copy()
     rng = np.random.default_rng(3)
