@@ -187,10 +187,13 @@ def test_topk_host_argument_errors_and_sizes(lib):
              None) == 2                                                                   # ALIGN ids
     sz = lib.w4a16_lm_head_topk_workspace_bytes
     assert sz(4, 0, 256, 1) == 0 and sz(4, 100, 256, 0) == 0 and sz(4, 100, 256, 129) == 0
-    for M in (1, 64, 2048):
+    for M in (1, 32, 64, 2048):
         am = lib.w4a16_lm_head_argmax_workspace_bytes(M, 128256, 4096)
         tk = sz(M, 128256, 4096, 50)
-        assert tk >= am + M * 128256 * 4 + M * (128256 // 32) * 8 + M * 4112
+        if M <= 32:  # fp32 logits, then per 4096-row chunk k candidate keys
+            assert tk >= am + M * 128256 * 4 + M * ((128256 + 4095) // 4096) * 50 * 8
+        else:        # candidate slots, group words and histograms of the epilogue route
+            assert tk >= am + M * 128256 * 4 + M * (128256 // 32) * 8 + M * 4112
 
 
 def test_w8a8_w4a4_topk_host_errors_and_sizes(lib):
