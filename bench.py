@@ -920,8 +920,8 @@ def run_profile_case(case: str):
         return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(
             torch.bfloat16).to(dev)
 
-    if case.startswith("moe_w13"):
-        Nm, Km = 2 * MOE_I, MOE_H
+    if case.startswith("moe_"):
+        Nm, Km = (2 * MOE_I, MOE_H) if case.startswith("moe_w13") else (MOE_H, MOE_I)
         qws = torch.empty(nv.nvfp4_quantize_workspace_bytes(Nm, Km), dtype=torch.uint8, device=dev)
         pk = torch.empty(MOE_E, Nm, Km // 2, dtype=torch.uint8, device=dev)
         sc = torch.empty(MOE_E, Nm, Km // 16, dtype=torch.float8_e4m3fn, device=dev)
@@ -929,8 +929,8 @@ def run_profile_case(case: str):
         for e in range(MOE_E):
             We = up(synth.quant_weight(N=Nm, K=Km, seed=1000 + e))
             nv.nvfp4_quantize_rows(We, pk[e], sc[e], gs[e:e + 1], workspace=qws)
-        offs = moe_offsets(64 if case == "moe_w13_decode" else 2048,
-                           seed=64 if case == "moe_w13_decode" else 2048)
+        tokens = 64 if case.endswith("_decode") else 2048
+        offs = moe_offsets(tokens, seed=tokens)
         x = up(synth.decode_x(int(offs[-1]), K=Km))
         od = torch.from_numpy(offs).to(dev)
         ws = torch.empty(nv.w4a16_grouped_workspace_bytes(int(offs[-1]), Nm, Km, MOE_E),
@@ -1024,7 +1024,8 @@ def main():
                                           "argmax64", "argmax_prefill", "fp8_quant",
                                           "fp8_decode1", "fp8_decode64", "fp8_prefill",
                                           "w4a4_decode1", "w4a4_decode64", "w4a4_prefill",
-                                          "moe_w13_decode", "moe_w13_prefill", "topk1",
+                                          "moe_w13_decode", "moe_w13_prefill", "moe_w2_decode",
+                                          "moe_w2_prefill", "topk1",
                                           "topk64", "topk_prefill"],
                     help="run one small fixed case for ncu instead of the benchmark")
     args = ap.parse_args()

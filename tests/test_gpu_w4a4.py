@@ -88,8 +88,12 @@ def test_tiny_workload():
 @pytest.mark.parametrize("M,N,K", [(1, 300, 512), (5, 129, 256), (16, 128, 768),
                                    (17, 1000, 512), (64, 777, 1024), (100, 513, 256),
                                    (130, 260, 512), (200, 384, 1280), (1, 1, 256),
-                                   (8, 216 * 128, 1024), (40, 300 * 128, 768)])
+                                   (8, 216 * 128, 1024), (40, 300 * 128, 768),
+                                   (256, 1000, 768), (250, 1000, 272), (1024, 10240, 512)])
 def test_product_shapes(M, N, K):
+    """Logits of every shape class: token tiles of 16 to 128, ragged token and
+    weight tiles, K % 32 != 0 (staged codes), and more 128 x 128 units than
+    CTAs (every CTA walks several units)."""
     W = synth.quant_weight(N=N, K=K, seed=M + N)
     x = synth.decode_x(M, K=K)
     host_q = oracle.quantize(W)
