@@ -622,6 +622,7 @@ static nvfp4_status lm_head_run(const void* x, int64_t M, int64_t K, const uint8
   const bool keys = argmax || topk || topk_logits;  // per-token lines the prep kernel clears
   const int BN = lm_head_token_tile(M);
   const int n_ttiles = (int)((M + BN - 1) / BN);
+  const int64_t m_pad = (int64_t)n_ttiles * BN;
   const WsLayout L = ws_layout(M, N, K, sms, argmax || topk_logits, ActFormat::kF16,
                                topk ? topk_k : 0);
   const TopkLogitsLayout TL = topk_logits_layout(L.total, M, N, topk_k);
@@ -640,7 +641,7 @@ static nvfp4_status lm_head_run(const void* x, int64_t M, int64_t K, const uint8
 
   CUtensorMap tm_packed, tm_scales, tm_x;
   if (!encode_weight_maps(&tm_packed, &tm_scales, wst, packed, scales, N, K, ws) ||
-      !encode_2d(&tm_x, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, x16, (uint64_t)K, (uint64_t)M,
+      !encode_2d(&tm_x, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, x16, (uint64_t)K, (uint64_t)m_pad,
                  (uint64_t)K * 2, 64, (uint32_t)BN, CU_TENSOR_MAP_SWIZZLE_128B))
     return NVFP4_ERR_CUDA;
   if (stage_weights(wst, packed, scales, N, K, ws, stream) != cudaSuccess) return NVFP4_ERR_CUDA;
@@ -652,17 +653,20 @@ static nvfp4_status lm_head_run(const void* x, int64_t M, int64_t K, const uint8
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cudaLaunchConfig_t cfg = {};
-    // few rows: a CTA per row (latency); many rows: a warp per row
-    // the activation map has M rows: the TMA zero-fills the rows of the last
-    // token tile past M, so the prep kernel writes only the M real rows
+    // few rows: a CTA per row (latency); many rows: a warp per row.  The
+    // activation map covers whole token tiles and the prep kernel writes
+    // the padding rows of the last one as zeros: a box mostly past the
+    // map's last row (a single token in a 16-row tile) made every
+    // activation load of the GEMM markedly slower than a box of rows
+    // that exist (7 µs of a 59 µs call at M = 1)
     const bool wide = M <= kPrepWideRows;
-    cfg.gridDim = dim3((unsigned)(wide ? M : (M + 7) / 8));
+    cfg.gridDim = dim3((unsigned)(wide ? m_pad : (m_pad + 7) / 8));
     cfg.blockDim = dim3(wide ? 128 : 256);
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     if (cudaLaunchKernelEx(&cfg, wide ? w4a16_prep_x_kernel<4> : w4a16_prep_x_kernel<1>,
-                           static_cast<const uint16_t*>(x), M, K, M,
+                           static_cast<const uint16_t*>(x), M, K, m_pad,
                            global_scale, x16, tok_scale, status, split_cnt,
                            (int)((L.part - L.cnt) / 4),
                            keys ? reinterpret_cast<unsigned long long*>(ws + L.keys) : nullptr,

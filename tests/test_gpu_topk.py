@@ -151,6 +151,25 @@ def test_rising_logits(M):
     assert_oracle_agrees(ids[:1], vals[:1], oracle.logits(x[:1], *host_q))
 
 
+@pytest.mark.parametrize("M", ROUTES)
+def test_large_logits_clustered_by_row_residue(M):
+    """50 large logit values, each repeated on every row with the same
+    residue mod 256 (16 copies in each 4096-row chunk, all in one thread of
+    the selection from logits): equal values crowd the top bins of every
+    chunk and of the merge, and the k largest must still come out by value,
+    then by row."""
+    N, K = 2 * 4096 + 300, 256
+    x = synth.decode_x(M, K=K)
+    xf = synth.bf16_bits_to_f32(x)
+    t = np.arange(N) % 256
+    c = np.where(t < 50, 1.0 + t / 64.0, 0.01).astype(np.float32)[:, None]
+    W = synth.f32_to_bf16_bits((c * xf[0][None, :]).astype(np.float32))
+    host_q = oracle.quantize(W)
+    for k in (1, 50, 128):
+        ids, vals = assert_same_as_plain(to_bf16_dev(x), upload(*host_q), k, f"clustered k={k}")
+        assert_oracle_agrees(ids[:1], vals[:1], oracle.logits(x[:1], *host_q))
+
+
 @pytest.mark.parametrize("M", [3, 70])
 def test_negative_nan_and_zero_tokens(M):
     """All-negative logits, a NaN token (every logit NaN: rows 0 .. k-1, all
