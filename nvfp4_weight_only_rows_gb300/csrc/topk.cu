@@ -275,12 +275,12 @@ cudaError_t topk_select_launch(const unsigned long long* lines, const uint2* grp
 // loads every chunk's candidates into shared memory and selects the k
 // largest the same way.  The keys are distinct, so the answer is that of a
 // sort of the fp32 logits, bit for bit.
-constexpr int kLogitThreads = 256;
-constexpr int kLogitPer = kLogitChunk / kLogitThreads;  // 16 logits per thread
+// A CTA has T threads: 1024 for one token, 512 for up to 8, 256 beyond (a
+// single token's 32 chunks are latency-bound and take more threads; many
+// tokens' chunks fill the GPU with smaller CTAs).
 constexpr int kRankCap = 256;     // keys ranked in shared memory at the end of a select
 constexpr int kDigitBits = 11;    // radix digit: 2048 bins (a quarter octave at the top)
 constexpr int kBins = 1 << kDigitBits;
-constexpr int kBinsPerThread = kBins / kLogitThreads;  // 8
 
 __device__ __forceinline__ unsigned long long logit_key(float v, uint32_t n) {
   uint32_t b = __float_as_uint(v);
@@ -290,7 +290,7 @@ __device__ __forceinline__ unsigned long long logit_key(float v, uint32_t n) {
 }
 
 // The `want` largest of the `count` distinct keys in shared memory (whole
-// block of kLogitThreads, want <= count, want <= kTopkMax): an 11-bit digit
+// block of T threads, want <= count, want <= kTopkMax): an 11-bit digit
 // at a time from the top, the histogram of the next digit over the keys
 // inside the range chosen so far picks the digit of the want-th largest,
 // until the keys at or above that prefix (zeros below it) are few enough to
@@ -298,12 +298,14 @@ __device__ __forceinline__ unsigned long long logit_key(float v, uint32_t n) {
 // distinct) and out[r] receives the key of rank r < want.  (Measured
 // against warp-aggregated histogram adds, an atomic-free gather and a
 // count-based threshold search: none was faster.)
+template <int T>
 __device__ void select_largest(const unsigned long long* keys, int count, int want,
                                unsigned long long* out, unsigned long long* s_rank,
                                uint32_t* hist) {
   __shared__ unsigned long long s_prefix;
   __shared__ uint32_t s_need, s_above, s_bin, s_n;
-  __shared__ uint32_t s_warp[kLogitThreads / 32];
+  constexpr int kBinsPerThread = kBins / T;
+  __shared__ uint32_t s_warp[T / 32];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   unsigned long long prefix = 0ull, mask = 0ull;
   // need: keys still to find inside the range; above: keys above the range
@@ -386,7 +388,8 @@ __device__ void select_largest(const unsigned long long* keys, int count, int wa
 }
 
 // Keys held in shared memory: max(kLogitChunk, chunks x k) (the merge's).
-__global__ void __launch_bounds__(kLogitThreads) topk_logits_kernel(
+template <int T>
+__global__ void __launch_bounds__(T) topk_logits_kernel(
     const float* __restrict__ logits, int64_t N, int k, unsigned long long* __restrict__ cand,
     unsigned long long* __restrict__ lines, int64_t* __restrict__ ids, float* __restrict__ vals) {
   // the logits come from the GEMM, which may still be running
@@ -403,20 +406,21 @@ __global__ void __launch_bounds__(kLogitThreads) topk_logits_kernel(
   const int rows = (int)min((int64_t)kLogitChunk, N - n0);
   const float* src = logits + m * N + n0;
   // all of this thread's loads in flight together
+  constexpr int kLogitPer = kLogitChunk / T;  // logits per thread
   float v[kLogitPer];
 #pragma unroll
   for (int j = 0; j < kLogitPer; ++j) {
-    const int i = threadIdx.x + j * kLogitThreads;
+    const int i = threadIdx.x + j * T;
     v[j] = i < rows ? __ldcg(src + i) : 0.0f;
   }
 #pragma unroll
   for (int j = 0; j < kLogitPer; ++j) {
-    const int i = threadIdx.x + j * kLogitThreads;
+    const int i = threadIdx.x + j * T;
     if (i < rows) s_keys[i] = logit_key(v[j], (uint32_t)(n0 + i));
   }
   __syncthreads();
   const int kc = min(k, rows);
-  select_largest(s_keys, rows, kc, s_out, s_rank, hist);
+  select_largest<T>(s_keys, rows, kc, s_out, s_rank, hist);
   unsigned long long* my = cand + (m * n_chunks + blockIdx.x) * (int64_t)k;
   for (int j = threadIdx.x; j < k; j += blockDim.x) my[j] = j < kc ? s_out[j] : 0ull;
   // the last CTA of the token merges (release: the list above is visible
@@ -436,21 +440,21 @@ __global__ void __launch_bounds__(kLogitThreads) topk_logits_kernel(
   // zeros are never among the k largest because the token has N >= k keys
   const int total = n_chunks * k;
   const unsigned long long* all = cand + m * (int64_t)total;
-  for (int i0 = 0; i0 < total; i0 += 8 * kLogitThreads) {  // eight loads in flight per thread
+  for (int i0 = 0; i0 < total; i0 += 8 * T) {  // eight loads in flight per thread
     unsigned long long c8[8];
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-      const int i = i0 + threadIdx.x + j * kLogitThreads;
+      const int i = i0 + threadIdx.x + j * T;
       c8[j] = i < total ? __ldcg(all + i) : 0ull;
     }
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-      const int i = i0 + threadIdx.x + j * kLogitThreads;
+      const int i = i0 + threadIdx.x + j * T;
       if (i < total) s_keys[i] = c8[j];
     }
   }
   __syncthreads();
-  select_largest(s_keys, total, k, s_out, s_rank, hist);
+  select_largest<T>(s_keys, total, k, s_out, s_rank, hist);
   for (int j = threadIdx.x; j < k; j += blockDim.x) {
     const unsigned long long kk = s_out[j];
     ids[m * k + j] = (int64_t)(uint32_t)~(uint32_t)kk;
@@ -467,16 +471,27 @@ static size_t topk_logits_smem(int64_t N, int k) {
 
 bool topk_logits_fits(int64_t N, int k) { return topk_logits_smem(N, k) <= kTopkLogitsMaxSmem; }
 
+template <int T>
+static cudaError_t topk_logits_launch_t(const float* logits, int64_t M, int64_t N, int k,
+                                        unsigned long long* cand, unsigned long long* lines,
+                                        int64_t* ids, float* vals, cudaStream_t stream) {
+  static std::atomic<uint64_t> limit_set{0};
+  const cudaError_t attr_err = smem_limit_once(
+      limit_set, reinterpret_cast<const void*>(topk_logits_kernel<T>), kTopkLogitsMaxSmem);
+  if (attr_err != cudaSuccess) return attr_err;
+  PdlLaunch l(dim3((unsigned)((N + kLogitChunk - 1) / kLogitChunk), (unsigned)M), dim3(T),
+              topk_logits_smem(N, k), stream);
+  return cudaLaunchKernelEx(&l.cfg, topk_logits_kernel<T>, logits, N, k, cand, lines, ids, vals);
+}
+
 cudaError_t topk_logits_launch(const float* logits, int64_t M, int64_t N, int k,
                                unsigned long long* cand, unsigned long long* lines, int64_t* ids,
                                float* vals, cudaStream_t stream) {
-  static std::atomic<uint64_t> limit_set{0};
-  const cudaError_t attr_err = smem_limit_once(
-      limit_set, reinterpret_cast<const void*>(topk_logits_kernel), kTopkLogitsMaxSmem);
-  if (attr_err != cudaSuccess) return attr_err;
-  PdlLaunch l(dim3((unsigned)((N + kLogitChunk - 1) / kLogitChunk), (unsigned)M),
-              dim3(kLogitThreads), topk_logits_smem(N, k), stream);
-  return cudaLaunchKernelEx(&l.cfg, topk_logits_kernel, logits, N, k, cand, lines, ids, vals);
+  // same-box, k = 50 over 128256 rows: 256 -> 1024 threads 64.0 -> 61.8 us a call at M = 1;
+  // 512 threads 66.3 -> 65.5 us at M = 8; 256 stay best from M = 32
+  if (M == 1) return topk_logits_launch_t<1024>(logits, M, N, k, cand, lines, ids, vals, stream);
+  if (M <= 8) return topk_logits_launch_t<512>(logits, M, N, k, cand, lines, ids, vals, stream);
+  return topk_logits_launch_t<256>(logits, M, N, k, cand, lines, ids, vals, stream);
 }
 
 }  // namespace nvfp4

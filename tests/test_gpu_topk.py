@@ -102,10 +102,11 @@ def test_first_column_is_the_argmax():
     assert torch.equal(vals[:, 0], a_vals)
 
 
-# Up to 32 tokens the call writes the fp32 logits and selects from them; more
+# Up to 32 tokens the call writes the fp32 logits and selects from them
+# (1024 threads a chunk for one token, 512 up to 8 tokens, 256 beyond); more
 # tokens keep thresholded candidates in the GEMM epilogue: the cases below
-# run both routes.
-ROUTES = [9, 70]
+# run every one of these.
+ROUTES = [1, 5, 9, 70]
 
 
 @pytest.mark.parametrize("M", ROUTES)
