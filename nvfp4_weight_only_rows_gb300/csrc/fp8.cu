@@ -136,20 +136,21 @@ constexpr int kW8Threads = 32 * (kW8FirstEpiWarp + 4);
 // threads of one CTA: the roles above, plus the threshold warp in top-k mode
 template <int kOut>
 constexpr int w8a8_threads() { return kW8Threads + (kOut == kOutTopk ? 32 : 0); }
-constexpr uint32_t kW8AStageBytes = kRows * kKB;  // 128 rows x 256 e4m3 = 32 KB
 
-template <int kOut, int kStages>
+template <int kOut, int kStages, int kKS = kKB, int kTokStride = kMaxBN>
 __global__ void __launch_bounds__(w8a8_threads<kOut>(), 1)
     w8a8_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_x,
                    const GemmArgs p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
+  constexpr uint32_t kAStageBytes = kRows * kKS;     // 128 rows x kKS e4m3
+  constexpr int kBoxes = kKS / 128;                   // 128-k TMA boxes per stage
   const int BN = p.BN;
   const uint32_t x_box_bytes = (uint32_t)BN * 128;  // one 128-k TMA box of activations
-  const uint32_t x_stage_bytes = 2 * x_box_bytes;
-  uint8_t* s_a = smem;                                // kStages x 32 KB weights
-  uint8_t* s_x = s_a + kStages * kW8AStageBytes;      // kStages x BN x 256 activations
+  const uint32_t x_stage_bytes = kBoxes * x_box_bytes;
+  uint8_t* s_a = smem;                                // kStages x kAStageBytes weights
+  uint8_t* s_x = s_a + kStages * kAStageBytes;        // kStages x BN x kKS activations
   uint64_t* bars = reinterpret_cast<uint64_t*>(s_x + kStages * x_stage_bytes);
   uint64_t* s_full = bars;                 // both operands of stage s landed (2 producers)
   uint64_t* s_empty = s_full + kStages;    // the MMAs reading stage s completed
@@ -158,9 +159,9 @@ __global__ void __launch_bounds__(w8a8_threads<kOut>(), 1)
   uint64_t* done_bar = d_empty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done_bar + 1);
   volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(tmem_slot + 1);
-  float* s_tok = reinterpret_cast<float*>(bars + 32);  // 4 epilogue warps x kMaxBN
-  int32_t* s_last = reinterpret_cast<int32_t*>(s_tok + 4 * kMaxBN);
-  float* s_thr = reinterpret_cast<float*>(s_last + 4);  // argmax, top-k: 4 warps x kMaxBN
+  float* s_tok = reinterpret_cast<float*>(bars + 32);  // 4 epilogue warps x kTokStride
+  int32_t* s_last = reinterpret_cast<int32_t*>(s_tok + 4 * kTokStride);
+  float* s_thr = reinterpret_cast<float*>(s_last + 4);  // argmax, top-k: 4 warps x kTokStride
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -193,7 +194,7 @@ __global__ void __launch_bounds__(w8a8_threads<kOut>(), 1)
   WaitCtl wc{p.status, abort_flag, kWaitLimitNs};
 
   if (warp == 0) {
-    // ---------------- weight producer: two 128-k boxes of 128 rows per stage
+    // ---------------- weight producer: kBoxes 128-k boxes of 128 rows per stage
     const uint64_t pol = p.n_ttiles == 1 ? policy_evict_first() : policy_evict_last();
     uint32_t issued = 0;
     for_each_piece(p, [&](const Piece& pc) {
@@ -202,12 +203,12 @@ __global__ void __launch_bounds__(w8a8_threads<kOut>(), 1)
         const uint32_t st = issued % kStages, ph = (issued / kStages) & 1;
         if (!warp_wait(&s_empty[st], ph ^ 1, wc)) return false;
         if (elect_one()) {
-          mbar_arrive_expect_tx(&s_full[st], kW8AStageBytes);
-          uint8_t* dst = s_a + st * kW8AStageBytes;
+          mbar_arrive_expect_tx(&s_full[st], kAStageBytes);
+          uint8_t* dst = s_a + st * kAStageBytes;
 #pragma unroll
-          for (int b = 0; b < 2; ++b)
-            tma_load_2d_hint(dst + b * (kW8AStageBytes / 2), &tm_w, kb * kKB + 128 * b, n0,
-                             &s_full[st], pol);
+          for (int b = 0; b < kBoxes; ++b)
+            tma_load_2d_hint(dst + b * (kRows * 128), &tm_w, kb * kKS + 128 * b, n0, &s_full[st],
+                             pol);
         }
         __syncwarp();
       }
@@ -228,8 +229,8 @@ __global__ void __launch_bounds__(w8a8_threads<kOut>(), 1)
           mbar_arrive_expect_tx(&s_full[st], x_stage_bytes);
           uint8_t* dst = s_x + st * x_stage_bytes;
 #pragma unroll
-          for (int b = 0; b < 2; ++b)
-            tma_load_2d_hint(dst + b * x_box_bytes, &tm_x, kb * kKB + 128 * b, t0, &s_full[st],
+          for (int b = 0; b < kBoxes; ++b)
+            tma_load_2d_hint(dst + b * x_box_bytes, &tm_x, kb * kKS + 128 * b, t0, &s_full[st],
                              pol);
         }
         __syncwarp();
@@ -238,11 +239,11 @@ __global__ void __launch_bounds__(w8a8_threads<kOut>(), 1)
     });
     drain_loads(s_full, kStages, issued, 2, p.status);
   } else if (warp == 2) {
-    // ---------------- MMA issuer: 8 x (M 128, N BN, K 32) per stage
+    // ---------------- MMA issuer: kKS / 32 x (M 128, N BN, K 32) per stage
     const uint32_t idesc = idesc_e4m3_f32((uint32_t)BN);
     const uint64_t adesc0 = smem_desc_sw128(smem_u32(s_a));
     const uint64_t xdesc0 = smem_desc_sw128(smem_u32(s_x));
-    const uint32_t a_box = (kW8AStageBytes / 2) >> 4, x_box = x_box_bytes >> 4;
+    const uint32_t a_box = (kRows * 128) >> 4, x_box = x_box_bytes >> 4;
     uint32_t g = 0;
     int64_t i = 0;
     for_each_piece(p, [&](const Piece& pc) {
@@ -255,11 +256,11 @@ __global__ void __launch_bounds__(w8a8_threads<kOut>(), 1)
         const uint32_t st = g % kStages, ph = (g / kStages) & 1;
         if (!warp_wait(&s_full[st], ph, wc)) return false;
         tc_fence_after();
-        const uint64_t ad = adesc0 + ((st * kW8AStageBytes) >> 4);
+        const uint64_t ad = adesc0 + ((st * kAStageBytes) >> 4);
         const uint64_t xd = xdesc0 + ((st * x_stage_bytes) >> 4);
         if (elect_one()) {
 #pragma unroll
-          for (int kk = 0; kk < kKB / 32; ++kk)
+          for (int kk = 0; kk < kKS / 32; ++kk)
             tc_mma_ss_f8(d_tmem, ad + (kk >> 2) * a_box + 2 * (kk & 3),
                          xd + (kk >> 2) * x_box + 2 * (kk & 3), idesc,
                          (kb != pc.kb0) || (kk != 0));
@@ -279,8 +280,9 @@ __global__ void __launch_bounds__(w8a8_threads<kOut>(), 1)
     mbar_wait(done_bar, 0, drain);
   } else if (warp < kW8FirstEpiWarp + 4) {
     // ---------------- epilogue: token scale, then the row's own scale
-    epilogue_role<kOut, true>(p, plain_sched(p), warp, warp - kW8FirstEpiWarp, lane, tmem_base, d_full, d_empty,
-                              wc, s_tok, s_thr);
+    epilogue_role<kOut, true, false, kTokStride>(p, plain_sched(p), warp, warp - kW8FirstEpiWarp,
+                                                 lane, tmem_base, d_full, d_empty, wc, s_tok,
+                                                 s_thr);
     if (kOut == kOutTopk && lane == 0) atomicAdd(s_last + 1, 1);  // this warp is done
   } else {
     // ---------------- top-k thresholds (only launched in top-k mode)
@@ -296,9 +298,12 @@ __global__ void __launch_bounds__(w8a8_threads<kOut>(), 1)
 }
 
 // ------------------------------------------------------------ host side
-static size_t w8a8_smem_bytes(int BN, int stages, bool argmax) {
-  return 1024 + stages * ((size_t)kW8AStageBytes + (size_t)BN * kKB) + 256 +
-         4 * kMaxBN * sizeof(float) + (argmax ? 16 + 4 * kMaxBN * sizeof(float) : 0);
+// A stage covers ks of K (256, or 128 for the wide token tile): 128 weight
+// rows x ks e4m3 and BN token rows x ks, in 128-byte-wide TMA boxes.
+static size_t w8a8_smem_bytes(int BN, int stages, bool argmax, int ks, int tok_stride) {
+  return 1024 + stages * ((size_t)kRows * ks + (size_t)BN * ks) + 256 +
+         4 * (size_t)tok_stride * sizeof(float) +
+         (argmax ? 16 + 4 * (size_t)tok_stride * sizeof(float) : 0);
 }
 
 // Threads per row of the row quantizer: each holds at most kFp8MaxVec
@@ -322,29 +327,41 @@ nvfp4_status fp8_quantize_launch(const void* W, int64_t N, int64_t K, uint8_t* q
   return cudaGetLastError() == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA;
 }
 
+// Logits of 256 tokens or more take 256-token tiles: an MMA of N = 256 reads
+// each weight byte from shared memory once per 256 tokens instead of 128,
+// and the shared-memory port, not the fp8 tensor rate, bounds the 128-token
+// tile (128 KB of TMA writes and MMA reads per 4.2 M MACs).  TMEM holds two
+// such accumulators (the fp8 product keeps no scales there).  The logits,
+// argmax and top-k products take the same tiles, so they add the same
+// partial sums in the same order.
+static bool w8a8_wide(int64_t M) { return M >= kWideBN; }
+
 size_t w8a8_workspace_bytes(int64_t M, int64_t N, int64_t K, bool argmax) {
-  return ws_layout(M, N, K, std::max(sm_count(), 1), argmax, ActFormat::kE4M3).total;
+  return ws_layout(M, N, K, std::max(sm_count(), 1), argmax, ActFormat::kE4M3, 0,
+                   w8a8_wide(M) ? kWideBN : 0)
+      .total;
 }
 
 size_t w8a8_topk_workspace_bytes(int64_t M, int64_t N, int64_t K, int k) {
   const int sms = std::max(sm_count(), 1);
   if (M <= kTopkLogitsMaxM && topk_logits_fits(N, k))  // fp32 logits, then the selection
     return topk_logits_layout(ws_layout(M, N, K, sms, true, ActFormat::kE4M3).total, M, N, k).total;
-  return ws_layout(M, N, K, sms, false, ActFormat::kE4M3, k).total;
+  return ws_layout(M, N, K, sms, false, ActFormat::kE4M3, k, w8a8_wide(M) ? kWideBN : 0).total;
 }
 
-template <int kOut, int kStages>
+template <int kOut, int kStages, int kKS = kKB, int kTokStride = kMaxBN>
 static cudaError_t launch_w8a8(const CUtensorMap& tm_w, const CUtensorMap& tm_x, const GemmArgs& a,
                                int grid, cudaStream_t stream) {
-  auto kern = w8a8_tc_kernel<kOut, kStages>;
+  auto kern = w8a8_tc_kernel<kOut, kStages, kKS, kTokStride>;
   constexpr bool kArgmax = kOut == kOutArgmax || kOut == kOutTopk;  // per-warp thresholds
-  constexpr int kMaxTileBN = kStages >= 4 ? 64 : kMaxBN;
+  constexpr int kMaxTileBN = kTokStride > kMaxBN ? kTokStride : (kStages >= 4 ? 64 : kMaxBN);
   static std::atomic<uint64_t> limit_set{0};
-  const cudaError_t attr_err = smem_limit_once(limit_set, reinterpret_cast<const void*>(kern),
-                                               w8a8_smem_bytes(kMaxTileBN, kStages, kArgmax));
+  const cudaError_t attr_err =
+      smem_limit_once(limit_set, reinterpret_cast<const void*>(kern),
+                      w8a8_smem_bytes(kMaxTileBN, kStages, kArgmax, kKS, kTokStride));
   if (attr_err != cudaSuccess) return attr_err;
   PdlLaunch l(dim3((unsigned)grid), dim3(w8a8_threads<kOut>()),
-              w8a8_smem_bytes(a.BN, kStages, kArgmax), stream);
+              w8a8_smem_bytes(a.BN, kStages, kArgmax, kKS, kTokStride), stream);
   return cudaLaunchKernelEx(&l.cfg, kern, tm_w, tm_x, a);
 }
 
@@ -363,11 +380,13 @@ static nvfp4_status w8a8_run(const void* x, int64_t M, int64_t K, const uint8_t*
   const bool topk_logits =
       out_mode == kOutTopk && M <= kTopkLogitsMaxM && topk_logits_fits(N, topk_k);
   const bool topk = out_mode == kOutTopk && !topk_logits;
-  const int BN = lm_head_token_tile(M);
+  const bool wide = !topk_logits && w8a8_wide(M);
+  const int BN = wide ? kWideBN : lm_head_token_tile(M);
+  const int ks = wide ? 128 : kKB;  // K per stage
   const int n_ttiles = (int)((M + BN - 1) / BN);
   const int64_t m_pad = (int64_t)n_ttiles * BN;
   const WsLayout L = ws_layout(M, N, K, sms, argmax || topk_logits, ActFormat::kE4M3,
-                               topk ? topk_k : 0);
+                               topk ? topk_k : 0, wide ? kWideBN : 0);
   const TopkLogitsLayout TL = topk_logits_layout(L.total, M, N, topk_k);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   if (topk_logits) {
@@ -406,7 +425,7 @@ static nvfp4_status w8a8_run(const void* x, int64_t M, int64_t K, const uint8_t*
   a.n_units = ((N + kRows - 1) / kRows) * n_ttiles;
   // K % 16: the last stage's k past K reads zeros (the weight and activation
   // maps end at K; a TMA box past the end is filled with zeros)
-  a.n_kb = (int)((K + kKB - 1) / kKB);
+  a.n_kb = (int)((K + ks - 1) / ks);
   schedule_units(a, L.grid);
   uint32_t cols = 32;
   while (cols < 2u * BN) cols *= 2;
@@ -427,16 +446,23 @@ static nvfp4_status w8a8_run(const void* x, int64_t M, int64_t K, const uint8_t*
   const int grid = L.grid;
   const bool small = BN <= 64;
   cudaError_t err;
-  if (argmax)
+  if (argmax && wide)
+    err = launch_w8a8<kOutArgmax, 4, 128, kWideBN>(tm_w, tm_x, a, grid, stream);
+  else if (argmax)
     err = small ? launch_w8a8<kOutArgmax, 4>(tm_w, tm_x, a, grid, stream)
                 : launch_w8a8<kOutArgmax, 3>(tm_w, tm_x, a, grid, stream);
   else if (topk) {
-    err = small ? launch_w8a8<kOutTopk, 4>(tm_w, tm_x, a, grid, stream)
-                : launch_w8a8<kOutTopk, 3>(tm_w, tm_x, a, grid, stream);
+    err = wide ? launch_w8a8<kOutTopk, 4, 128, kWideBN>(tm_w, tm_x, a, grid, stream)
+               : (small ? launch_w8a8<kOutTopk, 4>(tm_w, tm_x, a, grid, stream)
+                        : launch_w8a8<kOutTopk, 3>(tm_w, tm_x, a, grid, stream));
     if (err == cudaSuccess)
       err = topk_select_launch(a.am_keys, a.tk_grp, a.tk_cand, M, N, topk_k, token_ids,
                                max_logits, stream);
-  } else if (out_mode == NVFP4_OUT_BF16)
+  } else if (wide && out_mode == NVFP4_OUT_BF16)
+    err = launch_w8a8<NVFP4_OUT_BF16, 4, 128, kWideBN>(tm_w, tm_x, a, grid, stream);
+  else if (wide)
+    err = launch_w8a8<NVFP4_OUT_F32, 4, 128, kWideBN>(tm_w, tm_x, a, grid, stream);
+  else if (out_mode == NVFP4_OUT_BF16)
     err = small ? launch_w8a8<NVFP4_OUT_BF16, 4>(tm_w, tm_x, a, grid, stream)
                 : launch_w8a8<NVFP4_OUT_BF16, 3>(tm_w, tm_x, a, grid, stream);
   else

@@ -24,6 +24,7 @@ namespace nvfp4 {
 constexpr int kRows = 128;   // vocabulary rows per unit (MMA M)
 constexpr int kKB = 256;     // k per pipeline stage
 constexpr int kMaxBN = 128;  // largest token tile
+constexpr int kWideBN = 256;  // the W8A8 prefill's token tile (its TMEM holds no scales)
 constexpr int kOutArgmax = 2;   // third output mode (after NVFP4_OUT_F32, NVFP4_OUT_BF16)
 constexpr int kOutTopk = 3;     // fourth: the k largest logits of each token
 constexpr int kKeyStride = 16;  // argmax / top-k: one 128-byte line of per-token state (spreads the atomics)
@@ -477,7 +478,8 @@ __device__ __forceinline__ uint32_t cta_stages(const Sched& sc, uint32_t n_kb) {
 // other CTA's partial where a unit was split, scaled (token multiplier, then
 // the row's own scale for fp8 weights) and stored, or reduced to per-token
 // candidates (argmax, top-k).  `epi` is the warp's index among the four.
-template <int kOut, bool kRowScale, bool kGrouped = false>
+// kTokStride: floats per epilogue warp in s_tok / s_thr (>= the token tile)
+template <int kOut, bool kRowScale, bool kGrouped = false, int kTokStride = kMaxBN>
 __device__ __forceinline__ void epilogue_role(const GemmArgs& p, const Sched& sc, int warp, int epi,
                                               int lane, uint32_t tmem_base, uint64_t* d_full,
                                               uint64_t* d_empty, const WaitCtl& wc,
@@ -488,8 +490,8 @@ __device__ __forceinline__ void epilogue_role(const GemmArgs& p, const Sched& sc
   const int q = warp & 3;
   const int row = q * 32 + lane;
   const uint32_t lane_off = (uint32_t)(q * 32) << 16;
-  float* tok = s_tok + epi * kMaxBN;
-  float* wthr = s_thr + epi * kMaxBN;
+  float* tok = s_tok + epi * kTokStride;
+  float* wthr = s_thr + epi * kTokStride;
   int64_t i = 0;
   for_each_piece(sc, (uint32_t)n_kb, [&](const Piece& pc) {
     const uint32_t u = pc.u, kb0 = pc.kb0, kb1 = pc.kb1;
@@ -799,11 +801,12 @@ struct WsLayout {
 };
 
 
+// bn: the call's token tile when it is not lm_head_token_tile(M)
 static inline WsLayout ws_layout(int64_t M, int64_t N, int64_t K, int sms, bool argmax,
-                                 ActFormat act, int topk_k = 0) {
+                                 ActFormat act, int topk_k = 0, int bn = 0) {
   WsLayout l;
   const bool keys = argmax || topk_k > 0;
-  const int BN = lm_head_token_tile(M);
+  const int BN = bn > 0 ? bn : lm_head_token_tile(M);
   const int64_t m_pad = (M + BN - 1) / BN * BN;
   const int64_t n_units = ((N + kRows - 1) / kRows) * ((M + BN - 1) / BN);
   l.grid = (int)std::max<int64_t>(1, std::min<int64_t>(sms, n_units));

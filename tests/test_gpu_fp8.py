@@ -112,10 +112,13 @@ def test_tiny_workload():
 @pytest.mark.parametrize("M,N,K", [(1, 300, 512), (5, 129, 256), (16, 128, 768),
                                    (17, 1000, 512), (64, 777, 1024), (100, 513, 256),
                                    (130, 260, 512), (200, 384, 1280), (1, 1, 256),
-                                   (8, 216 * 128, 1024), (40, 300 * 128, 768), (3, 100, 16384)])
+                                   (8, 216 * 128, 1024), (40, 300 * 128, 768), (3, 100, 16384),
+                                   (256, 1000, 512), (300, 2000, 768), (600, 777, 272),
+                                   (1024, 160 * 128, 256)])
 def test_product_shapes(M, N, K):
     """Ragged tokens and rows, one and several token tiles, split-K tails,
-    the longest K."""
+    the longest K; from 256 tokens the 256-token tiles with 128-k stages
+    (ragged token tile, K % 128 != 0, several units per CTA)."""
     x, (wq, ws), (xq, xs) = product_case(N, K, M, seed=M + N)
     ref_cols = np.unique(np.linspace(0, N - 1, min(N, 3000)).astype(np.int64))
     ref = oracle.fp8_logits(xq, xs, wq, ws, cols=ref_cols)
