@@ -174,15 +174,17 @@ __global__ void __launch_bounds__(kEncodeThreads) nvfp4_encode_kernel(
         t = fminf(t, 448.0f);
         const __nv_fp8_storage_t s8 = __nv_cvt_float_to_fp8(t, __NV_SATFINITE, __NV_E4M3);
         const float r = r_of_code[s8 & 0x7F];
+        // x * r, two values per packed multiply (each lane rounds like the
+        // scalar binary32 multiply)
+        const float2 r2 = make_float2(r, r);
+        const uint32_t w4[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
         float q[8];
-        q[0] = __fmul_rn(bf16_lo(v[i].x), r);
-        q[1] = __fmul_rn(bf16_hi(v[i].x), r);
-        q[2] = __fmul_rn(bf16_lo(v[i].y), r);
-        q[3] = __fmul_rn(bf16_hi(v[i].y), r);
-        q[4] = __fmul_rn(bf16_lo(v[i].z), r);
-        q[5] = __fmul_rn(bf16_hi(v[i].z), r);
-        q[6] = __fmul_rn(bf16_lo(v[i].w), r);
-        q[7] = __fmul_rn(bf16_hi(v[i].w), r);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float2 p2 = __fmul2_rn(make_float2(bf16_lo(w4[j]), bf16_hi(w4[j])), r2);
+          q[2 * j] = p2.x;
+          q[2 * j + 1] = p2.y;
+        }
         const uint32_t word = cvt_e2m1x8(q);
         if (col < K) {
           prow[col >> 3] = word;
