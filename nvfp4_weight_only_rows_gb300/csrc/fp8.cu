@@ -344,8 +344,8 @@ size_t w8a8_workspace_bytes(int64_t M, int64_t N, int64_t K, bool argmax) {
 
 size_t w8a8_topk_workspace_bytes(int64_t M, int64_t N, int64_t K, int k) {
   const int sms = std::max(sm_count(), 1);
-  if (M <= kTopkLogitsMaxM && topk_logits_fits(N, k))  // fp32 logits, then the selection
-    return topk_logits_layout(ws_layout(M, N, K, sms, true, ActFormat::kE4M3).total, M, N, k).total;
+  if (M <= kTopkLogitsMaxM && topk_logits_fits(N))  // fp32 logits, then the selection
+    return topk_logits_layout(ws_layout(M, N, K, sms, false, ActFormat::kE4M3).total, M, N).total;
   return ws_layout(M, N, K, sms, false, ActFormat::kE4M3, k, w8a8_wide(M) ? kWideBN : 0).total;
 }
 
@@ -378,16 +378,16 @@ static nvfp4_status w8a8_run(const void* x, int64_t M, int64_t K, const uint8_t*
   // top-k of a few tokens: the fp32 logits are written and selected from;
   // of many tokens: thresholded candidates in the epilogue
   const bool topk_logits =
-      out_mode == kOutTopk && M <= kTopkLogitsMaxM && topk_logits_fits(N, topk_k);
+      out_mode == kOutTopk && M <= kTopkLogitsMaxM && topk_logits_fits(N);
   const bool topk = out_mode == kOutTopk && !topk_logits;
   const bool wide = !topk_logits && w8a8_wide(M);
   const int BN = wide ? kWideBN : lm_head_token_tile(M);
   const int ks = wide ? 128 : kKB;  // K per stage
   const int n_ttiles = (int)((M + BN - 1) / BN);
   const int64_t m_pad = (int64_t)n_ttiles * BN;
-  const WsLayout L = ws_layout(M, N, K, sms, argmax || topk_logits, ActFormat::kE4M3,
-                               topk ? topk_k : 0, wide ? kWideBN : 0);
-  const TopkLogitsLayout TL = topk_logits_layout(L.total, M, N, topk_k);
+  const WsLayout L = ws_layout(M, N, K, sms, argmax, ActFormat::kE4M3, topk ? topk_k : 0,
+                               wide ? kWideBN : 0);
+  const TopkLogitsLayout TL = topk_logits_layout(L.total, M, N);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   if (topk_logits) {
     out_mode = NVFP4_OUT_F32;
@@ -396,9 +396,8 @@ static nvfp4_status w8a8_run(const void* x, int64_t M, int64_t K, const uint8_t*
   int32_t* status = reinterpret_cast<int32_t*>(ws);
   uint8_t* xq = ws + L.x16;
   float* tok_scale = reinterpret_cast<float*>(ws + L.tok);
-  unsigned long long* keys = argmax || topk || topk_logits
-                                 ? reinterpret_cast<unsigned long long*>(ws + L.keys)
-                                 : nullptr;
+  unsigned long long* keys =
+      argmax || topk ? reinterpret_cast<unsigned long long*>(ws + L.keys) : nullptr;
 
   CUtensorMap tm_w, tm_x;
   if (!encode_2d(&tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, wq, (uint64_t)K, (uint64_t)N, (uint64_t)K,
@@ -442,11 +441,14 @@ static nvfp4_status w8a8_run(const void* x, int64_t M, int64_t K, const uint8_t*
   a.am_idx = token_ids;
   a.am_val = max_logits;
   a.row_scale = w_scale;
+  a.grp_max = topk_logits ? reinterpret_cast<uint32_t*>(ws + TL.gmax) : nullptr;
   if (topk) topk_args(a, ws, L, topk_k, N);
   const int grid = L.grid;
   const bool small = BN <= 64;
   cudaError_t err;
-  if (argmax && wide)
+  if (topk_logits)  // up to 64 tokens: a small tile
+    err = launch_w8a8<kOutLogitsGroups, 4>(tm_w, tm_x, a, grid, stream);
+  else if (argmax && wide)
     err = launch_w8a8<kOutArgmax, 4, 128, kWideBN>(tm_w, tm_x, a, grid, stream);
   else if (argmax)
     err = small ? launch_w8a8<kOutArgmax, 4>(tm_w, tm_x, a, grid, stream)
@@ -469,9 +471,8 @@ static nvfp4_status w8a8_run(const void* x, int64_t M, int64_t K, const uint8_t*
     err = small ? launch_w8a8<NVFP4_OUT_F32, 4>(tm_w, tm_x, a, grid, stream)
                 : launch_w8a8<NVFP4_OUT_F32, 3>(tm_w, tm_x, a, grid, stream);
   if (err == cudaSuccess && topk_logits)
-    err = topk_logits_launch(reinterpret_cast<const float*>(ws + TL.logits), M, N, topk_k,
-                             reinterpret_cast<unsigned long long*>(ws + TL.cand), keys, token_ids,
-                             max_logits, stream);
+    err = topk_logits_launch(reinterpret_cast<const float*>(ws + TL.logits), a.grp_max, M, N,
+                             topk_k, token_ids, max_logits, stream);
   if (err != cudaSuccess || cudaGetLastError() != cudaSuccess) return NVFP4_ERR_CUDA;
   return NVFP4_OK;
 }

@@ -27,6 +27,7 @@ constexpr int kMaxBN = 128;  // largest token tile
 constexpr int kWideBN = 256;  // the W8A8 prefill's token tile (its TMEM holds no scales)
 constexpr int kOutArgmax = 2;   // third output mode (after NVFP4_OUT_F32, NVFP4_OUT_BF16)
 constexpr int kOutTopk = 3;     // fourth: the k largest logits of each token
+constexpr int kOutLogitsGroups = 4;  // fifth: fp32 logits and their 32-row maxima (grp_max)
 constexpr int kKeyStride = 16;  // argmax / top-k: one 128-byte line of per-token state (spreads the atomics)
 constexpr int kTopkMax = 128;   // largest k of the fused top-k
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per pipeline wait
@@ -64,6 +65,9 @@ struct GemmArgs {
   uint32_t* tk_hist;            // [m_pad][kHistWords] histograms of the candidate keys
   int tk_k;                     // k, 1 .. kTopkMax
   const float* row_scale;       // [N] per-row weight scale (fp8 weights), else null
+  // output mode kOutLogitsGroups only: per token, the largest order key
+  // (logit_order) of every 32 rows of the fp32 logits, [M][ceil(N / 32)]
+  uint32_t* grp_max;
   // grouped product (experts) only
   const int32_t* grp_off;       // [n_groups + 1] token row offsets of the groups
   const float* grp_global;      // [n_groups] per-group weight global scale
@@ -255,6 +259,45 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const 
 __device__ __forceinline__ uint32_t order_key(float v) {
   const uint32_t b = __float_as_uint(v);
   return b ^ ((uint32_t)((int32_t)b >> 31) | 0x80000000u);
+}
+
+// Order key of a logit for the top-k selection: unsigned order equals the
+// float order, -0 counts as +0, a NaN sits above every number (positive
+// NaNs) or below (negative).
+__device__ __forceinline__ uint32_t logit_order(float v) {
+  uint32_t b = __float_as_uint(v);
+  if ((b & 0x7FFFFFFFu) == 0u) b = 0u;
+  return b ^ ((uint32_t)((int32_t)b >> 31) | 0x80000000u);
+}
+
+// Per token of a 16-token chunk, the largest order key of the warp's 32
+// rows (one group: the warp's rows start at a multiple of 32), into
+// p.grp_max[token][group].  A butterfly over the lanes halves the tokens
+// each lane keeps at every step (exchanging the half its partner keeps), so
+// that lanes 2u and 2u + 1 end with token u's maximum: 16 shuffles and one
+// store where a reduction per token would take 16 of each.
+__device__ __forceinline__ void group_maxima(const GemmArgs& p, int64_t tc, int64_t live,
+                                             const float (&val)[16], bool valid, uint32_t n_base,
+                                             int lane) {
+  uint32_t a[16];
+#pragma unroll
+  for (int t = 0; t < 16; ++t) a[t] = valid ? logit_order(val[t]) : 0u;
+#pragma unroll
+  for (int w = 8; w >= 1; w >>= 1) {  // keep w of 2w tokens: lane bit 2w (as a mask) picks the half
+    const bool upper = (lane & (2 * w)) != 0;
+#pragma unroll
+    for (int j = 0; j < w; ++j) {
+      const uint32_t mine = upper ? a[j + w] : a[j];
+      const uint32_t send = upper ? a[j] : a[j + w];
+      a[j] = max(mine, __shfl_xor_sync(0xFFFFFFFFu, send, 2 * w));
+    }
+  }
+  a[0] = max(a[0], __shfl_xor_sync(0xFFFFFFFFu, a[0], 1));
+  const int t = (lane >> 1) & 15;
+  if ((lane & 1) == 0 && t < live) {
+    const int64_t G = (p.N + 31) >> 5;
+    p.grp_max[(tc + t) * G + (n_base >> 5)] = a[0];
+  }
 }
 
 // 16 consecutive floats of shared memory (16-byte aligned)
@@ -632,6 +675,28 @@ __device__ __forceinline__ void epilogue_role(const GemmArgs& p, const Sched& sc
             }
           }
         }
+      } else if (kOut == kOutLogitsGroups) {
+        // the fp32 logits as below, then the maxima of the warp's group
+        const bool valid = n < p.N;
+        float mul[16], val[16];
+        lds_f32x16(tok + c, mul);
+#pragma unroll
+        for (int t = 0; t < 16; t += 2) {
+          float2 r = __fmul2_rn(make_float2(__uint_as_float(v[t]), __uint_as_float(v[t + 1])),
+                                make_float2(mul[t], mul[t + 1]));
+          if (kRowScale) r = __fmul2_rn(r, make_float2(rs, rs));
+          val[t] = r.x;
+          val[t + 1] = r.y;
+        }
+        const int64_t tc = t0 + c;
+        const int64_t live = t_end - tc;
+        if (valid) {
+          float* ptr = reinterpret_cast<float*>(p.out) + tc * p.N + n;
+#pragma unroll
+          for (int t = 0; t < 16; ++t, ptr += p.N)
+            if (t < live) *ptr = val[t];
+        }
+        if (n - lane < p.N) group_maxima(p, tc, live, val, valid, (uint32_t)(n - lane), lane);
       } else if (n < p.N) {
         // token multipliers by vector loads, scaled in pairs (each lane of
         // the packed multiply rounds like the scalar one), one store per
@@ -858,36 +923,32 @@ cudaError_t stage_rows_launch(const uint8_t* src, int64_t rows, int64_t row_byte
                               int64_t dst_stride, cudaStream_t stream);
 
 // Up to this many tokens a top-k call writes the fp32 logits (at most
-// 32 x N x 4 bytes, a twentieth of the weight bytes) and selects from them
-// (topk.cu, topk_logits_launch); beyond, the GEMM keeps thresholded
-// candidates in its epilogue and topk_select_launch picks from those.  (At
-// 64 tokens the selection's 2048 chunk CTAs cost as much as the epilogue
-// route, measured; at 1 to 32 tokens the logits route is 4 to 8 us faster.)
-constexpr int64_t kTopkLogitsMaxM = 32;
-constexpr int kLogitChunk = 4096;  // logits of one token per selecting CTA
+// 64 x N x 4 bytes, a tenth of the weight bytes) and the per-token maxima of
+// every 32 rows, and selects from them (topk.cu, topk_logits_launch);
+// beyond, the GEMM keeps thresholded candidates in its epilogue and
+// topk_select_launch picks from those.
+constexpr int64_t kTopkLogitsMaxM = 64;
+static_assert(kTopkLogitsMaxM <= 64, "the logits route launches the decode-tile GEMM shapes only");
+// The selecting CTA holds a token's group maxima in registers: vocabularies
+// up to this many rows take the logits route.
+constexpr int64_t kTopkLogitsMaxN = 32 * 8192;
 
 // Workspace of the logits route after a call's own layout ending at `base`:
-// [fp32 logits, M x N][per token and chunk of kLogitChunk rows, k candidate
-// keys].  The per-token chunk counters are word 0 of the argmax lines.
+// [fp32 logits, M x N][u32 group maxima, M x ceil(N / 32)].
 struct TopkLogitsLayout {
-  size_t logits, cand, total;
+  size_t logits, gmax, total;
 };
-static inline TopkLogitsLayout topk_logits_layout(size_t base, int64_t M, int64_t N, int k) {
+static inline TopkLogitsLayout topk_logits_layout(size_t base, int64_t M, int64_t N) {
   TopkLogitsLayout t;
   t.logits = align_up(base, 256);
-  t.cand = align_up(t.logits + (size_t)M * N * 4, 256);
-  t.total = t.cand + (size_t)M * ((N + kLogitChunk - 1) / kLogitChunk) * k * 8;
+  t.gmax = align_up(t.logits + (size_t)M * N * 4, 256);
+  t.total = t.gmax + (size_t)M * ((N + 31) / 32) * 4;
   return t;
 }
 
-cudaError_t topk_logits_launch(const float* logits, int64_t M, int64_t N, int k,
-                               unsigned long long* cand, unsigned long long* lines, int64_t* ids,
-                               float* vals, cudaStream_t stream);
-// The selecting CTA holds a chunk's keys or the merge's (chunks x k) in
-// shared memory, at most this many bytes: the logits route takes the call
-// only where they fit (every vocabulary up to 1.4 M rows at k = 128).
-constexpr size_t kTopkLogitsMaxSmem = 176 * 1024;
-bool topk_logits_fits(int64_t N, int k);
+cudaError_t topk_logits_launch(const float* logits, const uint32_t* gmax, int64_t M, int64_t N,
+                               int k, int64_t* ids, float* vals, cudaStream_t stream);
+static inline bool topk_logits_fits(int64_t N) { return N <= kTopkLogitsMaxN; }
 
 // The top-k selection kernel (topk.cu), launched after a top-k GEMM.
 cudaError_t topk_select_launch(const unsigned long long* lines, const uint2* grp,

@@ -595,9 +595,9 @@ static bool encode_weight_maps(CUtensorMap* tm_packed, CUtensorMap* tm_scales,
 
 size_t lm_head_topk_workspace_bytes(int64_t M, int64_t N, int64_t K, int k) {
   const int sms = std::max(sm_count(), 1);
-  if (M <= kTopkLogitsMaxM && topk_logits_fits(N, k)) {  // fp32 logits, then the selection
-    const WsLayout L = ws_layout(M, N, K, sms, true, ActFormat::kF16);
-    return weight_stage(N, K, topk_logits_layout(L.total, M, N, k).total, true).total;
+  if (M <= kTopkLogitsMaxM && topk_logits_fits(N)) {  // fp32 logits, then the selection
+    const WsLayout L = ws_layout(M, N, K, sms, false, ActFormat::kF16);
+    return weight_stage(N, K, topk_logits_layout(L.total, M, N).total, true).total;
   }
   const WsLayout L = ws_layout(M, N, K, sms, false, ActFormat::kF16, k);
   return weight_stage(N, K, L.total, true).total;
@@ -617,15 +617,14 @@ static nvfp4_status lm_head_run(const void* x, int64_t M, int64_t K, const uint8
   // top-k of a few tokens: the fp32 logits are written and selected from;
   // of many tokens: thresholded candidates in the epilogue
   const bool topk_logits =
-      out_mode == kOutTopk && M <= kTopkLogitsMaxM && topk_logits_fits(N, topk_k);
+      out_mode == kOutTopk && M <= kTopkLogitsMaxM && topk_logits_fits(N);
   const bool topk = out_mode == kOutTopk && !topk_logits;
-  const bool keys = argmax || topk || topk_logits;  // per-token lines the prep kernel clears
+  const bool keys = argmax || topk;  // per-token lines the prep kernel clears
   const int BN = lm_head_token_tile(M);
   const int n_ttiles = (int)((M + BN - 1) / BN);
   const int64_t m_pad = (int64_t)n_ttiles * BN;
-  const WsLayout L = ws_layout(M, N, K, sms, argmax || topk_logits, ActFormat::kF16,
-                               topk ? topk_k : 0);
-  const TopkLogitsLayout TL = topk_logits_layout(L.total, M, N, topk_k);
+  const WsLayout L = ws_layout(M, N, K, sms, argmax, ActFormat::kF16, topk ? topk_k : 0);
+  const TopkLogitsLayout TL = topk_logits_layout(L.total, M, N);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   int32_t* status = reinterpret_cast<int32_t*>(ws);
   __half* x16 = reinterpret_cast<__half*>(ws + L.x16);
@@ -693,6 +692,7 @@ static nvfp4_status lm_head_run(const void* x, int64_t M, int64_t K, const uint8
   a.am_val = max_logits;
   if (topk) topk_args(a, ws, L, topk_k, N);
   a.row_scale = nullptr;
+  a.grp_max = topk_logits ? reinterpret_cast<uint32_t*>(ws + TL.gmax) : nullptr;
   // decode-sized token tiles get a third A stage, six packed stages and a
   // third dequant warp per quadrant; 128-token tiles leave TMEM room for two
   // A stages only
@@ -710,7 +710,9 @@ static nvfp4_status lm_head_run(const void* x, int64_t M, int64_t K, const uint8
   // programmatic dependent launch: the GEMM starts streaming weights while
   // the prep kernel is still running
   cudaError_t err;
-  if (argmax)
+  if (topk_logits)  // up to 64 tokens: the decode shape
+    err = launch_gemm<kOutLogitsGroups, 3, 6, 3>(tm_packed, tm_scales, tm_x, a, grid, stream);
+  else if (argmax)
     err = deep ? launch_gemm<kOutArgmax, 3, 6, 3>(tm_packed, tm_scales, tm_x, a, grid, stream)
                : launch_gemm<kOutArgmax, 2, 4, 2>(tm_packed, tm_scales, tm_x, a, grid, stream);
   else if (topk) {
@@ -726,10 +728,8 @@ static nvfp4_status lm_head_run(const void* x, int64_t M, int64_t K, const uint8
     err = deep ? launch_gemm<NVFP4_OUT_F32, 3, 6, 3>(tm_packed, tm_scales, tm_x, a, grid, stream)
                : launch_gemm<NVFP4_OUT_F32, 2, 4, 2>(tm_packed, tm_scales, tm_x, a, grid, stream);
   if (err == cudaSuccess && topk_logits)
-    err = topk_logits_launch(reinterpret_cast<const float*>(ws + TL.logits), M, N, topk_k,
-                             reinterpret_cast<unsigned long long*>(ws + TL.cand),
-                             reinterpret_cast<unsigned long long*>(ws + L.keys), token_ids,
-                             max_logits, stream);
+    err = topk_logits_launch(reinterpret_cast<const float*>(ws + TL.logits), a.grp_max, M, N,
+                             topk_k, token_ids, max_logits, stream);
   if (err != cudaSuccess || cudaGetLastError() != cudaSuccess) return NVFP4_ERR_CUDA;
   return NVFP4_OK;
 }

@@ -265,43 +265,57 @@ cudaError_t topk_select_launch(const unsigned long long* lines, const uint2* grp
 }
 
 // ------------------------------------------------------------ from logits
-// Top-k of decode-sized products: the GEMM writes fp32 logits (M x N, a few
-// tens of MB next to hundreds of MB of weights), then one kernel selects.
-// CTA (c, m) takes token m's logits [c * kLogitChunk, (c + 1) * kLogitChunk):
-// it forms the 64-bit candidate keys (order key of the logit, -0 as +0,
-// << 32 | ~row), finds its min(k, rows) largest by a radix select and writes
-// them in order to the token's candidate list; the last of the token's CTAs
-// to finish (a counter in the token's line, cleared by the prep kernel)
-// loads every chunk's candidates into shared memory and selects the k
-// largest the same way.  The keys are distinct, so the answer is that of a
-// sort of the fp32 logits, bit for bit.
-// A CTA has T threads: 1024 for one token, 512 for up to 8, 256 beyond (a
-// single token's 32 chunks are latency-bound and take more threads; many
-// tokens' chunks fill the GPU with smaller CTAs).
-constexpr int kRankCap = 256;     // keys ranked in shared memory at the end of a select
+// Top-k of decode-sized products: the GEMM writes the fp32 logits (M x N, a
+// few tens of MB next to hundreds of MB of weights) and, per token, the
+// largest order key of every 32 rows (its epilogue warps hold 32
+// consecutive rows); then one CTA per token selects:
+// 1. the super-group maxima: the largest of every sg consecutive group
+//    maxima, sg the widest power of two up to 32 that leaves at least 2k of
+//    them (k of them where the vocabulary is that short);
+// 2. the bound: the k-th largest super-group maximum.  Each super-group
+//    maximum is a logit of its own rows, so at least k logits reach the
+//    bound and the k-th largest logit is not below it;
+// 3. the hot groups: those whose maximum reaches the bound (the others hold
+//    no logit that does);
+// 4. their logits that reach the bound (a few more than k: with s
+//    super-groups, about -s ln(1 - k / s)), ranked against each other.
+// The keys (order key << 32 | ~row) are distinct, so the answer is that of
+// a sort of the fp32 logits, bit for bit.  A radix select over all N keys
+// takes over where more than kHotCap groups or kRankCap logits reach the
+// bound (heavily tied logits) or where N < 32 k.
+constexpr int kRankCap = 512;     // keys ranked against each other in shared memory
 constexpr int kDigitBits = 11;    // radix digit: 2048 bins (a quarter octave at the top)
 constexpr int kBins = 1 << kDigitBits;
+constexpr int kSuperCap = 512;    // super-group maxima (at most max(256, 4k))
+constexpr int kHotCap = 2048;     // groups whose maximum reaches the bound
 
 __device__ __forceinline__ unsigned long long logit_key(float v, uint32_t n) {
-  uint32_t b = __float_as_uint(v);
-  if ((b & 0x7FFFFFFFu) == 0u) b = 0u;  // -0 counts as +0
-  return ((unsigned long long)(b ^ ((uint32_t)((int32_t)b >> 31) | 0x80000000u)) << 32) |
-         (uint32_t)~n;
+  return ((unsigned long long)logit_order(v) << 32) | (uint32_t)~n;
 }
 
-// The `want` largest of the `count` distinct keys in shared memory (whole
-// block of T threads, want <= count, want <= kTopkMax): an 11-bit digit
-// at a time from the top, the histogram of the next digit over the keys
-// inside the range chosen so far picks the digit of the want-th largest,
-// until the keys at or above that prefix (zeros below it) are few enough to
-// rank; each of those is then ranked against the others (the keys are
-// distinct) and out[r] receives the key of rank r < want.  (Measured
-// against warp-aggregated histogram adds, an atomic-free gather and a
-// count-based threshold search: none was faster.)
+// Every one of the `count` distinct keys in `keys` (shared memory, count <=
+// kRankCap) against the others: out[r] receives the key of rank r < want.
 template <int T>
-__device__ void select_largest(const unsigned long long* keys, int count, int want,
-                               unsigned long long* out, unsigned long long* s_rank,
-                               uint32_t* hist) {
+__device__ void rank_keys(const unsigned long long* keys, int count, int want,
+                          unsigned long long* out) {
+  for (int i = threadIdx.x; i < count; i += T) {
+    const unsigned long long kk = keys[i];
+    int rank = 0;
+#pragma unroll 8
+    for (int j = 0; j < count; ++j) rank += keys[j] > kk ? 1 : 0;
+    if (rank < want) out[rank] = kk;
+  }
+  __syncthreads();
+}
+
+// The `want` largest of the `count` distinct keys key_at(i) (whole block of
+// T threads, want <= count, want <= kTopkMax): an 11-bit digit at a time
+// from the top, the histogram of the next digit over the keys inside the
+// range chosen so far picks the digit of the want-th largest, until the keys
+// at or above that prefix (zeros below it) are few enough to rank.
+template <int T, typename KeyAt>
+__device__ void select_largest(KeyAt key_at, int count, int want, unsigned long long* out,
+                               unsigned long long* s_rank, uint32_t* hist) {
   __shared__ unsigned long long s_prefix;
   __shared__ uint32_t s_need, s_above, s_bin, s_n;
   constexpr int kBinsPerThread = kBins / T;
@@ -318,13 +332,14 @@ __device__ void select_largest(const unsigned long long* keys, int count, int wa
       for (int i = tid; i < kBins; i += blockDim.x) hist[i] = 0;
       __syncthreads();
       for (int i = tid; i < count; i += blockDim.x) {
-        const unsigned long long kk = keys[i];
+        const unsigned long long kk = key_at(i);
         if ((kk & mask) == prefix)
           atomicAdd(&hist[(uint32_t)(kk >> shift) & ((1u << width) - 1u)], 1u);
       }
       __syncthreads();
-      // thread t holds the 8 bins below kBins - 8t (from the top); a block
-      // scan from the top counts the range's keys in higher bins
+      // thread t holds the kBinsPerThread bins below kBins - kBinsPerThread t
+      // (from the top); a block scan from the top counts the range's keys in
+      // higher bins
       uint32_t c[kBinsPerThread], sum = 0;
 #pragma unroll
       for (int j = 0; j < kBinsPerThread; ++j) {
@@ -369,129 +384,188 @@ __device__ void select_largest(const unsigned long long* keys, int count, int wa
   if (tid == 0) s_n = 0;
   __syncthreads();
   for (int i = tid; i < count; i += blockDim.x) {
-    const unsigned long long kk = keys[i];
+    const unsigned long long kk = key_at(i);
     if (kk >= prefix) {
       const uint32_t pos = atomicAdd(&s_n, 1u);
       if (pos < (uint32_t)kRankCap) s_rank[pos] = kk;
     }
   }
   __syncthreads();
-  const int m = (int)min(s_n, (uint32_t)kRankCap);
-  for (int i = tid; i < m; i += blockDim.x) {
-    const unsigned long long kk = s_rank[i];
-    int rank = 0;
-#pragma unroll 8
-    for (int j = 0; j < m; ++j) rank += s_rank[j] > kk ? 1 : 0;
-    if (rank < want) out[rank] = kk;
-  }
-  __syncthreads();
+  rank_keys<T>(s_rank, (int)min(s_n, (uint32_t)kRankCap), want, out);
 }
 
-// Keys held in shared memory: max(kLogitChunk, chunks x k) (the merge's).
+// The element of rank r (0 = the largest; equal values by index) among
+// a[0, n) in shared memory, into *out: P threads an element share its
+// comparisons (whole block of T threads; the caller synchronises after).
+template <int T, typename V>
+__device__ void rank_select(const V* a, int n, int r, V* out) {
+  int P = 1;
+  while (P < 32 && 2 * P * n <= T) P *= 2;
+  const int part = threadIdx.x % P;
+  for (int s0 = 0; s0 < n * P; s0 += T) {  // uniform: whole warps reach the shuffles
+    const int e = (s0 + (int)threadIdx.x) / P;
+    const bool valid = e < n;
+    const V mine = valid ? a[e] : V(0);
+    uint32_t cnt = 0;
+    if (valid) {
+#pragma unroll 4
+      for (int j = part; j < n; j += P) {
+        const V x = a[j];
+        cnt += (x > mine || (x == mine && j < e)) ? 1u : 0u;
+      }
+    }
+    for (int o = 1; o < P; o <<= 1) cnt += __shfl_xor_sync(0xFFFFFFFFu, cnt, o);
+    if (valid && part == 0 && cnt == (uint32_t)r) *out = mine;
+  }
+}
+
+// Offset of this warp's first item in a block-wide compaction and the
+// total, from the per-warp counts in s_wcnt (after a barrier).
+template <int T>
+__device__ __forceinline__ uint32_t warp_offset(const uint32_t* s_wcnt, uint32_t* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const uint32_t c = lane < T / 32 ? s_wcnt[lane] : 0u;
+  *total = __reduce_add_sync(0xFFFFFFFFu, c);
+  return __reduce_add_sync(0xFFFFFFFFu, lane < warp ? c : 0u);
+}
+
+// Appends `key` to s_list (capacity kRankCap; the count in *s_n keeps
+// growing past it) where `take`; the whole warp calls it.
+__device__ __forceinline__ void append_key(bool take, unsigned long long key,
+                                           unsigned long long* s_list, uint32_t* s_n) {
+  const uint32_t bal = __ballot_sync(0xFFFFFFFFu, take);
+  if (bal == 0u) return;
+  const int lane = threadIdx.x & 31;
+  uint32_t pos0 = 0;
+  if (lane == 0) pos0 = atomicAdd(s_n, (uint32_t)__popc(bal));
+  pos0 = __shfl_sync(0xFFFFFFFFu, pos0, 0);
+  const uint32_t pos = pos0 + __popc(bal & ((1u << lane) - 1u));
+  if (take && pos < (uint32_t)kRankCap) s_list[pos] = key;
+}
+
+// Group maxima a thread holds: a token's ceil(N / 32) <= 8192 of them.
+template <int T>
+constexpr int groups_per_thread() { return (int)(kTopkLogitsMaxN / 32) / T; }
+
 template <int T>
 __global__ void __launch_bounds__(T) topk_logits_kernel(
-    const float* __restrict__ logits, int64_t N, int k, unsigned long long* __restrict__ cand,
-    unsigned long long* __restrict__ lines, int64_t* __restrict__ ids, float* __restrict__ vals) {
-  // the logits come from the GEMM, which may still be running
+    const float* __restrict__ logits, const uint32_t* __restrict__ gmax, int64_t N, int k,
+    int64_t* __restrict__ ids, float* __restrict__ vals) {
+  // the logits and group maxima come from the GEMM, which may still be running
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  extern __shared__ unsigned long long s_keys[];
+  constexpr int kPer = groups_per_thread<T>();
   __shared__ unsigned long long s_rank[kRankCap];
   __shared__ unsigned long long s_out[kTopkMax];
   __shared__ uint32_t hist[kBins];
-  __shared__ int s_last;
-  const int64_t m = blockIdx.y;
-  const int n_chunks = gridDim.x;
-  const int64_t n0 = (int64_t)blockIdx.x * kLogitChunk;
-  const int rows = (int)min((int64_t)kLogitChunk, N - n0);
-  const float* src = logits + m * N + n0;
-  // all of this thread's loads in flight together
-  constexpr int kLogitPer = kLogitChunk / T;  // logits per thread
-  float v[kLogitPer];
+  __shared__ uint32_t s_super[kSuperCap];
+  __shared__ uint32_t s_hot[kHotCap];
+  __shared__ uint32_t s_wcnt[T / 32];
+  __shared__ uint32_t s_bound, s_n;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const uint32_t lt = (1u << lane) - 1u;
+  const int64_t m = blockIdx.x;
+  const int G = (int)((N + 31) / 32);
+  const float* src = logits + m * N;
+  const uint32_t* gm = gmax + m * (int64_t)G;
+  // 1. the group maxima (group tid + j T), all loads in flight together
+  uint32_t g[kPer];
 #pragma unroll
-  for (int j = 0; j < kLogitPer; ++j) {
-    const int i = threadIdx.x + j * T;
-    v[j] = i < rows ? __ldcg(src + i) : 0.0f;
+  for (int j = 0; j < kPer; ++j) {
+    const int i = tid + j * T;
+    g[j] = i < G ? __ldcg(gm + i) : 0u;
   }
+  int sg = 32;
+  while (sg > 1 && (G + sg - 1) / sg < 2 * k) sg >>= 1;
+  const int n_super = (G + sg - 1) / sg;
+  // warp w holds groups j T + 32 w + lane in step j: a 32-group super-group,
+  // or 32 / sg of them
 #pragma unroll
-  for (int j = 0; j < kLogitPer; ++j) {
-    const int i = threadIdx.x + j * T;
-    if (i < rows) s_keys[i] = logit_key(v[j], (uint32_t)(n0 + i));
-  }
-  __syncthreads();
-  const int kc = min(k, rows);
-  select_largest<T>(s_keys, rows, kc, s_out, s_rank, hist);
-  unsigned long long* my = cand + (m * n_chunks + blockIdx.x) * (int64_t)k;
-  for (int j = threadIdx.x; j < k; j += blockDim.x) my[j] = j < kc ? s_out[j] : 0ull;
-  // the last CTA of the token merges (release: the list above is visible
-  // before the count; acquire: the others' lists are read after it)
-  __threadfence();
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    uint32_t old;
-    asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], 1;"
-                 : "=r"(old) : "l"(reinterpret_cast<uint32_t*>(lines + m * kKeyStride)) : "memory");
-    s_last = old == (uint32_t)n_chunks - 1u;
-  }
-  __syncthreads();
-  if (!s_last) return;
-  __threadfence();
-  // every chunk wrote k slots, the unused ones zero (below every key): the
-  // zeros are never among the k largest because the token has N >= k keys
-  const int total = n_chunks * k;
-  const unsigned long long* all = cand + m * (int64_t)total;
-  for (int i0 = 0; i0 < total; i0 += 8 * T) {  // eight loads in flight per thread
-    unsigned long long c8[8];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const int i = i0 + threadIdx.x + j * T;
-      c8[j] = i < total ? __ldcg(all + i) : 0ull;
-    }
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const int i = i0 + threadIdx.x + j * T;
-      if (i < total) s_keys[i] = c8[j];
+  for (int j = 0; j < kPer; ++j) {
+    const int i = tid + j * T;
+    if (j * T + warp * 32 < G) {  // warp-uniform
+      if (sg == 32) {
+        const uint32_t mx = __reduce_max_sync(0xFFFFFFFFu, g[j]);
+        if (lane == 0) s_super[i >> 5] = mx;
+      } else {
+        uint32_t mx = g[j];
+        for (int o = 1; o < sg; o <<= 1) mx = max(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
+        if ((lane & (sg - 1)) == 0 && i < G) s_super[i / sg] = mx;
+      }
     }
   }
+  if (tid == 0) {
+    s_n = 0;
+    s_bound = 0u;  // fewer than k groups: every logit is a candidate
+  }
   __syncthreads();
-  select_largest<T>(s_keys, total, k, s_out, s_rank, hist);
-  for (int j = threadIdx.x; j < k; j += blockDim.x) {
+  // 2. the bound: the k-th largest super-group maximum
+  if (n_super >= k) rank_select<T>(s_super, n_super, k - 1, &s_bound);
+  __syncthreads();
+  const uint32_t bound = s_bound;
+  // 3. the hot groups, compacted into s_hot (count per warp, then offsets)
+  uint32_t n_hot;
+  {
+    uint32_t cnt = 0;
+#pragma unroll
+    for (int j = 0; j < kPer; ++j)
+      cnt += __popc(__ballot_sync(0xFFFFFFFFu, tid + j * T < G && g[j] >= bound));
+    if (lane == 0) s_wcnt[warp] = cnt;
+    __syncthreads();
+    uint32_t pos = warp_offset<T>(s_wcnt, &n_hot);
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+      const int i = tid + j * T;
+      const bool hot = i < G && g[j] >= bound;
+      const uint32_t bal = __ballot_sync(0xFFFFFFFFu, hot);
+      if (hot) {
+        const uint32_t at = pos + __popc(bal & lt);
+        if (at < (uint32_t)kHotCap) s_hot[at] = (uint32_t)i;
+      }
+      pos += __popc(bal);
+    }
+    __syncthreads();
+  }
+  // 4. the hot groups' logits that reach the bound: a warp per group, two
+  // groups' loads in flight per warp
+  bool ranked = false;
+  if (n_hot <= (uint32_t)kHotCap) {
+    constexpr int kW = T / 32;
+    for (int h0 = warp; h0 < (int)n_hot; h0 += 2 * kW) {
+      float v[2];
+      int64_t row[2];
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int h = h0 + u * kW;
+        row[u] = h < (int)n_hot ? (int64_t)s_hot[h] * 32 + lane : N;
+        v[u] = row[u] < N ? __ldcg(src + row[u]) : 0.0f;
+      }
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const unsigned long long key = logit_key(v[u], (uint32_t)row[u]);
+        append_key(row[u] < N && (uint32_t)(key >> 32) >= bound, key, s_rank, &s_n);
+      }
+    }
+    __syncthreads();
+    if (s_n <= (uint32_t)kRankCap) {
+      rank_keys<T>(s_rank, (int)s_n, k, s_out);
+      ranked = true;
+    }
+  }
+  if (!ranked)  // block-uniform
+    select_largest<T>([&](int i) { return logit_key(__ldcg(src + i), (uint32_t)i); }, (int)N, k,
+                      s_out, s_rank, hist);
+  for (int j = tid; j < k; j += T) {
     const unsigned long long kk = s_out[j];
     ids[m * k + j] = (int64_t)(uint32_t)~(uint32_t)kk;
     if (vals) vals[m * k + j] = key_value((uint32_t)(kk >> 32));
   }
 }
 
-// Shared memory of the kernel for N rows and k: the chunk's keys and the
-// merge's (chunks x k), whichever is more.
-static size_t topk_logits_smem(int64_t N, int k) {
-  const int64_t chunks = (N + kLogitChunk - 1) / kLogitChunk;
-  return (size_t)std::max<int64_t>(kLogitChunk, chunks * k) * sizeof(unsigned long long);
-}
-
-bool topk_logits_fits(int64_t N, int k) { return topk_logits_smem(N, k) <= kTopkLogitsMaxSmem; }
-
-template <int T>
-static cudaError_t topk_logits_launch_t(const float* logits, int64_t M, int64_t N, int k,
-                                        unsigned long long* cand, unsigned long long* lines,
-                                        int64_t* ids, float* vals, cudaStream_t stream) {
-  static std::atomic<uint64_t> limit_set{0};
-  const cudaError_t attr_err = smem_limit_once(
-      limit_set, reinterpret_cast<const void*>(topk_logits_kernel<T>), kTopkLogitsMaxSmem);
-  if (attr_err != cudaSuccess) return attr_err;
-  PdlLaunch l(dim3((unsigned)((N + kLogitChunk - 1) / kLogitChunk), (unsigned)M), dim3(T),
-              topk_logits_smem(N, k), stream);
-  return cudaLaunchKernelEx(&l.cfg, topk_logits_kernel<T>, logits, N, k, cand, lines, ids, vals);
-}
-
-cudaError_t topk_logits_launch(const float* logits, int64_t M, int64_t N, int k,
-                               unsigned long long* cand, unsigned long long* lines, int64_t* ids,
-                               float* vals, cudaStream_t stream) {
-  // same-box, k = 50 over 128256 rows: 256 -> 1024 threads 64.0 -> 61.8 us a call at M = 1;
-  // 512 threads 66.3 -> 65.5 us at M = 8; 256 stay best from M = 32
-  if (M == 1) return topk_logits_launch_t<1024>(logits, M, N, k, cand, lines, ids, vals, stream);
-  if (M <= 8) return topk_logits_launch_t<512>(logits, M, N, k, cand, lines, ids, vals, stream);
-  return topk_logits_launch_t<256>(logits, M, N, k, cand, lines, ids, vals, stream);
+cudaError_t topk_logits_launch(const float* logits, const uint32_t* gmax, int64_t M, int64_t N,
+                               int k, int64_t* ids, float* vals, cudaStream_t stream) {
+  PdlLaunch l(dim3((unsigned)M), dim3(1024), 0, stream);
+  return cudaLaunchKernelEx(&l.cfg, topk_logits_kernel<1024>, logits, gmax, N, k, ids, vals);
 }
 
 }  // namespace nvfp4

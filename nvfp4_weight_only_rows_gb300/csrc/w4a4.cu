@@ -351,9 +351,9 @@ size_t w4a4_workspace_bytes(int64_t M, int64_t N, int64_t K, bool argmax) {
 
 size_t w4a4_topk_workspace_bytes(int64_t M, int64_t N, int64_t K, int k) {
   const int sms = std::max(sm_count(), 1);
-  if (M <= kTopkLogitsMaxM && topk_logits_fits(N, k)) {  // fp32 logits, then the selection
-    const WsLayout L = ws_layout(M, N, K, sms, true, ActFormat::kE2M1);
-    return weight_stage(N, K, topk_logits_layout(L.total, M, N, k).total, false).total;
+  if (M <= kTopkLogitsMaxM && topk_logits_fits(N)) {  // fp32 logits, then the selection
+    const WsLayout L = ws_layout(M, N, K, sms, false, ActFormat::kE2M1);
+    return weight_stage(N, K, topk_logits_layout(L.total, M, N).total, false).total;
   }
   const WsLayout L = ws_layout(M, N, K, sms, false, ActFormat::kE2M1, k);
   return weight_stage(N, K, L.total, false).total;
@@ -388,15 +388,14 @@ static nvfp4_status w4a4_run(const void* x, int64_t M, int64_t K, const uint8_t*
   // top-k of a few tokens: the fp32 logits are written and selected from;
   // of many tokens: thresholded candidates in the epilogue
   const bool topk_logits =
-      out_mode == kOutTopk && M <= kTopkLogitsMaxM && topk_logits_fits(N, topk_k);
+      out_mode == kOutTopk && M <= kTopkLogitsMaxM && topk_logits_fits(N);
   const bool topk = out_mode == kOutTopk && !topk_logits;
   const int BN = lm_head_token_tile(M);
   const int n_ttiles = (int)((M + BN - 1) / BN);
   const int64_t m_pad = (int64_t)n_ttiles * BN;
   const int64_t m_pad128 = round_up128(M);
-  const WsLayout L = ws_layout(M, N, K, sms, argmax || topk_logits, ActFormat::kE2M1,
-                               topk ? topk_k : 0);
-  const TopkLogitsLayout TL = topk_logits_layout(L.total, M, N, topk_k);
+  const WsLayout L = ws_layout(M, N, K, sms, argmax, ActFormat::kE2M1, topk ? topk_k : 0);
+  const TopkLogitsLayout TL = topk_logits_layout(L.total, M, N);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   if (topk_logits) {
     out_mode = NVFP4_OUT_F32;
@@ -408,9 +407,8 @@ static nvfp4_status w4a4_run(const void* x, int64_t M, int64_t K, const uint8_t*
   uint8_t* xsf = xq + align_up((size_t)m_pad * xs, 256);
   const WeightStage wst = weight_stage(N, K, topk_logits ? TL.total : L.total, false);
   float* tok_scale = reinterpret_cast<float*>(ws + L.tok);
-  unsigned long long* keys = argmax || topk || topk_logits
-                                 ? reinterpret_cast<unsigned long long*>(ws + L.keys)
-                                 : nullptr;
+  unsigned long long* keys =
+      argmax || topk ? reinterpret_cast<unsigned long long*>(ws + L.keys) : nullptr;
 
   CUtensorMap tm_w, tm_x;
   // both maps end at K/2 bytes: the TMA fills the k past K with zero codes
@@ -460,10 +458,13 @@ static nvfp4_status w4a4_run(const void* x, int64_t M, int64_t K, const uint8_t*
   a.am_idx = token_ids;
   a.am_val = max_logits;
   a.row_scale = nullptr;
+  a.grp_max = topk_logits ? reinterpret_cast<uint32_t*>(ws + TL.gmax) : nullptr;
   if (topk) topk_args(a, ws, L, topk_k, N);
   const int grid = L.grid;
   cudaError_t err;
-  if (argmax)
+  if (topk_logits)  // up to 64 tokens: a small tile
+    err = launch_w4a4<kOutLogitsGroups, 6>(tm_w, tm_x, wsf, xsf, a, grid, stream);
+  else if (argmax)
     err = small ? launch_w4a4<kOutArgmax, 6>(tm_w, tm_x, wsf, xsf, a, grid, stream)
                 : launch_w4a4<kOutArgmax, 5>(tm_w, tm_x, wsf, xsf, a, grid, stream);
   else if (topk) {
@@ -479,9 +480,8 @@ static nvfp4_status w4a4_run(const void* x, int64_t M, int64_t K, const uint8_t*
     err = small ? launch_w4a4<NVFP4_OUT_F32, 6>(tm_w, tm_x, wsf, xsf, a, grid, stream)
                 : launch_w4a4<NVFP4_OUT_F32, 5>(tm_w, tm_x, wsf, xsf, a, grid, stream);
   if (err == cudaSuccess && topk_logits)
-    err = topk_logits_launch(reinterpret_cast<const float*>(ws + TL.logits), M, N, topk_k,
-                             reinterpret_cast<unsigned long long*>(ws + TL.cand), keys, token_ids,
-                             max_logits, stream);
+    err = topk_logits_launch(reinterpret_cast<const float*>(ws + TL.logits), a.grp_max, M, N,
+                             topk_k, token_ids, max_logits, stream);
   if (err != cudaSuccess || cudaGetLastError() != cudaSuccess) return NVFP4_ERR_CUDA;
   return NVFP4_OK;
 }
