@@ -271,7 +271,8 @@ cudaError_t topk_select_launch(const unsigned long long* lines, const uint2* grp
 // consecutive rows); then one CTA per token selects:
 // 1. the super-group maxima: the largest of every sg consecutive group
 //    maxima, sg the widest power of two up to 32 that leaves at least 2k of
-//    them (k of them where the vocabulary is that short);
+//    them, or the narrowest that leaves at most 256 (at least k for k <=
+//    128 and N >= 32 k);
 // 2. the bound: the k-th largest super-group maximum.  Each super-group
 //    maximum is a logit of its own rows, so at least k logits reach the
 //    bound and the k-th largest logit is not below it;
@@ -286,7 +287,7 @@ cudaError_t topk_select_launch(const unsigned long long* lines, const uint2* grp
 constexpr int kRankCap = 512;     // keys ranked against each other in shared memory
 constexpr int kDigitBits = 11;    // radix digit: 2048 bins (a quarter octave at the top)
 constexpr int kBins = 1 << kDigitBits;
-constexpr int kSuperCap = 512;    // super-group maxima (at most max(256, 4k))
+constexpr int kSuperCap = 256;    // super-group maxima (sorted by one warp, 8 per lane)
 constexpr int kHotCap = 2048;     // groups whose maximum reaches the bound
 
 __device__ __forceinline__ unsigned long long logit_key(float v, uint32_t n) {
@@ -394,39 +395,71 @@ __device__ void select_largest(KeyAt key_at, int count, int want, unsigned long 
   rank_keys<T>(s_rank, (int)min(s_n, (uint32_t)kRankCap), want, out);
 }
 
-// The element of rank r (0 = the largest; equal values by index) among
-// a[0, n) in shared memory, into *out: P threads an element share its
-// comparisons (whole block of T threads; the caller synchronises after).
-template <int T, typename V>
-__device__ void rank_select(const V* a, int n, int r, V* out) {
-  int P = 1;
-  while (P < 32 && 2 * P * n <= T) P *= 2;
-  const int part = threadIdx.x % P;
-  for (int s0 = 0; s0 < n * P; s0 += T) {  // uniform: whole warps reach the shuffles
-    const int e = (s0 + (int)threadIdx.x) / P;
-    const bool valid = e < n;
-    const V mine = valid ? a[e] : V(0);
-    uint32_t cnt = 0;
-    if (valid) {
-#pragma unroll 4
-      for (int j = part; j < n; j += P) {
-        const V x = a[j];
-        cnt += (x > mine || (x == mine && j < e)) ? 1u : 0u;
+// Sorts the 32 R values a warp holds (R per lane, element lane R + r) into
+// descending order in registers: a bitonic network, partners R or more
+// elements apart exchanged by shuffles, nearer ones inside the lane.
+template <int R, typename V>
+__device__ __forceinline__ void warp_sort_desc(V (&a)[R], int lane) {
+#pragma unroll
+  for (int s = 2; s <= 32 * R; s <<= 1) {
+#pragma unroll
+    for (int d = s >> 1; d > 0; d >>= 1) {
+      if (d >= R) {
+        const bool lower = (lane & (d / R)) == 0;
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+          const bool desc = ((lane * R + r) & s) == 0;
+          const V other = __shfl_xor_sync(0xFFFFFFFFu, a[r], d / R);
+          a[r] = lower == desc ? (a[r] > other ? a[r] : other) : (a[r] < other ? a[r] : other);
+        }
+      } else {
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+          if ((r & d) == 0) {
+            const bool desc = ((lane * R + r) & s) == 0;
+            const V x = a[r], y = a[r + d];
+            if ((x < y) == desc) {
+              a[r] = y;
+              a[r + d] = x;
+            }
+          }
+        }
       }
     }
-    for (int o = 1; o < P; o <<= 1) cnt += __shfl_xor_sync(0xFFFFFFFFu, cnt, o);
-    if (valid && part == 0 && cnt == (uint32_t)r) *out = mine;
   }
 }
 
-// Offset of this warp's first item in a block-wide compaction and the
-// total, from the per-warp counts in s_wcnt (after a barrier).
-template <int T>
-__device__ __forceinline__ uint32_t warp_offset(const uint32_t* s_wcnt, uint32_t* total) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const uint32_t c = lane < T / 32 ? s_wcnt[lane] : 0u;
-  *total = __reduce_add_sync(0xFFFFFFFFu, c);
-  return __reduce_add_sync(0xFFFFFFFFu, lane < warp ? c : 0u);
+// The n values src[0, n) (shared memory, n <= 32 R) sorted by one warp,
+// larger first (zeros pad the rest); returns the one at position `pos`.
+template <int R, typename V>
+__device__ __forceinline__ V warp_kth(const V* src, int n, int pos, int lane) {
+  V a[R];
+#pragma unroll
+  for (int r = 0; r < R; ++r) a[r] = lane * R + r < n ? src[lane * R + r] : V(0);
+  warp_sort_desc<R>(a, lane);
+  V mine = a[0];
+#pragma unroll
+  for (int r = 1; r < R; ++r) mine = r == pos % R ? a[r] : mine;
+  return __shfl_sync(0xFFFFFFFFu, mine, pos / R);
+}
+
+// Keys src[0, n) (shared memory, distinct, n <= 32 R) sorted by one warp;
+// the first k (k <= n) go to ids / vals of token m.
+template <int R>
+__device__ __forceinline__ void warp_sort_out(const unsigned long long* src, int n, int k,
+                                              int64_t m, int64_t* ids, float* vals, int lane) {
+  unsigned long long a[R];
+#pragma unroll
+  for (int r = 0; r < R; ++r) a[r] = lane * R + r < n ? src[lane * R + r] : 0ull;
+  warp_sort_desc<R>(a, lane);
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    const int e = lane * R + r;
+    if (e < k) {
+      ids[m * k + e] = (int64_t)(uint32_t)~(uint32_t)a[r];
+      if (vals) vals[m * k + e] = key_value((uint32_t)(a[r] >> 32));
+    }
+  }
 }
 
 // Appends `key` to s_list (capacity kRankCap; the count in *s_n keeps
@@ -460,8 +493,7 @@ __global__ void __launch_bounds__(T) topk_logits_kernel(
   __shared__ uint32_t hist[kBins];
   __shared__ uint32_t s_super[kSuperCap];
   __shared__ uint32_t s_hot[kHotCap];
-  __shared__ uint32_t s_wcnt[T / 32];
-  __shared__ uint32_t s_bound, s_n;
+  __shared__ uint32_t s_bound, s_n, s_nhot;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const uint32_t lt = (1u << lane) - 1u;
   const int64_t m = blockIdx.x;
@@ -476,7 +508,7 @@ __global__ void __launch_bounds__(T) topk_logits_kernel(
     g[j] = i < G ? __ldcg(gm + i) : 0u;
   }
   int sg = 32;
-  while (sg > 1 && (G + sg - 1) / sg < 2 * k) sg >>= 1;
+  while (sg > 1 && (G + sg - 1) / sg < 2 * k && (G + sg / 2 - 1) / (sg / 2) <= kSuperCap) sg >>= 1;
   const int n_super = (G + sg - 1) / sg;
   // warp w holds groups j T + 32 w + lane in step j: a 32-group super-group,
   // or 32 / sg of them
@@ -496,36 +528,34 @@ __global__ void __launch_bounds__(T) topk_logits_kernel(
   }
   if (tid == 0) {
     s_n = 0;
+    s_nhot = 0;
     s_bound = 0u;  // fewer than k groups: every logit is a candidate
   }
   __syncthreads();
-  // 2. the bound: the k-th largest super-group maximum
-  if (n_super >= k) rank_select<T>(s_super, n_super, k - 1, &s_bound);
+  // 2. the bound: the k-th largest super-group maximum, sorted by warp 0
+  if (warp == 0 && n_super >= k) {
+    const uint32_t b = n_super <= 128 ? warp_kth<4>(s_super, n_super, k - 1, lane)
+                                      : warp_kth<8>(s_super, n_super, k - 1, lane);
+    if (lane == 0) s_bound = b;
+  }
   __syncthreads();
   const uint32_t bound = s_bound;
-  // 3. the hot groups, compacted into s_hot (count per warp, then offsets)
-  uint32_t n_hot;
-  {
-    uint32_t cnt = 0;
+  // 3. the hot groups, appended to s_hot (one shared counter per warp step)
 #pragma unroll
-    for (int j = 0; j < kPer; ++j)
-      cnt += __popc(__ballot_sync(0xFFFFFFFFu, tid + j * T < G && g[j] >= bound));
-    if (lane == 0) s_wcnt[warp] = cnt;
-    __syncthreads();
-    uint32_t pos = warp_offset<T>(s_wcnt, &n_hot);
-#pragma unroll
-    for (int j = 0; j < kPer; ++j) {
-      const int i = tid + j * T;
-      const bool hot = i < G && g[j] >= bound;
-      const uint32_t bal = __ballot_sync(0xFFFFFFFFu, hot);
-      if (hot) {
-        const uint32_t at = pos + __popc(bal & lt);
-        if (at < (uint32_t)kHotCap) s_hot[at] = (uint32_t)i;
-      }
-      pos += __popc(bal);
+  for (int j = 0; j < kPer; ++j) {
+    const int i = tid + j * T;
+    const bool hot = i < G && g[j] >= bound;
+    const uint32_t bal = __ballot_sync(0xFFFFFFFFu, hot);
+    if (bal != 0u) {
+      uint32_t pos0 = 0;
+      if (lane == 0) pos0 = atomicAdd(&s_nhot, (uint32_t)__popc(bal));
+      pos0 = __shfl_sync(0xFFFFFFFFu, pos0, 0);
+      const uint32_t at = pos0 + __popc(bal & lt);
+      if (hot && at < (uint32_t)kHotCap) s_hot[at] = (uint32_t)i;
     }
-    __syncthreads();
   }
+  __syncthreads();
+  const uint32_t n_hot = s_nhot;
   // 4. the hot groups' logits that reach the bound: a warp per group, two
   // groups' loads in flight per warp
   bool ranked = false;
@@ -547,8 +577,17 @@ __global__ void __launch_bounds__(T) topk_logits_kernel(
       }
     }
     __syncthreads();
-    if (s_n <= (uint32_t)kRankCap) {
-      rank_keys<T>(s_rank, (int)s_n, k, s_out);
+    const int n_cand = (int)s_n;
+    // 5. few candidates (the usual case): warp 0 sorts them and writes the k best
+    if (n_cand <= 128) {
+      if (warp == 0) {
+        if (n_cand <= 64) warp_sort_out<2>(s_rank, n_cand, k, m, ids, vals, lane);
+        else warp_sort_out<4>(s_rank, n_cand, k, m, ids, vals, lane);
+      }
+      return;
+    }
+    if (n_cand <= kRankCap) {
+      rank_keys<T>(s_rank, n_cand, k, s_out);
       ranked = true;
     }
   }
