@@ -63,9 +63,11 @@ def test_tiny_workload():
                                      (64, 777, 1024, 33), (100, 513, 256, 64),
                                      (130, 260, 512, 7), (200, 384, 1280, 100), (1, 1, 256, 1),
                                      (3, 7, 256, 7), (300, 5000, 256, 50),
-                                     (2, 262144, 256, 128)])
+                                     (2, 262144, 256, 128), (2, 262144 + 33, 256, 50),
+                                     (64, 40000, 256, 128)])
 def test_ragged_shapes(M, N, K, k):
-    """Ragged token and vocabulary tails, k up to N and up to the limit."""
+    """Ragged token and vocabulary tails, k up to N and up to the limit; the
+    largest vocabulary the logits route takes (262144 rows) and one past it."""
     W = synth.quant_weight(N=N, K=K, seed=M + N)
     x = synth.decode_x(M, K=K)
     host_q = oracle.quantize(W)
@@ -102,10 +104,9 @@ def test_first_column_is_the_argmax():
     assert torch.equal(vals[:, 0], a_vals)
 
 
-# Up to 32 tokens the call writes the fp32 logits and selects from them
-# (1024 threads a chunk for one token, 512 up to 8 tokens, 256 beyond); more
-# tokens keep thresholded candidates in the GEMM epilogue: the cases below
-# run every one of these.
+# Up to 64 tokens the call writes the fp32 logits and their 32-row maxima
+# and one CTA per token selects from them; more tokens keep thresholded
+# candidates in the GEMM epilogue: the cases below run both routes.
 ROUTES = [1, 5, 9, 70]
 
 
