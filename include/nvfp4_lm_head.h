@@ -21,8 +21,8 @@
  *     logits[m, n] = global * sum_k x[m, k] * e2m1(code[n, k]) * f32(scale[n, k/16]).
  *
  * Around them, in the order of the sections below: the greedy argmax and
- * the top-k of those logits fused into the product (the logits are never
- * written); the "fp8" lm_head copy (per-row E4M3 weights, W8A8 product) of
+ * the top-k of those logits fused into the product (the logits are written
+ * only to the workspace, and only up to 64 tokens); the "fp8" lm_head copy (per-row E4M3 weights, W8A8 product) of
  * `quantized_lm_head_copy` on the first page; the grouped W4A16 product of
  * all experts of an NVFP4 MoE layer; the W4A4 NVFP4 product of
  * `CompressedTensorsW4A4Fp4`; an allocation-free variant of the W4A16
@@ -263,12 +263,14 @@ nvfp4_status w4a16_lm_head_argmax(const void *x, int64_t M, int64_t K, const uin
 #define NVFP4_TOPK_MAX 128 /* largest k of w4a16_lm_head_topk */
 
 /*
- * Workspace bytes w4a16_lm_head_topk needs (0 for rejected shapes): those of
- * w4a16_lm_head_argmax plus the candidate store, M x N x 4 bytes (every
- * logit is a candidate at most once), 8 bytes per token and 32 rows of
- * candidate flags, and a 4,112-byte histogram per token (rounded up to the
- * token tile).  Only the candidates that reach their token's threshold are
- * ever written.
+ * Workspace bytes w4a16_lm_head_topk needs (0 for rejected shapes).  Up to
+ * 64 tokens and N <= 262144: those of w4a16_lm_head plus the fp32 logits,
+ * M x N x 4 bytes, and 4 bytes per token and 32 rows (their maxima).
+ * Otherwise: those of w4a16_lm_head_argmax plus the candidate store, M x N x
+ * 4 bytes (every logit is a candidate at most once), 8 bytes per token and
+ * 32 rows of candidate flags, and a 4,112-byte histogram per token (rounded
+ * up to the token tile); only the candidates that reach their token's
+ * threshold are ever written.
  */
 size_t w4a16_lm_head_topk_workspace_bytes(int64_t M, int64_t N, int64_t K, int64_t k);
 
@@ -280,11 +282,15 @@ size_t w4a16_lm_head_topk_workspace_bytes(int64_t M, int64_t N, int64_t K, int64
  * where the logits are bit for bit the fp32 values w4a16_lm_head writes with
  * NVFP4_OUT_F32 for the same inputs, with -0 and +0 equal (a zero is
  * returned as +0) and a NaN above every number, as in w4a16_lm_head_argmax
- * (whose answer is column 0 here).  The [M, N] logits are never written:
- * the epilogue keeps only the logits that reach the token's running
- * threshold, a lower bound of its k-th largest that rises with a histogram
- * of the candidates kept so far, and a second kernel selects the exact k
- * largest of those.  The result does not depend on the schedule.
+ * (whose answer is column 0 here).  Up to 64 tokens (N <= 262144) the
+ * product writes the fp32 logits and, per token, the largest of every 32
+ * rows into the workspace, and one CTA per token bounds its k-th largest
+ * logit from those maxima and ranks the few logits that reach the bound.
+ * Beyond, the [M, N] logits are never written: the epilogue keeps only the
+ * logits that reach the token's running threshold, a lower bound of its
+ * k-th largest that rises with a histogram of the candidates kept so far,
+ * and a second kernel selects the exact k largest of those.  The result
+ * does not depend on the route or the schedule.
  *
  * The pages define the logits, not a sampler; this is the top-k filter a
  * sampler applies to them, for the same reason as the argmax.
@@ -296,9 +302,10 @@ size_t w4a16_lm_head_topk_workspace_bytes(int64_t M, int64_t N, int64_t K, int64
  *   values       fp32 [M, k], device, 4-byte aligned, or NULL to skip.
  *   workspace    device, >= w4a16_lm_head_topk_workspace_bytes(M, N, K, k),
  *                256-byte aligned; no state is kept in it between calls.
- * Two kernels on `stream`, no host synchronisation; graph-capturable.  A
- * device-side timeout (NVFP4_ERR_TIMEOUT in the workspace status word)
- * leaves token_ids and values undefined.
+ * Three kernels on `stream` (activation prep, product, selection), no host
+ * synchronisation; graph-capturable.  A device-side timeout
+ * (NVFP4_ERR_TIMEOUT in the workspace status word) leaves token_ids and
+ * values undefined.
  */
 nvfp4_status w4a16_lm_head_topk(const void *x, int64_t M, int64_t K, const uint8_t *packed,
                                 const uint8_t *scales, const float *global_scale, int64_t N,
