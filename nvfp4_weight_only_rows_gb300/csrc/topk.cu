@@ -271,19 +271,21 @@ cudaError_t topk_select_launch(const unsigned long long* lines, const uint2* grp
 // consecutive rows); then one CTA per token selects:
 // 1. the super-group maxima: the largest of every sg consecutive group
 //    maxima, sg the widest power of two up to 32 that leaves at least 2k of
-//    them, or the narrowest that leaves at most 256 (at least k for k <=
-//    128 and N >= 32 k);
-// 2. the bound: the k-th largest super-group maximum.  Each super-group
-//    maximum is a logit of its own rows, so at least k logits reach the
-//    bound and the k-th largest logit is not below it;
+//    them, or the narrowest that leaves at most 256 (at least k of them
+//    whenever the token has k groups);
+// 2. the bound: the k-th largest super-group maximum (warp 0 sorts them in
+//    registers).  Each super-group maximum is a logit of its own rows, so
+//    at least k logits reach the bound and the k-th largest logit is not
+//    below it; with fewer than k groups the bound is 0 (every logit);
 // 3. the hot groups: those whose maximum reaches the bound (the others hold
 //    no logit that does);
 // 4. their logits that reach the bound (a few more than k: with s
-//    super-groups, about -s ln(1 - k / s)), ranked against each other.
+//    super-groups, about -s ln(1 - k / s)); up to 128 of them warp 0 sorts
+//    in registers, up to kRankCap the block ranks them against each other.
 // The keys (order key << 32 | ~row) are distinct, so the answer is that of
 // a sort of the fp32 logits, bit for bit.  A radix select over all N keys
 // takes over where more than kHotCap groups or kRankCap logits reach the
-// bound (heavily tied logits) or where N < 32 k.
+// bound (heavily tied logits, or a vocabulary of few groups).
 constexpr int kRankCap = 512;     // keys ranked against each other in shared memory
 constexpr int kDigitBits = 11;    // radix digit: 2048 bins (a quarter octave at the top)
 constexpr int kBins = 1 << kDigitBits;
