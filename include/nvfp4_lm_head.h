@@ -268,9 +268,10 @@ nvfp4_status w4a16_lm_head_argmax(const void *x, int64_t M, int64_t K, const uin
  * M x N x 4 bytes, and 4 bytes per token and 32 rows (their maxima).
  * Otherwise: those of w4a16_lm_head_argmax plus the candidate store, M x N x
  * 4 bytes (every logit is a candidate at most once), 8 bytes per token and
- * 32 rows of candidate flags, and a 4,112-byte histogram per token (rounded
- * up to the token tile); only the candidates that reach their token's
- * threshold are ever written.
+ * 32 rows of candidate flags, and per token a 4,112-byte histogram and a
+ * bitmap of one bit per 32 rows (rounded up to the token tile); only the
+ * candidates that reach their token's threshold, and their groups' flags,
+ * are ever written.
  */
 size_t w4a16_lm_head_topk_workspace_bytes(int64_t M, int64_t N, int64_t K, int64_t k);
 

@@ -107,7 +107,8 @@ __global__ void __launch_bounds__(256) w8a8_prep_x_kernel(const uint16_t* __rest
                                                           uint32_t* __restrict__ split_flags,
                                                           int n_split_flags,
                                                           unsigned long long* __restrict__ am_keys,
-                                                          uint32_t* __restrict__ tk_hist) {
+                                                          uint32_t* __restrict__ tk_hist,
+                                                          int tk_hstride) {
   // wait for the previous kernel in the stream (it may still read this
   // workspace), then let the GEMM launch: it streams the weights meanwhile
   asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -118,7 +119,7 @@ __global__ void __launch_bounds__(256) w8a8_prep_x_kernel(const uint16_t* __rest
     for (int i = threadIdx.x; i < n_split_flags; i += blockDim.x) split_flags[i] = 0;
   }
   const int64_t m = blockIdx.x;
-  token_state_clear(am_keys, tk_hist, m, threadIdx.x, blockDim.x);  // argmax / top-k
+  token_state_clear(am_keys, tk_hist, tk_hstride, m, threadIdx.x, blockDim.x);  // argmax / top-k
   uint8_t* dst = xq + m * K;
   if (m >= M) {  // padding tokens of the last tile
     for (int64_t i = threadIdx.x; i < K / 16; i += blockDim.x)
@@ -411,7 +412,8 @@ static nvfp4_status w8a8_run(const void* x, int64_t M, int64_t K, const uint8_t*
     if (cudaLaunchKernelEx(&l.cfg, w8a8_prep_x_kernel, static_cast<const uint16_t*>(x), M, K, xq,
                            tok_scale, status, reinterpret_cast<uint32_t*>(ws + L.cnt),
                            (int)((L.part - L.cnt) / 4), keys,
-                           topk ? reinterpret_cast<uint32_t*>(ws + L.hist) : nullptr) != cudaSuccess)
+                           topk ? reinterpret_cast<uint32_t*>(ws + L.hist) : nullptr,
+                           topk ? topk_hist_stride(N) : 0) != cudaSuccess)
       return NVFP4_ERR_CUDA;
   }
 
@@ -458,8 +460,8 @@ static nvfp4_status w8a8_run(const void* x, int64_t M, int64_t K, const uint8_t*
                : (small ? launch_w8a8<kOutTopk, 4>(tm_w, tm_x, a, grid, stream)
                         : launch_w8a8<kOutTopk, 3>(tm_w, tm_x, a, grid, stream));
     if (err == cudaSuccess)
-      err = topk_select_launch(a.am_keys, a.tk_grp, a.tk_cand, M, N, topk_k, token_ids,
-                               max_logits, stream);
+      err = topk_select_launch(a.am_keys, a.tk_grp, a.tk_cand, a.tk_hist, a.tk_hstride, M, N,
+                               topk_k, token_ids, max_logits, stream);
   } else if (wide && out_mode == NVFP4_OUT_BF16)
     err = launch_w8a8<NVFP4_OUT_BF16, 4, 128, kWideBN>(tm_w, tm_x, a, grid, stream);
   else if (wide)

@@ -62,7 +62,10 @@ struct GemmArgs {
   uint2* tk_grp;                // [M][tk_groups] per 32 rows: {largest candidate order key,
                                 //   bit j: slot 32g + j holds a candidate}
   int64_t tk_groups;            // ceil(N / 32)
-  uint32_t* tk_hist;            // [m_pad][kHistWords] histograms of the candidate keys
+  uint32_t* tk_hist;            // [m_pad][tk_hstride] per token: the histogram of the
+                                //   candidate keys (kHistWords), then one bit per group
+                                //   whose word this call wrote
+  int tk_hstride;               // u32 per token in tk_hist
   int tk_k;                     // k, 1 .. kTopkMax
   const float* row_scale;       // [N] per-row weight scale (fp8 weights), else null
   // output mode kOutLogitsGroups only: per token, the largest order key
@@ -321,10 +324,12 @@ __device__ __forceinline__ float key_value(uint32_t k) {
 // candidate key, so every one of its k largest logits reaches it), the
 // largest candidate order key, a histogram of candidate order keys and the
 // candidates themselves: the order key of a logit that reached T sits in
-// slot n of the token's N slots (the row is the slot).  Per token and group of 32 rows, the warp that
-// owns the group writes {largest candidate order key, bitmap of the slots
-// it filled} ({0, 0} without candidates), so the groups are complete
-// without clearing and the selection skips every group below its final T.
+// slot n of the token's N slots (the row is the slot).  Per token and group
+// of 32 rows that holds candidates, the warp that owns the group writes
+// {largest candidate order key, bitmap of the slots it filled} and sets the
+// group's bit in the token's group bitmap (cleared with the histogram by
+// the prep kernel): groups without candidates are neither written nor read,
+// and the selection skips every group below its final T.
 // Histogram bins: all negative keys; positive keys below 2^-32; a
 // sixteenth of an octave each from 2^-32 to 2^32 (exponent and top 4
 // mantissa bits); 2^32 and above.  A candidate within a quarter of an
@@ -337,7 +342,14 @@ __device__ __forceinline__ float key_value(uint32_t k) {
 // bin's lower edge: at least k candidates of the token reach it (counts and
 // the maximum only ever lag, which lowers the edge, never invalidates it).
 constexpr int kHistBins = 1027;
-constexpr int kHistWords = 1028;  // u32 per token (whole 16-byte vectors)
+constexpr int kHistWords = 1028;  // u32 of a token's histogram (whole 16-byte vectors)
+
+// u32 per token of the histogram region: the histogram, then the group
+// bitmap (one bit per 32 rows), padded to whole 16-byte vectors.
+static inline int topk_hist_stride(int64_t N) {
+  const int64_t words = ((N + 31) / 32 + 31) / 32;
+  return kHistWords + (int)((words + 3) / 4 * 4);
+}
 
 __host__ __device__ __forceinline__ uint32_t topk_bin(uint32_t ok) {
   if (ok < 0x80000000u) return 0u;
@@ -365,6 +377,9 @@ __device__ __forceinline__ uint32_t* topk_max(const GemmArgs& p, int64_t tok) {
 __device__ __forceinline__ void red_add_u32(uint32_t* a, uint32_t v) {
   asm volatile("red.relaxed.gpu.global.add.u32 [%0], %1;" ::"l"(a), "r"(v) : "memory");
 }
+__device__ __forceinline__ void red_or_u32(uint32_t* a, uint32_t v) {
+  asm volatile("red.relaxed.gpu.global.or.b32 [%0], %1;" ::"l"(a), "r"(v) : "memory");
+}
 __device__ __forceinline__ void red_max_u32(uint32_t* a, uint32_t v) {
   asm volatile("red.relaxed.gpu.global.max.u32 [%0], %1;" ::"l"(a), "r"(v) : "memory");
 }
@@ -373,7 +388,7 @@ __device__ __forceinline__ void red_max_u32(uint32_t* a, uint32_t v) {
 // holds its k-th largest counted candidate (whole warp): 32 bins per step,
 // downwards from the bin of the largest candidate key.
 __device__ __forceinline__ void topk_raise(const GemmArgs& p, int64_t tok, int lane) {
-  const uint32_t* h = p.tk_hist + tok * kHistWords;
+  const uint32_t* h = p.tk_hist + tok * p.tk_hstride;
   int hi = (int)topk_bin(__ldcg(topk_max(p, tok)));
   uint32_t need = (uint32_t)p.tk_k;
 #pragma unroll 1
@@ -446,28 +461,33 @@ __device__ __forceinline__ void topk_chunk(const GemmArgs& p, int64_t tc, int64_
         // a quarter of an exponent step below the group's largest: lower
         // candidates are not counted
         const uint32_t floor = mx >= 0x80200000u ? mx - 0x00200000u : 0u;
-        if (ok >= floor) red_add_u32(p.tk_hist + tok * kHistWords + topk_bin(ok), 1u);
+        if (ok >= floor) red_add_u32(p.tk_hist + tok * p.tk_hstride + topk_bin(ok), 1u);
       }
     }
     if (my_bal) red_max_u32(topk_max(p, tc + lane), my_mx);  // lane t < 16, live tokens only
   }
-  const int64_t my_tok = tc + lane;
-  if (lane < 16 && my_tok < t_end && (int64_t)n_base < p.N)
-    p.tk_grp[my_tok * p.tk_groups + (n_base >> 5)] = make_uint2(my_mx, my_bal);
+  // lane t < 16 holds token t's group word (my_bal != 0: live token with candidates)
+  if (my_bal) {
+    const int64_t my_tok = tc + lane;
+    const uint32_t g = n_base >> 5;
+    p.tk_grp[my_tok * p.tk_groups + g] = make_uint2(my_mx, my_bal);
+    red_or_u32(p.tk_hist + my_tok * p.tk_hstride + kHistWords + (g >> 5), 1u << (g & 31));
+  }
 }
 
 // The prep kernels' clearing of token m's argmax / top-k state (thread
 // `tid` of `nthreads` working on the token): the line's maximum or
-// threshold and the largest candidate key, and the top-k histogram.
+// threshold and the largest candidate key, and the top-k histogram and
+// group bitmap (hstride u32, a multiple of 4).
 __device__ __forceinline__ void token_state_clear(unsigned long long* am_keys, uint32_t* tk_hist,
-                                                  int64_t m, int tid, int nthreads) {
+                                                  int hstride, int64_t m, int tid, int nthreads) {
   if (am_keys && tid == 0) {
     am_keys[m * kKeyStride] = 0ull;
     am_keys[m * kKeyStride + 2] = 0ull;
   }
   if (tk_hist) {
-    uint4* h = reinterpret_cast<uint4*>(tk_hist + m * kHistWords);
-    for (int i = tid; i < kHistWords / 4; i += nthreads) h[i] = make_uint4(0, 0, 0, 0);
+    uint4* h = reinterpret_cast<uint4*>(tk_hist + m * hstride);
+    for (int i = tid; i < hstride / 4; i += nthreads) h[i] = make_uint4(0, 0, 0, 0);
   }
 }
 
@@ -883,7 +903,7 @@ static inline WsLayout ws_layout(int64_t M, int64_t N, int64_t K, int sms, bool 
   l.part = l.done + (keys ? 256 : 0);
   l.keys = l.part + align_up((size_t)l.grid * 4 * BN * 32 * 4, 256);
   l.hist = l.keys + (keys ? (size_t)m_pad * kKeyStride * 8 : 0);
-  l.grp = l.hist + (topk_k > 0 ? (size_t)m_pad * kHistWords * 4 : 0);
+  l.grp = l.hist + (topk_k > 0 ? (size_t)m_pad * topk_hist_stride(N) * 4 : 0);
   l.cand = l.grp + (topk_k > 0 ? align_up((size_t)M * ((N + 31) / 32) * 8, 256) : 0);
   l.total = l.cand + (topk_k > 0 ? (size_t)M * N * 4 : 0);
   return l;
@@ -952,8 +972,8 @@ static inline bool topk_logits_fits(int64_t N) { return N <= kTopkLogitsMaxN; }
 
 // The top-k selection kernel (topk.cu), launched after a top-k GEMM.
 cudaError_t topk_select_launch(const unsigned long long* lines, const uint2* grp,
-                               const uint32_t* cand, int64_t M, int64_t N, int k, int64_t* ids,
-                               float* vals, cudaStream_t stream);
+                               const uint32_t* cand, const uint32_t* hist, int hstride, int64_t M,
+                               int64_t N, int k, int64_t* ids, float* vals, cudaStream_t stream);
 
 // The top-k arguments of a GEMM whose workspace follows layout L.
 static inline void topk_args(GemmArgs& a, uint8_t* ws, const WsLayout& L, int k, int64_t N) {
@@ -961,6 +981,7 @@ static inline void topk_args(GemmArgs& a, uint8_t* ws, const WsLayout& L, int k,
   a.tk_hist = reinterpret_cast<uint32_t*>(ws + L.hist);
   a.tk_grp = reinterpret_cast<uint2*>(ws + L.grp);
   a.tk_groups = (N + 31) / 32;
+  a.tk_hstride = topk_hist_stride(N);
   a.tk_k = k;
 }
 

@@ -83,6 +83,7 @@ __global__ void __launch_bounds__(256) w4a16_prep_x_kernel(const uint16_t* __res
                                                            int n_split_flags,
                                                            unsigned long long* __restrict__ am_keys,
                                                            uint32_t* __restrict__ tk_hist,
+                                                           int tk_hstride,
                                                            const int32_t* __restrict__ grp_off,
                                                            const float* __restrict__ grp_global,
                                                            int n_groups) {
@@ -106,7 +107,7 @@ __global__ void __launch_bounds__(256) w4a16_prep_x_kernel(const uint16_t* __res
   const int lane = threadIdx.x % kT;
   const int64_t m = (int64_t)blockIdx.x * (blockDim.x / kT) + threadIdx.x / kT;
   if (m >= m_rows) return;  // uniform over the row's threads
-  token_state_clear(am_keys, tk_hist, m, lane, kT);  // argmax / top-k: nothing seen yet
+  token_state_clear(am_keys, tk_hist, tk_hstride, m, lane, kT);  // argmax / top-k: nothing seen yet
   uint4* d4 = reinterpret_cast<uint4*>(x16 + m * K);
   const int64_t nv = K / 8;
   if (m >= M) {  // padding rows of the last token tile
@@ -670,7 +671,7 @@ static nvfp4_status lm_head_run(const void* x, int64_t M, int64_t K, const uint8
                            (int)((L.part - L.cnt) / 4),
                            keys ? reinterpret_cast<unsigned long long*>(ws + L.keys) : nullptr,
                            topk ? reinterpret_cast<uint32_t*>(ws + L.hist) : nullptr,
-                           nullptr, nullptr, 0) != cudaSuccess)
+                           topk ? topk_hist_stride(N) : 0, nullptr, nullptr, 0) != cudaSuccess)
       return NVFP4_ERR_CUDA;
   }
 
@@ -719,8 +720,8 @@ static nvfp4_status lm_head_run(const void* x, int64_t M, int64_t K, const uint8
     err = deep ? launch_gemm<kOutTopk, 3, 6, 3>(tm_packed, tm_scales, tm_x, a, grid, stream)
                : launch_gemm<kOutTopk, 2, 4, 2>(tm_packed, tm_scales, tm_x, a, grid, stream);
     if (err == cudaSuccess)
-      err = topk_select_launch(a.am_keys, a.tk_grp, a.tk_cand, M, N, topk_k, token_ids,
-                               max_logits, stream);
+      err = topk_select_launch(a.am_keys, a.tk_grp, a.tk_cand, a.tk_hist, a.tk_hstride, M, N,
+                               topk_k, token_ids, max_logits, stream);
   } else if (out_mode == NVFP4_OUT_BF16)
     err = deep ? launch_gemm<NVFP4_OUT_BF16, 3, 6, 3>(tm_packed, tm_scales, tm_x, a, grid, stream)
                : launch_gemm<NVFP4_OUT_BF16, 2, 4, 2>(tm_packed, tm_scales, tm_x, a, grid, stream);
@@ -807,7 +808,7 @@ nvfp4_status grouped_launch(const void* x, int64_t M, int64_t K, const int32_t* 
                            static_cast<const uint16_t*>(x), M, K, M,
                            (const float*)nullptr, x16, tok_scale, status,
                            reinterpret_cast<uint32_t*>(ws + L.cnt), (int)((L.part - L.cnt) / 4),
-                           (unsigned long long*)nullptr, (uint32_t*)nullptr,
+                           (unsigned long long*)nullptr, (uint32_t*)nullptr, 0,
                            grp_off, grp_global,
                            (int)n_groups) != cudaSuccess)
       return NVFP4_ERR_CUDA;

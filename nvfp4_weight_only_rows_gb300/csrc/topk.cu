@@ -1,7 +1,9 @@
 // topk.cu -- the selection step of the fused top-k: the GEMM epilogue has
 // kept, per token, every logit that reached the token's running threshold
 // (a superset of its k largest; the order key of row n in slot n, flagged
-// in the word of its 32-row group); here one CTA per token picks the exact k
+// in the word of its 32-row group, a word written only for groups with
+// candidates and marked in the token's group bitmap); here one CTA per
+// token picks the exact k
 // largest candidate keys, sorts them (larger logit first, of equal logits
 // the smaller row; a NaN above every number) and writes their rows and
 // logits.
@@ -24,11 +26,13 @@ constexpr int kRankMax = 512;  // at most this many keys: selection by rank (one
 // Every candidate key of one token at or above T, through the group words,
 // one thread at a time (the overflow path only).
 template <typename F>
-__device__ __noinline__ void topk_scan_slow(const uint2* gw, const uint32_t* src, int64_t G,
-                                            int64_t N, unsigned long long T, F f) {
+__device__ __noinline__ void topk_scan_slow(const uint2* gw, const uint32_t* gbits,
+                                            const uint32_t* src, int64_t G, int64_t N,
+                                            unsigned long long T, F f) {
   const uint32_t t_hi = (uint32_t)(T >> 32);
 #pragma unroll 1
   for (int64_t g = threadIdx.x; g < G; g += blockDim.x) {
+    if (((__ldcg(gbits + (g >> 5)) >> (g & 31)) & 1u) == 0u) continue;  // no word this call
     const uint2 w = __ldcg(gw + g);
     if (w.x < t_hi) continue;
     uint32_t bits = w.y;
@@ -47,8 +51,8 @@ __device__ __noinline__ void topk_scan_slow(const uint2* gw, const uint32_t* src
 
 __global__ void __launch_bounds__(kSelThreads) topk_select_kernel(
     const unsigned long long* __restrict__ lines, const uint2* __restrict__ grp,
-    const uint32_t* __restrict__ cand, int64_t N, int k, int64_t* __restrict__ ids,
-    float* __restrict__ vals) {
+    const uint32_t* __restrict__ cand, const uint32_t* __restrict__ tk_hist, int hstride,
+    int64_t N, int k, int64_t* __restrict__ ids, float* __restrict__ vals) {
   // the candidates come from the GEMM, which may still be running
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -64,6 +68,8 @@ __global__ void __launch_bounds__(kSelThreads) topk_select_kernel(
   const uint32_t t_hi = (uint32_t)(T >> 32);  // key >= T  <=>  order key >= t_hi
   const int64_t G = (N + 31) / 32;
   const uint2* gw = grp + tok * G;
+  const uint32_t* gbits = tk_hist + tok * hstride + kHistWords;  // groups with a word this call
+  const int64_t GB = (G + 31) / 32;
   const uint32_t* src = cand + tok * N;
   if (tid == 0) {
     s_n = 0;
@@ -74,17 +80,22 @@ __global__ void __launch_bounds__(kSelThreads) topk_select_kernel(
   __syncthreads();
 
   // 1. the candidates at or above T, into shared memory while they fit:
-  // each lane loads kGW group words at once (a warp covers 32 x kGW
-  // groups) and keeps a mask of those whose largest candidate reaches T;
+  // lane u < kGW loads the bitmap word of the warp's groups 32 u .. 32 u +
+  // 31, then each lane loads the words of its kGW groups that have one (a
+  // warp covers 32 x kGW groups) and keeps a mask of those whose largest
+  // candidate reaches T;
   // then, kSelU groups at a time, the warp loads their flagged slots
   // (lane l: slot 32g + l) and appends the keys that reach T
   for (int64_t g0 = (int64_t)warp * 32 * kGW; g0 < G; g0 += (int64_t)n_warps * 32 * kGW) {
     uint32_t bits[kGW];
     uint32_t pass = 0;  // bit u: group g0 + 32u + lane has a candidate at or above T
+    const int64_t bw = (g0 >> 5) + lane;
+    const uint32_t my_bm = lane < kGW && bw < GB ? __ldcg(gbits + bw) : 0u;
 #pragma unroll
     for (int u = 0; u < kGW; ++u) {
       const int64_t g = g0 + u * 32 + lane;
-      const uint2 w = g < G ? __ldcg(gw + g) : make_uint2(0u, 0u);
+      const bool has = (__shfl_sync(0xFFFFFFFFu, my_bm, u) >> lane) & 1u;
+      const uint2 w = has ? __ldcg(gw + g) : make_uint2(0u, 0u);
       bits[u] = w.y;
       if (w.y != 0u && w.x >= t_hi) pass |= 1u << u;
     }
@@ -169,7 +180,7 @@ __global__ void __launch_bounds__(kSelThreads) topk_select_kernel(
     if (in_smem) {
       for (uint32_t i = tid; i < m; i += blockDim.x) count(s_keys[i]);
     } else {
-      topk_scan_slow(gw, src, G, N, T, count);
+      topk_scan_slow(gw, gbits, src, G, N, T, count);
     }
     __syncthreads();
     if (warp == 0) {
@@ -225,7 +236,7 @@ __global__ void __launch_bounds__(kSelThreads) topk_select_kernel(
   if (in_smem) {
     for (uint32_t i = tid; i < m; i += blockDim.x) collect(s_keys[i]);
   } else {
-    topk_scan_slow(gw, src, G, N, T, collect);
+    topk_scan_slow(gw, gbits, src, G, N, T, collect);
   }
   __syncthreads();
 
@@ -253,15 +264,16 @@ __global__ void __launch_bounds__(kSelThreads) topk_select_kernel(
 }
 
 cudaError_t topk_select_launch(const unsigned long long* lines, const uint2* grp,
-                               const uint32_t* cand, int64_t M, int64_t N, int k, int64_t* ids,
-                               float* vals, cudaStream_t stream) {
+                               const uint32_t* cand, const uint32_t* hist, int hstride, int64_t M,
+                               int64_t N, int k, int64_t* ids, float* vals, cudaStream_t stream) {
   const size_t smem = (size_t)kSelCap * sizeof(unsigned long long);
   static std::atomic<uint64_t> limit_set{0};
   const cudaError_t attr_err =
       smem_limit_once(limit_set, reinterpret_cast<const void*>(topk_select_kernel), smem);
   if (attr_err != cudaSuccess) return attr_err;
   PdlLaunch l(dim3((unsigned)M), dim3(kSelThreads), smem, stream);
-  return cudaLaunchKernelEx(&l.cfg, topk_select_kernel, lines, grp, cand, N, k, ids, vals);
+  return cudaLaunchKernelEx(&l.cfg, topk_select_kernel, lines, grp, cand, hist, hstride, N, k,
+                            ids, vals);
 }
 
 // ------------------------------------------------------------ from logits

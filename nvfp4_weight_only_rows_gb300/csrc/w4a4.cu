@@ -76,7 +76,7 @@ __global__ void __launch_bounds__(256) w4a4_prep_x_kernel(
     const float* __restrict__ g_in, const float* __restrict__ g_w, uint8_t* __restrict__ xq,
     uint8_t* __restrict__ xsf, float* __restrict__ tok_scale, int32_t* __restrict__ status,
     uint32_t* __restrict__ split_flags, int n_split_flags, unsigned long long* __restrict__ am_keys,
-    uint32_t* __restrict__ tk_hist) {
+    uint32_t* __restrict__ tk_hist, int tk_hstride) {
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (blockIdx.x == 0) {
@@ -93,7 +93,8 @@ __global__ void __launch_bounds__(256) w4a4_prep_x_kernel(
     if (m == 0 && !(g > 0.0f && g < __int_as_float(0x7F800000)))
       raise_status(status, NVFP4_ERR_NONFINITE);  // the input global must be positive and finite
   }
-  if (m < m_pad) token_state_clear(am_keys, tk_hist, m, threadIdx.x, blockDim.x);  // argmax / top-k
+  if (m < m_pad)  // argmax / top-k
+    token_state_clear(am_keys, tk_hist, tk_hstride, m, threadIdx.x, blockDim.x);
   const float ig = __frcp_rn(g);
   const float inv6 = 1.0f / 6.0f;
   for (int64_t c = threadIdx.x; c < kbp; c += blockDim.x) {
@@ -427,8 +428,8 @@ static nvfp4_status w4a4_run(const void* x, int64_t M, int64_t K, const uint8_t*
     if (cudaLaunchKernelEx(&l.cfg, w4a4_prep_x_kernel, static_cast<const uint16_t*>(x), M, K,
                            m_pad, g_in, g_w, xq, xsf, tok_scale, status,
                            reinterpret_cast<uint32_t*>(ws + L.cnt), (int)((L.part - L.cnt) / 4),
-                           keys, topk ? reinterpret_cast<uint32_t*>(ws + L.hist) : nullptr) !=
-        cudaSuccess)
+                           keys, topk ? reinterpret_cast<uint32_t*>(ws + L.hist) : nullptr,
+                           topk ? topk_hist_stride(N) : 0) != cudaSuccess)
       return NVFP4_ERR_CUDA;
   }
 
@@ -471,8 +472,8 @@ static nvfp4_status w4a4_run(const void* x, int64_t M, int64_t K, const uint8_t*
     err = small ? launch_w4a4<kOutTopk, 6>(tm_w, tm_x, wsf, xsf, a, grid, stream)
                 : launch_w4a4<kOutTopk, 5>(tm_w, tm_x, wsf, xsf, a, grid, stream);
     if (err == cudaSuccess)
-      err = topk_select_launch(a.am_keys, a.tk_grp, a.tk_cand, M, N, topk_k, token_ids,
-                               max_logits, stream);
+      err = topk_select_launch(a.am_keys, a.tk_grp, a.tk_cand, a.tk_hist, a.tk_hstride, M, N,
+                               topk_k, token_ids, max_logits, stream);
   } else if (out_mode == NVFP4_OUT_BF16)
     err = small ? launch_w4a4<NVFP4_OUT_BF16, 6>(tm_w, tm_x, wsf, xsf, a, grid, stream)
                 : launch_w4a4<NVFP4_OUT_BF16, 5>(tm_w, tm_x, wsf, xsf, a, grid, stream);
