@@ -22,8 +22,9 @@
  *
  * Around them, in the order of the sections below: the greedy argmax and
  * the top-k of those logits fused into the product (the logits are written
- * only to the workspace, and only up to 64 tokens); the "fp8" lm_head copy (per-row E4M3 weights, W8A8 product) of
- * `quantized_lm_head_copy` on the first page; the grouped W4A16 product of
+ * only to the workspace, and only up to 256 tokens); the "fp8" lm_head copy
+ * (per-row E4M3 weights, W8A8 product) of `quantized_lm_head_copy` on the
+ * first page; the grouped W4A16 product of
  * all experts of an NVFP4 MoE layer; the W4A4 NVFP4 product of
  * `CompressedTensorsW4A4Fp4`; an allocation-free variant of the W4A16
  * product; and two self-tests.
@@ -264,7 +265,7 @@ nvfp4_status w4a16_lm_head_argmax(const void *x, int64_t M, int64_t K, const uin
 
 /*
  * Workspace bytes w4a16_lm_head_topk needs (0 for rejected shapes).  Up to
- * 64 tokens and N <= 262144: those of w4a16_lm_head plus the fp32 logits,
+ * 256 tokens and N <= 262144: those of w4a16_lm_head plus the fp32 logits,
  * M x N x 4 bytes, and 4 bytes per token and 32 rows (their maxima).
  * Otherwise: those of w4a16_lm_head_argmax plus the candidate store, M x N x
  * 4 bytes (every logit is a candidate at most once), 8 bytes per token and
@@ -283,7 +284,7 @@ size_t w4a16_lm_head_topk_workspace_bytes(int64_t M, int64_t N, int64_t K, int64
  * where the logits are bit for bit the fp32 values w4a16_lm_head writes with
  * NVFP4_OUT_F32 for the same inputs, with -0 and +0 equal (a zero is
  * returned as +0) and a NaN above every number, as in w4a16_lm_head_argmax
- * (whose answer is column 0 here).  Up to 64 tokens (N <= 262144) the
+ * (whose answer is column 0 here).  Up to 256 tokens (N <= 262144) the
  * product writes the fp32 logits and, per token, the largest of every 32
  * rows into the workspace, and one CTA per token bounds its k-th largest
  * logit from those maxima and ranks the few logits that reach the bound.

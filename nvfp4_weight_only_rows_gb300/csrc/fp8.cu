@@ -448,8 +448,9 @@ static nvfp4_status w8a8_run(const void* x, int64_t M, int64_t K, const uint8_t*
   const int grid = L.grid;
   const bool small = BN <= 64;
   cudaError_t err;
-  if (topk_logits)  // up to 64 tokens: a small tile
-    err = launch_w8a8<kOutLogitsGroups, 4>(tm_w, tm_x, a, grid, stream);
+  if (topk_logits)
+    err = small ? launch_w8a8<kOutLogitsGroups, 4>(tm_w, tm_x, a, grid, stream)
+                : launch_w8a8<kOutLogitsGroups, 3>(tm_w, tm_x, a, grid, stream);
   else if (argmax && wide)
     err = launch_w8a8<kOutArgmax, 4, 128, kWideBN>(tm_w, tm_x, a, grid, stream);
   else if (argmax)

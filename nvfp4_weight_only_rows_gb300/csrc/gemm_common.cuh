@@ -943,12 +943,14 @@ cudaError_t stage_rows_launch(const uint8_t* src, int64_t rows, int64_t row_byte
                               int64_t dst_stride, cudaStream_t stream);
 
 // Up to this many tokens a top-k call writes the fp32 logits (at most
-// 64 x N x 4 bytes, a tenth of the weight bytes) and the per-token maxima of
-// every 32 rows, and selects from them (topk.cu, topk_logits_launch);
-// beyond, the GEMM keeps thresholded candidates in its epilogue and
-// topk_select_launch picks from those.
-constexpr int64_t kTopkLogitsMaxM = 64;
-static_assert(kTopkLogitsMaxM <= 64, "the logits route launches the decode-tile GEMM shapes only");
+// 256 x N x 4 bytes, under half the weight bytes of a 4096-wide head) and
+// the per-token maxima of every 32 rows, and selects from them (topk.cu,
+// topk_logits_launch); beyond, the GEMM keeps thresholded candidates in its
+// epilogue and topk_select_launch picks from those, so that a prefill never
+// writes its logits.  (Same-box, k = 50 over 128256 rows: the candidate
+// route took 104 / 123 / 149 / 243 us at 65 / 96 / 128 / 256 tokens
+// against 73 / 81 / 96 / 171 us for the fp32 logits alone.)
+constexpr int64_t kTopkLogitsMaxM = 256;
 // The selecting CTA holds a token's group maxima in registers: vocabularies
 // up to this many rows take the logits route.
 constexpr int64_t kTopkLogitsMaxN = 32 * 8192;

@@ -711,8 +711,9 @@ static nvfp4_status lm_head_run(const void* x, int64_t M, int64_t K, const uint8
   // programmatic dependent launch: the GEMM starts streaming weights while
   // the prep kernel is still running
   cudaError_t err;
-  if (topk_logits)  // up to 64 tokens: the decode shape
-    err = launch_gemm<kOutLogitsGroups, 3, 6, 3>(tm_packed, tm_scales, tm_x, a, grid, stream);
+  if (topk_logits)
+    err = deep ? launch_gemm<kOutLogitsGroups, 3, 6, 3>(tm_packed, tm_scales, tm_x, a, grid, stream)
+               : launch_gemm<kOutLogitsGroups, 2, 4, 2>(tm_packed, tm_scales, tm_x, a, grid, stream);
   else if (argmax)
     err = deep ? launch_gemm<kOutArgmax, 3, 6, 3>(tm_packed, tm_scales, tm_x, a, grid, stream)
                : launch_gemm<kOutArgmax, 2, 4, 2>(tm_packed, tm_scales, tm_x, a, grid, stream);

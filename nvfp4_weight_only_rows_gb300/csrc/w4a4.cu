@@ -463,8 +463,9 @@ static nvfp4_status w4a4_run(const void* x, int64_t M, int64_t K, const uint8_t*
   if (topk) topk_args(a, ws, L, topk_k, N);
   const int grid = L.grid;
   cudaError_t err;
-  if (topk_logits)  // up to 64 tokens: a small tile
-    err = launch_w4a4<kOutLogitsGroups, 6>(tm_w, tm_x, wsf, xsf, a, grid, stream);
+  if (topk_logits)
+    err = small ? launch_w4a4<kOutLogitsGroups, 6>(tm_w, tm_x, wsf, xsf, a, grid, stream)
+                : launch_w4a4<kOutLogitsGroups, 5>(tm_w, tm_x, wsf, xsf, a, grid, stream);
   else if (argmax)
     err = small ? launch_w4a4<kOutArgmax, 6>(tm_w, tm_x, wsf, xsf, a, grid, stream)
                 : launch_w4a4<kOutArgmax, 5>(tm_w, tm_x, wsf, xsf, a, grid, stream);

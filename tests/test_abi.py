@@ -187,10 +187,10 @@ def test_topk_host_argument_errors_and_sizes(lib):
              None) == 2                                                                   # ALIGN ids
     sz = lib.w4a16_lm_head_topk_workspace_bytes
     assert sz(4, 0, 256, 1) == 0 and sz(4, 100, 256, 0) == 0 and sz(4, 100, 256, 129) == 0
-    for M in (1, 32, 64, 2048):
+    for M in (1, 32, 64, 256, 257, 2048):
         am = lib.w4a16_lm_head_argmax_workspace_bytes(M, 128256, 4096)
         tk = sz(M, 128256, 4096, 50)
-        if M <= 64:  # fp32 logits and the u32 maximum of every 32 rows
+        if M <= 256:  # fp32 logits and the u32 maximum of every 32 rows
             plain = lib.w4a16_lm_head_workspace_bytes(M, 128256, 4096)
             assert tk >= plain + M * 128256 * 4 + M * (128256 // 32) * 4
         else:        # candidate slots, group words and histograms of the epilogue route

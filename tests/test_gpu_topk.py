@@ -104,10 +104,11 @@ def test_first_column_is_the_argmax():
     assert torch.equal(vals[:, 0], a_vals)
 
 
-# Up to 64 tokens the call writes the fp32 logits and their 32-row maxima
-# and one CTA per token selects from them; more tokens keep thresholded
-# candidates in the GEMM epilogue: the cases below run both routes.
-ROUTES = [1, 5, 9, 70]
+# Up to 256 tokens the call writes the fp32 logits and their 32-row maxima
+# and one CTA per token selects from them (64 tokens and fewer on the
+# decode-tile GEMM, more on the 128-token tile); more tokens keep
+# thresholded candidates in the GEMM epilogue: the cases below run all three.
+ROUTES = [1, 5, 70, 300]
 
 
 @pytest.mark.parametrize("M", ROUTES)
@@ -156,10 +157,10 @@ def test_rising_logits(M):
 @pytest.mark.parametrize("M", ROUTES)
 def test_large_logits_clustered_by_row_residue(M):
     """50 large logit values, each repeated on every row with the same
-    residue mod 256 (16 copies in each 4096-row chunk, all in one thread of
-    the selection from logits): equal values crowd the top bins of every
-    chunk and of the merge, and the k largest must still come out by value,
-    then by row."""
+    residue mod 256: equal values fill the largest group and super-group
+    maxima of the selection from logits and the top histogram bins of the
+    candidate route, and the k largest must still come out by value, then
+    by row."""
     N, K = 2 * 4096 + 300, 256
     x = synth.decode_x(M, K=K)
     xf = synth.bf16_bits_to_f32(x)
@@ -172,7 +173,7 @@ def test_large_logits_clustered_by_row_residue(M):
         assert_oracle_agrees(ids[:1], vals[:1], oracle.logits(x[:1], *host_q))
 
 
-@pytest.mark.parametrize("M", [3, 70])
+@pytest.mark.parametrize("M", [3, 70, 300])
 def test_negative_nan_and_zero_tokens(M):
     """All-negative logits, a NaN token (every logit NaN: rows 0 .. k-1, all
     values NaN) and an all-zero token (rows 0 .. k-1, values +0)."""
