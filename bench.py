@@ -386,7 +386,8 @@ def run_ours(args, world, rank, local):
     g_am = {M: [capture(lambda M=M, c=c: nv.w4a16_lm_head_argmax(
         x_am[M], *copies[c], token_ids=am_ids[M], max_logits=am_vals[M], workspace=aws))
         for c in range(2)] for M in x_am}
-    # the fused top-k (k largest logits per token, logits never stored), each call alone
+    # the fused top-k (k largest logits per token, logits kept in the workspace up to 256
+    # tokens and never stored beyond), each call alone
     tk_ids = {M: torch.empty((M, TOPK_K), dtype=torch.int64, device=dev) for M in x_am}
     tk_vals = {M: torch.empty((M, TOPK_K), dtype=torch.float32, device=dev) for M in x_am}
     tkws = torch.empty(nv.w4a16_lm_head_topk_workspace_bytes(PREFILL_M, N, K, TOPK_K),
@@ -589,7 +590,8 @@ def run_ours(args, world, rank, local):
         "frac": round(tk_tflops / peaks["bf16_tflops"], 4), "traffic": traffic.get("topk_prefill"),
         "peak_source": peaks["source"] + " dense bf16 burst (fp16 MMA, same rate)"}
     topk_part = {
-        "what": f"fused top-k, k={TOPK_K} (rows + logits of each token's k largest, logits not "
+        "what": f"fused top-k, k={TOPK_K} (rows + logits of each token's k largest; up to 256 "
+                "tokens the fp32 logits go to the workspace only, beyond that they are never "
                 "stored); each call alone from its own CUDA graph, not part of the timed step",
         "us_per_call_alone": {str(M): round(per_call_tk[M], 2) for M in x_am},
         "rooflines": tk_roofs,
