@@ -163,6 +163,17 @@ nvfp4_status nvfp4_selftest_bounded_wait(void *workspace, size_t workspace_bytes
  */
 int64_t nvfp4_selftest_topk_bins(void);
 
+/*
+ * Host-only check of the persistent products' work split: for a spread of
+ * unit counts, grids, stages per unit and tail skews, the whole-unit waves
+ * and the stream-K tail cover every stage exactly once, the tail ranges are
+ * contiguous and at least one unit long, no unit is cut more than once (the
+ * pairwise combine of a cut unit's partials relies on it), and an unskewed
+ * tail is the even split.  Returns -1 when every case passes, else the
+ * index of the first failing case.  Runs on the CPU; needs no GPU.
+ */
+int64_t nvfp4_selftest_schedule(void);
+
 /* --------------------------------------------------------- W4A16 GEMM */
 
 /*

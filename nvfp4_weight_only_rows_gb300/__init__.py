@@ -49,7 +49,8 @@ __all__ = [
     "nvfp4_refresh", "w4a16_lm_head", "nvfp4_quantize_workspace_bytes",
     "w4a16_lm_head_workspace_bytes", "nvfp4_read_device_status", "w4a16_lm_head_noalloc",
     "w4a16_lm_head_noalloc_status",
-    "nvfp4_selftest_bounded_wait", "nvfp4_selftest_topk_bins", "OUT_F32", "OUT_BF16", "w4a16_lm_head_argmax",
+    "nvfp4_selftest_bounded_wait", "nvfp4_selftest_topk_bins", "nvfp4_selftest_schedule",
+    "OUT_F32", "OUT_BF16", "w4a16_lm_head_argmax",
     "w4a16_lm_head_argmax_workspace_bytes", "fp8_quantize_rows", "fp8_refresh",
     "fp8_quantize_workspace_bytes", "w8a8_lm_head", "w8a8_lm_head_argmax",
     "w8a8_lm_head_workspace_bytes", "w8a8_lm_head_argmax_workspace_bytes",
@@ -176,6 +177,8 @@ def load_library() -> ctypes.CDLL:
     lib.nvfp4_selftest_bounded_wait.restype = st
     lib.nvfp4_selftest_topk_bins.argtypes = []
     lib.nvfp4_selftest_topk_bins.restype = ctypes.c_int64
+    lib.nvfp4_selftest_schedule.argtypes = []
+    lib.nvfp4_selftest_schedule.restype = ctypes.c_int64
     _lib = lib
     return lib
 
@@ -678,6 +681,13 @@ def nvfp4_selftest_topk_bins() -> int:
     """Host-only check of the fused top-k's histogram bins against every 32-bit
     order key: -1 when all pass, else the first failing key."""
     return int(load_library().nvfp4_selftest_topk_bins())
+
+
+def nvfp4_selftest_schedule() -> int:
+    """Host-only check of the persistent products' split of their units into
+    whole-unit waves and a stream-K tail: -1 when all cases pass, else the
+    index of the first failing case."""
+    return int(load_library().nvfp4_selftest_schedule())
 
 
 def nvfp4_selftest_bounded_wait(workspace: torch.Tensor, limit_us: int, stream=None) -> None:

@@ -40,7 +40,8 @@ struct GemmArgs {
   int n_kb;            // 256-k stages per unit
   uint32_t n_dp;       // whole units per CTA in strided waves (unit c + j * grid)
   uint64_t tail_s0;    // first stage of the stream-K tail (unit-major, k-minor)
-  uint64_t tail_len;   // stages in the tail, split evenly over the grid
+  uint64_t tail_len;   // stages in the tail, split over the grid (see tail_bound)
+  uint32_t tail_skew;  // 0: an even split; a: CTA c's share falls linearly by a / 64 each side
   uint32_t tmem_cols;  // allocated TMEM columns
   uint32_t dbuf_log2;  // accumulator buffers in TMEM: 1 << dbuf_log2 (2 or 4)
   const float* tok_scale;
@@ -87,6 +88,7 @@ struct Sched {
   uint32_t grid;      // CTAs that take part (blockIdx.x >= grid: no work)
   uint64_t tail_s0;   // first stage of the stream-K tail
   uint64_t tail_len;  // stages in the tail
+  uint32_t tail_skew;  // as GemmArgs::tail_skew
   uint32_t nt;        // grouped: weight tiles per group
   const uint32_t* unit_pre;  // grouped: [n_groups + 1] prefix of units per group (shared)
   const int32_t* off;        // grouped: [n_groups + 1] token row offsets (shared)
@@ -94,7 +96,8 @@ struct Sched {
 };
 
 __device__ __forceinline__ Sched plain_sched(const GemmArgs& p) {
-  return Sched{p.n_dp, gridDim.x, p.tail_s0, p.tail_len, 0u, nullptr, nullptr, p.n_dp * gridDim.x};
+  return Sched{p.n_dp, gridDim.x, p.tail_s0, p.tail_len, p.tail_skew, 0u, nullptr, nullptr,
+               p.n_dp * gridDim.x};
 }
 
 // Where a unit lives: its first weight row (the TMA coordinate), first
@@ -192,6 +195,7 @@ __device__ __forceinline__ void grouped_sched_build(const GemmArgs& p, Sched* s,
     s->tail_s0 = (uint64_t)dp * grid * n_kb;
     s->tail_len = (uint64_t)(n_units - dp * grid) * n_kb;
   }
+  s->tail_skew = 0;
   s->nt = nt;
   s->unit_pre = unit_pre;
   s->off = off;
@@ -501,6 +505,15 @@ struct Piece {
   uint32_t u, kb0, kb1;
 };
 
+// First stage of CTA c's tail range, relative to the tail (c in [0, grid]):
+// a split whose density falls linearly from (64 + a) / 64 of the mean at CTA
+// 0 to (64 - a) / 64 at the last CTA (a = sc.tail_skew; 0: even), so that
+// the CTAs that start later take fewer stages.
+__host__ __device__ __forceinline__ uint64_t tail_bound(uint64_t tail_len, uint64_t grid,
+                                                        uint64_t skew, uint64_t c) {
+  return tail_len * (c * ((64 + skew) * grid - skew * c)) / (64 * grid * grid);
+}
+
 template <typename F>
 __device__ __forceinline__ void for_each_piece(const Sched& sc, uint32_t n_kb, F&& body) {
   if (blockIdx.x >= sc.grid) return;
@@ -509,8 +522,8 @@ __device__ __forceinline__ void for_each_piece(const Sched& sc, uint32_t n_kb, F
     if (u >= sc.units_end) break;
     if (!body(Piece{u, 0u, n_kb})) return;
   }
-  const uint64_t t0 = sc.tail_s0 + sc.tail_len * blockIdx.x / sc.grid;
-  const uint64_t t1 = sc.tail_s0 + sc.tail_len * (blockIdx.x + 1) / sc.grid;
+  const uint64_t t0 = sc.tail_s0 + tail_bound(sc.tail_len, sc.grid, sc.tail_skew, blockIdx.x);
+  const uint64_t t1 = sc.tail_s0 + tail_bound(sc.tail_len, sc.grid, sc.tail_skew, blockIdx.x + 1);
   for (uint64_t s = t0; s < t1;) {
     const uint32_t u = (uint32_t)(s / n_kb), kb0 = (uint32_t)(s - (uint64_t)u * n_kb);
     const uint32_t kb1 = (uint32_t)(((uint64_t)kb0 + (t1 - s) < n_kb) ? kb0 + (t1 - s) : n_kb);
@@ -528,8 +541,8 @@ __device__ __forceinline__ uint32_t cta_stages(const Sched& sc, uint32_t n_kb) {
   if (blockIdx.x >= sc.grid) return 0;
   const uint32_t waves =
       sc.units_end > blockIdx.x ? min(sc.n_dp, (sc.units_end - blockIdx.x + sc.grid - 1) / sc.grid) : 0u;
-  const uint64_t t0 = sc.tail_len * blockIdx.x / sc.grid;
-  const uint64_t t1 = sc.tail_len * (blockIdx.x + 1) / sc.grid;
+  const uint64_t t0 = tail_bound(sc.tail_len, sc.grid, sc.tail_skew, blockIdx.x);
+  const uint64_t t1 = tail_bound(sc.tail_len, sc.grid, sc.tail_skew, blockIdx.x + 1);
   return (uint32_t)((uint64_t)waves * n_kb + (t1 - t0));
 }
 
@@ -991,11 +1004,24 @@ static inline void topk_args(GemmArgs& a, uint8_t* ws, const WsLayout& L, int k,
 // tail: all but the last one to two waves run whole; the rest is split
 // evenly, so every CTA's tail range holds at least one unit's stages and a
 // unit is cut at most once.
-static inline void schedule_units(GemmArgs& a, int64_t grid) {
+static inline void schedule_units(GemmArgs& a, int64_t grid, uint32_t max_skew = 0) {
   const int64_t dp_waves = a.n_units >= 2 * grid ? a.n_units / grid - 1 : 0;
   a.n_dp = (uint32_t)dp_waves;
   a.tail_s0 = (uint64_t)(dp_waves * grid) * a.n_kb;
   a.tail_len = (uint64_t)(a.n_units - dp_waves * grid) * a.n_kb;
+  // the largest skew up to max_skew that leaves every CTA's tail range at
+  // least one unit long (so that a unit is still cut at most once)
+  a.tail_skew = 0;
+  for (uint32_t s = max_skew; s > 0; --s) {
+    bool ok = true;
+    for (int64_t c = 0; c < grid && ok; ++c)
+      ok = tail_bound(a.tail_len, grid, s, c + 1) - tail_bound(a.tail_len, grid, s, c) >=
+           (uint64_t)a.n_kb;
+    if (ok) {
+      a.tail_skew = s;
+      break;
+    }
+  }
 }
 
 // Launch configuration of a programmatic dependent launch.

@@ -66,6 +66,14 @@ constexpr uint32_t kPackedStageBytes = kRows * (kKS / 2);   // 16384
 constexpr uint32_t kScaleStageBytes = kRows * (kKS / 16);   // 2048
 
 
+// The plain product's stream-K tail gives the CTAs of higher index (which
+// enter later: the first MMA of a decode call comes 2.8 to 5.6 us after the
+// first CTA's entry, correlated 0.8 with the index at M = 64) fewer stages,
+// up to 4/64 of the mean less (the skew bound passed to schedule_units).
+// Same box, the four decode calls M = 1, 8, 32, 64: 224.4 -> 223.5 us; M = 8
+// alone 52.8 -> 51.7 us; a skew of 8 gave 224.6 us, of 12 227.1 us.
+constexpr uint32_t kDecodeTailSkew = 4;
+
 // ------------------------------------------------------------ activations
 // kWarpsPerRow warps per token row (4, with a 128-thread CTA per row, for
 // few rows, where the latency of one row is what counts and the CTA must
@@ -683,7 +691,7 @@ static nvfp4_status lm_head_run(const void* x, int64_t M, int64_t K, const uint8
   a.n_ttiles = n_ttiles;
   a.n_units = ((N + kRows - 1) / kRows) * n_ttiles;
   a.n_kb = (int)((K + kKB - 1) / kKB);  // the last stage's k past K reads zeros
-  schedule_units(a, L.grid);
+  schedule_units(a, L.grid, kDecodeTailSkew);
   a.split_cnt = split_cnt;
   a.split_ready = split_ready;
   a.split_part = split_part;

@@ -1,6 +1,8 @@
 // selftest.cu -- nvfp4_selftest_bounded_wait: check, on the device, that the
 // library's pipeline waits give up instead of hanging; nvfp4_selftest_topk_bins:
-// check, on the host, the fused top-k's histogram bins against the order keys.
+// check, on the host, the fused top-k's histogram bins against the order keys;
+// nvfp4_selftest_schedule: check, on the host, the persistent GEMM's split of
+// its units into whole-unit waves and a (skewed) stream-K tail.
 //
 // The kernel waits on an mbarrier phase that nothing completes, with the same
 // bounded wait (mbar_wait) every kernel of this library uses, and then on a
@@ -84,3 +86,61 @@ extern "C" int64_t nvfp4_selftest_topk_bins(void) {
   }
   return -1;
 }
+
+// The persistent schedule's host split (schedule_units) over a spread of
+// unit counts, grids, stages per unit and skew bounds: the whole-unit waves
+// and the tail cover every stage once; the tail ranges are contiguous, each
+// at least one unit long, so that a unit is cut at most once (the pairwise
+// partial combine relies on it); an unskewed split is the even one.
+// Returns -1 when every case passes, else the index of the first failing
+// case.
+extern "C" int64_t nvfp4_selftest_schedule(void) {
+  using namespace nvfp4;
+  const int64_t units[] = {1, 2, 3, 7, 31, 100, 151, 152, 153, 303, 304, 305, 457, 1002, 1003,
+                           2004, 4096, 16032};
+  const int64_t grids[] = {1, 2, 7, 76, 148, 152};
+  const int n_kbs[] = {1, 2, 3, 16, 32};
+  const uint32_t skews[] = {0, 4, 8, 16};
+  int64_t idx = 0;
+  for (int64_t nu : units)
+    for (int64_t grid : grids)
+      for (int n_kb : n_kbs)
+        for (uint32_t skew : skews) {
+          ++idx;
+          if (grid > nu) continue;  // the launch never runs more CTAs than units
+          GemmArgs a = {};
+          a.n_units = nu;
+          a.n_kb = n_kb;
+          schedule_units(a, grid, skew);
+          const uint64_t total = (uint64_t)nu * n_kb;
+          if ((int64_t)a.n_dp * grid > nu || a.tail_skew > skew) return idx;
+          if (a.tail_s0 != (uint64_t)a.n_dp * grid * n_kb || a.tail_s0 + a.tail_len != total)
+            return idx;
+          uint64_t prev = 0;
+          for (int64_t c = 0; c < grid; ++c) {
+            const uint64_t b0 = tail_bound(a.tail_len, grid, a.tail_skew, c);
+            const uint64_t b1 = tail_bound(a.tail_len, grid, a.tail_skew, c + 1);
+            if (b0 != prev || b1 < b0) return idx;
+            if (a.tail_skew == 0 && b1 != a.tail_len * (c + 1) / grid) return idx;
+            // a range of at least one unit (ranges of a tail shorter than
+            // the grid are the even split, as before any skew)
+            if (a.tail_skew > 0 && b1 - b0 < (uint64_t)n_kb) return idx;
+            prev = b1;
+          }
+          if (prev != a.tail_len) return idx;
+          // no tail unit cut twice: the CTAs whose ranges touch each unit
+          if (a.tail_len >= (uint64_t)grid * n_kb) {
+            for (uint64_t u = 0; u < a.tail_len / n_kb; ++u) {
+              int touch = 0;
+              for (int64_t c = 0; c < grid; ++c) {
+                const uint64_t b0 = tail_bound(a.tail_len, grid, a.tail_skew, c);
+                const uint64_t b1 = tail_bound(a.tail_len, grid, a.tail_skew, c + 1);
+                if (b0 < (u + 1) * n_kb && b1 > u * n_kb) ++touch;
+              }
+              if (touch > 2) return idx;
+            }
+          }
+        }
+  return -1;
+}
+

@@ -225,3 +225,10 @@ def test_topk_histogram_bins_never_exceed_their_keys(lib):
     (a bin's lower edge) is never above a key of that bin, bins never
     decrease with the key, and each edge lies in its own bin."""
     assert lib.nvfp4_selftest_topk_bins() == -1
+
+
+def test_schedule_split_covers_every_stage_once(lib):
+    """Host check of the persistent GEMM's work split: waves plus tail cover
+    every stage once, tail ranges are contiguous and at least a unit long
+    (skewed or not), no unit is cut twice, an unskewed tail splits evenly."""
+    assert lib.nvfp4_selftest_schedule() == -1
