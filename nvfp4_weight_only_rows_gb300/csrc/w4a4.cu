@@ -441,7 +441,9 @@ static nvfp4_status w4a4_run(const void* x, int64_t M, int64_t K, const uint8_t*
   a.n_ttiles = n_ttiles;
   a.n_units = ((N + kRows - 1) / kRows) * n_ttiles;
   a.n_kb = (int)((K + kKB - 1) / kKB);
-  schedule_units(a, L.grid);
+  // later-starting CTAs take up to 4/64 fewer tail stages (same box, decode
+  // M = 32 / 64: 53.0 / 54.1 -> 52.6 / 53.7 us; the W8A8 product did not move)
+  schedule_units(a, L.grid, 4);
   const bool small = BN <= 64;
   const uint32_t need = 2u * BN + (small ? 6u : 5u) * kW4SfCols;
   uint32_t cols = 32;
