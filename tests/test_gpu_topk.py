@@ -64,10 +64,12 @@ def test_tiny_workload():
                                      (130, 260, 512, 7), (200, 384, 1280, 100), (1, 1, 256, 1),
                                      (3, 7, 256, 7), (300, 5000, 256, 50),
                                      (2, 262144, 256, 128), (2, 262144 + 33, 256, 50),
-                                     (64, 40000, 256, 128)])
+                                     (64, 40000, 256, 128), (256, 4097, 256, 128),
+                                     (257, 3000, 256, 50)])
 def test_ragged_shapes(M, N, K, k):
     """Ragged token and vocabulary tails, k up to N and up to the limit; the
-    largest vocabulary the logits route takes (262144 rows) and one past it."""
+    largest vocabulary the logits route takes (262144 rows) and one past it,
+    the most tokens it takes (256) and one more."""
     W = synth.quant_weight(N=N, K=K, seed=M + N)
     x = synth.decode_x(M, K=K)
     host_q = oracle.quantize(W)
