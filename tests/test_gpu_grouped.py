@@ -48,8 +48,12 @@ def run(x, offs, dev, dt=torch.float32):
 
 
 @pytest.mark.parametrize("offs", [[0, 5, 5, 6, 37], [0, 37, 37, 37, 37], [0, 1, 2, 3, 4],
-                                  [0, 0, 0, 0, 200], [0, 100, 130, 260, 300]])
+                                  [0, 0, 0, 0, 200], [0, 100, 130, 260, 300],
+                                  [0, 129, 129, 385, 400]])
 def test_ragged_and_empty_groups(offs):
+    """Empty, single-row and ragged groups; the last two sets take 128-token
+    tiles whose partly filled last tile per group gets MMAs only as wide as
+    its tokens (16 to 112 of them)."""
     E, N, K = 4, 300, 512
     offs = np.array(offs, dtype=np.int32)
     host, dev = experts(E, N, K, seed=3)
