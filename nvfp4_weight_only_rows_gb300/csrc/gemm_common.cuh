@@ -336,11 +336,12 @@ __device__ __forceinline__ float key_value(uint32_t k) {
 // and the selection skips every group below its final T.
 // Histogram bins: all negative keys; positive keys below 2^-32; a
 // sixteenth of an octave each from 2^-32 to 2^32 (exponent and top 4
-// mantissa bits); 2^32 and above.  A candidate within a quarter of an
-// exponent step of its group's largest (order keys differ by at most 2^21)
-// adds one to its bin (an atomic add without a reply; the token's largest
-// logits are almost always the largest of their groups, and leaving any
-// candidate out only lowers the bin found).  A threshold warp in
+// mantissa bits); 2^32 and above.  The largest candidate of each 32-row
+// group with candidates adds one to its bin (one atomic add without a reply
+// per group: the counted keys are distinct candidates, and leaving the
+// others out only lowers the bin found; counting every candidate within a
+// quarter exponent step of its group's largest cost the M = 2048 GEMM 1.48
+// against 1.25 ms, for its atomics).  A threshold warp in
 // every CTA keeps walking its tokens' bins down from the largest key's bin
 // to the one that holds the k-th counted candidate and raises T to that
 // bin's lower edge: at least k candidates of the token reach it (counts and
@@ -459,16 +460,12 @@ __device__ __forceinline__ void topk_chunk(const GemmArgs& p, int64_t tc, int64_
         my_bal = b[t];
         my_mx = mx;
       }
-      if (mine) {
-        const int64_t tok = tc + t;
-        p.tk_cand[tok * p.N + n] = ok;
-        // a quarter of an exponent step below the group's largest: lower
-        // candidates are not counted
-        const uint32_t floor = mx >= 0x80200000u ? mx - 0x00200000u : 0u;
-        if (ok >= floor) red_add_u32(p.tk_hist + tok * p.tk_hstride + topk_bin(ok), 1u);
-      }
+      if (mine) p.tk_cand[(tc + t) * p.N + n] = ok;
     }
-    if (my_bal) red_max_u32(topk_max(p, tc + lane), my_mx);  // lane t < 16, live tokens only
+    if (my_bal) {  // lane t < 16, live tokens only: the group's largest candidate is counted
+      red_max_u32(topk_max(p, tc + lane), my_mx);
+      red_add_u32(p.tk_hist + (tc + lane) * p.tk_hstride + topk_bin(my_mx), 1u);
+    }
   }
   // lane t < 16 holds token t's group word (my_bal != 0: live token with candidates)
   if (my_bal) {
