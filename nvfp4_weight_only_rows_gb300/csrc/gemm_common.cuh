@@ -460,7 +460,12 @@ __device__ __forceinline__ void topk_chunk(const GemmArgs& p, int64_t tc, int64_
         my_bal = b[t];
         my_mx = mx;
       }
-      if (mine) p.tk_cand[(tc + t) * p.N + n] = ok;
+      // every in-range lane of an 8-row segment that holds a candidate
+      // stores, 0 where it holds none (a slot the selection never reads):
+      // the 32-byte sector is written whole, so L2 need not fetch the rest
+      // of it from DRAM before writing it back
+      if (valid && ((b[t] >> (lane & 24)) & 0xFFu) != 0u)
+        p.tk_cand[(tc + t) * p.N + n] = mine ? ok : 0u;
     }
     if (my_bal) {  // lane t < 16, live tokens only: the group's largest candidate is counted
       red_max_u32(topk_max(p, tc + lane), my_mx);
