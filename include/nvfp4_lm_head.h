@@ -282,8 +282,9 @@ nvfp4_status w4a16_lm_head_argmax(const void *x, int64_t M, int64_t K, const uin
  * 4 bytes (every logit is a candidate at most once), 8 bytes per token and
  * 32 rows of candidate flags, and per token a 4,112-byte histogram and a
  * bitmap of one bit per 32 rows (rounded up to the token tile); only the
- * candidates that reach their token's threshold, and their groups' flags,
- * are ever written.
+ * 32-byte pieces of the candidate store that hold a candidate reaching its
+ * token's threshold (zeros beside it), and their groups' flags, are ever
+ * written.
  */
 size_t w4a16_lm_head_topk_workspace_bytes(int64_t M, int64_t N, int64_t K, int64_t k);
 
@@ -301,8 +302,8 @@ size_t w4a16_lm_head_topk_workspace_bytes(int64_t M, int64_t N, int64_t K, int64
  * logit from those maxima and ranks the few logits that reach the bound.
  * Beyond, the [M, N] logits are never written: the epilogue keeps only the
  * logits that reach the token's running threshold, a lower bound of its
- * k-th largest that rises with a histogram of the candidates kept so far,
- * and a second kernel selects the exact k largest of those.  The result
+ * k-th largest that rises with a histogram of the largest kept candidate of
+ * every 32 rows, and a second kernel selects the exact k largest of those.  The result
  * does not depend on the route or the schedule.
  *
  * The pages define the logits, not a sampler; this is the top-k filter a
