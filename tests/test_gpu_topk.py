@@ -79,9 +79,13 @@ def test_ragged_shapes(M, N, K, k):
 
 
 @pytest.mark.parametrize("M,N,K,k", [(8, 216 * 128, 1024, 50), (1, 153 * 128 + 5, 512, 20),
-                                     (40, 300 * 128, 768, 128)])
+                                     (40, 300 * 128, 768, 128), (260, 300 * 128 + 5, 512, 50),
+                                     (513, 2000 * 8 + 3, 256, 128)])
 def test_split_units_and_repeats(M, N, K, k):
-    """Units cut between two CTAs by the stream-K tail; repeated calls agree."""
+    """Units cut between two CTAs by the stream-K tail; repeated calls agree.
+    The cases past 256 tokens take the candidate route, with a vocabulary
+    that is not a multiple of 8 rows, so that the candidate slots of one
+    token start inside a 32-byte sector."""
     W = synth.quant_weight(N=N, K=K, seed=N % 89)
     x = synth.decode_x(M, K=K)
     host_q = oracle.quantize(W)
