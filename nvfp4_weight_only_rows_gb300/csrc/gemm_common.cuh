@@ -64,8 +64,8 @@ struct GemmArgs {
                                 //   bit j: slot 32g + j holds a candidate}
   int64_t tk_groups;            // ceil(N / 32)
   uint32_t* tk_hist;            // [m_pad][tk_hstride] per token: the histogram of the
-                                //   candidate keys (kHistWords), then one bit per group
-                                //   whose word this call wrote
+                                //   largest key of each candidate group (kHistWords), then
+                                //   one bit per group whose word this call wrote
   int tk_hstride;               // u32 per token in tk_hist
   int tk_k;                     // k, 1 .. kTopkMax
   const float* row_scale;       // [N] per-row weight scale (fp8 weights), else null
@@ -326,9 +326,9 @@ __device__ __forceinline__ float key_value(uint32_t k) {
 // ------------------------------------------------------------ fused top-k
 // Per token: a threshold key T (a lower bound of the token's k-th largest
 // candidate key, so every one of its k largest logits reaches it), the
-// largest candidate order key, a histogram of candidate order keys and the
-// candidates themselves: the order key of a logit that reached T sits in
-// slot n of the token's N slots (the row is the slot).  Per token and group
+// largest candidate order key, a histogram of the candidate groups' largest
+// order keys and the candidates themselves: the order key of a logit that
+// reached T sits in slot n of the token's N slots (the row is the slot).  Per token and group
 // of 32 rows that holds candidates, the warp that owns the group writes
 // {largest candidate order key, bitmap of the slots it filled} and sets the
 // group's bit in the token's group bitmap (cleared with the histogram by
@@ -890,11 +890,12 @@ static inline size_t act_region_bytes(ActFormat f, int64_t m_pad, int64_t M, int
 // grid x 4] and, for argmax and top-k, [CTAs done, 1]; these are zeroed by
 // the prep kernel's first CTA.  Then [split partials, grid x 4 x BN x 32
 // fp32] and, for argmax and top-k, [per-token state, m_pad x 128 bytes: the
-// maximum or the threshold key in word 0, the top-k candidate count in word
-// 1], both words zeroed by the prep CTA of the token.  Top-k only:
-// [histograms, m_pad x kHistWords u32, zeroed the same way][candidate
-// groups, M x ceil(N / 32) x 8 bytes, all written by the GEMM][candidates,
-// M x N u32 order keys, read only where the group words say].
+// maximum or the threshold key in word 0, the largest top-k candidate order
+// key in word 2], both words zeroed by the prep CTA of the token.  Top-k
+// only: [histograms and group bitmaps, m_pad x topk_hist_stride(N) u32,
+// zeroed the same way][candidate groups, M x ceil(N / 32) x 8 bytes, written
+// by the GEMM only where its bitmap bit is set][candidates, M x N u32 order
+// keys, read only where the group words say].
 struct WsLayout {
   size_t x16, tok, cnt, ready, done, keys, part, hist, grp, cand, total;
   int grid;
