@@ -1,12 +1,17 @@
-// topk.cu -- the selection step of the fused top-k: the GEMM epilogue has
-// kept, per token, every logit that reached the token's running threshold
-// (a superset of its k largest; the order key of row n in slot n, flagged
-// in the word of its 32-row group, a word written only for groups with
-// candidates and marked in the token's group bitmap); here one CTA per
-// token picks the exact k
-// largest candidate keys, sorts them (larger logit first, of equal logits
-// the smaller row; a NaN above every number) and writes their rows and
-// logits.
+// topk.cu -- the selection steps of the fused top-k, one CTA per token
+// each, both writing the rows and logits of the token's k largest, sorted
+// (larger logit first, of equal logits the smaller row; a NaN above every
+// number):
+// - topk_select_kernel, beyond 256 tokens: the GEMM epilogue has kept, per
+//   token, every logit that reached the token's running threshold (a
+//   superset of its k largest; the order key of row n in slot n, flagged in
+//   the word of its 32-row group, a word written only for groups with
+//   candidates and marked in the token's group bitmap), and this kernel
+//   picks the exact k largest of those keys;
+// - topk_logits_kernel (after "from logits" below), up to 256 tokens: the
+//   GEMM has written the fp32 logits and the largest of every 32 rows, and
+//   this kernel bounds the k-th largest from those maxima and ranks the few
+//   logits that reach the bound.
 //
 // The kernel runs once per call, briefly and cold, so its code is kept
 // small (instruction fetch, not memory, bounds a bloated version): the
