@@ -65,11 +65,12 @@ def test_tiny_workload():
                                      (3, 7, 256, 7), (300, 5000, 256, 50),
                                      (2, 262144, 256, 128), (2, 262144 + 33, 256, 50),
                                      (64, 40000, 256, 128), (256, 4097, 256, 128),
-                                     (257, 3000, 256, 50)])
+                                     (257, 3000, 256, 50), (300, 7, 256, 7), (270, 33, 512, 1)])
 def test_ragged_shapes(M, N, K, k):
     """Ragged token and vocabulary tails, k up to N and up to the limit; the
     largest vocabulary the logits route takes (262144 rows) and one past it,
-    the most tokens it takes (256) and one more."""
+    the most tokens it takes (256) and one more; past 256 tokens, a
+    vocabulary inside one 32-row group and one just past it."""
     W = synth.quant_weight(N=N, K=K, seed=M + N)
     x = synth.decode_x(M, K=K)
     host_q = oracle.quantize(W)
