@@ -93,11 +93,15 @@ struct Sched {
   const uint32_t* unit_pre;  // grouped: [n_groups + 1] prefix of units per group (shared)
   const int32_t* off;        // grouped: [n_groups + 1] token row offsets (shared)
   uint32_t units_end;  // the waves take units below this index (their last wave may be partial)
+  const uint32_t* grp_tab;   // grouped: group of this CTA's wave unit j (shared), j < n_tab
+  uint32_t n_tab;
 };
+
+constexpr int kGrpTab = 64;  // grouped: wave units per CTA whose group is looked up, not searched
 
 __device__ __forceinline__ Sched plain_sched(const GemmArgs& p) {
   return Sched{p.n_dp, gridDim.x, p.tail_s0, p.tail_len, p.tail_skew, 0u, nullptr, nullptr,
-               p.n_dp * gridDim.x};
+               p.n_dp * gridDim.x, nullptr, 0u};
 }
 
 // Where a unit lives: its first weight row (the TMA coordinate), first
@@ -108,8 +112,21 @@ struct UnitGeom {
   bool reused;
 };
 
+// Grouped: the group e with unit_pre[e] <= u < unit_pre[e + 1] (binary search).
+__device__ __forceinline__ int unit_group(const GemmArgs& p, const uint32_t* unit_pre, uint32_t u) {
+  int lo = 0, hi = p.n_groups;
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (unit_pre[mid] <= u) lo = mid; else hi = mid;
+  }
+  return lo;
+}
+
+// j: the piece's index in the CTA's sequence (the first n_tab pieces are its
+// wave units, whose groups the schedule build put in grp_tab)
 template <bool kGrouped>
-__device__ __forceinline__ UnitGeom unit_geom(const GemmArgs& p, const Sched& s, uint32_t u) {
+__device__ __forceinline__ UnitGeom unit_geom(const GemmArgs& p, const Sched& s, uint32_t u,
+                                              uint32_t j = 0xFFFFFFFFu) {
   UnitGeom g;
   if constexpr (!kGrouped) {
     g.n0 = g.w_row = (int64_t)(u / p.n_ttiles) * kRows;
@@ -117,11 +134,7 @@ __device__ __forceinline__ UnitGeom unit_geom(const GemmArgs& p, const Sched& s,
     g.t_end = p.M;
     g.reused = p.n_ttiles > 1;
   } else {
-    int lo = 0, hi = p.n_groups;  // the group e with unit_pre[e] <= u < unit_pre[e + 1]
-    while (hi - lo > 1) {
-      const int mid = (lo + hi) >> 1;
-      if (s.unit_pre[mid] <= u) lo = mid; else hi = mid;
-    }
+    const int lo = j < s.n_tab ? (int)s.grp_tab[j] : unit_group(p, s.unit_pre, u);
     const uint32_t local = u - s.unit_pre[lo];
     const uint32_t ttc = (s.unit_pre[lo + 1] - s.unit_pre[lo]) / s.nt;  // token tiles of group lo
     const uint32_t wt = local / ttc, tt = local % ttc;
@@ -150,7 +163,8 @@ __device__ __forceinline__ void grouped_offsets_load(const GemmArgs& p, int32_t*
 // Warp 0 (all lanes): lane l takes a contiguous run of groups, the warp
 // scans the run totals.
 __device__ __forceinline__ void grouped_sched_build(const GemmArgs& p, Sched* s, uint32_t* unit_pre,
-                                                    const int32_t* off, uint32_t n_kb, int lane) {
+                                                    const int32_t* off, uint32_t* grp_tab,
+                                                    uint32_t n_kb, int lane) {
   const uint32_t nt = (uint32_t)((p.N + kRows - 1) / kRows);
   const int shift = __ffs(p.BN) - 1;  // BN = 1 << shift
   const int E = p.n_groups;
@@ -174,31 +188,46 @@ __device__ __forceinline__ void grouped_sched_build(const GemmArgs& p, Sched* s,
     acc += nt * (uint32_t)((rows + p.BN - 1) >> shift);
   }
   const uint32_t n_units = __shfl_sync(0xFFFFFFFFu, incl, 31);
-  if (lane != 0) return;
-  unit_pre[E] = n_units;
+  if (lane == 0) unit_pre[E] = n_units;
+  __syncwarp();
   const uint32_t grid = n_units < gridDim.x ? n_units : gridDim.x;
-  s->grid = grid;
+  uint32_t n_dp, units_end;
+  uint64_t tail_s0, tail_len;
   if (grid > 0 && (n_kb <= 4 || n_units >= 8 * grid)) {
     // short units, or many per CTA: whole units only, the last wave partial
     // (a CTA ends at most one unit after another; splitting the last units
     // would cost each cut unit a partial tile through global memory; same
     // box, 64 tokens of a 128-expert top-8 layer: w2 35.4 -> 32.9 us,
     // w13 48.1 -> 47.2 us)
-    s->n_dp = (n_units + grid - 1) / grid;
-    s->units_end = n_units;
-    s->tail_s0 = (uint64_t)n_units * n_kb;
-    s->tail_len = 0;
+    n_dp = (n_units + grid - 1) / grid;
+    units_end = n_units;
+    tail_s0 = (uint64_t)n_units * n_kb;
+    tail_len = 0;
   } else {
     const uint32_t dp = (grid > 0 && n_units >= 2 * grid) ? n_units / grid - 1 : 0;
-    s->n_dp = dp;
-    s->units_end = dp * grid;
-    s->tail_s0 = (uint64_t)dp * grid * n_kb;
-    s->tail_len = (uint64_t)(n_units - dp * grid) * n_kb;
+    n_dp = dp;
+    units_end = dp * grid;
+    tail_s0 = (uint64_t)dp * grid * n_kb;
+    tail_len = (uint64_t)(n_units - dp * grid) * n_kb;
   }
+  // the groups of this CTA's wave units, one search per lane
+  const uint32_t n_tab = n_dp < (uint32_t)kGrpTab ? n_dp : (uint32_t)kGrpTab;
+  for (uint32_t j = (uint32_t)lane; j < n_tab; j += 32) {
+    const uint32_t u = blockIdx.x + j * grid;
+    grp_tab[j] = u < units_end ? (uint32_t)unit_group(p, unit_pre, u) : 0u;
+  }
+  if (lane != 0) return;
+  s->grid = grid;
+  s->n_dp = n_dp;
+  s->units_end = units_end;
+  s->tail_s0 = tail_s0;
+  s->tail_len = tail_len;
   s->tail_skew = 0;
   s->nt = nt;
   s->unit_pre = unit_pre;
   s->off = off;
+  s->grp_tab = grp_tab;
+  s->n_tab = blockIdx.x < grid ? n_tab : 0u;
 }
 
 // one lane of a converged warp (the lowest active lane)
@@ -576,7 +605,7 @@ __device__ __forceinline__ void epilogue_role(const GemmArgs& p, const Sched& sc
     const uint32_t buf = (uint32_t)(i & ((1 << p.dbuf_log2) - 1));
     const uint32_t dph = (uint32_t)((i >> p.dbuf_log2) & 1);
     ++i;
-    const UnitGeom geo = unit_geom<kGrouped>(p, sc, u);
+    const UnitGeom geo = unit_geom<kGrouped>(p, sc, u, (uint32_t)(i - 1));
     const int64_t n = geo.n0 + row;
     const int64_t t0 = geo.t0;
     const int64_t t_end = geo.t_end;

@@ -313,6 +313,7 @@ __global__ void __launch_bounds__((gemm_threads<kOut, kStages, kPStages, kDqPerQ
   Sched* s_sched = reinterpret_cast<Sched*>(s_thr + 4 * kMaxBN);
   uint32_t* s_unit_pre = reinterpret_cast<uint32_t*>(s_sched + 1);
   int32_t* s_off = reinterpret_cast<int32_t*>(s_unit_pre + kMaxGroups + 1);
+  uint32_t* s_grp_tab = reinterpret_cast<uint32_t*>(s_off + kMaxGroups + 1);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -341,7 +342,8 @@ __global__ void __launch_bounds__((gemm_threads<kOut, kStages, kPStages, kDqPerQ
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
   if constexpr (kGrouped)
-    if (warp == 0) grouped_sched_build(p, s_sched, s_unit_pre, s_off, (uint32_t)p.n_kb, lane);
+    if (warp == 0)
+      grouped_sched_build(p, s_sched, s_unit_pre, s_off, s_grp_tab, (uint32_t)p.n_kb, lane);
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tm_packed);
     tma_prefetch_desc(&tm_scales);
@@ -369,9 +371,9 @@ __global__ void __launch_bounds__((gemm_threads<kOut, kStages, kPStages, kDqPerQ
     // a weight tile read once (one token tile) is not kept in L2; one read
     // by several token tiles in a row is
     const uint64_t pol_once = policy_evict_first(), pol_reused = policy_evict_last();
-    uint32_t issued = 0;
+    uint32_t issued = 0, piece = 0;
     for_each_piece(sc, n_kb_u, [&](const Piece& pc) {
-      const UnitGeom geo = unit_geom<kGrouped>(p, sc, pc.u);
+      const UnitGeom geo = unit_geom<kGrouped>(p, sc, pc.u, piece++);
       const int32_t n0 = (int32_t)geo.w_row;
       const uint64_t pol = geo.reused ? pol_reused : pol_once;  // packed codes
       for (uint32_t kb = pc.kb0; kb < pc.kb1; ++kb, ++issued) {
@@ -400,9 +402,9 @@ __global__ void __launch_bounds__((gemm_threads<kOut, kStages, kPStages, kDqPerQ
     // ---------------- activation producer (four 64-k boxes per stage)
     grid_dependency_wait();  // the rescaled activations come from the prep kernel
     const uint64_t pol = policy_evict_last();
-    uint32_t issued = 0;
+    uint32_t issued = 0, piece = 0;
     for_each_piece(sc, n_kb_u, [&](const Piece& pc) {
-      const int32_t t0 = (int32_t)unit_geom<kGrouped>(p, sc, pc.u).t0;
+      const int32_t t0 = (int32_t)unit_geom<kGrouped>(p, sc, pc.u, piece++).t0;
       for (uint32_t kb = pc.kb0; kb < pc.kb1; ++kb, ++issued) {
         const uint32_t st = issued % kStages, ph = (issued / kStages) & 1;
         if (!warp_wait(&s_empty[st], ph ^ 1, wc)) return false;
@@ -433,12 +435,11 @@ __global__ void __launch_bounds__((gemm_threads<kOut, kStages, kPStages, kDqPerQ
       ++i;
       // grouped 128-token tiles: a group's last, partly filled tile takes MMAs
       // only as wide as its tokens, in 16-token steps (same box, 2048 tokens:
-      // w13 134.9 -> 132.5 us, w2 89.2 -> 88.7 us; the group search this
-      // needs per unit cost the 16-token decode tiles 2-3 us, so they keep BN)
+      // w13 134.9 -> 132.5 us, w2 89.2 -> 88.7 us; smaller tiles keep BN)
       uint32_t id = idesc;
       if constexpr (kGrouped) {
         if (BN == kMaxBN) {
-          const UnitGeom geo = unit_geom<kGrouped>(p, sc, pc.u);
+          const UnitGeom geo = unit_geom<kGrouped>(p, sc, pc.u, (uint32_t)(i - 1));
           const int64_t live = geo.t_end - geo.t0;
           if (live < BN) id = idesc_f16_f32(live > 0 ? (uint32_t)((live + 15) / 16 * 16) : 16u);
         }
@@ -563,7 +564,7 @@ static size_t gemm_smem_bytes(int BN, int stages, int pstages, bool argmax, bool
   return 1024 + pstages * (size_t)(kPackedStageBytes + kScaleStageBytes) +
          stages * (size_t)BN * kKB * 2 + 256 + 4 * kMaxBN * sizeof(float) +
          (argmax || grouped ? 16 + 4 * kMaxBN * sizeof(float) : 0) +
-         (grouped ? sizeof(Sched) + 2 * (kMaxGroups + 1) * sizeof(uint32_t) : 0);
+         (grouped ? sizeof(Sched) + (2 * (kMaxGroups + 1) + kGrpTab) * sizeof(uint32_t) : 0);
 }
 
 size_t lm_head_workspace_bytes(int64_t M, int64_t N, int64_t K, bool argmax) {
