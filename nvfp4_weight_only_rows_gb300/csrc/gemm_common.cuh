@@ -93,7 +93,8 @@ struct Sched {
   const uint32_t* unit_pre;  // grouped: [n_groups + 1] prefix of units per group (shared)
   const int32_t* off;        // grouped: [n_groups + 1] token row offsets (shared)
   uint32_t units_end;  // the waves take units below this index (their last wave may be partial)
-  const uint32_t* grp_tab;   // grouped: group of this CTA's wave unit j (shared), j < n_tab
+  const uint2* grp_tab;      // grouped: this CTA's wave unit j (shared), j < n_tab: {group |
+                             //   reused << 31, weight tile | token tile << 16}
   uint32_t n_tab;
 };
 
@@ -134,15 +135,26 @@ __device__ __forceinline__ UnitGeom unit_geom(const GemmArgs& p, const Sched& s,
     g.t_end = p.M;
     g.reused = p.n_ttiles > 1;
   } else {
-    const int lo = j < s.n_tab ? (int)s.grp_tab[j] : unit_group(p, s.unit_pre, u);
-    const uint32_t local = u - s.unit_pre[lo];
-    const uint32_t ttc = (s.unit_pre[lo + 1] - s.unit_pre[lo]) / s.nt;  // token tiles of group lo
-    const uint32_t wt = local / ttc, tt = local % ttc;
+    int lo;
+    uint32_t wt, tt;
+    if (j < s.n_tab) {
+      const uint2 e = s.grp_tab[j];
+      lo = (int)(e.x & 0x7FFFFFFFu);
+      wt = e.y & 0xFFFFu;
+      tt = e.y >> 16;
+      g.reused = (e.x >> 31) != 0u;
+    } else {
+      lo = unit_group(p, s.unit_pre, u);
+      const uint32_t local = u - s.unit_pre[lo];
+      const uint32_t ttc = (s.unit_pre[lo + 1] - s.unit_pre[lo]) / s.nt;  // token tiles of group lo
+      wt = local / ttc;
+      tt = local % ttc;
+      g.reused = ttc > 1;
+    }
     g.n0 = (int64_t)wt * kRows;
     g.w_row = (int64_t)lo * p.N + g.n0;
     g.t0 = s.off[lo] + (int64_t)tt * p.BN;
     g.t_end = s.off[lo + 1] > s.off[lo] ? s.off[lo + 1] : s.off[lo];  // offsets are within [0, M]
-    g.reused = ttc > 1;
   }
   return g;
 }
@@ -163,7 +175,7 @@ __device__ __forceinline__ void grouped_offsets_load(const GemmArgs& p, int32_t*
 // Warp 0 (all lanes): lane l takes a contiguous run of groups, the warp
 // scans the run totals.
 __device__ __forceinline__ void grouped_sched_build(const GemmArgs& p, Sched* s, uint32_t* unit_pre,
-                                                    const int32_t* off, uint32_t* grp_tab,
+                                                    const int32_t* off, uint2* grp_tab,
                                                     uint32_t n_kb, int lane) {
   const uint32_t nt = (uint32_t)((p.N + kRows - 1) / kRows);
   const int shift = __ffs(p.BN) - 1;  // BN = 1 << shift
@@ -210,11 +222,21 @@ __device__ __forceinline__ void grouped_sched_build(const GemmArgs& p, Sched* s,
     tail_s0 = (uint64_t)dp * grid * n_kb;
     tail_len = (uint64_t)(n_units - dp * grid) * n_kb;
   }
-  // the groups of this CTA's wave units, one search per lane
-  const uint32_t n_tab = n_dp < (uint32_t)kGrpTab ? n_dp : (uint32_t)kGrpTab;
+  // where this CTA's wave units lie (group, weight tile, token tile), one
+  // search per lane; weight and token tiles must fit 16 bits each
+  const bool fits = nt <= 0xFFFFu && ((uint64_t)p.M + p.BN - 1) / p.BN <= 0xFFFFu;
+  const uint32_t n_tab = fits ? (n_dp < (uint32_t)kGrpTab ? n_dp : (uint32_t)kGrpTab) : 0u;
   for (uint32_t j = (uint32_t)lane; j < n_tab; j += 32) {
     const uint32_t u = blockIdx.x + j * grid;
-    grp_tab[j] = u < units_end ? (uint32_t)unit_group(p, unit_pre, u) : 0u;
+    uint2 e = make_uint2(0u, 0u);
+    if (u < units_end) {
+      const int lo = unit_group(p, unit_pre, u);
+      const uint32_t local = u - unit_pre[lo];
+      const uint32_t ttc = (unit_pre[lo + 1] - unit_pre[lo]) / nt;
+      e = make_uint2((uint32_t)lo | (ttc > 1 ? 0x80000000u : 0u),
+                     (local / ttc) | ((local % ttc) << 16));
+    }
+    grp_tab[j] = e;
   }
   if (lane != 0) return;
   s->grid = grid;

@@ -313,7 +313,7 @@ __global__ void __launch_bounds__((gemm_threads<kOut, kStages, kPStages, kDqPerQ
   Sched* s_sched = reinterpret_cast<Sched*>(s_thr + 4 * kMaxBN);
   uint32_t* s_unit_pre = reinterpret_cast<uint32_t*>(s_sched + 1);
   int32_t* s_off = reinterpret_cast<int32_t*>(s_unit_pre + kMaxGroups + 1);
-  uint32_t* s_grp_tab = reinterpret_cast<uint32_t*>(s_off + kMaxGroups + 1);
+  uint2* s_grp_tab = reinterpret_cast<uint2*>(s_off + kMaxGroups + 1);  // 8-byte aligned
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -564,7 +564,8 @@ static size_t gemm_smem_bytes(int BN, int stages, int pstages, bool argmax, bool
   return 1024 + pstages * (size_t)(kPackedStageBytes + kScaleStageBytes) +
          stages * (size_t)BN * kKB * 2 + 256 + 4 * kMaxBN * sizeof(float) +
          (argmax || grouped ? 16 + 4 * kMaxBN * sizeof(float) : 0) +
-         (grouped ? sizeof(Sched) + (2 * (kMaxGroups + 1) + kGrpTab) * sizeof(uint32_t) : 0);
+         (grouped ? sizeof(Sched) + 2 * (kMaxGroups + 1) * sizeof(uint32_t) +
+                        kGrpTab * sizeof(uint2) : 0);
 }
 
 size_t lm_head_workspace_bytes(int64_t M, int64_t N, int64_t K, bool argmax) {
