@@ -98,7 +98,7 @@ struct Sched {
   uint32_t n_tab;
 };
 
-constexpr int kGrpTab = 64;  // grouped: wave units per CTA whose group is looked up, not searched
+constexpr int kGrpTab = 64;  // grouped: wave units per CTA whose place is looked up, not searched
 
 __device__ __forceinline__ Sched plain_sched(const GemmArgs& p) {
   return Sched{p.n_dp, gridDim.x, p.tail_s0, p.tail_len, p.tail_skew, 0u, nullptr, nullptr,
@@ -124,7 +124,7 @@ __device__ __forceinline__ int unit_group(const GemmArgs& p, const uint32_t* uni
 }
 
 // j: the piece's index in the CTA's sequence (the first n_tab pieces are its
-// wave units, whose groups the schedule build put in grp_tab)
+// wave units, whose group and tiles the schedule build put in grp_tab)
 template <bool kGrouped>
 __device__ __forceinline__ UnitGeom unit_geom(const GemmArgs& p, const Sched& s, uint32_t u,
                                               uint32_t j = 0xFFFFFFFFu) {
